@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid GDN + sink/SWA layer on GB300.
+
+Default: prefill of the LLaMA-3.1-8B-shaped layer (B=1, T=4096, 32 q / 8 kv
+heads, head_dim 128, bf16, 8 sinks + 56 window) -> tokens/s, plus the decode
+workload (64 sequences prefilled to 8192, ring 8 + 888) -> decode steps/s,
+both through the libhla C ABI on synthetic seeded inputs.
+
+One JSON line on stdout (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead (the reference arm).  Under torchrun every rank runs its own
+replica of the workload (the layer shards into independent sequences, so
+there is no data-path collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid GDN+sink/SWA layer prefill tokens/s & decode steps/s on 1 GB300; % roofline"
+L2_FLUSH_BYTES = 512 << 20
+FP32_ALU_TFLOPS_DERIVATION = "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c4"],
+                    help="prefill workload of the headline line")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing: one process per GPU, max over ranks
+class Dist:
+    def __init__(self):
+        import torch
+
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(self.local)
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    return dist.max(value)
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_traffic(kernel: str, source_files) -> float | None:
+    """DRAM bytes per launch recorded from an ncu capture of `kernel`, if the
+    kernel's sources are unchanged since (hash match); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for s in source_files:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for s in files:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# prefill
+GDN_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
+               "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+
+
+def prefill_work(wl):
+    """Algorithmic work of one prefill launch per stage."""
+    d, Hq, Hkv = wl.head_dim, wl.n_q_heads, wl.n_kv_heads
+    T = wl.total_tokens
+    absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens)
+    keys = 0
+    for L in wl.seqlens:
+        for p in range(L):
+            keys += min(p + 1, wl.n_sinks) + max(0, min(wl.window, p + 1 - wl.n_sinks))
+    eb = 2 if wl.dtype == "bf16" else 4
+    return {
+        # token-serial delta rule: k^T S, the rank-1 update, q^T S -> 6 d^2 flops per token-head
+        "gdn": {"bound": "alu", "flops": 6.0 * d * d * absorbed * Hq, "peak": FP32_ALU_TFLOPS,
+                "unit": "TFLOP/s", "sources": GDN_SOURCES},
+        # q.k and p.v over the visible keys of every (token, q-head)
+        "softmax": {"bound": "alu", "flops": 4.0 * d * keys * Hq, "peak": FP32_ALU_TFLOPS,
+                    "unit": "TFLOP/s", "sources": ["linearized_attention_rope_gb300/csrc/window_softmax.cu"]},
+        # read q, k, v; write RoPE'd q, k and qhat, khat, vhat
+        "features": {"bound": "hbm", "bytes": float(T * d * ((Hq + 2 * Hkv) * eb + (2 * Hq + 3 * Hkv) * eb)),
+                     "unit": "GB/s", "sources": ["linearized_attention_rope_gb300/csrc/features.cu"]},
+        "absorbed_token_heads": absorbed * Hq,
+    }
+
+
+def run_prefill_bench(args, dist, peaks):
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.workloads()[args.workload]
+    x = synth.make_inputs(wl, "cuda")
+    prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window,
+                     dtype=hla.DTYPE_BF16 if wl.dtype == "bf16" else hla.DTYPE_F32)
+    out = torch.empty_like(x["q"])
+    ws = hla.alloc_workspace(prm, wl.total_tokens, wl.n_seqs)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"],
+                    x["wv"], x["cu_seqlens"], out, ws=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    n_stage = 4
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
+    for row in ev:  # materialise the event handles
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with ClockSampler(dist.local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            hla.set_prefill_stage_events(ev[i])
+            step()
+            ends[i].record(stream)
+        hla.set_prefill_stage_events(None)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dist.barrier()
+    step_ms = [ev[i][0].elapsed_time(ends[i]) for i in range(args.steps)]
+    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                for j, name in enumerate(("features", "gdn", "softmax"))}
+    device_s = dist.max(sum(step_ms) / 1e3)
+    launches_per_step = 4  # rope tables, features, gdn, softmax
+
+    work = prefill_work(wl)
+    top = max(stage_ms, key=stage_ms.get)
+    w = work[top]
+    sec = stage_ms[top] / 1e3
+    if w["bound"] == "hbm":
+        achieved, peak = w["bytes"] / sec / 1e9, peaks["hbm_gbs"]
+    elif w["bound"] == "tensor":
+        achieved, peak = w["flops"] / sec / 1e12, peaks["bf16_tflops"]
+    else:
+        achieved, peak = w["flops"] / sec / 1e12, w["peak"]
+    roofline = {"kernel": top, "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
+                "unit": w["unit"], "frac": round(achieved / peak, 5),
+                "traffic": kernel_traffic(top, w["sources"]),
+                "peak_source": peaks["source"] if w["bound"] != "alu" else FP32_ALU_TFLOPS_DERIVATION}
+
+    # end to end through the C ABI: pinned host inputs in, result back to pinned host memory
+    host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in host:
+            x[k].copy_(host[k], non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_s = dist.max(sum(e2e_ms) / 1e3)
+    tokens = wl.total_tokens * dist.world * args.steps
+    return {
+        "value": tokens / device_s, "ms_per_step": device_s * 1e3 / args.steps, "wall_s": wall,
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "roofline": roofline,
+        "clocks": clocks.summary(), "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "workload": wl,
+    }
+
+
+# ---------------------------------------------------------------------------
+# decode
+def decode_bytes(wl, pos_mean: float) -> float:
+    """Algorithmic HBM bytes of one decode step over all sequences."""
+    N, Hq, Hkv, d = wl.n_seqs, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    eb = 2 if wl.dtype == "bf16" else 4
+    keys = min(pos_mean + 1, wl.n_sinks + wl.window)
+    b = N * Hq * d * d * 4 * 2                     # state read + write
+    b += N * Hkv * keys * d * eb * 2               # ring K and V read
+    b += N * Hkv * d * eb * 2                      # ring K and V write (new token)
+    b += N * Hkv * d * 4 * 2 * 2                   # pending khat/vhat: one read, one write
+    b += N * 7 * (Hq + 2 * Hkv) * d * 4 * 2        # conv caches read + write
+    b += N * (Hq + 2 * Hkv) * d * eb + N * Hq * d * eb   # q, k, v in; out
+    return float(b)
+
+
+def run_decode_bench(args, dist, peaks):
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.workloads()["c3"]
+    x = synth.make_inputs(wl, "cuda")
+    prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window)
+    out = torch.empty_like(x["q"])
+    st = hla.State(prm, wl.n_seqs).init()
+    hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"],
+                x["cu_seqlens"], out, state=st)
+    del out
+    torch.cuda.synchronize()
+    K = args.decode_steps or args.steps
+    W = args.warmup
+    assert W + K <= wl.decode_steps
+    dout = torch.empty(x["dq"].shape[1:], dtype=x["dq"].dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        hla.decode_step(prm, x["dq"][s], x["dk"][s], x["dv"][s], x["dg"][s], x["dbeta"][s], x["lam"],
+                        x["wq"], x["wk"], x["wv"], st, dout)
+
+    for s in range(W):
+        step(s)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    dist.barrier()
+    with ClockSampler(dist.local) as clocks:
+        for i in range(K):
+            evs[i][0].record(stream)
+            step(W + i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    assert st.check_error() == 0
+    ms = [a.elapsed_time(b) for a, b in evs]
+    dev_s = dist.max(sum(ms) / 1e3)
+    per_step = dev_s / K
+    nbytes = decode_bytes(wl, 8192 + W + K / 2)
+    achieved = nbytes / per_step / 1e9
+    return {"value": K * dist.world / dev_s, "unit": "steps/s", "ms_per_step": per_step * 1e3,
+            "tokens_per_s": K * dist.world * wl.n_seqs / dev_s,
+            "config": {"workload": wl.name, "sequences": wl.n_seqs, "prefill_len": 8192,
+                       "ring": wl.n_sinks + wl.window, "l2": "working set (state + ring) > L2"},
+            "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": round(achieved, 2),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": None, "algorithmic_bytes_per_step": nbytes},
+            "clocks": clocks.summary(), "gpu_launches": 2 * K}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and reference arm)
+def oracle_jobs(wl, x, heads):
+    import torch
+
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    cu = x["cu_seqlens"].tolist()
+    d, G = wl.head_dim, wl.n_q_heads // wl.n_kv_heads
+    jobs = []
+    for n in range(wl.n_seqs):
+        a, b = cu[n], cu[n + 1]
+        for h in heads:
+            kv = h // G
+            jobs.append(dict(q=f64(x["q"][a:b, h]), k=f64(x["k"][a:b, kv]), v=f64(x["v"][a:b, kv]),
+                             g=f64(x["g"][a:b, h]), beta=f64(x["beta"][a:b, h]),
+                             lam=float(x["lam"][h]), wq=f64(x["wq"][h * d:(h + 1) * d]),
+                             wk=f64(x["wk"][kv * d:(kv + 1) * d]), wv=f64(x["wv"][kv * d:(kv + 1) * d])))
+    return jobs
+
+
+def time_oracle(wl, heads, reps=1):
+    """Wall time of the oracle over `heads` of every sequence of wl, on all host cores."""
+    import oracle
+    from linearized_attention_rope_gb300 import synth
+
+    oracle.build()
+    x = synth.make_inputs(wl, "cpu")
+    jobs = oracle_jobs(wl, x, heads)
+    cfg = oracle.OracleCfg(d=wl.head_dim, n_sinks=wl.n_sinks, window=wl.window)
+    cores = min(os.cpu_count() or 1, len(jobs))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.layer_units(cfg, jobs, threads=cores)
+        times.append(time.perf_counter() - t0)
+    return times, cores
+
+
+def cpu_baseline(wl):
+    heads = list(range(wl.n_q_heads))
+    times, cores = time_oracle(wl, heads)
+    tokens = wl.total_tokens * len(heads) / wl.n_q_heads
+    return {"value": tokens / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{wl.name}: all {wl.n_q_heads} q-heads of every sequence "
+                      f"({wl.total_tokens} tokens), one pass, fp64 C oracle, {cores} threads"}
+
+
+def run_reference(args, dist):
+    from linearized_attention_rope_gb300 import synth
+
+    if dist.rank != 0:
+        return None
+    wl = synth.workloads()[args.workload]
+    heads = list(range(0, wl.n_q_heads, 2))  # half the q-heads per step: a bounded sample
+    times, cores = time_oracle(wl, heads, reps=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    tokens = wl.total_tokens * len(heads) / wl.n_q_heads
+    value = tokens * len(timed) / sum(timed)
+    sample = (f"{wl.name}: q-heads {heads[0]}..{heads[-1]} step 2 of every sequence per step "
+              f"({tokens:.0f} token-equivalents), fp64 C oracle, {cores} threads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(timed) / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "tokens": wl.total_tokens},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    if args.impl == "reference":
+        line = run_reference(args, dist)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        dist.close()
+        return
+    import torch
+
+    from linearized_attention_rope_gb300 import build as _build
+    from linearized_attention_rope_gb300 import hla
+
+    if dist.rank == 0 or not os.path.exists(hla.LIB_PATH):
+        _build.build()
+    dist.barrier()
+    hla.load()
+    peaks = measured_peaks()
+    pre = run_prefill_bench(args, dist, peaks)
+    dec = None if args.no_decode else run_decode_bench(args, dist, peaks)
+    torch.cuda.synchronize()
+    wl = pre.pop("workload")
+    line = {
+        "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded; shapes of the named layer, no trained weights)",
+        "config": {"workload": wl.name, "global_batch": wl.n_seqs * dist.world,
+                   "seq_len": max(wl.seqlens), "tokens_per_rank": wl.total_tokens,
+                   "parallelism": f"replicas x{dist.world}", "l2": "flushed between steps (512 MiB write)",
+                   "precision": "bf16 in/out, fp16 MMA operands, fp32 state and accumulation"},
+        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"], "clocks": pre["clocks"],
+        "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"] + (dec["gpu_launches"] if dec else 0),
+        "wall_s": round(pre["wall_s"], 3),
+    }
+    if dec:
+        line["decode"] = dec
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

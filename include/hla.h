@@ -1,0 +1,195 @@
+/*
+ * hla.h — C ABI of libhla, the GB300 (sm_103a) hybrid linear-attention layer.
+ *
+ * The layer replaces softmax attention in a frozen LLaMA/Qwen backbone, as in
+ * "The Key to Going Linear: Analysis-Driven Transformer Linearization"
+ * (summary page "迈向线性的关键：分析驱动的 Transformer 线性化"):
+ *   - exact softmax over a fixed cache budget of n_sinks sink tokens plus a
+ *     sliding window (section 填补近似缺口的实用设计);
+ *   - a Gated DeltaNet state S (d x d, fp32, one per query head) that absorbs
+ *     every non-sink token when it leaves the window (GDN equation, section
+ *     线性注意力替换机制, with a scalar gate alpha = exp(g));
+ *   - keys and queries of the linear branch go RoPE -> causal depthwise
+ *     short conv (width 8) -> L2 norm (section 实践建议, item 3);
+ *   - o_t = softmax_{j in sinks U window}(q_t k_j / sqrt(d)) V
+ *           + lambda_h * qhat_t^T S_t,
+ *     the inference-time weighting of the two branches of "Untangling
+ *     Component Imbalance in Hybrid Linear Attention Conversion", section
+ *     关键设计 (1).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless marked "host".  The
+ *     caller owns every buffer; the library allocates no device memory and
+ *     never synchronises the stream, except hla_check_device_error.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Argument errors are detected on the host, before any launch, and return
+ *     HLA_ERR_INVALID_ARG / HLA_ERR_UNSUPPORTED without touching the GPU.
+ *   - A failed launch returns HLA_ERR_CUDA (the CUDA error is consumed).
+ *   - Problems found on the device (malformed cu_seqlens, a bounded wait that
+ *     ran out) are recorded in a device error word and read back with
+ *     hla_check_device_error / hla_check_workspace_error.
+ *   - Results are deterministic: fixed reduction order, no atomics in the
+ *     numeric path.
+ *   - Tensors are dense and row-major; every pointer must be 16-byte aligned.
+ *   - Positions restart at 0 at the start of every sequence.
+ */
+#ifndef HLA_H
+#define HLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HLA_API __attribute__((visibility("default")))
+
+/* status codes */
+#define HLA_OK 0
+#define HLA_ERR_INVALID_ARG 1 /* bad pointer, size, alignment or parameter */
+#define HLA_ERR_UNSUPPORTED 2 /* valid but not implemented (e.g. head_dim 96) */
+#define HLA_ERR_STATE 3       /* decode state inconsistent (device error word) */
+#define HLA_ERR_CUDA 4        /* a CUDA call or launch failed */
+#define HLA_ERR_TIMEOUT 5     /* a bounded device-side wait ran out */
+#define HLA_ERR_WORKSPACE 6   /* workspace smaller than hla_prefill_workspace_bytes */
+
+/* element type of q, k, v, out and of the KV ring */
+#define HLA_DTYPE_F32 0
+#define HLA_DTYPE_BF16 1
+
+/* flags */
+#define HLA_FLAG_L2NORM_Q 0x1u       /* qhat = L2(conv(RoPE q)); set by default */
+#define HLA_FLAG_SOFTMAX_OFF 0x2u    /* test hook: drop the softmax branch */
+#define HLA_FLAG_LINEAR_OFF 0x4u     /* test hook: drop the linear branch */
+#define HLA_FLAG_GDN_RECURRENT 0x8u  /* use the token-serial fp32 GDN kernel in
+                                        place of the chunked tensor-core one */
+
+/* Layer shape.  n_q_heads must be a multiple of n_kv_heads (grouped-query
+ * attention: q-head h reads kv-head h / (n_q_heads / n_kv_heads)).
+ * head_dim: 64 or 128.  n_sinks >= 0, window >= 1 (the window includes the
+ * current token).  conv_width: 8.  rope_base: RoPE base (rotate-half pairs
+ * (i, i + d/2), angle p * base^(-2i/d)).  flags: HLA_FLAG_*. */
+typedef struct hla_params {
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int n_sinks;
+    int window;
+    int conv_width;
+    float rope_base;
+    int dtype;
+    unsigned flags;
+} hla_params;
+
+/* Decode state of n_seqs sequences: caller-owned device buffers.
+ *   S         fp32  [N, Hq, d, d]     GDN state, S[n][h][i][j], i = key dim
+ *   k_ring    dtype [N, Hkv, n_sinks + window, d]  RoPE'd keys: slot p for a
+ *             sink p < n_sinks, slot n_sinks + (p - n_sinks) % window otherwise
+ *   v_ring    dtype [N, Hkv, n_sinks + window, d]  raw values, same slots
+ *   pend_k    fp32  [N, Hkv, window + 1, d]  khat of tokens still in the window,
+ *             slot p % (window + 1)
+ *   pend_v    fp32  [N, Hkv, window + 1, d]  vhat, same slots
+ *   pend_g    fp32  [N, Hq, window + 1]      log-gate g of those tokens
+ *   pend_beta fp32  [N, Hq, window + 1]      beta of those tokens
+ *   conv_q    fp32  [N, 7, Hq, d]   RoPE'd q of positions p-7 .. p-1
+ *   conv_k    fp32  [N, 7, Hkv, d]  RoPE'd k of positions p-7 .. p-1
+ *   conv_v    fp32  [N, 7, Hkv, d]  raw v of positions p-7 .. p-1
+ *   pos       int64 [N]  next position of each sequence
+ *   err       int32 [4]  device error word (0 = fine)
+ * The whole struct is the resumable state: copying the buffers out and back
+ * in resumes decoding exactly. */
+typedef struct hla_state {
+    float* S;
+    void* k_ring;
+    void* v_ring;
+    float* pend_k;
+    float* pend_v;
+    float* pend_g;
+    float* pend_beta;
+    float* conv_q;
+    float* conv_k;
+    float* conv_v;
+    int64_t* pos;
+    int32_t* err;
+} hla_state;
+
+/* byte sizes of the hla_state buffers, in struct order */
+typedef struct hla_state_sizes {
+    size_t S, k_ring, v_ring, pend_k, pend_v, pend_g, pend_beta, conv_q, conv_k, conv_v, pos, err;
+} hla_state_sizes;
+
+/* Human-readable name of a status code (static string). */
+HLA_API const char* hla_status_string(int status);
+
+/* Sizes of the decode-state buffers for n_seqs sequences (host only). */
+HLA_API int hla_state_bytes(const hla_params* params, int n_seqs, hla_state_sizes* out);
+
+/* Workspace bytes hla_prefill needs for total_tokens tokens in n_seqs
+ * sequences (host only).  The workspace holds the feature-path outputs and
+ * the linear-branch output between kernels. */
+HLA_API int hla_prefill_workspace_bytes(const hla_params* params, int64_t total_tokens, int n_seqs,
+                                        size_t* bytes);
+
+/* Zeroes every buffer of `st` (positions 0, empty state, empty caches).
+ * Asynchronous on `stream`. */
+HLA_API int hla_state_init(const hla_params* params, int n_seqs, const hla_state* st, void* stream);
+
+/* Prefill: runs the layer over n_seqs packed sequences.
+ *   q [total, Hq, d], k, v [total, Hkv, d]  pre-RoPE, in params->dtype
+ *   g, beta [total, Hq] fp32      log alpha (<= 0) and beta in (0, 1), per
+ *                                 token and query head
+ *   lambda [Hq] fp32              weight of the linear branch per query head
+ *   conv_wq [Hq*d, 8], conv_wk [Hkv*d, 8], conv_wv [Hkv*d, 8] fp32  depthwise
+ *                                 filters, tap 7 on the current token
+ *   cu_seqlens int32 [n_seqs + 1] (device) sequence offsets: 0 = c_0 <= c_1
+ *                                 <= ... <= c_n = total_tokens
+ *   out [total, Hq, d]            params->dtype
+ *   st                            NULL, or a state freshly set up by
+ *                                 hla_state_init for n_seqs sequences: it
+ *                                 receives everything decoding needs
+ *   ws, ws_bytes                  workspace of at least
+ *                                 hla_prefill_workspace_bytes bytes
+ * With total_tokens == 0 the per-token pointers may be NULL.
+ * Asynchronous; no allocation, no synchronisation.  Malformed cu_seqlens are
+ * clamped on the device (no out-of-range access) and flagged in the workspace
+ * error word. */
+HLA_API int hla_prefill(const hla_params* params, const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* lambda,
+                        const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                        const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                        const hla_state* st, void* ws, size_t ws_bytes, void* stream);
+
+/* One decode step for every sequence of `st`: token pos[n] of sequence n.
+ *   q [N, Hq, d], k, v [N, Hkv, d]  (params->dtype), g, beta [N, Hq] fp32,
+ *   lambda and conv filters as for hla_prefill, out [N, Hq, d].
+ * The token leaving the window (position pos - window, if not a sink) is
+ * absorbed into S first; then the new token's output is formed; pos += 1.
+ * Asynchronous. */
+HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q, const void* k,
+                            const void* v, const float* g, const float* beta, const float* lambda,
+                            const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                            const hla_state* st, void* out, void* stream);
+
+/* Synchronises `stream`, reads the state's device error word into *code
+ * (may be NULL), clears it, and returns HLA_OK if it was zero, else the
+ * matching HLA_ERR_* status. */
+HLA_API int hla_check_device_error(const hla_state* st, void* stream, int32_t* code);
+
+/* Same for the error word at the head of a prefill workspace. */
+HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code);
+
+/* Measurement hook (not part of the layer): for the calling thread, makes
+ * hla_prefill record events[i] (cudaEvent_t handles owned by the caller) on
+ * its stream at stage boundaries: 0 before the first kernel, 1 after the
+ * feature path, 2 after the linear branch, 3 after the softmax + combine,
+ * 4 after the decode-state hand-off.  Entries beyond n_events, or NULL
+ * entries, are skipped; n_events = 0 switches the hook off.  The array must
+ * stay valid while the hook is on. */
+HLA_API int hla_prefill_stage_events(void** events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLA_H */

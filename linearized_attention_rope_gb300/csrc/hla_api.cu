@@ -1,0 +1,288 @@
+// Host side of the libhla C ABI: argument checks, workspace layout, launch
+// order.  Declarations and contracts: include/hla.h.
+#include <cmath>
+#include <cstring>
+
+#include "hla_common.cuh"
+
+using namespace hla;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_params(const hla_params* prm) {
+    if (!prm) return HLA_ERR_INVALID_ARG;
+    if (prm->n_q_heads <= 0 || prm->n_kv_heads <= 0 || prm->n_q_heads % prm->n_kv_heads != 0)
+        return HLA_ERR_INVALID_ARG;
+    if (prm->n_sinks < 0 || prm->window < 1 || !(prm->rope_base > 1.0f)) return HLA_ERR_INVALID_ARG;
+    if (prm->conv_width != kConvWidth) return HLA_ERR_UNSUPPORTED;
+    if (prm->head_dim != 64 && prm->head_dim != 128) return HLA_ERR_UNSUPPORTED;
+    if (prm->dtype != HLA_DTYPE_F32 && prm->dtype != HLA_DTYPE_BF16) return HLA_ERR_UNSUPPORTED;
+    const unsigned known = HLA_FLAG_L2NORM_Q | HLA_FLAG_SOFTMAX_OFF | HLA_FLAG_LINEAR_OFF |
+                           HLA_FLAG_GDN_RECURRENT;
+    if (prm->flags & ~known) return HLA_ERR_INVALID_ARG;
+    return HLA_OK;
+}
+
+LayerDims make_dims(const hla_params* prm, int n_seqs, int64_t total) {
+    LayerDims L;
+    std::memset(&L, 0, sizeof(L));
+    L.Hq = prm->n_q_heads;
+    L.Hkv = prm->n_kv_heads;
+    L.d = prm->head_dim;
+    L.G = prm->n_q_heads / prm->n_kv_heads;
+    L.n_sinks = prm->n_sinks;
+    L.window = prm->window;
+    L.n_seqs = n_seqs;
+    L.total = total;
+    L.flags = prm->flags;
+    for (int i = 0; i < prm->head_dim / 2; ++i)
+        L.theta[i] = std::pow((double)prm->rope_base, -2.0 * i / (double)prm->head_dim);
+    return L;
+}
+
+size_t dtype_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
+// feature (MMA operand) element size: fp32 layer keeps fp32, bf16 layer uses fp16
+size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
+
+// Workspace layout of one prefill.
+struct WsLayout {
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, total;
+    int n_coarse;
+};
+
+WsLayout ws_layout(const hla_params* prm, int64_t total) {
+    WsLayout w;
+    const size_t fb = feat_bytes(prm->dtype), d = (size_t)prm->head_dim, half = d / 2;
+    const size_t Hq = (size_t)prm->n_q_heads, Hkv = (size_t)prm->n_kv_heads, T = (size_t)total;
+    w.n_coarse = (int)(total / 64 + 1);
+    size_t off = 0;
+    w.err = off;    off = align_up(off + 16);
+    w.fine = off;   off = align_up(off + 64 * half * sizeof(float2));
+    w.coarse = off; off = align_up(off + (size_t)w.n_coarse * half * sizeof(float2));
+    w.qr = off;     off = align_up(off + T * Hq * d * fb);
+    w.kr = off;     off = align_up(off + T * Hkv * d * fb);
+    w.qhat = off;   off = align_up(off + T * Hq * d * fb);
+    w.khat = off;   off = align_up(off + T * Hkv * d * fb);
+    w.vhat = off;   off = align_up(off + T * Hkv * d * fb);
+    w.olin = off;   off = align_up(off + T * Hq * d * sizeof(float));
+    w.total = off;
+    return w;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? HLA_OK : HLA_ERR_CUDA; }
+
+// Measurement hook: events recorded between the stages of hla_prefill on the
+// calling thread (see hla_prefill_stage_events).
+thread_local cudaEvent_t* t_stage_events = nullptr;
+thread_local int t_n_stage_events = 0;
+
+cudaError_t mark_stage(int i, cudaStream_t s) {
+    if (i < t_n_stage_events && t_stage_events[i]) return cudaEventRecord(t_stage_events[i], s);
+    return cudaSuccess;
+}
+
+#define HLA_TRY(...)                                           \
+    do {                                                       \
+        cudaError_t e_ = (__VA_ARGS__);                             \
+        if (e_ != cudaSuccess) return HLA_ERR_CUDA;            \
+    } while (0)
+
+template <typename Tin, typename Tf>
+int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const void* k,
+                const void* v, const float* g, const float* beta, const float* lambda,
+                const float* wq, const float* wk, const float* wv, const int32_t* cu, void* out,
+                const hla_state* st, char* ws, const WsLayout& w, cudaStream_t stream) {
+    (void)prm;
+    int32_t* err = reinterpret_cast<int32_t*>(ws + w.err);
+    float2* fine = reinterpret_cast<float2*>(ws + w.fine);
+    float2* coarse = reinterpret_cast<float2*>(ws + w.coarse);
+    Tf* qr = reinterpret_cast<Tf*>(ws + w.qr);
+    Tf* kr = reinterpret_cast<Tf*>(ws + w.kr);
+    Tf* qh = reinterpret_cast<Tf*>(ws + w.qhat);
+    Tf* kh = reinterpret_cast<Tf*>(ws + w.khat);
+    Tf* vh = reinterpret_cast<Tf*>(ws + w.vhat);
+    float* olin = reinterpret_cast<float*>(ws + w.olin);
+    const Tin* qi = static_cast<const Tin*>(q);
+    const Tin* ki = static_cast<const Tin*>(k);
+    const Tin* vi = static_cast<const Tin*>(v);
+
+    HLA_TRY(cudaMemsetAsync(err, 0, 16, stream));
+    HLA_TRY(mark_stage(0, stream));
+    HLA_TRY(launch_rope_tables(L, fine, coarse, w.n_coarse, stream));
+    HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
+                                     err, stream));
+    HLA_TRY(mark_stage(1, stream));
+    HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, st ? st->S : nullptr, stream));
+    HLA_TRY(mark_stage(2, stream));
+    HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
+                                           stream));
+    HLA_TRY(mark_stage(3, stream));
+    if (st) HLA_TRY(launch_state_fill<Tin, Tf>(L, qi, ki, vi, g, beta, kh, vh, cu, *st, stream));
+    HLA_TRY(mark_stage(4, stream));
+    return HLA_OK;
+}
+
+bool state_ok(const hla_state* st) {
+    if (!st) return false;
+    const void* ptrs[] = {st->S, st->k_ring, st->v_ring, st->pend_k, st->pend_v, st->pend_g,
+                          st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return false;
+    return true;
+}
+
+int read_error_word(int32_t* dev, cudaStream_t stream, int32_t* code) {
+    int32_t h[4] = {0, 0, 0, 0};
+    HLA_TRY(cudaStreamSynchronize(stream));
+    HLA_TRY(cudaMemcpy(h, dev, sizeof(h), cudaMemcpyDeviceToHost));
+    HLA_TRY(cudaMemset(dev, 0, sizeof(h)));
+    if (code) *code = h[0];
+    if (h[0] == 0) return HLA_OK;
+    if (h[0] == kErrTimeout) return HLA_ERR_TIMEOUT;
+    return HLA_ERR_STATE;
+}
+
+}  // namespace
+
+extern "C" {
+
+HLA_API const char* hla_status_string(int status) {
+    switch (status) {
+        case HLA_OK: return "ok";
+        case HLA_ERR_INVALID_ARG: return "invalid argument";
+        case HLA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case HLA_ERR_STATE: return "inconsistent state or sequence table";
+        case HLA_ERR_CUDA: return "CUDA error";
+        case HLA_ERR_TIMEOUT: return "device-side wait timed out";
+        case HLA_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+HLA_API int hla_state_bytes(const hla_params* prm, int n_seqs, hla_state_sizes* out) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (n_seqs < 0 || !out) return HLA_ERR_INVALID_ARG;
+    const size_t N = (size_t)n_seqs, Hq = (size_t)prm->n_q_heads, Hkv = (size_t)prm->n_kv_heads;
+    const size_t d = (size_t)prm->head_dim, R = (size_t)(prm->n_sinks + prm->window);
+    const size_t P = (size_t)prm->window + 1, eb = dtype_bytes(prm->dtype);
+    out->S = N * Hq * d * d * 4;
+    out->k_ring = N * Hkv * R * d * eb;
+    out->v_ring = out->k_ring;
+    out->pend_k = N * Hkv * P * d * 4;
+    out->pend_v = out->pend_k;
+    out->pend_g = N * Hq * P * 4;
+    out->pend_beta = out->pend_g;
+    out->conv_q = N * kConvHalo * Hq * d * 4;
+    out->conv_k = N * kConvHalo * Hkv * d * 4;
+    out->conv_v = out->conv_k;
+    out->pos = N * 8;
+    out->err = 16;
+    return HLA_OK;
+}
+
+HLA_API int hla_prefill_workspace_bytes(const hla_params* prm, int64_t total_tokens, int n_seqs,
+                                        size_t* bytes) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (total_tokens < 0 || n_seqs < 0 || !bytes) return HLA_ERR_INVALID_ARG;
+    *bytes = ws_layout(prm, total_tokens).total;
+    return HLA_OK;
+}
+
+HLA_API int hla_state_init(const hla_params* prm, int n_seqs, const hla_state* st, void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (n_seqs < 0 || !state_ok(st)) return HLA_ERR_INVALID_ARG;
+    hla_state_sizes sz;
+    hla_state_bytes(prm, n_seqs, &sz);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ptrs[] = {st->S, st->k_ring, st->v_ring, st->pend_k, st->pend_v, st->pend_g,
+                    st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err};
+    size_t sizes[] = {sz.S, sz.k_ring, sz.v_ring, sz.pend_k, sz.pend_v, sz.pend_g,
+                      sz.pend_beta, sz.conv_q, sz.conv_k, sz.conv_v, sz.pos, sz.err};
+    for (int i = 0; i < 12; ++i)
+        if (sizes[i]) HLA_TRY(cudaMemsetAsync(ptrs[i], 0, sizes[i], s));
+    return HLA_OK;
+}
+
+HLA_API int hla_prefill(const hla_params* prm, const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* lambda,
+                        const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                        const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                        const hla_state* st, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (n_seqs < 1 || total_tokens < 0 || total_tokens > (int64_t)INT32_MAX) return HLA_ERR_INVALID_ARG;
+    // with no tokens, the per-token tensors may be empty (null)
+    const void* ptrs[] = {cu_seqlens, ws, lambda, conv_wq, conv_wk, conv_wv, q, k, v, g, beta, out};
+    const int n_required = total_tokens > 0 ? 12 : 2;
+    for (int i = 0; i < 12; ++i) {
+        if (!ptrs[i] && i >= n_required) continue;
+        if (!ptrs[i] || !aligned16(ptrs[i])) return HLA_ERR_INVALID_ARG;
+    }
+    if (st && !state_ok(st)) return HLA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(prm, total_tokens);
+    if (ws_bytes < w.total) return HLA_ERR_WORKSPACE;
+    const LayerDims L = make_dims(prm, n_seqs, total_tokens);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* wsb = static_cast<char*>(ws);
+    if (total_tokens == 0) {
+        // nothing to compute; a given state keeps its freshly initialised contents
+        HLA_TRY(cudaMemsetAsync(wsb + w.err, 0, 16, s));
+        return HLA_OK;
+    }
+    if (prm->dtype == HLA_DTYPE_F32)
+        return run_prefill<float, float>(prm, L, q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv,
+                                         cu_seqlens, out, st, wsb, w, s);
+    return run_prefill<__nv_bfloat16, __half>(prm, L, q, k, v, g, beta, lambda, conv_wq, conv_wk,
+                                              conv_wv, cu_seqlens, out, st, wsb, w, s);
+}
+
+HLA_API int hla_decode_step(const hla_params* prm, int n_seqs, const void* q, const void* k,
+                            const void* v, const float* g, const float* beta, const float* lambda,
+                            const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                            const hla_state* st, void* out, void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (n_seqs < 0) return HLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv, out};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return HLA_ERR_INVALID_ARG;
+    if (!state_ok(st)) return HLA_ERR_INVALID_ARG;
+    if (n_seqs == 0) return HLA_OK;
+    const LayerDims L = make_dims(prm, n_seqs, 0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prm->dtype == HLA_DTYPE_F32)
+        return cuda_status(launch_decode_step<float>(
+            L, static_cast<const float*>(q), static_cast<const float*>(k),
+            static_cast<const float*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, *st,
+            static_cast<float*>(out), s));
+    return cuda_status(launch_decode_step<__nv_bfloat16>(
+        L, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, *st,
+        static_cast<__nv_bfloat16*>(out), s));
+}
+
+HLA_API int hla_check_device_error(const hla_state* st, void* stream, int32_t* code) {
+    if (!st || !st->err) return HLA_ERR_INVALID_ARG;
+    return read_error_word(st->err, static_cast<cudaStream_t>(stream), code);
+}
+
+HLA_API int hla_prefill_stage_events(void** events, int n_events) {
+    if (n_events < 0 || (n_events > 0 && !events)) return HLA_ERR_INVALID_ARG;
+    t_stage_events = reinterpret_cast<cudaEvent_t*>(events);
+    t_n_stage_events = n_events;
+    return HLA_OK;
+}
+
+HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code) {
+    if (!ws || !aligned16(ws)) return HLA_ERR_INVALID_ARG;
+    return read_error_word(static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream), code);
+}
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+// Shared device-side definitions of libhla (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hla.h"
+
+namespace hla {
+
+constexpr int kConvWidth = 8;
+constexpr int kConvHalo = kConvWidth - 1;  // rows of history the conv needs
+constexpr int kMaxHalfDim = 64;            // head_dim <= 128
+
+// device error word codes (written with atomicExch / plain stores)
+constexpr int kErrSeqlens = 1;   // cu_seqlens not monotone / not ending at total
+constexpr int kErrTimeout = 2;   // a bounded wait ran out
+constexpr int kErrState = 3;     // decode position inconsistent with the state
+
+// Per-launch constants, passed by value.  theta[i] = base^(-2i/d) computed on
+// the host in double precision.
+struct LayerDims {
+    int Hq, Hkv, d, G;  // G = Hq / Hkv
+    int n_sinks, window;
+    int n_seqs;
+    int64_t total;
+    unsigned flags;
+    double theta[kMaxHalfDim];
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+
+// Loads E (2 or 4) consecutive elements starting at an E-aligned index as fp32.
+template <int E> __device__ __forceinline__ void load_vec(const float* p, float* o) {
+    if constexpr (E == 4) { float4 x = *reinterpret_cast<const float4*>(p); o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; }
+    else { float2 x = *reinterpret_cast<const float2*>(p); o[0] = x.x; o[1] = x.y; }
+}
+template <int E> __device__ __forceinline__ void load_vec(const __half* p, float* o) {
+    if constexpr (E == 4) {
+        uint2 x = *reinterpret_cast<const uint2*>(p);
+        float2 a = __half22float2(*reinterpret_cast<__half2*>(&x.x));
+        float2 b = __half22float2(*reinterpret_cast<__half2*>(&x.y));
+        o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    } else {
+        unsigned x = *reinterpret_cast<const unsigned*>(p);
+        float2 a = __half22float2(*reinterpret_cast<__half2*>(&x));
+        o[0] = a.x; o[1] = a.y;
+    }
+}
+template <int E> __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* o) {
+    if constexpr (E == 4) {
+        uint2 x = *reinterpret_cast<const uint2*>(p);
+        float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x.x));
+        float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x.y));
+        o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    } else {
+        unsigned x = *reinterpret_cast<const unsigned*>(p);
+        float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x));
+        o[0] = a.x; o[1] = a.y;
+    }
+}
+
+// Sequence that owns global token t: largest s with cu[s] <= t (cu clamped to
+// [0, total] so a malformed table can never send an access out of range).
+__device__ __forceinline__ int seq_of_token(const int32_t* __restrict__ cu, int n_seqs, int64_t t) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int64_t clamp_i64(int64_t x, int64_t lo, int64_t hi) {
+    return x < lo ? lo : (x > hi ? hi : x);
+}
+
+// (start, length) of sequence s, clamped into [0, total].
+__device__ __forceinline__ void seq_range(const int32_t* __restrict__ cu, int s, int64_t total,
+                                          int64_t* start, int64_t* len) {
+    int64_t a = clamp_i64(__ldg(cu + s), 0, total);
+    int64_t b = clamp_i64(__ldg(cu + s + 1), a, total);
+    *start = a;
+    *len = b - a;
+}
+
+// cos/sin of p * theta with the angle formed and reduced to [-pi, pi] in
+// double precision, then evaluated in fp32 (used where few angles are needed).
+__device__ __forceinline__ void rope_cs_exact(int64_t p, double theta, float* c, float* s) {
+    const double two_pi = 6.283185307179586476925286766559;
+    double a = (double)p * theta;
+    a -= two_pi * rint(a / two_pi);
+    sincosf((float)a, s, c);
+}
+
+// ---- kernel launchers (each returns the cudaError_t of its launch) --------
+
+// RoPE tables: fine[b][i] = (cos, sin)(b * theta_i), b < 64;
+// coarse[a][i] = (cos, sin)(64 a * theta_i), a < n_coarse.
+cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
+                               cudaStream_t st);
+
+// Feature path for every (token, head): RoPE'd q/k, and qhat, khat, vhat.
+// Tf = float (fp32 layer) or __half (bf16 layer).
+template <typename Tin, typename Tf>
+cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
+                            const float* wq, const float* wk, const float* wv, const int32_t* cu,
+                            const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
+                            Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st);
+
+// Token-serial fp32 GDN with delayed absorption: o_lin [total, Hq, d] fp32
+// for positions p >= n_sinks + window; final S into S_out (may be null).
+template <typename Tf>
+cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* khat, const Tf* vhat,
+                                 const float* g, const float* beta, const int32_t* cu, float* o_lin,
+                                 float* S_out, cudaStream_t st);
+
+// Sink + window softmax with the lambda-weighted linear branch added.
+template <typename Tin, typename Tf>
+cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr, const Tin* v,
+                                  const float* o_lin, const float* lambda, const int32_t* cu,
+                                  Tin* out, cudaStream_t st);
+
+// Prefill -> decode state hand-off.
+template <typename Tin, typename Tf>
+cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
+                              const float* g, const float* beta, const Tf* khat, const Tf* vhat,
+                              const int32_t* cu, const hla_state& s, cudaStream_t st);
+
+// One decode step for all sequences, then pos += 1.
+template <typename Tin>
+cudaError_t launch_decode_step(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
+                               const float* g, const float* beta, const float* lambda,
+                               const float* wq, const float* wk, const float* wv,
+                               const hla_state& s, Tin* out, cudaStream_t st);
+
+}  // namespace hla
