@@ -167,9 +167,11 @@ class State:
         return self
 
     def check_error(self, stream=None) -> int:
+        """Synchronises, reads and clears the device error word; returns it (0 = fine)."""
         code = ctypes.c_int32()
-        _check(load().hla_check_device_error(ctypes.byref(self.c), _stream(stream),
-                                             ctypes.byref(code)), "device error word")
+        rc = load().hla_check_device_error(ctypes.byref(self.c), _stream(stream), ctypes.byref(code))
+        if rc not in (HLA_OK, HLA_ERR_STATE, HLA_ERR_TIMEOUT):
+            _check(rc, "device error word")
         return code.value
 
 
@@ -202,9 +204,11 @@ def decode_step(params: Params, q, k, v, g, beta, lam, wq, wk, wv, state: State,
 
 
 def check_workspace_error(ws, stream=None) -> int:
+    """Synchronises, reads and clears a prefill workspace's error word; returns it."""
     code = ctypes.c_int32()
-    _check(load().hla_check_workspace_error(_ptr(ws), _stream(stream), ctypes.byref(code)),
-           "workspace error word")
+    rc = load().hla_check_workspace_error(_ptr(ws), _stream(stream), ctypes.byref(code))
+    if rc not in (HLA_OK, HLA_ERR_STATE, HLA_ERR_TIMEOUT):
+        _check(rc, "workspace error word")
     return code.value
 
 
