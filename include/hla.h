@@ -160,6 +160,30 @@ HLA_API int hla_prefill(const hla_params* params, const void* q, const void* k, 
                         const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
                         const hla_state* st, void* ws, size_t ws_bytes, void* stream);
 
+/* hla_prefill without a caller-supplied workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc, for instance a plugin inside a host framework that owns every
+ * byte of device memory through its own pool and gives the plugin no
+ * allocator, or a latency-critical caller that cannot afford the implicit
+ * device-wide synchronisation of cudaMalloc/cudaFree.
+ * Arguments and results are those of hla_prefill; the scratch memory comes
+ * from a 64 MiB buffer inside the library (one per GPU that loads it, held
+ * until the process exits).  Prefills whose hla_prefill_workspace_bytes
+ * exceeds 64 MiB (about 1,700 tokens of a 32 q / 8 kv head, head_dim 128
+ * bf16 layer) return HLA_ERR_WORKSPACE before any GPU work.
+ * The first call on each device looks up the buffer's device address (a
+ * host-side set-up step); make that first call before any stream capture.
+ * It allocates nothing: no cudaMalloc, no cudaFree.
+ * All calls share the one buffer and each overwrites what the last left in
+ * it: calls that overlap on the GPU (other streams, other threads) race, so
+ * order them on one stream.  The buffer's device error word is not readable
+ * by the caller. */
+HLA_API int hla_prefill_noalloc(const hla_params* params, const void* q, const void* k,
+                                const void* v, const float* g, const float* beta,
+                                const float* lambda, const float* conv_wq, const float* conv_wk,
+                                const float* conv_wv, const int32_t* cu_seqlens, int n_seqs,
+                                int64_t total_tokens, void* out, const hla_state* st, void* stream);
+
 /* One decode step for every sequence of `st`: token pos[n] of sequence n.
  *   q [N, Hq, d], k, v [N, Hkv, d]  (params->dtype), g, beta [N, Hq] fp32,
  *   lambda and conv filters as for hla_prefill, out [N, Hq, d].

@@ -81,6 +81,8 @@ def load():
         lib.hla_check_device_error.argtypes = [S, _vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_check_workspace_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_prefill_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+        lib.hla_prefill_noalloc.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, S, _vp]
+        lib.hla_prefill_noalloc.restype = ctypes.c_int
         for fn in ("hla_state_bytes", "hla_prefill_workspace_bytes", "hla_state_init", "hla_prefill",
                    "hla_decode_step", "hla_check_device_error", "hla_check_workspace_error",
                    "hla_prefill_stage_events"):
@@ -227,3 +229,15 @@ def set_prefill_stage_events(events):
         return
     _stage_handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(load().hla_prefill_stage_events(_stage_handles, len(events)), "hla_prefill_stage_events")
+
+
+def prefill_noalloc(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out, state=None,
+                    stream=None):
+    """hla_prefill_noalloc: the prefill with the library's own 64 MiB scratch, for
+    callers that cannot allocate device memory; raises HlaError(HLA_ERR_WORKSPACE)
+    for prefills that need more scratch than that."""
+    rc = load().hla_prefill_noalloc(ctypes.byref(params.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                    _ptr(beta), _ptr(lam), _ptr(wq), _ptr(wk), _ptr(wv),
+                                    _ptr(cu_seqlens), cu_seqlens.numel() - 1, q.shape[0], _ptr(out),
+                                    None if state is None else ctypes.byref(state.c), _stream(stream))
+    _check(rc, "hla_prefill_noalloc")
