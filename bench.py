@@ -183,8 +183,19 @@ def source_hash(files) -> str:
 
 # ---------------------------------------------------------------------------
 # prefill
-GDN_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
-               "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+GDN_RECURRENT_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
+                         "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+GDN_CHUNKED_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_chunked.cu",
+                       "linearized_attention_rope_gb300/csrc/umma.cuh",
+                       "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+
+
+def chunked_gdn_flops_per_token_head(d: int = 128, C: int = 64) -> float:
+    """Useful flops of the chunked GDN per absorbed token and q-head: the three
+    d x d products (W S0, Q S0, Kt^T U), the Gram triangle, the triangular
+    solve, and U~, Wm, masked Q K^T, P U (triangles halved)."""
+    macs = 3 * d * d + (C - 1) * d / 2 + (C * C - 1) / 6 + 4 * (C + 1) * d / 2
+    return 2.0 * macs
 
 
 def prefill_work(wl):
@@ -197,16 +208,23 @@ def prefill_work(wl):
         for p in range(L):
             keys += min(p + 1, wl.n_sinks) + max(0, min(wl.window, p + 1 - wl.n_sinks))
     eb = 2 if wl.dtype == "bf16" else 4
-    return {
+    if wl.dtype == "bf16" and d == 128:
+        gdn = {"bound": "tensor", "flops": chunked_gdn_flops_per_token_head(d) * absorbed * Hq,
+               "unit": "TFLOP/s", "sources": GDN_CHUNKED_SOURCES, "kernel": "gdn_chunked_kernel"}
+    else:
         # token-serial delta rule: k^T S, the rank-1 update, q^T S -> 6 d^2 flops per token-head
-        "gdn": {"bound": "alu", "flops": 6.0 * d * d * absorbed * Hq, "peak": FP32_ALU_TFLOPS,
-                "unit": "TFLOP/s", "sources": GDN_SOURCES},
+        gdn = {"bound": "alu", "flops": 6.0 * d * d * absorbed * Hq, "peak": FP32_ALU_TFLOPS,
+               "unit": "TFLOP/s", "sources": GDN_RECURRENT_SOURCES, "kernel": "gdn_recurrent_kernel"}
+    return {
+        "gdn": gdn,
         # q.k and p.v over the visible keys of every (token, q-head)
         "softmax": {"bound": "alu", "flops": 4.0 * d * keys * Hq, "peak": FP32_ALU_TFLOPS,
-                    "unit": "TFLOP/s", "sources": ["linearized_attention_rope_gb300/csrc/window_softmax.cu"]},
+                    "unit": "TFLOP/s", "sources": ["linearized_attention_rope_gb300/csrc/window_softmax.cu"],
+                    "kernel": "window_softmax_kernel"},
         # read q, k, v; write RoPE'd q, k and qhat, khat, vhat
         "features": {"bound": "hbm", "bytes": float(T * d * ((Hq + 2 * Hkv) * eb + (2 * Hq + 3 * Hkv) * eb)),
-                     "unit": "GB/s", "sources": ["linearized_attention_rope_gb300/csrc/features.cu"]},
+                     "unit": "GB/s", "sources": ["linearized_attention_rope_gb300/csrc/features.cu"],
+                     "kernel": "features_kernel"},
         "absorbed_token_heads": absorbed * Hq,
     }
 
@@ -269,9 +287,9 @@ def run_prefill_bench(args, dist, peaks):
         achieved, peak = w["flops"] / sec / 1e12, peaks["bf16_tflops"]
     else:
         achieved, peak = w["flops"] / sec / 1e12, w["peak"]
-    roofline = {"kernel": top, "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
+    roofline = {"kernel": w["kernel"], "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
                 "unit": w["unit"], "frac": round(achieved / peak, 5),
-                "traffic": kernel_traffic(top, w["sources"]),
+                "traffic": kernel_traffic(w["kernel"], w["sources"]),
                 "peak_source": peaks["source"] if w["bound"] != "alu" else FP32_ALU_TFLOPS_DERIVATION}
 
     # end to end through the C ABI: pinned host inputs in, result back to pinned host memory

@@ -2,6 +2,7 @@
 // order.  Declarations and contracts: include/hla.h.
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include "hla_common.cuh"
 
@@ -116,7 +117,16 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
                                      err, stream));
     HLA_TRY(mark_stage(1, stream));
-    HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, st ? st->S : nullptr, stream));
+    float* S_out = st ? st->S : nullptr;
+    bool chunked = false;
+    if constexpr (std::is_same<Tf, __half>::value)
+        chunked = L.d == 128 && !(L.flags & HLA_FLAG_GDN_RECURRENT);
+    if (chunked) {
+        if constexpr (std::is_same<Tf, __half>::value)
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, g, beta, cu, olin, S_out, err, stream));
+    } else {
+        HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
+    }
     HLA_TRY(mark_stage(2, stream));
     HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
                                            stream));

@@ -126,6 +126,12 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
                                  const float* g, const float* beta, const int32_t* cu, float* o_lin,
                                  float* S_out, cudaStream_t st);
 
+// Chunked (C = 64) GDN with delayed absorption on tcgen05 tensor cores,
+// head_dim 128, fp16 features: same outputs as launch_gdn_recurrent.
+cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat,
+                               const __half* vhat, const float* g, const float* beta, const int32_t* cu,
+                               float* o_lin, float* S_out, int32_t* err, cudaStream_t st);
+
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>
 cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr, const Tin* v,

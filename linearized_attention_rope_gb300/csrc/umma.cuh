@@ -1,0 +1,145 @@
+// Thin wrappers over the sm_100-family tensor-core instructions used by the
+// chunked kernels: tcgen05 MMA with fp16 operands in shared memory and fp32
+// accumulators in tensor memory (TMEM), TMEM allocation and loads, and
+// mbarrier waits with an iteration limit.
+//
+// Shared-memory operand tiles use the 128-byte swizzle: a tile is stored as
+// blocks of 64 16-bit elements per row (128 B), rows consecutive, and inside
+// each 8-row, 1024-byte atom the 16-byte chunk index is XORed with the row
+// index mod 8.  `sw128_offset` gives the byte offset of element (row, col) for
+// a tile with `rows` rows.  The same physical layout serves as
+//   - a K-major operand (rows = M or N, cols = K): descriptor SBO = 1024, and
+//     each K step of 16 elements starts 32 B further inside the same block;
+//   - an MN-major operand (rows = K, cols = M or N): descriptor LBO = the
+//     byte stride between 64-column blocks, SBO = 1024, and each K step of
+//     16 rows starts 2048 B further.
+#pragma once
+
+#include <stdint.h>
+
+namespace hla {
+namespace umma {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
+    const uint32_t blk = (uint32_t)col >> 6, c = (uint32_t)col & 63u;
+    const uint32_t chunk = c >> 3, within = (c & 7u) * 2u;
+    return blk * (uint32_t)rows * 128u + (uint32_t)row * 128u + ((chunk ^ ((uint32_t)row & 7u)) << 4) + within;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for this architecture family
+    d |= (uint64_t)2 << 61;  // 128-byte swizzle
+    return d;
+}
+
+// K-major tile descriptor at K step `s` (16 elements); `rows` = rows of the tile.
+__device__ __forceinline__ uint64_t kmajor(uint32_t base, int rows, int s) {
+    return sdesc(base + (uint32_t)(s >> 2) * (uint32_t)rows * 128u + (uint32_t)(s & 3) * 32u, 16u, 1024u);
+}
+
+// MN-major tile descriptor at K step `s` (16 rows); `block_stride` = bytes
+// between 64-column blocks.
+__device__ __forceinline__ uint64_t mnmajor(uint32_t base, uint32_t block_stride, int s) {
+    return sdesc(base + (uint32_t)s * 2048u, block_stride, 1024u);
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 accumulator.
+__host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn, bool neg_b) {
+    uint32_t d = 1u << 4;  // D: f32; A, B: f16 (format 0)
+    d |= (uint32_t)neg_b << 14;
+    d |= (uint32_t)a_mn << 15;
+    d |= (uint32_t)b_mn << 16;
+    d |= (uint32_t)(N >> 3) << 17;
+    d |= (uint32_t)(M >> 4) << 24;
+    return d;
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+// Arrives on the mbarrier once every MMA issued so far by this thread completes.
+__device__ __forceinline__ void commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of the mbarrier; gives up after `limit` polls
+// (each poll may itself suspend for a while) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(mbar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole-warp TMEM allocation; the base address is written to *dst (shared).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32 (w % 4) .. + 31).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace umma
+}  // namespace hla
