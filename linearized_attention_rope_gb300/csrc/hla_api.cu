@@ -128,8 +128,16 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
         HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
     }
     HLA_TRY(mark_stage(2, stream));
-    HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
-                                           stream));
+    bool softmax_tc = false;
+    if constexpr (std::is_same<Tf, __half>::value) softmax_tc = window_softmax_tc_supported(L);
+    if (softmax_tc) {
+        if constexpr (std::is_same<Tf, __half>::value)
+            HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out), err,
+                                             stream));
+    } else {
+        HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
+                                               stream));
+    }
     HLA_TRY(mark_stage(3, stream));
     if (st) HLA_TRY(launch_state_fill<Tin, Tf>(L, qi, ki, vi, g, beta, kh, vh, cu, *st, stream));
     HLA_TRY(mark_stage(4, stream));

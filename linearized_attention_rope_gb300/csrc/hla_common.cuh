@@ -138,6 +138,12 @@ cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr
                                   const float* o_lin, const float* lambda, const int32_t* cu,
                                   Tin* out, cudaStream_t st);
 
+// Sink + window softmax on tcgen05 (bf16 layer, head_dim 128, G in {1,2,4,8}).
+bool window_softmax_tc_supported(const LayerDims& L);
+cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr,
+                                     const __nv_bfloat16* v, const float* o_lin, const float* lambda,
+                                     const int32_t* cu, __nv_bfloat16* out, int32_t* err, cudaStream_t st);
+
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>
 cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,

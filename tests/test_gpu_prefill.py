@@ -54,9 +54,11 @@ def test_small_ragged_all_units(oracle_mod, dtype, d):
     check_prefill(wl, x, out, st, all_units(wl), oracle_mod)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("n_sinks,window", [(0, 1), (0, 40), (8, 1), (3, 7), (8, 120), (16, 400)])
-def test_budget_variants(oracle_mod, n_sinks, window):
-    wl = synth.small(f"budget {n_sinks}+{window}", [300, 77], n_q_heads=2, n_kv_heads=1, head_dim=64,
+def test_budget_variants(oracle_mod, n_sinks, window, d):
+    # windows over 128 keys make the tensor-core softmax merge several key groups
+    wl = synth.small(f"budget {n_sinks}+{window}", [300, 77, 530], n_q_heads=4, n_kv_heads=1, head_dim=d,
                      n_sinks=n_sinks, window=window)
     x = synth.make_inputs(wl, "cuda")
     out, st = run_prefill(wl, x, with_state=True)
@@ -132,7 +134,10 @@ def test_varlen_packing_matches_separate_runs():
         sub["cu_seqlens"] = torch.tensor([0, b - a], dtype=torch.int32, device="cuda")
         wl1 = synth.small("one", [b - a], n_q_heads=4, n_kv_heads=2, head_dim=128)
         o1, _ = run_prefill(wl1, sub)
-        assert torch.equal(o1, out[a:b]), f"sequence {n}"
+        # same arithmetic per row; only the tensor-core summation order over key
+        # slots differs (blocks follow the global token index), so compare to rounding
+        assert_close(o1.float().cpu().numpy(), out[a:b].float().cpu().numpy(), "bf16", f"sequence {n}")
+        assert (o1.float() - out[a:b].float()).abs().max().item() <= 2e-2
 
 
 def test_gqa_equals_mha_with_repeated_kv():
