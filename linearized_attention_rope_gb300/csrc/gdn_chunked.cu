@@ -19,8 +19,8 @@
 //   D_W    [dk x tok]     = K^T (T diag(beta gamma))^T          (= Wm^T)
 //   D_O    [dv x tok]     = S0^T (diag(gamma) Q)^T,  then  += U^T P^T
 //   D_S    [dv x dk]      = U^T Kt                             (= (Kt^T U)^T)
-// The triangular inverse T is formed on the CUDA cores in fp32 (16 x 16
-// diagonal blocks by forward substitution, then block rows).
+// The triangular inverse T is formed on the CUDA cores in fp32 (32 x 32
+// diagonal blocks by warp-level forward substitution, then one block merge).
 //
 // One CTA of 256 threads per (sequence, q-head), head_dim 128.  Thread t owns
 // TMEM lane L = 32 (warp % 4) + lane and the column half wg = warp / 4.
@@ -37,17 +37,21 @@ constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared-memory plan (bytes from a 1024-aligned base)
-constexpr uint32_t kStack = 0;                 // [K ; Q] 128 x 128 fp16, later [Kt ; gamma Q]
-constexpr uint32_t kVt = kStack + 32768;       // V (MN-major A), later Wm^T (MN-major B)
-constexpr uint32_t kP = kVt + 16384;           // P 64 x 64 K-major
+// The stack and V tiles are double-buffered: chunk c + 1 streams in (cp.async)
+// while chunk c is processed.
+constexpr uint32_t kStack0 = 0;                // [K ; Q] 128 x 128 fp16, later [Kt ; gamma Q]
+constexpr uint32_t kStack1 = 32768;
+constexpr uint32_t kVt0 = 65536;               // V (MN-major A), later Wm^T (MN-major B)
+constexpr uint32_t kVt1 = 81920;
+constexpr uint32_t kP = 98304;                 // P 64 x 64 K-major
 constexpr uint32_t kTb = kP + 8192;            // T diag(beta)
 constexpr uint32_t kTbg = kTb + 8192;          // T diag(beta gamma)
 constexpr uint32_t kSt = kTbg + 8192;          // S0^T 128 x 128 K-major
 constexpr uint32_t kUt = kSt + 32768;          // U^T 128 x 64 K-major
 constexpr uint32_t kA32 = kUt + 16384;         // A fp32 [64][68]
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;  // T fp32 [64][68]
-constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;  // block products [3][16][17]
-constexpr uint32_t kVec = kX32 + 3 * 16 * 17 * 4;  // G, beta, gamma, Kt decay: 4 x 64 fp32
+constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;  // block product [32][36]
+constexpr uint32_t kVec = kX32 + 32 * 36 * 4;  // G (log2 units), beta, gamma, Kt decay: 4 x 64 fp32
 constexpr uint32_t kSmemBytes = kVec + 4 * 64 * 4 + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for the 1024-byte alignment
 
@@ -76,6 +80,15 @@ __device__ __forceinline__ void unpack8(uint4 u, float* v) {
         v[2 * i + 1] = f.y;
     }
 }
+// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 scale8(uint4 u, float s) {
     float v[8];
     unpack8(u, v);
@@ -84,26 +97,26 @@ __device__ __forceinline__ uint4 scale8(uint4 u, float s) {
     return pack8(v);
 }
 
-// Forward substitution for a 16 x 16 unit lower-triangular block: each
-// 16-lane half-warp inverts one block (lane l owns row l).
-__device__ __forceinline__ void invert_diag_block(const float* sA, float* sT, int b, int l) {
-    float a[16], t[16];
+// Forward substitution for a 32 x 32 unit lower-triangular diagonal block of
+// (I + A): one warp per block, lane l owns row l of the inverse.
+__device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, int b, int l) {
+    float a[32], t[32];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        a[m] = sA[(16 * b + l) * 68 + 16 * b + m];
+    for (int m = 0; m < 32; ++m) {
+        a[m] = sA[(32 * b + l) * 68 + 32 * b + m];
         t[m] = (m == l) ? 1.f : 0.f;
     }
 #pragma unroll
-    for (int m = 0; m < 15; ++m) {
+    for (int m = 0; m < 31; ++m) {
         // row m is final once rows 0..m-1 have been folded into it
 #pragma unroll
         for (int k = 0; k <= m; ++k) {
-            const float tm = __shfl_sync(0xffffffffu, t[k], m, 16);
+            const float tm = __shfl_sync(0xffffffffu, t[k], m);
             if (l > m) t[k] = fmaf(-a[m], tm, t[k]);
         }
     }
 #pragma unroll
-    for (int m = 0; m < 16; ++m) sT[(16 * b + l) * 68 + 16 * b + m] = t[m];
+    for (int m = 0; m < 32; ++m) sT[(32 * b + l) * 68 + 32 * b + m] = t[m];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -173,16 +186,42 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         __syncthreads();
     };
 
+    // chunk rows -> (stack, V) buffer `buf` with cp.async; gates -> registers
+    float g_next = 0.f, b_next = 0.f;
+    auto prefetch = [&](int cc, int buf) {
+        const int64_t pj0 = L.n_sinks + (int64_t)cc * kC;
+        const int pnv = (int)min((int64_t)kC, j_end - pj0);
+        unsigned char* stk = sm + (buf ? kStack1 : kStack0);
+        unsigned char* vt = sm + (buf ? kVt1 : kVt0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
+            const uint32_t nb = r < pnv ? 16u : 0u;
+            const size_t t = (size_t)(start + pj0 + (r < pnv ? r : 0));
+            cp_async16(stk + umma::sw128_offset(r, c8, 128), khat + (t * L.Hkv + kv) * kD + c8, nb);
+            cp_async16(stk + umma::sw128_offset(64 + r, c8, 128), qhat + ((t + W) * L.Hq + h) * kD + c8, nb);
+            cp_async16(vt + umma::sw128_offset(r, c8, 64), vhat + (t * L.Hkv + kv) * kD + c8, nb);
+        }
+        cp_async_commit();
+        if (tid < kC) {
+            const size_t t = (size_t)(start + pj0 + tid);
+            g_next = tid < pnv ? g[t * L.Hq + h] : 0.f;
+            b_next = tid < pnv ? beta[t * L.Hq + h] : 0.f;
+        }
+    };
+    if (n_chunks > 0) prefetch(0, 0);
+
     for (int c = 0; c < n_chunks && ok; ++c) {
         const int64_t j0 = L.n_sinks + (int64_t)c * kC;
         const int nv = (int)min((int64_t)kC, j_end - j0);
+        const uint32_t oStk = (c & 1) ? kStack1 : kStack0;
+        const uint32_t oVt = (c & 1) ? kVt1 : kVt0;
 
         // ---- 1. gates of the chunk: G (inclusive cumsum), beta, gamma, Kt decay
         float gcum = 0.f;
         if (tid < kC) {
-            const size_t t = (size_t)(start + j0 + tid);
-            float gi = tid < nv ? g[t * L.Hq + h] : 0.f;
-            sBeta[tid] = tid < nv ? beta[t * L.Hq + h] : 0.f;
+            float gi = g_next * 1.4426950408889634f;  // log2 units
+            sBeta[tid] = b_next;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 float y = __shfl_up_sync(0xffffffffu, gi, o);
@@ -198,25 +237,13 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         }
         __syncthreads();
         if (tid < kC) {
-            sGam[tid] = expf(sG[tid]);
-            sKdec[tid] = expf(sG[kC - 1] - sG[tid]);
+            sGam[tid] = exp2f(sG[tid]);
+            sKdec[tid] = exp2f(sG[kC - 1] - sG[tid]);
         }
 
-        // ---- 2. chunk rows: K and Q into the stack, V into its MN-major tile
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + kThreads * u, r = e >> 4, cc = (e & 15) * 8;
-            uint4 kk = make_uint4(0, 0, 0, 0), qq = kk, vv = kk;
-            if (r < nv) {
-                const size_t t = (size_t)(start + j0 + r);
-                kk = *reinterpret_cast<const uint4*>(khat + (t * L.Hkv + kv) * kD + cc);
-                vv = *reinterpret_cast<const uint4*>(vhat + (t * L.Hkv + kv) * kD + cc);
-                qq = *reinterpret_cast<const uint4*>(qhat + ((t + W) * L.Hq + h) * kD + cc);
-            }
-            st16(sm + kStack, umma::sw128_offset(r, cc, 128), kk);
-            st16(sm + kStack, umma::sw128_offset(64 + r, cc, 128), qq);
-            st16(sm + kVt, umma::sw128_offset(r, cc, 64), vv);
-        }
+        // ---- 2. this chunk's rows have streamed into (stack, V)[c % 2]; start the next
+        cp_async_wait_all();
+        if (c + 1 < n_chunks) prefetch(c + 1, (c + 1) & 1);
         sync_for_mma();
 
         // ---- 3. Gram: D_G = [K; Q] K^T
@@ -225,8 +252,8 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             const uint32_t id = umma::idesc_f16(128, 64, false, false, false);
 #pragma unroll
             for (int s = 0; s < kD / 16; ++s)
-                umma::mma(tmem + kColG, umma::kmajor(sbase + kStack, 128, s),
-                          umma::kmajor(sbase + kStack, 128, s), id, s > 0);
+                umma::mma(tmem + kColG, umma::kmajor(sbase + oStk, 128, s),
+                          umma::kmajor(sbase + oStk, 128, s), id, s > 0);
             umma::commit(mbar);
         }
         if (!(ok = wait_mma())) break;
@@ -241,7 +268,7 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {
                     const int i = 32 * wg + ii;
-                    sA[r * 68 + i] = (i < r) ? br * expf(gr - sG[i]) * d[ii] : 0.f;
+                    sA[r * 68 + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
                 }
             } else {
                 const int r = Lr - 64;
@@ -249,7 +276,7 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {
                     const int i = 32 * wg + ii;
-                    d[ii] = (i <= r) ? expf(gr - sG[i]) * d[ii] : 0.f;
+                    d[ii] = (i <= r) ? exp2f(gr - sG[i]) * d[ii] : 0.f;
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -259,32 +286,30 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         umma::fence_before_sync();
         __syncthreads();
 
-        // ---- 5. T = (I + A)^{-1}: diagonal blocks, then block rows by distance
-        if (warp < 2) invert_diag_block(sA, sT, 2 * warp + (lane >> 4), lane & 15);
+        // ---- 5. T = (I + A)^{-1}: two 32 x 32 diagonal blocks by forward
+        // substitution, then T10 = -T11 (A10 T00)
+        if (warp < 2) invert_diag_block32(sA, sT, warp, lane);
         __syncthreads();
         {
-            const int bi = tid >> 4, bj = tid & 15;
-            for (int lvl = 1; lvl < 4; ++lvl) {
-                for (int b = 0; b < 4 - lvl; ++b) {
-                    const int I = lvl + b, J = b;
-                    float x = 0.f;
-                    for (int K = J; K < I; ++K)
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            x = fmaf(sA[(16 * I + bi) * 68 + 16 * K + k], sT[(16 * K + k) * 68 + 16 * J + bj], x);
-                    sX[(b * 16 + bi) * 17 + bj] = x;
-                }
-                __syncthreads();
-                for (int b = 0; b < 4 - lvl; ++b) {
-                    const int I = lvl + b, J = b;
-                    float y = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        y = fmaf(sT[(16 * I + bi) * 68 + 16 * I + k], sX[(b * 16 + k) * 17 + bj], y);
-                    sT[(16 * I + bi) * 68 + 16 * J + bj] = -y;
-                }
-                __syncthreads();
+            const int i = tid >> 3, j0c = (tid & 7) * 4;
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = j0c; k < 32; ++k) {  // T00 is lower triangular
+                const float a = sA[(32 + i) * 68 + k];
+                const float4 t4 = *reinterpret_cast<const float4*>(&sT[k * 68 + j0c]);
+                x[0] = fmaf(a, t4.x, x[0]); x[1] = fmaf(a, t4.y, x[1]);
+                x[2] = fmaf(a, t4.z, x[2]); x[3] = fmaf(a, t4.w, x[3]);
             }
+            *reinterpret_cast<float4*>(&sX[i * 36 + j0c]) = make_float4(x[0], x[1], x[2], x[3]);
+            __syncthreads();
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k <= i; ++k) {  // T11 is lower triangular
+                const float t = sT[(32 + i) * 68 + 32 + k];
+                const float4 x4 = *reinterpret_cast<const float4*>(&sX[k * 36 + j0c]);
+                y[0] = fmaf(t, x4.x, y[0]); y[1] = fmaf(t, x4.y, y[1]);
+                y[2] = fmaf(t, x4.z, y[2]); y[3] = fmaf(t, x4.w, y[3]);
+            }
+            *reinterpret_cast<float4*>(&sT[(32 + i) * 68 + j0c]) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+            __syncthreads();
         }
 
         // ---- 6. T diag(beta) and T diag(beta gamma) as fp16 K-major tiles
@@ -309,11 +334,11 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             const uint32_t id = umma::idesc_f16(128, 64, true, false, false);
 #pragma unroll
             for (int s = 0; s < kC / 16; ++s)
-                umma::mma(tmem + kColU, umma::mnmajor(sbase + kVt, 8192, s), umma::kmajor(sbase + kTb, 64, s), id,
+                umma::mma(tmem + kColU, umma::mnmajor(sbase + oVt, 8192, s), umma::kmajor(sbase + kTb, 64, s), id,
                           s > 0);
 #pragma unroll
             for (int s = 0; s < kC / 16; ++s)
-                umma::mma(tmem + kColW, umma::mnmajor(sbase + kStack, 16384, s), umma::kmajor(sbase + kTbg, 64, s),
+                umma::mma(tmem + kColW, umma::mnmajor(sbase + oStk, 16384, s), umma::kmajor(sbase + kTbg, 64, s),
                           id, s > 0);
             umma::commit(mbar);
         }
@@ -325,14 +350,14 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::tmem_ld32(tmem + lane_base + kColW + 32 * wg, w);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                st16(sm + kVt, umma::sw128_offset(Lr, 32 * wg + 8 * u, 128), pack8(w + 8 * u));
+                st16(sm + oVt, umma::sw128_offset(Lr, 32 * wg + 8 * u, 128), pack8(w + 8 * u));
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int e = tid + kThreads * u, row = e >> 4, cc = (e & 15) * 8;
             const uint32_t off = umma::sw128_offset(row, cc, 128);
             const float s = row < 64 ? sKdec[row] : sGam[row - 64];
-            st16(sm + kStack, off, scale8(ld16(sm + kStack, off), s));
+            st16(sm + oStk, off, scale8(ld16(sm + oStk, off), s));
         }
         sync_for_mma();
 
@@ -343,12 +368,12 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             const uint32_t id3 = umma::idesc_f16(128, 64, false, false, false);
 #pragma unroll
             for (int s = 0; s < kD / 16; ++s)
-                umma::mma(tmem + kColU, umma::kmajor(sbase + kSt, 128, s), umma::mnmajor(sbase + kVt, 16384, s), id1,
+                umma::mma(tmem + kColU, umma::kmajor(sbase + kSt, 128, s), umma::mnmajor(sbase + oVt, 16384, s), id1,
                           true);
 #pragma unroll
             for (int s = 0; s < kD / 16; ++s)
                 umma::mma(tmem + kColO, umma::kmajor(sbase + kSt, 128, s),
-                          umma::kmajor(sbase + kStack + 64 * 128, 128, s), id3, s > 0);
+                          umma::kmajor(sbase + oStk + 64 * 128, 128, s), id3, s > 0);
             umma::commit(mbar);
         }
         if (!(ok = wait_mma())) break;
@@ -370,7 +395,7 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             const uint32_t id3 = umma::idesc_f16(128, 64, false, false, false);
 #pragma unroll
             for (int s = 0; s < kC / 16; ++s)
-                umma::mma(tmem + kColS, umma::kmajor(sbase + kUt, 128, s), umma::mnmajor(sbase + kStack, 16384, s), id2,
+                umma::mma(tmem + kColS, umma::kmajor(sbase + kUt, 128, s), umma::mnmajor(sbase + oStk, 16384, s), id2,
                           s > 0);
 #pragma unroll
             for (int s = 0; s < kC / 16; ++s)
