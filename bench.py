@@ -275,7 +275,8 @@ def run_prefill_bench(args, dist, peaks):
     stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j, name in enumerate(("features", "gdn", "softmax"))}
     device_s = dist.max(sum(step_ms) / 1e3)
-    launches_per_step = 4  # rope tables, features, gdn, softmax
+    # rope tables, features, gdn (chunk table + inverse + state kernel when chunked), softmax
+    launches_per_step = 6 if (wl.dtype == "bf16" and wl.head_dim == 128) else 4
 
     work = prefill_work(wl)
     top = max(stage_ms, key=stage_ms.get)

@@ -1,0 +1,228 @@
+// Chunk-local part of the chunked GDN form that does not depend on the
+// state: for every chunk of 64 absorbed tokens and every query head,
+//   A[r,i] = beta_r e^{G_r - G_i} k_r . k_i  (i < r),   T = (I + A)^{-1}
+// (the UT transform of the GDN update of "迈向线性的关键：分析驱动的
+// Transformer 线性化", section 线性注意力替换机制).  All chunks are independent,
+// so this runs fully parallel, ahead of the state-carrying kernel, and leaves T
+// in fp16 as the byte image of a 64 x 64 K-major 128B-swizzled tile (8 KB) that
+// the state kernel copies into shared memory unchanged.
+//
+// Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
+// chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
+#include "hla_common.cuh"
+#include "umma.cuh"
+
+namespace hla {
+
+namespace {
+
+constexpr int kC = 64, kD = 128, kThreads = 128;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kK = 0;                        // K rows 0..63 (rows 64..127 zero), K-major
+constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]
+constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68]
+constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
+constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta
+constexpr uint32_t kMisc = kVec + 2 * 64 * 4;
+constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Forward substitution for a 32 x 32 unit lower-triangular diagonal block of
+// (I + A): one warp per block, lane l owns row l of the inverse.
+__device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, int b, int l) {
+    float a[32], t[32];
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+        a[m] = sA[(32 * b + l) * 68 + 32 * b + m];
+        t[m] = (m == l) ? 1.f : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 31; ++m) {
+        // row m is final once rows 0..m-1 have been folded into it
+#pragma unroll
+        for (int k = 0; k <= m; ++k) {
+            const float tm = __shfl_sync(0xffffffffu, t[k], m);
+            if (l > m) t[k] = fmaf(-a[m], tm, t[k]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 32; ++m) sT[(32 * b + l) * 68 + 32 * b + m] = t[m];
+}
+
+__global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ cu, int32_t* __restrict__ base) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int32_t acc = 0;
+    for (int s = 0; s < L.n_seqs; ++s) {
+        base[s] = acc;
+        int64_t start, len;
+        seq_range(cu, s, L.total, &start, &len);
+        const int64_t m = len - L.window - L.n_sinks;
+        acc += m > 0 ? (int32_t)((m + kC - 1) / kC) : 0;
+    }
+    base[L.n_seqs] = acc;
+}
+
+__global__ void __launch_bounds__(kThreads)
+gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __restrict__ g,
+                   const float* __restrict__ beta, const int32_t* __restrict__ cu,
+                   const int32_t* __restrict__ chunk_base, __half* __restrict__ t_out,
+                   int32_t* __restrict__ err) {
+    const int slot = blockIdx.x, h = blockIdx.y, kv = h / L.G;
+    if (slot >= __ldg(chunk_base + L.n_seqs)) return;  // whole CTA leaves together
+    // sequence owning the slot: the last s with chunk_base[s] <= slot
+    int lo = 0, hi = L.n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(chunk_base + mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo, c = slot - __ldg(chunk_base + s);
+    int64_t start, len;
+    seq_range(cu, s, L.total, &start, &len);
+    const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+    const int nv = (int)max((int64_t)0, min((int64_t)kC, len - L.window - j0));
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float* sA = reinterpret_cast<float*>(sm + kA32);
+    float* sT = reinterpret_cast<float*>(sm + kT32);
+    float* sX = reinterpret_cast<float*>(sm + kX32);
+    float* sG = reinterpret_cast<float*>(sm + kVec);
+    float* sBeta = sG + 64;
+    uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
+    float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t mbar = umma::smem_addr(mbar_p), sbase = umma::smem_addr(sm);
+
+    // ---- K rows (zero past the chunk and in rows 64..127), gates
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < nv)
+            val = *reinterpret_cast<const uint4*>(khat + ((size_t)(start + j0 + r) * L.Hkv + kv) * kD + c8);
+        *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(r, c8, 128)) = val;
+    }
+    float gi = 0.f;
+    if (tid < kC) {
+        const size_t t = (size_t)(start + j0 + tid);
+        gi = tid < nv ? g[t * L.Hq + h] * 1.4426950408889634f : 0.f;
+        sBeta[tid] = tid < nv ? beta[t * L.Hq + h] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, gi, o);
+            if (lane >= o) gi += y;
+        }
+        if (tid == 31) *carry = gi;
+    }
+    for (int i = tid; i < 32 * 32; i += kThreads) sT[(i >> 5) * 68 + 32 + (i & 31)] = 0.f;  // T01 = 0
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(tmem_slot, 64);
+    umma::fence_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    if (tid >= 32 && tid < kC) gi += *carry;
+    if (tid < kC) sG[tid] = gi;
+
+    // ---- Gram: D = [K; 0] K^T
+    if (tid == 0) {
+        const uint32_t id = umma::idesc_f16(128, kC, false, false, false);
+#pragma unroll
+        for (int s16 = 0; s16 < kD / 16; ++s16)
+            umma::mma(tmem, umma::kmajor(sbase + kK, 128, s16), umma::kmajor(sbase + kK, 128, s16), id, s16 > 0);
+        umma::commit(mbar);
+    }
+    const bool done = __syncthreads_and(umma::mbar_wait(mbar, 0, kWaitLimit));  // also: sG complete
+    if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
+    umma::fence_after_sync();
+    if (warp < 2 && done) {  // rows 0..63 of the Gram matrix
+        const int r = tid;
+        const float br = sBeta[r], gr = sG[r];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float d[32];
+            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * half, d);
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * half + ii;
+                sA[r * 68 + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
+            }
+        }
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 64);
+    if (!done) return;
+
+    // ---- T = (I + A)^{-1}: 32 x 32 diagonal blocks, then T10 = -T11 (A10 T00)
+    if (warp < 2) invert_diag_block32(sA, sT, warp, lane);
+    __syncthreads();
+    {
+        const int i = tid >> 2, j0c = (tid & 3) * 8;
+        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = j0c; k < 32; ++k) {  // T00 is lower triangular
+            const float a = sA[(32 + i) * 68 + k];
+            const float4 t0 = *reinterpret_cast<const float4*>(&sT[k * 68 + j0c]);
+            const float4 t1 = *reinterpret_cast<const float4*>(&sT[k * 68 + j0c + 4]);
+            x[0] = fmaf(a, t0.x, x[0]); x[1] = fmaf(a, t0.y, x[1]); x[2] = fmaf(a, t0.z, x[2]); x[3] = fmaf(a, t0.w, x[3]);
+            x[4] = fmaf(a, t1.x, x[4]); x[5] = fmaf(a, t1.y, x[5]); x[6] = fmaf(a, t1.z, x[6]); x[7] = fmaf(a, t1.w, x[7]);
+        }
+        *reinterpret_cast<float4*>(&sX[i * 36 + j0c]) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(&sX[i * 36 + j0c + 4]) = make_float4(x[4], x[5], x[6], x[7]);
+        __syncthreads();
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k <= i; ++k) {  // T11 is lower triangular
+            const float t = sT[(32 + i) * 68 + 32 + k];
+            const float4 x0 = *reinterpret_cast<const float4*>(&sX[k * 36 + j0c]);
+            const float4 x1 = *reinterpret_cast<const float4*>(&sX[k * 36 + j0c + 4]);
+            y[0] = fmaf(t, x0.x, y[0]); y[1] = fmaf(t, x0.y, y[1]); y[2] = fmaf(t, x0.z, y[2]); y[3] = fmaf(t, x0.w, y[3]);
+            y[4] = fmaf(t, x1.x, y[4]); y[5] = fmaf(t, x1.y, y[5]); y[6] = fmaf(t, x1.z, y[6]); y[7] = fmaf(t, x1.w, y[7]);
+        }
+        *reinterpret_cast<float4*>(&sT[(32 + i) * 68 + j0c]) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+        *reinterpret_cast<float4*>(&sT[(32 + i) * 68 + j0c + 4]) = make_float4(-y[4], -y[5], -y[6], -y[7]);
+        __syncthreads();
+    }
+
+    // ---- T -> fp16 image of the swizzled K-major tile
+    unsigned char* dst = reinterpret_cast<unsigned char*>(t_out + ((size_t)slot * L.Hq + h) * kC * kC);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = tid + kThreads * u, r = e >> 3, c8 = (e & 7) * 8;
+        const float* tr = sT + r * 68 + c8;
+        *reinterpret_cast<uint4*>(dst + umma::sw128_offset(r, c8, 64)) =
+            make_uint4(pack_h2(tr[0], tr[1]), pack_h2(tr[2], tr[3]), pack_h2(tr[4], tr[5]), pack_h2(tr[6], tr[7]));
+    }
+}
+
+}  // namespace
+
+size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
+
+cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* khat, const float* g, const float* beta,
+                               const int32_t* cu, int32_t* chunk_base, __half* t_out, int32_t* err,
+                               cudaStream_t st) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    gdn_chunk_table_kernel<<<1, 32, 0, st>>>(L, cu, chunk_base);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)gdn_chunk_slots(L.total, L.n_seqs), L.Hq);
+    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, khat, g, beta, cu, chunk_base, t_out, err);
+    return cudaGetLastError();
+}
+
+}  // namespace hla

@@ -51,11 +51,16 @@ size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
 
 // Workspace layout of one prefill.
 struct WsLayout {
-    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, total;
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, chunk_base, tinv, total;
     int n_coarse;
 };
 
-WsLayout ws_layout(const hla_params* prm, int64_t total) {
+// The tensor-core chunked GDN serves bf16 layers with head_dim 128.
+bool uses_chunked_gdn(const hla_params* prm) {
+    return prm->dtype == HLA_DTYPE_BF16 && prm->head_dim == 128 && !(prm->flags & HLA_FLAG_GDN_RECURRENT);
+}
+
+WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     WsLayout w;
     const size_t fb = feat_bytes(prm->dtype), d = (size_t)prm->head_dim, half = d / 2;
     const size_t Hq = (size_t)prm->n_q_heads, Hkv = (size_t)prm->n_kv_heads, T = (size_t)total;
@@ -70,6 +75,9 @@ WsLayout ws_layout(const hla_params* prm, int64_t total) {
     w.khat = off;   off = align_up(off + T * Hkv * d * fb);
     w.vhat = off;   off = align_up(off + T * Hkv * d * fb);
     w.olin = off;   off = align_up(off + T * Hq * d * sizeof(float));
+    const bool chunked = uses_chunked_gdn(prm);
+    w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
+    w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * 64 * 64 * 2 : 0));
     w.total = off;
     return w;
 }
@@ -97,7 +105,6 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
                 const void* v, const float* g, const float* beta, const float* lambda,
                 const float* wq, const float* wk, const float* wv, const int32_t* cu, void* out,
                 const hla_state* st, char* ws, const WsLayout& w, cudaStream_t stream) {
-    (void)prm;
     int32_t* err = reinterpret_cast<int32_t*>(ws + w.err);
     float2* fine = reinterpret_cast<float2*>(ws + w.fine);
     float2* coarse = reinterpret_cast<float2*>(ws + w.coarse);
@@ -119,11 +126,14 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     HLA_TRY(mark_stage(1, stream));
     float* S_out = st ? st->S : nullptr;
     bool chunked = false;
-    if constexpr (std::is_same<Tf, __half>::value)
-        chunked = L.d == 128 && !(L.flags & HLA_FLAG_GDN_RECURRENT);
+    if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
     if (chunked) {
-        if constexpr (std::is_same<Tf, __half>::value)
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, g, beta, cu, olin, S_out, err, stream));
+        if constexpr (std::is_same<Tf, __half>::value) {
+            int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
+            __half* tinv = reinterpret_cast<__half*>(ws + w.tinv);
+            HLA_TRY(launch_gdn_inverse(L, kh, g, beta, cu, chunk_base, tinv, err, stream));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, g, beta, cu, chunk_base, tinv, olin, S_out, err, stream));
+        }
     } else {
         HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
     }
@@ -208,7 +218,7 @@ HLA_API int hla_prefill_workspace_bytes(const hla_params* prm, int64_t total_tok
     int rc = check_params(prm);
     if (rc) return rc;
     if (total_tokens < 0 || n_seqs < 0 || !bytes) return HLA_ERR_INVALID_ARG;
-    *bytes = ws_layout(prm, total_tokens).total;
+    *bytes = ws_layout(prm, total_tokens, n_seqs).total;
     return HLA_OK;
 }
 
@@ -244,7 +254,7 @@ HLA_API int hla_prefill(const hla_params* prm, const void* q, const void* k, con
         if (!ptrs[i] || !aligned16(ptrs[i])) return HLA_ERR_INVALID_ARG;
     }
     if (st && !state_ok(st)) return HLA_ERR_INVALID_ARG;
-    const WsLayout w = ws_layout(prm, total_tokens);
+    const WsLayout w = ws_layout(prm, total_tokens, n_seqs);
     if (ws_bytes < w.total) return HLA_ERR_WORKSPACE;
     const LayerDims L = make_dims(prm, n_seqs, total_tokens);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
