@@ -1,11 +1,16 @@
 // Chunk-local part of the chunked GDN form that does not depend on the
-// state: for every chunk of 64 absorbed tokens and every query head,
-//   A[r,i] = beta_r e^{G_r - G_i} k_r . k_i  (i < r),   T = (I + A)^{-1}
+// state: for every chunk of 64 absorbed tokens and every query head, with the
+// gates cumulated inside the chunk (G_r = sum_{i<=r} g_i, gamma_r = e^{G_r}),
+//   A[r,i] = beta_r e^{G_r - G_i} k_r . k_i  (i < r),   T = (I + A)^{-1},
+//   P[r,i] = e^{G_r - G_i} q_r . k_i  (i <= r)
 // (the UT transform of the GDN update of "迈向线性的关键：分析驱动的
-// Transformer 线性化", section 线性注意力替换机制).  All chunks are independent,
-// so this runs fully parallel, ahead of the state-carrying kernel, and leaves T
-// in fp16 as the byte image of a 64 x 64 K-major 128B-swizzled tile (8 KB) that
-// the state kernel copies into shared memory unchanged.
+// Transformer 线性化", section 线性注意力替换机制; q_r is qhat at position
+// r + W).  All chunks are independent, so this runs fully parallel, ahead of
+// the state-carrying kernel.  Per (chunk, q-head) it writes a record:
+//   T diag(beta), T diag(beta gamma), P   as fp16 byte images of 64 x 64
+//                                          K-major 128B-swizzled tiles (8 KB each)
+//   gamma[64], e^{G_63 - G}[64]            fp32
+// which the state kernel copies into shared memory unchanged.
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
@@ -18,7 +23,7 @@ namespace {
 
 constexpr int kC = 64, kD = 128, kThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kK = 0;                        // K rows 0..63 (rows 64..127 zero), K-major
+constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
 constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68]
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
@@ -67,9 +72,10 @@ __global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ 
 }
 
 __global__ void __launch_bounds__(kThreads)
-gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __restrict__ g,
+gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
+                   const float* __restrict__ g,
                    const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                   const int32_t* __restrict__ chunk_base, __half* __restrict__ t_out,
+                   const int32_t* __restrict__ chunk_base, unsigned char* __restrict__ rec_out,
                    int32_t* __restrict__ err) {
     const int slot = blockIdx.x, h = blockIdx.y, kv = h / L.G;
     if (slot >= __ldg(chunk_base + L.n_seqs)) return;  // whole CTA leaves together
@@ -98,13 +104,18 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t mbar = umma::smem_addr(mbar_p), sbase = umma::smem_addr(sm);
 
-    // ---- K rows (zero past the chunk and in rows 64..127), gates
+    // ---- K rows into rows 0..63, the shifted queries into rows 64..127 (zero
+    //      past the chunk), gates
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
         const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
+        const int rr = r & 63;
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < nv)
-            val = *reinterpret_cast<const uint4*>(khat + ((size_t)(start + j0 + r) * L.Hkv + kv) * kD + c8);
+        if (rr < nv) {
+            const size_t t = (size_t)(start + j0 + rr);
+            val = r < 64 ? *reinterpret_cast<const uint4*>(khat + (t * L.Hkv + kv) * kD + c8)
+                         : *reinterpret_cast<const uint4*>(qhat + ((t + L.window) * L.Hq + h) * kD + c8);
+        }
         *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(r, c8, 128)) = val;
     }
     float gi = 0.f;
@@ -133,7 +144,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
     if (tid >= 32 && tid < kC) gi += *carry;
     if (tid < kC) sG[tid] = gi;
 
-    // ---- Gram: D = [K; 0] K^T
+    // ---- Gram: D = [K; Q] K^T
     if (tid == 0) {
         const uint32_t id = umma::idesc_f16(128, kC, false, false, false);
 #pragma unroll
@@ -144,7 +155,8 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
     const bool done = __syncthreads_and(umma::mbar_wait(mbar, 0, kWaitLimit));  // also: sG complete
     if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
     umma::fence_after_sync();
-    if (warp < 2 && done) {  // rows 0..63 of the Gram matrix
+    unsigned char* rec = rec_out + ((size_t)slot * L.Hq + h) * kRecordBytes;
+    if (warp < 2 && done) {  // rows 0..63: K K^T -> A
         const int r = tid;
         const float br = sBeta[r], gr = sG[r];
 #pragma unroll
@@ -157,6 +169,30 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
                 sA[r * 68 + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
             }
         }
+    } else if (done) {  // rows 64..127: Q K^T -> P
+        const int r = tid - 64;
+        const float gr = sG[r];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float d[32];
+            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * half, d);
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * half + ii;
+                d[ii] = (i <= r) ? exp2f(gr - sG[i]) * d[ii] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float* x = d + 8 * u;
+                *reinterpret_cast<uint4*>(rec + kRecP + umma::sw128_offset(r, 32 * half + 8 * u, 64)) =
+                    make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+            }
+        }
+    }
+    if (tid < kC) {  // gamma and the key decay over the rest of the chunk
+        float* vec = reinterpret_cast<float*>(rec + kRecVec);
+        vec[tid] = exp2f(sG[tid]);
+        vec[kC + tid] = exp2f(sG[kC - 1] - sG[tid]);
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -192,14 +228,22 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
         __syncthreads();
     }
 
-    // ---- T -> fp16 image of the swizzled K-major tile
-    unsigned char* dst = reinterpret_cast<unsigned char*>(t_out + ((size_t)slot * L.Hq + h) * kC * kC);
+    // ---- T diag(beta) and T diag(beta gamma) -> fp16 images of swizzled K-major tiles
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int e = tid + kThreads * u, r = e >> 3, c8 = (e & 7) * 8;
         const float* tr = sT + r * 68 + c8;
-        *reinterpret_cast<uint4*>(dst + umma::sw128_offset(r, c8, 64)) =
-            make_uint4(pack_h2(tr[0], tr[1]), pack_h2(tr[2], tr[3]), pack_h2(tr[4], tr[5]), pack_h2(tr[6], tr[7]));
+        float tb[8], tbg[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            tb[x] = tr[x] * sBeta[c8 + x];
+            tbg[x] = tb[x] * exp2f(sG[c8 + x]);
+        }
+        const uint32_t off = umma::sw128_offset(r, c8, 64);
+        *reinterpret_cast<uint4*>(rec + kRecTb + off) =
+            make_uint4(pack_h2(tb[0], tb[1]), pack_h2(tb[2], tb[3]), pack_h2(tb[4], tb[5]), pack_h2(tb[6], tb[7]));
+        *reinterpret_cast<uint4*>(rec + kRecTbg + off) = make_uint4(
+            pack_h2(tbg[0], tbg[1]), pack_h2(tbg[2], tbg[3]), pack_h2(tbg[4], tbg[5]), pack_h2(tbg[6], tbg[7]));
     }
 }
 
@@ -207,9 +251,9 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ khat, const float* __
 
 size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
 
-cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* khat, const float* g, const float* beta,
-                               const int32_t* cu, int32_t* chunk_base, __half* t_out, int32_t* err,
-                               cudaStream_t st) {
+cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
+                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
+                               int32_t* err, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -221,7 +265,7 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* khat, const flo
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)gdn_chunk_slots(L.total, L.n_seqs), L.Hq);
-    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, khat, g, beta, cu, chunk_base, t_out, err);
+    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
     return cudaGetLastError();
 }
 

@@ -77,7 +77,7 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     w.olin = off;   off = align_up(off + T * Hq * d * sizeof(float));
     const bool chunked = uses_chunked_gdn(prm);
     w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
-    w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * 64 * 64 * 2 : 0));
+    w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
     w.total = off;
     return w;
 }
@@ -130,9 +130,9 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     if (chunked) {
         if constexpr (std::is_same<Tf, __half>::value) {
             int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
-            __half* tinv = reinterpret_cast<__half*>(ws + w.tinv);
-            HLA_TRY(launch_gdn_inverse(L, kh, g, beta, cu, chunk_base, tinv, err, stream));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, g, beta, cu, chunk_base, tinv, olin, S_out, err, stream));
+            unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, stream));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, olin, S_out, err, stream));
         }
     } else {
         HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
