@@ -21,10 +21,10 @@
 //
 // One CTA of 256 threads per (sequence, q-head), two warp-specialised groups:
 //   prep   (warps 4-7): chunk c+1 -- cp.async loads one chunk ahead, gamma Q in
-//          place, D_U and D_W, Wm^T;
-//   serial (warps 0-3): chunk c -- D_U += S0^T(-Wm^T) and D_O, then (while
-//          those run) the o_lin rows of chunk c-1, U^T (twice), D_S and D_O +=
-//          U^T P^T, S <- gamma_C S + dS in fp32 registers.
+//          place, D_U and D_W, Wm^T; and the o_lin rows of chunk c-1 from its
+//          (double-buffered) output accumulator;
+//   serial (warps 0-3): chunk c -- D_U += S0^T(-Wm^T) and D_O, U^T (twice),
+//          D_S and D_O += U^T P^T, S <- gamma_C S + dS in fp32 registers.
 // Chunk buffers b = c % 2 pass between the groups through the mbarriers
 // ready[b] (prep -> serial) and free[b] (serial -> prep).  Every wait has an
 // iteration limit; on expiry the kernel records a timeout in the error word
@@ -153,6 +153,22 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         return done;
     };
 
+    // o_lin rows of chunk c (positions j + W), from D_O[c % 2]
+    auto store_out = [&](int c) {
+        const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+        const int nv = (int)min((int64_t)kC, j_end - j0);
+        float* orow = o_lin + ((size_t)(start + j0 + W) * L.Hq + h) * kD + Lr;
+        const size_t ostride = (size_t)L.Hq * kD;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float o[32];
+            umma::tmem_ld32(tmem + lane_base + kColO0 + 64 * (c & 1) + 32 * hf, o);
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii)
+                if (32 * hf + ii < nv) orow[(size_t)(32 * hf + ii) * ostride] = o[ii];
+        }
+    };
+
     if (warp >= 4) {
         // ================= prep group: one chunk ahead of the serial group =================
         const int pt = tid - 128;
@@ -220,16 +236,7 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             ph ^= 1u;
             if (!ok) break;
 
-            // -- c. the next chunk's loads, once the serial group has released its buffer
-            if (c + 1 < n_chunks) {
-                bool fr = true;
-                if (c + 1 >= 2) fr = wait(4 + ((c + 1) & 1), (uint32_t)(((c - 1) >> 1) & 1));
-                ok = group_all(2, fr);
-                if (!ok) break;
-                load(c + 1, (c + 1) & 1);
-            }
-
-            // -- d. Wm^T -> W[b] (MN-major B)
+            // -- c. Wm^T -> W[b] (MN-major B); chunk c is then ready for the serial group
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 float w[32];
@@ -242,6 +249,20 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::fence_before_sync();
             group_sync(2);
             if (pt == 0) mbar_arrive(bar(2 + b));
+
+            // -- d. once the serial group is done with chunk c-1: its o_lin rows, and the
+            //       next chunk's loads into the buffer it released
+            if (c >= 1) {
+                ok = group_all(2, wait(4 + ((c - 1) & 1), (uint32_t)(((c - 1) >> 1) & 1)));
+                if (!ok) break;
+                store_out(c - 1);
+            }
+            if (c + 1 < n_chunks) load(c + 1, (c + 1) & 1);
+
+        }
+        if (ok && n_chunks > 0) {  // the last chunk's o_lin rows
+            const int c = n_chunks - 1;
+            if (group_all(2, wait(4 + (c & 1), (uint32_t)((c >> 1) & 1)))) store_out(c);
         }
     } else {
         // ================= serial group: the state chain =================
@@ -250,21 +271,6 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         for (int i = 0; i < kD; ++i) S[i] = 0.f;
         uint32_t ph = 0;
         bool ok = true;
-        // o_lin rows of chunk c (positions j + W), from D_O[c % 2]
-        auto store_out = [&](int c) {
-            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-            const int nv = (int)min((int64_t)kC, j_end - j0);
-            float* orow = o_lin + ((size_t)(start + j0 + W) * L.Hq + h) * kD + Lr;
-            const size_t ostride = (size_t)L.Hq * kD;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float o[32];
-                umma::tmem_ld32(tmem + lane_base + kColO0 + 64 * (c & 1) + 32 * hf, o);
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii)
-                    if (32 * hf + ii < nv) orow[(size_t)(32 * hf + ii) * ostride] = o[ii];
-            }
-        };
         for (int c = 0; c < n_chunks && ok; ++c) {
             const int b = c & 1;
             const uint32_t ostk = b ? kStk1 : kStk0;
@@ -285,7 +291,6 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                               umma::kmajor(sbase + ostk + 64 * 128, 128, s), id3, s > 0);
                 umma::commit(bar(1));
             }
-            if (c > 0) store_out(c - 1);  // overlaps the MMAs above
             ok = group_all(1, wait(1, ph));
             ph ^= 1u;
             if (!ok) break;
@@ -349,7 +354,6 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::fence_before_sync();
             group_sync(1);
         }
-        if (ok && n_chunks > 0) store_out(n_chunks - 1);
         if (ok && S_out) {
             float* dst = S_out + ((size_t)n * L.Hq + h) * kD * kD + Lr;
 #pragma unroll

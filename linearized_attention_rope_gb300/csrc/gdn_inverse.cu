@@ -14,6 +14,8 @@
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
+#include <algorithm>
+
 #include "hla_common.cuh"
 #include "umma.cuh"
 
@@ -37,7 +39,8 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 }
 
 // Forward substitution for a 32 x 32 unit lower-triangular diagonal block of
-// (I + A): one warp per block, lane l owns row l of the inverse.
+// (I + A): one warp per block, lane l owns row l of the inverse.  (The kernel
+// is persistent, so this fully unrolled code stays in the instruction cache.)
 __device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, int b, int l) {
     float a[32], t[32];
 #pragma unroll
@@ -77,20 +80,6 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                    const float* __restrict__ beta, const int32_t* __restrict__ cu,
                    const int32_t* __restrict__ chunk_base, unsigned char* __restrict__ rec_out,
                    int32_t* __restrict__ err) {
-    const int slot = blockIdx.x, h = blockIdx.y, kv = h / L.G;
-    if (slot >= __ldg(chunk_base + L.n_seqs)) return;  // whole CTA leaves together
-    // sequence owning the slot: the last s with chunk_base[s] <= slot
-    int lo = 0, hi = L.n_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(chunk_base + mid) <= slot) lo = mid; else hi = mid - 1;
-    }
-    const int s = lo, c = slot - __ldg(chunk_base + s);
-    int64_t start, len;
-    seq_range(cu, s, L.total, &start, &len);
-    const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-    const int nv = (int)max((int64_t)0, min((int64_t)kC, len - L.window - j0));
-
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* sA = reinterpret_cast<float*>(sm + kA32);
@@ -103,6 +92,35 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t mbar = umma::smem_addr(mbar_p), sbase = umma::smem_addr(sm);
+    const int64_t n_items = (int64_t)__ldg(chunk_base + L.n_seqs) * L.Hq;
+    if ((int64_t)blockIdx.x >= n_items) return;  // whole CTA leaves together
+
+    if (tid == 0) {
+        umma::mbar_init(mbar, 1);
+        umma::fence_mbar_init();
+    }
+    if (warp == 0) umma::tmem_alloc(tmem_slot, 64);
+    for (int i = tid; i < 32 * 32; i += kThreads) sT[(i >> 5) * 68 + 32 + (i & 31)] = 0.f;  // T01 = 0
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t phase = 0;
+
+    // persistent loop over (chunk slot, q-head) items
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int slot = (int)(item / L.Hq), h = (int)(item % L.Hq), kv = h / L.G;
+    // sequence owning the slot: the last s with chunk_base[s] <= slot
+    int lo = 0, hi = L.n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(chunk_base + mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo, c = slot - __ldg(chunk_base + s);
+    int64_t start, len;
+    seq_range(cu, s, L.total, &start, &len);
+    const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+    const int nv = (int)max((int64_t)0, min((int64_t)kC, len - L.window - j0));
 
     // ---- K rows into rows 0..63, the shifted queries into rows 64..127 (zero
     //      past the chunk), gates
@@ -110,14 +128,15 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     for (int u = 0; u < 16; ++u) {
         const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
         const int rr = r & 63;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (rr < nv) {
-            const size_t t = (size_t)(start + j0 + rr);
-            val = r < 64 ? *reinterpret_cast<const uint4*>(khat + (t * L.Hkv + kv) * kD + c8)
-                         : *reinterpret_cast<const uint4*>(qhat + ((t + L.window) * L.Hq + h) * kD + c8);
-        }
-        *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(r, c8, 128)) = val;
+        const size_t t = (size_t)(start + j0 + (rr < nv ? rr : 0));
+        const void* src = r < 64 ? (const void*)(khat + (t * L.Hkv + kv) * kD + c8)
+                                 : (const void*)(qhat + ((t + L.window) * L.Hq + h) * kD + c8);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         umma::smem_addr(sm + kK + umma::sw128_offset(r, c8, 128))),
+                     "l"(src), "r"(rr < nv ? 16u : 0u)
+                     : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     float gi = 0.f;
     if (tid < kC) {
         const size_t t = (size_t)(start + j0 + tid);
@@ -130,17 +149,11 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         }
         if (tid == 31) *carry = gi;
     }
-    for (int i = tid; i < 32 * 32; i += kThreads) sT[(i >> 5) * 68 + 32 + (i & 31)] = 0.f;  // T01 = 0
-    if (tid == 0) {
-        umma::mbar_init(mbar, 1);
-        umma::fence_mbar_init();
-    }
-    if (warp == 0) umma::tmem_alloc(tmem_slot, 64);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     umma::fence_async_smem();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
     if (tid >= 32 && tid < kC) gi += *carry;
     if (tid < kC) sG[tid] = gi;
 
@@ -152,7 +165,8 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::mma(tmem, umma::kmajor(sbase + kK, 128, s16), umma::kmajor(sbase + kK, 128, s16), id, s16 > 0);
         umma::commit(mbar);
     }
-    const bool done = __syncthreads_and(umma::mbar_wait(mbar, 0, kWaitLimit));  // also: sG complete
+    const bool done = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));  // also: sG complete
+    phase ^= 1u;
     if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
     umma::fence_after_sync();
     unsigned char* rec = rec_out + ((size_t)slot * L.Hq + h) * kRecordBytes;
@@ -196,8 +210,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, 64);
-    if (!done) return;
+    if (!done) break;
 
     // ---- T = (I + A)^{-1}: 32 x 32 diagonal blocks, then T10 = -T11 (A10 T00)
     if (warp < 2) invert_diag_block32(sA, sT, warp, lane);
@@ -245,6 +258,11 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         *reinterpret_cast<uint4*>(rec + kRecTbg + off) = make_uint4(
             pack_h2(tbg[0], tbg[1]), pack_h2(tbg[2], tbg[3]), pack_h2(tbg[4], tbg[5]), pack_h2(tbg[6], tbg[7]));
     }
+    __syncthreads();  // shared tiles are refilled by the next item
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 64);
 }
 
 }  // namespace
@@ -264,7 +282,15 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
     gdn_chunk_table_kernel<<<1, 32, 0, st>>>(L, cu, chunk_base);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)gdn_chunk_slots(L.total, L.n_seqs), L.Hq);
+    static int n_sm = 0;  // per-process device property cache
+    if (!n_sm) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+            n_sm = 132;
+    }
+    const int64_t items = (int64_t)gdn_chunk_slots(L.total, L.n_seqs) * L.Hq;
+    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
     gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
     return cudaGetLastError();
 }

@@ -53,6 +53,16 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
+
 // Key position held by key slot i of a segment: the sinks first, then the window span.
 __device__ __forceinline__ int64_t key_at(int64_t i, int64_t n_sink, int64_t span_lo, int64_t n_keys) {
     if (i >= n_keys) return -1;
@@ -131,32 +141,36 @@ window_softmax_tc_kernel(LayerDims L, const __half* __restrict__ qr, const __hal
             hi2 = (int)(p >= span_lo ? n_sink + (p - span_lo) + 1 : lo2);
         }
 
-        // ---- Q rows of the block (zero outside the segment)
-        for (int e = tid; e < kRows * 16; e += kThreads) {
-            const int r = e >> 4, cc = (e & 15) * 8;
+        // ---- Q rows of the block (zero outside the segment), streamed with cp.async
+#pragma unroll
+        for (int u = 0; u < kRows * 16 / kThreads; ++u) {
+            const int e = tid + kThreads * u, r = e >> 4, cc = (e & 15) * 8;
             const int rg = r / QB, rq = r % QB;
             const int64_t t = t0 + rq;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (t >= ta && t < tb)
-                val = *reinterpret_cast<const uint4*>(qr + ((size_t)t * L.Hq + kv * G + rg) * kD + cc);
-            *reinterpret_cast<uint4*>(sm + kQ + (r >> 7) * 32768 + umma::sw128_offset(r & 127, cc, 128)) = val;
+            const bool in = t >= ta && t < tb;
+            cp_async16(sm + kQ + (r >> 7) * 32768 + umma::sw128_offset(r & 127, cc, 128),
+                       qr + ((size_t)(in ? t : ta) * L.Hq + kv * G + rg) * kD + cc, in ? 16u : 0u);
         }
 
         float m_run = -INFINITY, l_run = 0.f;
         for (int grp = 0; grp < n_groups; ++grp) {
             // ---- K (fp16) and V (bf16 -> fp16) rows of the group's key slots
-            for (int e = tid; e < kKeys * 16; e += kThreads) {
-                const int slot = e >> 4, cc = (e & 15) * 8;
+#pragma unroll
+            for (int u = 0; u < kKeys * 16 / kThreads; ++u) {
+                const int e = tid + kThreads * u, slot = e >> 4, cc = (e & 15) * 8;
                 const int64_t j = key_at((int64_t)grp * kKeys + slot, n_sink, span_lo, n_keys);
-                uint4 kk = make_uint4(0, 0, 0, 0), vv = kk;
-                if (j >= 0) {
-                    const size_t rowi = ((size_t)(start + j) * L.Hkv + kv) * kD + cc;
-                    kk = *reinterpret_cast<const uint4*>(kr + rowi);
-                    vv = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(v + rowi));
-                }
+                const size_t rowi = ((size_t)(start + (j >= 0 ? j : 0)) * L.Hkv + kv) * kD + cc;
                 const uint32_t off = umma::sw128_offset(slot, cc, 128);
-                *reinterpret_cast<uint4*>(sm + kK + off) = kk;
-                *reinterpret_cast<uint4*>(sm + kV + off) = vv;
+                cp_async16(sm + kK + off, kr + rowi, j >= 0 ? 16u : 0u);
+                cp_async16(sm + kV + off, v + rowi, j >= 0 ? 16u : 0u);
+            }
+            cp_async_wait_all();  // (Q rows too, on the first group)
+            // values arrive as bf16; the MMA takes fp16 for both operands
+#pragma unroll
+            for (int u = 0; u < kKeys * 16 / kThreads; ++u) {
+                const int e = tid + kThreads * u, slot = e >> 4, cc = (e & 15) * 8;
+                uint4* pv = reinterpret_cast<uint4*>(sm + kV + umma::sw128_offset(slot, cc, 128));
+                *pv = bf16x8_to_f16x8(*pv);
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
