@@ -185,17 +185,23 @@ def source_hash(files) -> str:
 # prefill
 GDN_RECURRENT_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
                          "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+GDN_PREP_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_inverse.cu",
+                    "linearized_attention_rope_gb300/csrc/umma.cuh",
+                    "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
 GDN_CHUNKED_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_chunked.cu",
                        "linearized_attention_rope_gb300/csrc/umma.cuh",
                        "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
 
 
-def chunked_gdn_flops_per_token_head(d: int = 128, C: int = 64) -> float:
-    """Useful flops of the chunked GDN per absorbed token and q-head: the three
-    d x d products (W S0, Q S0, Kt^T U), the Gram triangle, the triangular
-    solve, and U~, Wm, masked Q K^T, P U (triangles halved)."""
-    macs = 3 * d * d + (C - 1) * d / 2 + (C * C - 1) / 6 + 4 * (C + 1) * d / 2
-    return 2.0 * macs
+def chunked_gdn_flops_per_token_head(d: int = 128, C: int = 64) -> dict:
+    """Useful flops of the chunked GDN per absorbed token and q-head, split by
+    kernel (triangles halved).  Chunk-local kernel: the Gram triangle K K^T,
+    the masked Q K^T and the triangular solve for T.  State kernel: the three
+    d x d products (W S0, Q S0, Kt^T U) and U~ = T diag(b) V, Wm = T diag(b g) K,
+    P U."""
+    prep = (C - 1) * d / 2 + (C + 1) * d / 2 + (C * C - 1) / 6
+    state = 3 * d * d + 3 * (C + 1) * d / 2
+    return {"prep": 2.0 * prep, "state": 2.0 * state, "total": 2.0 * (prep + state)}
 
 
 def prefill_work(wl):
@@ -209,18 +215,29 @@ def prefill_work(wl):
             keys += min(p + 1, wl.n_sinks) + max(0, min(wl.window, p + 1 - wl.n_sinks))
     eb = 2 if wl.dtype == "bf16" else 4
     if wl.dtype == "bf16" and d == 128:
-        gdn = {"bound": "tensor", "flops": chunked_gdn_flops_per_token_head(d) * absorbed * Hq,
-               "unit": "TFLOP/s", "sources": GDN_CHUNKED_SOURCES, "kernel": "gdn_chunked_kernel"}
+        f = chunked_gdn_flops_per_token_head(d)
+        gdn_state = {"bound": "tensor", "flops": f["state"] * absorbed * Hq,
+                     "unit": "TFLOP/s", "sources": GDN_CHUNKED_SOURCES, "kernel": "gdn_chunked_kernel"}
+        gdn_prep = {"bound": "tensor", "flops": f["prep"] * absorbed * Hq,
+                    "unit": "TFLOP/s", "sources": GDN_PREP_SOURCES, "kernel": "gdn_inverse_kernel"}
     else:
         # token-serial delta rule: k^T S, the rank-1 update, q^T S -> 6 d^2 flops per token-head
-        gdn = {"bound": "alu", "flops": 6.0 * d * d * absorbed * Hq, "peak": FP32_ALU_TFLOPS,
-               "unit": "TFLOP/s", "sources": GDN_RECURRENT_SOURCES, "kernel": "gdn_recurrent_kernel"}
+        gdn_state = {"bound": "alu", "flops": 6.0 * d * d * absorbed * Hq, "peak": FP32_ALU_TFLOPS,
+                     "unit": "TFLOP/s", "sources": GDN_RECURRENT_SOURCES, "kernel": "gdn_recurrent_kernel"}
+        gdn_prep = None
     return {
-        "gdn": gdn,
+        "gdn_prep": gdn_prep,
+        "gdn_state": gdn_state,
         # q.k and p.v over the visible keys of every (token, q-head)
-        "softmax": {"bound": "alu", "flops": 4.0 * d * keys * Hq, "peak": FP32_ALU_TFLOPS,
-                    "unit": "TFLOP/s", "sources": ["linearized_attention_rope_gb300/csrc/window_softmax.cu"],
-                    "kernel": "window_softmax_kernel"},
+        "softmax": ({"bound": "tensor", "flops": 4.0 * d * keys * Hq, "unit": "TFLOP/s",
+                     "sources": ["linearized_attention_rope_gb300/csrc/window_softmax_tc.cu",
+                                 "linearized_attention_rope_gb300/csrc/umma.cuh",
+                                 "linearized_attention_rope_gb300/csrc/hla_common.cuh"],
+                     "kernel": "window_softmax_tc_kernel"}
+                    if wl.dtype == "bf16" and d == 128 else
+                    {"bound": "alu", "flops": 4.0 * d * keys * Hq, "peak": FP32_ALU_TFLOPS,
+                     "unit": "TFLOP/s", "sources": ["linearized_attention_rope_gb300/csrc/window_softmax.cu"],
+                     "kernel": "window_softmax_kernel"}),
         # read q, k, v; write RoPE'd q, k and qhat, khat, vhat
         "features": {"bound": "hbm", "bytes": float(T * d * ((Hq + 2 * Hkv) * eb + (2 * Hq + 3 * Hkv) * eb)),
                      "unit": "GB/s", "sources": ["linearized_attention_rope_gb300/csrc/features.cu"],
@@ -251,7 +268,7 @@ def run_prefill_bench(args, dist, peaks):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    n_stage = 4
+    n_stage = 5
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
     for row in ev:  # materialise the event handles
         for e in row:
@@ -273,25 +290,31 @@ def run_prefill_bench(args, dist, peaks):
     dist.barrier()
     step_ms = [ev[i][0].elapsed_time(ends[i]) for i in range(args.steps)]
     stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-                for j, name in enumerate(("features", "gdn", "softmax"))}
+                for j, name in enumerate(("features", "gdn_prep", "gdn_state", "softmax"))}
     device_s = dist.max(sum(step_ms) / 1e3)
     # rope tables, features, gdn (chunk table + inverse + state kernel when chunked), softmax
     launches_per_step = 6 if (wl.dtype == "bf16" and wl.head_dim == 128) else 4
 
     work = prefill_work(wl)
-    top = max(stage_ms, key=stage_ms.get)
-    w = work[top]
-    sec = stage_ms[top] / 1e3
-    if w["bound"] == "hbm":
-        achieved, peak = w["bytes"] / sec / 1e9, peaks["hbm_gbs"]
-    elif w["bound"] == "tensor":
-        achieved, peak = w["flops"] / sec / 1e12, peaks["bf16_tflops"]
-    else:
-        achieved, peak = w["flops"] / sec / 1e12, w["peak"]
-    roofline = {"kernel": w["kernel"], "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
+
+    def roof(name):
+        w, sec = work[name], stage_ms[name] / 1e3
+        if w["bound"] == "hbm":
+            achieved, peak = w["bytes"] / sec / 1e9, peaks["hbm_gbs"]
+        elif w["bound"] == "tensor":
+            achieved, peak = w["flops"] / sec / 1e12, peaks["bf16_tflops"]
+        else:
+            achieved, peak = w["flops"] / sec / 1e12, w["peak"]
+        return {"kernel": w["kernel"], "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
                 "unit": w["unit"], "frac": round(achieved / peak, 5),
                 "traffic": kernel_traffic(w["kernel"], w["sources"]),
                 "peak_source": peaks["source"] if w["bound"] != "alu" else FP32_ALU_TFLOPS_DERIVATION}
+
+    measured = [k for k in stage_ms if work.get(k)]
+    roofline = roof(max(measured, key=stage_ms.get))  # the dominant kernel
+    stage_roofline = {k: {kk: v for kk, v in roof(k).items() if kk in ("kernel", "bound", "achieved", "unit",
+                                                                         "frac")}
+                      for k in measured}
 
     # end to end through the C ABI: pinned host inputs in, result back to pinned host memory
     host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
@@ -316,6 +339,7 @@ def run_prefill_bench(args, dist, peaks):
     return {
         "value": tokens / device_s, "ms_per_step": device_s * 1e3 / args.steps, "wall_s": wall,
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "roofline": roofline,
+        "stage_roofline": stage_roofline,
         "clocks": clocks.summary(), "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -493,8 +517,8 @@ def main():
                    "seq_len": max(wl.seqlens), "tokens_per_rank": wl.total_tokens,
                    "parallelism": f"replicas x{dist.world}", "l2": "flushed between steps (512 MiB write)",
                    "precision": "bf16 in/out, fp16 MMA operands, fp32 state and accumulation"},
-        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"], "clocks": pre["clocks"],
-        "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"] + (dec["gpu_launches"] if dec else 0),
+        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"], "stage_roofline": pre["stage_roofline"],
+        "clocks": pre["clocks"], "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"],
         "wall_s": round(pre["wall_s"], 3),
     }
     if dec:

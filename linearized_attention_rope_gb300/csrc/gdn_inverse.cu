@@ -7,10 +7,12 @@
 // Transformer 线性化", section 线性注意力替换机制; q_r is qhat at position
 // r + W).  All chunks are independent, so this runs fully parallel, ahead of
 // the state-carrying kernel.  Per (chunk, q-head) it writes a record:
-//   T diag(beta), T diag(beta gamma), P   as fp16 byte images of 64 x 64
-//                                          K-major 128B-swizzled tiles (8 KB each)
+//   -Wm = -T diag(beta gamma) K             64 x 128 fp16 K-major 128B-swizzled
+//                                          image (two 8 KB key-dim halves)
+//   T diag(beta), P                        64 x 64 images of the same kind (8 KB each)
 //   gamma[64], e^{G_63 - G}[64]            fp32
-// which the state kernel copies into shared memory unchanged.
+// and, once per (chunk, kv head), V^T as a 128 x 64 image; the state kernel
+// copies all of them into shared memory unchanged.
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
@@ -25,8 +27,10 @@ namespace {
 
 constexpr int kC = 64, kD = 128, kThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kTmemCols = 128;               // Gram (64 columns), then Wm^T (128)
 constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
-constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]
+constexpr uint32_t kTbg = 8192;                   // T diag(beta gamma) image, over the first query block
+constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]; first holds V rows [64][128] fp16
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68]
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
 constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta
@@ -74,12 +78,12 @@ __global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ 
     base[L.n_seqs] = acc;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
-                   const float* __restrict__ g,
+                   const __half* __restrict__ vhat, const float* __restrict__ g,
                    const float* __restrict__ beta, const int32_t* __restrict__ cu,
                    const int32_t* __restrict__ chunk_base, unsigned char* __restrict__ rec_out,
-                   int32_t* __restrict__ err) {
+                   unsigned char* __restrict__ vt_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* sA = reinterpret_cast<float*>(sm + kA32);
@@ -99,7 +103,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         umma::mbar_init(mbar, 1);
         umma::fence_mbar_init();
     }
-    if (warp == 0) umma::tmem_alloc(tmem_slot, 64);
+    if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
     for (int i = tid; i < 32 * 32; i += kThreads) sT[(i >> 5) * 68 + 32 + (i & 31)] = 0.f;  // T01 = 0
     umma::fence_before_sync();
     __syncthreads();
@@ -136,6 +140,18 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                      "l"(src), "r"(rr < nv ? 16u : 0u)
                      : "memory");
     }
+    const bool vt_leader = (h % L.G) == 0;  // writes V^T for its kv head
+    if (vt_leader) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
+            const size_t t = (size_t)(start + j0 + (r < nv ? r : 0));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                             umma::smem_addr(sm + kA32 + r * 256 + c8 * 2)),
+                         "l"(vhat + (t * L.Hkv + kv) * kD + c8), "r"(r < nv ? 16u : 0u)
+                         : "memory");
+        }
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
     float gi = 0.f;
     if (tid < kC) {
@@ -165,7 +181,21 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::mma(tmem, umma::kmajor(sbase + kK, 128, s16), umma::kmajor(sbase + kK, 128, s16), id, s16 > 0);
         umma::commit(mbar);
     }
-    const bool done = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));  // also: sG complete
+    const size_t slot_kv = (size_t)slot * L.Hkv + kv;
+    if (vt_leader) {  // V^T image while the Gram runs: thread = value dim, 64 tokens per row
+        const unsigned char* vb = sm + kA32 + tid * 2;
+        uint32_t w[32];
+#pragma unroll
+        for (int r2 = 0; r2 < 32; ++r2)
+            w[r2] = (uint32_t)*reinterpret_cast<const uint16_t*>(vb + (2 * r2) * 256) |
+                    ((uint32_t)*reinterpret_cast<const uint16_t*>(vb + (2 * r2 + 1) * 256) << 16);
+        unsigned char* dst = vt_out + slot_kv * kVtBytes;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(dst + umma::sw128_offset(tid, 8 * u, 128)) =
+                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    }
+    const bool done = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));  // also: sG complete, V read
     phase ^= 1u;
     if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
     umma::fence_after_sync();
@@ -255,23 +285,62 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         const uint32_t off = umma::sw128_offset(r, c8, 64);
         *reinterpret_cast<uint4*>(rec + kRecTb + off) =
             make_uint4(pack_h2(tb[0], tb[1]), pack_h2(tb[2], tb[3]), pack_h2(tb[4], tb[5]), pack_h2(tb[6], tb[7]));
-        *reinterpret_cast<uint4*>(rec + kRecTbg + off) = make_uint4(
+        // T diag(beta gamma) over the query rows of the stack (no longer needed)
+        *reinterpret_cast<uint4*>(sm + kTbg + off) = make_uint4(
             pack_h2(tbg[0], tbg[1]), pack_h2(tbg[2], tbg[3]), pack_h2(tbg[4], tbg[5]), pack_h2(tbg[6], tbg[7]));
     }
-    __syncthreads();  // shared tiles are refilled by the next item
+    umma::fence_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+
+    // ---- Wm = T diag(beta gamma) K: M = 128 (rows 64..127 of A are don't-care),
+    //      N = 128 key dims, K = 64 tokens (the key rows of the stack, MN-major)
+    if (tid == 0) {
+        umma::fence_after_sync();
+        const uint32_t id = umma::idesc_f16(128, kD, false, true, false);
+#pragma unroll
+        for (int s16 = 0; s16 < kC / 16; ++s16)
+            umma::mma(tmem, umma::kmajor(sbase + kTbg, 128, s16), umma::mnmajor(sbase + kK, 16384, s16), id,
+                      s16 > 0);
+        umma::commit(mbar);
+    }
+    const bool done_w = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));
+    phase ^= 1u;
+    if (!done_w) {
+        if (tid == 0 && err) atomicExch(err, kErrTimeout);
+        break;
+    }
+    umma::fence_after_sync();
+    if (warp < 2) {  // -Wm row r -> record image
+        const int r = tid;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float wv[32];
+            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * q4, wv);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float* x = wv + 8 * u;
+                *reinterpret_cast<uint4*>(rec + kRecWm + umma::sw128_offset(r, 32 * q4 + 8 * u, 64)) =
+                    make_uint4(pack_h2(-x[0], -x[1]), pack_h2(-x[2], -x[3]), pack_h2(-x[4], -x[5]),
+                               pack_h2(-x[6], -x[7]));
+            }
+        }
+    }
+    umma::fence_before_sync();
+    __syncthreads();  // shared tiles and TMEM are reused by the next item
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, 64);
+    if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
 size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
 
-cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
-                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
-                               int32_t* err, cudaStream_t st) {
+cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
+                               const float* g, const float* beta, const int32_t* cu, int32_t* chunk_base,
+                               unsigned char* rec_out, unsigned char* vt_out, int32_t* err, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -291,7 +360,8 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
     }
     const int64_t items = (int64_t)gdn_chunk_slots(L.total, L.n_seqs) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
-    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
+    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, vhat, g, beta, cu, chunk_base, rec_out,
+                                                                    vt_out, err);
     return cudaGetLastError();
 }
 
