@@ -13,25 +13,35 @@
 // where the query of token j is qhat at position j + W.
 //
 // The value columns of S never mix (every product above acts on S from the
-// left), so a CTA owns one slice of NS value columns of one (sequence,
-// q-head) state: 128 / NS CTAs share a head and the state chain runs on that
-// many SMs at once.  With the chunk rows stacked on the 128 TMEM lanes every
-// MMA has M = 128 and N = NS:
+// left), so a CTA owns one 64-column slice of the value dims of one
+// (sequence, q-head) state: two CTAs share a head and the state chains run
+// on twice as many SMs.  With the chunk rows stacked on the 128 TMEM lanes
+// every MMA has M = 128 and N = 64:
 //   D1[b] = [-Wm ; Q] S0  +  [T diag(beta) ; 0] V      rows 0..63 = U, 64..127 = Q S0
 //   D2[b] = [0 ; P] U                                   rows 64..127 = P U
 //   DS    = K^T diag(e^{G_C - G}) U                     (key dims on the lanes)
 // fp16 operands in shared memory, fp32 accumulators in TMEM; the zero blocks
-// pad the 64-row operands to M = 128.  S0 stays in fp32 registers (one key
-// row per thread) and is re-rounded to fp16 for the next chunk's MMA.
+// pad the 64-row operands to M = 128.  S0, V, U are MN-major B operands (one
+// 128-byte row per key dim or token), so every epilogue thread writes its
+// own row.  S0 stays in fp32 registers (one key row per thread) and is
+// re-rounded to fp16 for the next chunk's MMA.
 //
-// Roles (256 threads): warps 0-3 run the chain (MMA issue, U and S
-// epilogues); warps 4-5 load chunk c+1 into the other buffer (cp.async);
-// warps 6-7 turn the double-buffered D1/D2 rows 64..127 into o_lin rows
-// (o = gamma Q S0 + P U).  Handoffs use mbarriers: ready[b] (load -> chain),
-// free[b] (chain + output -> load), ofull[b] (MMA -> output), ofree[b]
-// (output -> chain).  Every wait has an iteration limit; on expiry the kernel
-// records a timeout in the error word and all roles stop.
+// Roles (256 threads; the rest of warps 4-5 idle): one thread of warp 4 loads chunk c+1 into the other
+// buffer (TMA: tensor copies of the query, key and value rows, bulk copies
+// of the record) and starts its D1 with the S-independent [T diag(beta) ; 0] V;
+// warps 0-3 run the chain: D1 += [-Wm ; Q] S0, the U epilogue, DS and then
+// D2 (whose issue hides under DS's latency), the S epilogue; warps 6-7 turn
+// the double-buffered D1/D2 rows 64..127 into o_lin rows
+// (o = gamma Q S0 + P U).  Handoffs use mbarriers: loaded[b] (TMA bytes),
+// ready[b] (the V MMAs -> chain), free[b] (chain + output -> load), ofull[b]
+// (MMA -> output).  Token rows past a chunk's end hold whatever follows
+// (zeros past the tensor): they meet zero rows of -Wm, T diag(beta) and U,
+// or produce output rows that are not stored.  Every wait has an iteration limit; on expiry the kernel records
+// a timeout in the error word and all roles stop.  Loops stay rolled
+// where registers allow: the whole kernel is executed once per chunk by
+// every role, and compact code keeps it resident in the instruction cache.
 #include "hla_common.cuh"
+#include "tma.cuh"
 #include "umma.cuh"
 
 namespace hla {
@@ -40,43 +50,43 @@ namespace {
 
 constexpr int kC = 64;    // chunk length (absorbed tokens)
 constexpr int kD = 128;   // head dim
+constexpr int kNS = 64;   // value columns per CTA
+constexpr int kSlices = kD / kNS;
 constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// shared-memory plan for value-slice width NS (bytes from a 1024-aligned base)
-template <int NS>
-struct Plan {
-    // one chunk buffer
-    static constexpr uint32_t kA1 = 0;              // [-Wm ; Q] 128 x 128, K-major
-    static constexpr uint32_t kTZP = 32768;         // [T diag(beta) | 0 | P], three 64 x 64 K-major images
-    static constexpr uint32_t kK = 57344;           // K rows 64 x 128 (MN-major A of DS)
-    static constexpr uint32_t kVt = 73728;          // V^T slice NS x 64 (K-major B)
-    static constexpr uint32_t kVec = kVt + NS * 128;  // gamma[64], key decay[64]
-    static constexpr uint32_t kBuf = (kVec + 512 + 1023) / 1024 * 1024;
-    // chain operands
-    static constexpr uint32_t kS = 2 * kBuf;         // S0 slice, NS x 128 (K-major B)
-    static constexpr uint32_t kU = kS + NS * 256;    // U slice, NS x 64 (K-major B)
-    static constexpr uint32_t kUk = kU + NS * 128;   // diag(key decay) U slice
-    static constexpr uint32_t kBar = kUk + NS * 128;
-    static constexpr uint32_t kSmemAlloc = kBar + 128 + 1024;
-    // TMEM columns
-    static constexpr uint32_t kColD1 = 0, kColD2 = 2 * NS, kColS = 4 * NS;
-    static constexpr uint32_t kTmemCols = 5 * NS <= 256 ? 256 : 512;
-};
+// shared-memory plan (bytes from a 1024-aligned base); one chunk buffer:
+constexpr uint32_t kA1 = 0;         // [-Wm ; Q] 128 x 128, K-major
+constexpr uint32_t kTZP = 32768;    // [T diag(beta) | 0 | P], three 64 x 64 K-major images
+constexpr uint32_t kK = 57344;      // K rows 64 x 128 (MN-major A of DS)
+constexpr uint32_t kV = 73728;      // V slice rows 64 x 64 (MN-major B)
+constexpr uint32_t kVec = 81920;    // gamma[64], key decay[64]
+constexpr uint32_t kBuf = 82944;
+// chain operands
+constexpr uint32_t kS = 2 * kBuf;   // S0 slice rows 128 x 64 (MN-major B)
+constexpr uint32_t kU = kS + 16384;   // U slice rows 64 x 64 (MN-major B)
+constexpr uint32_t kUk = kU + 8192;   // diag(key decay) U
+constexpr uint32_t kBar = kUk + 8192;
+constexpr uint32_t kSmemAlloc = kBar + 128 + 1024;
+// TMEM columns
+constexpr uint32_t kColD1 = 0, kColD2 = 128, kColS = 256, kTmemCols = 512;
 
 // mbarrier indices
-constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kOFree = 8, kNumBars = 10;
+constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kNumBars = 10;
+constexpr uint32_t kLoadBytes = kRecordBytes + 5 * 8192;  // record + query, key rows (2 boxes each) + value slice
 
 __device__ __forceinline__ void st16(unsigned char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ uint4 pack8(const float* v, float s) {
+    return make_uint4(pack_h2(v[0] * s, v[1] * s), pack_h2(v[2] * s, v[3] * s), pack_h2(v[4] * s, v[5] * s),
+                      pack_h2(v[6] * s, v[7] * s));
+}
 // 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills zeros.
-__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_addr(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -99,53 +109,28 @@ __device__ __forceinline__ bool group_all(int id, int count, bool v) {
     return r != 0;
 }
 
-// NS fp32 TMEM columns of this thread's lane.
-template <int NS>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float* v) {
-#pragma unroll
-    for (int q = 0; q < NS / 32; ++q) umma::tmem_ld32(taddr + 32 * q, v + 32 * q);
-}
+// Descriptor offsets (address field, 16-byte units) of K step s: a 128-row
+// K-major tile advances 32 B inside a 64-column block and 16 KB per block;
+// an MN-major tile advances 16 rows = 2 KB.
+__device__ __forceinline__ uint64_t kstep128(int s) { return (uint64_t)((s >> 2) * 1024 + (s & 3) * 2); }
+__device__ __forceinline__ uint64_t mnstep(int s) { return (uint64_t)(s * 128); }
 
-// Writes x[0..NS) of this thread (row k of a K-major image with NS rows,
-// element (n, k) = x[n] of thread k) as fp16, pairing with the neighbour lane
-// k ^ 1 so every store is 4 bytes: the even lane stores even rows n, the odd
-// lane odd rows.  The thread's own values are scaled by own_scale, the
-// partner's by partner_scale (per-row factors of the K index).
-template <int NS>
-__device__ __forceinline__ void store_transposed(unsigned char* img, const float* x, int k, float own_scale,
-                                                 float partner_scale) {
-    const bool odd = k & 1;
-#pragma unroll
-    for (int m = 0; m < NS / 2; ++m) {
-        const float send = odd ? x[2 * m] : x[2 * m + 1];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-        const float own = odd ? x[2 * m + 1] : x[2 * m];
-        const float lo = odd ? recv * partner_scale : own * own_scale;
-        const float hi = odd ? own * own_scale : recv * partner_scale;
-        *reinterpret_cast<uint32_t*>(img + umma::sw128_offset(2 * m + (odd ? 1 : 0), k & ~1, NS)) =
-            pack_h2(lo, hi);
-    }
-}
-
-template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
-gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
-                   const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_base,
-                   const unsigned char* __restrict__ rec_in, const unsigned char* __restrict__ vt_in,
+gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ cu,
+                   const int32_t* __restrict__ chunk_base, const unsigned char* __restrict__ rec_in,
                    float* __restrict__ o_lin, float* __restrict__ S_out, int32_t* __restrict__ err) {
-    using P = Plan<NS>;
-    constexpr int kSlices = kD / NS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::kBar + 8 * kNumBars);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P::kBar + 8 * kNumBars + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
     const int h = blockIdx.x / kSlices, slice = blockIdx.x % kSlices, n = blockIdx.y;
     const int kv = h / L.G, W = L.window;
     const uint32_t sbase = umma::smem_addr(sm);
-    const uint32_t bar0 = umma::smem_addr(sm + P::kBar);
+    const uint32_t bar0 = umma::smem_addr(sm + kBar);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     int64_t start, len;
@@ -159,218 +144,209 @@ gdn_chunked_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         umma::fence_mbar_init();
         *abort_flag = 0;
     }
-    if (warp == 0) umma::tmem_alloc(tmem_slot, P::kTmemCols);
-    for (int i = tid; i < NS * 256 / 16; i += kThreads) st16(sm + P::kS + 16 * i, make_uint4(0, 0, 0, 0));
+    if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
+#pragma unroll 1
+    for (int i = tid; i < 16384 / 16; i += kThreads) st16(sm + kS + 16 * i, make_uint4(0, 0, 0, 0));
+#pragma unroll 1
     for (int i = tid; i < 2 * 512; i += kThreads)  // the zero blocks of both buffers
-        st16(sm + (i >> 9) * P::kBuf + P::kTZP + 8192 + 16 * (i & 511), make_uint4(0, 0, 0, 0));
+        st16(sm + (i >> 9) * kBuf + kTZP + 8192 + 16 * (i & 511), make_uint4(0, 0, 0, 0));
     umma::fence_async_smem();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    auto wait = [&](int i, uint32_t parity) -> bool {
-        if (*abort_flag) return false;
-        const bool done = umma::mbar_wait(bar(i), parity, kWaitLimit);
-        if (!done) {
-            *abort_flag = 1;
-            if (err) atomicExch(err, kErrTimeout);
+    // One leader per role polls the mbarrier (an inline try first, the bounded
+    // loop only if the phase is still open); the role (`count` threads on named
+    // barrier `id`; 0 for a one-thread role) then votes, so every thread takes
+    // the same branch, and fences before touching the results.
+    auto role_wait = [&](int i, uint32_t parity, int id, int count, bool leader) -> bool {
+        bool w = true;
+        if (leader) {
+            w = !*abort_flag && (umma::mbar_try_wait(bar(i), parity) || umma::mbar_wait(bar(i), parity, kWaitLimit));
+            if (!w) {
+                *abort_flag = 1;
+                if (err) atomicExch(err, kErrTimeout);
+            }
         }
+        const bool ok = count ? group_all(id, count, w) : w;
         umma::fence_after_sync();
-        return done;
+        return ok;
     };
 
     if (warp < 4) {
         // ================= the state chain =================
-        float S[NS];  // S0[tid][slice columns]: fp32 master copy
+        float S[kNS];  // S0[tid][slice columns]: fp32 master copy
 #pragma unroll
-        for (int i = 0; i < NS; ++i) S[i] = 0.f;
-        const uint32_t id = umma::idesc_f16(128, NS, false, false, false);
-        const uint32_t id_amn = umma::idesc_f16(128, NS, true, false, false);
+        for (int i = 0; i < kNS; ++i) S[i] = 0.f;
+        const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
+        const uint32_t id_ab = umma::idesc_f16(128, kNS, true, true, false);
         uint32_t ph1 = 0, ph2 = 0;
         bool ok = true;
+#pragma unroll 1
         for (int c = 0; c < n_chunks && ok; ++c) {
             const int b = c & 1;
-            const uint32_t buf = (uint32_t)b * P::kBuf;
-            ok = group_all(1, 128, wait(kReady + b, (uint32_t)((c >> 1) & 1)));
-            if (ok && c >= 2) ok = group_all(1, 128, wait(kOFree + b, (uint32_t)(((c - 2) >> 1) & 1)));
-            if (!ok) break;
+            const uint32_t buf = (uint32_t)b * kBuf;
+            // ready[b]: the chunk is loaded and D1[b] holds [T diag(beta) ; 0] V; the
+            // loader waited for free[b], so the output rows of chunk c - 2 are out of D1/D2[b]
+            if (!(ok = role_wait(kReady + b, (uint32_t)((c >> 1) & 1), 1, 128, tid == 0))) break;
 
-            // D1[b] = [-Wm ; Q] S0 + [T diag(beta) ; 0] V
+            // D1[b] += [-Wm ; Q] S0
             if (tid == 0) {
-                const uint32_t d1 = tmem + P::kColD1 + NS * b;
+                const uint32_t d1 = tmem + kColD1 + kNS * b;
+                const uint64_t a1 = umma::kmajor(sbase + buf + kA1, 128, 0), bs = umma::mnmajor(sbase + kS, 8192u, 0);
 #pragma unroll
-                for (int s = 0; s < kD / 16; ++s)
-                    umma::mma(d1, umma::kmajor(sbase + buf + P::kA1, 128, s), umma::kmajor(sbase + P::kS, NS, s), id,
-                              s > 0);
-#pragma unroll
-                for (int s = 0; s < kC / 16; ++s)
-                    umma::mma(d1, umma::kmajor(sbase + buf + P::kTZP, 128, s), umma::kmajor(sbase + buf + P::kVt, NS, s),
-                              id, true);
+                for (int s = 0; s < kD / 16; ++s) umma::mma(d1, a1 + kstep128(s), bs + mnstep(s), id_b, true);
                 umma::commit(bar(kMma1));
             }
-            ok = group_all(1, 128, wait(kMma1, ph1));
+            if (!(ok = role_wait(kMma1, ph1, 1, 128, tid == 0))) break;
             ph1 ^= 1u;
-            if (!ok) break;
 
-            // U (rows 0..63) -> fp16 K-major images U and diag(key decay) U
+            // U (rows 0..63) -> fp16 rows of U and diag(key decay) U
             if (warp < 2) {
-                const float* kdec = reinterpret_cast<const float*>(sm + buf + P::kVec) + kC;
-                float u[NS];
-                tmem_ld<NS>(tmem + lane_base + P::kColD1 + NS * b, u);
-                store_transposed<NS>(sm + P::kU, u, tid, 1.f, 1.f);
-                store_transposed<NS>(sm + P::kUk, u, tid, kdec[tid], kdec[tid ^ 1]);
+                const float kd = reinterpret_cast<const float*>(sm + buf + kVec)[kC + tid];
+#pragma unroll 1
+                for (int q = 0; q < 2; ++q) {
+                    float u[32];
+                    umma::tmem_ld32(tmem + lane_base + kColD1 + kNS * b + 32 * q, u);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t off = umma::sw128_offset(tid, 32 * q + 8 * j, 64);
+                        st16(sm + kU + off, pack8(u + 8 * j, 1.f));
+                        st16(sm + kUk + off, pack8(u + 8 * j, kd));
+                    }
+                }
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
             group_sync(1, 128);
 
-            // D2[b] = [0 ; P] U;  DS = K^T diag(key decay) U
+            // DS = K^T diag(key decay) U (the chain waits for this), then D2[b] = [0 ; P] U
             if (tid == 0) {
                 umma::fence_after_sync();
+                const uint64_t zp = umma::kmajor(sbase + buf + kTZP + 8192, 128, 0), bu = umma::mnmajor(sbase + kU, 8192u, 0);
+                const uint64_t ak = umma::mnmajor(sbase + buf + kK, 8192u, 0), buk = umma::mnmajor(sbase + kUk, 8192u, 0);
 #pragma unroll
-                for (int s = 0; s < kC / 16; ++s)
-                    umma::mma(tmem + P::kColD2 + NS * b, umma::kmajor(sbase + buf + P::kTZP + 8192, 128, s),
-                              umma::kmajor(sbase + P::kU, NS, s), id, s > 0);
-#pragma unroll
-                for (int s = 0; s < kC / 16; ++s)
-                    umma::mma(tmem + P::kColS, umma::mnmajor(sbase + buf + P::kK, 8192, s),
-                              umma::kmajor(sbase + P::kUk, NS, s), id_amn, s > 0);
+                for (int s = 0; s < kC / 16; ++s) umma::mma(tmem + kColS, ak + mnstep(s), buk + mnstep(s), id_ab, s > 0);
                 umma::commit(bar(kMma2));
+#pragma unroll
+                for (int s = 0; s < kC / 16; ++s)
+                    umma::mma(tmem + kColD2 + kNS * b, zp + kstep128(s), bu + mnstep(s), id_b, s > 0);
                 umma::commit(bar(kOFull + b));
             }
-            ok = group_all(1, 128, wait(kMma2, ph2));
+            if (!(ok = role_wait(kMma2, ph2, 1, 128, tid == 0))) break;
             ph2 ^= 1u;
-            if (!ok) break;
-            const float gC = reinterpret_cast<const float*>(sm + buf + P::kVec)[kC - 1];  // gamma_C
+            const float gC = reinterpret_cast<const float*>(sm + buf + kVec)[kC - 1];  // gamma_C
             group_sync(1, 128);
-            if (tid == 0) mbar_arrive(bar(kFree + b));  // the chain is done with buffer b
+            // the chain is done with buffer b (D2's reads of it end before the output arrives)
+            if (tid == 0) mbar_arrive(bar(kFree + b));
 
-            // S <- gamma_C S + DS; fp16 copy for the next chunk
-            {
-                float ds[NS];
-                tmem_ld<NS>(tmem + lane_base + P::kColS, ds);
+            // S <- gamma_C S + DS; fp16 row for the next chunk
 #pragma unroll
-                for (int i = 0; i < NS; ++i) S[i] = fmaf(gC, S[i], ds[i]);
-                store_transposed<NS>(sm + P::kS, S, tid, 1.f, 1.f);
+            for (int q = 0; q < 2; ++q) {
+                float ds[32];
+                umma::tmem_ld32(tmem + lane_base + kColS + 32 * q, ds);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) S[32 * q + i] = fmaf(gC, S[32 * q + i], ds[i]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st16(sm + kS + umma::sw128_offset(tid, 32 * q + 8 * j, 128), pack8(S + 32 * q + 8 * j, 1.f));
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
             group_sync(1, 128);
         }
         if (ok && S_out) {
-            float* dst = S_out + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * NS;
+            float* dst = S_out + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
 #pragma unroll
-            for (int i = 0; i < NS; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+            for (int i = 0; i < kNS; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
         }
-    } else if (warp < 6) {
-        // ================= loads, one chunk ahead =================
-        const int p = tid - 128;
+    } else if (tid == 128) {
+        // ================= loads, one chunk ahead (one thread) =================
+        const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
+#pragma unroll 1
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
-            if (c >= 2 && !group_all(2, 64, wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1)))) break;
-            unsigned char* buf = sm + b * P::kBuf;
-            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-            const int nv = (int)min((int64_t)kC, j_end - j0);
-#pragma unroll 4
-            for (int u = 0; u < 16; ++u) {  // query rows (positions j + W) and key rows, zero past the chunk
-                const int e = p + 64 * u, r = e >> 4, c8 = (e & 15) * 8;
-                const uint32_t nb = r < nv ? 16u : 0u;
-                const size_t t = (size_t)(start + j0 + (r < nv ? r : 0));
-                cp_async16(buf + P::kA1 + umma::sw128_offset(64 + r, c8, 128), qhat + ((t + W) * L.Hq + h) * kD + c8, nb);
-                cp_async16(buf + P::kK + umma::sw128_offset(r, c8, 64), khat + (t * L.Hkv + kv) * kD + c8, nb);
-            }
+            if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true)) break;
+            const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
+            const int tok = (int)(start + L.n_sinks + (int64_t)c * kC);  // first absorbed token of the chunk
             const unsigned char* rec = rec_in + ((size_t)(slot0 + c) * L.Hq + h) * kRecordBytes;
-#pragma unroll 4
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t o = 16u * (uint32_t)(p + 64 * u);
-                cp_async16(buf + P::kA1 + o, rec + kRecWm + o, 16u);                 // -Wm, key dims 0..63
-                cp_async16(buf + P::kA1 + 16384 + o, rec + kRecWm + 8192 + o, 16u);  // key dims 64..127
-                cp_async16(buf + P::kTZP + o, rec + kRecTb + o, 16u);
-                cp_async16(buf + P::kTZP + 16384 + o, rec + kRecP + o, 16u);
-            }
-            if (p < 32) cp_async16(buf + P::kVec + 16 * p, rec + kRecVec + 16 * p, 16u);
-            const unsigned char* vt =
-                vt_in + ((size_t)(slot0 + c) * L.Hkv + kv) * kVtBytes + (size_t)slice * NS * 128;
+            tma::expect_tx(ld, kLoadBytes);
+            tma::bulk_load(buf + kA1, rec + kRecWm, 8192, ld);                   // -Wm, key dims 0..63
+            tma::bulk_load(buf + kA1 + 16384, rec + kRecWm + 8192, 8192, ld);    // key dims 64..127
+            tma::bulk_load(buf + kTZP, rec + kRecTb, 8192, ld);
+            tma::bulk_load(buf + kTZP + 16384, rec + kRecP, 8192, ld);
+            tma::bulk_load(buf + kVec, rec + kRecVec, kRecordBytes - kRecVec, ld);
+            tma::tensor_load_3d(buf + kA1 + 8192, &map_q, 0, h, tok + W, ld);    // query rows (positions j + W)
+            tma::tensor_load_3d(buf + kA1 + 16384 + 8192, &map_q, 64, h, tok + W, ld);
+            tma::tensor_load_3d(buf + kK, &map_k, 0, kv, tok, ld);
+            tma::tensor_load_3d(buf + kK + 8192, &map_k, 64, kv, tok, ld);
+            tma::tensor_load_3d(buf + kV, &map_v, slice * kNS, kv, tok, ld);
+            if (!role_wait(kLoaded + b, (uint32_t)((c >> 1) & 1), 0, 0, true)) break;
+            // D1[b] = [T diag(beta) ; 0] V; its completion releases the chunk to the chain
+            const uint64_t tb = umma::kmajor(buf + kTZP, 128, 0), bv = umma::mnmajor(buf + kV, 8192u, 0);
 #pragma unroll
-            for (int u = 0; u < NS * 128 / 16 / 64; ++u) {
-                const uint32_t o = 16u * (uint32_t)(p + 64 * u);
-                cp_async16(buf + P::kVt + o, vt + o, 16u);
-            }
-            cp_async_commit();
-            cp_async_wait_all();
-            umma::fence_async_smem();
-            group_sync(2, 64);
-            if (p == 0) mbar_arrive(bar(kReady + b));
+            for (int s = 0; s < kC / 16; ++s) umma::mma(tmem + kColD1 + kNS * b, tb + kstep128(s), bv + mnstep(s), id_b, s > 0);
+            umma::commit(bar(kReady + b));
         }
-    } else {
+    } else if (warp >= 6) {
         // ================= o_lin rows: gamma (Q S0) + P U =================
         const int r = tid - 192;  // chunk row; TMEM lane 64 + r
+#pragma unroll 1
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
-            if (!group_all(3, 64, wait(kOFull + b, (uint32_t)((c >> 1) & 1)))) break;
-            const float gr = reinterpret_cast<const float*>(sm + b * P::kBuf + P::kVec)[r];
-            float d1[NS], d2[NS];
-            tmem_ld<NS>(tmem + lane_base + P::kColD1 + NS * b, d1);
-            tmem_ld<NS>(tmem + lane_base + P::kColD2 + NS * b, d2);
+            if (!role_wait(kOFull + b, (uint32_t)((c >> 1) & 1), 3, 64, r == 0)) break;
+            const float gr = reinterpret_cast<const float*>(sm + b * kBuf + kVec)[r];
+            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+            const bool row_on = r < j_end - j0;
+            float* orow = o_lin + ((size_t)(start + j0 + (row_on ? r : 0) + W) * L.Hq + h) * kD + slice * kNS;
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {
+                float d1[32], d2[32];
+                umma::tmem_ld32(tmem + lane_base + kColD1 + kNS * b + 32 * q, d1);
+                umma::tmem_ld32(tmem + lane_base + kColD2 + kNS * b + 32 * q, d2);
+                if (row_on) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(orow + 32 * q + i) =
+                            make_float4(fmaf(gr, d1[i], d2[i]), fmaf(gr, d1[i + 1], d2[i + 1]),
+                                        fmaf(gr, d1[i + 2], d2[i + 2]), fmaf(gr, d1[i + 3], d2[i + 3]));
+                }
+            }
             umma::fence_before_sync();
             group_sync(3, 64);
-            if (r == 0) {
-                mbar_arrive(bar(kOFree + b));
-                mbar_arrive(bar(kFree + b));
-            }
-            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-            if (r < j_end - j0) {
-                float* orow = o_lin + ((size_t)(start + j0 + r + W) * L.Hq + h) * kD + slice * NS;
-#pragma unroll
-                for (int i = 0; i < NS; i += 4)
-                    *reinterpret_cast<float4*>(orow + i) =
-                        make_float4(fmaf(gr, d1[i], d2[i]), fmaf(gr, d1[i + 1], d2[i + 1]),
-                                    fmaf(gr, d1[i + 2], d2[i + 2]), fmaf(gr, d1[i + 3], d2[i + 3]));
-            }
+            if (r == 0) mbar_arrive(bar(kFree + b));
         }
     }
 
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, P::kTmemCols);
-}
-
-template <int NS>
-cudaError_t launch_ns(const LayerDims& L, const __half* qhat, const __half* khat, const int32_t* cu,
-                      const int32_t* chunk_base, const unsigned char* rec_in, const unsigned char* vt_in,
-                      float* o_lin, float* S_out, int32_t* err, cudaStream_t st) {
-    static bool configured = false;  // the attribute is per instantiation
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Plan<NS>::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    dim3 grid(L.Hq * (kD / NS), L.n_seqs);
-    gdn_chunked_kernel<NS><<<grid, kThreads, Plan<NS>::kSmemAlloc, st>>>(L, qhat, khat, cu, chunk_base, rec_in,
-                                                                        vt_in, o_lin, S_out, err);
-    return cudaGetLastError();
+    if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
-cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const int32_t* cu,
-                               const int32_t* chunk_base, const unsigned char* rec_in,
-                               const unsigned char* vt_in, float* o_lin, float* S_out, int32_t* err,
-                               cudaStream_t st) {
-    static int n_sm = 0;  // per-process device property cache
-    if (!n_sm) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
-            n_sm = 148;
+cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
+                               const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
+                               float* o_lin, float* S_out, int32_t* err, cudaStream_t st) {
+    static bool configured = false;  // the attribute is per function
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured = true;
     }
-    // narrow slices while the state chains alone do not fill the SMs
-    const int64_t chains = (int64_t)L.n_seqs * L.Hq;
-    if (chains * (kD / 32) <= n_sm)
-        return launch_ns<32>(L, qhat, khat, cu, chunk_base, rec_in, vt_in, o_lin, S_out, err, st);
-    return launch_ns<64>(L, qhat, khat, cu, chunk_base, rec_in, vt_in, o_lin, S_out, err, st);
+    if (L.total <= 0)  // no token anywhere: the final states are zero
+        return S_out ? cudaMemsetAsync(S_out, 0, (size_t)L.n_seqs * L.Hq * kD * kD * sizeof(float), st) : cudaSuccess;
+    CUtensorMap mq, mk, mv;
+    if (!tma::make_map_f16_3d(&mq, qhat, kD, (uint64_t)L.Hq, (uint64_t)L.total) ||
+        !tma::make_map_f16_3d(&mk, khat, kD, (uint64_t)L.Hkv, (uint64_t)L.total) ||
+        !tma::make_map_f16_3d(&mv, vhat, kD, (uint64_t)L.Hkv, (uint64_t)L.total))
+        return cudaErrorInvalidValue;
+    dim3 grid(L.Hq * kSlices, L.n_seqs);
+    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, rec_in, o_lin, S_out, err);
+    return cudaGetLastError();
 }
 
 }  // namespace hla

@@ -11,8 +11,7 @@
 //                                          image (two 8 KB key-dim halves)
 //   T diag(beta), P                        64 x 64 images of the same kind (8 KB each)
 //   gamma[64], e^{G_63 - G}[64]            fp32
-// and, once per (chunk, kv head), V^T as a 128 x 64 image; the state kernel
-// copies all of them into shared memory unchanged.
+// which the state kernel copies into shared memory unchanged.
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
@@ -30,7 +29,7 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kTmemCols = 128;               // Gram (64 columns), then Wm^T (128)
 constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
 constexpr uint32_t kTbg = 8192;                   // T diag(beta gamma) image, over the first query block
-constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]; first holds V rows [64][128] fp16
+constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68]
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
 constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta
@@ -80,10 +79,10 @@ __global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ 
 
 __global__ void __launch_bounds__(kThreads, 3)
 gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
-                   const __half* __restrict__ vhat, const float* __restrict__ g,
+                   const float* __restrict__ g,
                    const float* __restrict__ beta, const int32_t* __restrict__ cu,
                    const int32_t* __restrict__ chunk_base, unsigned char* __restrict__ rec_out,
-                   unsigned char* __restrict__ vt_out, int32_t* __restrict__ err) {
+                   int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* sA = reinterpret_cast<float*>(sm + kA32);
@@ -140,18 +139,6 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                      "l"(src), "r"(rr < nv ? 16u : 0u)
                      : "memory");
     }
-    const bool vt_leader = (h % L.G) == 0;  // writes V^T for its kv head
-    if (vt_leader) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
-            const size_t t = (size_t)(start + j0 + (r < nv ? r : 0));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                             umma::smem_addr(sm + kA32 + r * 256 + c8 * 2)),
-                         "l"(vhat + (t * L.Hkv + kv) * kD + c8), "r"(r < nv ? 16u : 0u)
-                         : "memory");
-        }
-    }
     asm volatile("cp.async.commit_group;" ::: "memory");
     float gi = 0.f;
     if (tid < kC) {
@@ -181,21 +168,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
             umma::mma(tmem, umma::kmajor(sbase + kK, 128, s16), umma::kmajor(sbase + kK, 128, s16), id, s16 > 0);
         umma::commit(mbar);
     }
-    const size_t slot_kv = (size_t)slot * L.Hkv + kv;
-    if (vt_leader) {  // V^T image while the Gram runs: thread = value dim, 64 tokens per row
-        const unsigned char* vb = sm + kA32 + tid * 2;
-        uint32_t w[32];
-#pragma unroll
-        for (int r2 = 0; r2 < 32; ++r2)
-            w[r2] = (uint32_t)*reinterpret_cast<const uint16_t*>(vb + (2 * r2) * 256) |
-                    ((uint32_t)*reinterpret_cast<const uint16_t*>(vb + (2 * r2 + 1) * 256) << 16);
-        unsigned char* dst = vt_out + slot_kv * kVtBytes;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(dst + umma::sw128_offset(tid, 8 * u, 128)) =
-                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-    }
-    const bool done = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));  // also: sG complete, V read
+    const bool done = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));  // also: sG complete
     phase ^= 1u;
     if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
     umma::fence_after_sync();
@@ -338,9 +311,9 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 
 size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
 
-cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
-                               const float* g, const float* beta, const int32_t* cu, int32_t* chunk_base,
-                               unsigned char* rec_out, unsigned char* vt_out, int32_t* err, cudaStream_t st) {
+cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
+                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
+                               int32_t* err, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -360,8 +333,7 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
     }
     const int64_t items = (int64_t)gdn_chunk_slots(L.total, L.n_seqs) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
-    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, vhat, g, beta, cu, chunk_base, rec_out,
-                                                                    vt_out, err);
+    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
     return cudaGetLastError();
 }
 

@@ -51,7 +51,7 @@ size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
 
 // Workspace layout of one prefill.
 struct WsLayout {
-    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, chunk_base, tinv, vt, total;
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, chunk_base, tinv, total;
     int n_coarse;
 };
 
@@ -78,7 +78,6 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     const bool chunked = uses_chunked_gdn(prm);
     w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
     w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
-    w.vt = off;     off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hkv * kVtBytes : 0));
     w.total = off;
     return w;
 }
@@ -132,10 +131,9 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
         if constexpr (std::is_same<Tf, __half>::value) {
             int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
-            unsigned char* vt = reinterpret_cast<unsigned char*>(ws + w.vt);
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, vh, g, beta, cu, chunk_base, rec, vt, err, stream));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, stream));
             HLA_TRY(mark_stage(2, stream));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, cu, chunk_base, rec, vt, olin, S_out, err, stream));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, olin, S_out, err, stream));
         }
     } else {
         HLA_TRY(mark_stage(2, stream));

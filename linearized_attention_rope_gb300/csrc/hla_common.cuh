@@ -134,16 +134,13 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
 // images, then gamma and the key decay (fp32, 64 each).
 // Step 2: the state-carrying kernel.
 constexpr uint32_t kRecWm = 0, kRecTb = 16384, kRecP = 24576, kRecVec = 32768, kRecordBytes = 33280;
-// and, per chunk and kv head, V^T as a 128 x 64 fp16 K-major swizzled image.
-constexpr uint32_t kVtBytes = 16384;
 size_t gdn_chunk_slots(int64_t total, int n_seqs);
-cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
-                               const float* g, const float* beta, const int32_t* cu, int32_t* chunk_base,
-                               unsigned char* rec_out, unsigned char* vt_out, int32_t* err, cudaStream_t st);
-cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const int32_t* cu,
-                               const int32_t* chunk_base, const unsigned char* rec_in,
-                               const unsigned char* vt_in, float* o_lin, float* S_out, int32_t* err,
-                               cudaStream_t st);
+cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
+                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
+                               int32_t* err, cudaStream_t st);
+cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
+                               const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
+                               float* o_lin, float* S_out, int32_t* err, cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>

@@ -96,8 +96,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of the mbarrier; gives up after `limit` polls
-// (each poll may itself suspend for a while) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+// (each poll may itself suspend for a while) and returns false.  Kept out of
+// line with a rolled loop: an unrolled copy at every call site bloats the
+// kernels well past the instruction cache.
+static __device__ __noinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+#pragma unroll 1
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(mbar, parity)) return true;
     return false;
