@@ -38,12 +38,67 @@ cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse,
     return cudaGetLastError();
 }
 
-constexpr int kFeatTokens = 32;    // tokens per CTA
-constexpr int kFeatThreads = 128;
+constexpr int kRun = 32;          // output tokens per CTA
+constexpr int kHist = 8;          // tokens before the run that are read for the conv history (7 used)
+constexpr int kReseed = 16;       // cos/sin re-formed from the tables every 16 positions
+constexpr int kFeatThreads = 256;
 
-// One CTA = 32 tokens x one head (q, k or v head, chosen by blockIdx.y).
+// Eight consecutive raw elements of one row, as loaded (16 B for bf16, 32 B for fp32).
+template <typename Tin> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    static constexpr int kWords = 4;
+    uint32_t w[4];
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+    __device__ __forceinline__ void unpack(float* x) const {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            x[2 * i] = f.x; x[2 * i + 1] = f.y;
+        }
+    }
+};
+template <> struct Raw8<float> {
+    static constexpr int kWords = 8;
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const float* p) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        w[0] = __float_as_uint(a.x); w[1] = __float_as_uint(a.y); w[2] = __float_as_uint(a.z); w[3] = __float_as_uint(a.w);
+        w[4] = __float_as_uint(b.x); w[5] = __float_as_uint(b.y); w[6] = __float_as_uint(b.z); w[7] = __float_as_uint(b.w);
+    }
+    __device__ __forceinline__ void unpack(float* x) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(w[i]);
+    }
+};
+
+__device__ __forceinline__ void store8(__half* p, const float* x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float* p, const float* x) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+}
+
+// One CTA = kRun tokens x HPC feature rows (q heads, then k heads, then v
+// heads).  D / 8 lanes cover one row, 8 channels each, and walk the tokens in
+// order in batches of 8 (every batch starts at a multiple of 8): the rotated
+// values of the last 8 tokens sit in a register ring indexed by token mod 8,
+// which serves as the conv history; RoPE's partner half (channel c +- D/2)
+// comes from lane xor D/16, and cos/sin advance by one position with a
+// rotation by theta_i, re-formed from the tables (angle addition, both
+// reduced in double precision) at every 16th position of a sequence and at
+// the CTA's first token.
 template <typename Tin, typename Tf, int D>
-__global__ void __launch_bounds__(kFeatThreads)
+__global__ void __launch_bounds__(kFeatThreads, 1)
 features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
                 const Tin* __restrict__ v, const float* __restrict__ wq,
                 const float* __restrict__ wk, const float* __restrict__ wv,
@@ -51,114 +106,135 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
                 const float2* __restrict__ coarse, Tf* __restrict__ qr, Tf* __restrict__ kr,
                 Tf* __restrict__ qhat, Tf* __restrict__ khat, Tf* __restrict__ vhat,
                 int32_t* __restrict__ err) {
-    constexpr int TT = kFeatTokens;
-    constexpr int ROWS = TT + kConvHalo;
-    constexpr int HALF = D / 2;
-    constexpr int RPT = TT * D / kFeatThreads;   // output rows per thread
-    constexpr int RSTEP = kFeatThreads / D;      // row stride between them
-    constexpr int WPR = D / 32;                  // warps covering one row
-    __shared__ float xs[ROWS][D];
-    __shared__ int rpos[ROWS];
-    __shared__ float red[TT][WPR];
-
-    const int tid = threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.x * TT;
-    int head = blockIdx.y;
+    constexpr int G8 = D / 8, HALF = D / 2, RPW = 32 / G8, HPC = (kFeatThreads / 32) * RPW;
+    constexpr bool kPrefetch = sizeof(Tin) == 2;  // bf16 rows of a batch are loaded up front
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cg = lane % G8, c0 = 8 * cg;
+    const int n_rows = L.Hq + 2 * L.Hkv;
+    int head = blockIdx.y * HPC + warp * RPW + lane / G8;
+    const bool active = head < n_rows;  // idle lanes still take part in the shuffles
+    if (!active) head = n_rows - 1;
     int kind = 0;  // 0 = q, 1 = k, 2 = v
     if (head >= L.Hq + L.Hkv) { kind = 2; head -= L.Hq + L.Hkv; }
     else if (head >= L.Hq) { kind = 1; head -= L.Hq; }
-    const int H = kind == 0 ? L.Hq : L.Hkv;
-    const Tin* src = kind == 0 ? q : (kind == 1 ? k : v);
-    const float* w = kind == 0 ? wq : (kind == 1 ? wk : wv);
+    const size_t row_stride = (size_t)(kind == 0 ? L.Hq : L.Hkv) * D;  // elements between tokens
+    const bool do_rot = kind != 2;
+    const bool do_norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));
+    const float sgn = c0 < HALF ? -1.f : 1.f;  // x1' = x1 c - x2 s,  x2' = x2 c + x1 s
+    const int f0 = c0 % HALF;
 
-    if (tid < ROWS) {
-        int64_t t = t0 - kConvHalo + tid;
-        int p = -1;
-        if (t >= 0 && t < L.total) {
-            int s = seq_of_token(cu, L.n_seqs, t);
-            int64_t start, len;
-            seq_range(cu, s, L.total, &start, &len);
-            if (t >= start && t < start + len) p = (int)(t - start);
-            else if (err && blockIdx.y == 0) atomicExch(err, kErrSeqlens);
-        }
-        rpos[tid] = p;
-    }
-    for (int idx = tid; idx < ROWS * D; idx += kFeatThreads) {
-        int r = idx / D, c = idx % D;
-        int64_t t = t0 - kConvHalo + r;
-        float x = 0.f;
-        if (t >= 0 && t < L.total) x = to_f32(src[((size_t)t * H + head) * D + c]);
-        xs[r][c] = x;
-    }
-    __syncthreads();
-
-    if (kind != 2) {
-        for (int idx = tid; idx < ROWS * HALF; idx += kFeatThreads) {
-            int r = idx / HALF, i = idx % HALF;
-            int p = rpos[r];
-            if (p < 0) continue;
-            float2 f = __ldg(fine + (p & 63) * HALF + i);
-            float2 g = __ldg(coarse + (p >> 6) * HALF + i);
-            float cs = g.x * f.x - g.y * f.y;
-            float sn = g.y * f.x + g.x * f.y;
-            float x1 = xs[r][i], x2 = xs[r][i + HALF];
-            xs[r][i] = x1 * cs - x2 * sn;
-            xs[r][i + HALF] = x2 * cs + x1 * sn;
-        }
-        __syncthreads();
-        Tf* rot = kind == 0 ? qr : kr;
-        for (int idx = tid; idx < TT * D; idx += kFeatThreads) {
-            int r = idx / D, c = idx % D;
-            int64_t t = t0 + r;
-            if (t < L.total) rot[((size_t)t * H + head) * D + c] = from_f32<Tf>(xs[r + kConvHalo][c]);
+    float wt[8][kConvWidth];
+    {
+        const float4* wp = reinterpret_cast<const float4*>((kind == 0 ? wq : (kind == 1 ? wk : wv)) +
+                                                           ((size_t)head * D + c0) * kConvWidth);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 a = __ldg(wp + 2 * j), b = __ldg(wp + 2 * j + 1);
+            wt[j][0] = a.x; wt[j][1] = a.y; wt[j][2] = a.z; wt[j][3] = a.w;
+            wt[j][4] = b.x; wt[j][5] = b.y; wt[j][6] = b.z; wt[j][7] = b.w;
         }
     }
+    float2 stp[8];  // (cos, sin) of theta_i
+#pragma unroll
+    for (int j = 0; j < 8; ++j) stp[j] = __ldg(fine + HALF + f0 + j);
 
-    // causal depthwise conv, zero history before the start of each sequence
-    const int c = tid % D;
-    const int r0 = tid / D;
-    float wr[kConvWidth];
-#pragma unroll
-    for (int m = 0; m < kConvWidth; ++m) wr[m] = __ldg(w + ((size_t)head * D + c) * kConvWidth + m);
-    float acc[RPT];
-#pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-        int r = r0 + j * RSTEP;
-        int p = rpos[r + kConvHalo];
-        float a = 0.f;
-#pragma unroll
-        for (int m = 0; m < kConvWidth; ++m)
-            if (p - kConvHalo + m >= 0) a = fmaf(wr[m], xs[r + m][c], a);
-        acc[j] = a;
-    }
+    const int64_t t_out = (int64_t)blockIdx.x * kRun;
+    const int64_t t_first = t_out - kHist > 0 ? t_out - kHist : 0;
+    const int64_t t_end = t_out + kRun < L.total ? t_out + kRun : L.total;
+    int s = seq_of_token(cu, L.n_seqs, t_first);
+    int64_t s_start, s_len;
+    seq_range(cu, s, L.total, &s_start, &s_len);
 
-    Tf* dst = kind == 0 ? qhat : (kind == 1 ? khat : vhat);
-    bool norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));
-    if (norm) {
-        const int lane = tid & 31;
-        const int wir = c / 32;  // which warp of the row this thread's channel sits in
+    const Tin* src = (kind == 0 ? q : (kind == 1 ? k : v)) + (size_t)head * D + c0;
+    Tf* rot_dst = (kind == 0 ? qr : kr) + (size_t)head * D + c0;
+    Tf* hat_dst = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + c0;
+
+    float ring[8][8];  // rotated rows of tokens t = 8 b + slot
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            float ss = acc[j] * acc[j];
+    for (int m = 0; m < 8; ++m)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) red[r0 + j * RSTEP][wir] = ss;
+        for (int j = 0; j < 8; ++j) ring[m][j] = 0.f;
+    float cs[8], sn[8];
+    bool seeded = false;
+
+#pragma unroll 1
+    for (int64_t tb = t_out - kHist; tb < t_end; tb += 8) {
+        Raw8<Tin> raw[8];
+        if (kPrefetch) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (tb + u >= t_first && tb + u < t_end) raw[u].load(src + (size_t)(tb + u) * row_stride);
         }
-        __syncthreads();
 #pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            int r = r0 + j * RSTEP;
+        for (int u = 0; u < 8; ++u) {
+            const int64_t t = tb + u;
+            if (t < t_first || t >= t_end) continue;  // same t across the CTA: uniform
+            if (!kPrefetch) raw[u].load(src + (size_t)t * row_stride);
+            while (t >= s_start + s_len && s + 1 < L.n_seqs) {
+                ++s;
+                seq_range(cu, s, L.total, &s_start, &s_len);
+            }
+            const bool in_seq = t >= s_start && t < s_start + s_len;
+            if (!in_seq && err && threadIdx.x == 0 && blockIdx.y == 0) atomicExch(err, kErrSeqlens);
+            const int pos = in_seq ? (int)(t - s_start) : 0;
+            if (pos == 0) {  // a sequence starts: zero conv history
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) ring[m][j] = 0.f;
+            }
+            if (!seeded || (pos & (kReseed - 1)) == 0) {
+                const float2* fp = fine + (pos & 63) * HALF + f0;
+                const float2* gp = coarse + (pos >> 6) * HALF + f0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float2 f = __ldg(fp + j), g = __ldg(gp + j);
+                    cs[j] = g.x * f.x - g.y * f.y;
+                    sn[j] = g.y * f.x + g.x * f.y;
+                }
+                seeded = true;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float c = cs[j] * stp[j].x - sn[j] * stp[j].y;
+                    sn[j] = sn[j] * stp[j].x + cs[j] * stp[j].y;
+                    cs[j] = c;
+                }
+            }
+            Raw8<Tin> partner;
+#pragma unroll
+            for (int i = 0; i < Raw8<Tin>::kWords; ++i) partner.w[i] = __shfl_xor_sync(0xffffffffu, raw[u].w[i], G8 / 2);
+            float x[8], xp[8];
+            raw[u].unpack(x);
+            partner.unpack(xp);
+            if (do_rot && in_seq) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = fmaf(x[j], cs[j], sgn * xp[j] * sn[j]);
+            }
+            const bool out_row = t >= t_out && active;
+            if (out_row && do_rot) store8(rot_dst + (size_t)t * row_stride, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ring[u][j] = in_seq ? x[j] : 0.f;
+            // causal depthwise conv: tap m multiplies token t - 7 + m, ring slot (u + 1 + m) mod 8
+            float y[8];
             float ss = 0.f;
 #pragma unroll
-            for (int u = 0; u < WPR; ++u) ss += red[r][u];
-            acc[j] *= rsqrtf(ss + 1e-6f);
-        }
-    }
+            for (int j = 0; j < 8; ++j) {
+                float a = 0.f;
 #pragma unroll
-    for (int j = 0; j < RPT; ++j) {
-        int r = r0 + j * RSTEP;
-        int64_t t = t0 + r;
-        if (t < L.total) dst[((size_t)t * H + head) * D + c] = from_f32<Tf>(acc[j]);
+                for (int m = 0; m < kConvWidth; ++m) a = fmaf(wt[j][m], ring[(u + 1 + m) & 7][j], a);
+                y[j] = a;
+                ss = fmaf(a, a, ss);
+            }
+#pragma unroll
+            for (int o = G8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (do_norm) {
+                const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] *= r;
+            }
+            if (out_row) store8(hat_dst + (size_t)t * row_stride, y);
+        }
     }
 }
 
@@ -167,7 +243,9 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float* wq, const float* wk, const float* wv, const int32_t* cu,
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st) {
-    dim3 grid((unsigned)((L.total + kFeatTokens - 1) / kFeatTokens), L.Hq + 2 * L.Hkv);
+    const int hpc = (kFeatThreads / 32) * (32 / (L.d / 8));
+    dim3 grid((unsigned)((L.total + kRun - 1) / kRun), (unsigned)((L.Hq + 2 * L.Hkv + hpc - 1) / hpc));
+    if (L.total <= 0) return cudaSuccess;
     if (L.d == 128)
         features_kernel<Tin, Tf, 128><<<grid, kFeatThreads, 0, st>>>(
             L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err);
