@@ -185,6 +185,9 @@ def source_hash(files) -> str:
 # prefill
 GDN_RECURRENT_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
                          "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+# stage boundaries recorded by the library, in launch order
+STAGES_CHUNKED = ("features", "softmax", "gdn_prep", "gdn_state")
+STAGES_SERIAL = ("features", "none", "gdn_state", "softmax")
 GDN_PREP_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_inverse.cu",
                     "linearized_attention_rope_gb300/csrc/umma.cuh",
                     "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
@@ -269,6 +272,7 @@ def run_prefill_bench(args, dist, peaks):
         step()
     torch.cuda.synchronize()
     n_stage = 5
+    chunked = wl.dtype == "bf16" and wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads in (1, 2, 4, 8)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
     for row in ev:  # materialise the event handles
         for e in row:
@@ -290,10 +294,11 @@ def run_prefill_bench(args, dist, peaks):
     dist.barrier()
     step_ms = [ev[i][0].elapsed_time(ends[i]) for i in range(args.steps)]
     stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-                for j, name in enumerate(("features", "gdn_prep", "gdn_state", "softmax"))}
+                for j, name in enumerate(STAGES_CHUNKED if chunked else STAGES_SERIAL)}
     device_s = dist.max(sum(step_ms) / 1e3)
-    # rope tables, features, gdn (chunk table + inverse + state kernel when chunked), softmax
-    launches_per_step = 6 if (wl.dtype == "bf16" and wl.head_dim == 128) else 4
+    # rope tables, features, then block table + softmax, chunk table + chunk kernel, state kernel
+    # (tensor-core path) or GDN + softmax (token-serial path)
+    launches_per_step = 7 if chunked else 4
 
     work = prefill_work(wl)
 

@@ -31,8 +31,9 @@
 // of the record) and starts its D1 with the S-independent [T diag(beta) ; 0] V;
 // warps 0-3 run the chain: D1 += [-Wm ; Q] S0, the U epilogue, DS and then
 // D2 (whose issue hides under DS's latency), the S epilogue; warps 6-7 turn
-// the double-buffered D1/D2 rows 64..127 into o_lin rows
-// (o = gamma Q S0 + P U).  Handoffs use mbarriers: loaded[b] (TMA bytes),
+// the double-buffered D1/D2 rows 64..127 into the layer output of their
+// positions: out = o_sm + lambda_h (gamma Q S0 + P U), o_sm being the
+// normalised softmax branch the softmax kernel left for these rows.  Handoffs use mbarriers: loaded[b] (TMA bytes),
 // ready[b] (the V MMAs -> chain), free[b] (chain + output -> load), ofull[b]
 // (MMA -> output).  Token rows past a chunk's end hold whatever follows
 // (zeros past the tensor): they meet zero rows of -Wm, T diag(beta) and U,
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ cu,
                    const int32_t* __restrict__ chunk_base, const unsigned char* __restrict__ rec_in,
-                   float* __restrict__ o_lin, float* __restrict__ S_out, int32_t* __restrict__ err) {
+                   const __half* __restrict__ o_sm, const float* __restrict__ lambda,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ S_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
@@ -291,16 +293,18 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             umma::commit(bar(kReady + b));
         }
     } else if (warp >= 6) {
-        // ================= o_lin rows: gamma (Q S0) + P U =================
+        // ================= output rows: o_sm + lambda_h (gamma (Q S0) + P U) =================
         const int r = tid - 192;  // chunk row; TMEM lane 64 + r
+        const bool emit = out && !(L.flags & HLA_FLAG_LINEAR_OFF);
+        const float lam = __ldg(lambda + h);
 #pragma unroll 1
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
             if (!role_wait(kOFull + b, (uint32_t)((c >> 1) & 1), 3, 64, r == 0)) break;
-            const float gr = reinterpret_cast<const float*>(sm + b * kBuf + kVec)[r];
+            const float gr = reinterpret_cast<const float*>(sm + b * kBuf + kVec)[r] * lam;
             const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-            const bool row_on = r < j_end - j0;
-            float* orow = o_lin + ((size_t)(start + j0 + (row_on ? r : 0) + W) * L.Hq + h) * kD + slice * kNS;
+            const bool row_on = emit && r < j_end - j0;
+            const size_t base = ((size_t)(start + j0 + (row_on ? r : 0) + W) * L.Hq + h) * kD + slice * kNS;
 #pragma unroll 1
             for (int q = 0; q < 2; ++q) {
                 float d1[32], d2[32];
@@ -308,10 +312,20 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                 umma::tmem_ld32(tmem + lane_base + kColD2 + kNS * b + 32 * q, d2);
                 if (row_on) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(orow + 32 * q + i) =
-                            make_float4(fmaf(gr, d1[i], d2[i]), fmaf(gr, d1[i + 1], d2[i + 1]),
-                                        fmaf(gr, d1[i + 2], d2[i + 2]), fmaf(gr, d1[i + 3], d2[i + 3]));
+                    for (int i = 0; i < 32; i += 8) {
+                        const uint4 sv = *reinterpret_cast<const uint4*>(o_sm + base + 32 * q + i);
+                        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+                        uint32_t ow[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[e]));
+                            const int k = i + 2 * e;
+                            const __nv_bfloat162 o2 = __floats2bfloat162_rn(fmaf(gr, d1[k], fmaf(lam, d2[k], f.x)),
+                                                                            fmaf(gr, d1[k + 1], fmaf(lam, d2[k + 1], f.y)));
+                            ow[e] = *reinterpret_cast<const uint32_t*>(&o2);
+                        }
+                        *reinterpret_cast<uint4*>(out + base + 32 * q + i) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                    }
                 }
             }
             umma::fence_before_sync();
@@ -329,7 +343,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
-                               float* o_lin, float* S_out, int32_t* err, cudaStream_t st) {
+                               const __half* o_sm, const float* lambda, __nv_bfloat16* out, float* S_out,
+                               int32_t* err, cudaStream_t st) {
     static bool configured = false;  // the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -345,7 +360,8 @@ cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __h
         !tma::make_map_f16_3d(&mv, vhat, kD, (uint64_t)L.Hkv, (uint64_t)L.total))
         return cudaErrorInvalidValue;
     dim3 grid(L.Hq * kSlices, L.n_seqs);
-    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, rec_in, o_lin, S_out, err);
+    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, rec_in, o_sm, lambda, out,
+                                                          S_out, err);
     return cudaGetLastError();
 }
 

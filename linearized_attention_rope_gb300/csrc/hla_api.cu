@@ -51,13 +51,16 @@ size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
 
 // Workspace layout of one prefill.
 struct WsLayout {
-    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, chunk_base, tinv, total;
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, osm, blk_base, chunk_base, tinv, total;
     int n_coarse;
 };
 
-// The tensor-core chunked GDN serves bf16 layers with head_dim 128.
+// The tensor-core path (chunked GDN + tensor-core softmax) serves bf16 layers
+// with head_dim 128 and 1, 2, 4 or 8 query heads per kv head.
 bool uses_chunked_gdn(const hla_params* prm) {
-    return prm->dtype == HLA_DTYPE_BF16 && prm->head_dim == 128 && !(prm->flags & HLA_FLAG_GDN_RECURRENT);
+    const int G = prm->n_kv_heads > 0 ? prm->n_q_heads / prm->n_kv_heads : 0;
+    return prm->dtype == HLA_DTYPE_BF16 && prm->head_dim == 128 && !(prm->flags & HLA_FLAG_GDN_RECURRENT) &&
+           (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
 WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
@@ -74,8 +77,11 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     w.qhat = off;   off = align_up(off + T * Hq * d * fb);
     w.khat = off;   off = align_up(off + T * Hkv * d * fb);
     w.vhat = off;   off = align_up(off + T * Hkv * d * fb);
-    w.olin = off;   off = align_up(off + T * Hq * d * sizeof(float));
     const bool chunked = uses_chunked_gdn(prm);
+    // token-serial path: fp32 o_lin; chunked path: fp16 softmax rows for the GDN kernel to finish
+    w.olin = off;   off = align_up(off + (chunked ? 0 : T * Hq * d * sizeof(float)));
+    w.osm = off;    off = align_up(off + (chunked ? T * Hq * d * sizeof(__half) : 0));
+    w.blk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
     w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
     w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
     w.total = off;
@@ -128,25 +134,24 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     bool chunked = false;
     if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
     if (chunked) {
+        // features -> softmax (final rows, fp16 rows to finish) -> chunk-local GDN -> GDN state + combine
         if constexpr (std::is_same<Tf, __half>::value) {
+            __half* osm = reinterpret_cast<__half*>(ws + w.osm);
+            int32_t* blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
             int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, stream));
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+            HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, olin, S_out, err, stream));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, stream));
+            HLA_TRY(mark_stage(3, stream));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, osm, lambda, o, S_out, err, stream));
         }
     } else {
+        // features -> GDN (fp32 o_lin) -> softmax + combine
         HLA_TRY(mark_stage(2, stream));
         HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
-    }
-    HLA_TRY(mark_stage(3, stream));
-    bool softmax_tc = false;
-    if constexpr (std::is_same<Tf, __half>::value) softmax_tc = window_softmax_tc_supported(L);
-    if (softmax_tc) {
-        if constexpr (std::is_same<Tf, __half>::value)
-            HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out), err,
-                                             stream));
-    } else {
+        HLA_TRY(mark_stage(3, stream));
         HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
                                                stream));
     }

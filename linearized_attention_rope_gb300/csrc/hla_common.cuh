@@ -138,9 +138,12 @@ size_t gdn_chunk_slots(int64_t total, int n_seqs);
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
                                const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
                                int32_t* err, cudaStream_t st);
+// out rows of positions >= n_sinks + W: bf16(o_sm + lambda_h o_lin) (none if
+// out is null or the linear branch is switched off).
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
-                               float* o_lin, float* S_out, int32_t* err, cudaStream_t st);
+                               const __half* o_sm, const float* lambda, __nv_bfloat16* out, float* S_out,
+                               int32_t* err, cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>
@@ -149,10 +152,15 @@ cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr
                                   Tin* out, cudaStream_t st);
 
 // Sink + window softmax on tcgen05 (bf16 layer, head_dim 128, G in {1,2,4,8}).
+// Tensor-core sink + window softmax (head_dim 128, G in {1, 2, 4, 8}; bf16
+// values).  Rows of positions >= n_sinks + W (unless the linear branch is
+// off) get the normalised softmax output in o_sm (fp16) for the GDN kernel to
+// finish; all other rows are written to out.  blk_base: n_seqs + 1 int32 of
+// workspace (per-sequence block table).
 bool window_softmax_tc_supported(const LayerDims& L);
-cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr,
-                                     const __nv_bfloat16* v, const float* o_lin, const float* lambda,
-                                     const int32_t* cu, __nv_bfloat16* out, int32_t* err, cudaStream_t st);
+cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
+                                     const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
+                                     int32_t* err, cudaStream_t st);
 
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>

@@ -17,9 +17,15 @@
 namespace hla {
 namespace tma {
 
-// Host: a 3-D fp16 map over [n2][n1][n0] with a (64, 1, 64) box and 128-byte
-// swizzle.  Returns false if the driver rejects it.
-bool make_map_f16_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2);
+// Host: a 3-D 16-bit map (fp16, or bf16 if `bf16`) over [n2][n1][n0] with
+// box (b0, b1, b2), b0 * 2 <= 128 bytes, and 128-byte swizzle.  Returns false
+// if the driver rejects it.
+bool make_map_3d(CUtensorMap* map, const void* base, bool bf16, uint64_t n0, uint64_t n1, uint64_t n2, uint32_t b0,
+                 uint32_t b1, uint32_t b2);
+// The (64, 1, 64) fp16 box used for chunks of 64 token rows.
+inline bool make_map_f16_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2) {
+    return make_map_3d(map, base, false, n0, n1, n2, 64, 1, 64);
+}
 
 __device__ __forceinline__ void expect_tx(uint32_t mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");

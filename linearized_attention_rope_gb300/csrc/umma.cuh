@@ -63,6 +63,11 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool a_mn, 
     return d;
 }
 
+// Same with bf16 A and B.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_f16(M, N, a_mn, b_mn, false) | (1u << 7) | (1u << 10);
+}
+
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -95,14 +100,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for phase `parity` of the mbarrier; gives up after `limit` polls
-// (each poll may itself suspend for a while) and returns false.  Kept out of
-// line with a rolled loop: an unrolled copy at every call site bloats the
-// kernels well past the instruction cache.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for phase `parity` of the mbarrier; gives up and returns false after
+// `limit` polls or two seconds of wall-clock time, whichever comes first (a
+// single poll may suspend the thread for a while).  Kept out of line with a
+// rolled loop: an unrolled copy at every call site bloats the kernels well
+// past the instruction cache.
 static __device__ __noinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+    const uint64_t t0 = global_ns();
 #pragma unroll 1
-    for (uint32_t i = 0; i < limit; ++i)
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(mbar, parity)) return true;
+        if (global_ns() - t0 > 2000000000ull) return false;
+    }
     return false;
 }
 
@@ -142,6 +157,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Stores 32 consecutive fp32 columns of this thread's TMEM lane and waits

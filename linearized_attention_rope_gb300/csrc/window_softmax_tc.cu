@@ -1,22 +1,32 @@
 // Exact branch on the tcgen05 tensor cores: softmax over the sink tokens plus
 // the sliding window ("迈向线性的关键：分析驱动的 Transformer 线性化", section
 // 填补近似缺口的实用设计; scale 1/sqrt(d) from Lemma 1 of section
-// 从 softmax 到 delta 规则的一阶近似), with the lambda-weighted linear branch
-// added in the epilogue ("Untangling Component Imbalance in Hybrid Linear
-// Attention Conversion", section 关键设计 (1)).
+// 从 softmax 到 delta 规则的一阶近似).  The lambda-weighted linear branch
+// ("Untangling Component Imbalance in Hybrid Linear Attention Conversion",
+// section 关键设计 (1)) is added afterwards by the GDN state kernel: rows that
+// have a linear term (position >= n_sinks + W) leave here as the normalised
+// softmax output in fp16 (o_sm); every other row is final and goes to `out`.
 //
-// One CTA of 256 threads per (kv head, block of QB = 256 / G query positions):
-// the G query heads of the kv group are stacked into 256 rows, two M = 128
-// halves.  The keys a block can see are gathered as [sinks | window span]
-// into groups of 128 key slots; per group:
-//   D_S[half] = Q_half K^T            (tcgen05, fp16 operands, fp32 in TMEM)
-//   masked softmax, one thread per row, P (fp16) -> shared memory
-//   D_O[half] (+)= P_half V           (tcgen05)
-// with a running max and sum per row; when a block needs more than one group
-// the accumulated output is rescaled in TMEM before the next P V.  For the
-// 8 + 56 budget every block's keys fit one group.  A block that straddles a
-// sequence boundary is processed one sequence segment at a time.
+// Work item = (kv head, block of QB = 128 / G query positions inside one
+// sequence); the G query heads of the kv group and the QB positions form the
+// 128 rows of one M = 128 tile (row = position * G + head, the order a TMA box
+// (64, G, QB) of the [tokens][heads][128] feature tensor lands in).  The keys
+// the block can see are gathered as key slots [sinks (padded to 8) | window
+// span] in TMA boxes (64 rows for aligned runs of window slots, else 8) and
+// processed in groups of up to 128 slots:
+//   D_S = Q K^T                       (fp16 operands, fp32 in TMEM)
+//   online softmax, two threads per row (one per half of the group's slots),
+//   P (bf16) over the key tile, which the MMA above has finished with
+//   D_O (+)= P V                      (bf16 operands; V straight from the input)
+// with the running max and sum per row, rescaling D_O in TMEM between groups.
+// Slots past the visible keys hold whatever rows follow (zeros past the
+// tensor's end) and are masked.  Persistent CTAs (two per SM: 96 KB of shared
+// memory, 256 TMEM columns each) walk the items; every wait is bounded and
+// reports a timeout in the error word.
+#include <algorithm>
+
 #include "hla_common.cuh"
+#include "tma.cuh"
 #include "umma.cuh"
 
 namespace hla {
@@ -24,75 +34,65 @@ namespace hla {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRows = 256;
 constexpr int kThreads = 256;
-constexpr int kKeys = 128;  // key slots per group
+constexpr int kGroup = 128;  // key slots per group
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-constexpr uint32_t kQ = 0;          // two halves, 128 x 128 fp16 K-major each
-constexpr uint32_t kK = 65536;      // 128 keys x 128 fp16 K-major
-constexpr uint32_t kV = 98304;      // 128 keys x 128 fp16 MN-major
-constexpr uint32_t kP = 131072;     // two halves, 128 rows x 128 keys fp16 K-major
-constexpr uint32_t kMisc = 196608;  // mbarrier, TMEM slot
-constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;
+constexpr uint32_t kQ = 0;        // 128 rows x 128 fp16, K-major (two 16 KB column blocks)
+constexpr uint32_t kK = 32768;    // group keys kGroup x 128 fp16 K-major; then P, 128 rows x kGroup bf16 K-major
+constexpr uint32_t kV = 65536;    // group values kGroup x 128 bf16 (MN-major B)
+constexpr uint32_t kRed = 98304;  // per-row partial max / sum of the two column halves: [2][2][128] fp32
+constexpr uint32_t kBar = kRed + 2048;
+constexpr uint32_t kSmemAlloc = kBar + 64 + 1024;
+constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
 
-constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
-
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-        o[i] = pack_h2(f.x, f.y);
+
+__global__ void block_table_kernel(LayerDims L, int QB, const int32_t* __restrict__ cu, int32_t* __restrict__ base) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int32_t acc = 0;
+    for (int s = 0; s < L.n_seqs; ++s) {
+        base[s] = acc;
+        int64_t start, len;
+        seq_range(cu, s, L.total, &start, &len);
+        acc += (int32_t)((len + QB - 1) / QB);
     }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    base[L.n_seqs] = acc;
 }
 
-// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills zeros.
-__device__ __forceinline__ void cp_async16(unsigned char* dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_addr(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
-}
-
-// Key position held by key slot i of a segment: the sinks first, then the window span.
-__device__ __forceinline__ int64_t key_at(int64_t i, int64_t n_sink, int64_t span_lo, int64_t n_keys) {
-    if (i >= n_keys) return -1;
-    return i < n_sink ? i : span_lo + (i - n_sink);
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
-window_softmax_tc_kernel(LayerDims L, const __half* __restrict__ qr, const __half* __restrict__ kr,
-                         const __nv_bfloat16* __restrict__ v, const float* __restrict__ o_lin,
-                         const float* __restrict__ lambda, const int32_t* __restrict__ cu,
-                         __nv_bfloat16* __restrict__ out, int32_t* __restrict__ err) {
+__global__ void __launch_bounds__(kThreads, 2)
+window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_k64, const __grid_constant__ CUtensorMap map_v64,
+                         const int32_t* __restrict__ cu, const int32_t* __restrict__ blk_base,
+                         __half* __restrict__ o_sm, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
+    float* red = reinterpret_cast<float*>(sm + kRed);  // [0: max | 1: sum][column half][row]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 16);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, half = warp >> 2;
-    const int Lr = ((warp & 3) << 5) + lane;
-    const int row = half * 128 + Lr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = ((warp & 3) << 5) + lane, chalf = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const int G = L.G, QB = kRows / G;
-    const int kv = blockIdx.y;
-    const int g = row / QB, qi = row % QB, h = kv * G + g;
-    const int64_t t0 = (int64_t)blockIdx.x * QB;
+    const int G = L.G, QB = kD / G;
+    const int qi = row / G, gq = row % G;
     const uint32_t sbase = umma::smem_addr(sm);
-    const uint32_t mbar = umma::smem_addr(mbar_p);
+    const uint32_t bar_ld = umma::smem_addr(sm + kBar), bar_mma = bar_ld + 8;
     const float qscale = 0.088388347648318447f * 1.4426950408889634f;  // 1/sqrt(128) * log2(e)
+    const int64_t n_blocks = __ldg(blk_base + L.n_seqs);
+    const int64_t n_items = n_blocks * L.Hkv;
+    if ((int64_t)blockIdx.x >= n_items) return;  // whole CTA leaves together
 
     if (tid == 0) {
-        umma::mbar_init(mbar, 1);
+        umma::mbar_init(bar_ld, 1);
+        umma::mbar_init(bar_mma, 1);
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
@@ -100,205 +100,189 @@ window_softmax_tc_kernel(LayerDims L, const __half* __restrict__ qr, const __hal
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t srow = tmem + lane_base + kColS + 128 * half;
-    const uint32_t orow = tmem + lane_base + kColO + 128 * half;
-    uint32_t phase = 0;
-    bool ok = true;
+    uint32_t ph_ld = 0, ph_mma = 0;
 
-    auto wait_mma = [&]() {
-        bool done = umma::mbar_wait(mbar, phase, kWaitLimit);
-        phase ^= 1u;
-        if (!done && err) atomicExch(err, kErrTimeout);
+    // tid 0 waits with a bound; the CTA then agrees on the outcome
+    auto cta_wait = [&](uint32_t mbar, uint32_t& ph) -> bool {
+        bool w = true;
+        if (tid == 0) {
+            w = umma::mbar_try_wait(mbar, ph) || umma::mbar_wait(mbar, ph, kWaitLimit);
+            if (!w && err) atomicExch(err, kErrTimeout);
+        }
+        ph ^= 1u;
+        const bool ok = __syncthreads_and(w);
         umma::fence_after_sync();
-        return __syncthreads_or(!done) == 0;
+        return ok;
     };
 
-    const int64_t t_end = min(t0 + QB, L.total);
-    int64_t ta = t0;
-    while (ta < t_end && ok) {
-        // ---- the part of this block that lies in one sequence
-        const int s = seq_of_token(cu, L.n_seqs, ta);
+    const bool sm_on = !(L.flags & HLA_FLAG_SOFTMAX_OFF), lin_off = (L.flags & HLA_FLAG_LINEAR_OFF) != 0;
+    bool ok = true;
+#pragma unroll 1
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int kv = (int)(item / n_blocks);
+        const int blk = (int)(item % n_blocks);
+        int lo = 0, hi = L.n_seqs - 1;  // sequence owning the block
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(blk_base + mid) <= blk) lo = mid; else hi = mid - 1;
+        }
         int64_t start, len;
-        seq_range(cu, s, L.total, &start, &len);
-        if (ta < start || ta >= start + len) break;  // malformed table: flagged by the feature pass
-        const int64_t tb = min(t_end, start + len);
-        const int64_t pa = ta - start, pb = tb - start;  // query positions [pa, pb)
+        seq_range(cu, lo, L.total, &start, &len);
+        const int64_t pa = (int64_t)(blk - __ldg(blk_base + lo)) * QB, pb = min(len, pa + QB);
         const int64_t n_sink = min((int64_t)L.n_sinks, pb);
+        const int sink_pad = (int)((n_sink + 7) & ~7);
         const int64_t span_lo = max((int64_t)L.n_sinks, pa - L.window + 1);
         const int64_t n_span = pb > span_lo ? pb - span_lo : 0;
-        const int64_t n_keys = n_sink + n_span;
-        const int n_groups = (int)((n_keys + kKeys - 1) / kKeys);
+        const int n_slots = (int)((sink_pad + n_span + 15) & ~15);
+        const int n_groups = (n_slots + kGroup - 1) / kGroup;
 
-        // this thread's row: query position p (valid when row_on); the key slots
-        // it sees form two ranges, [0, hi1) (sinks) and [lo2, hi2) (window)
-        const int64_t t_row = t0 + qi;
-        const bool row_on = t_row >= ta && t_row < tb;
-        const int64_t p = row_on ? t_row - start : -1;
+        // this row's query position and its visible key slots [0, hi1) and [lo2, hi2)
+        const int64_t p = pa + qi;
+        const bool row_on = p < pb;
         int hi1 = 0, lo2 = 0, hi2 = 0;
         if (row_on) {
             hi1 = (int)min(n_sink, p + 1);
-            lo2 = (int)(n_sink + max((int64_t)0, p - L.window + 1 - span_lo));
-            hi2 = (int)(p >= span_lo ? n_sink + (p - span_lo) + 1 : lo2);
-        }
-
-        // ---- Q rows of the block (zero outside the segment), streamed with cp.async
-#pragma unroll
-        for (int u = 0; u < kRows * 16 / kThreads; ++u) {
-            const int e = tid + kThreads * u, r = e >> 4, cc = (e & 15) * 8;
-            const int rg = r / QB, rq = r % QB;
-            const int64_t t = t0 + rq;
-            const bool in = t >= ta && t < tb;
-            cp_async16(sm + kQ + (r >> 7) * 32768 + umma::sw128_offset(r & 127, cc, 128),
-                       qr + ((size_t)(in ? t : ta) * L.Hq + kv * G + rg) * kD + cc, in ? 16u : 0u);
+            lo2 = sink_pad + (int)max((int64_t)0, p - L.window + 1 - span_lo);
+            hi2 = p >= span_lo ? sink_pad + (int)(p - span_lo) + 1 : lo2;
         }
 
         float m_run = -INFINITY, l_run = 0.f;
-        for (int grp = 0; grp < n_groups; ++grp) {
-            // ---- K (fp16) and V (bf16 -> fp16) rows of the group's key slots
-#pragma unroll
-            for (int u = 0; u < kKeys * 16 / kThreads; ++u) {
-                const int e = tid + kThreads * u, slot = e >> 4, cc = (e & 15) * 8;
-                const int64_t j = key_at((int64_t)grp * kKeys + slot, n_sink, span_lo, n_keys);
-                const size_t rowi = ((size_t)(start + (j >= 0 ? j : 0)) * L.Hkv + kv) * kD + cc;
-                const uint32_t off = umma::sw128_offset(slot, cc, 128);
-                cp_async16(sm + kK + off, kr + rowi, j >= 0 ? 16u : 0u);
-                cp_async16(sm + kV + off, v + rowi, j >= 0 ? 16u : 0u);
-            }
-            cp_async_wait_all();  // (Q rows too, on the first group)
-            // values arrive as bf16; the MMA takes fp16 for both operands
-#pragma unroll
-            for (int u = 0; u < kKeys * 16 / kThreads; ++u) {
-                const int e = tid + kThreads * u, slot = e >> 4, cc = (e & 15) * 8;
-                uint4* pv = reinterpret_cast<uint4*>(sm + kV + umma::sw128_offset(slot, cc, 128));
-                *pv = bf16x8_to_f16x8(*pv);
-            }
-            umma::fence_async_smem();
-            umma::fence_before_sync();
-            __syncthreads();
-
-            // ---- D_S = Q K^T for both halves
+        for (int grp = 0; grp < n_groups && ok; ++grp) {
+            const int g0 = grp * kGroup, n = min(kGroup, n_slots - g0);  // a multiple of 16
+            // ---- loads: the query tile with the first group, then this group's keys and values
             if (tid == 0) {
-                umma::fence_after_sync();
-                const uint32_t id = umma::idesc_f16(128, kKeys, false, false, false);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int s16 = 0; s16 < kD / 16; ++s16)
-                        umma::mma(tmem + kColS + 128 * hh, umma::kmajor(sbase + kQ + 32768 * hh, 128, s16),
-                                  umma::kmajor(sbase + kK, 128, s16), id, s16 > 0);
-                umma::commit(mbar);
+                const uint32_t bytes = (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u;
+                tma::expect_tx(bar_ld, bytes);
+                if (grp == 0) {
+                    const int tq = (int)(start + pa);
+                    tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
+                    tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
+                }
+                for (int j = 0; j < n;) {
+                    const int slot = g0 + j;
+                    const int tk = (int)(start + (slot < sink_pad ? slot : span_lo + (slot - sink_pad)));
+                    const uint32_t off = (uint32_t)j * 128u;
+                    const bool wide = slot >= sink_pad && (j & 63) == 0 && j + 64 <= n;  // 64 window rows
+                    const CUtensorMap* mk = wide ? &map_k64 : &map_k;
+                    const CUtensorMap* mv = wide ? &map_v64 : &map_v;
+                    tma::tensor_load_3d(sbase + kK + off, mk, 0, kv, tk, bar_ld);
+                    tma::tensor_load_3d(sbase + kK + 16384 + off, mk, 64, kv, tk, bar_ld);
+                    tma::tensor_load_3d(sbase + kV + off, mv, 0, kv, tk, bar_ld);
+                    tma::tensor_load_3d(sbase + kV + 16384 + off, mv, 64, kv, tk, bar_ld);
+                    j += wide ? 64 : 8;
+                }
             }
-            if (!(ok = wait_mma())) break;
+            if (!(ok = cta_wait(bar_ld, ph_ld))) break;
 
-            // ---- masked softmax of this row (two passes over TMEM, 32 columns at a time)
+            // ---- D_S = Q K^T (N = n)
+            if (tid == 0) {
+                const uint32_t id = umma::idesc_f16(128, n, false, false, false);
+                const uint64_t a0 = umma::kmajor(sbase + kQ, 128, 0), b0 = umma::kmajor(sbase + kK, kGroup, 0);
+#pragma unroll
+                for (int s = 0; s < kD / 16; ++s) {
+                    const uint64_t ks = (uint64_t)((s >> 2) * 1024 + (s & 3) * 2);  // 16 KB per block, 32 B per step
+                    umma::mma(tmem + kColS, a0 + ks, b0 + ks, id, s > 0);
+                }
+                umma::commit(bar_mma);
+            }
+            if (!(ok = cta_wait(bar_mma, ph_mma))) break;
+
+            // ---- online softmax: this thread covers slots [c_lo, c_hi) of the group
+            const int c_lo = chalf * 64, c_hi = min(n, c_lo + 64);
             float mg = -INFINITY;
+            for (int c = c_lo; c < c_hi; c += 16) {
+                float sc[16];
+                umma::tmem_ld16(tmem + lane_base + kColS + c, sc);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float sc[32];
-                umma::tmem_ld32(srow + 32 * q4, sc);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int gi = grp * kKeys + 32 * q4 + i;
+                for (int i = 0; i < 16; ++i) {
+                    const int gi = g0 + c + i;
                     if (gi < hi1 || (gi >= lo2 && gi < hi2)) mg = fmaxf(mg, sc[i] * qscale);
                 }
             }
-            const float m_new = fmaxf(m_run, mg);
-            const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            red[chalf * 128 + row] = mg;
+            __syncthreads();
+            const float m_new = fmaxf(m_run, fmaxf(red[row], red[128 + row]));
+            const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
             float lsum = 0.f;
+            for (int c = c_lo; c < c_hi; c += 16) {
+                float sc[16];
+                umma::tmem_ld16(tmem + lane_base + kColS + c, sc);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float sc[32];
-                umma::tmem_ld32(srow + 32 * q4, sc);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int gi = grp * kKeys + 32 * q4 + i;
+                for (int i = 0; i < 16; ++i) {
+                    const int gi = g0 + c + i;
                     const bool vis = gi < hi1 || (gi >= lo2 && gi < hi2);
                     sc[i] = vis ? exp2f(sc[i] * qscale - m_new) : 0.f;
                     lsum += sc[i];
                 }
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    const float* x = sc + 8 * c8;
-                    const uint4 pk = make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]),
-                                                pack_h2(x[6], x[7]));
-                    *reinterpret_cast<uint4*>(sm + kP + 32768 * half +
-                                              umma::sw128_offset(Lr, 32 * q4 + 8 * c8, 128)) = pk;
+                for (int h8 = 0; h8 < 2; ++h8) {  // P over the key tile: K-major, slots = K
+                    const float* x = sc + 8 * h8;
+                    *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(row, c + 8 * h8, 128)) =
+                        make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
+                                   pack_bf2(x[6], x[7]));
                 }
             }
-            l_run = l_run * corr + lsum;
-            m_run = m_new;
-            if (grp > 0) {  // rescale the output accumulated over the earlier groups
+            red[256 + chalf * 128 + row] = lsum;
+            if (grp > 0) {  // rescale this thread's half of the accumulated output (warp-uniform: TMEM access is collective)
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q = 0; q < 2; ++q) {
                     float o[32];
-                    umma::tmem_ld32(orow + 32 * q4, o);
+                    const uint32_t ta = tmem + lane_base + kColO + chalf * 64 + 32 * q;
+                    umma::tmem_ld32(ta, o);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] *= corr;
-                    umma::tmem_st32(orow + 32 * q4, o);
+                    for (int i = 0; i < 32; ++i) o[i] *= corr;
+                    umma::tmem_st32(ta, o);
                 }
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
             __syncthreads();
+            l_run = l_run * corr + red[256 + row] + red[256 + 128 + row];
+            m_run = m_new;
 
-            // ---- D_O (+)= P V for both halves
+            // ---- D_O (+)= P V (K = n)
             if (tid == 0) {
                 umma::fence_after_sync();
-                const uint32_t id = umma::idesc_f16(128, kD, false, true, false);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int s16 = 0; s16 < kKeys / 16; ++s16)
-                        umma::mma(tmem + kColO + 128 * hh, umma::kmajor(sbase + kP + 32768 * hh, 128, s16),
-                                  umma::mnmajor(sbase + kV, 16384, s16), id, grp > 0 || s16 > 0);
-                umma::commit(mbar);
+                const uint32_t id = umma::idesc_bf16(128, kD, false, true);
+                const uint64_t a0 = umma::kmajor(sbase + kK, 128, 0), b0 = umma::mnmajor(sbase + kV, 16384u, 0);
+                for (int s = 0; s < n / 16; ++s)
+                    umma::mma(tmem + kColO, a0 + (uint64_t)((s >> 2) * 1024 + (s & 3) * 2), b0 + (uint64_t)(s * 128),
+                              id, grp > 0 || s > 0);
+                umma::commit(bar_mma);
             }
-            if (!(ok = wait_mma())) break;
+            if (!(ok = cta_wait(bar_mma, ph_mma))) break;
         }
         if (!ok) break;
 
-        // ---- epilogue: o = o_sm + lambda_h o_lin for the rows of this segment
+        // ---- epilogue: this thread's 64 output columns of its row
         {
-            const bool sm_on = !(L.flags & HLA_FLAG_SOFTMAX_OFF);
-            const bool lin_on = row_on && !(L.flags & HLA_FLAG_LINEAR_OFF) && (p - L.window >= L.n_sinks);
-            const float inv_l = (sm_on && row_on) ? 1.f / l_run : 0.f;
-            const float lam = lin_on ? __ldg(lambda + h) : 0.f;
-            const size_t base = ((size_t)(row_on ? t_row : 0) * L.Hq + h) * kD;
+            const float inv_l = (sm_on && row_on && l_run > 0.f) ? 1.f / l_run : 0.f;
+            const bool lin_row = !lin_off && p >= (int64_t)L.n_sinks + L.window;
+            const size_t base = ((size_t)(start + (row_on ? p : 0)) * L.Hq + kv * G + gq) * kD + chalf * 64;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q = 0; q < 2; ++q) {
                 float o[32];
-                umma::tmem_ld32(orow + 32 * q4, o);  // every warp loads; rows outside the segment drop it
+                umma::tmem_ld32(tmem + lane_base + kColO + chalf * 64 + 32 * q, o);
                 if (!row_on) continue;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
-                    float r8[8];
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) r8[x] = o[8 * c8 + x] * inv_l;
-                    const int col = 32 * q4 + 8 * c8;
-                    if (lin_on) {
-                        const float4 a = *reinterpret_cast<const float4*>(o_lin + base + col);
-                        const float4 b = *reinterpret_cast<const float4*>(o_lin + base + col + 4);
-                        r8[0] = fmaf(lam, a.x, r8[0]); r8[1] = fmaf(lam, a.y, r8[1]);
-                        r8[2] = fmaf(lam, a.z, r8[2]); r8[3] = fmaf(lam, a.w, r8[3]);
-                        r8[4] = fmaf(lam, b.x, r8[4]); r8[5] = fmaf(lam, b.y, r8[5]);
-                        r8[6] = fmaf(lam, b.z, r8[6]); r8[7] = fmaf(lam, b.w, r8[7]);
-                    }
-                    uint32_t w[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        __nv_bfloat162 bb = __floats2bfloat162_rn(r8[2 * x], r8[2 * x + 1]);
-                        w[x] = *reinterpret_cast<uint32_t*>(&bb);
-                    }
-                    *reinterpret_cast<uint4*>(out + base + col) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const float* x = o + 8 * c8;
+                    const int col = 32 * q + 8 * c8;
+                    if (lin_row)
+                        *reinterpret_cast<uint4*>(o_sm + base + col) =
+                            make_uint4(pack_h2(x[0] * inv_l, x[1] * inv_l), pack_h2(x[2] * inv_l, x[3] * inv_l),
+                                       pack_h2(x[4] * inv_l, x[5] * inv_l), pack_h2(x[6] * inv_l, x[7] * inv_l));
+                    else
+                        *reinterpret_cast<uint4*>(out + base + col) =
+                            make_uint4(pack_bf2(x[0] * inv_l, x[1] * inv_l), pack_bf2(x[2] * inv_l, x[3] * inv_l),
+                                       pack_bf2(x[4] * inv_l, x[5] * inv_l), pack_bf2(x[6] * inv_l, x[7] * inv_l));
                 }
             }
         }
         umma::fence_before_sync();
-        __syncthreads();  // shared tiles and TMEM are reused by the next segment
-        ta = tb;
+        __syncthreads();  // shared tiles and TMEM are reused by the next item
     }
 
-    if (!ok && tid == 0) umma::mbar_wait(mbar, phase ^ 1u, kWaitLimit);
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
@@ -310,19 +294,37 @@ bool window_softmax_tc_supported(const LayerDims& L) {
     return L.d == kD && (L.G == 1 || L.G == 2 || L.G == 4 || L.G == 8);
 }
 
-cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr,
-                                     const __nv_bfloat16* v, const float* o_lin, const float* lambda,
-                                     const int32_t* cu, __nv_bfloat16* out, int32_t* err, cudaStream_t st) {
+cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
+                                     const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
+                                     int32_t* err, cudaStream_t st) {
     static bool configured = false;
+    static int n_sm = 0;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(window_softmax_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+        cudaError_t e = cudaFuncSetAttribute(window_softmax_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemAlloc);
         if (e != cudaSuccess) return e;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+            n_sm = 148;
         configured = true;
     }
-    const int QB = kRows / L.G;
-    dim3 grid((unsigned)((L.total + QB - 1) / QB), L.Hkv);
-    window_softmax_tc_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qr, kr, v, o_lin, lambda, cu, out, err);
+    if (L.total <= 0) return cudaSuccess;
+    const int QB = kD / L.G;
+    block_table_kernel<<<1, 32, 0, st>>>(L, QB, cu, blk_base);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap mq, mk, mv, mk64, mv64;
+    if (!tma::make_map_3d(&mq, qr, false, kD, (uint64_t)L.Hq, (uint64_t)L.total, 64, (uint32_t)L.G, (uint32_t)QB) ||
+        !tma::make_map_3d(&mk, kr, false, kD, (uint64_t)L.Hkv, (uint64_t)L.total, 64, 1, 8) ||
+        !tma::make_map_3d(&mv, v, true, kD, (uint64_t)L.Hkv, (uint64_t)L.total, 64, 1, 8) ||
+        !tma::make_map_3d(&mk64, kr, false, kD, (uint64_t)L.Hkv, (uint64_t)L.total, 64, 1, 64) ||
+        !tma::make_map_3d(&mv64, v, true, kD, (uint64_t)L.Hkv, (uint64_t)L.total, 64, 1, 64))
+        return cudaErrorInvalidValue;
+    const int64_t items_max = (L.total / QB + L.n_seqs + 1) * (int64_t)L.Hkv;
+    const unsigned grid = (unsigned)std::min<int64_t>(items_max, (int64_t)n_sm * 2);
+    window_softmax_tc_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, mk64, mv64, cu, blk_base, o_sm, out,
+                                                                err);
     return cudaGetLastError();
 }
 
