@@ -302,35 +302,36 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             const int b = c & 1;
             if (!role_wait(kOFull + b, (uint32_t)((c >> 1) & 1), 3, 64, r == 0)) break;
             const float gr = reinterpret_cast<const float*>(sm + b * kBuf + kVec)[r] * lam;
-            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
-            const bool row_on = emit && r < j_end - j0;
-            const size_t base = ((size_t)(start + j0 + (row_on ? r : 0) + W) * L.Hq + h) * kD + slice * kNS;
-#pragma unroll 1
+            // lambda o_lin of this row into registers, then release the chunk buffer and D1/D2[b]
+            float o[kNS];
+#pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float d1[32], d2[32];
                 umma::tmem_ld32(tmem + lane_base + kColD1 + kNS * b + 32 * q, d1);
                 umma::tmem_ld32(tmem + lane_base + kColD2 + kNS * b + 32 * q, d2);
-                if (row_on) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        const uint4 sv = *reinterpret_cast<const uint4*>(o_sm + base + 32 * q + i);
-                        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-                        uint32_t ow[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[e]));
-                            const int k = i + 2 * e;
-                            const __nv_bfloat162 o2 = __floats2bfloat162_rn(fmaf(gr, d1[k], fmaf(lam, d2[k], f.x)),
-                                                                            fmaf(gr, d1[k + 1], fmaf(lam, d2[k + 1], f.y)));
-                            ow[e] = *reinterpret_cast<const uint32_t*>(&o2);
-                        }
-                        *reinterpret_cast<uint4*>(out + base + 32 * q + i) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                    }
-                }
+                for (int i = 0; i < 32; ++i) o[32 * q + i] = fmaf(gr, d1[i], lam * d2[i]);
             }
             umma::fence_before_sync();
             group_sync(3, 64);
             if (r == 0) mbar_arrive(bar(kFree + b));
+            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+            if (emit && r < j_end - j0) {
+                const size_t base = ((size_t)(start + j0 + r + W) * L.Hq + h) * kD + slice * kNS;
+#pragma unroll
+                for (int i = 0; i < kNS; i += 8) {
+                    const uint4 sv = *reinterpret_cast<const uint4*>(o_sm + base + i);
+                    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[e]));
+                        const __nv_bfloat162 o2 = __floats2bfloat162_rn(f.x + o[i + 2 * e], f.y + o[i + 2 * e + 1]);
+                        ow[e] = *reinterpret_cast<const uint32_t*>(&o2);
+                    }
+                    *reinterpret_cast<uint4*>(out + base + i) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+            }
         }
     }
 
