@@ -188,12 +188,11 @@ GDN_RECURRENT_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu"
 # stage boundaries recorded by the library, in launch order
 STAGES_CHUNKED = ("features", "softmax", "gdn_prep", "gdn_state")
 STAGES_SERIAL = ("features", "none", "gdn_state", "softmax")
-GDN_PREP_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_inverse.cu",
-                    "linearized_attention_rope_gb300/csrc/umma.cuh",
-                    "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
-GDN_CHUNKED_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_chunked.cu",
-                       "linearized_attention_rope_gb300/csrc/umma.cuh",
-                       "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
+CSRC = "linearized_attention_rope_gb300/csrc/"
+GDN_PREP_SOURCES = [CSRC + "gdn_inverse.cu", CSRC + "umma.cuh", CSRC + "hla_common.cuh"]
+GDN_CHUNKED_SOURCES = [CSRC + "gdn_chunked.cu", CSRC + "umma.cuh", CSRC + "tma.cuh", CSRC + "hla_common.cuh"]
+SOFTMAX_TC_SOURCES = [CSRC + "window_softmax_tc.cu", CSRC + "umma.cuh", CSRC + "tma.cuh", CSRC + "hla_common.cuh"]
+FEATURES_SOURCES = [CSRC + "features.cu", CSRC + "hla_common.cuh"]
 
 
 def chunked_gdn_flops_per_token_head(d: int = 128, C: int = 64) -> dict:
@@ -233,9 +232,7 @@ def prefill_work(wl):
         "gdn_state": gdn_state,
         # q.k and p.v over the visible keys of every (token, q-head)
         "softmax": ({"bound": "tensor", "flops": 4.0 * d * keys * Hq, "unit": "TFLOP/s",
-                     "sources": ["linearized_attention_rope_gb300/csrc/window_softmax_tc.cu",
-                                 "linearized_attention_rope_gb300/csrc/umma.cuh",
-                                 "linearized_attention_rope_gb300/csrc/hla_common.cuh"],
+                     "sources": SOFTMAX_TC_SOURCES,
                      "kernel": "window_softmax_tc_kernel"}
                     if wl.dtype == "bf16" and d == 128 else
                     {"bound": "alu", "flops": 4.0 * d * keys * Hq, "peak": FP32_ALU_TFLOPS,
@@ -243,7 +240,7 @@ def prefill_work(wl):
                      "kernel": "window_softmax_kernel"}),
         # read q, k, v; write RoPE'd q, k and qhat, khat, vhat
         "features": {"bound": "hbm", "bytes": float(T * d * ((Hq + 2 * Hkv) * eb + (2 * Hq + 3 * Hkv) * eb)),
-                     "unit": "GB/s", "sources": ["linearized_attention_rope_gb300/csrc/features.cu"],
+                     "unit": "GB/s", "sources": FEATURES_SOURCES,
                      "kernel": "features_kernel"},
         "absorbed_token_heads": absorbed * Hq,
     }
