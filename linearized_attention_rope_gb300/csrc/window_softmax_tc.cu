@@ -149,27 +149,33 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         float m_run = -INFINITY, l_run = 0.f;
         for (int grp = 0; grp < n_groups && ok; ++grp) {
             const int g0 = grp * kGroup, n = min(kGroup, n_slots - g0);  // a multiple of 16
-            // ---- loads: the query tile with the first group, then this group's keys and values
-            if (tid == 0) {
-                const uint32_t bytes = (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u;
-                tma::expect_tx(bar_ld, bytes);
-                if (grp == 0) {
-                    const int tq = (int)(start + pa);
-                    tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
-                    tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
+            // ---- loads: the query tile with the first group, then this group's keys and values;
+            //      lane 0 posts the byte count, the lanes of warp 0 issue the boxes
+            if (warp == 0) {
+                if (lane == 0) {
+                    tma::expect_tx(bar_ld, (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u);
+                    if (grp == 0) {
+                        const int tq = (int)(start + pa);
+                        tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
+                        tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
+                    }
                 }
-                for (int j = 0; j < n;) {
+                __syncwarp();
+                // boxes of 8 slots; a 64-slot run of window rows at a 64-aligned offset is one box
+                for (int j = 8 * lane; j < n; j += 8 * 32) {
                     const int slot = g0 + j;
+                    const bool wide = slot >= sink_pad && (j & 63) == 0 && j + 64 <= n;
+                    const bool covered = slot >= sink_pad && (j & 63) != 0 && (j & ~63) + 64 <= n &&
+                                         g0 + (j & ~63) >= sink_pad;  // inside a wide box issued by another lane
+                    if (covered) continue;
                     const int tk = (int)(start + (slot < sink_pad ? slot : span_lo + (slot - sink_pad)));
                     const uint32_t off = (uint32_t)j * 128u;
-                    const bool wide = slot >= sink_pad && (j & 63) == 0 && j + 64 <= n;  // 64 window rows
                     const CUtensorMap* mk = wide ? &map_k64 : &map_k;
                     const CUtensorMap* mv = wide ? &map_v64 : &map_v;
                     tma::tensor_load_3d(sbase + kK + off, mk, 0, kv, tk, bar_ld);
                     tma::tensor_load_3d(sbase + kK + 16384 + off, mk, 64, kv, tk, bar_ld);
                     tma::tensor_load_3d(sbase + kV + off, mv, 0, kv, tk, bar_ld);
                     tma::tensor_load_3d(sbase + kV + 16384 + off, mv, 64, kv, tk, bar_ld);
-                    j += wide ? 64 : 8;
                 }
             }
             if (!(ok = cta_wait(bar_ld, ph_ld))) break;
@@ -187,19 +193,20 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
             }
             if (!(ok = cta_wait(bar_mma, ph_mma))) break;
 
-            // ---- online softmax: this thread covers slots [c_lo, c_hi) of the group
-            const int c_lo = chalf * 64, c_hi = min(n, c_lo + 64);
-            float mg = -INFINITY;
+            // ---- online softmax: this thread covers slots [c_lo, c_hi) of the group (16-slot chunks,
+            //      split evenly between the two threads of the row)
+            const int n16 = n >> 4, c_lo = chalf ? ((n16 + 1) >> 1) * 16 : 0, c_hi = chalf ? n : ((n16 + 1) >> 1) * 16;
+            float mg = -INFINITY;  // raw scores: the scale is positive
             for (int c = c_lo; c < c_hi; c += 16) {
                 float sc[16];
                 umma::tmem_ld16(tmem + lane_base + kColS + c, sc);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int gi = g0 + c + i;
-                    if (gi < hi1 || (gi >= lo2 && gi < hi2)) mg = fmaxf(mg, sc[i] * qscale);
+                    if (gi < hi1 || (gi >= lo2 && gi < hi2)) mg = fmaxf(mg, sc[i]);
                 }
             }
-            red[chalf * 128 + row] = mg;
+            red[chalf * 128 + row] = mg * qscale;
             __syncthreads();
             const float m_new = fmaxf(m_run, fmaxf(red[row], red[128 + row]));
             const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
