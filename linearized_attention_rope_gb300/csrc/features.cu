@@ -38,21 +38,17 @@ cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse,
     return cudaGetLastError();
 }
 
-constexpr int kRun = 32;          // output tokens per CTA
-constexpr int kHist = 8;          // tokens before the run that are read for the conv history (7 used)
-constexpr int kReseed = 16;       // cos/sin re-formed from the tables every 16 positions
-constexpr int kFeatThreads = 256;
+constexpr int kTT = 32;                   // output tokens per CTA
+constexpr int kRowsPerCta = 4;            // feature rows (q, k or v heads) per CTA
+constexpr int kStage = kTT + kConvHalo;   // staged tokens: 7 of conv history, then the outputs
+constexpr int kFeatThreads = 128;
 
-// Eight consecutive raw elements of one row, as loaded (16 B for bf16, 32 B for fp32).
-template <typename Tin> struct Raw8;
-template <> struct Raw8<__nv_bfloat16> {
-    static constexpr int kWords = 4;
-    uint32_t w[4];
-    __device__ __forceinline__ void load(const __nv_bfloat16* p) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    }
-    __device__ __forceinline__ void unpack(float* x) const {
+template <typename T> struct Vec8;  // eight elements as one or two 16-byte words
+template <> struct Vec8<__nv_bfloat16> {
+    static constexpr int kChunks = 1;
+    __device__ static void unpack(const unsigned char* p, float* x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
@@ -60,45 +56,50 @@ template <> struct Raw8<__nv_bfloat16> {
         }
     }
 };
-template <> struct Raw8<float> {
-    static constexpr int kWords = 8;
-    uint32_t w[8];
-    __device__ __forceinline__ void load(const float* p) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-        w[0] = __float_as_uint(a.x); w[1] = __float_as_uint(a.y); w[2] = __float_as_uint(a.z); w[3] = __float_as_uint(a.w);
-        w[4] = __float_as_uint(b.x); w[5] = __float_as_uint(b.y); w[6] = __float_as_uint(b.z); w[7] = __float_as_uint(b.w);
-    }
-    __device__ __forceinline__ void unpack(float* x) const {
+template <> struct Vec8<__half> {
+    static constexpr int kChunks = 1;
+    __device__ static void unpack(const unsigned char* p, float* x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(w[i]);
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            x[2 * i] = f.x; x[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void pack(unsigned char* p, const float* x) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct Vec8<float> {
+    static constexpr int kChunks = 2;
+    __device__ static void unpack(const unsigned char* p, float* x) {
+        const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 16);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    __device__ static void pack(unsigned char* p, const float* x) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(p + 16) = make_float4(x[4], x[5], x[6], x[7]);
     }
 };
 
-__device__ __forceinline__ void store8(__half* p, const float* x) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-}
-__device__ __forceinline__ void store8(float* p, const float* x) {
-    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
-}
-
-// One CTA = kRun tokens x HPC feature rows (q heads, then k heads, then v
-// heads).  D / 8 lanes cover one row, 8 channels each, and walk the tokens in
-// order in batches of 8 (every batch starts at a multiple of 8): the rotated
-// values of the last 8 tokens sit in a register ring indexed by token mod 8,
-// which serves as the conv history; RoPE's partner half (channel c +- D/2)
-// comes from lane xor D/16, and cos/sin advance by one position with a
-// rotation by theta_i, re-formed from the tables (angle addition, both
-// reduced in double precision) at every 16th position of a sequence and at
-// the CTA's first token.
+// One CTA = kTT tokens x kRowsPerCta feature rows (q heads, then k heads,
+// then v heads, in that order across the grid).  The rows of the kTT tokens
+// and their 7 predecessors are staged in shared memory, rotated there in
+// place (RoPE on q and k; cos/sin from the fine and coarse tables by angle
+// addition, both reduced in double precision) and written out as the RoPE'd
+// q and k; then one thread per (token, row, 8 channels) runs the width-8
+// causal conv over the staged rows with its 64 weights held in registers,
+// and the D / 8 lanes of a row finish the L2 norm with shuffles.  Conv taps
+// before a sequence's first token read as zero.
 template <typename Tin, typename Tf, int D>
-__global__ void __launch_bounds__(kFeatThreads, 1)
+__global__ void __launch_bounds__(kFeatThreads, 4)
 features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
                 const Tin* __restrict__ v, const float* __restrict__ wq,
                 const float* __restrict__ wk, const float* __restrict__ wv,
@@ -106,135 +107,136 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
                 const float2* __restrict__ coarse, Tf* __restrict__ qr, Tf* __restrict__ kr,
                 Tf* __restrict__ qhat, Tf* __restrict__ khat, Tf* __restrict__ vhat,
                 int32_t* __restrict__ err) {
-    constexpr int G8 = D / 8, HALF = D / 2, RPW = 32 / G8, HPC = (kFeatThreads / 32) * RPW;
-    constexpr bool kPrefetch = sizeof(Tin) == 2;  // bf16 rows of a batch are loaded up front
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cg = lane % G8, c0 = 8 * cg;
+    static_assert(sizeof(Tin) == sizeof(Tf), "rows are rotated in place");
+    constexpr int HALF = D / 2, G8 = D / 8, E = (int)sizeof(Tin);
+    constexpr int ROWB = D * E;                                     // bytes per staged row
+    constexpr int CH = 16 / E;                                      // elements per 16-byte chunk
+    extern __shared__ __align__(16) unsigned char xs[];             // [kStage tokens][kRowsPerCta][D]
+    __shared__ int pos_s[kStage];
+    const int tid = threadIdx.x;
+    const int64_t t0 = (int64_t)blockIdx.x * kTT;
     const int n_rows = L.Hq + 2 * L.Hkv;
-    int head = blockIdx.y * HPC + warp * RPW + lane / G8;
-    const bool active = head < n_rows;  // idle lanes still take part in the shuffles
-    if (!active) head = n_rows - 1;
-    int kind = 0;  // 0 = q, 1 = k, 2 = v
-    if (head >= L.Hq + L.Hkv) { kind = 2; head -= L.Hq + L.Hkv; }
-    else if (head >= L.Hq) { kind = 1; head -= L.Hq; }
-    const size_t row_stride = (size_t)(kind == 0 ? L.Hq : L.Hkv) * D;  // elements between tokens
-    const bool do_rot = kind != 2;
-    const bool do_norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));
-    const float sgn = c0 < HALF ? -1.f : 1.f;  // x1' = x1 c - x2 s,  x2' = x2 c + x1 s
-    const int f0 = c0 % HALF;
 
+    // row j of this CTA: kind (0 q, 1 k, 2 v), head, and whether it exists
+    auto row_info = [&](int j, int* kind, int* head) {
+        int hr = blockIdx.y * kRowsPerCta + j;
+        const bool on = hr < n_rows;
+        if (!on) hr = n_rows - 1;
+        *kind = 0;
+        if (hr >= L.Hq + L.Hkv) { *kind = 2; hr -= L.Hq + L.Hkv; }
+        else if (hr >= L.Hq) { *kind = 1; hr -= L.Hq; }
+        *head = hr;
+        return on;
+    };
+
+    // ---- stage the rows (zeros outside the token range)
+    for (int idx = tid; idx < kStage * kRowsPerCta * (ROWB / 16); idx += kFeatThreads) {
+        const int chunk = idx % (ROWB / 16), rj = idx / (ROWB / 16), j = rj % kRowsPerCta, tk = rj / kRowsPerCta;
+        int kind, head;
+        const bool on = row_info(j, &kind, &head);
+        const int64_t t = t0 - kConvHalo + tk;
+        const bool in = on && t >= 0 && t < L.total;
+        const Tin* src = kind == 0 ? q : (kind == 1 ? k : v);
+        const size_t H = kind == 0 ? L.Hq : L.Hkv;
+        const Tin* gp = src + ((size_t)(in ? t : 0) * H + head) * D + chunk * CH;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(xs + (size_t)rj * ROWB + chunk * 16)),
+                     "l"(gp), "r"(in ? 16u : 0u)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (tid < kStage) {  // position of each staged token inside its sequence (-1: none)
+        const int64_t t = t0 - kConvHalo + tid;
+        int p = -1;
+        if (t >= 0 && t < L.total) {
+            const int s = seq_of_token(cu, L.n_seqs, t);
+            int64_t start, len;
+            seq_range(cu, s, L.total, &start, &len);
+            if (t >= start && t < start + len) p = (int)(t - start);
+            else if (err && blockIdx.y == 0) atomicExch(err, kErrSeqlens);
+        }
+        pos_s[tid] = p;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+
+    // ---- RoPE in place on q and k rows (bf16 -> fp16 or fp32 -> fp32), RoPE'd rows out
+    for (int idx = tid; idx < kStage * kRowsPerCta * (HALF / 8); idx += kFeatThreads) {
+        const int f8 = idx % (HALF / 8), rj = idx / (HALF / 8), j = rj % kRowsPerCta, tk = rj / kRowsPerCta;
+        int kind, head;
+        const bool on = row_info(j, &kind, &head);
+        unsigned char* r = xs + (size_t)rj * ROWB;
+        float x1[8], x2[8];
+        Vec8<Tin>::unpack(r + f8 * 8 * E, x1);
+        Vec8<Tin>::unpack(r + (HALF + f8 * 8) * E, x2);
+        const int p = pos_s[tk];
+        if (kind != 2 && p >= 0) {
+            const float2* fp = fine + (p & 63) * HALF + f8 * 8;
+            const float2* gp = coarse + (p >> 6) * HALF + f8 * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 f = __ldg(fp + i), g = __ldg(gp + i);
+                const float c = g.x * f.x - g.y * f.y, sn = g.y * f.x + g.x * f.y;
+                const float a = x1[i], b = x2[i];
+                x1[i] = a * c - b * sn;
+                x2[i] = b * c + a * sn;
+            }
+        }
+        Vec8<Tf>::pack(r + f8 * 8 * E, x1);
+        Vec8<Tf>::pack(r + (HALF + f8 * 8) * E, x2);
+        const int64_t t = t0 - kConvHalo + tk;
+        if (on && kind != 2 && tk >= kConvHalo && t < L.total) {
+            Tf* dst = (kind == 0 ? qr : kr) + ((size_t)t * (kind == 0 ? L.Hq : L.Hkv) + head) * D;
+            Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(dst + f8 * 8), x1);
+            Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(dst + HALF + f8 * 8), x2);
+        }
+    }
+    __syncthreads();
+
+    // ---- causal conv (tap m reads token t - 7 + m) and L2 norm; a thread keeps one (row, 8 channels)
+    static_assert((kFeatThreads % (kRowsPerCta * G8)) == 0, "a thread keeps its row and channels");
+    const int cg = tid % G8, j = (tid / G8) % kRowsPerCta;
+    int kind, head;
+    const bool on = row_info(j, &kind, &head);
+    const bool do_norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));
     float wt[8][kConvWidth];
     {
         const float4* wp = reinterpret_cast<const float4*>((kind == 0 ? wq : (kind == 1 ? wk : wv)) +
-                                                           ((size_t)head * D + c0) * kConvWidth);
+                                                           ((size_t)head * D + cg * 8) * kConvWidth);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 a = __ldg(wp + 2 * j), b = __ldg(wp + 2 * j + 1);
-            wt[j][0] = a.x; wt[j][1] = a.y; wt[j][2] = a.z; wt[j][3] = a.w;
-            wt[j][4] = b.x; wt[j][5] = b.y; wt[j][6] = b.z; wt[j][7] = b.w;
+        for (int c = 0; c < 8; ++c) {
+            const float4 a = __ldg(wp + 2 * c), b = __ldg(wp + 2 * c + 1);
+            wt[c][0] = a.x; wt[c][1] = a.y; wt[c][2] = a.z; wt[c][3] = a.w;
+            wt[c][4] = b.x; wt[c][5] = b.y; wt[c][6] = b.z; wt[c][7] = b.w;
         }
     }
-    float2 stp[8];  // (cos, sin) of theta_i
-#pragma unroll
-    for (int j = 0; j < 8; ++j) stp[j] = __ldg(fine + HALF + f0 + j);
-
-    const int64_t t_out = (int64_t)blockIdx.x * kRun;
-    const int64_t t_first = t_out - kHist > 0 ? t_out - kHist : 0;
-    const int64_t t_end = t_out + kRun < L.total ? t_out + kRun : L.total;
-    int s = seq_of_token(cu, L.n_seqs, t_first);
-    int64_t s_start, s_len;
-    seq_range(cu, s, L.total, &s_start, &s_len);
-
-    const Tin* src = (kind == 0 ? q : (kind == 1 ? k : v)) + (size_t)head * D + c0;
-    Tf* rot_dst = (kind == 0 ? qr : kr) + (size_t)head * D + c0;
-    Tf* hat_dst = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + c0;
-
-    float ring[8][8];  // rotated rows of tokens t = 8 b + slot
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ring[m][j] = 0.f;
-    float cs[8], sn[8];
-    bool seeded = false;
-
+    Tf* hat = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + cg * 8;
+    const size_t H = kind == 0 ? L.Hq : L.Hkv;
+    constexpr int kTokStep = kFeatThreads / (kRowsPerCta * G8);
 #pragma unroll 1
-    for (int64_t tb = t_out - kHist; tb < t_end; tb += 8) {
-        Raw8<Tin> raw[8];
-        if (kPrefetch) {
+    for (int to = tid / (kRowsPerCta * G8); to < kTT; to += kTokStep) {
+        const int64_t t = t0 + to;
+        const int p = pos_s[to + kConvHalo];
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (tb + u >= t_first && tb + u < t_end) raw[u].load(src + (size_t)(tb + u) * row_stride);
+        for (int m = 0; m < kConvWidth; ++m) {
+            if (m < kConvHalo - p) continue;  // before the sequence's first token (p < 0: none)
+            float x[8];
+            Vec8<Tf>::unpack(xs + ((size_t)(to + m) * kRowsPerCta + j) * ROWB + cg * 8 * E, x);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][m], x[c], y[c]);
         }
+        float ss = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int64_t t = tb + u;
-            if (t < t_first || t >= t_end) continue;  // same t across the CTA: uniform
-            if (!kPrefetch) raw[u].load(src + (size_t)t * row_stride);
-            while (t >= s_start + s_len && s + 1 < L.n_seqs) {
-                ++s;
-                seq_range(cu, s, L.total, &s_start, &s_len);
-            }
-            const bool in_seq = t >= s_start && t < s_start + s_len;
-            if (!in_seq && err && threadIdx.x == 0 && blockIdx.y == 0) atomicExch(err, kErrSeqlens);
-            const int pos = in_seq ? (int)(t - s_start) : 0;
-            if (pos == 0) {  // a sequence starts: zero conv history
+        for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
+        for (int o = G8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (do_norm) {
+            const float rs = rsqrtf(ss + 1e-6f);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) ring[m][j] = 0.f;
-            }
-            if (!seeded || (pos & (kReseed - 1)) == 0) {
-                const float2* fp = fine + (pos & 63) * HALF + f0;
-                const float2* gp = coarse + (pos >> 6) * HALF + f0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float2 f = __ldg(fp + j), g = __ldg(gp + j);
-                    cs[j] = g.x * f.x - g.y * f.y;
-                    sn[j] = g.y * f.x + g.x * f.y;
-                }
-                seeded = true;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float c = cs[j] * stp[j].x - sn[j] * stp[j].y;
-                    sn[j] = sn[j] * stp[j].x + cs[j] * stp[j].y;
-                    cs[j] = c;
-                }
-            }
-            Raw8<Tin> partner;
-#pragma unroll
-            for (int i = 0; i < Raw8<Tin>::kWords; ++i) partner.w[i] = __shfl_xor_sync(0xffffffffu, raw[u].w[i], G8 / 2);
-            float x[8], xp[8];
-            raw[u].unpack(x);
-            partner.unpack(xp);
-            if (do_rot && in_seq) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] = fmaf(x[j], cs[j], sgn * xp[j] * sn[j]);
-            }
-            const bool out_row = t >= t_out && active;
-            if (out_row && do_rot) store8(rot_dst + (size_t)t * row_stride, x);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ring[u][j] = in_seq ? x[j] : 0.f;
-            // causal depthwise conv: tap m multiplies token t - 7 + m, ring slot (u + 1 + m) mod 8
-            float y[8];
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float a = 0.f;
-#pragma unroll
-                for (int m = 0; m < kConvWidth; ++m) a = fmaf(wt[j][m], ring[(u + 1 + m) & 7][j], a);
-                y[j] = a;
-                ss = fmaf(a, a, ss);
-            }
-#pragma unroll
-            for (int o = G8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (do_norm) {
-                const float r = rsqrtf(ss + 1e-6f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) y[j] *= r;
-            }
-            if (out_row) store8(hat_dst + (size_t)t * row_stride, y);
+            for (int c = 0; c < 8; ++c) y[c] *= rs;
         }
+        if (on && t < L.total && p >= 0) Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(hat + (size_t)t * H * D), y);
     }
 }
 
@@ -243,15 +245,23 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float* wq, const float* wk, const float* wv, const int32_t* cu,
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st) {
-    const int hpc = (kFeatThreads / 32) * (32 / (L.d / 8));
-    dim3 grid((unsigned)((L.total + kRun - 1) / kRun), (unsigned)((L.Hq + 2 * L.Hkv + hpc - 1) / hpc));
+    dim3 grid((unsigned)((L.total + kTT - 1) / kTT), (unsigned)((L.Hq + 2 * L.Hkv + kRowsPerCta - 1) / kRowsPerCta));
     if (L.total <= 0) return cudaSuccess;
-    if (L.d == 128)
-        features_kernel<Tin, Tf, 128><<<grid, kFeatThreads, 0, st>>>(
+    const size_t smem = (size_t)kStage * kRowsPerCta * L.d * sizeof(Tin);
+    if (L.d == 128) {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(features_kernel<Tin, Tf, 128>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            configured = true;
+        }
+        features_kernel<Tin, Tf, 128><<<grid, kFeatThreads, smem, st>>>(
             L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err);
-    else
-        features_kernel<Tin, Tf, 64><<<grid, kFeatThreads, 0, st>>>(
+    } else {
+        features_kernel<Tin, Tf, 64><<<grid, kFeatThreads, smem, st>>>(
             L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err);
+    }
     return cudaGetLastError();
 }
 
