@@ -185,9 +185,6 @@ def source_hash(files) -> str:
 # prefill
 GDN_RECURRENT_SOURCES = ["linearized_attention_rope_gb300/csrc/gdn_recurrent.cu",
                          "linearized_attention_rope_gb300/csrc/hla_common.cuh"]
-# stage boundaries recorded by the library, in launch order
-STAGES_CHUNKED = ("features", "softmax", "gdn_prep", "gdn_state")
-STAGES_SERIAL = ("features", "none", "gdn_state", "softmax")
 CSRC = "linearized_attention_rope_gb300/csrc/"
 GDN_PREP_SOURCES = [CSRC + "gdn_inverse.cu", CSRC + "umma.cuh", CSRC + "hla_common.cuh"]
 GDN_CHUNKED_SOURCES = [CSRC + "gdn_chunked.cu", CSRC + "umma.cuh", CSRC + "tma.cuh", CSRC + "hla_common.cuh"]
@@ -268,7 +265,7 @@ def run_prefill_bench(args, dist, peaks):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    n_stage = 5
+    n_stage = 7
     chunked = wl.dtype == "bf16" and wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads in (1, 2, 4, 8)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
     for row in ev:  # materialise the event handles
@@ -290,8 +287,15 @@ def run_prefill_bench(args, dist, peaks):
     wall = time.perf_counter() - t0
     dist.barrier()
     step_ms = [ev[i][0].elapsed_time(ends[i]) for i in range(args.steps)]
-    stage_ms = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
-                for j, name in enumerate(STAGES_CHUNKED if chunked else STAGES_SERIAL)}
+    def stages(row):
+        t = [0.0] + [row[0].elapsed_time(row[j]) for j in range(1, n_stage)]  # ms from mark 0
+        if chunked:  # the chunk-local GDN kernel runs on the library's side stream beside the softmax
+            return {"features": t[1], "softmax": t[2] - t[1], "gdn_prep": t[4] - t[3],
+                    "gdn_state": t[5] - max(t[2], t[4])}
+        return {"features": t[1], "gdn_state": t[4] - t[3], "softmax": t[5] - t[4]}
+
+    per_step = [stages(ev[i]) for i in range(args.steps)]
+    stage_ms = {k: statistics.mean(st[k] for st in per_step) for k in per_step[0]}
     device_s = dist.max(sum(step_ms) / 1e3)
     # rope tables, features, then block table + softmax, chunk table + chunk kernel, state kernel
     # (tensor-core path) or GDN + softmax (token-serial path)

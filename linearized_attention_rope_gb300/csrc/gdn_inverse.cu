@@ -29,11 +29,12 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kTmemCols = 128;               // Gram (64 columns), then Wm^T (128)
 constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
 constexpr uint32_t kTbg = 8192;                   // T diag(beta gamma) image, over the first query block
-constexpr uint32_t kA32 = 32768;                  // A fp32 [64][68]
-constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68]
+constexpr int kSA = 65;                           // row stride of A (odd: row-per-thread writes hit distinct banks)
+constexpr uint32_t kA32 = 32768;                  // A fp32 [64][kSA]
+constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68] (rows 16-byte aligned)
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
-constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta
-constexpr uint32_t kMisc = kVec + 2 * 64 * 4;
+constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta, gamma
+constexpr uint32_t kMisc = kVec + 3 * 64 * 4;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -48,7 +49,7 @@ __device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, 
     float a[32], t[32];
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
-        a[m] = sA[(32 * b + l) * 68 + 32 * b + m];
+        a[m] = sA[(32 * b + l) * kSA + 32 * b + m];
         t[m] = (m == l) ? 1.f : 0.f;
     }
 #pragma unroll
@@ -90,6 +91,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     float* sX = reinterpret_cast<float*>(sm + kX32);
     float* sG = reinterpret_cast<float*>(sm + kVec);
     float* sBeta = sG + 64;
+    float* sGam = sG + 128;
     uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
     float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
@@ -183,7 +185,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
             for (int ii = 0; ii < 32; ++ii) {
                 const int i = 32 * half + ii;
-                sA[r * 68 + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
+                sA[r * kSA + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
             }
         }
     } else if (done) {  // rows 64..127: Q K^T -> P
@@ -208,7 +210,9 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     }
     if (tid < kC) {  // gamma and the key decay over the rest of the chunk
         float* vec = reinterpret_cast<float*>(rec + kRecVec);
-        vec[tid] = exp2f(sG[tid]);
+        const float gam = exp2f(sG[tid]);
+        vec[tid] = gam;
+        sGam[tid] = gam;
         vec[kC + tid] = exp2f(sG[kC - 1] - sG[tid]);
     }
     umma::fence_before_sync();
@@ -222,7 +226,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         const int i = tid >> 2, j0c = (tid & 3) * 8;
         float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = j0c; k < 32; ++k) {  // T00 is lower triangular
-            const float a = sA[(32 + i) * 68 + k];
+            const float a = sA[(32 + i) * kSA + k];
             const float4 t0 = *reinterpret_cast<const float4*>(&sT[k * 68 + j0c]);
             const float4 t1 = *reinterpret_cast<const float4*>(&sT[k * 68 + j0c + 4]);
             x[0] = fmaf(a, t0.x, x[0]); x[1] = fmaf(a, t0.y, x[1]); x[2] = fmaf(a, t0.z, x[2]); x[3] = fmaf(a, t0.w, x[3]);
@@ -253,7 +257,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
             tb[x] = tr[x] * sBeta[c8 + x];
-            tbg[x] = tb[x] * exp2f(sG[c8 + x]);
+            tbg[x] = tb[x] * sGam[c8 + x];
         }
         const uint32_t off = umma::sw128_offset(r, c8, 64);
         *reinterpret_cast<uint4*>(rec + kRecTb + off) =

@@ -100,6 +100,33 @@ cudaError_t mark_stage(int i, cudaStream_t s) {
     return cudaSuccess;
 }
 
+// Per host thread and device: a side stream for the chunk-local GDN kernel,
+// which runs beside the softmax kernel (both depend only on the feature
+// path), and the events that fork it off the caller's stream and join it
+// back before the GDN state kernel.  Created on first use, kept for the
+// thread's lifetime.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+thread_local SideStream t_side[kMaxDevices];
+
+cudaError_t side_stream(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream& ss = t_side[dev];
+    if (!ss.s) {
+        if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
+
 #define HLA_TRY(...)                                           \
     do {                                                       \
         cudaError_t e_ = (__VA_ARGS__);                             \
@@ -134,30 +161,39 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     bool chunked = false;
     if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
     if (chunked) {
-        // features -> softmax (final rows, fp16 rows to finish) -> chunk-local GDN -> GDN state + combine
+        // features -> { softmax (final rows, fp16 rows to finish) on the caller's stream,
+        //               chunk-local GDN on the side stream } -> GDN state + combine
         if constexpr (std::is_same<Tf, __half>::value) {
             __half* osm = reinterpret_cast<__half*>(ws + w.osm);
             int32_t* blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
             int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+            SideStream* side = nullptr;
+            HLA_TRY(side_stream(&side));
+            HLA_TRY(cudaEventRecord(side->fork, stream));
+            HLA_TRY(cudaStreamWaitEvent(side->s, side->fork, 0));
+            HLA_TRY(mark_stage(3, side->s));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, side->s));
+            HLA_TRY(mark_stage(4, side->s));
+            HLA_TRY(cudaEventRecord(side->join, side->s));
             HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, stream));
-            HLA_TRY(mark_stage(3, stream));
+            HLA_TRY(cudaStreamWaitEvent(stream, side->join, 0));
             HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, osm, lambda, o, S_out, err, stream));
         }
     } else {
         // features -> GDN (fp32 o_lin) -> softmax + combine
         HLA_TRY(mark_stage(2, stream));
-        HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
         HLA_TRY(mark_stage(3, stream));
+        HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
+        HLA_TRY(mark_stage(4, stream));
         HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
                                                stream));
     }
-    HLA_TRY(mark_stage(4, stream));
-    if (st) HLA_TRY(launch_state_fill<Tin, Tf>(L, qi, ki, vi, g, beta, kh, vh, cu, *st, stream));
     HLA_TRY(mark_stage(5, stream));
+    if (st) HLA_TRY(launch_state_fill<Tin, Tf>(L, qi, ki, vi, g, beta, kh, vh, cu, *st, stream));
+    HLA_TRY(mark_stage(6, stream));
     return HLA_OK;
 }
 
