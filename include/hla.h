@@ -97,7 +97,9 @@ typedef struct hla_params {
  *   conv_v    fp32  [N, 7, Hkv, d]  raw v of positions p-7 .. p-1
  *   pos       int64 [N]  next position of each sequence
  *   err       int32 [4]  device error word (0 = fine)
- * The whole struct is the resumable state: copying the buffers out and back
+ *   scratch   per-step temporaries of hla_decode_step (size from
+ *             hla_state_bytes); dead between calls, not part of the state
+ * Every buffer but scratch is the resumable state: copying them out and back
  * in resumes decoding exactly. */
 typedef struct hla_state {
     float* S;
@@ -112,11 +114,12 @@ typedef struct hla_state {
     float* conv_v;
     int64_t* pos;
     int32_t* err;
+    void* scratch;
 } hla_state;
 
 /* byte sizes of the hla_state buffers, in struct order */
 typedef struct hla_state_sizes {
-    size_t S, k_ring, v_ring, pend_k, pend_v, pend_g, pend_beta, conv_q, conv_k, conv_v, pos, err;
+    size_t S, k_ring, v_ring, pend_k, pend_v, pend_g, pend_beta, conv_q, conv_k, conv_v, pos, err, scratch;
 } hla_state_sizes;
 
 /* Human-readable name of a status code (static string). */

@@ -111,58 +111,75 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
     const float*, const __half*, const __half*, const int32_t*, const hla_state&, cudaStream_t);
 
 // ---------------------------------------------------------------------------
-// One decode step.  CTA (kv head, sequence n), 256 threads, owning the G
-// query heads of the group, so the new token's key/value features, the ring
-// and the pending ring are touched by one CTA only:
-//  1. RoPE q, k of the new token p; short conv of q (G heads), k and v with
-//     their histories; L2 norms -> qhat (G heads), khat.  The new token is
-//     written into the KV ring (slot p, or n_sinks + (p - n_sinks) % W) and
-//     into the pending ring (slot p % (W + 1)) with each head's g and beta.
-//  2. If token j = p - W is not a sink it leaves the window now.  Per head,
-//     the d x d state is read once into registers: x = khat_j^T S and
-//     y = qhat_p^T S; then S <- alpha S + khat_j u^T with u = beta (vhat_j -
-//     alpha x) is written back, and o_lin = alpha y + (qhat_p . khat_j) u.
-//  3. Softmax over the ring (sinks + window, the new token included), in
-//     tiles of up to kTile keys: logits of all G heads per key row (8 lanes
-//     per row), per-head max and sum, then P V with the value rows read
-//     coalesced; tiles are merged with a running max.
-//  4. o = o_sm + lambda_h o_lin.
-constexpr int kDecThreads = 256;
-constexpr int kDecWarps = kDecThreads / 32;
+// One decode step, in four kernels over per-step scratch (hla_state.scratch):
+//  1. features (CTA per kv head and sequence): RoPE q, k of the new token p;
+//     short conv of q (the G heads of the group), k and v with their
+//     histories; L2 norms.  The new token goes into the KV ring (slot p, or
+//     n_sinks + (p - n_sinks) % W) and the pending ring (slot p % (W + 1))
+//     with each head's g and beta; RoPE'd q and qhat go to scratch.
+//  2. state (CTA per q-head and sequence): if token j = p - W is not a sink it
+//     leaves the window now: the 64 KiB state is read once into registers,
+//     x = khat_j^T S and y = qhat_p^T S are reduced across the CTA, and
+//     S <- alpha S + khat_j u^T with u = beta (vhat_j - alpha x) is written
+//     back; o_lin = alpha y + (qhat_p . khat_j) u.  Otherwise o_lin = 0.
+//  3. softmax (CTA per kv head, key split and sequence): the ring's valid slots
+//     are [0, min(n_sinks, p + 1)) and [n_sinks, n_sinks + n_window) (the
+//     window fills its slots in order, then stays full), so a split is a
+//     plain range of slots; per head of the group a running max, sum and P V
+//     over its keys go to scratch.
+//  4. combine (CTA per sequence): splits merged by their maxima,
+//     o = o_sm + lambda_h o_lin.
+// Kernels 2 and 3 stream the state and the ring, the step's bulk traffic,
+// with many CTAs per SM.
 constexpr int kMaxG = 8;
-constexpr int kTile = 1024;
-constexpr int kUnrollK = 4;   // key rows in flight per lane (logits)
-constexpr int kUnrollV = 8;   // value rows in flight per thread (P V)
+constexpr int kFeatThreads = 256;
+constexpr int kStateThreads = 128;
+constexpr int kSmThreads = 128;
+constexpr int kSplitKeys = 256;   // key slots per softmax split (at most)
+constexpr int kUnrollK = 4;       // key rows in flight per lane (logits)
+constexpr int kUnrollV = 8;       // value rows in flight per thread (P V)
+
+// Per-step scratch layout (floats): qrot, qhat, olin [N, Hq, D]; pm, pl [N, Hq, splits];
+// pacc [N, Hq, splits, D].
+struct DecScratch {
+    float *qrot, *qhat, *olin, *pm, *pl, *pacc;
+    int splits;
+};
+__host__ __device__ inline int decode_splits(int n_sinks, int window) {
+    return (n_sinks + window + kSplitKeys - 1) / kSplitKeys;
+}
+inline DecScratch dec_scratch(float* base, int n_seqs, int Hq, int D, int splits) {
+    DecScratch d;
+    const size_t nh = (size_t)n_seqs * Hq;
+    d.qrot = base;
+    d.qhat = d.qrot + nh * D;
+    d.olin = d.qhat + nh * D;
+    d.pm = d.olin + nh * D;
+    d.pl = d.pm + nh * splits;
+    d.pacc = d.pl + nh * splits;
+    d.splits = splits;
+    return d;
+}
+size_t decode_scratch_bytes(int n_seqs, int Hq, int D, int n_sinks, int window) {
+    const size_t nh = (size_t)n_seqs * Hq, sp = (size_t)decode_splits(n_sinks, window);
+    return sizeof(float) * (3 * nh * D + 2 * nh * sp + nh * sp * D);
+}
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kDecThreads, 2)
-decode_step_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
-                   const Tin* __restrict__ v, const float* __restrict__ g,
-                   const float* __restrict__ beta, const float* __restrict__ lambda,
-                   const float* __restrict__ wq, const float* __restrict__ wk,
-                   const float* __restrict__ wv, hla_state s, Tin* __restrict__ out) {
+__global__ void __launch_bounds__(kFeatThreads)
+decode_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
+                       const Tin* __restrict__ v, const float* __restrict__ g,
+                       const float* __restrict__ beta, const float* __restrict__ wq,
+                       const float* __restrict__ wk, const float* __restrict__ wv, hla_state s, DecScratch sc) {
     constexpr int HALF = D / 2;
-    constexpr int CG = D / 4;              // float4 column groups of S
-    constexpr int RG = kDecThreads / CG;   // row groups
-    constexpr int RPT = D / RG;            // rows of S per thread
-    constexpr int DL = D / 8;              // channels per lane in the 8-lane key groups
-    constexpr int NKS = kDecThreads / CG;  // key subsets in P V
-    extern __shared__ __align__(16) float dyn[];  // logits [G][kTile], later P V partials [NKS][G][D]
-    __shared__ __align__(16) float qrot_s[kMaxG][D], qhat_s[kMaxG][D], olin_s[kMaxG][D];
-    __shared__ __align__(16) float krot_s[D], vraw_s[D], khat_s[D], kj_s[D], vj_s[D];
-    __shared__ __align__(16) float redx[RG][D], redy[RG][D];
-    __shared__ float cs_s[HALF], sn_s[HALF];
-    __shared__ float alpha_s[kMaxG], b_s[kMaxG], cdot_s[kMaxG], inv_s[kMaxG + 1];
-    __shared__ float m_s[kMaxG], l_s[kMaxG], corr_s[kMaxG];
-
+    __shared__ __align__(16) float qhat_s[kMaxG][D];
+    __shared__ __align__(16) float krot_s[D], vraw_s[D], khat_s[D], vhat_s[D];
+    __shared__ float cs_s[HALF], sn_s[HALF], inv_s[kMaxG + 1];
     const int kv = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.G, ns = L.n_sinks, W = L.window, R = ns + W, P = W + 1;
     const int64_t p = s.pos[n];
-    Tin* kring = static_cast<Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D;
-    Tin* vring = static_cast<Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
     const size_t kvrow = ((size_t)n * L.Hkv + kv) * D;
 
-    // ---- 1. features of the new token
     if (tid < HALF) {
         float c, sn;
         rope_cs_exact(p, L.theta[tid], &c, &sn);
@@ -175,46 +192,38 @@ decode_step_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict
         const float x1 = to_f32(x[i]), x2 = to_f32(x[i + HALF]);
         return c < HALF ? x1 * cs_s[i] - x2 * sn_s[i] : x2 * cs_s[i] + x1 * sn_s[i];
     };
+    // short conv with the history; tap 7 on the new token
+    auto conv = [&](float xr, float* hist, size_t step, const float* w) {
+        float hst[kConvHalo];
+#pragma unroll
+        for (int m = 0; m < kConvHalo; ++m) hst[m] = hist[m * step];
+        float acc = w[kConvHalo] * xr;
+#pragma unroll
+        for (int m = 0; m < kConvHalo; ++m) acc = fmaf(w[m], hst[m], acc);
+#pragma unroll
+        for (int m = 0; m + 1 < kConvHalo; ++m) hist[m * step] = hst[m + 1];
+        hist[(kConvHalo - 1) * step] = xr;
+        return acc;
+    };
     if (tid < 2 * D) {  // k channels, then v channels
         const bool is_k = tid < D;
         const int c = is_k ? tid : tid - D;
         const float xr = is_k ? rot(k + kvrow, c) : to_f32(v[kvrow + c]);
-        float* hist = (is_k ? s.conv_k : s.conv_v) + ((size_t)n * kConvHalo * L.Hkv + kv) * D + c;
-        const size_t step = (size_t)L.Hkv * D;
-        const float* w = (is_k ? wk : wv) + ((size_t)kv * D + c) * kConvWidth;
-        float hst[kConvHalo];
-#pragma unroll
-        for (int m = 0; m < kConvHalo; ++m) hst[m] = hist[m * step];
-        float acc = w[kConvHalo] * xr;
-#pragma unroll
-        for (int m = 0; m < kConvHalo; ++m) acc = fmaf(w[m], hst[m], acc);
-#pragma unroll
-        for (int m = 0; m + 1 < kConvHalo; ++m) hist[m * step] = hst[m + 1];
-        hist[(kConvHalo - 1) * step] = xr;
+        const float acc = conv(xr, (is_k ? s.conv_k : s.conv_v) + ((size_t)n * kConvHalo * L.Hkv + kv) * D + c,
+                               (size_t)L.Hkv * D, (is_k ? wk : wv) + ((size_t)kv * D + c) * kConvWidth);
         if (is_k) { krot_s[c] = xr; khat_s[c] = acc; }
-        else { vraw_s[c] = xr; vj_s[c] = acc; }  // vj_s holds vhat_p until phase 2
+        else { vraw_s[c] = xr; vhat_s[c] = acc; }
     }
-    for (int e = tid; e < G * D; e += kDecThreads) {
+    for (int e = tid; e < G * D; e += kFeatThreads) {
         const int gg = e / D, c = e % D, h = kv * G + gg;
         const float xr = rot(q + ((size_t)n * L.Hq + h) * D, c);
-        float* hist = s.conv_q + ((size_t)n * kConvHalo * L.Hq + h) * D + c;
-        const size_t step = (size_t)L.Hq * D;
-        const float* w = wq + ((size_t)h * D + c) * kConvWidth;
-        float hst[kConvHalo];
-#pragma unroll
-        for (int m = 0; m < kConvHalo; ++m) hst[m] = hist[m * step];
-        float acc = w[kConvHalo] * xr;
-#pragma unroll
-        for (int m = 0; m < kConvHalo; ++m) acc = fmaf(w[m], hst[m], acc);
-#pragma unroll
-        for (int m = 0; m + 1 < kConvHalo; ++m) hist[m * step] = hst[m + 1];
-        hist[(kConvHalo - 1) * step] = xr;
-        qrot_s[gg][c] = xr;
-        qhat_s[gg][c] = acc;
+        qhat_s[gg][c] = conv(xr, s.conv_q + ((size_t)n * kConvHalo * L.Hq + h) * D + c, (size_t)L.Hq * D,
+                             wq + ((size_t)h * D + c) * kConvWidth);
+        sc.qrot[((size_t)n * L.Hq + h) * D + c] = xr;
     }
     __syncthreads();
     // L2 norms: job gg < G is q-head gg, job G is the key
-    for (int job = warp; job <= G; job += kDecWarps) {
+    for (int job = warp; job <= G; job += kFeatThreads / 32) {
         const float* x = job < G ? qhat_s[job] : khat_s;
         float ss = 0.f;
         for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
@@ -223,223 +232,247 @@ decode_step_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict
         if (lane == 0) inv_s[job] = (job == G || (L.flags & HLA_FLAG_L2NORM_Q)) ? rsqrtf(ss + 1e-6f) : 1.f;
     }
     __syncthreads();
-    for (int e = tid; e < G * D; e += kDecThreads) qhat_s[e / D][e % D] *= inv_s[e / D];
+    for (int e = tid; e < G * D; e += kFeatThreads)
+        sc.qhat[((size_t)n * L.Hq + kv * G) * D + e] = qhat_s[e / D][e % D] * inv_s[e / D];
     const size_t pslot = (size_t)(p % P);
     if (tid < D) {
-        const float kh = khat_s[tid] * inv_s[G];
+        Tin* kring = static_cast<Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D;
+        Tin* vring = static_cast<Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
         const size_t slot = (size_t)ring_slot(p, ns, W) * D + tid;
         kring[slot] = from_f32<Tin>(krot_s[tid]);
         vring[slot] = from_f32<Tin>(vraw_s[tid]);
         const size_t ps = (((size_t)n * L.Hkv + kv) * P + pslot) * D + tid;
-        s.pend_k[ps] = kh;
-        s.pend_v[ps] = vj_s[tid];
+        s.pend_k[ps] = khat_s[tid] * inv_s[G];
+        s.pend_v[ps] = vhat_s[tid];
     }
-    const int64_t j = p - W;  // the token leaving the window
-    const bool absorb = j >= ns;
-    const size_t jslot = absorb ? (size_t)(j % P) : 0;
     if (tid < G) {
         const size_t gs = ((size_t)n * L.Hq + kv * G + tid) * P;
-        if (absorb) {
-            alpha_s[tid] = expf(s.pend_g[gs + jslot]);
-            b_s[tid] = s.pend_beta[gs + jslot];
-        }
         s.pend_g[gs + pslot] = g[(size_t)n * L.Hq + kv * G + tid];
         s.pend_beta[gs + pslot] = beta[(size_t)n * L.Hq + kv * G + tid];
     }
-    __syncthreads();  // ring slot p, pending slot p written; vj_s free
+}
 
-    // ---- 2. absorb token j and read the state out, one head at a time
-    if (absorb) {
-        if (tid < D) {
-            const size_t ps = (((size_t)n * L.Hkv + kv) * P + jslot) * D + tid;
-            kj_s[tid] = s.pend_k[ps];
-            vj_s[tid] = s.pend_v[ps];
-        }
-        __syncthreads();
-        for (int job = warp; job < G; job += kDecWarps) {
-            float d = 0.f;
-            for (int c = lane; c < D; c += 32) d += qhat_s[job][c] * kj_s[c];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) cdot_s[job] = d;
-        }
-        const int cg = tid % CG, rg = tid / CG;
-        for (int gg = 0; gg < G; ++gg) {
-            float4* S4 = reinterpret_cast<float4*>(s.S + ((size_t)n * L.Hq + kv * G + gg) * D * D);
-            float4 Sr[RPT];
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) Sr[r] = S4[(size_t)(rg * RPT + r) * CG + cg];
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const float kk = kj_s[rg * RPT + r], qq = qhat_s[gg][rg * RPT + r];
-                x.x = fmaf(kk, Sr[r].x, x.x); x.y = fmaf(kk, Sr[r].y, x.y);
-                x.z = fmaf(kk, Sr[r].z, x.z); x.w = fmaf(kk, Sr[r].w, x.w);
-                y.x = fmaf(qq, Sr[r].x, y.x); y.y = fmaf(qq, Sr[r].y, y.y);
-                y.z = fmaf(qq, Sr[r].z, y.z); y.w = fmaf(qq, Sr[r].w, y.w);
-            }
-            reinterpret_cast<float4*>(redx[rg])[cg] = x;
-            reinterpret_cast<float4*>(redy[rg])[cg] = y;
-            __syncthreads();
-            const float alpha = alpha_s[gg], b = b_s[gg], cdot = cdot_s[gg];
-            float u[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 4 * cg + e;
-                float xs = 0.f, ys = 0.f;
-#pragma unroll
-                for (int r = 0; r < RG; ++r) { xs += redx[r][col]; ys += redy[r][col]; }
-                u[e] = b * (vj_s[col] - alpha * xs);
-                if (rg == 0) olin_s[gg][col] = fmaf(alpha, ys, cdot * u[e]);
-            }
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const float kk = kj_s[rg * RPT + r];
-                float4 o;
-                o.x = fmaf(alpha, Sr[r].x, kk * u[0]);
-                o.y = fmaf(alpha, Sr[r].y, kk * u[1]);
-                o.z = fmaf(alpha, Sr[r].z, kk * u[2]);
-                o.w = fmaf(alpha, Sr[r].w, kk * u[3]);
-                S4[(size_t)(rg * RPT + r) * CG + cg] = o;
-            }
-            __syncthreads();  // redx/redy reused by the next head
-        }
-    } else {
-        // nothing has been absorbed yet: the state is still empty
-        for (int e = tid; e < G * D; e += kDecThreads) olin_s[e / D][e % D] = 0.f;
+// CTA (q-head h, sequence n).  Thread t owns column group t % (D/4) (four
+// value dims, float4) of rows (t / (D/4)) * RPT .. + RPT - 1.
+template <int D>
+__global__ void __launch_bounds__(kStateThreads, 3)
+decode_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
+    constexpr int CG = D / 4, RG = kStateThreads / CG, RPT = D / RG;
+    __shared__ __align__(16) float kj_s[D], vj_s[D], qh_s[D];
+    __shared__ __align__(16) float redx[RG][D], redy[RG][D];
+    __shared__ float cdot_s;
+    const int h = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, kv = h / L.G;
+    const int ns = L.n_sinks, W = L.window, P = W + 1;
+    const int64_t p = s.pos[n], j = p - W;  // the token leaving the window
+    float* olin = sc.olin + ((size_t)n * L.Hq + h) * D;
+    if (j < ns) {  // nothing leaves the window into the state this step
+        for (int c = tid; c < D; c += kStateThreads) olin[c] = 0.f;
+        return;
     }
+    const size_t jslot = (size_t)(j % P);
+    const size_t gs = ((size_t)n * L.Hq + h) * P + jslot;
+    const float alpha = expf(s.pend_g[gs]), b = s.pend_beta[gs];
+    const int cg = tid % CG, rg = tid / CG;
+    float4* S4 = reinterpret_cast<float4*>(s.S + ((size_t)n * L.Hq + h) * D * D);
+    float4 Sr[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) Sr[r] = S4[(size_t)(rg * RPT + r) * CG + cg];
+    for (int c = tid; c < D; c += kStateThreads) {
+        const size_t ps = (((size_t)n * L.Hkv + kv) * P + jslot) * D + c;
+        kj_s[c] = s.pend_k[ps];
+        vj_s[c] = s.pend_v[ps];
+        qh_s[c] = sc.qhat[((size_t)n * L.Hq + h) * D + c];
+    }
+    __syncthreads();
+    if (tid < 32) {
+        float d = 0.f;
+        for (int c = tid; c < D; c += 32) d += qh_s[c] * kj_s[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (tid == 0) cdot_s = d;
+    }
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const float kk = kj_s[rg * RPT + r], qq = qh_s[rg * RPT + r];
+        x.x = fmaf(kk, Sr[r].x, x.x); x.y = fmaf(kk, Sr[r].y, x.y);
+        x.z = fmaf(kk, Sr[r].z, x.z); x.w = fmaf(kk, Sr[r].w, x.w);
+        y.x = fmaf(qq, Sr[r].x, y.x); y.y = fmaf(qq, Sr[r].y, y.y);
+        y.z = fmaf(qq, Sr[r].z, y.z); y.w = fmaf(qq, Sr[r].w, y.w);
+    }
+    reinterpret_cast<float4*>(redx[rg])[cg] = x;
+    reinterpret_cast<float4*>(redy[rg])[cg] = y;
+    __syncthreads();
+    float u[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int col = 4 * cg + e;
+        float xs = 0.f, ys = 0.f;
+#pragma unroll
+        for (int r = 0; r < RG; ++r) { xs += redx[r][col]; ys += redy[r][col]; }
+        u[e] = b * (vj_s[col] - alpha * xs);
+        if (rg == 0) olin[col] = fmaf(alpha, ys, cdot_s * u[e]);
+    }
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const float kk = kj_s[rg * RPT + r];
+        float4 o;
+        o.x = fmaf(alpha, Sr[r].x, kk * u[0]);
+        o.y = fmaf(alpha, Sr[r].y, kk * u[1]);
+        o.z = fmaf(alpha, Sr[r].z, kk * u[2]);
+        o.w = fmaf(alpha, Sr[r].w, kk * u[3]);
+        S4[(size_t)(rg * RPT + r) * CG + cg] = o;
+    }
+}
 
-    // ---- 3. softmax over the ring: sinks j < min(ns, p + 1), window [w_lo, p]
-    const int64_t nsk = p + 1 < ns ? p + 1 : ns;
-    const int64_t w_lo = (p - W + 1) > ns ? (p - W + 1) : ns;
-    const int64_t n_win = p >= w_lo ? p - w_lo + 1 : 0;
-    const int64_t n_keys = nsk + n_win;
+// CTA (kv head x split, sequence n): softmax partials of the G heads of the
+// group over key slots [split * KS, (split + 1) * KS) of the valid-slot list.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kSmThreads)
+decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
+    constexpr int DL = D / 8;                // channels per lane in the 8-lane key groups
+    constexpr int CG = D / 4, NKS = kSmThreads / CG;
+    __shared__ __align__(16) float qrot_s[kMaxG][D];
+    __shared__ float logit[kMaxG][kSplitKeys];
+    __shared__ __align__(16) float part[kSmThreads / (D / 4)][kMaxG][D];
+    __shared__ float m_s[kMaxG], l_s[kMaxG];
+    const int split = blockIdx.x % sc.splits, kv = blockIdx.x / sc.splits, n = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = L.G, ns = L.n_sinks, W = L.window, R = ns + W;
+    const int64_t p = s.pos[n];
+    const int nsk = (int)(p + 1 < ns ? p + 1 : ns);
+    const int n_win = p >= ns ? (int)min((int64_t)W, p - ns + 1) : 0;
+    const int n_keys = nsk + n_win;
+    const int KS = (R + sc.splits - 1) / sc.splits;
+    const int k0 = split * KS, nt = max(0, min(KS, n_keys - k0));
+    const Tin* kring = static_cast<const Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D;
+    const Tin* vring = static_cast<const Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
+    auto slot_of = [&](int i) { return i < nsk ? i : ns + (i - nsk); };  // valid-slot list entry -> ring slot
     const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
-    float* logit = dyn;  // [G][kTile]
+
+    for (int e = tid; e < G * D; e += kSmThreads) qrot_s[e / D][e % D] = sc.qrot[((size_t)n * L.Hq + kv * G) * D + e];
+    __syncthreads();
+    // logits: 8 lanes per key row, DL channels per lane, kUnrollK rows in flight per lane; the
+    // trip count is the same for the whole warp (shuffles with every lane present)
     const int l8 = tid & 7, grp8 = tid >> 3;
+    for (int i0 = 0; i0 < nt; i0 += (kSmThreads / 8) * kUnrollK) {
+        float kx[kUnrollK][DL];
+#pragma unroll
+        for (int u = 0; u < kUnrollK; ++u) {
+            const int i = i0 + grp8 + (kSmThreads / 8) * u;
+            if (i < nt) {
+                const Tin* kr = kring + (size_t)slot_of(k0 + i) * D + DL * l8;
+#pragma unroll
+                for (int e = 0; e < DL; e += 4) load_vec<4>(kr + e, kx[u] + e);
+            } else {
+#pragma unroll
+                for (int e = 0; e < DL; ++e) kx[u][e] = 0.f;
+            }
+        }
+        for (int gg = 0; gg < G; ++gg) {
+            float pt[kUnrollK];
+#pragma unroll
+            for (int u = 0; u < kUnrollK; ++u) {
+                pt[u] = 0.f;
+#pragma unroll
+                for (int e = 0; e < DL; ++e) pt[u] = fmaf(qrot_s[gg][DL * l8 + e], kx[u][e], pt[u]);
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+                for (int u = 0; u < kUnrollK; ++u) pt[u] += __shfl_xor_sync(0xffffffffu, pt[u], o);
+#pragma unroll
+            for (int u = 0; u < kUnrollK; ++u) {
+                const int i = i0 + grp8 + (kSmThreads / 8) * u;
+                if (i < nt && l8 == 0) logit[gg][i] = pt[u] * qscale;
+            }
+        }
+    }
+    __syncthreads();
+    for (int gg = warp; gg < G; gg += kSmThreads / 32) {  // per-head max and sum; logits -> probabilities
+        float mx = -INFINITY;
+        for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, logit[gg][i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.f;
+        for (int i = lane; i < nt; i += 32) {
+            const float e = exp2f(logit[gg][i] - mx);
+            logit[gg][i] = e;
+            sum += e;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) { m_s[gg] = mx; l_s[gg] = sum; }
+    }
+    __syncthreads();
+    // P V: thread (key subset ks, 4 channels cg4), value rows read coalesced
     const int cg4 = tid % CG, ks = tid / CG;
     float acc[kMaxG][4];
 #pragma unroll
     for (int gg = 0; gg < kMaxG; ++gg)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[gg][e] = 0.f;
-    if (tid < G) { m_s[tid] = -INFINITY; l_s[tid] = 0.f; }
-    for (int64_t t0 = 0; t0 < n_keys; t0 += kTile) {
-        const int nt = (int)min((int64_t)kTile, n_keys - t0);
-        __syncthreads();  // logits of the previous tile consumed
-        // logits: 8 lanes per key row, DL channels per lane, kUnrollK rows in
-        // flight per lane.  The trip count is the same for the whole warp (the
-        // shuffles run with every lane present); tail rows are predicated.
-        for (int i0 = 0; i0 < nt; i0 += (kDecThreads / 8) * kUnrollK) {
-            float kx[kUnrollK][DL];
+    for (int i0 = ks; i0 < nt; i0 += NKS * kUnrollV) {
+        float vx[kUnrollV][4];
 #pragma unroll
-            for (int u = 0; u < kUnrollK; ++u) {
-                const int i = i0 + grp8 + (kDecThreads / 8) * u;
-                if (i < nt) {
-                    const int64_t ii = t0 + i;
-                    const int64_t jj = ii < nsk ? ii : w_lo + (ii - nsk);
-                    const Tin* kr = kring + (size_t)ring_slot(jj, ns, W) * D + DL * l8;
+        for (int u = 0; u < kUnrollV; ++u) {
+            const int i = i0 + NKS * u;
+            if (i < nt) load_vec<4>(vring + (size_t)slot_of(k0 + i) * D + 4 * cg4, vx[u]);
+            else {
 #pragma unroll
-                    for (int e = 0; e < DL; e += 4) load_vec<4>(kr + e, kx[u] + e);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < DL; ++e) kx[u][e] = 0.f;
-                }
-            }
-            for (int gg = 0; gg < G; ++gg) {
-                float part[kUnrollK];
-#pragma unroll
-                for (int u = 0; u < kUnrollK; ++u) {
-                    part[u] = 0.f;
-#pragma unroll
-                    for (int e = 0; e < DL; ++e) part[u] = fmaf(qrot_s[gg][DL * l8 + e], kx[u][e], part[u]);
-                }
-#pragma unroll
-                for (int o = 1; o < 8; o <<= 1)
-#pragma unroll
-                    for (int u = 0; u < kUnrollK; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
-#pragma unroll
-                for (int u = 0; u < kUnrollK; ++u) {
-                    const int i = i0 + grp8 + (kDecThreads / 8) * u;
-                    if (i < nt && l8 == 0) logit[gg * kTile + i] = part[u] * qscale;
-                }
+                for (int e = 0; e < 4; ++e) vx[u][e] = 0.f;
             }
         }
-        __syncthreads();
-        // per-head running max and sum; logits -> probabilities
-        for (int gg = warp; gg < G; gg += kDecWarps) {
-            float mx = -INFINITY;
-            for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, logit[gg * kTile + i]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_old = m_s[gg], m_new = fmaxf(m_old, mx);
-            float sum = 0.f;
-            for (int i = lane; i < nt; i += 32) {
-                const float e = exp2f(logit[gg * kTile + i] - m_new);
-                logit[gg * kTile + i] = e;
-                sum += e;
-            }
+        for (int u = 0; u < kUnrollV; ++u) {
+            const int i = min(i0 + NKS * u, nt - 1);  // rows past the tail carry zero values
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (lane == 0) {
-                const float corr = exp2f(m_old - m_new);  // 0 on the first tile
-                corr_s[gg] = corr;
-                l_s[gg] = l_s[gg] * corr + sum;
-                m_s[gg] = m_new;
-            }
-        }
-        __syncthreads();
-        // P V: thread (key subset ks, 4 channels cg4), value rows read coalesced
+            for (int gg = 0; gg < kMaxG; ++gg)
+                if (gg < G) {
+                    const float pr = logit[gg][i];
 #pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg)
-            if (gg < G) {
-                const float c = corr_s[gg];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[gg][e] *= c;
-            }
-        for (int i0 = ks; i0 < nt; i0 += NKS * kUnrollV) {
-            float vx[kUnrollV][4];
-#pragma unroll
-            for (int u = 0; u < kUnrollV; ++u) {
-                const int i = i0 + NKS * u;
-                if (i < nt) {
-                    const int64_t ii = t0 + i;
-                    const int64_t jj = ii < nsk ? ii : w_lo + (ii - nsk);
-                    load_vec<4>(vring + (size_t)ring_slot(jj, ns, W) * D + 4 * cg4, vx[u]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) vx[u][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) acc[gg][e] = fmaf(pr, vx[u][e], acc[gg][e]);
                 }
-            }
-#pragma unroll
-            for (int u = 0; u < kUnrollV; ++u) {
-                const int i = min(i0 + NKS * u, nt - 1);  // rows past the tail carry zero values
-#pragma unroll
-                for (int gg = 0; gg < kMaxG; ++gg)
-                    if (gg < G) {
-                        const float pr = logit[gg * kTile + i];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[gg][e] = fmaf(pr, vx[u][e], acc[gg][e]);
-                    }
-            }
         }
     }
-    __syncthreads();
-    float* part = dyn;  // [NKS][G][D]
 #pragma unroll
     for (int gg = 0; gg < kMaxG; ++gg)
         if (gg < G)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) part[((size_t)ks * G + gg) * D + 4 * cg4 + e] = acc[gg][e];
+            for (int e = 0; e < 4; ++e) part[ks][gg][4 * cg4 + e] = acc[gg][e];
     __syncthreads();
-
-    // ---- 4. combine
-    for (int e = tid; e < G * D; e += kDecThreads) {
-        const int gg = e / D, c = e % D, h = kv * G + gg;
+    for (int e = tid; e < G * D; e += kSmThreads) {
+        const int gg = e / D, c = e % D;
         float o = 0.f;
-        for (int r = 0; r < NKS; ++r) o += part[((size_t)r * G + gg) * D + c];
-        o = (L.flags & HLA_FLAG_SOFTMAX_OFF) ? 0.f : o / l_s[gg];
-        if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), olin_s[gg][c], o);
+#pragma unroll
+        for (int r = 0; r < NKS; ++r) o += part[r][gg][c];
+        const size_t hs = ((size_t)n * L.Hq + kv * G + gg) * sc.splits + split;
+        sc.pacc[hs * D + c] = o;
+        if (c == 0) {
+            sc.pm[hs] = nt > 0 ? m_s[gg] : -INFINITY;
+            sc.pl[hs] = nt > 0 ? l_s[gg] : 0.f;
+        }
+    }
+}
+
+// CTA per sequence: o = softmax (splits merged by their maxima) + lambda_h o_lin.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(256)
+decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out) {
+    const int n = blockIdx.x;
+    for (int e = threadIdx.x; e < L.Hq * D; e += blockDim.x) {
+        const int h = e / D, c = e % D;
+        const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
+        float m = -INFINITY;
+        for (int r = 0; r < sc.splits; ++r) m = fmaxf(m, sc.pm[hs + r]);
+        float l = 0.f, o = 0.f;
+        for (int r = 0; r < sc.splits; ++r) {
+            const float w = sc.pl[hs + r] > 0.f ? exp2f(sc.pm[hs + r] - m) : 0.f;
+            l = fmaf(sc.pl[hs + r], w, l);
+            o = fmaf(sc.pacc[(hs + r) * D + c], w, o);
+        }
+        o = (L.flags & HLA_FLAG_SOFTMAX_OFF) || l <= 0.f ? 0.f : o / l;
+        if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), sc.olin[((size_t)n * L.Hq + h) * D + c], o);
         out[((size_t)n * L.Hq + h) * D + c] = from_f32<Tin>(o);
     }
 }
@@ -449,11 +482,16 @@ __global__ void advance_pos_kernel(int64_t* pos, int n) {
     if (i < n) pos[i] += 1;
 }
 
-template <int D>
-constexpr size_t decode_dyn_smem() {
-    return sizeof(float) * (size_t)(kMaxG * kTile > (kDecThreads / (D / 4)) * kMaxG * D
-                                         ? kMaxG * kTile
-                                         : (kDecThreads / (D / 4)) * kMaxG * D);
+template <typename Tin, int D>
+cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v, const float* g,
+                           const float* beta, const float* lambda, const float* wq, const float* wk,
+                           const float* wv, const hla_state& s, Tin* out, cudaStream_t st) {
+    const DecScratch sc = dec_scratch(static_cast<float*>(s.scratch), L.n_seqs, L.Hq, D, decode_splits(L.n_sinks, L.window));
+    decode_features_kernel<Tin, D><<<dim3(L.Hkv, L.n_seqs), kFeatThreads, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, s, sc);
+    decode_state_kernel<D><<<dim3(L.Hq, L.n_seqs), kStateThreads, 0, st>>>(L, s, sc);
+    decode_softmax_kernel<Tin, D><<<dim3(L.Hkv * sc.splits, L.n_seqs), kSmThreads, 0, st>>>(L, s, sc);
+    decode_combine_kernel<Tin, D><<<L.n_seqs, 256, 0, st>>>(L, sc, lambda, out);
+    return cudaGetLastError();
 }
 
 template <typename Tin>
@@ -462,17 +500,9 @@ cudaError_t launch_decode_step(const LayerDims& L, const Tin* q, const Tin* k, c
                                const float* wq, const float* wk, const float* wv,
                                const hla_state& s, Tin* out, cudaStream_t st) {
     if (L.G > kMaxG) return cudaErrorInvalidValue;
-    dim3 grid(L.Hkv, L.n_seqs);
-    if (L.d == 128) {
-        constexpr size_t dyn = decode_dyn_smem<128>();
-        cudaFuncSetAttribute(decode_step_kernel<Tin, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-        decode_step_kernel<Tin, 128><<<grid, kDecThreads, dyn, st>>>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out);
-    } else {
-        constexpr size_t dyn = decode_dyn_smem<64>();
-        cudaFuncSetAttribute(decode_step_kernel<Tin, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-        decode_step_kernel<Tin, 64><<<grid, kDecThreads, dyn, st>>>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out);
-    }
-    cudaError_t e = cudaGetLastError();
+    if (L.n_seqs <= 0) return cudaSuccess;
+    cudaError_t e = L.d == 128 ? decode_kernels<Tin, 128>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out, st)
+                               : decode_kernels<Tin, 64>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out, st);
     if (e != cudaSuccess) return e;
     advance_pos_kernel<<<(L.n_seqs + 255) / 256, 256, 0, st>>>(s.pos, L.n_seqs);
     return cudaGetLastError();

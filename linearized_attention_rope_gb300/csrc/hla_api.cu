@@ -200,7 +200,7 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
 bool state_ok(const hla_state* st) {
     if (!st) return false;
     const void* ptrs[] = {st->S, st->k_ring, st->v_ring, st->pend_k, st->pend_v, st->pend_g,
-                          st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err};
+                          st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err, st->scratch};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return false;
     return true;
@@ -253,6 +253,7 @@ HLA_API int hla_state_bytes(const hla_params* prm, int n_seqs, hla_state_sizes* 
     out->conv_v = out->conv_k;
     out->pos = N * 8;
     out->err = 16;
+    out->scratch = decode_scratch_bytes(n_seqs, prm->n_q_heads, prm->head_dim, prm->n_sinks, prm->window);
     return HLA_OK;
 }
 
@@ -273,10 +274,10 @@ HLA_API int hla_state_init(const hla_params* prm, int n_seqs, const hla_state* s
     hla_state_bytes(prm, n_seqs, &sz);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ptrs[] = {st->S, st->k_ring, st->v_ring, st->pend_k, st->pend_v, st->pend_g,
-                    st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err};
+                    st->pend_beta, st->conv_q, st->conv_k, st->conv_v, st->pos, st->err, st->scratch};
     size_t sizes[] = {sz.S, sz.k_ring, sz.v_ring, sz.pend_k, sz.pend_v, sz.pend_g,
-                      sz.pend_beta, sz.conv_q, sz.conv_k, sz.conv_v, sz.pos, sz.err};
-    for (int i = 0; i < 12; ++i)
+                      sz.pend_beta, sz.conv_q, sz.conv_k, sz.conv_v, sz.pos, sz.err, sz.scratch};
+    for (int i = 0; i < 13; ++i)
         if (sizes[i]) HLA_TRY(cudaMemsetAsync(ptrs[i], 0, sizes[i], s));
     return HLA_OK;
 }

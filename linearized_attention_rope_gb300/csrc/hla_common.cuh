@@ -169,6 +169,8 @@ cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, co
                               const int32_t* cu, const hla_state& s, cudaStream_t st);
 
 // One decode step for all sequences, then pos += 1.
+// Bytes of the per-step decode scratch (hla_state.scratch).
+size_t decode_scratch_bytes(int n_seqs, int Hq, int D, int n_sinks, int window);
 template <typename Tin>
 cudaError_t launch_decode_step(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
                                const float* g, const float* beta, const float* lambda,

@@ -32,7 +32,7 @@ FLAG_LINEAR_OFF = 0x4
 FLAG_GDN_RECURRENT = 0x8
 
 STATE_FIELDS = ("S", "k_ring", "v_ring", "pend_k", "pend_v", "pend_g", "pend_beta", "conv_q",
-                "conv_k", "conv_v", "pos", "err")
+                "conv_k", "conv_v", "pos", "err", "scratch")
 
 
 class HlaError(RuntimeError):

@@ -39,8 +39,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(hla.CParams) == 9 * 4
-    assert ctypes.sizeof(hla.CState) == 12 * 8
-    assert ctypes.sizeof(hla.CStateSizes) == 12 * 8
+    assert ctypes.sizeof(hla.CState) == 13 * 8
+    assert ctypes.sizeof(hla.CStateSizes) == 13 * 8
 
 
 def test_status_strings(lib):
@@ -63,6 +63,9 @@ def test_state_sizes(lib):
     assert sz["pend_g"] == 64 * 32 * 889 * 4
     assert sz["conv_q"] == 64 * 7 * 32 * 128 * 4
     assert sz["pos"] == 64 * 8
+    # per-step decode scratch: q rot, qhat, o_lin [N, Hq, d]; per split of 256 key slots
+    # (4 for an 896-slot ring) the running max, sum and P V
+    assert sz["scratch"] == 4 * (3 * 64 * 32 * 128 + 2 * 64 * 32 * 4 + 64 * 32 * 4 * 128)
     f32 = hla.state_sizes(_p(dtype=hla.DTYPE_F32, head_dim=64), 1)
     assert f32["k_ring"] == 8 * 64 * 64 * 4
 
@@ -102,7 +105,7 @@ def test_prefill_rejects_null_and_misaligned_pointers_without_gpu(lib):
     assert rc == hla.HLA_ERR_INVALID_ARG  # no sequences
     rc = lib.hla_prefill(ctypes.byref(prm), *args, 1, 16, fake, None, fake, 16, None)
     assert rc == hla.HLA_ERR_WORKSPACE
-    bad_state = hla.CState(*([0x1000] * 11 + [0]))
+    bad_state = hla.CState(*([0x1000] * 11 + [0] + [0x1000]))  # no error word
     rc = lib.hla_prefill(ctypes.byref(prm), *args, 1, 16, fake, ctypes.byref(bad_state), fake,
                          1 << 30, None)
     assert rc == hla.HLA_ERR_INVALID_ARG
@@ -111,7 +114,7 @@ def test_prefill_rejects_null_and_misaligned_pointers_without_gpu(lib):
 def test_decode_rejects_bad_state_without_gpu(lib):
     prm = _p().c()
     fake = ctypes.c_void_p(0x1000)
-    bad_state = hla.CState(*([0x1000] * 5 + [0x1008] + [0x1000] * 6))  # misaligned pend_g
+    bad_state = hla.CState(*([0x1000] * 5 + [0x1008] + [0x1000] * 7))  # misaligned pend_g
     rc = lib.hla_decode_step(ctypes.byref(prm), 4, *([fake] * 9), ctypes.byref(bad_state), fake, None)
     assert rc == hla.HLA_ERR_INVALID_ARG
     rc = lib.hla_decode_step(ctypes.byref(prm), -1, *([fake] * 9), ctypes.byref(bad_state), fake, None)
