@@ -135,7 +135,7 @@ constexpr int kMaxG = 8;
 constexpr int kFeatThreads = 256;
 constexpr int kStateThreads = 128;
 constexpr int kSmThreads = 128;
-constexpr int kSplitKeys = 256;   // key slots per softmax split (at most)
+constexpr int kSplitKeys = 128;   // key slots per softmax split (at most)
 constexpr int kUnrollK = 4;       // key rows in flight per lane (logits)
 constexpr int kUnrollV = 8;       // value rows in flight per thread (P V)
 
@@ -327,14 +327,20 @@ decode_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
 
 // CTA (kv head x split, sequence n): softmax partials of the G heads of the
 // group over key slots [split * KS, (split + 1) * KS) of the valid-slot list.
+// The split's key and value rows are copied into shared memory at once (two
+// cp.async groups: logits need only the keys), so every CTA has its whole
+// share of the ring in flight.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(kSmThreads)
 decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
     constexpr int DL = D / 8;                // channels per lane in the 8-lane key groups
     constexpr int CG = D / 4, NKS = kSmThreads / CG;
-    __shared__ __align__(16) float qrot_s[kMaxG][D];
-    __shared__ float logit[kMaxG][kSplitKeys];
-    __shared__ __align__(16) float part[kSmThreads / (D / 4)][kMaxG][D];
+    constexpr int ROWB = D * (int)sizeof(Tin), CHUNKS = ROWB / 16;
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char* ks_s = smem;                                  // [kSplitKeys][D] keys; later P V partials
+    unsigned char* vs_s = smem + kSplitKeys * ROWB;              // [kSplitKeys][D] values
+    float* qrot_s = reinterpret_cast<float*>(vs_s + kSplitKeys * ROWB);  // [G][D]
+    float* logit = qrot_s + kMaxG * D;                           // [G][kSplitKeys]
     __shared__ float m_s[kMaxG], l_s[kMaxG];
     const int split = blockIdx.x % sc.splits, kv = blockIdx.x / sc.splits, n = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -350,24 +356,32 @@ decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
     auto slot_of = [&](int i) { return i < nsk ? i : ns + (i - nsk); };  // valid-slot list entry -> ring slot
     const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
 
-    for (int e = tid; e < G * D; e += kSmThreads) qrot_s[e / D][e % D] = sc.qrot[((size_t)n * L.Hq + kv * G) * D + e];
+    for (int base = 0; base < 2; ++base) {  // keys, then values
+        const Tin* ring = base ? vring : kring;
+        unsigned char* dst = base ? vs_s : ks_s;
+        for (int e = tid; e < nt * CHUNKS; e += kSmThreads) {
+            const int i = e / CHUNKS, c = e % CHUNKS;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             (uint32_t)__cvta_generic_to_shared(dst + (size_t)i * ROWB + 16 * c)),
+                         "l"(reinterpret_cast<const unsigned char*>(ring + (size_t)slot_of(k0 + i) * D) + 16 * c)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int e = tid; e < G * D; e += kSmThreads) qrot_s[e] = sc.qrot[((size_t)n * L.Hq + kv * G) * D + e];
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // the keys
     __syncthreads();
-    // logits: 8 lanes per key row, DL channels per lane, kUnrollK rows in flight per lane; the
-    // trip count is the same for the whole warp (shuffles with every lane present)
+    // logits: 8 lanes per key row, DL channels per lane; the trip count is the same for the
+    // whole warp (shuffles with every lane present)
     const int l8 = tid & 7, grp8 = tid >> 3;
     for (int i0 = 0; i0 < nt; i0 += (kSmThreads / 8) * kUnrollK) {
         float kx[kUnrollK][DL];
 #pragma unroll
         for (int u = 0; u < kUnrollK; ++u) {
             const int i = i0 + grp8 + (kSmThreads / 8) * u;
-            if (i < nt) {
-                const Tin* kr = kring + (size_t)slot_of(k0 + i) * D + DL * l8;
+            const Tin* kr = reinterpret_cast<const Tin*>(ks_s + (size_t)min(i, kSplitKeys - 1) * ROWB) + DL * l8;
 #pragma unroll
-                for (int e = 0; e < DL; e += 4) load_vec<4>(kr + e, kx[u] + e);
-            } else {
-#pragma unroll
-                for (int e = 0; e < DL; ++e) kx[u][e] = 0.f;
-            }
+            for (int e = 0; e < DL; e += 4) load_vec<4>(kr + e, kx[u] + e);
         }
         for (int gg = 0; gg < G; ++gg) {
             float pt[kUnrollK];
@@ -375,7 +389,7 @@ decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
             for (int u = 0; u < kUnrollK; ++u) {
                 pt[u] = 0.f;
 #pragma unroll
-                for (int e = 0; e < DL; ++e) pt[u] = fmaf(qrot_s[gg][DL * l8 + e], kx[u][e], pt[u]);
+                for (int e = 0; e < DL; ++e) pt[u] = fmaf(qrot_s[gg * D + DL * l8 + e], kx[u][e], pt[u]);
             }
 #pragma unroll
             for (int o = 1; o < 8; o <<= 1)
@@ -384,68 +398,58 @@ decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
 #pragma unroll
             for (int u = 0; u < kUnrollK; ++u) {
                 const int i = i0 + grp8 + (kSmThreads / 8) * u;
-                if (i < nt && l8 == 0) logit[gg][i] = pt[u] * qscale;
+                if (i < nt && l8 == 0) logit[gg * kSplitKeys + i] = pt[u] * qscale;
             }
         }
     }
     __syncthreads();
     for (int gg = warp; gg < G; gg += kSmThreads / 32) {  // per-head max and sum; logits -> probabilities
         float mx = -INFINITY;
-        for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, logit[gg][i]);
+        for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, logit[gg * kSplitKeys + i]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float sum = 0.f;
         for (int i = lane; i < nt; i += 32) {
-            const float e = exp2f(logit[gg][i] - mx);
-            logit[gg][i] = e;
+            const float e = exp2f(logit[gg * kSplitKeys + i] - mx);
+            logit[gg * kSplitKeys + i] = e;
             sum += e;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         if (lane == 0) { m_s[gg] = mx; l_s[gg] = sum; }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // the values
     __syncthreads();
-    // P V: thread (key subset ks, 4 channels cg4), value rows read coalesced
+    // P V: thread (key subset ks, 4 channels cg4)
     const int cg4 = tid % CG, ks = tid / CG;
     float acc[kMaxG][4];
 #pragma unroll
     for (int gg = 0; gg < kMaxG; ++gg)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[gg][e] = 0.f;
-    for (int i0 = ks; i0 < nt; i0 += NKS * kUnrollV) {
-        float vx[kUnrollV][4];
+    for (int i = ks; i < nt; i += NKS) {
+        float vx[4];
+        load_vec<4>(reinterpret_cast<const Tin*>(vs_s + (size_t)i * ROWB) + 4 * cg4, vx);
 #pragma unroll
-        for (int u = 0; u < kUnrollV; ++u) {
-            const int i = i0 + NKS * u;
-            if (i < nt) load_vec<4>(vring + (size_t)slot_of(k0 + i) * D + 4 * cg4, vx[u]);
-            else {
+        for (int gg = 0; gg < kMaxG; ++gg)
+            if (gg < G) {
+                const float pr = logit[gg * kSplitKeys + i];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) vx[u][e] = 0.f;
+                for (int e = 0; e < 4; ++e) acc[gg][e] = fmaf(pr, vx[e], acc[gg][e]);
             }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnrollV; ++u) {
-            const int i = min(i0 + NKS * u, nt - 1);  // rows past the tail carry zero values
-#pragma unroll
-            for (int gg = 0; gg < kMaxG; ++gg)
-                if (gg < G) {
-                    const float pr = logit[gg][i];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[gg][e] = fmaf(pr, vx[u][e], acc[gg][e]);
-                }
-        }
     }
+    float* part = reinterpret_cast<float*>(ks_s);  // [NKS][G][D]; the keys are no longer needed
 #pragma unroll
     for (int gg = 0; gg < kMaxG; ++gg)
         if (gg < G)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) part[ks][gg][4 * cg4 + e] = acc[gg][e];
+            for (int e = 0; e < 4; ++e) part[((size_t)ks * G + gg) * D + 4 * cg4 + e] = acc[gg][e];
     __syncthreads();
     for (int e = tid; e < G * D; e += kSmThreads) {
         const int gg = e / D, c = e % D;
         float o = 0.f;
 #pragma unroll
-        for (int r = 0; r < NKS; ++r) o += part[r][gg][c];
+        for (int r = 0; r < NKS; ++r) o += part[((size_t)r * G + gg) * D + c];
         const size_t hs = ((size_t)n * L.Hq + kv * G + gg) * sc.splits + split;
         sc.pacc[hs * D + c] = o;
         if (c == 0) {
@@ -455,13 +459,18 @@ decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
     }
 }
 
-// CTA per sequence: o = softmax (splits merged by their maxima) + lambda_h o_lin.
 template <typename Tin, int D>
-__global__ void __launch_bounds__(256)
+constexpr size_t decode_softmax_smem() {
+    return 2 * (size_t)kSplitKeys * D * sizeof(Tin) + sizeof(float) * (size_t)kMaxG * (D + kSplitKeys);
+}
+
+// CTA per (q-head, sequence), thread per channel: o = softmax (splits merged by
+// their maxima) + lambda_h o_lin.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(D)
 decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out) {
-    const int n = blockIdx.x;
-    for (int e = threadIdx.x; e < L.Hq * D; e += blockDim.x) {
-        const int h = e / D, c = e % D;
+    const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x;
+    {
         const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
         float m = -INFINITY;
         for (int r = 0; r < sc.splits; ++r) m = fmaxf(m, sc.pm[hs + r]);
@@ -489,8 +498,16 @@ cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const
     const DecScratch sc = dec_scratch(static_cast<float*>(s.scratch), L.n_seqs, L.Hq, D, decode_splits(L.n_sinks, L.window));
     decode_features_kernel<Tin, D><<<dim3(L.Hkv, L.n_seqs), kFeatThreads, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, s, sc);
     decode_state_kernel<D><<<dim3(L.Hq, L.n_seqs), kStateThreads, 0, st>>>(L, s, sc);
-    decode_softmax_kernel<Tin, D><<<dim3(L.Hkv * sc.splits, L.n_seqs), kSmThreads, 0, st>>>(L, s, sc);
-    decode_combine_kernel<Tin, D><<<L.n_seqs, 256, 0, st>>>(L, sc, lambda, out);
+    constexpr size_t sm_smem = decode_softmax_smem<Tin, D>();
+    static bool configured = false;  // per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_softmax_kernel<Tin, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sm_smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    decode_softmax_kernel<Tin, D><<<dim3(L.Hkv * sc.splits, L.n_seqs), kSmThreads, sm_smem, st>>>(L, s, sc);
+    decode_combine_kernel<Tin, D><<<dim3(L.Hq, L.n_seqs), D, 0, st>>>(L, sc, lambda, out);
     return cudaGetLastError();
 }
 
