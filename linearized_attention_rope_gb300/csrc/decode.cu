@@ -8,6 +8,7 @@
 
 namespace hla {
 
+
 __device__ __forceinline__ int64_t ring_slot(int64_t p, int n_sinks, int window) {
     return p < n_sinks ? p : n_sinks + (p - n_sinks) % window;
 }
@@ -130,7 +131,7 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
 //  4. combine (CTA per sequence): splits merged by their maxima,
 //     o = o_sm + lambda_h o_lin.
 // Kernels 2 and 3 stream the state and the ring, the step's bulk traffic,
-// with many CTAs per SM.
+// with many CTAs per SM; 2 runs on the side stream beside 3.
 constexpr int kMaxG = 8;
 constexpr int kFeatThreads = 256;
 constexpr int kStateThreads = 128;
@@ -497,7 +498,14 @@ cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const
                            const float* wv, const hla_state& s, Tin* out, cudaStream_t st) {
     const DecScratch sc = dec_scratch(static_cast<float*>(s.scratch), L.n_seqs, L.Hq, D, decode_splits(L.n_sinks, L.window));
     decode_features_kernel<Tin, D><<<dim3(L.Hkv, L.n_seqs), kFeatThreads, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, s, sc);
-    decode_state_kernel<D><<<dim3(L.Hq, L.n_seqs), kStateThreads, 0, st>>>(L, s, sc);
+    // the state update runs on the side stream beside the softmax (independent, both HBM-bound)
+    SideStream* side = nullptr;
+    cudaError_t e0 = side_stream(&side);
+    if (e0 == cudaSuccess) e0 = cudaEventRecord(side->fork, st);
+    if (e0 == cudaSuccess) e0 = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e0 != cudaSuccess) return e0;
+    decode_state_kernel<D><<<dim3(L.Hq, L.n_seqs), kStateThreads, 0, side->s>>>(L, s, sc);
+    if ((e0 = cudaEventRecord(side->join, side->s)) != cudaSuccess) return e0;
     constexpr size_t sm_smem = decode_softmax_smem<Tin, D>();
     static bool configured = false;  // per instantiation
     if (!configured) {
@@ -507,6 +515,7 @@ cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const
         configured = true;
     }
     decode_softmax_kernel<Tin, D><<<dim3(L.Hkv * sc.splits, L.n_seqs), kSmThreads, sm_smem, st>>>(L, s, sc);
+    if ((e0 = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess) return e0;
     decode_combine_kernel<Tin, D><<<dim3(L.Hq, L.n_seqs), D, 0, st>>>(L, sc, lambda, out);
     return cudaGetLastError();
 }

@@ -100,32 +100,6 @@ cudaError_t mark_stage(int i, cudaStream_t s) {
     return cudaSuccess;
 }
 
-// Per host thread and device: a side stream for the chunk-local GDN kernel,
-// which runs beside the softmax kernel (both depend only on the feature
-// path), and the events that fork it off the caller's stream and join it
-// back before the GDN state kernel.  Created on first use, kept for the
-// thread's lifetime.
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-constexpr int kMaxDevices = 64;
-thread_local SideStream t_side[kMaxDevices];
-
-cudaError_t side_stream(SideStream** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    SideStream& ss = t_side[dev];
-    if (!ss.s) {
-        if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-    }
-    *out = &ss;
-    return cudaSuccess;
-}
 
 #define HLA_TRY(...)                                           \
     do {                                                       \
@@ -170,7 +144,7 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
             SideStream* side = nullptr;
-            HLA_TRY(side_stream(&side));
+            HLA_TRY(side_stream(&side));  // per host thread and device; see hla_common.cuh
             HLA_TRY(cudaEventRecord(side->fork, stream));
             HLA_TRY(cudaStreamWaitEvent(side->s, side->fork, 0));
             HLA_TRY(mark_stage(3, side->s));
