@@ -74,8 +74,7 @@ constexpr uint32_t kColD1 = 0, kColD2 = 128, kColS = 256, kTmemCols = 512;
 
 // mbarrier indices
 constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kNumBars = 10;
-// record (all but M) + query, key rows (2 boxes each) + value slice
-constexpr uint32_t kLoadBytes = kRecVec + kRecVecBytes + 5 * 8192;
+constexpr uint32_t kLoadBytes = kRecordBytes + 5 * 8192;  // record + query, key rows (2 boxes each) + value slice
 
 __device__ __forceinline__ void st16(unsigned char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -280,7 +279,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             tma::bulk_load(buf + kA1 + 16384, rec + kRecWm + 8192, 8192, ld);    // key dims 64..127
             tma::bulk_load(buf + kTZP, rec + kRecTb, 8192, ld);
             tma::bulk_load(buf + kTZP + 16384, rec + kRecP, 8192, ld);
-            tma::bulk_load(buf + kVec, rec + kRecVec, kRecVecBytes, ld);
+            tma::bulk_load(buf + kVec, rec + kRecVec, kRecordBytes - kRecVec, ld);
             tma::tensor_load_3d(buf + kA1 + 8192, &map_q, 0, h, tok + W, ld);    // query rows (positions j + W)
             tma::tensor_load_3d(buf + kA1 + 16384 + 8192, &map_q, 64, h, tok + W, ld);
             tma::tensor_load_3d(buf + kK, &map_k, 0, kv, tok, ld);

@@ -11,12 +11,7 @@
 //                                          image (two 8 KB key-dim halves)
 //   T diag(beta), P                        64 x 64 images of the same kind (8 KB each)
 //   gamma[64], e^{G_63 - G}[64]            fp32
-//   M = [-Wm ; Q] (diag(e^{G'_63 - G'}) K')^T  128 x 64 fp16 K-major image, K', G'
-//                                          the keys and gate cumsum of the previous
-//                                          chunk (chunks c >= 1 of a sequence)
-// which the state kernel copies into shared memory unchanged.  M carries the
-// previous chunk's state update into this chunk's products (the state kernel
-// uses it to overlap consecutive chunks).
+// which the state kernel copies into shared memory unchanged.
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
@@ -32,19 +27,15 @@ namespace {
 constexpr int kC = 64, kD = 128, kThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kTmemCols = 128;               // Gram (64 columns), then Wm^T (128)
-constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major; later [-Wm ; Q]
+constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
+constexpr uint32_t kTbg = 8192;                   // T diag(beta gamma) image, over the first query block
 constexpr int kSA = 65;                           // row stride of A (odd: row-per-thread writes hit distinct banks)
 constexpr uint32_t kA32 = 32768;                  // A fp32 [64][kSA]
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68] (rows 16-byte aligned)
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
-constexpr uint32_t kKp = 73728;                   // previous chunk's key rows 64 x 128, K-major (B of M)
-constexpr uint32_t kVec = kKp + 16384;            // G (log2 units), beta, gamma, previous key decay
-constexpr uint32_t kMisc = kVec + 4 * 64 * 4;
-constexpr uint32_t kTbg = kA32;                   // T diag(beta gamma) over A once T is formed (rows 64..127 zero)
+constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta, gamma
+constexpr uint32_t kMisc = kVec + 3 * 64 * 4;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;
-
-// barrier of warps 2 and 3 (64 threads)
-__device__ __forceinline__ void named_sync_64() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
@@ -101,7 +92,6 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     float* sG = reinterpret_cast<float*>(sm + kVec);
     float* sBeta = sG + 64;
     float* sGam = sG + 128;
-    float* sKdp = sG + 192;  // key decay of the previous chunk
     uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
     float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
@@ -151,29 +141,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                      "l"(src), "r"(rr < nv ? 16u : 0u)
                      : "memory");
     }
-    const bool has_prev = c > 0;  // chunk c - 1 exists: M is formed
-    if (has_prev) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + kThreads * u, r = e >> 4, c8 = (e & 15) * 8;
-            const size_t t = (size_t)(start + j0 - kC + r);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                             umma::smem_addr(sm + kKp + umma::sw128_offset(r, c8, 64))),
-                         "l"(khat + (t * L.Hkv + kv) * kD + c8)
-                         : "memory");
-        }
-    }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    if (has_prev && warp >= 2) {  // the previous chunk's gate cumsum -> its key decay e^{G'_63 - G'_r}
-        const int r = tid - 64;
-        float gp = g[(size_t)(start + j0 - kC + r) * L.Hq + h] * 1.4426950408889634f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, gp, o);
-            if (lane >= o) gp += y;
-        }
-        sKdp[r] = gp;  // partial sums per warp; finished below
-    }
     float gi = 0.f;
     if (tid < kC) {
         const size_t t = (size_t)(start + j0 + tid);
@@ -193,14 +161,6 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     umma::fence_after_sync();
     if (tid >= 32 && tid < kC) gi += *carry;
     if (tid < kC) sG[tid] = gi;
-    if (has_prev && warp >= 2) {
-        const float part1 = sKdp[31];                    // total of the first 32 gates
-        const float gp = sKdp[tid - 64] + (warp == 3 ? part1 : 0.f);
-        const float total = sKdp[63] + part1;            // G'_63
-        __syncwarp();
-        named_sync_64();
-        sKdp[tid - 64] = exp2f(total - gp);
-    }
 
     // ---- Gram: D = [K; Q] K^T
     if (tid == 0) {
@@ -302,13 +262,10 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         const uint32_t off = umma::sw128_offset(r, c8, 64);
         *reinterpret_cast<uint4*>(rec + kRecTb + off) =
             make_uint4(pack_h2(tb[0], tb[1]), pack_h2(tb[2], tb[3]), pack_h2(tb[4], tb[5]), pack_h2(tb[6], tb[7]));
-        // T diag(beta gamma) over A (no longer needed); rows 64..127 of that operand are zero
+        // T diag(beta gamma) over the query rows of the stack (no longer needed)
         *reinterpret_cast<uint4*>(sm + kTbg + off) = make_uint4(
             pack_h2(tbg[0], tbg[1]), pack_h2(tbg[2], tbg[3]), pack_h2(tbg[4], tbg[5]), pack_h2(tbg[6], tbg[7]));
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(sm + kTbg + 8192 + 16 * (tid + kThreads * u)) = make_uint4(0, 0, 0, 0);
     umma::fence_async_smem();
     umma::fence_before_sync();
     __syncthreads();
@@ -331,7 +288,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         break;
     }
     umma::fence_after_sync();
-    if (warp < 2) {  // -Wm row r -> record image, and over the key rows of the stack: [-Wm ; Q]
+    if (warp < 2) {  // -Wm row r -> record image
         const int r = tid;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -340,55 +297,9 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float* x = wv + 8 * u;
-                const uint4 pk = make_uint4(pack_h2(-x[0], -x[1]), pack_h2(-x[2], -x[3]), pack_h2(-x[4], -x[5]),
-                                            pack_h2(-x[6], -x[7]));
-                *reinterpret_cast<uint4*>(rec + kRecWm + umma::sw128_offset(r, 32 * q4 + 8 * u, 64)) = pk;
-                *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(r, 32 * q4 + 8 * u, 128)) = pk;
-            }
-        }
-    }
-    if (has_prev) {  // previous chunk's key rows x its key decay (B of M)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int w = tid + kThreads * u;  // 16-byte chunk of a 64-row block: row (w mod 512) / 8
-            uint4 x = *reinterpret_cast<const uint4*>(sm + kKp + 16 * w);
-            const __half2 s2 = __float2half2_rn(sKdp[(w & 511) >> 3]);
-            __half2* hh = reinterpret_cast<__half2*>(&x);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) hh[e] = __hmul2(hh[e], s2);
-            *reinterpret_cast<uint4*>(sm + kKp + 16 * w) = x;
-        }
-    }
-    umma::fence_async_smem();
-    umma::fence_before_sync();
-    __syncthreads();
-
-    // ---- M = [-Wm ; Q] Kd'^T: M = 128, N = 64 tokens of the previous chunk, K = 128 key dims
-    if (has_prev) {
-        if (tid == 0) {
-            umma::fence_after_sync();
-            const uint32_t id = umma::idesc_f16(128, kC, false, false, false);
-#pragma unroll
-            for (int s16 = 0; s16 < kD / 16; ++s16)
-                umma::mma(tmem, umma::kmajor(sbase + kK, 128, s16), umma::kmajor(sbase + kKp, 64, s16), id, s16 > 0);
-            umma::commit(mbar);
-        }
-        const bool done_m = __syncthreads_and(umma::mbar_wait(mbar, phase, kWaitLimit));
-        phase ^= 1u;
-        if (!done_m) {
-            if (tid == 0 && err) atomicExch(err, kErrTimeout);
-            break;
-        }
-        umma::fence_after_sync();
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // row tid of M -> record image (K-major, 128 rows x 64)
-            float mv[32];
-            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * half, mv);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float* x = mv + 8 * u;
-                *reinterpret_cast<uint4*>(rec + kRecM + umma::sw128_offset(tid, 32 * half + 8 * u, 128)) =
-                    make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]), pack_h2(x[6], x[7]));
+                *reinterpret_cast<uint4*>(rec + kRecWm + umma::sw128_offset(r, 32 * q4 + 8 * u, 64)) =
+                    make_uint4(pack_h2(-x[0], -x[1]), pack_h2(-x[2], -x[3]), pack_h2(-x[4], -x[5]),
+                               pack_h2(-x[6], -x[7]));
             }
         }
     }
@@ -425,7 +336,7 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
             n_sm = 132;
     }
     const int64_t items = (int64_t)gdn_chunk_slots(L.total, L.n_seqs) * L.Hq;
-    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 2);
+    const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
     gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
     return cudaGetLastError();
 }

@@ -141,11 +141,9 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
 // Step 1 (parallel over chunks): chunk table (n_seqs + 1 entries) and, per
 // chunk and q-head, a record of kRecordBytes: -Wm = -T diag(beta gamma) K
 // (64 x 128), T diag(beta) and P (64 x 64) as fp16 swizzled K-major tile
-// images, then gamma and the key decay (fp32, 64 each), then (chunks c >= 1)
-// M = [-Wm ; Q] (diag(key decay') K')^T of the previous chunk's keys and decay.
+// images, then gamma and the key decay (fp32, 64 each).
 // Step 2: the state-carrying kernel.
-constexpr uint32_t kRecWm = 0, kRecTb = 16384, kRecP = 24576, kRecVec = 32768, kRecVecBytes = 512,
-                   kRecM = 33280, kRecordBytes = 49664;
+constexpr uint32_t kRecWm = 0, kRecTb = 16384, kRecP = 24576, kRecVec = 32768, kRecordBytes = 33280;
 size_t gdn_chunk_slots(int64_t total, int n_seqs);
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
                                const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
