@@ -38,68 +38,234 @@ cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse,
     return cudaGetLastError();
 }
 
-constexpr int kTT = 32;                   // output tokens per CTA
-constexpr int kRowsPerCta = 4;            // feature rows (q, k or v heads) per CTA
-constexpr int kStage = kTT + kConvHalo;   // staged tokens: 7 of conv history, then the outputs
-constexpr int kFeatThreads = 128;
+constexpr int kTT = 64;           // output tokens per warp
+constexpr int kFeatWarps = 4;     // feature rows (q, k or v heads) per CTA, one per warp
+constexpr int kBlk = 8;           // tokens per unrolled step = conv width (the window is a ring of 8)
+constexpr int kRing = 4;          // steps of input rows in flight per warp (shared-memory ring)
 
-template <typename T> struct Vec8;  // eight elements as one or two 16-byte words
-template <> struct Vec8<__nv_bfloat16> {
-    static constexpr int kChunks = 1;
-    __device__ static void unpack(const unsigned char* p, float* x) {
-        const uint4 v = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-            x[2 * i] = f.x; x[2 * i + 1] = f.y;
-        }
+// NP consecutive elements of one lane, as fp32 (loads of the layer's input
+// type, stores and rounding of the feature type).
+template <typename T, int NP> struct LaneIO;
+template <> struct LaneIO<__nv_bfloat16, 2> {
+    __device__ static void read(const __nv_bfloat16* p, float* x) {  // shared memory
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        x[0] = f.x; x[1] = f.y;
     }
 };
-template <> struct Vec8<__half> {
-    static constexpr int kChunks = 1;
-    __device__ static void unpack(const unsigned char* p, float* x) {
-        const uint4 v = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-            x[2 * i] = f.x; x[2 * i + 1] = f.y;
-        }
+template <> struct LaneIO<__nv_bfloat16, 1> {
+    __device__ static void read(const __nv_bfloat16* p, float* x) { x[0] = __bfloat162float(*p); }
+};
+template <> struct LaneIO<float, 2> {
+    __device__ static void read(const float* p, float* x) {
+        const float2 f = *reinterpret_cast<const float2*>(p);
+        x[0] = f.x; x[1] = f.y;
     }
-    __device__ static void pack(unsigned char* p, const float* x) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    __device__ static void store(float* p, const float* x) { *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]); }
+    __device__ static void round(float*) {}
+};
+template <> struct LaneIO<float, 1> {
+    __device__ static void read(const float* p, float* x) { x[0] = *p; }
+    __device__ static void store(float* p, const float* x) { *p = x[0]; }
+    __device__ static void round(float*) {}
+};
+template <> struct LaneIO<__half, 2> {
+    __device__ static void store(__half* p, const float* x) {
+        *reinterpret_cast<__half2*>(p) = __floats2half2_rn(x[0], x[1]);
+    }
+    __device__ static void round(float* x) {
+        const float2 f = __half22float2(__floats2half2_rn(x[0], x[1]));
+        x[0] = f.x; x[1] = f.y;
     }
 };
-template <> struct Vec8<float> {
-    static constexpr int kChunks = 2;
-    __device__ static void unpack(const unsigned char* p, float* x) {
-        const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 16);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    }
-    __device__ static void pack(unsigned char* p, const float* x) {
-        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(p + 16) = make_float4(x[4], x[5], x[6], x[7]);
-    }
+template <> struct LaneIO<__half, 1> {
+    __device__ static void store(__half* p, const float* x) { *p = __float2half_rn(x[0]); }
+    __device__ static void round(float* x) { x[0] = __half2float(__float2half_rn(x[0])); }
 };
 
-// One CTA = kTT tokens x kRowsPerCta feature rows (q heads, then k heads,
-// then v heads, in that order across the grid).  The rows of the kTT tokens
-// and their 7 predecessors are staged in shared memory, rotated there in
-// place (RoPE on q and k; cos/sin from the fine and coarse tables by angle
-// addition, both reduced in double precision) and written out as the RoPE'd
-// q and k; then one thread per (token, row, 8 channels) runs the width-8
-// causal conv over the staged rows with its 64 weights held in registers,
-// and the D / 8 lanes of a row finish the L2 norm with shuffles.  Conv taps
-// before a sequence's first token read as zero.
+// Per-warp state of one feature row (see features_kernel).
 template <typename Tin, typename Tf, int D>
-__global__ void __launch_bounds__(kFeatThreads, 4)
+struct FeatRow {
+    static constexpr int NP = D / 64, HALF = D / 2, NC = 2 * NP;  // RoPE pairs and channels per lane
+    const float2* fine;
+    const float2* coarse;
+    Tf* rot;       // RoPE'd rows (q and k), lane's first pair already added
+    Tf* hat;       // conv (+ norm) rows, lane offset added
+    size_t rowstride;  // elements between consecutive tokens of one head
+    float w[NC][kConvWidth];
+    float ring[kBlk][NC];
+};
+
+// Eight tokens t_first .. + 7 of one step, the inputs read from the warp's
+// shared-memory slot `rows` (lane offset added).  CHECK = false is the fast
+// path: every token has a position p0 + u >= 7 in one sequence and lies
+// inside the tensor, so the step is straight-line code the compiler can
+// interleave across tokens; CHECK = true tracks sequences token by token,
+// masks the conv taps before a sequence's first token and skips the outputs
+// of tokens outside every sequence.  OUT = false only fills the ring.
+template <typename Tin, typename Tf, int D, bool ROPE, bool NORM, bool CHECK, bool OUT>
+__device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* rows, int64_t t_first, int p0,
+                                          const LayerDims& L, const int32_t* cu, int& s, int64_t& s_start,
+                                          int64_t& s_len, int32_t* err, int lane) {
+    using Row = FeatRow<Tin, Tf, D>;
+    constexpr int NP = Row::NP, HALF = Row::HALF, NC = Row::NC;
+    using In = LaneIO<Tin, NP>;
+    using Out = LaneIO<Tf, NP>;
+#pragma unroll
+    for (int u = 0; u < kBlk; ++u) {
+        const int64_t t = t_first + u;
+        int p = p0 + u;
+        if constexpr (CHECK) {  // position in its sequence (-1: outside every sequence); warp-uniform
+            p = -1;
+            if (t >= 0 && t < L.total) {
+                while (t >= s_start + s_len && s + 1 < L.n_seqs) {
+                    ++s;
+                    seq_range(cu, s, L.total, &s_start, &s_len);
+                }
+                if (t >= s_start && t < s_start + s_len) p = (int)(t - s_start);
+                else if (err && blockIdx.y == 0 && lane == 0) atomicExch(err, kErrSeqlens);
+            }
+        }
+        float x[NC];
+        In::read(rows + u * D, x);
+        In::read(rows + u * D + HALF, x + NP);
+        if constexpr (ROPE) {
+            if (!CHECK || p >= 0) {
+                float2 f[NP], g[NP];
+                if constexpr (NP == 2) {  // both pairs' table entries in one 16-byte load per table
+                    const float4 fa = __ldg(reinterpret_cast<const float4*>(fr.fine + (p & 63) * HALF + 2 * lane));
+                    const float4 ga = __ldg(reinterpret_cast<const float4*>(fr.coarse + (p >> 6) * HALF + 2 * lane));
+                    f[0] = make_float2(fa.x, fa.y); f[1] = make_float2(fa.z, fa.w);
+                    g[0] = make_float2(ga.x, ga.y); g[1] = make_float2(ga.z, ga.w);
+                } else {
+                    f[0] = __ldg(fr.fine + (p & 63) * HALF + lane);
+                    g[0] = __ldg(fr.coarse + (p >> 6) * HALF + lane);
+                }
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    const float cs = g[c].x * f[c].x - g[c].y * f[c].y, sn = g[c].y * f[c].x + g[c].x * f[c].y;
+                    const float a = x[c], b = x[NP + c];
+                    x[c] = a * cs - b * sn;
+                    x[NP + c] = b * cs + a * sn;
+                }
+            }
+        }
+        Out::round(x);
+        Out::round(x + NP);
+        const bool out_tok = OUT && (!CHECK || (t < L.total && p >= 0));
+        if constexpr (ROPE && OUT) {
+            if (out_tok) {
+                Tf* dst = fr.rot + (size_t)t * fr.rowstride;
+                Out::store(dst, x);
+                Out::store(dst + HALF, x + NP);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < NC; ++c) fr.ring[u][c] = x[c];
+        if constexpr (OUT) {
+            // tap m reads token t - 7 + m (ring slot (u + 1 + m) mod 8); none before the sequence start
+            float y[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) y[c] = 0.f;
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) {
+                if (CHECK && m < kConvHalo - p) continue;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) y[c] = fmaf(fr.w[c][m], fr.ring[(u + 1 + m) & (kBlk - 1)][c], y[c]);
+            }
+            if constexpr (NORM) {
+                float ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) ss = fmaf(y[c], y[c], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float rs = rsqrtf(ss + 1e-6f);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) y[c] *= rs;
+            }
+            if (out_tok) {
+                Tf* dst = fr.hat + (size_t)t * fr.rowstride;
+                Out::store(dst, y);
+                Out::store(dst + HALF, y + NP);
+            }
+        }
+    }
+}
+
+// One warp = one feature row (a q, k or v head) over kTT tokens, streamed in
+// token order.  Lane l owns the RoPE pairs i = NP l .. NP l + NP - 1 (channels
+// i and D/2 + i), so every token row is read and written as coalesced lines
+// and the rotation needs no exchange.  Each token is rotated (q and k; cos/sin
+// from the fine and coarse tables by angle addition, both reduced in double
+// precision), rounded to the feature type and written out as the RoPE'd row,
+// then enters a ring of the last 8 inputs held in registers; the width-8
+// causal conv of the token is 8 FMAs per channel over the ring, and the L2
+// norm a warp reduction.  The warp starts 8 tokens early to fill the ring;
+// taps before a sequence's first token read as zero.  Input rows arrive by
+// cp.async in steps of 8 tokens, kRing steps in flight per warp, each warp
+// with its own slice of shared memory (no CTA-wide barrier).
+template <typename Tin, typename Tf, int D, bool ROPE, bool NORM>
+__device__ __forceinline__ void feat_row(FeatRow<Tin, Tf, D>& fr, const Tin* src, unsigned char* wring, int64_t tb,
+                                         const LayerDims& L, const int32_t* cu, int32_t* err, int lane) {
+    constexpr int ROWB = D * (int)sizeof(Tin), STEPB = kBlk * ROWB, CPT = ROWB / 16;  // 16-byte chunks per row
+    constexpr int kSteps = kTT / kBlk + 1;  // the first step only fills the ring
+    constexpr int NP = FeatRow<Tin, Tf, D>::NP;
+    const size_t H = fr.rowstride / D;
+    // sequence of the first token the warp touches (positions advance by one per token)
+    int s = seq_of_token(cu, L.n_seqs, tb < 0 ? 0 : tb);
+    int64_t s_start, s_len;
+    seq_range(cu, s, L.total, &s_start, &s_len);
+
+    // the rows of step `st` into ring slot st % kRing, one commit group per step (empty past the end)
+    auto issue = [&](int st) {
+        if (st < kSteps) {
+            unsigned char* dst = wring + (size_t)(st % kRing) * STEPB;
+#pragma unroll
+            for (int e = lane; e < kBlk * CPT; e += 32) {
+                const int u = e / CPT, ch = e % CPT;
+                const int64_t t = tb + (int64_t)kBlk * st + u;
+                const bool in = t >= 0 && t < L.total;
+                const Tin* gp = src + (size_t)(in ? t : 0) * H * D + ch * (16 / (int)sizeof(Tin));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                 (uint32_t)__cvta_generic_to_shared(dst + u * ROWB + ch * 16)),
+                             "l"(gp), "r"(in ? 16u : 0u)
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int st = 0; st < kRing - 1; ++st) issue(st);
+
+#pragma unroll 1
+    for (int step = 0; step < kSteps; ++step) {
+        const int64_t t_first = tb + (int64_t)kBlk * step;
+        issue(step + kRing - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+        __syncwarp();
+        const Tin* rows = reinterpret_cast<const Tin*>(wring + (size_t)(step % kRing) * STEPB) + NP * lane;
+        if (step == 0) {
+            feat_step<Tin, Tf, D, ROPE, NORM, true, false>(fr, rows, t_first, 0, L, cu, s, s_start, s_len, err, lane);
+        } else {
+            // the step's sequence: advance past sequences that end before it
+            while (t_first >= s_start + s_len && s + 1 < L.n_seqs) {
+                ++s;
+                seq_range(cu, s, L.total, &s_start, &s_len);
+            }
+            const bool fast = t_first >= s_start + kConvHalo && t_first + kBlk <= s_start + s_len &&
+                              t_first + kBlk <= L.total;
+            if (fast)
+                feat_step<Tin, Tf, D, ROPE, NORM, false, true>(fr, rows, t_first, (int)(t_first - s_start), L, cu, s,
+                                                               s_start, s_len, err, lane);
+            else
+                feat_step<Tin, Tf, D, ROPE, NORM, true, true>(fr, rows, t_first, 0, L, cu, s, s_start, s_len, err,
+                                                              lane);
+        }
+        __syncwarp();  // the slot is refilled by the next step's issue
+    }
+}
+
+template <typename Tin, typename Tf, int D>
+__global__ void __launch_bounds__(32 * kFeatWarps, 4)
 features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
                 const Tin* __restrict__ v, const float* __restrict__ wq,
                 const float* __restrict__ wk, const float* __restrict__ wv,
@@ -107,137 +273,50 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
                 const float2* __restrict__ coarse, Tf* __restrict__ qr, Tf* __restrict__ kr,
                 Tf* __restrict__ qhat, Tf* __restrict__ khat, Tf* __restrict__ vhat,
                 int32_t* __restrict__ err) {
-    static_assert(sizeof(Tin) == sizeof(Tf), "rows are rotated in place");
-    constexpr int HALF = D / 2, G8 = D / 8, E = (int)sizeof(Tin);
-    constexpr int ROWB = D * E;                                     // bytes per staged row
-    constexpr int CH = 16 / E;                                      // elements per 16-byte chunk
-    extern __shared__ __align__(16) unsigned char xs[];             // [kStage tokens][kRowsPerCta][D]
-    __shared__ int pos_s[kStage];
-    const int tid = threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.x * kTT;
-    const int n_rows = L.Hq + 2 * L.Hkv;
-
-    // row j of this CTA: kind (0 q, 1 k, 2 v), head, and whether it exists
-    auto row_info = [&](int j, int* kind, int* head) {
-        int hr = blockIdx.y * kRowsPerCta + j;
-        const bool on = hr < n_rows;
-        if (!on) hr = n_rows - 1;
-        *kind = 0;
-        if (hr >= L.Hq + L.Hkv) { *kind = 2; hr -= L.Hq + L.Hkv; }
-        else if (hr >= L.Hq) { *kind = 1; hr -= L.Hq; }
-        *head = hr;
-        return on;
-    };
-
-    // ---- stage the rows (zeros outside the token range)
-    for (int idx = tid; idx < kStage * kRowsPerCta * (ROWB / 16); idx += kFeatThreads) {
-        const int chunk = idx % (ROWB / 16), rj = idx / (ROWB / 16), j = rj % kRowsPerCta, tk = rj / kRowsPerCta;
-        int kind, head;
-        const bool on = row_info(j, &kind, &head);
-        const int64_t t = t0 - kConvHalo + tk;
-        const bool in = on && t >= 0 && t < L.total;
-        const Tin* src = kind == 0 ? q : (kind == 1 ? k : v);
-        const size_t H = kind == 0 ? L.Hq : L.Hkv;
-        const Tin* gp = src + ((size_t)(in ? t : 0) * H + head) * D + chunk * CH;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                         (uint32_t)__cvta_generic_to_shared(xs + (size_t)rj * ROWB + chunk * 16)),
-                     "l"(gp), "r"(in ? 16u : 0u)
-                     : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    if (tid < kStage) {  // position of each staged token inside its sequence (-1: none)
-        const int64_t t = t0 - kConvHalo + tid;
-        int p = -1;
-        if (t >= 0 && t < L.total) {
-            const int s = seq_of_token(cu, L.n_seqs, t);
-            int64_t start, len;
-            seq_range(cu, s, L.total, &start, &len);
-            if (t >= start && t < start + len) p = (int)(t - start);
-            else if (err && blockIdx.y == 0) atomicExch(err, kErrSeqlens);
-        }
-        pos_s[tid] = p;
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-
-    // ---- RoPE in place on q and k rows (bf16 -> fp16 or fp32 -> fp32), RoPE'd rows out
-    for (int idx = tid; idx < kStage * kRowsPerCta * (HALF / 8); idx += kFeatThreads) {
-        const int f8 = idx % (HALF / 8), rj = idx / (HALF / 8), j = rj % kRowsPerCta, tk = rj / kRowsPerCta;
-        int kind, head;
-        const bool on = row_info(j, &kind, &head);
-        unsigned char* r = xs + (size_t)rj * ROWB;
-        float x1[8], x2[8];
-        Vec8<Tin>::unpack(r + f8 * 8 * E, x1);
-        Vec8<Tin>::unpack(r + (HALF + f8 * 8) * E, x2);
-        const int p = pos_s[tk];
-        if (kind != 2 && p >= 0) {
-            const float2* fp = fine + (p & 63) * HALF + f8 * 8;
-            const float2* gp = coarse + (p >> 6) * HALF + f8 * 8;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 f = __ldg(fp + i), g = __ldg(gp + i);
-                const float c = g.x * f.x - g.y * f.y, sn = g.y * f.x + g.x * f.y;
-                const float a = x1[i], b = x2[i];
-                x1[i] = a * c - b * sn;
-                x2[i] = b * c + a * sn;
-            }
-        }
-        Vec8<Tf>::pack(r + f8 * 8 * E, x1);
-        Vec8<Tf>::pack(r + (HALF + f8 * 8) * E, x2);
-        const int64_t t = t0 - kConvHalo + tk;
-        if (on && kind != 2 && tk >= kConvHalo && t < L.total) {
-            Tf* dst = (kind == 0 ? qr : kr) + ((size_t)t * (kind == 0 ? L.Hq : L.Hkv) + head) * D;
-            Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(dst + f8 * 8), x1);
-            Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(dst + HALF + f8 * 8), x2);
-        }
-    }
-    __syncthreads();
-
-    // ---- causal conv (tap m reads token t - 7 + m) and L2 norm; a thread keeps one (row, 8 channels)
-    static_assert((kFeatThreads % (kRowsPerCta * G8)) == 0, "a thread keeps its row and channels");
-    const int cg = tid % G8, j = (tid / G8) % kRowsPerCta;
-    int kind, head;
-    const bool on = row_info(j, &kind, &head);
-    const bool do_norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));
-    float wt[8][kConvWidth];
-    {
-        const float4* wp = reinterpret_cast<const float4*>((kind == 0 ? wq : (kind == 1 ? wk : wv)) +
-                                                           ((size_t)head * D + cg * 8) * kConvWidth);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float4 a = __ldg(wp + 2 * c), b = __ldg(wp + 2 * c + 1);
-            wt[c][0] = a.x; wt[c][1] = a.y; wt[c][2] = a.z; wt[c][3] = a.w;
-            wt[c][4] = b.x; wt[c][5] = b.y; wt[c][6] = b.z; wt[c][7] = b.w;
-        }
-    }
-    Tf* hat = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + cg * 8;
+    using Row = FeatRow<Tin, Tf, D>;
+    constexpr int NP = Row::NP, HALF = Row::HALF, NC = Row::NC;
+    constexpr int STEPB = kBlk * D * (int)sizeof(Tin);
+    extern __shared__ __align__(16) unsigned char ring_s[];  // [warp][kRing][kBlk tokens][D]
+    const int lane = threadIdx.x & 31;
+    unsigned char* wring = ring_s + (size_t)(threadIdx.x >> 5) * kRing * STEPB;
+    int hr = blockIdx.y * kFeatWarps + (threadIdx.x >> 5);
+    if (hr >= L.Hq + 2 * L.Hkv) return;  // whole warp; no CTA-wide barrier below
+    int kind = 0;
+    if (hr >= L.Hq + L.Hkv) { kind = 2; hr -= L.Hq + L.Hkv; }
+    else if (hr >= L.Hq) { kind = 1; hr -= L.Hq; }
+    const int head = hr;
     const size_t H = kind == 0 ? L.Hq : L.Hkv;
-    constexpr int kTokStep = kFeatThreads / (kRowsPerCta * G8);
-#pragma unroll 1
-    for (int to = tid / (kRowsPerCta * G8); to < kTT; to += kTokStep) {
-        const int64_t t = t0 + to;
-        const int p = pos_s[to + kConvHalo];
-        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const Tin* src = (kind == 0 ? q : (kind == 1 ? k : v)) + (size_t)head * D;
+
+    Row fr;
+    fr.fine = fine;
+    fr.coarse = coarse;
+    fr.rowstride = H * D;
+    fr.rot = (kind == 0 ? qr : kr) + (size_t)head * D + NP * lane;
+    fr.hat = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + NP * lane;
+    {  // conv weights of the lane's channels: c < NP -> channel NP lane + c, else HALF + NP lane + c - NP
+        const float* wb = (kind == 0 ? wq : (kind == 1 ? wk : wv)) + (size_t)head * D * kConvWidth;
 #pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) {
-            if (m < kConvHalo - p) continue;  // before the sequence's first token (p < 0: none)
-            float x[8];
-            Vec8<Tf>::unpack(xs + ((size_t)(to + m) * kRowsPerCta + j) * ROWB + cg * 8 * E, x);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][m], x[c], y[c]);
+        for (int c = 0; c < NC; ++c) {
+            const int ch = (c < NP ? 0 : HALF) + NP * lane + (c % NP);
+            const float4 a = __ldg(reinterpret_cast<const float4*>(wb + (size_t)ch * kConvWidth));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(wb + (size_t)ch * kConvWidth + 4));
+            fr.w[c][0] = a.x; fr.w[c][1] = a.y; fr.w[c][2] = a.z; fr.w[c][3] = a.w;
+            fr.w[c][4] = b.x; fr.w[c][5] = b.y; fr.w[c][6] = b.z; fr.w[c][7] = b.w;
         }
-        float ss = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
-#pragma unroll
-        for (int o = G8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (do_norm) {
-            const float rs = rsqrtf(ss + 1e-6f);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) y[c] *= rs;
-        }
-        if (on && t < L.total && p >= 0) Vec8<Tf>::pack(reinterpret_cast<unsigned char*>(hat + (size_t)t * H * D), y);
     }
+#pragma unroll
+    for (int u = 0; u < kBlk; ++u)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) fr.ring[u][c] = 0.f;
+
+    const int64_t tb = (int64_t)blockIdx.x * kTT - kBlk;
+    if (kind == 2)
+        feat_row<Tin, Tf, D, false, false>(fr, src, wring, tb, L, cu, err, lane);
+    else if (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q))
+        feat_row<Tin, Tf, D, true, true>(fr, src, wring, tb, L, cu, err, lane);
+    else
+        feat_row<Tin, Tf, D, true, false>(fr, src, wring, tb, L, cu, err, lane);
 }
 
 template <typename Tin, typename Tf>
@@ -245,22 +324,22 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float* wq, const float* wk, const float* wv, const int32_t* cu,
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st) {
-    dim3 grid((unsigned)((L.total + kTT - 1) / kTT), (unsigned)((L.Hq + 2 * L.Hkv + kRowsPerCta - 1) / kRowsPerCta));
     if (L.total <= 0) return cudaSuccess;
-    const size_t smem = (size_t)kStage * kRowsPerCta * L.d * sizeof(Tin);
+    dim3 grid((unsigned)((L.total + kTT - 1) / kTT), (unsigned)((L.Hq + 2 * L.Hkv + kFeatWarps - 1) / kFeatWarps));
+    const size_t smem = (size_t)kFeatWarps * kRing * kBlk * L.d * sizeof(Tin);
     if (L.d == 128) {
-        static bool configured = false;
+        static bool configured = false;  // the attribute is per instantiation
         if (!configured) {
             cudaError_t e = cudaFuncSetAttribute(features_kernel<Tin, Tf, 128>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             configured = true;
         }
-        features_kernel<Tin, Tf, 128><<<grid, kFeatThreads, smem, st>>>(
-            L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err);
+        features_kernel<Tin, Tf, 128><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse,
+                                                                             qr, kr, qhat, khat, vhat, err);
     } else {
-        features_kernel<Tin, Tf, 64><<<grid, kFeatThreads, smem, st>>>(
-            L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err);
+        features_kernel<Tin, Tf, 64><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse,
+                                                                            qr, kr, qhat, khat, vhat, err);
     }
     return cudaGetLastError();
 }
