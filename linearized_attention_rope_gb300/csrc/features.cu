@@ -93,6 +93,7 @@ struct FeatRow {
     size_t rowstride;  // elements between consecutive tokens of one head
     float w[NC][kConvWidth];
     float ring[kBlk][NC];
+    float2 step1[NP];  // (cos, sin) of one position step for the lane's pairs
 };
 
 // Eight tokens t_first .. + 7 of one step, the inputs read from the warp's
@@ -110,6 +111,7 @@ __device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* ro
     constexpr int NP = Row::NP, HALF = Row::HALF, NC = Row::NC;
     using In = LaneIO<Tin, NP>;
     using Out = LaneIO<Tf, NP>;
+    float2 cs_run[NP];  // fast path: (cos, sin) at p0 + u, advanced by one position step per token
 #pragma unroll
     for (int u = 0; u < kBlk; ++u) {
         const int64_t t = t_first + u;
@@ -130,22 +132,33 @@ __device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* ro
         In::read(rows + u * D + HALF, x + NP);
         if constexpr (ROPE) {
             if (!CHECK || p >= 0) {
-                float2 f[NP], g[NP];
-                if constexpr (NP == 2) {  // both pairs' table entries in one 16-byte load per table
-                    const float4 fa = __ldg(reinterpret_cast<const float4*>(fr.fine + (p & 63) * HALF + 2 * lane));
-                    const float4 ga = __ldg(reinterpret_cast<const float4*>(fr.coarse + (p >> 6) * HALF + 2 * lane));
-                    f[0] = make_float2(fa.x, fa.y); f[1] = make_float2(fa.z, fa.w);
-                    g[0] = make_float2(ga.x, ga.y); g[1] = make_float2(ga.z, ga.w);
-                } else {
-                    f[0] = __ldg(fr.fine + (p & 63) * HALF + lane);
-                    g[0] = __ldg(fr.coarse + (p >> 6) * HALF + lane);
+                float2 csn[NP];
+                if (CHECK || u == 0) {  // from the tables (angle addition of two reduced entries)
+                    float2 f[NP], g[NP];
+                    if constexpr (NP == 2) {  // both pairs' table entries in one 16-byte load per table
+                        const float4 fa = __ldg(reinterpret_cast<const float4*>(fr.fine + (p & 63) * HALF + 2 * lane));
+                        const float4 ga = __ldg(reinterpret_cast<const float4*>(fr.coarse + (p >> 6) * HALF + 2 * lane));
+                        f[0] = make_float2(fa.x, fa.y); f[1] = make_float2(fa.z, fa.w);
+                        g[0] = make_float2(ga.x, ga.y); g[1] = make_float2(ga.z, ga.w);
+                    } else {
+                        f[0] = __ldg(fr.fine + (p & 63) * HALF + lane);
+                        g[0] = __ldg(fr.coarse + (p >> 6) * HALF + lane);
+                    }
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        csn[c] = make_float2(g[c].x * f[c].x - g[c].y * f[c].y, g[c].y * f[c].x + g[c].x * f[c].y);
+                } else {  // the previous token's angle plus one step (at most 7 steps from a table value)
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        csn[c] = make_float2(cs_run[c].x * fr.step1[c].x - cs_run[c].y * fr.step1[c].y,
+                                             cs_run[c].y * fr.step1[c].x + cs_run[c].x * fr.step1[c].y);
                 }
 #pragma unroll
                 for (int c = 0; c < NP; ++c) {
-                    const float cs = g[c].x * f[c].x - g[c].y * f[c].y, sn = g[c].y * f[c].x + g[c].x * f[c].y;
+                    cs_run[c] = csn[c];
                     const float a = x[c], b = x[NP + c];
-                    x[c] = a * cs - b * sn;
-                    x[NP + c] = b * cs + a * sn;
+                    x[c] = a * csn[c].x - b * csn[c].y;
+                    x[NP + c] = b * csn[c].x + a * csn[c].y;
                 }
             }
         }
@@ -291,6 +304,8 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
     Row fr;
     fr.fine = fine;
     fr.coarse = coarse;
+#pragma unroll
+    for (int c = 0; c < NP; ++c) fr.step1[c] = __ldg(fine + HALF + NP * lane + c);  // angle of position 1
     fr.rowstride = H * D;
     fr.rot = (kind == 0 ? qr : kr) + (size_t)head * D + NP * lane;
     fr.hat = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + NP * lane;
