@@ -4,6 +4,8 @@
 // item 3 (a kernel-8 short convolution after RoPE and before L2
 // normalisation).  The RoPE'd q and k are also written out: the exact
 // softmax branch reads them (frozen-backbone attention).
+#include <algorithm>
+
 #include "hla_common.cuh"
 
 namespace hla {
@@ -38,7 +40,6 @@ cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse,
     return cudaGetLastError();
 }
 
-constexpr int kTT = 64;           // output tokens per warp
 constexpr int kFeatWarps = 4;     // feature rows (q, k or v heads) per CTA, one per warp
 constexpr int kBlk = 8;           // tokens per unrolled step = conv width (the window is a ring of 8)
 constexpr int kRing = 4;          // steps of input rows in flight per warp (shared-memory ring)
@@ -204,8 +205,9 @@ __device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* ro
     }
 }
 
-// One warp = one feature row (a q, k or v head) over kTT tokens, streamed in
-// token order.  Lane l owns the RoPE pairs i = NP l .. NP l + NP - 1 (channels
+// One warp = one feature row (a q, k or v head) over a span of `span` tokens
+// (a multiple of 8, chosen by the launcher so the grid is one wave), streamed
+// in token order.  Lane l owns the RoPE pairs i = NP l .. NP l + NP - 1 (channels
 // i and D/2 + i), so every token row is read and written as coalesced lines
 // and the rotation needs no exchange.  Each token is rotated (q and k; cos/sin
 // from the fine and coarse tables by angle addition, both reduced in double
@@ -218,9 +220,9 @@ __device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* ro
 // with its own slice of shared memory (no CTA-wide barrier).
 template <typename Tin, typename Tf, int D, bool ROPE, bool NORM>
 __device__ __forceinline__ void feat_row(FeatRow<Tin, Tf, D>& fr, const Tin* src, unsigned char* wring, int64_t tb,
-                                         const LayerDims& L, const int32_t* cu, int32_t* err, int lane) {
+                                         int span, const LayerDims& L, const int32_t* cu, int32_t* err, int lane) {
     constexpr int ROWB = D * (int)sizeof(Tin), STEPB = kBlk * ROWB, CPT = ROWB / 16;  // 16-byte chunks per row
-    constexpr int kSteps = kTT / kBlk + 1;  // the first step only fills the ring
+    const int kSteps = span / kBlk + 1;  // the first step only fills the ring
     constexpr int NP = FeatRow<Tin, Tf, D>::NP;
     const size_t H = fr.rowstride / D;
     // sequence of the first token the warp touches (positions advance by one per token)
@@ -285,7 +287,7 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
                 const int32_t* __restrict__ cu, const float2* __restrict__ fine,
                 const float2* __restrict__ coarse, Tf* __restrict__ qr, Tf* __restrict__ kr,
                 Tf* __restrict__ qhat, Tf* __restrict__ khat, Tf* __restrict__ vhat,
-                int32_t* __restrict__ err) {
+                int32_t* __restrict__ err, int span) {
     using Row = FeatRow<Tin, Tf, D>;
     constexpr int NP = Row::NP, HALF = Row::HALF, NC = Row::NC;
     constexpr int STEPB = kBlk * D * (int)sizeof(Tin);
@@ -325,13 +327,48 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
 #pragma unroll
         for (int c = 0; c < NC; ++c) fr.ring[u][c] = 0.f;
 
-    const int64_t tb = (int64_t)blockIdx.x * kTT - kBlk;
+    const int64_t tb = (int64_t)blockIdx.x * span - kBlk;
     if (kind == 2)
-        feat_row<Tin, Tf, D, false, false>(fr, src, wring, tb, L, cu, err, lane);
+        feat_row<Tin, Tf, D, false, false>(fr, src, wring, tb, span, L, cu, err, lane);
     else if (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q))
-        feat_row<Tin, Tf, D, true, true>(fr, src, wring, tb, L, cu, err, lane);
+        feat_row<Tin, Tf, D, true, true>(fr, src, wring, tb, span, L, cu, err, lane);
     else
-        feat_row<Tin, Tf, D, true, false>(fr, src, wring, tb, L, cu, err, lane);
+        feat_row<Tin, Tf, D, true, false>(fr, src, wring, tb, span, L, cu, err, lane);
+}
+
+// Token span per warp: the smallest multiple of 8 for which the whole grid
+// (row groups x spans CTAs) fits in one wave of resident CTAs.
+static int64_t feature_span(int64_t total, int row_groups, int resident_ctas) {
+    const int64_t spans = std::max<int64_t>(1, resident_ctas / std::max(1, row_groups));
+    const int64_t span = (total + spans - 1) / spans;
+    return std::max<int64_t>(kBlk, (span + kBlk - 1) / kBlk * kBlk);
+}
+
+template <typename Tin, typename Tf, int D>
+static cudaError_t launch_features_d(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v, const float* wq,
+                                     const float* wk, const float* wv, const int32_t* cu, const float2* fine,
+                                     const float2* coarse, Tf* qr, Tf* kr, Tf* qhat, Tf* khat, Tf* vhat,
+                                     int32_t* err, cudaStream_t st) {
+    const size_t smem = (size_t)kFeatWarps * kRing * kBlk * D * sizeof(Tin);
+    static int resident = 0;  // CTAs resident on the device at once (per instantiation)
+    if (!resident) {
+        cudaError_t e = cudaFuncSetAttribute(features_kernel<Tin, Tf, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        int dev = 0, n_sm = 0, per_sm = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, features_kernel<Tin, Tf, D>, 32 * kFeatWarps,
+                                                              smem);
+        if (e != cudaSuccess) return e;
+        resident = std::max(1, n_sm * std::max(1, per_sm));
+    }
+    const int row_groups = (L.Hq + 2 * L.Hkv + kFeatWarps - 1) / kFeatWarps;
+    const int64_t span = feature_span(L.total, row_groups, resident);
+    dim3 grid((unsigned)((L.total + span - 1) / span), (unsigned)row_groups);
+    features_kernel<Tin, Tf, D><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr,
+                                                                       kr, qhat, khat, vhat, err, (int)span);
+    return cudaGetLastError();
 }
 
 template <typename Tin, typename Tf>
@@ -340,23 +377,11 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st) {
     if (L.total <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((L.total + kTT - 1) / kTT), (unsigned)((L.Hq + 2 * L.Hkv + kFeatWarps - 1) / kFeatWarps));
-    const size_t smem = (size_t)kFeatWarps * kRing * kBlk * L.d * sizeof(Tin);
-    if (L.d == 128) {
-        static bool configured = false;  // the attribute is per instantiation
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(features_kernel<Tin, Tf, 128>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            configured = true;
-        }
-        features_kernel<Tin, Tf, 128><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse,
-                                                                             qr, kr, qhat, khat, vhat, err);
-    } else {
-        features_kernel<Tin, Tf, 64><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse,
-                                                                            qr, kr, qhat, khat, vhat, err);
-    }
-    return cudaGetLastError();
+    if (L.d == 128)
+        return launch_features_d<Tin, Tf, 128>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat,
+                                               err, st);
+    return launch_features_d<Tin, Tf, 64>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err,
+                                          st);
 }
 
 template cudaError_t launch_features<float, float>(const LayerDims&, const float*, const float*,
