@@ -119,9 +119,10 @@ __device__ __forceinline__ uint64_t mnstep(int s) { return (uint64_t)(s * 128); 
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ cu,
-                   const int32_t* __restrict__ chunk_base, const unsigned char* __restrict__ rec_in,
-                   const __half* __restrict__ o_sm, const float* __restrict__ lambda,
-                   __nv_bfloat16* __restrict__ out, float* __restrict__ S_out, int32_t* __restrict__ err) {
+                   const int32_t* __restrict__ chunk_base, int slot_lo, int slot_hi,
+                   const unsigned char* __restrict__ rec_in, const __half* __restrict__ o_sm,
+                   const float* __restrict__ lambda, __nv_bfloat16* __restrict__ out,
+                   const float* __restrict__ S_in, float* __restrict__ S_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
@@ -138,8 +139,13 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
     const int64_t j_end = len - W;
-    const int n_chunks = j_end > L.n_sinks ? (int)((j_end - L.n_sinks + kC - 1) / kC) : 0;
+    const int seq_chunks = j_end > L.n_sinks ? (int)((j_end - L.n_sinks + kC - 1) / kC) : 0;
     const int slot0 = __ldg(chunk_base + n);
+    // this launch: the sequence's chunks c_lo .. c_lo + n_chunks - 1 (those in slots [slot_lo, slot_hi)),
+    // loop index c = chunk - c_lo
+    const int c_lo = min(max(slot_lo - slot0, 0), seq_chunks);
+    const int n_chunks = min(max(slot_hi - slot0, 0), seq_chunks) - c_lo;
+    const bool resume = S_in && c_lo > 0;  // continue from the state the previous launch left
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) umma::mbar_init(bar(i), (i == kFree || i == kFree + 1) ? 2 : 1);
@@ -181,6 +187,20 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
         float S[kNS];  // S0[tid][slice columns]: fp32 master copy
 #pragma unroll
         for (int i = 0; i < kNS; ++i) S[i] = 0.f;
+        if (resume) {  // the saved state and its fp16 image (the zero image above is overwritten)
+            const float* src = S_in + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
+#pragma unroll
+            for (int i = 0; i < kNS; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + i);
+                S[i] = x.x; S[i + 1] = x.y; S[i + 2] = x.z; S[i + 3] = x.w;
+            }
+#pragma unroll
+            for (int j = 0; j < kNS / 8; ++j)
+                st16(sm + kS + umma::sw128_offset(tid, 8 * j, 128), pack8(S + 8 * j, 1.f));
+            umma::fence_async_smem();
+            umma::fence_before_sync();
+            group_sync(1, 128);
+        }
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
         const uint32_t id_ab = umma::idesc_f16(128, kNS, true, true, false);
         uint32_t ph1 = 0, ph2 = 0;
@@ -272,8 +292,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             const int b = c & 1;
             if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true)) break;
             const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
-            const int tok = (int)(start + L.n_sinks + (int64_t)c * kC);  // first absorbed token of the chunk
-            const unsigned char* rec = rec_in + ((size_t)(slot0 + c) * L.Hq + h) * kRecordBytes;
+            const int tok = (int)(start + L.n_sinks + (int64_t)(c_lo + c) * kC);  // first absorbed token of the chunk
+            const unsigned char* rec = rec_in + ((size_t)(slot0 + c_lo + c) * L.Hq + h) * kRecordBytes;
             tma::expect_tx(ld, kLoadBytes);
             tma::bulk_load(buf + kA1, rec + kRecWm, 8192, ld);                   // -Wm, key dims 0..63
             tma::bulk_load(buf + kA1 + 16384, rec + kRecWm + 8192, 8192, ld);    // key dims 64..127
@@ -315,7 +335,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             umma::fence_before_sync();
             group_sync(3, 64);
             if (r == 0) mbar_arrive(bar(kFree + b));
-            const int64_t j0 = L.n_sinks + (int64_t)c * kC;
+            const int64_t j0 = L.n_sinks + (int64_t)(c_lo + c) * kC;
             if (emit && r < j_end - j0) {
                 const size_t base = ((size_t)(start + j0 + r + W) * L.Hq + h) * kD + slice * kNS;
 #pragma unroll
@@ -343,9 +363,9 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 }  // namespace
 
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
-                               const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
-                               const __half* o_sm, const float* lambda, __nv_bfloat16* out, float* S_out,
-                               int32_t* err, cudaStream_t st) {
+                               const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
+                               const unsigned char* rec_in, const __half* o_sm, const float* lambda,
+                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, cudaStream_t st) {
     static bool configured = false;  // the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -361,8 +381,8 @@ cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __h
         !tma::make_map_f16_3d(&mv, vhat, kD, (uint64_t)L.Hkv, (uint64_t)L.total))
         return cudaErrorInvalidValue;
     dim3 grid(L.Hq * kSlices, L.n_seqs);
-    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, rec_in, o_sm, lambda, out,
-                                                          S_out, err);
+    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, slot_lo, slot_hi, rec_in,
+                                                          o_sm, lambda, out, S_in, S_out, err);
     return cudaGetLastError();
 }
 

@@ -65,8 +65,10 @@ __device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, 
     for (int m = 0; m < 32; ++m) sT[(32 * b + l) * 68 + 32 * b + m] = t[m];
 }
 
-__global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ cu, int32_t* __restrict__ base) {
+__global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ cu, int32_t* __restrict__ base,
+                                       int32_t* __restrict__ counters, int n_counters) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    for (int i = 0; i < n_counters; ++i) counters[i] = 0;
     int32_t acc = 0;
     for (int s = 0; s < L.n_seqs; ++s) {
         base[s] = acc;
@@ -82,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
                    const float* __restrict__ g,
                    const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                   const int32_t* __restrict__ chunk_base, unsigned char* __restrict__ rec_out,
-                   int32_t* __restrict__ err) {
+                   const int32_t* __restrict__ chunk_base, int slot_lo, int slot_hi,
+                   int32_t* __restrict__ counter, unsigned char* __restrict__ rec_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* sA = reinterpret_cast<float*>(sm + kA32);
@@ -95,10 +97,13 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
     float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
+    volatile int* next_s = reinterpret_cast<volatile int*>(sm + kMisc + 24);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t mbar = umma::smem_addr(mbar_p), sbase = umma::smem_addr(sm);
-    const int64_t n_items = (int64_t)__ldg(chunk_base + L.n_seqs) * L.Hq;
-    if ((int64_t)blockIdx.x >= n_items) return;  // whole CTA leaves together
+    // items (chunk slot, q-head) of slots [slot_lo, slot_hi), taken one at a time from `counter`
+    const int64_t item_lo = (int64_t)slot_lo * L.Hq;
+    const int64_t item_hi = (int64_t)min(slot_hi, __ldg(chunk_base + L.n_seqs)) * L.Hq;
+    if (item_lo >= item_hi) return;  // whole CTA leaves together
 
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -112,8 +117,13 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     const uint32_t tmem = *tmem_slot;
     uint32_t phase = 0;
 
-    // persistent loop over (chunk slot, q-head) items
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // persistent loop over (chunk slot, q-head) items, fetched dynamically so the CTAs that are
+    // resident (possibly beside another kernel) share all of them
+    for (;;) {
+    if (tid == 0) *next_s = atomicAdd(counter, 1);
+    __syncthreads();
+    const int64_t item = item_lo + *next_s;
+    if (item >= item_hi) break;
     const int slot = (int)(item / L.Hq), h = (int)(item % L.Hq), kv = h / L.G;
     // sequence owning the slot: the last s with chunk_base[s] <= slot
     int lo = 0, hi = L.n_seqs - 1;
@@ -315,9 +325,15 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 
 size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
 
+cudaError_t launch_gdn_chunk_table(const LayerDims& L, const int32_t* cu, int32_t* chunk_base, int32_t* counters,
+                                   int n_counters, cudaStream_t st) {
+    gdn_chunk_table_kernel<<<1, 32, 0, st>>>(L, cu, chunk_base, counters, n_counters);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
-                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
-                               int32_t* err, cudaStream_t st) {
+                               const float* beta, const int32_t* cu, const int32_t* chunk_base, int slot_lo,
+                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -325,9 +341,7 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    gdn_chunk_table_kernel<<<1, 32, 0, st>>>(L, cu, chunk_base);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (slot_hi <= slot_lo) return cudaSuccess;
     static int n_sm = 0;  // per-process device property cache
     if (!n_sm) {
         int dev = 0;
@@ -335,9 +349,10 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
             cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
             n_sm = 132;
     }
-    const int64_t items = (int64_t)gdn_chunk_slots(L.total, L.n_seqs) * L.Hq;
+    const int64_t items = (int64_t)(slot_hi - slot_lo) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
-    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, rec_out, err);
+    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, slot_lo, slot_hi,
+                                                          counter, rec_out, err);
     return cudaGetLastError();
 }
 

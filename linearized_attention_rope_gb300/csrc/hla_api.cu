@@ -51,7 +51,7 @@ size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
 
 // Workspace layout of one prefill.
 struct WsLayout {
-    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, osm, blk_base, chunk_base, tinv, total;
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, osm, blk_base, chunk_base, counters, tinv, smid, total;
     int n_coarse;
 };
 
@@ -83,7 +83,10 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     w.osm = off;    off = align_up(off + (chunked ? T * Hq * d * sizeof(__half) : 0));
     w.blk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
     w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
+    w.counters = off; off = align_up(off + (chunked ? 2 * sizeof(int32_t) : 0));
     w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
+    // the state between the two halves of the chunked GDN (fp32, per sequence and q-head)
+    w.smid = off;   off = align_up(off + (chunked ? (size_t)n_seqs * Hq * d * d * sizeof(float) : 0));
     w.total = off;
     return w;
 }
@@ -141,20 +144,39 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             __half* osm = reinterpret_cast<__half*>(ws + w.osm);
             int32_t* blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
             int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
+            int32_t* counters = reinterpret_cast<int32_t*>(ws + w.counters);
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
+            float* smid = reinterpret_cast<float*>(ws + w.smid);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+            // The GDN runs in two halves of the chunk slots.  The chunk kernel of the first half runs
+            // on a low-priority side stream beside the softmax; the state kernel of the first half
+            // (64 or so CTAs) then runs beside the chunk kernel of the second half, which takes the
+            // SMs left free; the state kernel of the second half continues from the saved state.
+            const int n_slots = (int)gdn_chunk_slots(L.total, L.n_seqs), split = (n_slots + 1) / 2;
             SideStream* side = nullptr;
             HLA_TRY(side_stream(&side));  // per host thread and device; see hla_common.cuh
             HLA_TRY(cudaEventRecord(side->fork, stream));
-            HLA_TRY(cudaStreamWaitEvent(side->s, side->fork, 0));
-            HLA_TRY(mark_stage(3, side->s));
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, rec, err, side->s));
-            HLA_TRY(mark_stage(4, side->s));
-            HLA_TRY(cudaEventRecord(side->join, side->s));
+            HLA_TRY(cudaStreamWaitEvent(side->lo, side->fork, 0));
+            HLA_TRY(mark_stage(3, side->lo));
+            HLA_TRY(launch_gdn_chunk_table(L, cu, chunk_base, counters, 2, side->lo));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, 0, split, counters, rec, err, side->lo));
+            HLA_TRY(cudaEventRecord(side->mid, side->lo));
             HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
+            // the second chunk-kernel launch only once the softmax is done, so that the first state
+            // launch, ready at the same time and on the higher-priority stream, is placed first
+            HLA_TRY(cudaEventRecord(side->main_mid, stream));
+            HLA_TRY(cudaStreamWaitEvent(side->lo, side->main_mid, 0));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, split, n_slots, counters + 1, rec, err,
+                                       side->lo));
+            HLA_TRY(mark_stage(4, side->lo));
+            HLA_TRY(cudaEventRecord(side->join, side->lo));
+            HLA_TRY(cudaStreamWaitEvent(stream, side->mid, 0));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, 0, split, rec, osm, lambda, o, nullptr, smid,
+                                       err, stream));
             HLA_TRY(cudaStreamWaitEvent(stream, side->join, 0));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, rec, osm, lambda, o, S_out, err, stream));
+            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, split, n_slots, rec, osm, lambda, o, smid,
+                                       S_out, err, stream));
         }
     } else {
         // features -> GDN (fp32 o_lin) -> softmax + combine

@@ -120,12 +120,14 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st);
 
 // Per host thread and device: a second stream for kernels that can run
-// beside the caller's stream, and the events that fork it off the caller's
-// stream and join it back.  Created on first use and kept for the thread's
-// lifetime.
+// beside the caller's stream, a low-priority one for work that should only
+// take the SMs the caller's stream leaves free, and the events that fork them
+// off the caller's stream and join them back (fork, join) or order steps
+// between the two (mid, main_mid).  Created on first use and kept for the
+// thread's lifetime.
 struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t s = nullptr, lo = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr, main_mid = nullptr;
 };
 cudaError_t side_stream(SideStream** out);
 
@@ -144,16 +146,26 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
 // images, then gamma and the key decay (fp32, 64 each).
 // Step 2: the state-carrying kernel.
 constexpr uint32_t kRecWm = 0, kRecTb = 16384, kRecP = 24576, kRecVec = 32768, kRecordBytes = 33280;
+// The chunk table (n_seqs + 1 entries, on the device) comes from
+// launch_gdn_chunk_table, which also zeroes the item counters; each
+// launch_gdn_inverse covers the chunk slots [slot_lo, slot_hi) (clipped to
+// the table's total), its CTAs taking items from its own counter.
 size_t gdn_chunk_slots(int64_t total, int n_seqs);
+cudaError_t launch_gdn_chunk_table(const LayerDims& L, const int32_t* cu, int32_t* chunk_base, int32_t* counters,
+                                   int n_counters, cudaStream_t st);
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
-                               const float* beta, const int32_t* cu, int32_t* chunk_base, unsigned char* rec_out,
-                               int32_t* err, cudaStream_t st);
-// out rows of positions >= n_sinks + W: bf16(o_sm + lambda_h o_lin) (none if
-// out is null or the linear branch is switched off).
+                               const float* beta, const int32_t* cu, const int32_t* chunk_base, int slot_lo,
+                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, cudaStream_t st);
+// The chunks of slots [slot_lo, slot_hi) of every sequence, continuing from
+// S_in (fp32 [n_seqs][Hq][d][d]; read only for sequences with chunks before
+// slot_lo, zero state otherwise; may be null if none has).  out rows of
+// positions >= n_sinks + W of those chunks: bf16(o_sm + lambda_h o_lin) (none
+// if out is null or the linear branch is switched off); the state after the
+// last chunk in range into S_out (may be null).
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
-                               const int32_t* cu, const int32_t* chunk_base, const unsigned char* rec_in,
-                               const __half* o_sm, const float* lambda, __nv_bfloat16* out, float* S_out,
-                               int32_t* err, cudaStream_t st);
+                               const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
+                               const unsigned char* rec_in, const __half* o_sm, const float* lambda,
+                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>
