@@ -265,13 +265,14 @@ def run_prefill_bench(args, dist, peaks):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    n_stage = 7
+    n_stage = 11
     chunked = wl.dtype == "bf16" and wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads in (1, 2, 4, 8)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
     for row in ev:  # materialise the event handles
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     dist.barrier()
     torch.cuda.synchronize()
@@ -279,27 +280,37 @@ def run_prefill_bench(args, dist, peaks):
     with ClockSampler(dist.local) as clocks:
         for i in range(args.steps):
             flush.zero_()
-            hla.set_prefill_stage_events(ev[i])
+            starts[i].record(stream)
             step()
             ends[i].record(stream)
-        hla.set_prefill_stage_events(None)
         torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ends[i]) for i in range(args.steps)]
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    # Per-kernel durations: the same number of steps again with the library's stage events on (events
+    # timed between the launches that overlap on two streams would serialise them inside the timed
+    # region above).
+    for i in range(args.steps):
+        flush.zero_()
+        hla.set_prefill_stage_events(ev[i])
+        step()
+    hla.set_prefill_stage_events(None)
+    torch.cuda.synchronize()
+
     def stages(row):
         t = [0.0] + [row[0].elapsed_time(row[j]) for j in range(1, n_stage)]  # ms from mark 0
-        if chunked:  # the chunk-local GDN kernel runs on the library's side stream beside the softmax
-            return {"features": t[1], "softmax": t[2] - t[1], "gdn_prep": t[4] - t[3],
-                    "gdn_state": t[5] - max(t[2], t[4])}
+        if chunked:  # each GDN kernel runs twice (two halves of the chunk slots), the chunk-local one on
+            # the library's side stream: a stage is the sum of its launches' durations on their streams
+            return {"features": t[1], "softmax": t[2] - t[1], "gdn_prep": (t[7] - t[3]) + (t[4] - t[10]),
+                    "gdn_state": (t[8] - t[9]) + (t[5] - max(t[8], t[4]))}
         return {"features": t[1], "gdn_state": t[4] - t[3], "softmax": t[5] - t[4]}
 
     per_step = [stages(ev[i]) for i in range(args.steps)]
     stage_ms = {k: statistics.mean(st[k] for st in per_step) for k in per_step[0]}
     device_s = dist.max(sum(step_ms) / 1e3)
-    # rope tables, features, then block table + softmax, chunk table + chunk kernel, state kernel
-    # (tensor-core path) or GDN + softmax (token-serial path)
-    launches_per_step = 7 if chunked else 4
+    # rope tables, features, then block table + softmax, chunk table + two chunk-kernel and two
+    # state-kernel launches (tensor-core path) or GDN + softmax (token-serial path)
+    launches_per_step = 9 if chunked else 4
 
     work = prefill_work(wl)
 
@@ -523,7 +534,10 @@ def main():
                    "seq_len": max(wl.seqlens), "tokens_per_rank": wl.total_tokens,
                    "parallelism": f"replicas x{dist.world}", "l2": "flushed between steps (512 MiB write)",
                    "precision": "bf16 in/out, fp16 MMA operands, fp32 state and accumulation"},
-        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"], "stage_roofline": pre["stage_roofline"],
+        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"],
+        "stage_ms_source": "each kernel's launches timed on their streams over --steps instrumented steps run "
+                           "right after the timed region",
+        "stage_roofline": pre["stage_roofline"],
         "clocks": pre["clocks"], "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"],
         "wall_s": round(pre["wall_s"], 3),
     }

@@ -210,14 +210,17 @@ HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code);
  * hla_prefill record events[i] (cudaEvent_t handles owned by the caller) on
  * its stream at stage boundaries.  Tensor-core path (bf16, head_dim 128):
  * 0 before the first kernel, 1 after the feature path, 2 after the softmax
- * branch, 3 and 4 around the chunk-local part of the linear branch (recorded
- * on the library's side stream, where it runs beside the softmax), 5 after
- * the GDN state kernel (which also combines the two branches and starts once
- * both 2 and 4 are reached), 6 after the decode-state hand-off.  Token-serial
- * path: 0, 1 as above, 2 = 3 = 1, 4 after the GDN kernel, 5 after the softmax
- * + combine, 6 after the hand-off.  Entries beyond n_events, or NULL
- * entries, are skipped; n_events = 0 switches the hook off.  The array must
- * stay valid while the hook is on. */
+ * branch, 6 after the decode-state hand-off; the linear branch runs in two
+ * halves of the chunk slots, each a chunk-local launch on the library's
+ * low-priority side stream and a state launch (which also combines the two
+ * branches) on the caller's stream: 3 before and 7 after the first
+ * chunk-local launch (beside the softmax), 10 before and 4 after the second
+ * (once 2 is reached), 9 before and 8 after the first state launch (once 2
+ * and 7 are reached), 5 after the second (once 8 and 4 are reached).
+ * Token-serial path: 0, 1 as above, 2 = 3 = 1, 4 after the GDN kernel, 5
+ * after the softmax + combine, 6 after the hand-off (7 to 10 not recorded).
+ * Entries beyond n_events, or NULL entries, are skipped; n_events = 0
+ * switches the hook off.  The array must stay valid while the hook is on. */
 HLA_API int hla_prefill_stage_events(void** events, int n_events);
 
 #ifdef __cplusplus

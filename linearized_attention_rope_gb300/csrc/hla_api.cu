@@ -160,6 +160,7 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             HLA_TRY(mark_stage(3, side->lo));
             HLA_TRY(launch_gdn_chunk_table(L, cu, chunk_base, counters, 2, side->lo));
             HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, 0, split, counters, rec, err, side->lo));
+            HLA_TRY(mark_stage(7, side->lo));
             HLA_TRY(cudaEventRecord(side->mid, side->lo));
             HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
@@ -167,13 +168,16 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             // launch, ready at the same time and on the higher-priority stream, is placed first
             HLA_TRY(cudaEventRecord(side->main_mid, stream));
             HLA_TRY(cudaStreamWaitEvent(side->lo, side->main_mid, 0));
+            HLA_TRY(mark_stage(10, side->lo));
             HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, split, n_slots, counters + 1, rec, err,
                                        side->lo));
             HLA_TRY(mark_stage(4, side->lo));
             HLA_TRY(cudaEventRecord(side->join, side->lo));
             HLA_TRY(cudaStreamWaitEvent(stream, side->mid, 0));
+            HLA_TRY(mark_stage(9, stream));
             HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, 0, split, rec, osm, lambda, o, nullptr, smid,
                                        err, stream));
+            HLA_TRY(mark_stage(8, stream));
             HLA_TRY(cudaStreamWaitEvent(stream, side->join, 0));
             HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, split, n_slots, rec, osm, lambda, o, smid,
                                        S_out, err, stream));
