@@ -265,7 +265,7 @@ def run_prefill_bench(args, dist, peaks):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    n_stage = 11
+    n_stage = 23
     chunked = wl.dtype == "bf16" and wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads in (1, 2, 4, 8)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
     for row in ev:  # materialise the event handles
@@ -299,18 +299,17 @@ def run_prefill_bench(args, dist, peaks):
 
     def stages(row):
         t = [0.0] + [row[0].elapsed_time(row[j]) for j in range(1, n_stage)]  # ms from mark 0
-        if chunked:  # each GDN kernel runs twice (two halves of the chunk slots), the chunk-local one on
-            # the library's side stream: a stage is the sum of its launches' durations on their streams
-            return {"features": t[1], "softmax": t[2] - t[1], "gdn_prep": (t[7] - t[3]) + (t[4] - t[10]),
-                    "gdn_state": (t[8] - t[9]) + (t[5] - max(t[8], t[4]))}
+        if chunked:  # each GDN kernel runs once per part of the chunk slots, the chunk-local one on the
+            # library's side stream: a stage is the sum of its launches' durations on their streams
+            return {"features": t[1], "softmax": t[2] - t[1],
+                    "gdn_prep": sum(t[8 + 4 * p] - t[7 + 4 * p] for p in range(4)),
+                    "gdn_state": sum(t[10 + 4 * p] - t[9 + 4 * p] for p in range(4))}
         return {"features": t[1], "gdn_state": t[4] - t[3], "softmax": t[5] - t[4]}
 
     per_step = [stages(ev[i]) for i in range(args.steps)]
     stage_ms = {k: statistics.mean(st[k] for st in per_step) for k in per_step[0]}
     device_s = dist.max(sum(step_ms) / 1e3)
-    # rope tables, features, then block table + softmax, chunk table + two chunk-kernel and two
-    # state-kernel launches (tensor-core path) or GDN + softmax (token-serial path)
-    launches_per_step = 9 if chunked else 4
+    launches_per_step = hla.prefill_launch_count(prm)
 
     work = prefill_work(wl)
 

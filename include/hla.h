@@ -210,18 +210,27 @@ HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code);
  * hla_prefill record events[i] (cudaEvent_t handles owned by the caller) on
  * its stream at stage boundaries.  Tensor-core path (bf16, head_dim 128):
  * 0 before the first kernel, 1 after the feature path, 2 after the softmax
- * branch, 6 after the decode-state hand-off; the linear branch runs in two
- * halves of the chunk slots, each a chunk-local launch on the library's
+ * branch, 6 after the decode-state hand-off.  The linear branch runs in up to
+ * four parts of the chunk slots, each a chunk-local launch on the library's
  * low-priority side stream and a state launch (which also combines the two
- * branches) on the caller's stream: 3 before and 7 after the first
- * chunk-local launch (beside the softmax), 10 before and 4 after the second
- * (once 2 is reached), 9 before and 8 after the first state launch (once 2
- * and 7 are reached), 5 after the second (once 8 and 4 are reached).
+ * branches) on the caller's stream: for part p, 7 + 4p before and 8 + 4p
+ * after its chunk-local launch (the first beside the softmax, a later one
+ * once 2 and the previous part's chunk-local launch are reached), 9 + 4p
+ * before and 10 + 4p after its state launch (once 2, 8 + 4p and the previous
+ * state launch are reached); marks of parts not run are recorded together
+ * after the last state launch.  3 before the first and 4 after the last
+ * chunk-local launch (side stream), 5 after the last state launch.
  * Token-serial path: 0, 1 as above, 2 = 3 = 1, 4 after the GDN kernel, 5
- * after the softmax + combine, 6 after the hand-off (7 to 10 not recorded).
+ * after the softmax + combine, 6 after the hand-off (7 to 22 not recorded).
  * Entries beyond n_events, or NULL entries, are skipped; n_events = 0
  * switches the hook off.  The array must stay valid while the hook is on. */
 HLA_API int hla_prefill_stage_events(void** events, int n_events);
+
+/* Measurement hook (not part of the layer): *out = the number of kernels one
+ * hla_prefill call with these params launches (with_state != 0: with a
+ * decode state to fill).  Memsets and event records are not counted.  Returns
+ * the params check's status. */
+HLA_API int hla_prefill_launch_count(const hla_params* params, int with_state, int* out);
 
 #ifdef __cplusplus
 }

@@ -83,7 +83,7 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     w.osm = off;    off = align_up(off + (chunked ? T * Hq * d * sizeof(__half) : 0));
     w.blk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
     w.chunk_base = off; off = align_up(off + (chunked ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
-    w.counters = off; off = align_up(off + (chunked ? 2 * sizeof(int32_t) : 0));
+    w.counters = off; off = align_up(off + (chunked ? kMaxGdnParts * sizeof(int32_t) : 0));
     w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
     // the state between the two halves of the chunked GDN (fp32, per sequence and q-head)
     w.smid = off;   off = align_up(off + (chunked ? (size_t)n_seqs * Hq * d * d * sizeof(float) : 0));
@@ -92,6 +92,10 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HLA_OK : HLA_ERR_CUDA; }
+
+// Parts of the chunk slots the chunked GDN runs in (1 .. kMaxGdnParts).
+constexpr int kGdnParts = 2;
+static_assert(kGdnParts >= 1 && kGdnParts <= kMaxGdnParts, "GDN parts");
 
 // Measurement hook: events recorded between the stages of hla_prefill on the
 // calling thread (see hla_prefill_stage_events).
@@ -148,39 +152,48 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
             float* smid = reinterpret_cast<float*>(ws + w.smid);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-            // The GDN runs in two halves of the chunk slots.  The chunk kernel of the first half runs
-            // on a low-priority side stream beside the softmax; the state kernel of the first half
-            // (64 or so CTAs) then runs beside the chunk kernel of the second half, which takes the
-            // SMs left free; the state kernel of the second half continues from the saved state.
-            const int n_slots = (int)gdn_chunk_slots(L.total, L.n_seqs), split = (n_slots + 1) / 2;
+            // The GDN runs in kGdnParts parts of the chunk slots.  The chunk-local kernel of the first
+            // part runs on a low-priority side stream beside the softmax; the state kernel of each part
+            // (64 or so CTAs) then runs beside the chunk-local kernel of the next, which takes the SMs
+            // left free; each state launch continues from the state the previous one saved.
+            const int n_slots = (int)gdn_chunk_slots(L.total, L.n_seqs);
+            int bound[kGdnParts + 1];
+            for (int p = 0; p <= kGdnParts; ++p) bound[p] = (int)((int64_t)n_slots * p / kGdnParts);
             SideStream* side = nullptr;
             HLA_TRY(side_stream(&side));  // per host thread and device; see hla_common.cuh
             HLA_TRY(cudaEventRecord(side->fork, stream));
             HLA_TRY(cudaStreamWaitEvent(side->lo, side->fork, 0));
             HLA_TRY(mark_stage(3, side->lo));
-            HLA_TRY(launch_gdn_chunk_table(L, cu, chunk_base, counters, 2, side->lo));
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, 0, split, counters, rec, err, side->lo));
+            HLA_TRY(launch_gdn_chunk_table(L, cu, chunk_base, counters, kGdnParts, side->lo));
             HLA_TRY(mark_stage(7, side->lo));
-            HLA_TRY(cudaEventRecord(side->mid, side->lo));
+            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, bound[0], bound[1], counters, rec, err,
+                                       side->lo));
+            HLA_TRY(mark_stage(8, side->lo));
+            HLA_TRY(cudaEventRecord(side->part[0], side->lo));
             HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
-            // the second chunk-kernel launch only once the softmax is done, so that the first state
-            // launch, ready at the same time and on the higher-priority stream, is placed first
+            // the second chunk-local launch only once the softmax is done, so that the first state
+            // launch, ready at the same time and on the higher-priority stream, is placed first (a
+            // later one waits for the chunk-local launch before it, as the state launch it races does)
             HLA_TRY(cudaEventRecord(side->main_mid, stream));
             HLA_TRY(cudaStreamWaitEvent(side->lo, side->main_mid, 0));
-            HLA_TRY(mark_stage(10, side->lo));
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, split, n_slots, counters + 1, rec, err,
-                                       side->lo));
+            for (int p = 1; p < kGdnParts; ++p) {
+                HLA_TRY(mark_stage(7 + 4 * p, side->lo));
+                HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, bound[p], bound[p + 1], counters + p,
+                                           rec, err, side->lo));
+                HLA_TRY(mark_stage(8 + 4 * p, side->lo));
+                HLA_TRY(cudaEventRecord(side->part[p], side->lo));
+            }
             HLA_TRY(mark_stage(4, side->lo));
-            HLA_TRY(cudaEventRecord(side->join, side->lo));
-            HLA_TRY(cudaStreamWaitEvent(stream, side->mid, 0));
-            HLA_TRY(mark_stage(9, stream));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, 0, split, rec, osm, lambda, o, nullptr, smid,
-                                       err, stream));
-            HLA_TRY(mark_stage(8, stream));
-            HLA_TRY(cudaStreamWaitEvent(stream, side->join, 0));
-            HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, split, n_slots, rec, osm, lambda, o, smid,
-                                       S_out, err, stream));
+            for (int p = 0; p < kGdnParts; ++p) {
+                HLA_TRY(cudaStreamWaitEvent(stream, side->part[p], 0));
+                HLA_TRY(mark_stage(9 + 4 * p, stream));
+                HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, bound[p], bound[p + 1], rec, osm, lambda, o,
+                                           p > 0 ? smid : nullptr, p + 1 < kGdnParts ? smid : S_out, err, stream));
+                HLA_TRY(mark_stage(10 + 4 * p, stream));
+            }
+            for (int p = kGdnParts; p < kMaxGdnParts; ++p)  // absent parts: zero-length marks
+                for (int m = 7; m <= 10; ++m) HLA_TRY(mark_stage(m + 4 * p, stream));
         }
     } else {
         // features -> GDN (fp32 o_lin) -> softmax + combine
@@ -349,6 +362,16 @@ HLA_API int hla_prefill_stage_events(void** events, int n_events) {
     if (n_events < 0 || (n_events > 0 && !events)) return HLA_ERR_INVALID_ARG;
     t_stage_events = reinterpret_cast<cudaEvent_t*>(events);
     t_n_stage_events = n_events;
+    return HLA_OK;
+}
+
+HLA_API int hla_prefill_launch_count(const hla_params* prm, int with_state, int* out) {
+    const int rc = check_params(prm);
+    if (rc != HLA_OK) return rc;
+    if (!out) return HLA_ERR_INVALID_ARG;
+    // rope tables, features; tensor-core path: softmax block table + softmax, chunk table, one
+    // chunk-local and one state launch per part; token-serial path: GDN, softmax
+    *out = (uses_chunked_gdn(prm) ? 5 + 2 * kGdnParts : 4) + (with_state ? 1 : 0);
     return HLA_OK;
 }
 

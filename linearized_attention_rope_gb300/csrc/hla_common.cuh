@@ -123,11 +123,13 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
 // beside the caller's stream, a low-priority one for work that should only
 // take the SMs the caller's stream leaves free, and the events that fork them
 // off the caller's stream and join them back (fork, join) or order steps
-// between the two (mid, main_mid).  Created on first use and kept for the
+// between the two (part[k], main_mid).  Created on first use and kept for the
 // thread's lifetime.
+constexpr int kMaxGdnParts = 4;
 struct SideStream {
     cudaStream_t s = nullptr, lo = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr, main_mid = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, main_mid = nullptr;
+    cudaEvent_t part[kMaxGdnParts] = {};  // a step of the low-priority stream done
 };
 cudaError_t side_stream(SideStream** out);
 

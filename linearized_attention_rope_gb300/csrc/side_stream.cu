@@ -17,8 +17,10 @@ cudaError_t side_stream(SideStream** out) {
         if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
         if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
         if ((e = cudaStreamCreateWithPriority(&ss.lo, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
-        for (cudaEvent_t* ev : {&ss.fork, &ss.join, &ss.mid, &ss.main_mid})
+        for (cudaEvent_t* ev : {&ss.fork, &ss.join, &ss.main_mid})
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (cudaEvent_t& ev : ss.part)
+            if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     *out = &ss;
     return cudaSuccess;

@@ -81,11 +81,12 @@ def load():
         lib.hla_check_device_error.argtypes = [S, _vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_check_workspace_error.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_prefill_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+        lib.hla_prefill_launch_count.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         lib.hla_prefill_noalloc.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, S, _vp]
         lib.hla_prefill_noalloc.restype = ctypes.c_int
         for fn in ("hla_state_bytes", "hla_prefill_workspace_bytes", "hla_state_init", "hla_prefill",
                    "hla_decode_step", "hla_check_device_error", "hla_check_workspace_error",
-                   "hla_prefill_stage_events"):
+                   "hla_prefill_stage_events", "hla_prefill_launch_count"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -229,6 +230,14 @@ def set_prefill_stage_events(events):
         return
     _stage_handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(load().hla_prefill_stage_events(_stage_handles, len(events)), "hla_prefill_stage_events")
+
+
+def prefill_launch_count(params: Params, with_state: bool = False) -> int:
+    """hla_prefill_launch_count: kernels launched by one prefill call."""
+    n = ctypes.c_int(0)
+    _check(load().hla_prefill_launch_count(ctypes.byref(params.c()), int(with_state), ctypes.byref(n)),
+           "hla_prefill_launch_count")
+    return n.value
 
 
 def prefill_noalloc(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out, state=None,
