@@ -74,6 +74,7 @@ constexpr uint32_t kColD1 = 0, kColD2 = 128, kColS = 256, kTmemCols = 512;
 
 // mbarrier indices
 constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kNumBars = 10;
+static_assert(8 * kNumBars + 8 + 32 <= 128, "barrier area: mbarriers, TMEM base, abort flag, 2 slots x 4 ids");
 constexpr uint32_t kLoadBytes = kRecordBytes + 5 * 8192;  // record + query, key rows (2 boxes each) + value slice
 
 __device__ __forceinline__ void st16(unsigned char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
@@ -98,17 +99,6 @@ __device__ __forceinline__ void group_sync(int id, int count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
-// All `count` threads of role `id` vote; true only if every one passes `v`.
-__device__ __forceinline__ bool group_all(int id, int count, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
 
 // Descriptor offsets (address field, 16-byte units) of K step s: a 128-row
 // K-major tile advances 32 B inside a 64-column block and 16 KB per block;
@@ -127,6 +117,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
+    volatile int* decision = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 8);  // [role id][2]
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
@@ -165,10 +156,13 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     const uint32_t tmem = *tmem_slot;
 
     // One leader per role polls the mbarrier (an inline try first, the bounded
-    // loop only if the phase is still open); the role (`count` threads on named
-    // barrier `id`; 0 for a one-thread role) then votes, so every thread takes
-    // the same branch, and fences before touching the results.
-    auto role_wait = [&](int i, uint32_t parity, int id, int count, bool leader) -> bool {
+    // loop only if the phase is still open) and posts the outcome in a shared
+    // slot; the role (`count` threads on named barrier `id`; 0 for a one-thread
+    // role) then meets on the barrier and every thread reads the same outcome,
+    // so all take the same branch, and fences before touching the results.  The
+    // two slots of a role alternate (counter k), so a slot is rewritten only
+    // after the whole role has passed the barrier in between.
+    auto role_wait = [&](int i, uint32_t parity, int id, int count, bool leader, int& k) -> bool {
         bool w = true;
         if (leader) {
             w = !*abort_flag && (umma::mbar_try_wait(bar(i), parity) || umma::mbar_wait(bar(i), parity, kWaitLimit));
@@ -176,10 +170,15 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                 *abort_flag = 1;
                 if (err) atomicExch(err, kErrTimeout);
             }
+            if (count) decision[2 * id + (k & 1)] = w;
         }
-        const bool ok = count ? group_all(id, count, w) : w;
+        if (count) {
+            group_sync(id, count);
+            w = decision[2 * id + (k & 1)] != 0;
+            ++k;
+        }
         umma::fence_after_sync();
-        return ok;
+        return w;
     };
 
     if (warp < 4) {
@@ -204,6 +203,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
         const uint32_t id_ab = umma::idesc_f16(128, kNS, true, true, false);
         uint32_t ph1 = 0, ph2 = 0;
+        int kr = 0;
         bool ok = true;
 #pragma unroll 1
         for (int c = 0; c < n_chunks && ok; ++c) {
@@ -211,7 +211,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             const uint32_t buf = (uint32_t)b * kBuf;
             // ready[b]: the chunk is loaded and D1[b] holds [T diag(beta) ; 0] V; the
             // loader waited for free[b], so the output rows of chunk c - 2 are out of D1/D2[b]
-            if (!(ok = role_wait(kReady + b, (uint32_t)((c >> 1) & 1), 1, 128, tid == 0))) break;
+            if (!(ok = role_wait(kReady + b, (uint32_t)((c >> 1) & 1), 1, 128, tid == 0, kr))) break;
 
             // D1[b] += [-Wm ; Q] S0
             if (tid == 0) {
@@ -221,7 +221,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                 for (int s = 0; s < kD / 16; ++s) umma::mma(d1, a1 + kstep128(s), bs + mnstep(s), id_b, true);
                 umma::commit(bar(kMma1));
             }
-            if (!(ok = role_wait(kMma1, ph1, 1, 128, tid == 0))) break;
+            if (!(ok = role_wait(kMma1, ph1, 1, 128, tid == 0, kr))) break;
             ph1 ^= 1u;
 
             // U (rows 0..63) -> fp16 rows of U and diag(key decay) U
@@ -256,7 +256,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                     umma::mma(tmem + kColD2 + kNS * b, zp + kstep128(s), bu + mnstep(s), id_b, s > 0);
                 umma::commit(bar(kOFull + b));
             }
-            if (!(ok = role_wait(kMma2, ph2, 1, 128, tid == 0))) break;
+            if (!(ok = role_wait(kMma2, ph2, 1, 128, tid == 0, kr))) break;
             ph2 ^= 1u;
             const float gC = reinterpret_cast<const float*>(sm + buf + kVec)[kC - 1];  // gamma_C
             group_sync(1, 128);
@@ -287,10 +287,11 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     } else if (tid == 128) {
         // ================= loads, one chunk ahead (one thread) =================
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
+        int kl = 0;  // (unused by one-thread waits)
 #pragma unroll 1
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
-            if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true)) break;
+            if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true, kl)) break;
             const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
             const int tok = (int)(start + L.n_sinks + (int64_t)(c_lo + c) * kC);  // first absorbed token of the chunk
             const unsigned char* rec = rec_in + ((size_t)(slot0 + c_lo + c) * L.Hq + h) * kRecordBytes;
@@ -305,7 +306,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             tma::tensor_load_3d(buf + kK, &map_k, 0, kv, tok, ld);
             tma::tensor_load_3d(buf + kK + 8192, &map_k, 64, kv, tok, ld);
             tma::tensor_load_3d(buf + kV, &map_v, slice * kNS, kv, tok, ld);
-            if (!role_wait(kLoaded + b, (uint32_t)((c >> 1) & 1), 0, 0, true)) break;
+            if (!role_wait(kLoaded + b, (uint32_t)((c >> 1) & 1), 0, 0, true, kl)) break;
             // D1[b] = [T diag(beta) ; 0] V; its completion releases the chunk to the chain
             const uint64_t tb = umma::kmajor(buf + kTZP, 128, 0), bv = umma::mnmajor(buf + kV, 8192u, 0);
 #pragma unroll
@@ -317,10 +318,11 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
         const int r = tid - 192;  // chunk row; TMEM lane 64 + r
         const bool emit = out && !(L.flags & HLA_FLAG_LINEAR_OFF);
         const float lam = __ldg(lambda + h);
+        int ko = 0;
 #pragma unroll 1
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
-            if (!role_wait(kOFull + b, (uint32_t)((c >> 1) & 1), 3, 64, r == 0)) break;
+            if (!role_wait(kOFull + b, (uint32_t)((c >> 1) & 1), 3, 64, r == 0, ko)) break;
             const float gr = reinterpret_cast<const float*>(sm + b * kBuf + kVec)[r] * lam;
             // lambda o_lin of this row into registers, then release the chunk buffer and D1/D2[b]
             float o[kNS];
