@@ -155,8 +155,9 @@ def measured_peaks() -> dict:
 
 
 def kernel_traffic(kernel: str, source_files) -> float | None:
-    """DRAM bytes per launch recorded from an ncu capture of `kernel`, if the
-    kernel's sources are unchanged since (hash match); else None."""
+    """DRAM bytes per step (summed over the kernel's launches in one prefill
+    call) recorded from an ncu capture of `kernel`, if the kernel's sources are
+    unchanged since (hash match); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -170,7 +171,7 @@ def kernel_traffic(kernel: str, source_files) -> float | None:
             h.update(f.read())
     if h.hexdigest() != rec.get("source_sha256"):
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec.get("dram_bytes_per_step")
 
 
 def source_hash(files) -> str:
