@@ -172,7 +172,7 @@ HLA_API int hla_prefill(const hla_params* params, const void* q, const void* k, 
  * Arguments and results are those of hla_prefill; the scratch memory comes
  * from a 64 MiB buffer inside the library (one per GPU that loads it, held
  * until the process exits).  Prefills whose hla_prefill_workspace_bytes
- * exceeds 64 MiB (about 1,700 tokens of a 32 q / 8 kv head, head_dim 128
+ * exceeds 64 MiB (about 1,300 tokens of a 32 q / 8 kv head, head_dim 128
  * bf16 layer) return HLA_ERR_WORKSPACE before any GPU work.
  * The first call on each device looks up the buffer's device address (a
  * host-side set-up step); make that first call before any stream capture.
