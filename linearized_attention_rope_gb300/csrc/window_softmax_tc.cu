@@ -150,19 +150,20 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         for (int grp = 0; grp < n_groups && ok; ++grp) {
             const int g0 = grp * kGroup, n = min(kGroup, n_slots - g0);  // a multiple of 16
             // ---- loads: the query tile with the first group, then this group's keys and values;
-            //      lane 0 posts the byte count, the lanes of warp 0 issue the boxes
-            if (warp == 0) {
-                if (lane == 0) {
-                    tma::expect_tx(bar_ld, (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u);
-                    if (grp == 0) {
-                        const int tq = (int)(start + pa);
-                        tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
-                        tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
-                    }
+            //      thread 0 posts the byte count; box b goes to lane b / 8 of warp b % 8, so the
+            //      copies are issued by all warps at once (copies issued back to back by one thread
+            //      serialise; an early complete_tx just leaves the count below zero until the post)
+            if (tid == 0) {
+                tma::expect_tx(bar_ld, (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u);
+                if (grp == 0) {
+                    const int tq = (int)(start + pa);
+                    tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
+                    tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
                 }
-                __syncwarp();
+            }
+            {
                 // boxes of 8 slots; a 64-slot run of window rows at a 64-aligned offset is one box
-                for (int j = 8 * lane; j < n; j += 8 * 32) {
+                for (int j = 8 * (warp + 8 * lane); j < n; j += 8 * kThreads) {
                     const int slot = g0 + j;
                     const bool wide = slot >= sink_pad && (j & 63) == 0 && j + 64 <= n;
                     const bool covered = slot >= sink_pad && (j & 63) != 0 && (j & ~63) + 64 <= n &&
@@ -194,37 +195,46 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
             if (!(ok = cta_wait(bar_mma, ph_mma))) break;
 
             // ---- online softmax: this thread covers slots [c_lo, c_hi) of the group (16-slot chunks,
-            //      split evenly between the two threads of the row)
+            //      split evenly between the two threads of the row), read from TMEM once: 64 columns
+            //      from c_lo (inside the 128 allocated), the ones at or past c_hi masked
             const int n16 = n >> 4, c_lo = chalf ? ((n16 + 1) >> 1) * 16 : 0, c_hi = chalf ? n : ((n16 + 1) >> 1) * 16;
-            float mg = -INFINITY;  // raw scores: the scale is positive
-            for (int c = c_lo; c < c_hi; c += 16) {
-                float sc[16];
-                umma::tmem_ld16(tmem + lane_base + kColS + c, sc);
+            float sc[64];
+            {
+                uint32_t r0[32], r1[32];
+                umma::tmem_ld32_async(tmem + lane_base + kColS + c_lo, r0);
+                umma::tmem_ld32_async(tmem + lane_base + kColS + c_lo + 32, r1);
+                umma::tmem_wait_ld();
+                umma::reg_fence32(r0);
+                umma::reg_fence32(r1);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int gi = g0 + c + i;
-                    if (gi < hi1 || (gi >= lo2 && gi < hi2)) mg = fmaxf(mg, sc[i]);
+                for (int x = 0; x < 32; ++x) {
+                    sc[x] = __uint_as_float(r0[x]);
+                    sc[32 + x] = __uint_as_float(r1[x]);
                 }
+            }
+            float mg = -INFINITY;  // raw scores: the scale is positive
+#pragma unroll
+            for (int x = 0; x < 64; ++x) {
+                const int gi = g0 + c_lo + x;
+                const bool vis = c_lo + x < c_hi && (gi < hi1 || (gi >= lo2 && gi < hi2));
+                sc[x] = vis ? sc[x] : -INFINITY;
+                mg = fmaxf(mg, sc[x]);
             }
             red[chalf * 128 + row] = mg * qscale;
             __syncthreads();
             const float m_new = fmaxf(m_run, fmaxf(red[row], red[128 + row]));
             const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
             float lsum = 0.f;
-            for (int c = c_lo; c < c_hi; c += 16) {
-                float sc[16];
-                umma::tmem_ld16(tmem + lane_base + kColS + c, sc);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int gi = g0 + c + i;
-                    const bool vis = gi < hi1 || (gi >= lo2 && gi < hi2);
-                    sc[i] = vis ? exp2f(sc[i] * qscale - m_new) : 0.f;
-                    lsum += sc[i];
-                }
+            for (int x = 0; x < 64; ++x) {
+                sc[x] = sc[x] == -INFINITY ? 0.f : exp2f(sc[x] * qscale - m_new);
+                lsum += sc[x];
+            }
 #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {  // P over the key tile: K-major, slots = K
-                    const float* x = sc + 8 * h8;
-                    *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(row, c + 8 * h8, 128)) =
+            for (int j = 0; j < 8; ++j) {  // P over the key tile: K-major, slots = K (this thread's chunks only)
+                if (c_lo + 8 * j < c_hi) {
+                    const float* x = sc + 8 * j;
+                    *reinterpret_cast<uint4*>(sm + kK + umma::sw128_offset(row, c_lo + 8 * j, 128)) =
                         make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
                                    pack_bf2(x[6], x[7]));
                 }
@@ -266,10 +276,17 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
             const float inv_l = (sm_on && row_on && l_run > 0.f) ? 1.f / l_run : 0.f;
             const bool lin_row = !lin_off && p >= (int64_t)L.n_sinks + L.window;
             const size_t base = ((size_t)(start + (row_on ? p : 0)) * L.Hq + kv * G + gq) * kD + chalf * 64;
+            uint32_t oa[32], ob[32];  // both halves in flight together, one wait
+            umma::tmem_ld32_async(tmem + lane_base + kColO + chalf * 64, oa);
+            umma::tmem_ld32_async(tmem + lane_base + kColO + chalf * 64 + 32, ob);
+            umma::tmem_wait_ld();
+            umma::reg_fence32(oa);
+            umma::reg_fence32(ob);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float o[32];
-                umma::tmem_ld32(tmem + lane_base + kColO + chalf * 64 + 32 * q, o);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) o[x] = __uint_as_float(q ? ob[x] : oa[x]);
                 if (!row_on) continue;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
