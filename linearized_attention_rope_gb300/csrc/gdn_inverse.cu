@@ -185,17 +185,29 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     if (!done && err && tid == 0) atomicExch(err, kErrTimeout);
     umma::fence_after_sync();
     unsigned char* rec = rec_out + ((size_t)slot * L.Hq + h) * kRecordBytes;
+    // both 32-column halves of this thread's Gram row in flight together, one wait
+    uint32_t dg[2][32];
+    if (done) {
+        umma::tmem_ld32_async(tmem + ((uint32_t)(warp * 32) << 16), dg[0]);
+        umma::tmem_ld32_async(tmem + ((uint32_t)(warp * 32) << 16) + 32, dg[1]);
+        umma::tmem_wait_ld();
+        umma::reg_fence32(dg[0]);
+        umma::reg_fence32(dg[1]);
+    }
     if (warp < 2 && done) {  // rows 0..63: K K^T -> A
         const int r = tid;
         const float br = sBeta[r], gr = sG[r];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            float d[32];
-            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * half, d);
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
-                const int i = 32 * half + ii;
-                sA[r * kSA + i] = (i < r) ? br * exp2f(gr - sG[i]) * d[ii] : 0.f;
+            for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(sG + 32 * half + 4 * i4);
+                const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int ii = 4 * i4 + e, i = 32 * half + ii;
+                    sA[r * kSA + i] = (i < r) ? br * exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
+                }
             }
         }
     } else if (done) {  // rows 64..127: Q K^T -> P
@@ -204,11 +216,15 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float d[32];
-            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * half, d);
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
-                const int i = 32 * half + ii;
-                d[ii] = (i <= r) ? exp2f(gr - sG[i]) * d[ii] : 0.f;
+            for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(sG + 32 * half + 4 * i4);
+                const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int ii = 4 * i4 + e, i = 32 * half + ii;
+                    d[ii] = (i <= r) ? exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
+                }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -301,15 +317,24 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     if (warp < 2) {  // -Wm row r -> record image
         const int r = tid;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float wv[32];
-            umma::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * q4, wv);
+        for (int q2 = 0; q2 < 2; ++q2) {  // two 32-column TMEM loads in flight per wait
+            uint32_t w2[2][32];
+            umma::tmem_ld32_async(tmem + ((uint32_t)(warp * 32) << 16) + 64 * q2, w2[0]);
+            umma::tmem_ld32_async(tmem + ((uint32_t)(warp * 32) << 16) + 64 * q2 + 32, w2[1]);
+            umma::tmem_wait_ld();
+            umma::reg_fence32(w2[0]);
+            umma::reg_fence32(w2[1]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float* x = wv + 8 * u;
-                *reinterpret_cast<uint4*>(rec + kRecWm + umma::sw128_offset(r, 32 * q4 + 8 * u, 64)) =
-                    make_uint4(pack_h2(-x[0], -x[1]), pack_h2(-x[2], -x[3]), pack_h2(-x[4], -x[5]),
-                               pack_h2(-x[6], -x[7]));
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(w2[hh][8 * u + e]);
+                    *reinterpret_cast<uint4*>(rec + kRecWm + umma::sw128_offset(r, 64 * q2 + 32 * hh + 8 * u, 64)) =
+                        make_uint4(pack_h2(-x[0], -x[1]), pack_h2(-x[2], -x[3]), pack_h2(-x[4], -x[5]),
+                                   pack_h2(-x[6], -x[7]));
+                }
             }
         }
     }
