@@ -211,15 +211,14 @@ HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code);
  * its stream at stage boundaries.  Tensor-core path (bf16, head_dim 128):
  * 0 before the first kernel, 1 after the feature path, 2 after the softmax
  * branch, 6 after the decode-state hand-off.  The linear branch runs in up to
- * four parts of the chunk slots, each a chunk-local launch on the library's
- * low-priority side stream and a state launch (which also combines the two
- * branches) on the caller's stream: for part p, 7 + 4p before and 8 + 4p
- * after its chunk-local launch (the first beside the softmax, a later one
- * once 2 and the previous part's chunk-local launch are reached), 9 + 4p
- * before and 10 + 4p after its state launch (once 2, 8 + 4p and the previous
- * state launch are reached); marks of parts not run are recorded together
- * after the last state launch.  3 before the first and 4 after the last
- * chunk-local launch (side stream), 5 after the last state launch.
+ * four parts of the chunk slots, each a chunk-local launch and a state launch
+ * (which also combines the two branches), all on the caller's stream: for
+ * part p, 7 + 4p before and 8 + 4p after its chunk-local launch, 9 + 4p
+ * before and 10 + 4p after its state launch.  Without the hook each
+ * chunk-local launch runs beside the launch before it (the softmax, or the
+ * previous part's state launch); with the hook on, every launch runs alone,
+ * so each interval times one launch.  3 = 4 = 2; marks of parts not run are
+ * recorded together after the last state launch, 5 after it.
  * Token-serial path: 0, 1 as above, 2 = 3 = 1, 4 after the GDN kernel, 5
  * after the softmax + combine, 6 after the hand-off (7 to 22 not recorded).
  * Entries beyond n_events, or NULL entries, are skipped; n_events = 0

@@ -12,9 +12,13 @@ namespace hla {
 
 // RoPE angles at position p = 64 a + b come from two small tables and the
 // angle-addition identities, so the per-token work is fp32 only while every
-// table entry is formed and range-reduced in double precision.
-__global__ void rope_tables_kernel(LayerDims L, float2* __restrict__ fine,
-                                   float2* __restrict__ coarse, int n_coarse) {
+// table entry is formed and range-reduced in double precision.  The same
+// launch clears the error word and the item counters and writes the
+// per-sequence work tables of the softmax and chunked-GDN kernels, which all
+// depend on cu_seqlens alone: one launch ahead of the feature path instead of
+// four small ones spread over the step.
+__global__ void prefill_tables_kernel(LayerDims L, float2* __restrict__ fine, float2* __restrict__ coarse,
+                                      int n_coarse, PrefillTables t) {
     const int half = L.d / 2;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t n_fine = 64 * half;
@@ -30,13 +34,35 @@ __global__ void rope_tables_kernel(LayerDims L, float2* __restrict__ fine,
         rope_cs_exact(64 * a, L.theta[i], &c, &s);
         coarse[j] = make_float2(c, s);
     }
+    if (blockIdx.x != 0) return;
+    if (threadIdx.x < 4) t.err[threadIdx.x] = 0;
+    if (threadIdx.x < t.n_counters) t.counters[threadIdx.x] = 0;
+    // Work tables: base[s] = items of the sequences before s, base[n_seqs] = all.
+    int32_t* base = nullptr;
+    int per = 1;
+    int64_t skip = 0;
+    if (threadIdx.x == 32) base = t.blk_base, per = t.blk_rows;                                 // row blocks
+    if (threadIdx.x == 64) base = t.chunk_base, per = t.chunk_rows, skip = L.window + L.n_sinks;  // chunks
+    if (!base) return;
+    int32_t acc = 0;
+    for (int q = 0; q < L.n_seqs; ++q) {
+        base[q] = acc;
+        int64_t start, len;
+        seq_range(t.cu, q, L.total, &start, &len);
+        const int64_t m = len - skip;
+        acc += m > 0 ? (int32_t)((m + per - 1) / per) : 0;
+    }
+    base[L.n_seqs] = acc;
 }
 
-cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
-                               cudaStream_t st) {
+cudaError_t launch_prefill_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
+                                  const PrefillTables& t, cudaStream_t st) {
+    if (t.n_counters < 0 || t.n_counters > 32 || (t.blk_base && t.blk_rows <= 0) ||
+        (t.chunk_base && t.chunk_rows <= 0))
+        return cudaErrorInvalidValue;
     int64_t n = (int64_t)(64 + n_coarse) * (L.d / 2);
-    int blocks = (int)((n + 255) / 256);
-    rope_tables_kernel<<<blocks, 256, 0, st>>>(L, fine, coarse, n_coarse);
+    int blocks = (int)std::max<int64_t>(1, (n + 255) / 256);
+    prefill_tables_kernel<<<blocks, 256, 0, st>>>(L, fine, coarse, n_coarse, t);
     return cudaGetLastError();
 }
 

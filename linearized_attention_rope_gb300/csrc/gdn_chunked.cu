@@ -49,7 +49,7 @@ namespace hla {
 
 namespace {
 
-constexpr int kC = 64;    // chunk length (absorbed tokens)
+constexpr int kC = kGdnChunk;  // chunk length (absorbed tokens)
 constexpr int kD = 128;   // head dim
 constexpr int kNS = 64;   // value columns per CTA
 constexpr int kSlices = kD / kNS;
@@ -114,6 +114,9 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                    const float* __restrict__ lambda, __nv_bfloat16* __restrict__ out,
                    const float* __restrict__ S_in, float* __restrict__ S_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
+    // A launch that follows this one with programmatic stream serialization may start as soon as every
+    // CTA of this grid has reached this point, i.e. is resident (no effect on a plain launch).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);

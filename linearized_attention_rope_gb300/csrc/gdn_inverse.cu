@@ -24,7 +24,7 @@ namespace hla {
 
 namespace {
 
-constexpr int kC = 64, kD = 128, kThreads = 128;
+constexpr int kC = kGdnChunk, kD = 128, kThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kTmemCols = 128;               // Gram (64 columns), then Wm^T (128)
 constexpr uint32_t kK = 0;                        // [K ; Q] rows, K-major
@@ -42,43 +42,31 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Forward substitution for a 32 x 32 unit lower-triangular diagonal block of
-// (I + A): one warp per block, lane l owns row l of the inverse.  (The kernel
-// is persistent, so this fully unrolled code stays in the instruction cache.)
+// Inverse of a 32 x 32 unit lower-triangular diagonal block b of (I + A),
+// one warp per block: lane l owns column l of the inverse and runs the
+// forward substitution x_r = [r == l] - sum_{m < r} A[r][m] x_m in row order
+// (the A entries are shared-memory broadcasts, x stays in registers; four
+// partial sums per row keep the dependent chain short).  (The kernel is
+// persistent, so this fully unrolled code stays in the instruction cache.)
 __device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, int b, int l) {
-    float a[32], t[32];
+    float x[32];
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-        a[m] = sA[(32 * b + l) * kSA + 32 * b + m];
-        t[m] = (m == l) ? 1.f : 0.f;
+    for (int r = 0; r < 32; ++r) {
+        const float* ar = sA + (32 * b + r) * kSA + 32 * b;
+        float acc[4] = {r == l ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < r; ++m) acc[m & 3] = fmaf(-ar[m], x[m], acc[m & 3]);
+        x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
 #pragma unroll
-    for (int m = 0; m < 31; ++m) {
-        // row m is final once rows 0..m-1 have been folded into it
-#pragma unroll
-        for (int k = 0; k <= m; ++k) {
-            const float tm = __shfl_sync(0xffffffffu, t[k], m);
-            if (l > m) t[k] = fmaf(-a[m], tm, t[k]);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < 32; ++m) sT[(32 * b + l) * 68 + 32 * b + m] = t[m];
+    for (int r = 0; r < 32; ++r) sT[(32 * b + r) * 68 + 32 * b + l] = x[r];
 }
 
-__global__ void gdn_chunk_table_kernel(LayerDims L, const int32_t* __restrict__ cu, int32_t* __restrict__ base,
-                                       int32_t* __restrict__ counters, int n_counters) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    for (int i = 0; i < n_counters; ++i) counters[i] = 0;
-    int32_t acc = 0;
-    for (int s = 0; s < L.n_seqs; ++s) {
-        base[s] = acc;
-        int64_t start, len;
-        seq_range(cu, s, L.total, &start, &len);
-        const int64_t m = len - L.window - L.n_sinks;
-        acc += m > 0 ? (int32_t)((m + kC - 1) / kC) : 0;
-    }
-    base[L.n_seqs] = acc;
-}
+// Launched with programmatic stream serialization, this grid may run beside the one before it in the
+// stream (it reads nothing that grid writes); waiting for that grid before leaving keeps "this grid is
+// done" implying "the one before it is done" for whatever follows in the stream.  No effect on a plain
+// launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 3)
 gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
@@ -103,7 +91,10 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     // items (chunk slot, q-head) of slots [slot_lo, slot_hi), taken one at a time from `counter`
     const int64_t item_lo = (int64_t)slot_lo * L.Hq;
     const int64_t item_hi = (int64_t)min(slot_hi, __ldg(chunk_base + L.n_seqs)) * L.Hq;
-    if (item_lo >= item_hi) return;  // whole CTA leaves together
+    if (item_lo >= item_hi) {  // whole CTA leaves together
+        grid_dependency_wait();
+        return;
+    }
 
     if (tid == 0) {
         umma::mbar_init(mbar, 1);
@@ -344,21 +335,17 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
+    grid_dependency_wait();
 }
 
 }  // namespace
 
 size_t gdn_chunk_slots(int64_t total, int n_seqs) { return (size_t)(total / kC) + (size_t)n_seqs + 1; }
 
-cudaError_t launch_gdn_chunk_table(const LayerDims& L, const int32_t* cu, int32_t* chunk_base, int32_t* counters,
-                                   int n_counters, cudaStream_t st) {
-    gdn_chunk_table_kernel<<<1, 32, 0, st>>>(L, cu, chunk_base, counters, n_counters);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
                                const float* beta, const int32_t* cu, const int32_t* chunk_base, int slot_lo,
-                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, cudaStream_t st) {
+                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, bool beside_prior,
+                               cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -376,9 +363,18 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
     }
     const int64_t items = (int64_t)(slot_hi - slot_lo) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
-    gdn_inverse_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, qhat, khat, g, beta, cu, chunk_base, slot_lo, slot_hi,
-                                                          counter, rec_out, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = beside_prior ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gdn_inverse_kernel, L, qhat, khat, g, beta, cu, chunk_base, slot_lo, slot_hi,
+                              counter, rec_out, err);
 }
 
 }  // namespace hla

@@ -132,18 +132,26 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     const Tin* ki = static_cast<const Tin*>(k);
     const Tin* vi = static_cast<const Tin*>(v);
 
-    HLA_TRY(cudaMemsetAsync(err, 0, 16, stream));
-    HLA_TRY(mark_stage(0, stream));
-    HLA_TRY(launch_rope_tables(L, fine, coarse, w.n_coarse, stream));
-    HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
-                                     err, stream));
-    HLA_TRY(mark_stage(1, stream));
     float* S_out = st ? st->S : nullptr;
     bool chunked = false;
     if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
+    PrefillTables tabs = {cu, err, nullptr, 0, nullptr, 0, nullptr, 0};
     if (chunked) {
-        // features -> { softmax (final rows, fp16 rows to finish) on the caller's stream,
-        //               chunk-local GDN on the side stream } -> GDN state + combine
+        tabs.counters = reinterpret_cast<int32_t*>(ws + w.counters);
+        tabs.n_counters = kGdnParts;
+        tabs.blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
+        tabs.blk_rows = window_softmax_tc_rows(L);
+        tabs.chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
+        tabs.chunk_rows = kGdnChunk;
+    }
+    HLA_TRY(mark_stage(0, stream));
+    HLA_TRY(launch_prefill_tables(L, fine, coarse, w.n_coarse, tabs, stream));
+    HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
+                                     err, stream));
+    HLA_TRY(mark_stage(1, stream));
+    if (chunked) {
+        // features -> softmax (final rows, fp16 rows to finish) -> per part: chunk-local GDN (beside
+        // the launch before it) -> GDN state + combine
         if constexpr (std::is_same<Tf, __half>::value) {
             __half* osm = reinterpret_cast<__half*>(ws + w.osm);
             int32_t* blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
@@ -152,41 +160,26 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
             float* smid = reinterpret_cast<float*>(ws + w.smid);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-            // The GDN runs in kGdnParts parts of the chunk slots.  The chunk-local kernel of the first
-            // part runs on a low-priority side stream beside the softmax; the state kernel of each part
-            // (64 or so CTAs) then runs beside the chunk-local kernel of the next, which takes the SMs
-            // left free; each state launch continues from the state the previous one saved.
+            // The GDN runs in kGdnParts parts of the chunk slots, all on the caller's stream.  Each
+            // chunk-local launch follows the launch before it (the softmax, then the state kernel of the
+            // previous part) with programmatic stream serialization: its CTAs are placed once every CTA of
+            // that launch is resident and take the SMs it leaves free (a state CTA, of 227 KB, needs an
+            // SM to itself), and it completes only after that launch has.  Each state launch continues
+            // from the state the previous one saved.  With the stage hook on, the launches run one after
+            // another so that each can be timed alone.
             const int n_slots = (int)gdn_chunk_slots(L.total, L.n_seqs);
             int bound[kGdnParts + 1];
             for (int p = 0; p <= kGdnParts; ++p) bound[p] = (int)((int64_t)n_slots * p / kGdnParts);
-            SideStream* side = nullptr;
-            HLA_TRY(side_stream(&side));  // per host thread and device; see hla_common.cuh
-            HLA_TRY(cudaEventRecord(side->fork, stream));
-            HLA_TRY(cudaStreamWaitEvent(side->lo, side->fork, 0));
-            HLA_TRY(mark_stage(3, side->lo));
-            HLA_TRY(launch_gdn_chunk_table(L, cu, chunk_base, counters, kGdnParts, side->lo));
-            HLA_TRY(mark_stage(7, side->lo));
-            HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, bound[0], bound[1], counters, rec, err,
-                                       side->lo));
-            HLA_TRY(mark_stage(8, side->lo));
-            HLA_TRY(cudaEventRecord(side->part[0], side->lo));
+            const bool overlap = t_n_stage_events == 0;
             HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
             HLA_TRY(mark_stage(2, stream));
-            // the second chunk-local launch only once the softmax is done, so that the first state
-            // launch, ready at the same time and on the higher-priority stream, is placed first (a
-            // later one waits for the chunk-local launch before it, as the state launch it races does)
-            HLA_TRY(cudaEventRecord(side->main_mid, stream));
-            HLA_TRY(cudaStreamWaitEvent(side->lo, side->main_mid, 0));
-            for (int p = 1; p < kGdnParts; ++p) {
-                HLA_TRY(mark_stage(7 + 4 * p, side->lo));
-                HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, bound[p], bound[p + 1], counters + p,
-                                           rec, err, side->lo));
-                HLA_TRY(mark_stage(8 + 4 * p, side->lo));
-                HLA_TRY(cudaEventRecord(side->part[p], side->lo));
-            }
-            HLA_TRY(mark_stage(4, side->lo));
+            HLA_TRY(mark_stage(3, stream));
+            HLA_TRY(mark_stage(4, stream));
             for (int p = 0; p < kGdnParts; ++p) {
-                HLA_TRY(cudaStreamWaitEvent(stream, side->part[p], 0));
+                HLA_TRY(mark_stage(7 + 4 * p, stream));
+                HLA_TRY(launch_gdn_inverse(L, qh, kh, g, beta, cu, chunk_base, bound[p], bound[p + 1], counters + p,
+                                           rec, err, overlap, stream));
+                HLA_TRY(mark_stage(8 + 4 * p, stream));
                 HLA_TRY(mark_stage(9 + 4 * p, stream));
                 HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, bound[p], bound[p + 1], rec, osm, lambda, o,
                                            p > 0 ? smid : nullptr, p + 1 < kGdnParts ? smid : S_out, err, stream));
@@ -371,7 +364,7 @@ HLA_API int hla_prefill_launch_count(const hla_params* prm, int with_state, int*
     if (!out) return HLA_ERR_INVALID_ARG;
     // rope tables, features; tensor-core path: softmax block table + softmax, chunk table, one
     // chunk-local and one state launch per part; token-serial path: GDN, softmax
-    *out = (uses_chunked_gdn(prm) ? 5 + 2 * kGdnParts : 4) + (with_state ? 1 : 0);
+    *out = (uses_chunked_gdn(prm) ? 3 + 2 * kGdnParts : 4) + (with_state ? 1 : 0);
     return HLA_OK;
 }
 

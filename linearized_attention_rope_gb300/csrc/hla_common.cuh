@@ -106,10 +106,27 @@ __device__ __forceinline__ void rope_cs_exact(int64_t p, double theta, float* c,
 
 // ---- kernel launchers (each returns the cudaError_t of its launch) --------
 
+// What the first launch of a prefill writes besides the RoPE tables (device
+// pointers; a null table is skipped): err[0..3] = 0, counters[0..n_counters)
+// = 0 (n_counters <= 32), and per-sequence work tables blk_base / chunk_base
+// (n_seqs + 1 int32 each): base[s] = the items of sequences before s, where
+// a sequence of len rows has ceil(len / blk_rows) softmax row blocks and
+// ceil((len - n_sinks - W) / chunk_rows) GDN chunks (none if not positive).
+struct PrefillTables {
+    const int32_t* cu;
+    int32_t* err;
+    int32_t* counters;
+    int n_counters;
+    int32_t* blk_base;
+    int blk_rows;
+    int32_t* chunk_base;
+    int chunk_rows;
+};
 // RoPE tables: fine[b][i] = (cos, sin)(b * theta_i), b < 64;
-// coarse[a][i] = (cos, sin)(64 a * theta_i), a < n_coarse.
-cudaError_t launch_rope_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
-                               cudaStream_t st);
+// coarse[a][i] = (cos, sin)(64 a * theta_i), a < n_coarse; plus the tables
+// above.  One launch.
+cudaError_t launch_prefill_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
+                                  const PrefillTables& t, cudaStream_t st);
 
 // Feature path for every (token, head): RoPE'd q/k, and qhat, khat, vhat.
 // Tf = float (fp32 layer) or __half (bf16 layer).
@@ -120,16 +137,13 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st);
 
 // Per host thread and device: a second stream for kernels that can run
-// beside the caller's stream, a low-priority one for work that should only
-// take the SMs the caller's stream leaves free, and the events that fork them
-// off the caller's stream and join them back (fork, join) or order steps
-// between the two (part[k], main_mid).  Created on first use and kept for the
-// thread's lifetime.
+// beside the caller's stream, and the events that fork it off the caller's
+// stream and join it back.  Created on first use and kept for the thread's
+// lifetime.
 constexpr int kMaxGdnParts = 4;
 struct SideStream {
-    cudaStream_t s = nullptr, lo = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, main_mid = nullptr;
-    cudaEvent_t part[kMaxGdnParts] = {};  // a step of the low-priority stream done
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
 cudaError_t side_stream(SideStream** out);
 
@@ -147,17 +161,21 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
 // (64 x 128), T diag(beta) and P (64 x 64) as fp16 swizzled K-major tile
 // images, then gamma and the key decay (fp32, 64 each).
 // Step 2: the state-carrying kernel.
+constexpr int kGdnChunk = 64;  // C, rows of a chunk
 constexpr uint32_t kRecWm = 0, kRecTb = 16384, kRecP = 24576, kRecVec = 32768, kRecordBytes = 33280;
-// The chunk table (n_seqs + 1 entries, on the device) comes from
-// launch_gdn_chunk_table, which also zeroes the item counters; each
+// The chunk table (n_seqs + 1 entries, on the device; chunk_rows = 64) and
+// zeroed item counters come from launch_prefill_tables; each
 // launch_gdn_inverse covers the chunk slots [slot_lo, slot_hi) (clipped to
-// the table's total), its CTAs taking items from its own counter.
+// the table's total), its CTAs taking items from its own counter.  With
+// beside_prior it is launched with programmatic stream serialization: its
+// CTAs are placed once every CTA of the launch before it in the stream (a
+// softmax or state launch, which signal this at entry) is resident, and it
+// completes only after that launch has.
 size_t gdn_chunk_slots(int64_t total, int n_seqs);
-cudaError_t launch_gdn_chunk_table(const LayerDims& L, const int32_t* cu, int32_t* chunk_base, int32_t* counters,
-                                   int n_counters, cudaStream_t st);
 cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __half* khat, const float* g,
                                const float* beta, const int32_t* cu, const int32_t* chunk_base, int slot_lo,
-                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, cudaStream_t st);
+                               int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, bool beside_prior,
+                               cudaStream_t st);
 // The chunks of slots [slot_lo, slot_hi) of every sequence, continuing from
 // S_in (fp32 [n_seqs][Hq][d][d]; read only for sequences with chunks before
 // slot_lo, zero state otherwise; may be null if none has).  out rows of
@@ -179,9 +197,10 @@ cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr
 // Tensor-core sink + window softmax (head_dim 128, G in {1, 2, 4, 8}; bf16
 // values).  Rows of positions >= n_sinks + W (unless the linear branch is
 // off) get the normalised softmax output in o_sm (fp16) for the GDN kernel to
-// finish; all other rows are written to out.  blk_base: n_seqs + 1 int32 of
-// workspace (per-sequence block table).
+// finish; all other rows are written to out.  blk_base: the per-sequence
+// block table from launch_prefill_tables with blk_rows = 128 / G.
 bool window_softmax_tc_supported(const LayerDims& L);
+inline int window_softmax_tc_rows(const LayerDims& L) { return 128 / L.G; }
 cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
                                      const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
                                      int32_t* err, cudaStream_t st);

@@ -13,14 +13,9 @@ cudaError_t side_stream(SideStream** out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     SideStream& ss = t_side[dev];
     if (!ss.s) {
-        int least = 0, greatest = 0;  // numerically largest = lowest priority
-        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
         if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaStreamCreateWithPriority(&ss.lo, cudaStreamNonBlocking, least)) != cudaSuccess) return e;
-        for (cudaEvent_t* ev : {&ss.fork, &ss.join, &ss.main_mid})
+        for (cudaEvent_t* ev : {&ss.fork, &ss.join})
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
-        for (cudaEvent_t& ev : ss.part)
-            if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     *out = &ss;
     return cudaSuccess;

@@ -55,18 +55,6 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void block_table_kernel(LayerDims L, int QB, const int32_t* __restrict__ cu, int32_t* __restrict__ base) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int32_t acc = 0;
-    for (int s = 0; s < L.n_seqs; ++s) {
-        base[s] = acc;
-        int64_t start, len;
-        seq_range(cu, s, L.total, &start, &len);
-        acc += (int32_t)((len + QB - 1) / QB);
-    }
-    base[L.n_seqs] = acc;
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
 window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -74,6 +62,10 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
                          const int32_t* __restrict__ cu, const int32_t* __restrict__ blk_base,
                          __half* __restrict__ o_sm, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
+    // A launch that follows this one with programmatic stream serialization may start once every CTA of
+    // this grid has reached this point (no effect on a plain launch); its CTAs then take the room these
+    // leave free.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* red = reinterpret_cast<float*>(sm + kRed);  // [0: max | 1: sum][column half][row]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 16);
@@ -335,7 +327,6 @@ cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const
     }
     if (L.total <= 0) return cudaSuccess;
     const int QB = kD / L.G;
-    block_table_kernel<<<1, 32, 0, st>>>(L, QB, cu, blk_base);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mk64, mv64;
