@@ -34,6 +34,7 @@ __global__ void prefill_tables_kernel(LayerDims L, float2* __restrict__ fine, fl
         rope_cs_exact(64 * a, L.theta[i], &c, &s);
         coarse[j] = make_float2(c, s);
     }
+    pdl_trigger();  // the features launch may start; it waits for this grid before reading
     if (blockIdx.x != 0) return;
     if (threadIdx.x < 4) t.err[threadIdx.x] = 0;
     if (threadIdx.x < t.n_counters) t.counters[threadIdx.x] = 0;
@@ -318,6 +319,8 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
     constexpr int NP = Row::NP, HALF = Row::HALF, NC = Row::NC;
     constexpr int STEPB = kBlk * D * (int)sizeof(Tin);
     extern __shared__ __align__(16) unsigned char ring_s[];  // [warp][kRing][kBlk tokens][D]
+    pdl_trigger();  // the softmax launch may set up beside this one; it waits for this grid before reading
+    pdl_wait();     // after the table launch (no effect on a plain launch)
     const int lane = threadIdx.x & 31;
     unsigned char* wring = ring_s + (size_t)(threadIdx.x >> 5) * kRing * STEPB;
     int hr = blockIdx.y * kFeatWarps + (threadIdx.x >> 5);
@@ -374,7 +377,7 @@ template <typename Tin, typename Tf, int D>
 static cudaError_t launch_features_d(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v, const float* wq,
                                      const float* wk, const float* wv, const int32_t* cu, const float2* fine,
                                      const float2* coarse, Tf* qr, Tf* kr, Tf* qhat, Tf* khat, Tf* vhat,
-                                     int32_t* err, cudaStream_t st) {
+                                     int32_t* err, bool after_prior, cudaStream_t st) {
     const size_t smem = (size_t)kFeatWarps * kRing * kBlk * D * sizeof(Tin);
     static int resident = 0;  // CTAs resident on the device at once (per instantiation)
     if (!resident) {
@@ -391,33 +394,33 @@ static cudaError_t launch_features_d(const LayerDims& L, const Tin* q, const Tin
     }
     const int row_groups = (L.Hq + 2 * L.Hkv + kFeatWarps - 1) / kFeatWarps;
     const int64_t span = feature_span(L.total, row_groups, resident);
-    dim3 grid((unsigned)((L.total + span - 1) / span), (unsigned)row_groups);
-    features_kernel<Tin, Tf, D><<<grid, 32 * kFeatWarps, smem, st>>>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr,
-                                                                       kr, qhat, khat, vhat, err, (int)span);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3((unsigned)((L.total + span - 1) / span), (unsigned)row_groups), dim3(32 * kFeatWarps), smem,
+                 st, after_prior);
+    return cudaLaunchKernelEx(&lc.cfg, features_kernel<Tin, Tf, D>, L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr,
+                              qhat, khat, vhat, err, (int)span);
 }
 
 template <typename Tin, typename Tf>
 cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
                             const float* wq, const float* wk, const float* wv, const int32_t* cu,
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
-                            Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st) {
+                            Tf* khat, Tf* vhat, int32_t* err, bool after_prior, cudaStream_t st) {
     if (L.total <= 0) return cudaSuccess;
     if (L.d == 128)
         return launch_features_d<Tin, Tf, 128>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat,
-                                               err, st);
+                                               err, after_prior, st);
     return launch_features_d<Tin, Tf, 64>(L, q, k, v, wq, wk, wv, cu, fine, coarse, qr, kr, qhat, khat, vhat, err,
-                                          st);
+                                          after_prior, st);
 }
 
 template cudaError_t launch_features<float, float>(const LayerDims&, const float*, const float*,
                                                    const float*, const float*, const float*,
                                                    const float*, const int32_t*, const float2*,
                                                    const float2*, float*, float*, float*, float*,
-                                                   float*, int32_t*, cudaStream_t);
+                                                   float*, int32_t*, bool, cudaStream_t);
 template cudaError_t launch_features<__nv_bfloat16, __half>(
     const LayerDims&, const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*,
     const float*, const float*, const float*, const int32_t*, const float2*, const float2*, __half*,
-    __half*, __half*, __half*, __half*, int32_t*, cudaStream_t);
+    __half*, __half*, __half*, __half*, int32_t*, bool, cudaStream_t);
 
 }  // namespace hla

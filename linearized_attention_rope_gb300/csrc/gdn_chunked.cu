@@ -114,9 +114,11 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                    const float* __restrict__ lambda, __nv_bfloat16* __restrict__ out,
                    const float* __restrict__ S_in, float* __restrict__ S_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
-    // A launch that follows this one with programmatic stream serialization may start as soon as every
-    // CTA of this grid has reached this point, i.e. is resident (no effect on a plain launch).
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // A launch that follows this one with programmatic stream serialization (the next part's chunk-local
+    // kernel) may start as soon as every CTA of this grid has reached this point, i.e. is resident, even
+    // before the wait below: it reads only what the features and table launches wrote, which completed
+    // before the chunk-local launch this one waits for started.  No effect on a plain launch.
+    pdl_trigger();
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
@@ -129,17 +131,6 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     const uint32_t sbase = umma::smem_addr(sm);
     const uint32_t bar0 = umma::smem_addr(sm + kBar);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-
-    int64_t start, len;
-    seq_range(cu, n, L.total, &start, &len);
-    const int64_t j_end = len - W;
-    const int seq_chunks = j_end > L.n_sinks ? (int)((j_end - L.n_sinks + kC - 1) / kC) : 0;
-    const int slot0 = __ldg(chunk_base + n);
-    // this launch: the sequence's chunks c_lo .. c_lo + n_chunks - 1 (those in slots [slot_lo, slot_hi)),
-    // loop index c = chunk - c_lo
-    const int c_lo = min(max(slot_lo - slot0, 0), seq_chunks);
-    const int n_chunks = min(max(slot_hi - slot0, 0), seq_chunks) - c_lo;
-    const bool resume = S_in && c_lo > 0;  // continue from the state the previous launch left
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) umma::mbar_init(bar(i), (i == kFree || i == kFree + 1) ? 2 : 1);
@@ -157,6 +148,21 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // Launched with programmatic stream serialization, the CTAs get here while the launch before this
+    // one (the chunk-local kernel) may still run: wait for it to complete, and its writes (and those of
+    // every launch before it) to be visible, before the first global read.  No effect on a plain launch.
+    pdl_wait();
+
+    int64_t start, len;
+    seq_range(cu, n, L.total, &start, &len);
+    const int64_t j_end = len - W;
+    const int seq_chunks = j_end > L.n_sinks ? (int)((j_end - L.n_sinks + kC - 1) / kC) : 0;
+    const int slot0 = __ldg(chunk_base + n);
+    // this launch: the sequence's chunks c_lo .. c_lo + n_chunks - 1 (those in slots [slot_lo, slot_hi)),
+    // loop index c = chunk - c_lo
+    const int c_lo = min(max(slot_lo - slot0, 0), seq_chunks);
+    const int n_chunks = min(max(slot_hi - slot0, 0), seq_chunks) - c_lo;
+    const bool resume = S_in && c_lo > 0;  // continue from the state the previous launch left
 
     // One leader per role polls the mbarrier (an inline try first, the bounded
     // loop only if the phase is still open) and posts the outcome in a shared
@@ -370,7 +376,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
                                const unsigned char* rec_in, const __half* o_sm, const float* lambda,
-                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, cudaStream_t st) {
+                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, bool beside_prior,
+                               cudaStream_t st) {
     static bool configured = false;  // the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -385,10 +392,9 @@ cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __h
         !tma::make_map_f16_3d(&mk, khat, kD, (uint64_t)L.Hkv, (uint64_t)L.total) ||
         !tma::make_map_f16_3d(&mv, vhat, kD, (uint64_t)L.Hkv, (uint64_t)L.total))
         return cudaErrorInvalidValue;
-    dim3 grid(L.Hq * kSlices, L.n_seqs);
-    gdn_chunked_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, cu, chunk_base, slot_lo, slot_hi, rec_in,
-                                                          o_sm, lambda, out, S_in, S_out, err);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3(L.Hq * kSlices, L.n_seqs), dim3(kThreads), kSmemAlloc, st, beside_prior);
+    return cudaLaunchKernelEx(&lc.cfg, gdn_chunked_kernel, L, mq, mk, mv, cu, chunk_base, slot_lo, slot_hi, rec_in, o_sm,
+                              lambda, out, S_in, S_out, err);
 }
 
 }  // namespace hla

@@ -66,7 +66,7 @@ __device__ __forceinline__ void invert_diag_block32(const float* sA, float* sT, 
 // stream (it reads nothing that grid writes); waiting for that grid before leaving keeps "this grid is
 // done" implying "the one before it is done" for whatever follows in the stream.  No effect on a plain
 // launch.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { pdl_wait(); }
 
 __global__ void __launch_bounds__(kThreads, 3)
 gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* __restrict__ khat,
@@ -75,6 +75,9 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
                    const int32_t* __restrict__ chunk_base, int slot_lo, int slot_hi,
                    int32_t* __restrict__ counter, unsigned char* __restrict__ rec_out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
+    // The state launch that follows with programmatic stream serialization may place its CTAs (each needs
+    // an SM to itself) as SMs drain, and set up; it waits for this grid before its first global read.
+    pdl_trigger();
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* sA = reinterpret_cast<float*>(sm + kA32);
     float* sT = reinterpret_cast<float*>(sm + kT32);
@@ -363,17 +366,8 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
     }
     const int64_t items = (int64_t)(slot_hi - slot_lo) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemAlloc;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = beside_prior ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gdn_inverse_kernel, L, qhat, khat, g, beta, cu, chunk_base, slot_lo, slot_hi,
+    LaunchCfg lc(dim3(grid), dim3(kThreads), kSmemAlloc, st, beside_prior);
+    return cudaLaunchKernelEx(&lc.cfg, gdn_inverse_kernel, L, qhat, khat, g, beta, cu, chunk_base, slot_lo, slot_hi,
                               counter, rec_out, err);
 }
 

@@ -146,8 +146,17 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     }
     HLA_TRY(mark_stage(0, stream));
     HLA_TRY(launch_prefill_tables(L, fine, coarse, w.n_coarse, tabs, stream));
+    // The GDN launches run with programmatic stream serialization (their CTAs set up while the launch
+    // before them drains), unless the stage hook wants each launch timed alone; the features and softmax
+    // launches are plain (CTAs waiting beside the kernel before them slowed it by more than the launch
+    // latency they hid).  The order
+    // stays transitive: a kernel that reads data without waiting for its predecessor (the chunk-local
+    // GDN) starts only after a trigger that its predecessor gives once its own wait has returned, and
+    // every kernel waits for its predecessor before it completes, so a completed launch implies that
+    // all launches before it completed.
+    const bool overlap = t_n_stage_events == 0;
     HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
-                                     err, stream));
+                                     err, false, stream));
     HLA_TRY(mark_stage(1, stream));
     if (chunked) {
         // features -> softmax (final rows, fp16 rows to finish) -> per part: chunk-local GDN (beside
@@ -160,18 +169,18 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
             unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
             float* smid = reinterpret_cast<float*>(ws + w.smid);
             __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-            // The GDN runs in kGdnParts parts of the chunk slots, all on the caller's stream.  Each
-            // chunk-local launch follows the launch before it (the softmax, then the state kernel of the
-            // previous part) with programmatic stream serialization: its CTAs are placed once every CTA of
-            // that launch is resident and take the SMs it leaves free (a state CTA, of 227 KB, needs an
-            // SM to itself), and it completes only after that launch has.  Each state launch continues
-            // from the state the previous one saved.  With the stage hook on, the launches run one after
-            // another so that each can be timed alone.
+            // The GDN runs in kGdnParts parts of the chunk slots, all on the caller's stream, every launch
+            // after the softmax with programmatic stream serialization.  A chunk-local launch follows the
+            // softmax or the previous part's state launch: its CTAs are placed once every CTA of that
+            // launch is resident and take the SMs it leaves free (a state CTA, of 227 KB, needs an SM to
+            // itself), and it completes only after that launch has.  A state launch follows its part's
+            // chunk-local launch: its CTAs are placed as SMs drain and set up, then wait for that launch
+            // to complete.  Each state launch continues from the state the previous one saved.  With the
+            // stage hook on, the launches run one after another so that each can be timed alone.
             const int n_slots = (int)gdn_chunk_slots(L.total, L.n_seqs);
             int bound[kGdnParts + 1];
             for (int p = 0; p <= kGdnParts; ++p) bound[p] = (int)((int64_t)n_slots * p / kGdnParts);
-            const bool overlap = t_n_stage_events == 0;
-            HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, stream));
+            HLA_TRY(launch_window_softmax_tc(L, qr, kr, vi, cu, blk_base, osm, o, err, false, stream));
             HLA_TRY(mark_stage(2, stream));
             HLA_TRY(mark_stage(3, stream));
             HLA_TRY(mark_stage(4, stream));
@@ -182,7 +191,8 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
                 HLA_TRY(mark_stage(8 + 4 * p, stream));
                 HLA_TRY(mark_stage(9 + 4 * p, stream));
                 HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, bound[p], bound[p + 1], rec, osm, lambda, o,
-                                           p > 0 ? smid : nullptr, p + 1 < kGdnParts ? smid : S_out, err, stream));
+                                           p > 0 ? smid : nullptr, p + 1 < kGdnParts ? smid : S_out, err, overlap,
+                                           stream));
                 HLA_TRY(mark_stage(10 + 4 * p, stream));
             }
             for (int p = kGdnParts; p < kMaxGdnParts; ++p)  // absent parts: zero-length marks

@@ -106,6 +106,30 @@ __device__ __forceinline__ void rope_cs_exact(int64_t p, double theta, float* c,
 
 // ---- kernel launchers (each returns the cudaError_t of its launch) --------
 
+// Launch configuration for cudaLaunchKernelEx; with after_prior, programmatic
+// stream serialization: the kernel's CTAs may start once every CTA of the
+// launch before it in the stream has executed griddepcontrol.launch_dependents
+// (or exited), and the kernel orders itself after that launch with
+// griddepcontrol.wait.  Used in place (cfg points at attr).
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool after_prior) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = after_prior ? 1 : 0;
+    }
+    LaunchCfg(const LaunchCfg&) = delete;
+    LaunchCfg& operator=(const LaunchCfg&) = delete;
+};
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // What the first launch of a prefill writes besides the RoPE tables (device
 // pointers; a null table is skipped): err[0..3] = 0, counters[0..n_counters)
 // = 0 (n_counters <= 32), and per-sequence work tables blk_base / chunk_base
@@ -130,11 +154,13 @@ cudaError_t launch_prefill_tables(const LayerDims& L, float2* fine, float2* coar
 
 // Feature path for every (token, head): RoPE'd q/k, and qhat, khat, vhat.
 // Tf = float (fp32 layer) or __half (bf16 layer).
+// With after_prior, launched with programmatic stream serialization after the
+// table launch (its CTAs wait for it before their first read).
 template <typename Tin, typename Tf>
 cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
                             const float* wq, const float* wk, const float* wv, const int32_t* cu,
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
-                            Tf* khat, Tf* vhat, int32_t* err, cudaStream_t st);
+                            Tf* khat, Tf* vhat, int32_t* err, bool after_prior, cudaStream_t st);
 
 // Per host thread and device: a second stream for kernels that can run
 // beside the caller's stream, and the events that fork it off the caller's
@@ -181,11 +207,15 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
 // slot_lo, zero state otherwise; may be null if none has).  out rows of
 // positions >= n_sinks + W of those chunks: bf16(o_sm + lambda_h o_lin) (none
 // if out is null or the linear branch is switched off); the state after the
-// last chunk in range into S_out (may be null).
+// last chunk in range into S_out (may be null).  With beside_prior it is
+// launched with programmatic stream serialization: its CTAs may be placed and
+// set up while the launch before it (which signals this at entry) still
+// runs, and wait for that launch to complete before their first global read.
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
                                const unsigned char* rec_in, const __half* o_sm, const float* lambda,
-                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, cudaStream_t st);
+                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, bool beside_prior,
+                               cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>
@@ -201,9 +231,11 @@ cudaError_t launch_window_softmax(const LayerDims& L, const Tf* qr, const Tf* kr
 // block table from launch_prefill_tables with blk_rows = 128 / G.
 bool window_softmax_tc_supported(const LayerDims& L);
 inline int window_softmax_tc_rows(const LayerDims& L) { return 128 / L.G; }
+// With after_prior, launched with programmatic stream serialization after the
+// features launch: CTAs set up beside it, then wait for it.
 cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
                                      const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
-                                     int32_t* err, cudaStream_t st);
+                                     int32_t* err, bool after_prior, cudaStream_t st);
 
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>

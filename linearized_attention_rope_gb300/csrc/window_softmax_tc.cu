@@ -62,10 +62,6 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
                          const int32_t* __restrict__ cu, const int32_t* __restrict__ blk_base,
                          __half* __restrict__ o_sm, __nv_bfloat16* __restrict__ out, int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
-    // A launch that follows this one with programmatic stream serialization may start once every CTA of
-    // this grid has reached this point (no effect on a plain launch); its CTAs then take the room these
-    // leave free.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float* red = reinterpret_cast<float*>(sm + kRed);  // [0: max | 1: sum][column half][row]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 16);
@@ -78,10 +74,6 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
     const uint32_t sbase = umma::smem_addr(sm);
     const uint32_t bar_ld = umma::smem_addr(sm + kBar), bar_mma = bar_ld + 8;
     const float qscale = 0.088388347648318447f * 1.4426950408889634f;  // 1/sqrt(128) * log2(e)
-    const int64_t n_blocks = __ldg(blk_base + L.n_seqs);
-    const int64_t n_items = n_blocks * L.Hkv;
-    if ((int64_t)blockIdx.x >= n_items) return;  // whole CTA leaves together
-
     if (tid == 0) {
         umma::mbar_init(bar_ld, 1);
         umma::mbar_init(bar_mma, 1);
@@ -92,6 +84,20 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // Launched with programmatic stream serialization, the CTAs get here while the features launch may
+    // still run: wait for it (and everything before it) before the first global read.  Only then may a
+    // launch that follows this one with programmatic stream serialization start (the chunk-local GDN,
+    // which reads the features without a wait of its own); its CTAs take the room these leave free.
+    pdl_wait();
+    pdl_trigger();
+    const int64_t n_blocks = __ldg(blk_base + L.n_seqs);
+    const int64_t n_items = n_blocks * L.Hkv;
+    if ((int64_t)blockIdx.x >= n_items) {  // whole CTA leaves together
+        umma::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
     uint32_t ph_ld = 0, ph_mma = 0;
 
     // tid 0 waits with a bound; the CTA then agrees on the outcome
@@ -312,7 +318,7 @@ bool window_softmax_tc_supported(const LayerDims& L) {
 
 cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
                                      const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
-                                     int32_t* err, cudaStream_t st) {
+                                     int32_t* err, bool after_prior, cudaStream_t st) {
     static bool configured = false;
     static int n_sm = 0;
     if (!configured) {
@@ -338,9 +344,9 @@ cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const
         return cudaErrorInvalidValue;
     const int64_t items_max = (L.total / QB + L.n_seqs + 1) * (int64_t)L.Hkv;
     const unsigned grid = (unsigned)std::min<int64_t>(items_max, (int64_t)n_sm * 2);
-    window_softmax_tc_kernel<<<grid, kThreads, kSmemAlloc, st>>>(L, mq, mk, mv, mk64, mv64, cu, blk_base, o_sm, out,
-                                                                err);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3(grid), dim3(kThreads), kSmemAlloc, st, after_prior);
+    return cudaLaunchKernelEx(&lc.cfg, window_softmax_tc_kernel, L, mq, mk, mv, mk64, mv64, cu, blk_base, o_sm, out,
+                              err);
 }
 
 }  // namespace hla
