@@ -430,7 +430,7 @@ def run_decode_bench(args, dist, peaks):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": None, "algorithmic_bytes_per_step": nbytes},
-            "clocks": clocks.summary(), "gpu_launches": 5 * K}  # features, state, softmax, combine, position
+            "clocks": clocks.summary(), "gpu_launches": 3 * K}  # features; state + softmax; combine
 
 
 # ---------------------------------------------------------------------------

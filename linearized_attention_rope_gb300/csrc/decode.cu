@@ -112,7 +112,7 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
     const float*, const __half*, const __half*, const int32_t*, const hla_state&, cudaStream_t);
 
 // ---------------------------------------------------------------------------
-// One decode step, in four kernels over per-step scratch (hla_state.scratch):
+// One decode step, in three launches over per-step scratch (hla_state.scratch):
 //  1. features (CTA per kv head and sequence): RoPE q, k of the new token p;
 //     short conv of q (the G heads of the group), k and v with their
 //     histories; L2 norms.  The new token goes into the KV ring (slot p, or
@@ -128,17 +128,16 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
 //     window fills its slots in order, then stays full), so a split is a
 //     plain range of slots; per head of the group a running max, sum and P V
 //     over its keys go to scratch.
-//  4. combine (CTA per sequence): splits merged by their maxima,
-//     o = o_sm + lambda_h o_lin.
-// Kernels 2 and 3 stream the state and the ring, the step's bulk traffic,
-// with many CTAs per SM; 2 runs on the side stream beside 3.
+//  4. combine (CTA per q-head and sequence): splits merged by their maxima,
+//     o = o_sm + lambda_h o_lin; then pos += 1.
+// Steps 2 and 3 stream the state and the ring, the step's bulk traffic; they
+// run as one launch whose CTAs are state units and softmax splits in turn, so
+// both streams share every wave.
 constexpr int kMaxG = 8;
 constexpr int kFeatThreads = 256;
 constexpr int kStateThreads = 128;
 constexpr int kSmThreads = 128;
-constexpr int kSplitKeys = 128;   // key slots per softmax split (at most)
-constexpr int kUnrollK = 4;       // key rows in flight per lane (logits)
-constexpr int kUnrollV = 8;       // value rows in flight per thread (P V)
+constexpr int kSplitKeys = 64;    // key slots per softmax split (at most)
 
 // Per-step scratch layout (floats): qrot, qhat, olin [N, Hq, D]; pm, pl [N, Hq, splits];
 // pacc [N, Hq, splits, D].
@@ -253,16 +252,17 @@ decode_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __rest
     }
 }
 
-// CTA (q-head h, sequence n).  Thread t owns column group t % (D/4) (four
-// value dims, float4) of rows (t / (D/4)) * RPT .. + RPT - 1.
+// State unit (q-head h, sequence n), one CTA.  Thread t owns column group
+// t % (D/4) (four value dims, float4) of rows (t / (D/4)) * RPT .. + RPT - 1;
+// the 64 KiB state is read once into registers and written back once.
 template <int D>
-__global__ void __launch_bounds__(kStateThreads, 3)
-decode_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
+__device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_state& s, const DecScratch& sc,
+                                                  int h, int n) {
     constexpr int CG = D / 4, RG = kStateThreads / CG, RPT = D / RG;
     __shared__ __align__(16) float kj_s[D], vj_s[D], qh_s[D];
     __shared__ __align__(16) float redx[RG][D], redy[RG][D];
     __shared__ float cdot_s;
-    const int h = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, kv = h / L.G;
+    const int tid = threadIdx.x, kv = h / L.G;
     const int ns = L.n_sinks, W = L.window, P = W + 1;
     const int64_t p = s.pos[n], j = p - W;  // the token leaving the window
     float* olin = sc.olin + ((size_t)n * L.Hq + h) * D;
@@ -326,24 +326,69 @@ decode_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
     }
 }
 
-// CTA (kv head x split, sequence n): softmax partials of the G heads of the
-// group over key slots [split * KS, (split + 1) * KS) of the valid-slot list.
-// The split's key and value rows are copied into shared memory at once (two
-// cp.async groups: logits need only the keys), so every CTA has its whole
-// share of the ring in flight.
-template <typename Tin, int D>
-__global__ void __launch_bounds__(kSmThreads)
-decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
-    constexpr int DL = D / 8;                // channels per lane in the 8-lane key groups
-    constexpr int CG = D / 4, NKS = kSmThreads / CG;
-    constexpr int ROWB = D * (int)sizeof(Tin), CHUNKS = ROWB / 16;
-    extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char* ks_s = smem;                                  // [kSplitKeys][D] keys; later P V partials
-    unsigned char* vs_s = smem + kSplitKeys * ROWB;              // [kSplitKeys][D] values
-    float* qrot_s = reinterpret_cast<float*>(vs_s + kSplitKeys * ROWB);  // [G][D]
-    float* logit = qrot_s + kMaxG * D;                           // [G][kSplitKeys]
-    __shared__ float m_s[kMaxG], l_s[kMaxG];
-    const int split = blockIdx.x % sc.splits, kv = blockIdx.x / sc.splits, n = blockIdx.y;
+// Packed fp32 FMA: d = a * b + c on both lanes, each rounded as fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+// The 16 / sizeof(T) values of a 16-byte chunk as fp32 pairs.
+template <typename T> struct Chunk;
+template <> struct Chunk<__nv_bfloat16> {
+    static constexpr int kPairs = 4;
+    static __device__ __forceinline__ void unpack(uint4 u, float2* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+    }
+};
+template <> struct Chunk<float> {
+    static constexpr int kPairs = 2;
+    static __device__ __forceinline__ void unpack(uint4 u, float2* f) {
+        f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+};
+
+// CTA (kv head x split, sequence n): softmax partials of the G <= GM heads of
+// the group over key slots [split * KS, (split + 1) * KS) of the valid-slot
+// list.  No shared-memory staging of the ring: every thread loads, straight
+// into registers with 16-byte loads issued up front, exactly the key and value
+// chunks it uses.  Logits: lane pairs per key (adjacent chunks, so a warp's
+// load covers whole 32-byte sectors), q broadcast from shared memory, one
+// shuffle per head.  P V: thread (value chunk, key subset), packed FMAs,
+// subsets summed through shared memory.
+template <typename Tin, int D, int GM>
+struct DecSm {
+    static constexpr int kEpc = 16 / (int)sizeof(Tin);  // values per chunk
+    static constexpr int kCh = D / kEpc;                // chunks per row
+    static constexpr int kKc = kCh / 2;                 // key chunks per thread (two lanes per key)
+    static constexpr int kNks = kSmThreads / kCh;       // key subsets in P V
+    static constexpr int kKpt = kSplitKeys / kNks;      // value rows per thread
+    // shared memory (floats): q [GM][D], logits [GM][keys], P [keys][GM], P V partials [kNks][GM][D]
+    static constexpr int kQ = 0, kLg = kQ + GM * D, kP = kLg + GM * kSplitKeys, kPart = kP + kSplitKeys * GM;
+    static constexpr size_t kSmemBytes = sizeof(float) * (size_t)(kPart + kNks * GM * D);
+    static_assert(kSmThreads == 2 * kSplitKeys, "two lanes per key");
+    static_assert(kCh % 2 == 0 && kSmThreads % kCh == 0 && kSplitKeys % kNks == 0, "mapping");
+};
+
+template <typename Tin, int D, int GM>
+__device__ __forceinline__ void decode_softmax_unit(const LayerDims& L, const hla_state& s, const DecScratch& sc,
+                                                    int split, int kv, int n, float* fsm) {
+    using P = DecSm<Tin, D, GM>;
+    using C = Chunk<Tin>;
+    constexpr int NP = C::kPairs;
+    float* q_s = fsm + P::kQ;
+    float* lg_s = fsm + P::kLg;
+    float* p_s = fsm + P::kP;
+    float* part_s = fsm + P::kPart;
+    __shared__ float m_s[GM], l_s[GM];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.G, ns = L.n_sinks, W = L.window, R = ns + W;
     const int64_t p = s.pos[n];
@@ -352,144 +397,195 @@ decode_softmax_kernel(LayerDims L, hla_state s, DecScratch sc) {
     const int n_keys = nsk + n_win;
     const int KS = (R + sc.splits - 1) / sc.splits;
     const int k0 = split * KS, nt = max(0, min(KS, n_keys - k0));
-    const Tin* kring = static_cast<const Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D;
-    const Tin* vring = static_cast<const Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
+    const uint4* kring = reinterpret_cast<const uint4*>(static_cast<const Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D);
+    const uint4* vring = reinterpret_cast<const uint4*>(static_cast<const Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D);
     auto slot_of = [&](int i) { return i < nsk ? i : ns + (i - nsk); };  // valid-slot list entry -> ring slot
-    const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
 
-    for (int base = 0; base < 2; ++base) {  // keys, then values
-        const Tin* ring = base ? vring : kring;
-        unsigned char* dst = base ? vs_s : ks_s;
-        for (int e = tid; e < nt * CHUNKS; e += kSmThreads) {
-            const int i = e / CHUNKS, c = e % CHUNKS;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                             (uint32_t)__cvta_generic_to_shared(dst + (size_t)i * ROWB + 16 * c)),
-                         "l"(reinterpret_cast<const unsigned char*>(ring + (size_t)slot_of(k0 + i) * D) + 16 * c)
-                         : "memory");
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-    for (int e = tid; e < G * D; e += kSmThreads) qrot_s[e] = sc.qrot[((size_t)n * L.Hq + kv * G) * D + e];
-    asm volatile("cp.async.wait_group 1;" ::: "memory");  // the keys
-    __syncthreads();
-    // logits: 8 lanes per key row, DL channels per lane; the trip count is the same for the
-    // whole warp (shuffles with every lane present)
-    const int l8 = tid & 7, grp8 = tid >> 3;
-    for (int i0 = 0; i0 < nt; i0 += (kSmThreads / 8) * kUnrollK) {
-        float kx[kUnrollK][DL];
+    // loads first: this thread's key chunks (key ki, chunks 2c + kh) and value chunks (chunk vc of
+    // rows vk + kNks r); rows past the split's keys read as zero
+    const int ki = tid >> 1, kh = tid & 1;
+    const int vc = tid % P::kCh, vk = tid / P::kCh;
+    uint4 kraw[P::kKc], vraw[P::kKpt];
+    {
+        const uint4* kr = kring + (size_t)slot_of(k0 + min(ki, max(nt - 1, 0))) * P::kCh;
 #pragma unroll
-        for (int u = 0; u < kUnrollK; ++u) {
-            const int i = i0 + grp8 + (kSmThreads / 8) * u;
-            const Tin* kr = reinterpret_cast<const Tin*>(ks_s + (size_t)min(i, kSplitKeys - 1) * ROWB) + DL * l8;
+        for (int c = 0; c < P::kKc; ++c) kraw[c] = ki < nt ? __ldg(kr + 2 * c + kh) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int e = 0; e < DL; e += 4) load_vec<4>(kr + e, kx[u] + e);
-        }
-        for (int gg = 0; gg < G; ++gg) {
-            float pt[kUnrollK];
-#pragma unroll
-            for (int u = 0; u < kUnrollK; ++u) {
-                pt[u] = 0.f;
-#pragma unroll
-                for (int e = 0; e < DL; ++e) pt[u] = fmaf(qrot_s[gg * D + DL * l8 + e], kx[u][e], pt[u]);
-            }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1)
-#pragma unroll
-                for (int u = 0; u < kUnrollK; ++u) pt[u] += __shfl_xor_sync(0xffffffffu, pt[u], o);
-#pragma unroll
-            for (int u = 0; u < kUnrollK; ++u) {
-                const int i = i0 + grp8 + (kSmThreads / 8) * u;
-                if (i < nt && l8 == 0) logit[gg * kSplitKeys + i] = pt[u] * qscale;
-            }
+        for (int r = 0; r < P::kKpt; ++r) {
+            const int i = vk + P::kNks * r;
+            vraw[r] = i < nt ? __ldg(vring + (size_t)slot_of(k0 + i) * P::kCh + vc) : make_uint4(0, 0, 0, 0);
         }
     }
+    for (int e = tid; e < G * D; e += kSmThreads) q_s[e] = sc.qrot[((size_t)n * L.Hq + kv * G) * D + e];
     __syncthreads();
-    for (int gg = warp; gg < G; gg += kSmThreads / 32) {  // per-head max and sum; logits -> probabilities
+
+    // logits of key ki: this lane's half of the dot products, then the pair's sum
+    const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+    {
+        float2 acc[GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < P::kKc; ++c) {
+            float2 kf[NP];
+            C::unpack(kraw[c], kf);
+            const int d0 = (2 * c + kh) * P::kEpc;
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                if (g < G) {
+#pragma unroll
+                    for (int e = 0; e < NP; e += 2) {
+                        const float4 qv = *reinterpret_cast<const float4*>(q_s + g * D + d0 + 2 * e);
+                        acc[g] = ffma2(make_float2(qv.x, qv.y), kf[e], acc[g]);
+                        acc[g] = ffma2(make_float2(qv.z, qv.w), kf[e + 1], acc[g]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            float t = acc[g].x + acc[g].y;
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            if (g < G && kh == 0) lg_s[g * kSplitKeys + ki] = t * qscale;
+        }
+    }
+    __syncthreads();
+    for (int g = warp; g < G; g += kSmThreads / 32) {  // per-head max and sum; P into [key][head]
         float mx = -INFINITY;
-        for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, logit[gg * kSplitKeys + i]);
+        for (int i = lane; i < nt; i += 32) mx = fmaxf(mx, lg_s[g * kSplitKeys + i]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float sum = 0.f;
-        for (int i = lane; i < nt; i += 32) {
-            const float e = exp2f(logit[gg * kSplitKeys + i] - mx);
-            logit[gg * kSplitKeys + i] = e;
+        for (int i = lane; i < kSplitKeys; i += 32) {
+            const float e = i < nt ? exp2f(lg_s[g * kSplitKeys + i] - mx) : 0.f;
+            p_s[i * GM + g] = e;
             sum += e;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) { m_s[gg] = mx; l_s[gg] = sum; }
+        if (lane == 0) { m_s[g] = mx; l_s[g] = sum; }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");  // the values
     __syncthreads();
-    // P V: thread (key subset ks, 4 channels cg4)
-    const int cg4 = tid % CG, ks = tid / CG;
-    float acc[kMaxG][4];
+
+    // P V over this thread's value rows, then the key subsets summed
+    {
+        float2 acc[GM][NP];
 #pragma unroll
-    for (int gg = 0; gg < kMaxG; ++gg)
+        for (int g = 0; g < GM; ++g)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[gg][e] = 0.f;
-    for (int i = ks; i < nt; i += NKS) {
-        float vx[4];
-        load_vec<4>(reinterpret_cast<const Tin*>(vs_s + (size_t)i * ROWB) + 4 * cg4, vx);
+            for (int e = 0; e < NP; ++e) acc[g][e] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg)
-            if (gg < G) {
-                const float pr = logit[gg * kSplitKeys + i];
+        for (int r = 0; r < P::kKpt; ++r) {
+            const int i = vk + P::kNks * r;
+            float2 vf[NP];
+            C::unpack(vraw[r], vf);
+            float pr[GM];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[gg][e] = fmaf(pr, vx[e], acc[gg][e]);
+            for (int g = 0; g < GM; g += 4) {
+                if constexpr (GM >= 4) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(p_s + i * GM + g);
+                    pr[g] = p4.x; pr[g + 1] = p4.y; pr[g + 2] = p4.z; pr[g + 3] = p4.w;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < GM; ++u) pr[u] = p_s[i * GM + u];
+                }
             }
+#pragma unroll
+            for (int g = 0; g < GM; ++g)
+                if (g < G)
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) acc[g][e] = ffma2(make_float2(pr[g], pr[g]), vf[e], acc[g][e]);
+        }
+#pragma unroll
+        for (int g = 0; g < GM; ++g)
+            if (g < G)
+#pragma unroll
+                for (int e = 0; e < NP; ++e)
+                    *reinterpret_cast<float2*>(part_s + (vk * GM + g) * D + vc * P::kEpc + 2 * e) = acc[g][e];
     }
-    float* part = reinterpret_cast<float*>(ks_s);  // [NKS][G][D]; the keys are no longer needed
-#pragma unroll
-    for (int gg = 0; gg < kMaxG; ++gg)
-        if (gg < G)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) part[((size_t)ks * G + gg) * D + 4 * cg4 + e] = acc[gg][e];
     __syncthreads();
     for (int e = tid; e < G * D; e += kSmThreads) {
-        const int gg = e / D, c = e % D;
+        const int g = e / D, c = e % D;
         float o = 0.f;
 #pragma unroll
-        for (int r = 0; r < NKS; ++r) o += part[((size_t)r * G + gg) * D + c];
-        const size_t hs = ((size_t)n * L.Hq + kv * G + gg) * sc.splits + split;
+        for (int r = 0; r < P::kNks; ++r) o += part_s[(r * GM + g) * D + c];
+        const size_t hs = ((size_t)n * L.Hq + kv * G + g) * sc.splits + split;
         sc.pacc[hs * D + c] = o;
         if (c == 0) {
-            sc.pm[hs] = nt > 0 ? m_s[gg] : -INFINITY;
-            sc.pl[hs] = nt > 0 ? l_s[gg] : 0.f;
+            sc.pm[hs] = nt > 0 ? m_s[g] : -INFINITY;
+            sc.pl[hs] = nt > 0 ? l_s[g] : 0.f;
         }
     }
 }
 
-template <typename Tin, int D>
-constexpr size_t decode_softmax_smem() {
-    return 2 * (size_t)kSplitKeys * D * sizeof(Tin) + sizeof(float) * (size_t)kMaxG * (D + kSplitKeys);
+// One launch for the step's two streams over HBM: per (kv head, sequence) a
+// run of G state units (the group's heads) followed by the softmax splits, so
+// the state updates and the ring reads share every wave of CTAs.
+template <typename Tin, int D, int GM>
+__global__ void __launch_bounds__(kSmThreads, 3)
+decode_attn_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
+    static_assert(kStateThreads == kSmThreads, "one CTA shape for both units");
+    extern __shared__ __align__(16) float fsm[];
+    const int run = L.G + sc.splits, kv = blockIdx.x / run, r = blockIdx.x % run, n = blockIdx.y;
+    if (r < L.G) decode_state_unit<D>(L, s, sc, kv * L.G + r, n);
+    else decode_softmax_unit<Tin, D, GM>(L, s, sc, r - L.G, kv, n, fsm);
 }
 
-// CTA per (q-head, sequence), thread per channel: o = softmax (splits merged by
-// their maxima) + lambda_h o_lin.
+// CTA per (q-head, sequence), thread per channel: splits merged by their
+// maxima (read eight at a time, so their loads overlap), o = o_sm + lambda_h
+// o_lin; then the sequence's position advances (CTA of head 0: no CTA of this
+// launch reads it).
+constexpr int kCombineBatch = 8;
 template <typename Tin, int D>
 __global__ void __launch_bounds__(D)
-decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out) {
+decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out,
+                      int64_t* __restrict__ pos) {
     const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x;
-    {
-        const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
-        float m = -INFINITY;
-        for (int r = 0; r < sc.splits; ++r) m = fmaxf(m, sc.pm[hs + r]);
-        float l = 0.f, o = 0.f;
-        for (int r = 0; r < sc.splits; ++r) {
-            const float w = sc.pl[hs + r] > 0.f ? exp2f(sc.pm[hs + r] - m) : 0.f;
-            l = fmaf(sc.pl[hs + r], w, l);
-            o = fmaf(sc.pacc[(hs + r) * D + c], w, o);
+    const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
+    float m = -INFINITY, l = 0.f, o = 0.f;  // running merge
+    for (int r0 = 0; r0 < sc.splits; r0 += kCombineBatch) {
+        float pm[kCombineBatch], pl[kCombineBatch], pa[kCombineBatch];
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+            const bool in = r0 + u < sc.splits;
+            pm[u] = in ? sc.pm[hs + r0 + u] : -INFINITY;
+            pl[u] = in ? sc.pl[hs + r0 + u] : 0.f;
+            pa[u] = in ? sc.pacc[(hs + r0 + u) * D + c] : 0.f;
         }
-        o = (L.flags & HLA_FLAG_SOFTMAX_OFF) || l <= 0.f ? 0.f : o / l;
-        if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), sc.olin[((size_t)n * L.Hq + h) * D + c], o);
-        out[((size_t)n * L.Hq + h) * D + c] = from_f32<Tin>(o);
+        float mb = m;
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) mb = fmaxf(mb, pl[u] > 0.f ? pm[u] : -INFINITY);
+        if (mb == -INFINITY) continue;  // nothing in this batch or before it
+        const float w0 = l > 0.f ? exp2f(m - mb) : 0.f;
+        l *= w0;
+        o *= w0;
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+            const float w = pl[u] > 0.f ? exp2f(pm[u] - mb) : 0.f;
+            l = fmaf(pl[u], w, l);
+            o = fmaf(pa[u], w, o);
+        }
+        m = mb;
     }
+    o = (L.flags & HLA_FLAG_SOFTMAX_OFF) || l <= 0.f ? 0.f : o / l;
+    if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), sc.olin[((size_t)n * L.Hq + h) * D + c], o);
+    out[((size_t)n * L.Hq + h) * D + c] = from_f32<Tin>(o);
+    if (h == 0 && c == 0) pos[n] += 1;
 }
 
-__global__ void advance_pos_kernel(int64_t* pos, int n) {
-    int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) pos[i] += 1;
+template <typename Tin, int D, int GM>
+cudaError_t launch_decode_attn_state(const LayerDims& L, const hla_state& s, const DecScratch& sc, cudaStream_t st) {
+    using P = DecSm<Tin, D, GM>;
+    static bool configured = false;  // per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_attn_state_kernel<Tin, D, GM>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    decode_attn_state_kernel<Tin, D, GM><<<dim3(L.Hkv * (L.G + sc.splits), L.n_seqs), kSmThreads, P::kSmemBytes,
+                                           st>>>(L, s, sc);
+    return cudaGetLastError();
 }
 
 template <typename Tin, int D>
@@ -498,25 +594,12 @@ cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const
                            const float* wv, const hla_state& s, Tin* out, cudaStream_t st) {
     const DecScratch sc = dec_scratch(static_cast<float*>(s.scratch), L.n_seqs, L.Hq, D, decode_splits(L.n_sinks, L.window));
     decode_features_kernel<Tin, D><<<dim3(L.Hkv, L.n_seqs), kFeatThreads, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, s, sc);
-    // the state update runs on the side stream beside the softmax (independent, both HBM-bound)
-    SideStream* side = nullptr;
-    cudaError_t e0 = side_stream(&side);
-    if (e0 == cudaSuccess) e0 = cudaEventRecord(side->fork, st);
-    if (e0 == cudaSuccess) e0 = cudaStreamWaitEvent(side->s, side->fork, 0);
+    cudaError_t e0 = L.G <= 1 ? launch_decode_attn_state<Tin, D, 1>(L, s, sc, st)
+                   : L.G <= 2 ? launch_decode_attn_state<Tin, D, 2>(L, s, sc, st)
+                   : L.G <= 4 ? launch_decode_attn_state<Tin, D, 4>(L, s, sc, st)
+                              : launch_decode_attn_state<Tin, D, 8>(L, s, sc, st);
     if (e0 != cudaSuccess) return e0;
-    decode_state_kernel<D><<<dim3(L.Hq, L.n_seqs), kStateThreads, 0, side->s>>>(L, s, sc);
-    if ((e0 = cudaEventRecord(side->join, side->s)) != cudaSuccess) return e0;
-    constexpr size_t sm_smem = decode_softmax_smem<Tin, D>();
-    static bool configured = false;  // per instantiation
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_softmax_kernel<Tin, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sm_smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    decode_softmax_kernel<Tin, D><<<dim3(L.Hkv * sc.splits, L.n_seqs), kSmThreads, sm_smem, st>>>(L, s, sc);
-    if ((e0 = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess) return e0;
-    decode_combine_kernel<Tin, D><<<dim3(L.Hq, L.n_seqs), D, 0, st>>>(L, sc, lambda, out);
+    decode_combine_kernel<Tin, D><<<dim3(L.Hq, L.n_seqs), D, 0, st>>>(L, sc, lambda, out, s.pos);
     return cudaGetLastError();
 }
 
@@ -529,9 +612,7 @@ cudaError_t launch_decode_step(const LayerDims& L, const Tin* q, const Tin* k, c
     if (L.n_seqs <= 0) return cudaSuccess;
     cudaError_t e = L.d == 128 ? decode_kernels<Tin, 128>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out, st)
                                : decode_kernels<Tin, 64>(L, q, k, v, g, beta, lambda, wq, wk, wv, s, out, st);
-    if (e != cudaSuccess) return e;
-    advance_pos_kernel<<<(L.n_seqs + 255) / 256, 256, 0, st>>>(s.pos, L.n_seqs);
-    return cudaGetLastError();
+    return e;
 }
 
 template cudaError_t launch_decode_step<float>(const LayerDims&, const float*, const float*,

@@ -162,16 +162,7 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float2* fine, const float2* coarse, Tf* qr, Tf* kr, Tf* qhat,
                             Tf* khat, Tf* vhat, int32_t* err, bool after_prior, cudaStream_t st);
 
-// Per host thread and device: a second stream for kernels that can run
-// beside the caller's stream, and the events that fork it off the caller's
-// stream and join it back.  Created on first use and kept for the thread's
-// lifetime.
-constexpr int kMaxGdnParts = 4;
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-cudaError_t side_stream(SideStream** out);
+constexpr int kMaxGdnParts = 4;  // parts of the chunk slots the chunked GDN may run in
 
 // Token-serial fp32 GDN with delayed absorption: o_lin [total, Hq, d] fp32
 // for positions p >= n_sinks + window; final S into S_out (may be null).

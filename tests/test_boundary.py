@@ -63,9 +63,9 @@ def test_state_sizes(lib):
     assert sz["pend_g"] == 64 * 32 * 889 * 4
     assert sz["conv_q"] == 64 * 7 * 32 * 128 * 4
     assert sz["pos"] == 64 * 8
-    # per-step decode scratch: q rot, qhat, o_lin [N, Hq, d]; per split of 128 key slots
-    # (7 for an 896-slot ring) the running max, sum and P V
-    assert sz["scratch"] == 4 * (3 * 64 * 32 * 128 + 2 * 64 * 32 * 7 + 64 * 32 * 7 * 128)
+    # per-step decode scratch: q rot, qhat, o_lin [N, Hq, d]; per split of 64 key slots
+    # (14 for an 896-slot ring) the running max, sum and P V
+    assert sz["scratch"] == 4 * (3 * 64 * 32 * 128 + 2 * 64 * 32 * 14 + 64 * 32 * 14 * 128)
     f32 = hla.state_sizes(_p(dtype=hla.DTYPE_F32, head_dim=64), 1)
     assert f32["k_ring"] == 8 * 64 * 64 * 4
 
