@@ -17,6 +17,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,6 +42,11 @@ def parse():
     ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c4"],
                     help="prefill workload of the headline line")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the decode measurement (one JSON line with its results)")
+    ap.add_argument("--traffic-from", metavar="NCU_REP", default=None,
+                    help="write profiles/traffic.json from an ncu report of the prefill kernels (one "
+                         "prefill call's launches) and exit; runs here, without a GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=None)
     return ap.parse_args()
@@ -393,7 +399,10 @@ def run_decode_bench(args, dist, peaks):
     hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"],
                 x["cu_seqlens"], out, state=st)
     del out
+    for key in ("q", "k", "v", "g", "beta"):  # the prefill inputs (~6.5 GB) are not needed any more
+        x.pop(key)
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     K = args.decode_steps or args.steps
     W = args.warmup
     assert W + K <= wl.decode_steps
@@ -502,8 +511,62 @@ def run_reference(args, dist):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
+    "features_kernel": FEATURES_SOURCES,
+    "window_softmax_tc_kernel": SOFTMAX_TC_SOURCES,
+    "gdn_inverse_kernel": GDN_PREP_SOURCES,
+    "gdn_chunked_kernel": GDN_CHUNKED_SOURCES,
+}
+
+
+def write_traffic(rep: str):
+    """profiles/traffic.json from `ncu -i rep --page raw --csv`: per kernel the DRAM bytes summed over
+    its launches in the report (one prefill call), keyed by a hash of its sources."""
+    import csv
+    import io
+
+    raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
+                         text=True).stdout
+    rows = list(csv.reader(io.StringIO(raw)))
+    head, body = rows[0], [r for r in rows[2:] if r]  # rows[1] holds the units
+    col = {k: head.index(k) for k in ("Kernel Name", "dram__bytes_read.sum", "dram__bytes_write.sum",
+                                      "gpu__time_duration.sum")}
+    units = rows[1]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-3, "nsecond": 1e-3, "us": 1.0,
+             "usecond": 1.0, "ms": 1e3, "msecond": 1e3}  # to bytes and microseconds
+    out = {"_command": "ncu --set full --clock-control none -k regex:\"features_kernel|gdn_inverse_kernel|"
+                       "gdn_chunked_kernel|window_softmax_tc_kernel\" -s 6 -c 6 -o prof python bench.py "
+                       "--no-decode --no-cpu-baseline --steps 3 --warmup 3",
+           "_workload": synth_workload_name("c1") + " (the launches of one prefill call; cold caches: ncu "
+                                                   "flushes them before each pass)",
+           "_note": "per step = summed over the kernel's launches in one prefill call (the GDN kernels run "
+                    "once per part of the chunk slots)"}
+    for name, srcs in TRAFFIC_KERNELS.items():
+        mine = [r for r in body if re.search(r"(^|[\s:])" + name + r"[<(]", r[col["Kernel Name"]])]
+        if not mine:
+            continue
+        val = lambda r, k: float(r[col[k]].replace(",", "")) * scale[units[col[k]]]
+        rd = sum(val(r, "dram__bytes_read.sum") for r in mine)
+        wr = sum(val(r, "dram__bytes_write.sum") for r in mine)
+        out[name] = {"source_sha256": source_hash(srcs), "launches_per_step": len(mine),
+                     "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_step": rd + wr,
+                     "duration_us_ncu": round(sum(val(r, "gpu__time_duration.sum") for r in mine), 3)}
+    with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+
+
+def synth_workload_name(key: str) -> str:
+    from linearized_attention_rope_gb300 import synth
+
+    return synth.workloads()[key].name
+
+
 def main():
     args = parse()
+    if args.traffic_from:
+        write_traffic(args.traffic_from)
+        return
     dist = Dist()
     if args.impl == "reference":
         line = run_reference(args, dist)
@@ -521,6 +584,12 @@ def main():
     dist.barrier()
     hla.load()
     peaks = measured_peaks()
+    if args.decode_only:
+        dec = run_decode_bench(args, dist, peaks)
+        if dist.rank == 0:
+            print(json.dumps({"decode": dec}), flush=True)
+        dist.close()
+        return
     pre = run_prefill_bench(args, dist, peaks)
     dec = None if args.no_decode else run_decode_bench(args, dist, peaks)
     torch.cuda.synchronize()

@@ -326,18 +326,6 @@ __device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_
     }
 }
 
-// Packed fp32 FMA: d = a * b + c on both lanes, each rounded as fmaf.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long ra, rb, rc, rd;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-    return d;
-}
-
 // The 16 / sizeof(T) values of a 16-byte chunk as fp32 pairs.
 template <typename T> struct Chunk;
 template <> struct Chunk<__nv_bfloat16> {

@@ -119,8 +119,8 @@ struct FeatRow {
     Tf* rot;       // RoPE'd rows (q and k), lane's first pair already added
     Tf* hat;       // conv (+ norm) rows, lane offset added
     size_t rowstride;  // elements between consecutive tokens of one head
-    float w[NC][kConvWidth];
-    float ring[kBlk][NC];
+    float2 w[NC / 2][kConvWidth];  // conv taps of channel pairs (2j, 2j + 1) of the lane
+    float2 ring[kBlk][NC / 2];      // the last 8 inputs, same pairing
     float2 step1[NP];  // (cos, sin) of one position step for the lane's pairs
 };
 
@@ -201,18 +201,22 @@ __device__ __forceinline__ void feat_step(FeatRow<Tin, Tf, D>& fr, const Tin* ro
             }
         }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) fr.ring[u][c] = x[c];
+        for (int j = 0; j < NC / 2; ++j) fr.ring[u][j] = make_float2(x[2 * j], x[2 * j + 1]);
         if constexpr (OUT) {
-            // tap m reads token t - 7 + m (ring slot (u + 1 + m) mod 8); none before the sequence start
-            float y[NC];
+            // tap m reads token t - 7 + m (ring slot (u + 1 + m) mod 8); none before the sequence start;
+            // two channels per packed FMA
+            float2 y2[NC / 2];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) y[c] = 0.f;
+            for (int j = 0; j < NC / 2; ++j) y2[j] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < kConvWidth; ++m) {
                 if (CHECK && m < kConvHalo - p) continue;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) y[c] = fmaf(fr.w[c][m], fr.ring[(u + 1 + m) & (kBlk - 1)][c], y[c]);
+                for (int j = 0; j < NC / 2; ++j) y2[j] = ffma2(fr.w[j][m], fr.ring[(u + 1 + m) & (kBlk - 1)][j], y2[j]);
             }
+            float y[NC];
+#pragma unroll
+            for (int j = 0; j < NC / 2; ++j) { y[2 * j] = y2[j].x; y[2 * j + 1] = y2[j].y; }
             if constexpr (NORM) {
                 float ss = 0.f;
 #pragma unroll
@@ -342,19 +346,24 @@ features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
     fr.hat = (kind == 0 ? qhat : (kind == 1 ? khat : vhat)) + (size_t)head * D + NP * lane;
     {  // conv weights of the lane's channels: c < NP -> channel NP lane + c, else HALF + NP lane + c - NP
         const float* wb = (kind == 0 ? wq : (kind == 1 ? wk : wv)) + (size_t)head * D * kConvWidth;
+        float wc[NC][kConvWidth];
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             const int ch = (c < NP ? 0 : HALF) + NP * lane + (c % NP);
             const float4 a = __ldg(reinterpret_cast<const float4*>(wb + (size_t)ch * kConvWidth));
             const float4 b = __ldg(reinterpret_cast<const float4*>(wb + (size_t)ch * kConvWidth + 4));
-            fr.w[c][0] = a.x; fr.w[c][1] = a.y; fr.w[c][2] = a.z; fr.w[c][3] = a.w;
-            fr.w[c][4] = b.x; fr.w[c][5] = b.y; fr.w[c][6] = b.z; fr.w[c][7] = b.w;
+            wc[c][0] = a.x; wc[c][1] = a.y; wc[c][2] = a.z; wc[c][3] = a.w;
+            wc[c][4] = b.x; wc[c][5] = b.y; wc[c][6] = b.z; wc[c][7] = b.w;
         }
+#pragma unroll
+        for (int j = 0; j < NC / 2; ++j)
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) fr.w[j][m] = make_float2(wc[2 * j][m], wc[2 * j + 1][m]);
     }
 #pragma unroll
     for (int u = 0; u < kBlk; ++u)
 #pragma unroll
-        for (int c = 0; c < NC; ++c) fr.ring[u][c] = 0.f;
+        for (int j = 0; j < NC / 2; ++j) fr.ring[u][j] = make_float2(0.f, 0.f);
 
     const int64_t tb = (int64_t)blockIdx.x * span - kBlk;
     if (kind == 2)

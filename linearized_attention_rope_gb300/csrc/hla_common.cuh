@@ -41,6 +41,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
+// Packed fp32 FMA (fma.rn.f32x2): d = a * b + c on both lanes, each rounded
+// as fmaf, in one instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
 // Loads E (2 or 4) consecutive elements starting at an E-aligned index as fp32.
 template <int E> __device__ __forceinline__ void load_vec(const float* p, float* o) {
     if constexpr (E == 4) { float4 x = *reinterpret_cast<const float4*>(p); o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; }
