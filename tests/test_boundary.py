@@ -70,6 +70,15 @@ def test_state_sizes(lib):
     assert f32["k_ring"] == 8 * 64 * 64 * 4
 
 
+def test_prefill_launch_count(lib):
+    # tensor-core path: one table launch, features, softmax, then a chunk-local and a state launch
+    # for each of the two parts of the chunk slots; plus the decode-state hand-off when asked
+    assert hla.prefill_launch_count(_p()) == 7
+    assert hla.prefill_launch_count(_p(), with_state=True) == 8
+    # token-serial path (fp32 layer): tables, features, recurrent GDN, softmax + combine
+    assert hla.prefill_launch_count(_p(dtype=hla.DTYPE_F32, head_dim=64)) == 4
+
+
 def test_workspace_grows_with_tokens(lib):
     a = hla.workspace_bytes(_p(), 4096, 1)
     b = hla.workspace_bytes(_p(), 8192, 1)
