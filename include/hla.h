@@ -22,9 +22,8 @@
  *     caller owns every buffer; the library allocates no device memory and
  *     never synchronises the stream, except hla_check_device_error.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
- *     Every kernel of a call runs on it (no stream or event of the library's
- *     own), some with programmatic dependent launch, so a call can be captured
- *     into a CUDA graph like any sequence of launches.
+ *     Every kernel of a call runs on it, some with programmatic dependent
+ *     launch; the library creates no stream or event of its own.
  *   - Argument errors are detected on the host, before any launch, and return
  *     HLA_ERR_INVALID_ARG / HLA_ERR_UNSUPPORTED without touching the GPU.
  *   - A failed launch returns HLA_ERR_CUDA (the CUDA error is consumed).
