@@ -149,11 +149,10 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     // The GDN launches run with programmatic stream serialization (their CTAs set up while the launch
     // before them drains), unless the stage hook wants each launch timed alone; the features and softmax
     // launches are plain (CTAs waiting beside the kernel before them slowed it by more than the launch
-    // latency they hid).  The order
-    // stays transitive: a kernel that reads data without waiting for its predecessor (the chunk-local
-    // GDN) starts only after a trigger that its predecessor gives once its own wait has returned, and
-    // every kernel waits for its predecessor before it completes, so a completed launch implies that
-    // all launches before it completed.
+    // latency they hid).  The order stays transitive: a kernel that reads data without waiting for its
+    // predecessor (the chunk-local GDN) starts only after a trigger that its predecessor gives once its
+    // own wait has returned, and every kernel waits for its predecessor before it completes, so a
+    // completed launch implies that all launches before it completed.
     const bool overlap = t_n_stage_events == 0;
     HLA_TRY(launch_features<Tin, Tf>(L, qi, ki, vi, wq, wk, wv, cu, fine, coarse, qr, kr, qh, kh, vh,
                                      err, false, stream));
