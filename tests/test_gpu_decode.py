@@ -45,6 +45,26 @@ def test_decode_small_all_units(oracle_mod, dtype, d):
     assert st.view("pos").cpu().tolist() == [L + 40 for L in wl.seqlens]
 
 
+@pytest.mark.parametrize("dtype,hq,hkv,d,n_sinks,window", [
+    ("bf16", 8, 1, 128, 0, 70),   # G = 8, no sinks, two key splits
+    ("bf16", 2, 2, 64, 3, 130),   # G = 1, three key splits
+    ("bf16", 6, 2, 128, 8, 40),   # G = 3 (padded to four heads per group)
+    ("f32", 8, 2, 64, 0, 20),     # fp32 layer, no sinks
+])
+def test_decode_head_groups_and_budgets(oracle_mod, dtype, hq, hkv, d, n_sinks, window):
+    # group sizes and budgets beside the ones above: every head-group width of the decode softmax,
+    # windows over several 64-key splits, no sinks at all (four sequences, so that every step's slice
+    # of g and beta, n_seqs x Hq fp32, starts on the 16-byte boundary the C ABI asks for)
+    wl = synth.small(f"decode G{hq // hkv} {n_sinks}+{window}", [5, 60, 150, 33], n_q_heads=hq,
+                     n_kv_heads=hkv, head_dim=d, dtype=dtype, n_sinks=n_sinks, window=window, decode_steps=30)
+    x = synth.make_inputs(wl, "cuda")
+    _, st = run_prefill(wl, x, with_state=True)
+    outs = run_decode(wl, x, st)
+    units = [(n, h) for n in range(wl.n_seqs) for h in range(wl.n_q_heads)]
+    check_decode(wl, x, st, outs, units, oracle_mod, wl.decode_steps)
+    assert st.view("pos").cpu().tolist() == [L + 30 for L in wl.seqlens]
+
+
 def test_decode_from_empty_state(oracle_mod):
     wl = synth.small("decode only", [0, 0], n_q_heads=2, n_kv_heads=1, head_dim=64, n_sinks=2,
                      window=5, decode_steps=30)
