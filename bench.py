@@ -520,13 +520,20 @@ TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
 
 
 def write_traffic(rep: str):
-    """profiles/traffic.json from `ncu -i rep --page raw --csv`: per kernel the DRAM bytes summed over
-    its launches in the report (one prefill call), keyed by a hash of its sources."""
+    """profiles/traffic.json from `ncu -i rep --page raw --csv`."""
+    raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
+                         text=True).stdout
+    with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
+        json.dump(traffic_from_csv(raw), f, indent=1)
+        f.write("\n")
+
+
+def traffic_from_csv(raw: str) -> dict:
+    """Per kernel of TRAFFIC_KERNELS, the DRAM bytes and ncu durations summed over its launches in an
+    ncu raw-page CSV (one prefill call), keyed by a hash of the kernel's sources."""
     import csv
     import io
 
-    raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
-                         text=True).stdout
     rows = list(csv.reader(io.StringIO(raw)))
     head, body = rows[0], [r for r in rows[2:] if r]  # rows[1] holds the units
     col = {k: head.index(k) for k in ("Kernel Name", "dram__bytes_read.sum", "dram__bytes_write.sum",
@@ -551,9 +558,7 @@ def write_traffic(rep: str):
         out[name] = {"source_sha256": source_hash(srcs), "launches_per_step": len(mine),
                      "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_step": rd + wr,
                      "duration_us_ncu": round(sum(val(r, "gpu__time_duration.sum") for r in mine), 3)}
-    with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
-        json.dump(out, f, indent=1)
-        f.write("\n")
+    return out
 
 
 def synth_workload_name(key: str) -> str:
