@@ -36,19 +36,28 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000,
+                    help="timed steps of the headline prefill workload (about 0.5 s of c1 steps)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c4"],
                     help="prefill workload of the headline line")
+    ap.add_argument("--extra", default="c2,c4",
+                    help="further prefill workloads reported as prefill_<name> objects ('' for none)")
+    ap.add_argument("--extra-seconds", type=float, default=0.5,
+                    help="approximate timed region of each further workload (steps derived from a trial)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode measurement (one JSON line with its results)")
     ap.add_argument("--traffic-from", metavar="NCU_REP", default=None,
-                    help="write profiles/traffic.json from an ncu report of the prefill kernels (one "
-                         "prefill call's launches) and exit; runs here, without a GPU")
+                    help="write the counters of an ncu report into profiles/traffic.json under --traffic-key "
+                         "and exit; runs here, without a GPU")
+    ap.add_argument("--traffic-key", default="c1", help="workload key of the report given to --traffic-from")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--decode-steps", type=int, default=4000,
+                    help="timed decode steps (step s feeds the inputs of synthetic step s mod 512)")
+    ap.add_argument("--e2e-steps", type=int, default=200, help="timed steps of each end-to-end measurement")
+    ap.add_argument("--stage-steps", type=int, default=50, help="instrumented steps for per-kernel times")
     return ap.parse_args()
 
 
@@ -160,15 +169,15 @@ def measured_peaks() -> dict:
             "source": "fallback"}
 
 
-def kernel_traffic(kernel: str, source_files) -> float | None:
-    """DRAM bytes per step (summed over the kernel's launches in one prefill
-    call) recorded from an ncu capture of `kernel`, if the kernel's sources are
-    unchanged since (hash match); else None."""
+def kernel_traffic(kernel: str, source_files, workload: str = "c1") -> float | None:
+    """DRAM bytes per step (summed over the kernel's launches in one call)
+    recorded for `workload` from an ncu capture of `kernel`, if the kernel's
+    sources are unchanged since (hash match); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(workload, {}).get(kernel)
     if not rec:
         return None
     h = hashlib.sha256()
@@ -215,10 +224,7 @@ def prefill_work(wl):
     d, Hq, Hkv = wl.head_dim, wl.n_q_heads, wl.n_kv_heads
     T = wl.total_tokens
     absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens)
-    keys = 0
-    for L in wl.seqlens:
-        for p in range(L):
-            keys += min(p + 1, wl.n_sinks) + max(0, min(wl.window, p + 1 - wl.n_sinks))
+    keys = sum(visible_keys(L, wl.n_sinks, wl.window) for L in wl.seqlens)
     eb = 2 if wl.dtype == "bf16" else 4
     if wl.dtype == "bf16" and d == 128:
         f = chunked_gdn_flops_per_token_head(d)
@@ -250,12 +256,15 @@ def prefill_work(wl):
     }
 
 
-def run_prefill_bench(args, dist, peaks):
+def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_steps=50, trial_seconds=None):
+    """Prefill of workload `key`: `steps` timed steps (or, with trial_seconds, as many as fill about that
+    long after a short trial), per-kernel times, the roofline of the dominant kernel, and the end-to-end
+    number through the C ABI with host buffers."""
     import torch
 
     from linearized_attention_rope_gb300 import hla, synth
 
-    wl = synth.workloads()[args.workload]
+    wl = synth.workloads()[key]
     x = synth.make_inputs(wl, "cuda")
     prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window,
                      dtype=hla.DTYPE_BF16 if wl.dtype == "bf16" else hla.DTYPE_F32)
@@ -268,24 +277,30 @@ def run_prefill_bench(args, dist, peaks):
         hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"],
                     x["wv"], x["cu_seqlens"], out, ws=ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
+    if trial_seconds:  # size the timed region from a short trial
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            step()
+        b.record(stream)
+        b.synchronize()
+        per = a.elapsed_time(b) / 3 / 1e3
+        steps = max(10, int(trial_seconds / max(per, 1e-6)))
+        steps = int(dist.max(float(steps)))
+    assert hla.check_workspace_error(ws) == 0
     n_stage = 23
     chunked = wl.dtype == "bf16" and wl.head_dim == 128 and wl.n_q_heads // wl.n_kv_heads in (1, 2, 4, 8)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(args.steps)]
-    for row in ev:  # materialise the event handles
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with ClockSampler(dist.local) as clocks:
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             starts[i].record(stream)
             step()
@@ -293,11 +308,17 @@ def run_prefill_bench(args, dist, peaks):
         torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     dist.barrier()
-    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    # Per-kernel durations: the same number of steps again with the library's stage events on (events
-    # timed between the launches that overlap on two streams would serialise them inside the timed
-    # region above).
-    for i in range(args.steps):
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(steps)]
+    # Per-kernel durations: further steps with the library's stage events on, right after the timed
+    # region (with the hook on every launch runs alone; events inside the timed region would serialise
+    # the launches that overlap there).
+    n_inst = max(1, min(stage_steps, steps))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(n_inst)]
+    for row in ev:  # materialise the event handles
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(n_inst):
         flush.zero_()
         hla.set_prefill_stage_events(ev[i])
         step()
@@ -306,14 +327,13 @@ def run_prefill_bench(args, dist, peaks):
 
     def stages(row):
         t = [0.0] + [row[0].elapsed_time(row[j]) for j in range(1, n_stage)]  # ms from mark 0
-        if chunked:  # each GDN kernel runs once per part of the chunk slots, the chunk-local one on the
-            # library's side stream: a stage is the sum of its launches' durations on their streams
+        if chunked:  # each GDN kernel runs once per part of the chunk slots: a stage sums its launches
             return {"features": t[1], "softmax": t[2] - t[1],
                     "gdn_prep": sum(t[8 + 4 * p] - t[7 + 4 * p] for p in range(4)),
                     "gdn_state": sum(t[10 + 4 * p] - t[9 + 4 * p] for p in range(4))}
         return {"features": t[1], "gdn_state": t[4] - t[3], "softmax": t[5] - t[4]}
 
-    per_step = [stages(ev[i]) for i in range(args.steps)]
+    per_step = [stages(ev[i]) for i in range(n_inst)]
     stage_ms = {k: statistics.mean(st[k] for st in per_step) for k in per_step[0]}
     device_s = dist.max(sum(step_ms) / 1e3)
     launches_per_step = hla.prefill_launch_count(prm)
@@ -330,22 +350,31 @@ def run_prefill_bench(args, dist, peaks):
             achieved, peak = w["flops"] / sec / 1e12, w["peak"]
         return {"kernel": w["kernel"], "bound": w["bound"], "achieved": round(achieved, 3), "peak": peak,
                 "unit": w["unit"], "frac": round(achieved / peak, 5),
-                "traffic": kernel_traffic(w["kernel"], w["sources"]),
-                "peak_source": peaks["source"] if w["bound"] != "alu" else FP32_ALU_TFLOPS_DERIVATION}
+                "traffic": kernel_traffic(w["kernel"], w["sources"], key),
+                "algorithmic": w.get("bytes", w.get("flops")),
+                "peak_source": (peaks["source"] + " burst" if w["bound"] == "tensor" else peaks["source"])
+                if w["bound"] != "alu" else FP32_ALU_TFLOPS_DERIVATION}
 
     measured = [k for k in stage_ms if work.get(k)]
     roofline = roof(max(measured, key=stage_ms.get))  # the dominant kernel
     stage_roofline = {k: {kk: v for kk, v in roof(k).items() if kk in ("kernel", "bound", "achieved", "unit",
                                                                          "frac")}
                       for k in measured}
+    # the whole layer against its own bound: the larger of the HBM time of the algorithmic bytes and the
+    # tensor time of the algorithmic flops
+    layer = layer_work(wl)
+    t_bound = max(layer["bytes"] / (peaks["hbm_gbs"] * 1e9), layer["flops"] / (peaks["bf16_tflops"] * 1e12))
+    layer_roof = {"bytes": layer["bytes"], "flops": layer["flops"], "bound_ms": round(t_bound * 1e3, 5),
+                  "frac": round(t_bound / (device_s / steps), 5)}
 
     # end to end through the C ABI: pinned host inputs in, result back to pinned host memory
     host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out.numel() * host_out.element_size()
+    e2e_n = max(1, min(e2e_steps, steps))
     e2e_ms = []
-    for i in range(args.warmup + args.steps):
+    for i in range(2 + e2e_n):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -355,19 +384,46 @@ def run_prefill_bench(args, dist, peaks):
         host_out.copy_(out, non_blocking=True)
         b.record(stream)
         b.synchronize()
-        if i >= args.warmup:
+        if i >= 2:
             e2e_ms.append(a.elapsed_time(b))
     e2e_s = dist.max(sum(e2e_ms) / 1e3)
-    tokens = wl.total_tokens * dist.world * args.steps
-    return {
-        "value": tokens / device_s, "ms_per_step": device_s * 1e3 / args.steps, "wall_s": wall,
+    del host, host_out
+    tokens = wl.total_tokens * dist.world
+    res = {
+        "value": tokens * steps / device_s, "unit": "tokens/s", "steps": steps, "warmup": warmup,
+        "ms_per_step": device_s * 1e3 / steps, "wall_s": wall,
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "roofline": roofline,
-        "stage_roofline": stage_roofline,
-        "clocks": clocks.summary(), "gpu_launches": launches_per_step * args.steps,
-        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "workload": wl,
+        "stage_roofline": stage_roofline, "layer_roofline": layer_roof,
+        "clocks": clocks.summary(), "gpu_launches": launches_per_step * steps,
+        "e2e": {"value": tokens * e2e_n / e2e_s, "unit": "tokens/s", "steps": e2e_n,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "workload": wl, "inputs": x,
     }
+    del ws, out, flush
+    return res
+
+
+def layer_work(wl) -> dict:
+    """Algorithmic work of the whole layer per prefill: bytes = q and o in the layer dtype, k and v per kv
+    head, g and beta fp32 (intermediates excluded); flops = the chunked GDN's useful flops per absorbed
+    token-head plus 4 d per visible key per (token, q-head) of the softmax."""
+    d, Hq, Hkv = wl.head_dim, wl.n_q_heads, wl.n_kv_heads
+    eb = 2 if wl.dtype == "bf16" else 4
+    T = wl.total_tokens
+    absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens)
+    keys = sum(visible_keys(L, wl.n_sinks, wl.window) for L in wl.seqlens)
+    nbytes = T * (2 * Hq * d * eb + 2 * Hkv * d * eb + 2 * Hq * 4)
+    flops = chunked_gdn_flops_per_token_head(d)["total"] * absorbed * Hq + 4.0 * d * keys * Hq
+    return {"bytes": float(nbytes), "flops": float(flops)}
+
+
+def visible_keys(L: int, n_sinks: int, window: int) -> int:
+    """Keys the softmax branch visits over a sequence of L positions: min(p + 1, n_sinks) sinks plus
+    the window positions after the sinks, for every position p."""
+    total = 0
+    for p in range(L):
+        total += min(p + 1, n_sinks) + max(0, min(window, p + 1 - n_sinks))
+    return total
 
 
 # ---------------------------------------------------------------------------
@@ -384,6 +440,17 @@ def decode_bytes(wl, pos_mean: float) -> float:
     b += N * 7 * (Hq + 2 * Hkv) * d * 4 * 2        # conv caches read + write
     b += N * (Hq + 2 * Hkv) * d * eb + N * Hq * d * eb   # q, k, v in; out
     return float(b)
+
+
+DECODE_SOURCES = [CSRC + "decode.cu", CSRC + "hla_common.cuh"]
+DECODE_KERNELS = ("decode_features_kernel", "decode_attn_state_kernel", "decode_combine_kernel")
+
+
+def decode_traffic() -> float | None:
+    """DRAM bytes of one decode step (all its launches) from the committed capture, if decode.cu is
+    unchanged since."""
+    parts = [kernel_traffic(k, DECODE_SOURCES, "c3") for k in DECODE_KERNELS]
+    return None if any(p is None for p in parts) else float(sum(parts))
 
 
 def run_decode_bench(args, dist, peaks):
@@ -403,13 +470,14 @@ def run_decode_bench(args, dist, peaks):
         x.pop(key)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    K = args.decode_steps or args.steps
+    K = args.decode_steps
     W = args.warmup
-    assert W + K <= wl.decode_steps
+    n_in = wl.decode_steps  # synthetic step inputs; step s feeds those of step s mod n_in
     dout = torch.empty(x["dq"].shape[1:], dtype=x["dq"].dtype, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step(s):
+        s %= n_in
         hla.decode_step(prm, x["dq"][s], x["dk"][s], x["dv"][s], x["dg"][s], x["dbeta"][s], x["lam"],
                         x["wq"], x["wk"], x["wv"], st, dout)
 
@@ -429,47 +497,86 @@ def run_decode_bench(args, dist, peaks):
     ms = [a.elapsed_time(b) for a, b in evs]
     dev_s = dist.max(sum(ms) / 1e3)
     per_step = dev_s / K
-    nbytes = decode_bytes(wl, 8192 + W + K / 2)
+    nbytes = decode_bytes(wl, 8192 + W + K / 2)  # the ring is full from the first step on
     achieved = nbytes / per_step / 1e9
-    return {"value": K * dist.world / dev_s, "unit": "steps/s", "ms_per_step": per_step * 1e3,
-            "tokens_per_s": K * dist.world * wl.n_seqs / dev_s,
+    # end to end: this step's q, k, v, g, beta from pinned host memory, the output back
+    keys = ("dq", "dk", "dv", "dg", "dbeta")
+    host = {k: x[k][:8].cpu().pin_memory() for k in keys}
+    dev_in = {k: torch.empty_like(x[k][0]) for k in keys}
+    host_out = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
+    h2d = sum(dev_in[k].numel() * dev_in[k].element_size() for k in keys)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_n = min(K, 1000)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(e2e_n):
+        for k in keys:
+            dev_in[k].copy_(host[k][i % 8], non_blocking=True)
+        hla.decode_step(prm, dev_in["dq"], dev_in["dk"], dev_in["dv"], dev_in["dg"], dev_in["dbeta"], x["lam"],
+                        x["wq"], x["wk"], x["wv"], st, dout)
+        host_out.copy_(dout, non_blocking=True)
+    b.record(stream)
+    b.synchronize()
+    e2e_s = dist.max(a.elapsed_time(b) / 1e3)
+    traffic = decode_traffic()
+    return {"value": K * dist.world / dev_s, "unit": "steps/s", "steps": K, "warmup": W,
+            "ms_per_step": per_step * 1e3, "tokens_per_s": K * dist.world * wl.n_seqs / dev_s,
             "config": {"workload": wl.name, "sequences": wl.n_seqs, "prefill_len": 8192,
-                       "ring": wl.n_sinks + wl.window, "l2": "working set (state + ring) > L2"},
+                       "ring": wl.n_sinks + wl.window, "l2": "working set (state + ring) > L2",
+                       "inputs": f"step s feeds the synthetic inputs of step s mod {n_in}"},
             "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": round(achieved, 2),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": None, "algorithmic_bytes_per_step": nbytes},
-            "clocks": clocks.summary(), "gpu_launches": 3 * K}  # features; state + softmax; combine
+                         "traffic": traffic, "algorithmic_bytes_per_step": nbytes,
+                         "peak_source": peaks["source"]},
+            "e2e": {"value": e2e_n * dist.world / e2e_s, "unit": "steps/s", "steps": e2e_n,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clocks.summary(), "gpu_launches": DECODE_LAUNCHES * K}
+
+
+DECODE_LAUNCHES = 3  # features; state + softmax; combine
 
 
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and reference arm)
-def oracle_jobs(wl, x, heads):
+def oracle_jobs(wl, x, units):
+    """Oracle inputs of the (sequence, q-head) units, cut from the input tensors x (any device)."""
     import torch
 
     f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
     cu = x["cu_seqlens"].tolist()
     d, G = wl.head_dim, wl.n_q_heads // wl.n_kv_heads
     jobs = []
-    for n in range(wl.n_seqs):
+    for n, h in units:
         a, b = cu[n], cu[n + 1]
-        for h in heads:
-            kv = h // G
-            jobs.append(dict(q=f64(x["q"][a:b, h]), k=f64(x["k"][a:b, kv]), v=f64(x["v"][a:b, kv]),
-                             g=f64(x["g"][a:b, h]), beta=f64(x["beta"][a:b, h]),
-                             lam=float(x["lam"][h]), wq=f64(x["wq"][h * d:(h + 1) * d]),
-                             wk=f64(x["wk"][kv * d:(kv + 1) * d]), wv=f64(x["wv"][kv * d:(kv + 1) * d])))
+        kv = h // G
+        jobs.append(dict(q=f64(x["q"][a:b, h]), k=f64(x["k"][a:b, kv]), v=f64(x["v"][a:b, kv]),
+                         g=f64(x["g"][a:b, h]), beta=f64(x["beta"][a:b, h]),
+                         lam=float(x["lam"][h]), wq=f64(x["wq"][h * d:(h + 1) * d]),
+                         wk=f64(x["wk"][kv * d:(kv + 1) * d]), wv=f64(x["wv"][kv * d:(kv + 1) * d])))
     return jobs
 
 
-def time_oracle(wl, heads, reps=1):
-    """Wall time of the oracle over `heads` of every sequence of wl, on all host cores."""
+def oracle_units(wl, target_token_heads: float):
+    """A strided sample of (sequence, q-head) units whose token-heads add up to about the target
+    (all units if they add up to less): every sequence, q-heads spread evenly."""
+    total = wl.total_tokens * wl.n_q_heads
+    frac = min(1.0, target_token_heads / total)
+    per_seq = max(1, round(wl.n_q_heads * frac))
+    stride = wl.n_q_heads / per_seq
+    return [(n, int(i * stride)) for n in range(wl.n_seqs) for i in range(per_seq)]
+
+
+# fp64 oracle token-heads per second and core, for sizing the samples (about 10-30 s of CPU work)
+ORACLE_TOKEN_HEADS_PER_CORE_S = 1.7e4
+
+
+def time_oracle(wl, x, units, reps=1):
+    """Wall times of the oracle over `units` of wl, on all host cores."""
     import oracle
-    from linearized_attention_rope_gb300 import synth
 
     oracle.build()
-    x = synth.make_inputs(wl, "cpu")
-    jobs = oracle_jobs(wl, x, heads)
+    jobs = oracle_jobs(wl, x, units)
     cfg = oracle.OracleCfg(d=wl.head_dim, n_sinks=wl.n_sinks, window=wl.window)
     cores = min(os.cpu_count() or 1, len(jobs))
     times = []
@@ -480,13 +587,19 @@ def time_oracle(wl, heads, reps=1):
     return times, cores
 
 
-def cpu_baseline(wl):
-    heads = list(range(wl.n_q_heads))
-    times, cores = time_oracle(wl, heads)
-    tokens = wl.total_tokens * len(heads) / wl.n_q_heads
-    return {"value": tokens / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{wl.name}: all {wl.n_q_heads} q-heads of every sequence "
-                      f"({wl.total_tokens} tokens), one pass, fp64 C oracle, {cores} threads"}
+def cpu_baseline(wl, x, seconds: float = 10.0):
+    """The oracle as it stands, on the host cores, over a strided sample of units sized to about
+    `seconds`; reported in token-equivalents (a token needs all q-heads) per second."""
+    cores = os.cpu_count() or 1
+    units = oracle_units(wl, seconds * cores * ORACLE_TOKEN_HEADS_PER_CORE_S)
+    times, used = time_oracle(wl, x, units)
+    seqlens = wl.seqlens
+    token_heads = sum(seqlens[n] for n, _ in units)
+    tokens = token_heads / wl.n_q_heads
+    return {"value": tokens / times[0], "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{wl.name}: {len(units)} (sequence, q-head) units, q-heads strided evenly over every "
+                      f"sequence ({token_heads} token-heads = {tokens:.0f} token-equivalents), one pass, "
+                      f"fp64 C oracle, {used} threads, {times[0]:.1f} s"}
 
 
 def run_reference(args, dist):
@@ -495,18 +608,22 @@ def run_reference(args, dist):
     if dist.rank != 0:
         return None
     wl = synth.workloads()[args.workload]
-    heads = list(range(0, wl.n_q_heads, 2))  # half the q-heads per step: a bounded sample
-    times, cores = time_oracle(wl, heads, reps=args.warmup + args.steps)
+    x = synth.make_inputs(wl, "cpu")
+    cores = os.cpu_count() or 1
+    # each step a bounded sample: about 1 s of oracle work per step
+    units = oracle_units(wl, 1.0 * cores * ORACLE_TOKEN_HEADS_PER_CORE_S)
+    times, used = time_oracle(wl, x, units, reps=args.warmup + args.steps)
     timed = times[args.warmup:]
-    tokens = wl.total_tokens * len(heads) / wl.n_q_heads
+    token_heads = sum(wl.seqlens[n] for n, _ in units)
+    tokens = token_heads / wl.n_q_heads
     value = tokens * len(timed) / sum(timed)
-    sample = (f"{wl.name}: q-heads {heads[0]}..{heads[-1]} step 2 of every sequence per step "
-              f"({tokens:.0f} token-equivalents), fp64 C oracle, {cores} threads")
+    sample = (f"{wl.name}: {len(units)} (sequence, q-head) units per step, q-heads strided evenly over every "
+              f"sequence ({tokens:.0f} token-equivalents), fp64 C oracle, {used} threads")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(timed) / len(timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "tokens": wl.total_tokens},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -516,21 +633,33 @@ TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
     "window_softmax_tc_kernel": SOFTMAX_TC_SOURCES,
     "gdn_inverse_kernel": GDN_PREP_SOURCES,
     "gdn_chunked_kernel": GDN_CHUNKED_SOURCES,
+    "decode_features_kernel": DECODE_SOURCES,
+    "decode_attn_state_kernel": DECODE_SOURCES,
+    "decode_combine_kernel": DECODE_SOURCES,
 }
 
 
-def write_traffic(rep: str):
-    """profiles/traffic.json from `ncu -i rep --page raw --csv`."""
+def write_traffic(rep: str, key: str, calls: int = 1):
+    """Stores the counters of an ncu report (`ncu -i rep --page raw --csv`) in profiles/traffic.json under
+    workload `key`; the report holds the launches of `calls` calls (prefill calls or decode steps)."""
     raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
                          text=True).stdout
-    with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
-        json.dump(traffic_from_csv(raw), f, indent=1)
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    data = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            data = json.load(f)
+    data[key] = traffic_from_csv(raw, calls)
+    data[key]["_report"] = os.path.basename(rep)
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1)
         f.write("\n")
 
 
-def traffic_from_csv(raw: str) -> dict:
-    """Per kernel of TRAFFIC_KERNELS, the DRAM bytes and ncu durations summed over its launches in an
-    ncu raw-page CSV (one prefill call), keyed by a hash of the kernel's sources."""
+def traffic_from_csv(raw: str, calls: int = 1) -> dict:
+    """Per kernel of TRAFFIC_KERNELS, the DRAM bytes and ncu durations of its launches in an ncu raw-page
+    CSV, summed and divided by the number of calls the capture covers (per call: the GDN kernels run once
+    per part of the chunk slots), keyed by a hash of the kernel's sources."""
     import csv
     import io
 
@@ -541,36 +670,42 @@ def traffic_from_csv(raw: str) -> dict:
     units = rows[1]
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-3, "nsecond": 1e-3, "us": 1.0,
              "usecond": 1.0, "ms": 1e3, "msecond": 1e3}  # to bytes and microseconds
-    out = {"_command": "ncu --set full --clock-control none -k regex:\"features_kernel|gdn_inverse_kernel|"
-                       "gdn_chunked_kernel|window_softmax_tc_kernel\" -s 6 -c 6 -o prof python bench.py "
-                       "--no-decode --no-cpu-baseline --steps 3 --warmup 3",
-           "_workload": synth_workload_name("c1") + " (the launches of one prefill call; cold caches: ncu "
-                                                   "flushes them before each pass)",
-           "_note": "per step = summed over the kernel's launches in one prefill call (the GDN kernels run "
-                    "once per part of the chunk slots)"}
+    out = {"_note": "per step = the kernel's launches in one call (cold caches: ncu flushes them before "
+                    "each pass)"}
     for name, srcs in TRAFFIC_KERNELS.items():
         mine = [r for r in body if re.search(r"(^|[\s:])" + name + r"[<(]", r[col["Kernel Name"]])]
         if not mine:
             continue
         val = lambda r, k: float(r[col[k]].replace(",", "")) * scale[units[col[k]]]
-        rd = sum(val(r, "dram__bytes_read.sum") for r in mine)
-        wr = sum(val(r, "dram__bytes_write.sum") for r in mine)
-        out[name] = {"source_sha256": source_hash(srcs), "launches_per_step": len(mine),
+        rd = sum(val(r, "dram__bytes_read.sum") for r in mine) / calls
+        wr = sum(val(r, "dram__bytes_write.sum") for r in mine) / calls
+        out[name] = {"source_sha256": source_hash(srcs), "launches_per_step": len(mine) / calls,
                      "dram_bytes_read": rd, "dram_bytes_write": wr, "dram_bytes_per_step": rd + wr,
-                     "duration_us_ncu": round(sum(val(r, "gpu__time_duration.sum") for r in mine), 3)}
+                     "duration_us_ncu": round(sum(val(r, "gpu__time_duration.sum") for r in mine) / calls, 3)}
     return out
 
 
-def synth_workload_name(key: str) -> str:
-    from linearized_attention_rope_gb300 import synth
-
-    return synth.workloads()[key].name
+def prefill_line(pre: dict, key: str, dist, with_cpu: bool) -> dict:
+    """The reported object of one prefill workload."""
+    wl = pre.pop("workload")
+    x = pre.pop("inputs")
+    obj = {"value": pre["value"], "unit": "tokens/s", "steps": pre["steps"], "warmup": pre["warmup"],
+           "ms_per_step": pre["ms_per_step"],
+           "config": {"workload": wl.name, "key": key, "global_batch": wl.n_seqs * dist.world,
+                      "seq_len": max(wl.seqlens), "tokens_per_rank": wl.total_tokens,
+                      "l2": "flushed between steps (512 MiB write)"},
+           "roofline": pre["roofline"], "layer_roofline": pre["layer_roofline"], "stage_ms": pre["stage_ms"],
+           "stage_roofline": pre["stage_roofline"], "clocks": pre["clocks"], "e2e": pre["e2e"],
+           "gpu_launches": pre["gpu_launches"], "wall_s": round(pre["wall_s"], 3)}
+    if with_cpu:
+        obj["cpu_baseline"] = cpu_baseline(wl, x)
+    return obj
 
 
 def main():
     args = parse()
     if args.traffic_from:
-        write_traffic(args.traffic_from)
+        write_traffic(args.traffic_from, args.traffic_key)
         return
     dist = Dist()
     if args.impl == "reference":
@@ -595,30 +730,40 @@ def main():
             print(json.dumps({"decode": dec}), flush=True)
         dist.close()
         return
-    pre = run_prefill_bench(args, dist, peaks)
+    with_cpu = dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
+    pre = run_prefill_bench(args.workload, args.steps, args.warmup, dist, peaks, args.e2e_steps, args.stage_steps)
+    wl = pre["workload"]
+    head = prefill_line(pre, args.workload, dist, with_cpu)
+    del pre
+    torch.cuda.empty_cache()
+    extras = {}
+    for key in [k for k in args.extra.split(",") if k and k != args.workload]:
+        p = run_prefill_bench(key, 0, 3, dist, peaks, min(args.e2e_steps, 10), min(args.stage_steps, 10),
+                              trial_seconds=args.extra_seconds)
+        extras["prefill_" + key] = prefill_line(p, key, dist, with_cpu)
+        del p
+        torch.cuda.empty_cache()
     dec = None if args.no_decode else run_decode_bench(args, dist, peaks)
     torch.cuda.synchronize()
-    wl = pre.pop("workload")
     line = {
-        "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms_per_step"],
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded; shapes of the named layer, no trained weights)",
-        "config": {"workload": wl.name, "global_batch": wl.n_seqs * dist.world,
-                   "seq_len": max(wl.seqlens), "tokens_per_rank": wl.total_tokens,
-                   "parallelism": f"replicas x{dist.world}", "l2": "flushed between steps (512 MiB write)",
-                   "precision": "bf16 in/out, fp16 MMA operands, fp32 state and accumulation"},
-        "roofline": pre["roofline"], "stage_ms": pre["stage_ms"],
-        "stage_ms_source": "each kernel's launches timed on their streams over --steps instrumented steps run "
-                           "right after the timed region",
-        "stage_roofline": pre["stage_roofline"],
-        "clocks": pre["clocks"], "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"],
-        "wall_s": round(pre["wall_s"], 3),
+        "config": dict(head["config"], parallelism=f"replicas x{dist.world}",
+                       precision="bf16 in/out, fp16 MMA operands, fp32 state and accumulation"),
+        "roofline": head["roofline"], "layer_roofline": head["layer_roofline"], "stage_ms": head["stage_ms"],
+        "stage_ms_source": "each kernel's launches timed on their stream over --stage-steps instrumented steps "
+                           "run right after the timed region (every launch alone)",
+        "stage_roofline": head["stage_roofline"],
+        "clocks": head["clocks"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "wall_s": head["wall_s"],
     }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    line.update(extras)
     if dec:
         line["decode"] = dec
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()

@@ -66,6 +66,17 @@ extern "C" {
 #define HLA_FLAG_LINEAR_OFF 0x4u     /* test hook: drop the linear branch */
 #define HLA_FLAG_GDN_RECURRENT 0x8u  /* use the token-serial fp32 GDN kernel in
                                         place of the chunked tensor-core one */
+#define HLA_FLAG_GLA 0x10u           /* gated linear attention in place of the
+                                        delta rule: S <- alpha S + khat vhat^T
+                                        (no erase term, beta unused), the other
+                                        update of section 线性注意力替换机制 */
+#define HLA_FLAG_TEST_STALL 0x20u    /* test hook (tensor-core path): the GDN
+                                        state kernel loads nothing, so its
+                                        bounded waits run out after about a
+                                        millisecond; the call completes and the
+                                        workspace error word reads back
+                                        HLA_ERR_TIMEOUT.  Outputs are then
+                                        undefined. */
 
 /* Layer shape.  n_q_heads must be a multiple of n_kv_heads (grouped-query
  * attention: q-head h reads kv-head h / (n_q_heads / n_kv_heads)).
@@ -152,7 +163,13 @@ HLA_API int hla_state_init(const hla_params* params, int n_seqs, const hla_state
  *   out [total, Hq, d]            params->dtype
  *   st                            NULL, or a state freshly set up by
  *                                 hla_state_init for n_seqs sequences: it
- *                                 receives everything decoding needs
+ *                                 receives everything decoding needs.  A
+ *                                 state with a position other than 0 is
+ *                                 not fresh: the first kernel flags it in
+ *                                 the state's error word (then
+ *                                 hla_check_device_error returns
+ *                                 HLA_ERR_STATE) and its contents are
+ *                                 undefined; `out` is unaffected
  *   ws, ws_bytes                  workspace of at least
  *                                 hla_prefill_workspace_bytes bytes
  * With total_tokens == 0 the per-token pointers may be NULL.
@@ -172,29 +189,46 @@ HLA_API int hla_prefill(const hla_params* params, const void* q, const void* k, 
  * allocator, or a latency-critical caller that cannot afford the implicit
  * device-wide synchronisation of cudaMalloc/cudaFree.
  * Arguments and results are those of hla_prefill; the scratch memory comes
- * from a 64 MiB buffer inside the library (one per GPU that loads it, held
- * until the process exits).  Prefills whose hla_prefill_workspace_bytes
- * exceeds 64 MiB (about 1,300 tokens of a 32 q / 8 kv head, head_dim 128
- * bf16 layer) return HLA_ERR_WORKSPACE before any GPU work.
- * The first call on each device looks up the buffer's device address (a
- * host-side set-up step); make that first call before any stream capture.
+ * from a 64 MiB buffer inside the library.  That buffer is device memory of
+ * every process that loads libhla.so, on every GPU where the library's
+ * device code gets loaded (at context creation under eager module loading;
+ * under lazy loading, the CUDA default, once this entry point first runs on
+ * that GPU), whether or not the process ever calls hla_prefill_noalloc, and
+ * it is held until the process exits.  Prefills whose
+ * hla_prefill_workspace_bytes exceeds 64 MiB (about 1,300 tokens of a
+ * 32 q / 8 kv head, head_dim 128 bf16 layer) return HLA_ERR_WORKSPACE before
+ * any GPU work.
+ * The first call on each device (and the first after that device's context
+ * was reset) looks up the buffer's device address, a host-side set-up step;
+ * make that first call before any stream capture.
  * It allocates nothing: no cudaMalloc, no cudaFree.
  * All calls share the one buffer and each overwrites what the last left in
  * it: calls that overlap on the GPU (other streams, other threads) race, so
- * order them on one stream.  The buffer's device error word is not readable
- * by the caller. */
+ * order them on one stream.  Problems found on the device (malformed
+ * cu_seqlens, a bounded wait that ran out) land in the buffer's error word:
+ * read it with hla_prefill_noalloc_check_error. */
 HLA_API int hla_prefill_noalloc(const hla_params* params, const void* q, const void* k,
                                 const void* v, const float* g, const float* beta,
                                 const float* lambda, const float* conv_wq, const float* conv_wk,
                                 const float* conv_wv, const int32_t* cu_seqlens, int n_seqs,
                                 int64_t total_tokens, void* out, const hla_state* st, void* stream);
 
+/* The device error word of hla_prefill_noalloc's buffer on the current
+ * device, as hla_check_workspace_error reads a workspace's: synchronises
+ * `stream`, stores the word in *code (may be NULL), clears it, and returns
+ * HLA_OK if it was zero, else the matching HLA_ERR_* status.  Allocates
+ * nothing. */
+HLA_API int hla_prefill_noalloc_check_error(void* stream, int32_t* code);
+
 /* One decode step for every sequence of `st`: token pos[n] of sequence n.
  *   q [N, Hq, d], k, v [N, Hkv, d]  (params->dtype), g, beta [N, Hq] fp32,
  *   lambda and conv filters as for hla_prefill, out [N, Hq, d].
  * The token leaving the window (position pos - window, if not a sink) is
  * absorbed into S first; then the new token's output is formed; pos += 1.
- * Asynchronous. */
+ * At most 8 query heads per kv head (else HLA_ERR_UNSUPPORTED).  A sequence
+ * whose pos is negative (no prefill or decode step leaves one) is left as it
+ * is, its output row is undefined, and the state's error word reports
+ * HLA_ERR_STATE.  Asynchronous. */
 HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q, const void* k,
                             const void* v, const float* g, const float* beta, const float* lambda,
                             const float* conv_wq, const float* conv_wk, const float* conv_wv,

@@ -133,7 +133,7 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
 // Steps 2 and 3 stream the state and the ring, the step's bulk traffic; they
 // run as one launch whose CTAs are state units and softmax splits in turn, so
 // both streams share every wave.
-constexpr int kMaxG = 8;
+constexpr int kMaxG = kMaxDecodeGroup;
 constexpr int kFeatThreads = 256;
 constexpr int kStateThreads = 128;
 constexpr int kSmThreads = 128;
@@ -178,6 +178,10 @@ decode_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __rest
     const int kv = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.G, ns = L.n_sinks, W = L.window, R = ns + W, P = W + 1;
     const int64_t p = s.pos[n];
+    if (p < 0) {  // not a position a prefill or a decode step can leave: flag it, touch nothing
+        if (tid == 0) atomicExch(s.err, kErrState);
+        return;
+    }
     const size_t kvrow = ((size_t)n * L.Hkv + kv) * D;
 
     if (tid < HALF) {
@@ -264,6 +268,7 @@ __device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_
     __shared__ float cdot_s;
     const int tid = threadIdx.x, kv = h / L.G;
     const int ns = L.n_sinks, W = L.window, P = W + 1;
+    const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
     const int64_t p = s.pos[n], j = p - W;  // the token leaving the window
     float* olin = sc.olin + ((size_t)n * L.Hq + h) * D;
     if (j < ns) {  // nothing leaves the window into the state this step
@@ -311,7 +316,7 @@ __device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_
         float xs = 0.f, ys = 0.f;
 #pragma unroll
         for (int r = 0; r < RG; ++r) { xs += redx[r][col]; ys += redy[r][col]; }
-        u[e] = b * (vj_s[col] - alpha * xs);
+        u[e] = gla ? vj_s[col] : b * (vj_s[col] - alpha * xs);  // GLA: no erase, write gain 1
         if (rg == 0) olin[col] = fmaf(alpha, ys, cdot_s * u[e]);
     }
 #pragma unroll
@@ -528,6 +533,7 @@ template <typename Tin, int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out,
                       int64_t* __restrict__ pos) {
+    // (a negative position was flagged by the features launch; it is left as it is)
     const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x;
     const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
     float m = -INFINITY, l = 0.f, o = 0.f;  // running merge
@@ -558,19 +564,18 @@ decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lamb
     o = (L.flags & HLA_FLAG_SOFTMAX_OFF) || l <= 0.f ? 0.f : o / l;
     if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), sc.olin[((size_t)n * L.Hq + h) * D + c], o);
     out[((size_t)n * L.Hq + h) * D + c] = from_f32<Tin>(o);
-    if (h == 0 && c == 0) pos[n] += 1;
+    if (h == 0 && c == 0 && pos[n] >= 0) pos[n] += 1;
 }
 
 template <typename Tin, int D, int GM>
 cudaError_t launch_decode_attn_state(const LayerDims& L, const hla_state& s, const DecScratch& sc, cudaStream_t st) {
     using P = DecSm<Tin, D, GM>;
-    static bool configured = false;  // per instantiation
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_attn_state_kernel<Tin, D, GM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static DeviceCache cache;  // the shared-memory attribute, per device and instantiation
+    cudaError_t e = device_cached(cache, nullptr, [](int, int*) {
+        return cudaFuncSetAttribute(decode_attn_state_kernel<Tin, D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)P::kSmemBytes);
+    });
+    if (e != cudaSuccess) return e;
     decode_attn_state_kernel<Tin, D, GM><<<dim3(L.Hkv * (L.G + sc.splits), L.n_seqs), kSmThreads, P::kSmemBytes,
                                            st>>>(L, s, sc);
     return cudaGetLastError();

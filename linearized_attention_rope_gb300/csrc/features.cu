@@ -38,6 +38,11 @@ __global__ void prefill_tables_kernel(LayerDims L, float2* __restrict__ fine, fl
     if (blockIdx.x != 0) return;
     if (threadIdx.x < 4) t.err[threadIdx.x] = 0;
     if (threadIdx.x < t.n_counters) t.counters[threadIdx.x] = 0;
+    if (threadIdx.x == 96 && t.st_pos) {  // the state to fill must be fresh (every position 0)
+        bool fresh = true;
+        for (int q = 0; q < L.n_seqs; ++q) fresh = fresh && t.st_pos[q] == 0;
+        if (!fresh) atomicExch(t.st_err, kErrState);
+    }
     // Work tables: base[s] = items of the sequences before s, base[n_seqs] = all.
     int32_t* base = nullptr;
     int per = 1;
@@ -388,19 +393,20 @@ static cudaError_t launch_features_d(const LayerDims& L, const Tin* q, const Tin
                                      const float2* coarse, Tf* qr, Tf* kr, Tf* qhat, Tf* khat, Tf* vhat,
                                      int32_t* err, bool after_prior, cudaStream_t st) {
     const size_t smem = (size_t)kFeatWarps * kRing * kBlk * D * sizeof(Tin);
-    static int resident = 0;  // CTAs resident on the device at once (per instantiation)
-    if (!resident) {
-        cudaError_t e = cudaFuncSetAttribute(features_kernel<Tin, Tf, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static DeviceCache cache;  // CTAs resident on the device at once, per device and instantiation
+    int resident = 0;
+    cudaError_t e = device_cached(cache, &resident, [smem](int dev, int* v) {
+        int n_sm = 0, per_sm = 0;
+        cudaError_t r = cudaFuncSetAttribute(features_kernel<Tin, Tf, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
-        int dev = 0, n_sm = 0, per_sm = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, features_kernel<Tin, Tf, D>, 32 * kFeatWarps,
+        if (r == cudaSuccess) r = sm_count(dev, &n_sm);
+        if (r == cudaSuccess)
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, features_kernel<Tin, Tf, D>, 32 * kFeatWarps,
                                                               smem);
-        if (e != cudaSuccess) return e;
-        resident = std::max(1, n_sm * std::max(1, per_sm));
-    }
+        *v = std::max(1, n_sm * std::max(1, per_sm));
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     const int row_groups = (L.Hq + 2 * L.Hkv + kFeatWarps - 1) / kFeatWarps;
     const int64_t span = feature_span(L.total, row_groups, resident);
     LaunchCfg lc(dim3((unsigned)((L.total + span - 1) / span), (unsigned)row_groups), dim3(32 * kFeatWarps), smem,

@@ -164,6 +164,11 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     const int n_chunks = min(max(slot_hi - slot0, 0), seq_chunks) - c_lo;
     const bool resume = S_in && c_lo > 0;  // continue from the state the previous launch left
 
+    // The stall test hook: the loader issues nothing, so every wait below runs out (after a millisecond
+    // instead of the usual two seconds) and the kernel reports a timeout without any copy or MMA in flight.
+    const bool stall = (L.flags & HLA_FLAG_TEST_STALL) != 0;
+    const uint64_t wait_ns = stall ? 1000000ull : 2000000000ull;
+
     // One leader per role polls the mbarrier (an inline try first, the bounded
     // loop only if the phase is still open) and posts the outcome in a shared
     // slot; the role (`count` threads on named barrier `id`; 0 for a one-thread
@@ -174,7 +179,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     auto role_wait = [&](int i, uint32_t parity, int id, int count, bool leader, int& k) -> bool {
         bool w = true;
         if (leader) {
-            w = !*abort_flag && (umma::mbar_try_wait(bar(i), parity) || umma::mbar_wait(bar(i), parity, kWaitLimit));
+            w = !*abort_flag &&
+                (umma::mbar_try_wait(bar(i), parity) || umma::mbar_wait(bar(i), parity, kWaitLimit, wait_ns));
             if (!w) {
                 *abort_flag = 1;
                 if (err) atomicExch(err, kErrTimeout);
@@ -298,7 +304,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
         int kl = 0;  // (unused by one-thread waits)
 #pragma unroll 1
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = 0; c < (stall ? 0 : n_chunks); ++c) {
             const int b = c & 1;
             if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true, kl)) break;
             const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
@@ -378,13 +384,11 @@ cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __h
                                const unsigned char* rec_in, const __half* o_sm, const float* lambda,
                                __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, bool beside_prior,
                                cudaStream_t st) {
-    static bool configured = false;  // the attribute is per function
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static DeviceCache cache;  // the shared-memory attribute, per device
+    cudaError_t e = device_cached(cache, nullptr, [](int, int*) {
+        return cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    });
+    if (e != cudaSuccess) return e;
     if (L.total <= 0)  // no token anywhere: the final states are zero
         return S_out ? cudaMemsetAsync(S_out, 0, (size_t)L.n_seqs * L.Hq * kD * kD * sizeof(float), st) : cudaSuccess;
     CUtensorMap mq, mk, mv;

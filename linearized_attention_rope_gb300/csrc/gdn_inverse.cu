@@ -15,6 +15,12 @@
 //
 // Chunk slots: sequence s owns slots [chunk_base[s], chunk_base[s+1]); its
 // chunk c covers absorbed tokens n_sinks + 64 c .. + 63.
+//
+// With HLA_FLAG_GLA (gated linear attention, S <- alpha S + k v^T, the other
+// update of section 线性注意力替换机制) the same record serves the state
+// kernel unchanged: A = 0 gives T = I, the write gain is 1 in place of beta,
+// and nothing is erased, so -Wm = 0; then U = V, O = diag(gamma) Q S0 + P V
+// and S1 = gamma_C S0 + (diag(e^{G_C - G}) K)^T V.
 #include <algorithm>
 
 #include "hla_common.cuh"
@@ -91,6 +97,8 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     volatile int* next_s = reinterpret_cast<volatile int*>(sm + kMisc + 24);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t mbar = umma::smem_addr(mbar_p), sbase = umma::smem_addr(sm);
+    // GLA (no erase, write gain 1): A = 0, so T = I; beta taken as 1; Wm = 0
+    const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
     // items (chunk slot, q-head) of slots [slot_lo, slot_hi), taken one at a time from `counter`
     const int64_t item_lo = (int64_t)slot_lo * L.Hq;
     const int64_t item_hi = (int64_t)min(slot_hi, __ldg(chunk_base + L.n_seqs)) * L.Hq;
@@ -150,7 +158,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     if (tid < kC) {
         const size_t t = (size_t)(start + j0 + tid);
         gi = tid < nv ? g[t * L.Hq + h] * 1.4426950408889634f : 0.f;
-        sBeta[tid] = tid < nv ? beta[t * L.Hq + h] : 0.f;
+        sBeta[tid] = tid < nv ? (gla ? 1.f : beta[t * L.Hq + h]) : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, gi, o);
@@ -200,7 +208,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int ii = 4 * i4 + e, i = 32 * half + ii;
-                    sA[r * kSA + i] = (i < r) ? br * exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
+                    sA[r * kSA + i] = (i < r && !gla) ? br * exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
                 }
             }
         }
@@ -277,7 +285,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
             tb[x] = tr[x] * sBeta[c8 + x];
-            tbg[x] = tb[x] * sGam[c8 + x];
+            tbg[x] = gla ? 0.f : tb[x] * sGam[c8 + x];
         }
         const uint32_t off = umma::sw128_offset(r, c8, 64);
         *reinterpret_cast<uint4*>(rec + kRecTb + off) =
@@ -349,21 +357,15 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
                                const float* beta, const int32_t* cu, const int32_t* chunk_base, int slot_lo,
                                int slot_hi, int32_t* counter, unsigned char* rec_out, int32_t* err, bool beside_prior,
                                cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
     if (slot_hi <= slot_lo) return cudaSuccess;
-    static int n_sm = 0;  // per-process device property cache
-    if (!n_sm) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
-            n_sm = 132;
-    }
+    static DeviceCache cache;  // the shared-memory attribute and the SM count, per device
+    int n_sm = 0;
+    cudaError_t e = device_cached(cache, &n_sm, [](int dev, int* v) {
+        cudaError_t r = cudaFuncSetAttribute(gdn_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemAlloc);
+        return r == cudaSuccess ? sm_count(dev, v) : r;
+    });
+    if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)(slot_hi - slot_lo) * L.Hq;
     const unsigned grid = (unsigned)std::min<int64_t>(items, (int64_t)n_sm * 3);
     LaunchCfg lc(dim3(grid), dim3(kThreads), kSmemAlloc, st, beside_prior);

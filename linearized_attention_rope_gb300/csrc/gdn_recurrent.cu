@@ -4,7 +4,8 @@
 // with a scalar gate), applied to token j when it leaves the window, i.e. at
 // position j + W (section 填补近似缺口的实用设计: the linear path covers the
 // tokens outside the sink + window budget), followed by the read-out
-// o_lin[j + W] = S^T qhat[j + W].
+// o_lin[j + W] = S^T qhat[j + W].  With HLA_FLAG_GLA the update is the gated
+// linear attention of the same section, S <- alpha_j S + khat_j vhat_j^T.
 //
 // One CTA per (sequence, query head); four adjacent threads own one column of
 // S (the value dim), a quarter of its key rows each, in registers; dot
@@ -41,6 +42,7 @@ gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restr
     const int h = blockIdx.x, n = blockIdx.y, kv = h / L.G;
     const int col = threadIdx.x / kRecParts, part = threadIdx.x % kRecParts;
     const int W = L.window;
+    const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
 
@@ -81,7 +83,8 @@ gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restr
             float x = (x0 + x1) + (x2 + x3);
             x += __shfl_xor_sync(0xffffffffu, x, 1);
             x += __shfl_xor_sync(0xffffffffu, x, 2);  // (k^T S)[col]
-            const float u = b * (vs[r][col] - alpha * x);
+            // delta rule: u = beta (v - alpha k^T S); GLA (no erase): u = v
+            const float u = gla ? vs[r][col] : b * (vs[r][col] - alpha * x);
             float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
             for (int i = 0; i < Q / 4; ++i) {

@@ -23,7 +23,7 @@ int check_params(const hla_params* prm) {
     if (prm->head_dim != 64 && prm->head_dim != 128) return HLA_ERR_UNSUPPORTED;
     if (prm->dtype != HLA_DTYPE_F32 && prm->dtype != HLA_DTYPE_BF16) return HLA_ERR_UNSUPPORTED;
     const unsigned known = HLA_FLAG_L2NORM_Q | HLA_FLAG_SOFTMAX_OFF | HLA_FLAG_LINEAR_OFF |
-                           HLA_FLAG_GDN_RECURRENT;
+                           HLA_FLAG_GDN_RECURRENT | HLA_FLAG_GLA | HLA_FLAG_TEST_STALL;
     if (prm->flags & ~known) return HLA_ERR_INVALID_ARG;
     return HLA_OK;
 }
@@ -135,7 +135,7 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     float* S_out = st ? st->S : nullptr;
     bool chunked = false;
     if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
-    PrefillTables tabs = {cu, err, nullptr, 0, nullptr, 0, nullptr, 0};
+    PrefillTables tabs = {cu, err, nullptr, 0, nullptr, 0, nullptr, 0, st ? st->pos : nullptr, st ? st->err : nullptr};
     if (chunked) {
         tabs.counters = reinterpret_cast<int32_t*>(ws + w.counters);
         tabs.n_counters = kGdnParts;
@@ -337,6 +337,7 @@ HLA_API int hla_decode_step(const hla_params* prm, int n_seqs, const void* q, co
     int rc = check_params(prm);
     if (rc) return rc;
     if (n_seqs < 0) return HLA_ERR_INVALID_ARG;
+    if (prm->n_q_heads / prm->n_kv_heads > kMaxDecodeGroup) return HLA_ERR_UNSUPPORTED;
     const void* ptrs[] = {q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv, out};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return HLA_ERR_INVALID_ARG;

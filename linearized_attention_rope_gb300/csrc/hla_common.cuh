@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/hla.h"
 
 namespace hla {
@@ -117,6 +119,46 @@ __device__ __forceinline__ void rope_cs_exact(int64_t p, double theta, float* c,
     sincosf((float)a, s, c);
 }
 
+// ---- per-device set-up ------------------------------------------------------
+
+constexpr int kMaxDevices = 64;
+
+// Host-side values a launcher needs once per device (a kernel attribute set,
+// an SM or occupancy count).  One instance per launcher (per kernel
+// instantiation); safe to share between threads and devices.
+struct DeviceCache {
+    std::mutex m;
+    bool ready[kMaxDevices] = {};
+    int value[kMaxDevices] = {};
+};
+
+// With the current device dev: the first call runs setup(dev, &v) under the
+// cache's lock and keeps v (a failed setup is retried by the next call);
+// every call stores the device's value in *value (may be null).
+template <class F>
+cudaError_t device_cached(DeviceCache& c, int* value, F setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(c.m);
+    if (!c.ready[dev]) {
+        int v = 0;
+        e = setup(dev, &v);
+        if (e != cudaSuccess) return e;
+        c.value[dev] = v;
+        c.ready[dev] = true;
+    }
+    if (value) *value = c.value[dev];
+    return cudaSuccess;
+}
+
+// Streaming multiprocessors of device dev.
+inline cudaError_t sm_count(int dev, int* n) {
+    cudaError_t e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+    return e == cudaSuccess && *n <= 0 ? cudaErrorInvalidValue : e;
+}
+
 // ---- kernel launchers (each returns the cudaError_t of its launch) --------
 
 // Launch configuration for cudaLaunchKernelEx; with after_prior, programmatic
@@ -145,7 +187,8 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // What the first launch of a prefill writes besides the RoPE tables (device
 // pointers; a null table is skipped): err[0..3] = 0, counters[0..n_counters)
-// = 0 (n_counters <= 32), and per-sequence work tables blk_base / chunk_base
+// = 0 (n_counters <= 32), st_err[0] = kErrState if some st_pos[n] != 0, and
+// per-sequence work tables blk_base / chunk_base
 // (n_seqs + 1 int32 each): base[s] = the items of sequences before s, where
 // a sequence of len rows has ceil(len / blk_rows) softmax row blocks and
 // ceil((len - n_sinks - W) / chunk_rows) GDN chunks (none if not positive).
@@ -158,6 +201,10 @@ struct PrefillTables {
     int blk_rows;
     int32_t* chunk_base;
     int chunk_rows;
+    // decode state to fill (may be null): a position that is not 0 marks a
+    // state that was not freshly initialised; st_err[0] = kErrState then
+    const int64_t* st_pos;
+    int32_t* st_err;
 };
 // RoPE tables: fine[b][i] = (cos, sin)(b * theta_i), b < 64;
 // coarse[a][i] = (cos, sin)(64 a * theta_i), a < n_coarse; plus the tables
@@ -247,7 +294,10 @@ cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, co
                               const float* g, const float* beta, const Tf* khat, const Tf* vhat,
                               const int32_t* cu, const hla_state& s, cudaStream_t st);
 
-// One decode step for all sequences, then pos += 1.
+// One decode step for all sequences, then pos += 1.  At most kMaxDecodeGroup
+// query heads per kv head.  A negative position is flagged in the state's
+// error word (kErrState) and that sequence is left as it is.
+constexpr int kMaxDecodeGroup = 8;
 // Bytes of the per-step decode scratch (hla_state.scratch).
 size_t decode_scratch_bytes(int n_seqs, int Hq, int D, int n_sinks, int window);
 template <typename Tin>

@@ -107,16 +107,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Waits for phase `parity` of the mbarrier; gives up and returns false after
-// `limit` polls or two seconds of wall-clock time, whichever comes first (a
-// single poll may suspend the thread for a while).  Kept out of line with a
-// rolled loop: an unrolled copy at every call site bloats the kernels well
-// past the instruction cache.
-static __device__ __noinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+// `limit` polls or `limit_ns` nanoseconds of wall-clock time (two seconds by
+// default), whichever comes first (a single poll may suspend the thread for a
+// while).  Kept out of line with a rolled loop: an unrolled copy at every
+// call site bloats the kernels well past the instruction cache.
+static __device__ __noinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit,
+                                              uint64_t limit_ns = 2000000000ull) {
     const uint64_t t0 = global_ns();
 #pragma unroll 1
     for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(mbar, parity)) return true;
-        if (global_ns() - t0 > 2000000000ull) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

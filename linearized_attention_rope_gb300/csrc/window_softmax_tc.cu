@@ -319,21 +319,17 @@ bool window_softmax_tc_supported(const LayerDims& L) {
 cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const __half* kr, const __nv_bfloat16* v,
                                      const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
                                      int32_t* err, bool after_prior, cudaStream_t st) {
-    static bool configured = false;
-    static int n_sm = 0;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(window_softmax_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static DeviceCache cache;  // the shared-memory attribute and the SM count, per device
+    int n_sm = 0;
+    cudaError_t e = device_cached(cache, &n_sm, [](int dev, int* v) {
+        cudaError_t r = cudaFuncSetAttribute(window_softmax_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
-            n_sm = 148;
-        configured = true;
-    }
+        return r == cudaSuccess ? sm_count(dev, v) : r;
+    });
+    if (e != cudaSuccess) return e;
     if (L.total <= 0) return cudaSuccess;
     const int QB = kD / L.G;
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap mq, mk, mv, mk64, mv64;
     if (!tma::make_map_3d(&mq, qr, false, kD, (uint64_t)L.Hq, (uint64_t)L.total, 64, (uint32_t)L.G, (uint32_t)QB) ||

@@ -30,6 +30,8 @@ FLAG_L2NORM_Q = 0x1
 FLAG_SOFTMAX_OFF = 0x2
 FLAG_LINEAR_OFF = 0x4
 FLAG_GDN_RECURRENT = 0x8
+FLAG_GLA = 0x10
+FLAG_TEST_STALL = 0x20
 
 STATE_FIELDS = ("S", "k_ring", "v_ring", "pend_k", "pend_v", "pend_g", "pend_beta", "conv_q",
                 "conv_k", "conv_v", "pos", "err", "scratch")
@@ -84,6 +86,8 @@ def load():
         lib.hla_prefill_launch_count.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         lib.hla_prefill_noalloc.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, S, _vp]
         lib.hla_prefill_noalloc.restype = ctypes.c_int
+        lib.hla_prefill_noalloc_check_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.hla_prefill_noalloc_check_error.restype = ctypes.c_int
         for fn in ("hla_state_bytes", "hla_prefill_workspace_bytes", "hla_state_init", "hla_prefill",
                    "hla_decode_step", "hla_check_device_error", "hla_check_workspace_error",
                    "hla_prefill_stage_events", "hla_prefill_launch_count"):
@@ -250,3 +254,13 @@ def prefill_noalloc(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlen
                                     _ptr(cu_seqlens), cu_seqlens.numel() - 1, q.shape[0], _ptr(out),
                                     None if state is None else ctypes.byref(state.c), _stream(stream))
     _check(rc, "hla_prefill_noalloc")
+
+
+def prefill_noalloc_check_error(stream=None) -> int:
+    """hla_prefill_noalloc_check_error: synchronises, reads and clears the error
+    word of the library's own prefill buffer on the current device; returns it."""
+    code = ctypes.c_int32()
+    rc = load().hla_prefill_noalloc_check_error(_stream(stream), ctypes.byref(code))
+    if rc not in (HLA_OK, HLA_ERR_STATE, HLA_ERR_TIMEOUT):
+        _check(rc, "hla_prefill_noalloc_check_error")
+    return code.value

@@ -130,3 +130,17 @@ def test_decode_rejects_bad_state_without_gpu(lib):
     assert rc == hla.HLA_ERR_INVALID_ARG
     rc = lib.hla_state_init(ctypes.byref(prm), 4, None, None)
     assert rc == hla.HLA_ERR_INVALID_ARG
+
+
+def test_decode_rejects_head_groups_over_eight_without_gpu(lib):
+    # 16 query heads per kv head: refused on the host before any pointer is looked at
+    prm = _p(n_q_heads=32, n_kv_heads=2).c()
+    fake = ctypes.c_void_p(0x1000)
+    state = hla.CState(*([0x1000] * 13))
+    rc = lib.hla_decode_step(ctypes.byref(prm), 4, *([fake] * 9), ctypes.byref(state), fake, None)
+    assert rc == hla.HLA_ERR_UNSUPPORTED
+
+
+def test_gla_and_stall_flags_are_known(lib):
+    assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_GLA), 16, 1) > 0
+    assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_TEST_STALL), 16, 1) > 0

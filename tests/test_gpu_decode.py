@@ -19,9 +19,9 @@ def built():
     build.build()
 
 
-def check_decode(wl, x, st, outs, units, oracle, steps):
+def check_decode(wl, x, st, outs, units, oracle, steps, **cfg_kw):
     jobs = [unit_job(wl, x, n, h, decode_steps=steps) for n, h in units]
-    refs = oracle.layer_units(oracle_cfg(wl, oracle), jobs)
+    refs = oracle.layer_units(oracle_cfg(wl, oracle, **cfg_kw), jobs)
     d = wl.head_dim
     for (n, h), ref in zip(units, refs):
         L = wl.seqlens[n]
@@ -120,3 +120,17 @@ def test_state_save_and_restore_resumes_exactly():
         b.copy_(saved[k].to(b.device))  # restore
     b2 = run_decode(wl, x, st, steps=8, first=4)
     assert torch.equal(a, b2)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_decode_gla_variant(oracle_mod, dtype, d):
+    # gated linear attention (no erase term): prefill on the tensor-core path (bf16 d128) or the
+    # token-serial path (fp32), then decode steps that absorb a token each
+    wl = synth.small(f"decode gla {dtype} d{d}", [10, 90, 200, 64], n_q_heads=4, n_kv_heads=2, head_dim=d,
+                     dtype=dtype, n_sinks=8, window=24, decode_steps=30)
+    x = synth.make_inputs(wl, "cuda")
+    flags = hla.FLAG_L2NORM_Q | hla.FLAG_GLA
+    _, st = run_prefill(wl, x, flags=flags, with_state=True)
+    outs = run_decode(wl, x, st, flags=flags)
+    units = [(n, h) for n in range(wl.n_seqs) for h in range(wl.n_q_heads)]
+    check_decode(wl, x, st, outs, units, oracle_mod, wl.decode_steps, erase_off=True)

@@ -82,6 +82,18 @@ def test_without_q_normalisation(oracle_mod):
     check_prefill(wl, x, out, None, all_units(wl), oracle_mod, l2norm_q=False)
 
 
+@pytest.mark.parametrize("dtype,d,seqlens", [("f32", 64, [512, 77]), ("bf16", 128, [700, 64, 333]),
+                                             ("bf16", 64, [300, 65])])
+def test_gla_variant(oracle_mod, dtype, d, seqlens):
+    # gated linear attention in place of the delta rule (no erase term, write gain 1), on the
+    # token-serial path (fp32 layer, bf16 d64) and on the tensor-core path (bf16 d128)
+    wl = synth.small(f"gla {dtype} d{d}", seqlens, n_q_heads=4, n_kv_heads=2, head_dim=d, dtype=dtype)
+    x = synth.make_inputs(wl, "cuda")
+    flags = hla.FLAG_L2NORM_Q | hla.FLAG_GLA
+    out, st = run_prefill(wl, x, flags=flags, with_state=True)
+    check_prefill(wl, x, out, st, all_units(wl), oracle_mod, flags=flags, erase_off=True)
+
+
 def test_recurrent_kernel_selected_by_flag(oracle_mod):
     wl = synth.small("recurrent flag", [333, 64], n_q_heads=4, n_kv_heads=1, head_dim=128)
     x = synth.make_inputs(wl, "cuda")

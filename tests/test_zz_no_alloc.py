@@ -73,3 +73,20 @@ def test_noalloc_refuses_prefills_beyond_the_static_scratch():
                                         ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(w.data_ptr()),
                                         ctypes.c_void_p(cu.data_ptr()), 1, total, None, None, None)
     assert rc == hla.HLA_ERR_WORKSPACE
+
+
+def test_noalloc_error_word_is_readable_and_cleared():
+    # A cu_seqlens table that ends short of the tokens passed is clamped on the device and flagged
+    # in the error word at the head of the library's buffer; the accessor reads it back (allocating
+    # nothing) and clears it, and a correct call afterwards leaves it clear.
+    wl = synth.small("bad cu noalloc", [40, 24], n_q_heads=2, n_kv_heads=1, head_dim=64)
+    x = synth.make_inputs(wl, "cuda")
+    prm = params_for(wl)
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"])
+    out = torch.zeros_like(x["q"])
+    bad = torch.tensor([0, 20, 40], dtype=torch.int32, device="cuda")
+    hla.prefill_noalloc(prm, *args, bad, out)
+    assert hla.prefill_noalloc_check_error() != 0
+    assert hla.prefill_noalloc_check_error() == 0
+    hla.prefill_noalloc(prm, *args, x["cu_seqlens"], out)
+    assert hla.prefill_noalloc_check_error() == 0
