@@ -525,10 +525,10 @@ decode_attn_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
 }
 
 // CTA per (q-head, sequence), thread per channel: splits merged by their
-// maxima (read eight at a time, so their loads overlap), o = o_sm + lambda_h
-// o_lin; then the sequence's position advances (CTA of head 0: no CTA of this
-// launch reads it).
-constexpr int kCombineBatch = 8;
+// maxima (read sixteen at a time, so their loads overlap: one batch for an
+// 896-slot ring), o = o_sm + lambda_h o_lin; then the sequence's position
+// advances (CTA of head 0: no CTA of this launch reads it).
+constexpr int kCombineBatch = 16;
 template <typename Tin, int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out,
