@@ -10,6 +10,7 @@ from .oracle import (  # noqa: F401
     build,
     conv,
     gdn_delayed,
+    key_stats,
     key_visible,
     l2norm,
     layer_unit,

@@ -254,3 +254,51 @@ ORACLE_API int oracle_layer_unit(const oracle_cfg* cfg, int len,
     free(qr); free(kr); free(tq); free(tk); free(vh); free(qh); free(kh); free(osm); free(olin);
     return 0;
 }
+
+/* Key concentration and projection residual, the quantities of the analysis
+ * in "迈向线性的关键：分析驱动的 Transformer 线性化", sections
+ * 从 softmax 到 delta 规则的一阶近似 (Lemma 2 replaces "subtract the mean
+ * key" by "project onto the orthogonal complement of the mean key", assuming
+ * normalised, concentrated keys), 填补近似缺口的实用设计 (when keys do not
+ * line up with one main direction the projection residual grows) and
+ * 实验结果分析 (Fig. 3).  For the keys kr of one sequence and head (the
+ * softmax branch's RoPE'd keys), at every position p, with u_i = kr_i/|kr_i|
+ * and the prefix mean m_p = (1/(p+1)) sum_{i<=p} u_i:
+ *   concentration[p] = |m_p|
+ *   residual[p]      = |u_p - (mhat_p . u_p) mhat_p|,  mhat_p = m_p/|m_p|
+ * (residual[p] = 1 where m_p = 0; a zero key counts as u = 0). */
+ORACLE_API void oracle_key_stats(int len, int d, const double* kr, double* concentration, double* residual)
+{
+    double* m = (double*)calloc((size_t)(d > 0 ? d : 1), sizeof(double));
+    double* u = (double*)malloc((size_t)(d > 0 ? d : 1) * sizeof(double));
+    for (int p = 0; p < len; ++p) {
+        double nk = 0.0;
+        for (int c = 0; c < d; ++c) nk += kr[(size_t)p * d + c] * kr[(size_t)p * d + c];
+        nk = sqrt(nk);
+        for (int c = 0; c < d; ++c) {
+            u[c] = nk > 0.0 ? kr[(size_t)p * d + c] / nk : 0.0;
+            m[c] += u[c];
+        }
+        double nm = 0.0, dot = 0.0;
+        for (int c = 0; c < d; ++c) {
+            double mc = m[c] / (double)(p + 1);
+            nm += mc * mc;
+            dot += mc * u[c];
+        }
+        nm = sqrt(nm);
+        concentration[p] = nm;
+        if (nm == 0.0) {
+            residual[p] = 1.0;
+        } else {
+            double proj = dot / nm, r = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double e = u[c] - proj * (m[c] / (double)(p + 1)) / nm;
+                r += e * e;
+            }
+            residual[p] = sqrt(r);
+        }
+    }
+    free(u);
+    free(m);
+}
+

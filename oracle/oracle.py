@@ -84,6 +84,7 @@ def _load():
                 + [_dp] * 9
             )
             lib.oracle_layer_unit.restype = ctypes.c_int
+            lib.oracle_key_stats.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp]
             _lib = lib
     return _lib
 
@@ -183,3 +184,14 @@ def layer_units(cfg: OracleCfg, jobs, threads: int | None = None, want=()) -> li
         return [one(j) for j in jobs]
     with ThreadPoolExecutor(max_workers=threads) as ex:
         return list(ex.map(one, jobs))
+
+
+def key_stats(kr):
+    """Key concentration |m_p| and projection residual at every position of one
+    sequence and head (rows of kr, the RoPE'd keys); returns two float64 arrays."""
+    kr = _in(kr)
+    L, d = kr.shape
+    conc = np.empty(L)
+    res = np.empty(L)
+    _load().oracle_key_stats(L, d, _p(kr), _p(conc), _p(res))
+    return conc, res
