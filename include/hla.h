@@ -234,6 +234,38 @@ HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q,
                             const float* conv_wq, const float* conv_wk, const float* conv_wv,
                             const hla_state* st, void* out, void* stream);
 
+/* Component-usage diagnostics of a prefill (synthetic analysis; not part of
+ * the layer's output path).  Arguments as for hla_prefill, without a decode
+ * state, plus:
+ *   out [total, Hq, d]      params->dtype, scratch for the branch outputs:
+ *                           afterwards it holds lambda_h o_lin (the linear
+ *                           branch alone)
+ *   branch_sq [n_seqs, Hq, 2] fp32: per sequence and q-head, the sums over
+ *                           its positions of |o_sm|^2 (index 0) and of
+ *                           |lambda_h o_lin|^2 (index 1), from the rounded
+ *                           branch outputs: how much each branch carries
+ *                           ("Untangling Component Imbalance in Hybrid Linear
+ *                           Attention Conversion", sections 摘要, 方法详解)
+ *   key_stats [total, Hkv, 2] fp32: per position p and kv head, with u_i the
+ *                           RoPE'd key i scaled to unit length and m_p the mean
+ *                           of u_0..u_p within the sequence: the key
+ *                           concentration |m_p| (index 0) and the projection
+ *                           residual |u_p - (mhat_p . u_p) mhat_p| (index 1;
+ *                           1 where m_p = 0), the quantities of the analysis in
+ *                           "迈向线性的关键：分析驱动的 Transformer 线性化",
+ *                           sections 从 softmax 到 delta 规则的一阶近似 (Lemma 2)
+ *                           and 填补近似缺口的实用设计
+ *   ws, ws_bytes            as for hla_prefill
+ * Runs the prefill twice (each branch alone; HLA_FLAG_SOFTMAX_OFF and
+ * HLA_FLAG_LINEAR_OFF in params are overridden) and three reduction kernels.
+ * Asynchronous; no allocation. */
+HLA_API int hla_prefill_diagnostics(const hla_params* params, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* lambda,
+                                    const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                                    const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                                    float* branch_sq, float* key_stats, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Synchronises `stream`, reads the state's device error word into *code
  * (may be NULL), clears it, and returns HLA_OK if it was zero, else the
  * matching HLA_ERR_* status. */

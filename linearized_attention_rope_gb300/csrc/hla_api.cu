@@ -378,6 +378,41 @@ HLA_API int hla_prefill_launch_count(const hla_params* prm, int with_state, int*
     return HLA_OK;
 }
 
+HLA_API int hla_prefill_diagnostics(const hla_params* prm, const void* q, const void* k, const void* v,
+                                    const float* g, const float* beta, const float* lambda,
+                                    const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                                    const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                                    float* branch_sq, float* key_stats, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (!branch_sq || !key_stats || !aligned16(branch_sq) || !aligned16(key_stats)) return HLA_ERR_INVALID_ARG;
+    // the two branches alone, each through the whole prefill path (argument checks included)
+    hla_params run = *prm;
+    run.flags = (prm->flags & ~(unsigned)HLA_FLAG_SOFTMAX_OFF) | HLA_FLAG_LINEAR_OFF;
+    rc = hla_prefill(&run, q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, n_seqs, total_tokens,
+                     out, nullptr, ws, ws_bytes, stream);
+    if (rc) return rc;
+    const LayerDims L = make_dims(prm, n_seqs, total_tokens);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool f32 = prm->dtype == HLA_DTYPE_F32;
+    if (total_tokens == 0)  // no rows: every sum is zero
+        return cuda_status(cudaMemsetAsync(branch_sq, 0, (size_t)n_seqs * prm->n_q_heads * 2 * sizeof(float), s));
+    HLA_TRY(f32 ? launch_branch_sq(L, static_cast<const float*>(out), cu_seqlens, branch_sq, 0, s)
+                : launch_branch_sq(L, static_cast<const __nv_bfloat16*>(out), cu_seqlens, branch_sq, 0, s));
+    run.flags = (prm->flags & ~(unsigned)HLA_FLAG_LINEAR_OFF) | HLA_FLAG_SOFTMAX_OFF;
+    rc = hla_prefill(&run, q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, n_seqs, total_tokens,
+                     out, nullptr, ws, ws_bytes, stream);
+    if (rc) return rc;
+    HLA_TRY(f32 ? launch_branch_sq(L, static_cast<const float*>(out), cu_seqlens, branch_sq, 1, s)
+                : launch_branch_sq(L, static_cast<const __nv_bfloat16*>(out), cu_seqlens, branch_sq, 1, s));
+    // the RoPE'd keys the feature path left in the workspace
+    const WsLayout w = ws_layout(prm, total_tokens, n_seqs);
+    const char* wsb = static_cast<const char*>(ws);
+    HLA_TRY(f32 ? launch_key_stats(L, reinterpret_cast<const float*>(wsb + w.kr), cu_seqlens, key_stats, s)
+                : launch_key_stats(L, reinterpret_cast<const __half*>(wsb + w.kr), cu_seqlens, key_stats, s));
+    return HLA_OK;
+}
+
 HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code) {
     if (!ws || !aligned16(ws)) return HLA_ERR_INVALID_ARG;
     return read_error_word(static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream), code);

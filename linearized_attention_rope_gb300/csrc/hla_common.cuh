@@ -288,6 +288,14 @@ cudaError_t launch_window_softmax_tc(const LayerDims& L, const __half* qr, const
                                      const int32_t* cu, int32_t* blk_base, __half* o_sm, __nv_bfloat16* out,
                                      int32_t* err, bool after_prior, cudaStream_t st);
 
+// Diagnostics: sq[(n Hq + h) 2 + which] = sum over the rows of sequence n of |out[p][h]|^2; and per
+// position p and kv head the key concentration and projection residual of the RoPE'd keys kr
+// (stats[(p Hkv + kv) 2 + {0, 1}]).
+template <typename T>
+cudaError_t launch_branch_sq(const LayerDims& L, const T* out, const int32_t* cu, float* sq, int which, cudaStream_t st);
+template <typename Tf>
+cudaError_t launch_key_stats(const LayerDims& L, const Tf* kr, const int32_t* cu, float* stats, cudaStream_t st);
+
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>
 cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,

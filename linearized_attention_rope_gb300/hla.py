@@ -86,6 +86,9 @@ def load():
         lib.hla_prefill_launch_count.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         lib.hla_prefill_noalloc.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, S, _vp]
         lib.hla_prefill_noalloc.restype = ctypes.c_int
+        lib.hla_prefill_diagnostics.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, _vp, _vp,
+                                                                   _vp, ctypes.c_size_t, _vp]
+        lib.hla_prefill_diagnostics.restype = ctypes.c_int
         lib.hla_prefill_noalloc_check_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_prefill_noalloc_check_error.restype = ctypes.c_int
         for fn in ("hla_state_bytes", "hla_prefill_workspace_bytes", "hla_state_init", "hla_prefill",
@@ -200,6 +203,27 @@ def prefill(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out, 
                             ws.numel(), _stream(stream))
     _check(rc, "hla_prefill")
     return ws
+
+
+def prefill_diagnostics(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out=None, ws=None,
+                        stream=None):
+    """hla_prefill_diagnostics: returns (branch_sq [n_seqs, Hq, 2], key_stats [total, Hkv, 2]), fp32
+    tensors on the GPU (|o_sm|^2 and |lambda o_lin|^2 summed per sequence and head; key concentration
+    and projection residual per position and kv head)."""
+    n_seqs = cu_seqlens.numel() - 1
+    total = q.shape[0]
+    if ws is None:
+        ws = alloc_workspace(params, total, n_seqs, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    branch_sq = torch.empty((n_seqs, params.n_q_heads, 2), dtype=torch.float32, device=q.device)
+    key_stats = torch.empty((total, params.n_kv_heads, 2), dtype=torch.float32, device=q.device)
+    rc = load().hla_prefill_diagnostics(ctypes.byref(params.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        _ptr(lam), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(cu_seqlens), n_seqs, total,
+                                        _ptr(out), _ptr(branch_sq), _ptr(key_stats), _ptr(ws), ws.numel(),
+                                        _stream(stream))
+    _check(rc, "hla_prefill_diagnostics")
+    return branch_sq, key_stats
 
 
 def decode_step(params: Params, q, k, v, g, beta, lam, wq, wk, wv, state: State, out, stream=None):
