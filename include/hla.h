@@ -234,6 +234,26 @@ HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q,
                             const float* conv_wq, const float* conv_wk, const float* conv_wv,
                             const hla_state* st, void* out, void* stream);
 
+/* Prefill that continues from a decode state: appends the tokens of each
+ * sequence to the context st already holds (after hla_prefill with a state,
+ * hla_decode_step, or an earlier call of this one), the first at position
+ * st->pos[n].  Arguments as for hla_prefill, except that st is required and
+ * is read and advanced: the conv histories, the window keys and values, the
+ * tokens still waiting to be absorbed and S carry across the boundary, and
+ * pos[n] grows by the sequence's token count.  The outputs and the state
+ * afterwards are those of one prefill over the whole sequence (equivalently,
+ * of decoding the new tokens one at a time).  A state that never passed
+ * through hla_state_init starts from whatever its buffers hold; pos < 0 is
+ * flagged in the state's error word (HLA_ERR_STATE) and that sequence is left
+ * as it is.  Token-serial inside each sequence (one CTA per query head), a
+ * path for prompts appended to live sequences, not the throughput path of a
+ * fresh prefill.  ws as for hla_prefill.  Asynchronous; no allocation. */
+HLA_API int hla_prefill_continue(const hla_params* params, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const float* lambda,
+                                 const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                                 const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                                 const hla_state* st, void* ws, size_t ws_bytes, void* stream);
+
 /* Component-usage diagnostics of a prefill (synthetic analysis; not part of
  * the layer's output path).  Arguments as for hla_prefill, without a decode
  * state, plus:

@@ -378,6 +378,40 @@ HLA_API int hla_prefill_launch_count(const hla_params* prm, int with_state, int*
     return HLA_OK;
 }
 
+HLA_API int hla_prefill_continue(const hla_params* prm, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const float* lambda,
+                                 const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                                 const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
+                                 const hla_state* st, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (n_seqs < 1 || total_tokens < 0 || total_tokens > (int64_t)INT32_MAX) return HLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {cu_seqlens, ws, lambda, conv_wq, conv_wk, conv_wv, q, k, v, g, beta, out};
+    const int n_required = total_tokens > 0 ? 12 : 2;
+    for (int i = 0; i < 12; ++i) {
+        if (!ptrs[i] && i >= n_required) continue;
+        if (!ptrs[i] || !aligned16(ptrs[i])) return HLA_ERR_INVALID_ARG;
+    }
+    if (!state_ok(st)) return HLA_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(prm, total_tokens, n_seqs);
+    if (ws_bytes < w.total) return HLA_ERR_WORKSPACE;
+    if (total_tokens == 0) return HLA_OK;  // nothing appended; the state is unchanged
+    const LayerDims L = make_dims(prm, n_seqs, total_tokens);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* wsb = static_cast<char*>(ws);
+    if (prm->dtype == HLA_DTYPE_F32)
+        return cuda_status(launch_prefill_continue<float, float>(
+            L, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), g, beta,
+            lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, *st, reinterpret_cast<float*>(wsb + w.kr),
+            reinterpret_cast<float*>(wsb + w.khat), reinterpret_cast<float*>(wsb + w.vhat), static_cast<float*>(out),
+            s));
+    return cuda_status(launch_prefill_continue<__nv_bfloat16, __half>(
+        L, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, *st,
+        reinterpret_cast<__half*>(wsb + w.kr), reinterpret_cast<__half*>(wsb + w.khat),
+        reinterpret_cast<__half*>(wsb + w.vhat), static_cast<__nv_bfloat16*>(out), s));
+}
+
 HLA_API int hla_prefill_diagnostics(const hla_params* prm, const void* q, const void* k, const void* v,
                                     const float* g, const float* beta, const float* lambda,
                                     const float* conv_wq, const float* conv_wk, const float* conv_wv,

@@ -296,6 +296,14 @@ cudaError_t launch_branch_sq(const LayerDims& L, const T* out, const int32_t* cu
 template <typename Tf>
 cudaError_t launch_key_stats(const LayerDims& L, const Tf* kr, const int32_t* cu, float* stats, cudaStream_t st);
 
+// Prefill that continues every sequence from its decode state (positions from pos[n]); kr, khat,
+// vhat: [total, Hkv, d] scratch in the feature type.  Four launches on st; pos advances last.
+template <typename Tin, typename Tf>
+cudaError_t launch_prefill_continue(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v, const float* g,
+                                    const float* beta, const float* lambda, const float* wq, const float* wk,
+                                    const float* wv, const int32_t* cu, const hla_state& s, Tf* kr, Tf* khat,
+                                    Tf* vhat, Tin* out, cudaStream_t st);
+
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>
 cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,
