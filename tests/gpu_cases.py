@@ -95,3 +95,10 @@ def assert_close(got, ref, dtype: str, what: str):
 def unit_rows(x, n):
     cu = x["cu_seqlens"].tolist()
     return cu[n], cu[n + 1]
+
+
+def strided_units(n_seqs: int, n_heads: int, count: int, offset: int = 0):
+    """`count` (sequence, q-head) units spread over every sequence and over the heads: unit i takes
+    sequence i mod n_seqs and head (offset + 7 i) mod n_heads (7 is coprime with the head counts
+    used, so the heads of a sequence differ)."""
+    return [(i % n_seqs, (offset + 7 * i) % n_heads) for i in range(count)]
