@@ -53,6 +53,8 @@ def parse():
                     help="write the counters of an ncu report into profiles/traffic.json under --traffic-key "
                          "and exit; runs here, without a GPU")
     ap.add_argument("--traffic-key", default="c1", help="workload key of the report given to --traffic-from")
+    ap.add_argument("--traffic-calls", type=int, default=1,
+                    help="calls (prefill calls or decode steps) each report given to --traffic-from covers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=4000,
                     help="timed decode steps (step s feeds the inputs of synthetic step s mod 512)")
@@ -639,18 +641,27 @@ TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
 }
 
 
-def write_traffic(rep: str, key: str, calls: int = 1):
-    """Stores the counters of an ncu report (`ncu -i rep --page raw --csv`) in profiles/traffic.json under
-    workload `key`; the report holds the launches of `calls` calls (prefill calls or decode steps)."""
-    raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
-                         text=True).stdout
+def write_traffic(reps: str, key: str, calls: int = 1):
+    """Stores the counters of ncu reports (comma-separated paths of reports, or of their
+    `ncu -i rep --page raw --csv` exports ending in .csv) in
+    profiles/traffic.json under workload `key`; each report holds the launches of `calls` calls (prefill
+    calls or decode steps) of the kernels it captured.  A kernel in several reports keeps the last."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     data = {}
     if os.path.exists(path):
         with open(path) as f:
             data = json.load(f)
-    data[key] = traffic_from_csv(raw, calls)
-    data[key]["_report"] = os.path.basename(rep)
+    entry = {}
+    for rep in reps.split(","):
+        if rep.endswith(".csv"):  # an export of `ncu -i <report> --page raw --csv`
+            with open(rep) as f:
+                raw = f.read()
+        else:
+            raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
+                                 text=True).stdout
+        entry.update(traffic_from_csv(raw, calls))
+    data[key] = entry
+    data[key]["_reports"] = [os.path.basename(r) for r in reps.split(",")]
     with open(path, "w") as f:
         json.dump(data, f, indent=1)
         f.write("\n")
@@ -705,7 +716,7 @@ def prefill_line(pre: dict, key: str, dist, with_cpu: bool) -> dict:
 def main():
     args = parse()
     if args.traffic_from:
-        write_traffic(args.traffic_from, args.traffic_key)
+        write_traffic(args.traffic_from, args.traffic_key, args.traffic_calls)
         return
     dist = Dist()
     if args.impl == "reference":
