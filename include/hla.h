@@ -286,6 +286,52 @@ HLA_API int hla_prefill_diagnostics(const hla_params* params, const void* q, con
                                     float* branch_sq, float* key_stats, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Workspace bytes hla_backward needs for total_tokens tokens in n_seqs
+ * sequences (host only).  It holds the recomputed features, the per-head
+ * gradients before the kv-group sums, the softmax row statistics, the GDN
+ * state every 64 absorptions of every sequence and q-head, and one segment of
+ * 65 states per sequence and q-head for the reverse pass: about
+ * total * Hq * d * 4 * 13 + (total / 64 + 2 n_seqs) * Hq * d * d * 4 * 66 / 65
+ * bytes (fp32). */
+HLA_API int hla_backward_workspace_bytes(const hla_params* params, int64_t total_tokens, int n_seqs,
+                                         size_t* bytes);
+
+/* Backward of the layer: the gradients of sum(dout . o) with respect to every
+ * input of hla_prefill, for the training of the layer's new parameters (the
+ * gates, beta, lambda and the conv filters) on a frozen backbone ("迈向线性的
+ * 关键：分析驱动的 Transformer 线性化", section 实践建议).  Arguments q .. n_seqs,
+ * total_tokens as for hla_prefill, plus:
+ *   dout [total, Hq, d]        params->dtype, the gradient of the output
+ *   dq [total, Hq, d], dk, dv [total, Hkv, d]   fp32 (a kv head's gradient
+ *                              sums over the q-heads that read it)
+ *   dg, dbeta [total, Hq]      fp32 (zero for tokens no state absorbs: the
+ *                              sinks and the last `window` positions)
+ *   dlambda [Hq]               fp32
+ *   dconv_wq [Hq*d, 8], dconv_wk, dconv_wv [Hkv*d, 8]   fp32
+ *   ws, ws_bytes               workspace of at least
+ *                              hla_backward_workspace_bytes bytes
+ * Every output is overwritten.  The forward is recomputed inside (the
+ * features, the softmax row statistics, the GDN states), in fp32 from the
+ * stored inputs, whatever the forward path (the tensor-core prefill's bf16 and
+ * fp16 operands are not reproduced).  GDN: a forward pass stores the state
+ * every 64 absorptions; the reverse pass recomputes each segment from its
+ * checkpoint and runs the absorption and read-out steps backwards, token-serial
+ * per sequence and q-head.  HLA_FLAG_GLA differentiates the GLA update;
+ * HLA_FLAG_SOFTMAX_OFF / HLA_FLAG_LINEAR_OFF the layer without that branch;
+ * HLA_FLAG_GDN_RECURRENT has no effect; HLA_FLAG_TEST_STALL is rejected
+ * (HLA_ERR_INVALID_ARG).  Deterministic (fixed reduction order, no atomics).
+ * Malformed cu_seqlens are clamped on the device and flagged in the
+ * workspace's error word (hla_check_workspace_error).  With total_tokens == 0
+ * the per-token pointers may be NULL and the parameter gradients are zeroed.
+ * Asynchronous; no allocation. */
+HLA_API int hla_backward(const hla_params* params, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, const float* lambda,
+                         const float* conv_wq, const float* conv_wk, const float* conv_wv,
+                         const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, const void* dout,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlambda,
+                         float* dconv_wq, float* dconv_wk, float* dconv_wv, void* ws, size_t ws_bytes,
+                         void* stream);
+
 /* Synchronises `stream`, reads the state's device error word into *code
  * (may be NULL), clears it, and returns HLA_OK if it was zero, else the
  * matching HLA_ERR_* status. */

@@ -447,6 +447,57 @@ HLA_API int hla_prefill_diagnostics(const hla_params* prm, const void* q, const 
     return HLA_OK;
 }
 
+HLA_API int hla_backward_workspace_bytes(const hla_params* prm, int64_t total_tokens, int n_seqs, size_t* bytes) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (total_tokens < 0 || total_tokens > (int64_t)INT32_MAX || n_seqs < 0 || !bytes) return HLA_ERR_INVALID_ARG;
+    *bytes = bwd_layout(make_dims(prm, n_seqs, total_tokens)).total;
+    return HLA_OK;
+}
+
+HLA_API int hla_backward(const hla_params* prm, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* lambda, const float* conv_wq, const float* conv_wk,
+                         const float* conv_wv, const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens,
+                         const void* dout, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dlambda,
+                         float* dconv_wq, float* dconv_wk, float* dconv_wv, void* ws, size_t ws_bytes,
+                         void* stream) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (prm->flags & HLA_FLAG_TEST_STALL) return HLA_ERR_INVALID_ARG;
+    if (n_seqs < 1 || total_tokens < 0 || total_tokens > (int64_t)INT32_MAX) return HLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {cu_seqlens, ws, lambda, conv_wq, conv_wk, conv_wv, dlambda, dconv_wq, dconv_wk, dconv_wv,
+                          q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta};
+    const int n_ptrs = (int)(sizeof(ptrs) / sizeof(ptrs[0])), n_required = total_tokens > 0 ? n_ptrs : 10;
+    for (int i = 0; i < n_ptrs; ++i) {
+        if (!ptrs[i] && i >= n_required) continue;
+        if (!ptrs[i] || !aligned16(ptrs[i])) return HLA_ERR_INVALID_ARG;
+    }
+    const LayerDims L = make_dims(prm, n_seqs, total_tokens);
+    const BwdLayout b = bwd_layout(L);
+    if (ws_bytes < b.total) return HLA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* wsb = static_cast<char*>(ws);
+    if (total_tokens == 0) {  // no tokens: the output, and every gradient, is empty or zero
+        const size_t Hq = (size_t)prm->n_q_heads, Hkv = (size_t)prm->n_kv_heads, d = (size_t)prm->head_dim;
+        HLA_TRY(cudaMemsetAsync(wsb + b.err, 0, 16, s));
+        HLA_TRY(cudaMemsetAsync(dlambda, 0, Hq * sizeof(float), s));
+        HLA_TRY(cudaMemsetAsync(dconv_wq, 0, Hq * d * kConvWidth * sizeof(float), s));
+        HLA_TRY(cudaMemsetAsync(dconv_wk, 0, Hkv * d * kConvWidth * sizeof(float), s));
+        HLA_TRY(cudaMemsetAsync(dconv_wv, 0, Hkv * d * kConvWidth * sizeof(float), s));
+        return HLA_OK;
+    }
+    if (prm->dtype == HLA_DTYPE_F32)
+        return cuda_status(launch_backward<float>(
+            L, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), g, beta,
+            lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, static_cast<const float*>(dout), dq, dk, dv, dg, dbeta,
+            dlambda, dconv_wq, dconv_wk, dconv_wv, wsb, b, s));
+    return cuda_status(launch_backward<__nv_bfloat16>(
+        L, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens,
+        static_cast<const __nv_bfloat16*>(dout), dq, dk, dv, dg, dbeta, dlambda, dconv_wq, dconv_wk, dconv_wv, wsb, b,
+        s));
+}
+
 HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code) {
     if (!ws || !aligned16(ws)) return HLA_ERR_INVALID_ARG;
     return read_error_word(static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream), code);

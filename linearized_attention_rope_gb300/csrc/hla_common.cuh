@@ -304,6 +304,22 @@ cudaError_t launch_prefill_continue(const LayerDims& L, const Tin* q, const Tin*
                                     const float* wv, const int32_t* cu, const hla_state& s, Tf* kr, Tf* khat,
                                     Tf* vhat, Tin* out, cudaStream_t st);
 
+// Backward of the layer (fp32): workspace layout (byte offsets) and launches.  Gradients of
+// sum(dout . o): dq [total, Hq, d], dk, dv [total, Hkv, d], dg, dbeta [total, Hq], dlam [Hq],
+// dwq [Hq, d, 8], dwk, dwv [Hkv, d, 8], all fp32.
+struct BwdLayout {
+    size_t err, qr, kr, qt, qh, kt, kh, vh, dqh, dkh_h, dvh_h, dqr_sm, dkr_h, dv_h, dqt, dkt, dvt, stats, ckpt,
+        scratch, dlam_part, convw_part, total;
+    int n_blocks;
+};
+BwdLayout bwd_layout(const LayerDims& L);
+template <typename Tin>
+cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v, const float* g,
+                            const float* beta, const float* lambda, const float* wq, const float* wk, const float* wv,
+                            const int32_t* cu, const Tin* dout, float* dq, float* dk, float* dv, float* dg,
+                            float* dbeta, float* dlam, float* dwq, float* dwk, float* dwv, char* ws,
+                            const BwdLayout& b, cudaStream_t st);
+
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>
 cudaError_t launch_state_fill(const LayerDims& L, const Tin* q, const Tin* k, const Tin* v,

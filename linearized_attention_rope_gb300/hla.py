@@ -92,6 +92,12 @@ def load():
         lib.hla_prefill_diagnostics.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, _vp, _vp,
                                                                    _vp, ctypes.c_size_t, _vp]
         lib.hla_prefill_diagnostics.restype = ctypes.c_int
+        lib.hla_backward_workspace_bytes.argtypes = [P, ctypes.c_int64, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+        lib.hla_backward_workspace_bytes.restype = ctypes.c_int
+        lib.hla_backward.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64] + [_vp] * 10 + [
+            _vp, ctypes.c_size_t, _vp]
+        lib.hla_backward.restype = ctypes.c_int
         lib.hla_prefill_noalloc_check_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32)]
         lib.hla_prefill_noalloc_check_error.restype = ctypes.c_int
         for fn in ("hla_state_bytes", "hla_prefill_workspace_bytes", "hla_state_init", "hla_prefill",
@@ -241,6 +247,36 @@ def prefill_diagnostics(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_se
                                         _stream(stream))
     _check(rc, "hla_prefill_diagnostics")
     return branch_sq, key_stats
+
+
+def backward_workspace_bytes(params: Params, total_tokens: int, n_seqs: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().hla_backward_workspace_bytes(ctypes.byref(params.c()), total_tokens, n_seqs, ctypes.byref(n)),
+           "hla_backward_workspace_bytes")
+    return n.value
+
+
+BACKWARD_GRADS = ("q", "k", "v", "g", "beta", "lam", "wq", "wk", "wv")
+
+
+def backward(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, dout, grads=None, ws=None,
+             stream=None):
+    """hla_backward: the gradients of sum(dout * o) as a dict of fp32 GPU tensors named as in
+    BACKWARD_GRADS, shaped like the inputs (q [total, Hq, d]; k, v [total, Hkv, d]; g, beta
+    [total, Hq]; lam [Hq]; wq [Hq * d, 8]; wk, wv [Hkv * d, 8]).  `grads` (same dict) and `ws`
+    (a uint8 tensor of backward_workspace_bytes) may be passed in to be reused."""
+    n_seqs = cu_seqlens.numel() - 1
+    total = q.shape[0]
+    if ws is None:
+        ws = torch.empty(backward_workspace_bytes(params, total, n_seqs), dtype=torch.uint8, device=q.device)
+    if grads is None:
+        src = dict(zip(BACKWARD_GRADS, (q, k, v, g, beta, lam, wq, wk, wv)))
+        grads = {n: torch.empty(t.shape, dtype=torch.float32, device=q.device) for n, t in src.items()}
+    rc = load().hla_backward(ctypes.byref(params.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam),
+                             _ptr(wq), _ptr(wk), _ptr(wv), _ptr(cu_seqlens), n_seqs, total, _ptr(dout),
+                             *[_ptr(grads[n]) for n in BACKWARD_GRADS], _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "hla_backward")
+    return grads
 
 
 def decode_step(params: Params, q, k, v, g, beta, lam, wq, wk, wv, state: State, out, stream=None):

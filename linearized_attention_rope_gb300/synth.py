@@ -133,6 +133,12 @@ def make_inputs(wl: Workload, device="cpu") -> dict:
     return out
 
 
+def cotangent(wl: Workload, device="cpu", seed_offset: int = 0) -> torch.Tensor:
+    """dO [T, Hq, d] ~ N(0, 1) in the storage dtype: the output gradient a backward pass receives."""
+    T, Hq, d = wl.total_tokens, wl.n_q_heads, wl.head_dim
+    return _randn((T, Hq, d), device, wl.seed * 64 + 40 + seed_offset).to(wl.torch_dtype)
+
+
 def small(name: str, seqlens, n_q_heads=4, n_kv_heads=2, head_dim=64, dtype="bf16", n_sinks=8,
           window=56, decode_steps=0, seed=BASE_SEED + 100, sigma=0.3, lam="uniform") -> Workload:
     """A reduced workload with the same value recipe (for parity and edge cases)."""

@@ -37,6 +37,29 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def declared_arities():
+    """{entry point: number of parameters} from the declarations in include/hla.h."""
+    text = open(os.path.join(ROOT, "include", "hla.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for name, args in re.findall(r"HLA_API\s+[\w\s\*]+?\b(hla_\w+)\s*\(([^)]*)\)", text):
+        args = args.strip()
+        out[name] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header(lib):
+    # every entry point the binding declares argtypes for passes exactly the header's parameters
+    ar = declared_arities()
+    checked = 0
+    for name, n in ar.items():
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is not None:
+            assert len(argtypes) == n, f"{name}: binding passes {len(argtypes)}, header declares {n}"
+            checked += 1
+    assert checked == len(ar)
+
+
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(hla.CParams) == 9 * 4
     assert ctypes.sizeof(hla.CState) == 13 * 8
