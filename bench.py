@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--extra-seconds", type=float, default=0.5,
                     help="approximate timed region of each further workload (steps derived from a trial)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--backward", default="c1", choices=["", "c1", "c2", "c4"],
+                    help="workload of the backward (hla_backward) measurement; empty to skip")
+    ap.add_argument("--backward-seconds", type=float, default=2.0,
+                    help="about how long the backward's timed region runs")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode measurement (one JSON line with its results)")
     ap.add_argument("--traffic-from", metavar="NCU_REP", default=None,
@@ -405,6 +409,135 @@ def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_step
     return res
 
 
+BWD_SOURCES = [CSRC + "backward.cu", CSRC + "hla_common.cuh"]
+# hla_backward's launches, in order (stage marks 1 .. 8 follow them)
+BWD_STAGES = ("rope", "conv", "gdn", "softmax", "l2", "feat_out", "conv_filters", "lambda")
+
+
+def backward_work(wl) -> dict:
+    """Algorithmic fp32 flops of the backward's two compute stages.  GDN, per absorbed token and
+    q-head (every such token is also a read-out position): the forward's absorption (k^T S and the
+    rank-1 update, 4 d^2) and read-out (2 d^2, for lambda's gradient), the read-out backward (S dO and
+    q dO^T, 4 d^2) and the absorption backward (k^T S again, k^T dS, <dS, S_prev>, dS u, S_prev du and
+    the dS update, 12 d^2): 22 d^2; the checkpoint recompute is overhead, not counted.  Softmax, per
+    visible (query, key) pair and q-head: the logit, dP = dO . v, and the three products into dq, dk,
+    dv, 2 d each: 10 d."""
+    d, Hq = wl.head_dim, wl.n_q_heads
+    absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens) * Hq
+    keys = sum(visible_keys(L, wl.n_sinks, wl.window) for L in wl.seqlens) * Hq
+    return {"gdn": {"bound": "alu", "flops": 22.0 * d * d * absorbed, "kernel": "bwd_gdn_kernel"},
+            "softmax": {"bound": "alu", "flops": 10.0 * d * keys, "kernel": "bwd_softmax_kernel"}}
+
+
+def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_steps=5, e2e_steps=5):
+    """hla_backward on workload `key`: as many timed steps as fill about trial_seconds, per-launch
+    times, the roofline of the dominant kernel, and the end-to-end number with host buffers."""
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.workloads()[key]
+    x = synth.make_inputs(wl, "cuda")
+    dout = synth.cotangent(wl, "cuda")
+    prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window,
+                     dtype=hla.DTYPE_BF16 if wl.dtype == "bf16" else hla.DTYPE_F32)
+    ws = torch.empty(hla.backward_workspace_bytes(prm, wl.total_tokens, wl.n_seqs), dtype=torch.uint8,
+                     device="cuda")
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"], x["cu_seqlens"])
+    grads = hla.backward(prm, *args, dout, ws=ws)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        hla.backward(prm, *args, dout, grads=grads, ws=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert hla.check_workspace_error(ws) == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    step()
+    b.record(stream)
+    b.synchronize()
+    steps = int(dist.max(float(max(3, int(trial_seconds / max(a.elapsed_time(b) / 1e3, 1e-6))))))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dist.local) as clocks:
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    device_s = dist.max(sum(starts[i].elapsed_time(ends[i]) for i in range(steps)) / 1e3)
+    # per-launch times from the library's stage marks (the launches run one after another anyway)
+    n_marks = len(BWD_STAGES) + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(stage_steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(stage_steps):
+        flush.zero_()
+        hla.set_prefill_stage_events(ev[i])
+        step()
+    hla.set_prefill_stage_events(None)
+    torch.cuda.synchronize()
+    stage_ms = {name: statistics.mean(row[j].elapsed_time(row[j + 1]) for row in ev)
+                for j, name in enumerate(BWD_STAGES)}
+    work = backward_work(wl)
+
+    def roof(name):
+        w = work[name]
+        achieved = w["flops"] / (stage_ms[name] / 1e3) / 1e12
+        return {"kernel": w["kernel"], "bound": "alu", "achieved": round(achieved, 4), "peak": FP32_ALU_TFLOPS,
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 5),
+                "traffic": kernel_traffic(w["kernel"], BWD_SOURCES, key), "algorithmic": w["flops"],
+                "peak_source": FP32_ALU_TFLOPS_DERIVATION}
+
+    dominant = max(work, key=lambda n: stage_ms[n])
+    # end to end: inputs and dO from pinned host memory, every gradient back to pinned host memory
+    host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+    host["dout"] = dout.cpu().pin_memory()
+    dev = dict(x, dout=dout)
+    host_g = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in grads.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_g.values())
+    e2e_ms = []
+    for i in range(1 + e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        step()
+        for n in grads:
+            host_g[n].copy_(grads[n], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 1:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_s = dist.max(sum(e2e_ms) / 1e3)
+    tokens = wl.total_tokens * dist.world
+    res = {"value": tokens * steps / device_s, "unit": "tokens/s", "steps": steps, "warmup": warmup,
+           "ms_per_step": device_s * 1e3 / steps,
+           "config": {"workload": wl.name, "key": key, "l2": "flushed between steps (512 MiB write)",
+                      "precision": "fp32 recompute and gradients from the stored bf16/fp32 inputs"},
+           "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+           "roofline": roof(dominant), "stage_roofline": {n: roof(n) for n in work},
+           "clocks": clocks.summary(), "gpu_launches": len(BWD_STAGES) * steps + steps,
+           "gpu_launches_note": "9 kernels per call (the conv-filter stage is two launches)",
+           "e2e": {"value": tokens * e2e_steps / e2e_s, "unit": "tokens/s", "steps": e2e_steps,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
+    del ws, grads, flush, host, host_g
+    return res
+
+
 def layer_work(wl) -> dict:
     """Algorithmic work of the whole layer per prefill: bytes = q and o in the layer dtype, k and v per kv
     head, g and beta fp32 (intermediates excluded); flops = the chunked GDN's useful flops per absorbed
@@ -754,6 +887,10 @@ def main():
         extras["prefill_" + key] = prefill_line(p, key, dist, with_cpu)
         del p
         torch.cuda.empty_cache()
+    bwd = None
+    if args.backward:
+        bwd = run_backward_bench(args.backward, dist, peaks, trial_seconds=args.backward_seconds)
+        torch.cuda.empty_cache()
     dec = None if args.no_decode else run_decode_bench(args, dist, peaks)
     torch.cuda.synchronize()
     line = {
@@ -773,6 +910,8 @@ def main():
     if "cpu_baseline" in head:
         line["cpu_baseline"] = head["cpu_baseline"]
     line.update(extras)
+    if bwd:
+        line["backward_" + args.backward] = bwd
     if dec:
         line["decode"] = dec
     if dist.rank == 0:

@@ -490,12 +490,12 @@ HLA_API int hla_backward(const hla_params* prm, const void* q, const void* k, co
         return cuda_status(launch_backward<float>(
             L, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), g, beta,
             lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, static_cast<const float*>(dout), dq, dk, dv, dg, dbeta,
-            dlambda, dconv_wq, dconv_wk, dconv_wv, wsb, b, s));
+            dlambda, dconv_wq, dconv_wk, dconv_wv, wsb, b, t_stage_events, t_n_stage_events, s));
     return cuda_status(launch_backward<__nv_bfloat16>(
         L, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         static_cast<const __nv_bfloat16*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens,
         static_cast<const __nv_bfloat16*>(dout), dq, dk, dv, dg, dbeta, dlambda, dconv_wq, dconv_wk, dconv_wv, wsb, b,
-        s));
+        t_stage_events, t_n_stage_events, s));
 }
 
 HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code) {

@@ -309,8 +309,8 @@ cudaError_t launch_prefill_continue(const LayerDims& L, const Tin* q, const Tin*
 // dwq [Hq, d, 8], dwk, dwv [Hkv, d, 8], all fp32.
 struct BwdLayout {
     size_t err, qr, kr, qt, qh, kt, kh, vh, dqh, dkh_h, dvh_h, dqr_sm, dkr_h, dv_h, dqt, dkt, dvt, stats, ckpt,
-        scratch, dlam_part, convw_part, total;
-    int n_blocks;
+        sub, dlam_part, convw_part, sm_base, sink_k, sink_v, total;
+    int n_blocks, n_sm_blocks;
 };
 BwdLayout bwd_layout(const LayerDims& L);
 template <typename Tin>
@@ -318,7 +318,7 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const float* beta, const float* lambda, const float* wq, const float* wk, const float* wv,
                             const int32_t* cu, const Tin* dout, float* dq, float* dk, float* dv, float* dg,
                             float* dbeta, float* dlam, float* dwq, float* dwk, float* dwv, char* ws,
-                            const BwdLayout& b, cudaStream_t st);
+                            const BwdLayout& b, const cudaEvent_t* marks, int n_marks, cudaStream_t st);
 
 // Prefill -> decode state hand-off.
 template <typename Tin, typename Tf>
