@@ -70,6 +70,18 @@ extern "C" {
                                         delta rule: S <- alpha S + khat vhat^T
                                         (no erase term, beta unused), the other
                                         update of section 线性注意力替换机制 */
+#define HLA_FLAG_GDN_SCAN 0x40u      /* token-serial GDN path (fp32 layers, head
+                                        dim 64, or with HLA_FLAG_GDN_RECURRENT)
+                                        in its context-parallel form: each
+                                        sequence's absorptions are cut into
+                                        parts; every part's state map
+                                        S -> P S + R is formed at once, a scan
+                                        over the parts gives their start
+                                        states, then all parts run at once.
+                                        Three times the work on many more
+                                        SMs: for long sequences with few
+                                        (sequence, head) units.  No effect on
+                                        the tensor-core path. */
 #define HLA_FLAG_TEST_STALL 0x20u    /* test hook (tensor-core path): the GDN
                                         state kernel loads nothing, so its
                                         bounded waits run out after about a
@@ -287,12 +299,13 @@ HLA_API int hla_prefill_diagnostics(const hla_params* params, const void* q, con
                                     void* stream);
 
 /* Workspace bytes hla_backward needs for total_tokens tokens in n_seqs
- * sequences (host only).  It holds the recomputed features, the per-head
- * gradients before the kv-group sums, the softmax row statistics, the GDN
- * state every 64 absorptions of every sequence and q-head, and one segment of
- * 65 states per sequence and q-head for the reverse pass: about
- * total * Hq * d * 4 * 13 + (total / 64 + 2 n_seqs) * Hq * d * d * 4 * 66 / 65
- * bytes (fp32). */
+ * sequences (host only).  fp32 throughout: the recomputed features and the
+ * per-head gradients before the kv-group sums (about 10 T Hq d + 6 T Hkv d
+ * floats for T tokens), the softmax rows' max, sum and D (3 T Hq), the GDN
+ * state every 64 absorptions ((T / 64 + n_seqs + 1) Hq d^2), the states of
+ * one 64-absorption block per sequence and q-head (n_seqs Hq 8 d^2 for d 128,
+ * 4 d^2 for d 64), and the sink keys' partial sums per 64-query block
+ * (2 (T / 64 + n_seqs) Hq n_sinks d). */
 HLA_API int hla_backward_workspace_bytes(const hla_params* params, int64_t total_tokens, int n_seqs,
                                          size_t* bytes);
 
@@ -313,12 +326,15 @@ HLA_API int hla_backward_workspace_bytes(const hla_params* params, int64_t total
  * Every output is overwritten.  The forward is recomputed inside (the
  * features, the softmax row statistics, the GDN states), in fp32 from the
  * stored inputs, whatever the forward path (the tensor-core prefill's bf16 and
- * fp16 operands are not reproduced).  GDN: a forward pass stores the state
- * every 64 absorptions; the reverse pass recomputes each segment from its
- * checkpoint and runs the absorption and read-out steps backwards, token-serial
- * per sequence and q-head.  HLA_FLAG_GLA differentiates the GLA update;
+ * fp16 operands are not reproduced).  GDN: per sequence and q-head a cluster
+ * of 8 CTAs, each with d / 8 value columns of S; a forward pass stores the
+ * state every 64 absorptions, then per 64-absorption block (last first) the
+ * states every 8 (d 128) or 16 (d 64) absorptions are recomputed, and per such
+ * stage its states are held in registers while the read-out and absorption
+ * steps run backwards.  Softmax: 64 x 64 fp32 tiles, per query block then per
+ * key block.  HLA_FLAG_GLA differentiates the GLA update;
  * HLA_FLAG_SOFTMAX_OFF / HLA_FLAG_LINEAR_OFF the layer without that branch;
- * HLA_FLAG_GDN_RECURRENT has no effect; HLA_FLAG_TEST_STALL is rejected
+ * HLA_FLAG_GDN_RECURRENT and HLA_FLAG_GDN_SCAN have no effect; HLA_FLAG_TEST_STALL is rejected
  * (HLA_ERR_INVALID_ARG).  Deterministic (fixed reduction order, no atomics).
  * Malformed cu_seqlens are clamped on the device and flagged in the
  * workspace's error word (hla_check_workspace_error).  With total_tokens == 0

@@ -49,6 +49,7 @@ __global__ void prefill_tables_kernel(LayerDims L, float2* __restrict__ fine, fl
     int64_t skip = 0;
     if (threadIdx.x == 32) base = t.blk_base, per = t.blk_rows;                                 // row blocks
     if (threadIdx.x == 64) base = t.chunk_base, per = t.chunk_rows, skip = L.window + L.n_sinks;  // chunks
+    if (threadIdx.x == 128) base = t.part_base, per = t.part_rows, skip = L.window + L.n_sinks;   // parts
     if (!base) return;
     int32_t acc = 0;
     for (int q = 0; q < L.n_seqs; ++q) {
@@ -64,7 +65,7 @@ __global__ void prefill_tables_kernel(LayerDims L, float2* __restrict__ fine, fl
 cudaError_t launch_prefill_tables(const LayerDims& L, float2* fine, float2* coarse, int n_coarse,
                                   const PrefillTables& t, cudaStream_t st) {
     if (t.n_counters < 0 || t.n_counters > 32 || (t.blk_base && t.blk_rows <= 0) ||
-        (t.chunk_base && t.chunk_rows <= 0))
+        (t.chunk_base && t.chunk_rows <= 0) || (t.part_base && t.part_rows <= 0))
         return cudaErrorInvalidValue;
     int64_t n = (int64_t)(64 + n_coarse) * (L.d / 2);
     int blocks = (int)std::max<int64_t>(1, (n + 255) / 256);

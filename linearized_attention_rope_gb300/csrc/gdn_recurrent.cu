@@ -11,6 +11,18 @@
 // S (the value dim), a quarter of its key rows each, in registers; dot
 // products over the key dim finish with two shuffles.  fp32 throughout; this is
 // the fp32 layer's path and the cross-check for the chunked kernel.
+//
+// Context-parallel form (HLA_FLAG_GDN_SCAN): the absorptions of a sequence
+// are cut into parts of part_len; the state after a part is an affine map of
+// the state before it, S' = P S + R, since every update is.  Three launches:
+//   1. per part (all parts at once): R, the part run from S = 0, and P, the
+//      part run from S = I with zero values (d x d; the part's state
+//      transition);
+//   2. per (sequence, q-head, 8 value columns): the scan S_{i+1} = P_i S_i +
+//      R_i over the parts, giving every part its start state;
+//   3. per part (all at once): the part from its start state, with the
+//      read-outs; the sequence's last part writes the final state.
+// Three times the work of one pass, on parts-times as many CTAs.
 #include "hla_common.cuh"
 
 namespace hla {
@@ -25,12 +37,16 @@ template <int D> __device__ __forceinline__ int rec_pad(int c) {
     return (c / Q) * (Q + 4) + c % Q;
 }
 
+constexpr int kRecWhole = 0;  // grid (Hq, n_seqs): whole sequences from S = 0
+constexpr int kRecMap = 1;    // grid (Hq, parts, 2): a part's R (z = 0) and P (z = 1) into pr; no read-outs
+constexpr int kRecPart = 2;   // grid (Hq, parts): a part from its start state, with the read-outs
+
 template <typename Tf, int D>
 __global__ void __launch_bounds__(D * kRecParts)
 gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restrict__ khat,
                      const Tf* __restrict__ vhat, const float* __restrict__ g,
                      const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                     float* __restrict__ o_lin, float* __restrict__ S_out) {
+                     float* __restrict__ o_lin, float* __restrict__ S_out, int mode, RecScan rs) {
     constexpr int Q = D / kRecParts;           // rows of S per thread
     constexpr int ROW = kRecParts * (Q + 4);   // padded row length
     constexpr int NT = D * kRecParts;
@@ -39,27 +55,55 @@ gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restr
     __shared__ float vs[kRecTile][D];
     __shared__ float as[kRecTile], bs[kRecTile];
 
-    const int h = blockIdx.x, n = blockIdx.y, kv = h / L.G;
+    const int h = blockIdx.x, kv = h / L.G;
     const int col = threadIdx.x / kRecParts, part = threadIdx.x % kRecParts;
     const int W = L.window;
     const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
+    int n = blockIdx.y, kind = 0;
+    int64_t gp = 0, ip = 0;  // global and in-sequence part index
+    bool last = true;
+    if (mode != kRecWhole) {
+        gp = blockIdx.y;
+        if (gp >= __ldg(rs.base + L.n_seqs)) return;
+        int lo = 0, hi = L.n_seqs - 1;  // the sequence owning part gp
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(rs.base + mid) <= gp) lo = mid; else hi = mid - 1;
+        }
+        n = lo;
+        ip = gp - __ldg(rs.base + n);
+        last = ip == (int64_t)__ldg(rs.base + n + 1) - __ldg(rs.base + n) - 1;
+        kind = mode == kRecMap ? (int)blockIdx.z : 0;
+        if (mode == kRecMap && last) return;  // the scan needs no map of a sequence's last part
+    }
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
+    // absorbed tokens [j_lo, j_end) of this CTA
+    int64_t j_lo = L.n_sinks, j_end = len - W;
+    if (mode != kRecWhole) {
+        j_lo = L.n_sinks + ip * rs.part_len;
+        j_end = min(j_end, j_lo + rs.part_len);
+    }
+    const bool readout = mode != kRecMap, unit = mode == kRecMap && kind == 1;  // unit: S from I, values 0
 
     float S[Q];  // S[part*Q + i][col]
 #pragma unroll
-    for (int i = 0; i < Q; ++i) S[i] = 0.f;
+    for (int i = 0; i < Q; ++i) S[i] = unit && part * Q + i == col ? 1.f : 0.f;
+    if (mode == kRecPart && ip > 0) {
+        const float* src = rs.s_part + ((size_t)gp * L.Hq + h) * D * D;
+#pragma unroll
+        for (int i = 0; i < Q; ++i) S[i] = src[(size_t)(part * Q + i) * D + col];
+    }
 
-    const int64_t j_end = len - W;  // tokens n_sinks .. j_end-1 get absorbed
-    for (int64_t jt = L.n_sinks; jt < j_end; jt += kRecTile) {
+    for (int64_t jt = j_lo; jt < j_end; jt += kRecTile) {
         const int cnt = (int)min((int64_t)kRecTile, j_end - jt);
         __syncthreads();
         for (int idx = threadIdx.x; idx < cnt * D; idx += NT) {
             int r = idx / D, c = idx % D;
             size_t t = (size_t)(start + jt + r);
             ks[r][rec_pad<D>(c)] = to_f32(khat[(t * L.Hkv + kv) * D + c]);
-            qs[r][rec_pad<D>(c)] = to_f32(qhat[((t + W) * L.Hq + h) * D + c]);
-            vs[r][c] = to_f32(vhat[(t * L.Hkv + kv) * D + c]);
+            qs[r][rec_pad<D>(c)] = readout ? to_f32(qhat[((t + W) * L.Hq + h) * D + c]) : 0.f;
+            vs[r][c] = unit ? 0.f : to_f32(vhat[(t * L.Hkv + kv) * D + c]);
         }
         if (threadIdx.x < cnt) {
             size_t t = (size_t)(start + jt + threadIdx.x);
@@ -102,36 +146,102 @@ gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restr
             float o = (o0 + o1) + (o2 + o3);
             o += __shfl_xor_sync(0xffffffffu, o, 1);
             o += __shfl_xor_sync(0xffffffffu, o, 2);
-            if (part == 0) {
+            if (part == 0 && readout) {
                 size_t t = (size_t)(start + jt + r + W);
                 o_lin[(t * L.Hq + h) * D + col] = o;
             }
         }
     }
-    if (S_out) {
-        float* dst = S_out + ((size_t)n * L.Hq + h) * D * D;
+    float* dst = nullptr;
+    if (mode == kRecMap)
+        dst = rs.pr + (((size_t)gp * L.Hq + h) * 2 + kind) * D * D;
+    else if (last && S_out)
+        dst = S_out + ((size_t)n * L.Hq + h) * D * D;
+    if (dst) {
 #pragma unroll
         for (int i = 0; i < Q; ++i) dst[(size_t)(part * Q + i) * D + col] = S[i];
+    }
+}
+
+// The scan over a sequence's parts, for 8 value columns of one q-head: S_0 = 0, S_{i+1} = P_i S_i + R_i
+// (fp32, fixed order) into s_part for parts 1 ..; a sequence without parts gets S_out = 0 here.
+template <int D>
+__global__ void __launch_bounds__(256)
+gdn_part_scan_kernel(LayerDims L, RecScan rs, float* __restrict__ S_out) {
+    constexpr int TPR = 256 / D, CPT = 8 / TPR;  // threads per row, columns per thread
+    __shared__ __align__(16) float Ss[D][8];
+    const int h = blockIdx.x / (D / 8), cg = blockIdx.x % (D / 8), n = blockIdx.y, tid = threadIdx.x;
+    const int r = tid / TPR, c0 = (tid % TPR) * CPT;
+    const int b0 = __ldg(rs.base + n), np = __ldg(rs.base + n + 1) - b0;
+    for (int idx = tid; idx < D * 8; idx += 256) Ss[idx / 8][idx % 8] = 0.f;
+    __syncthreads();
+    if (np <= 0) {
+        if (S_out) {
+            float* dst = S_out + (((size_t)n * L.Hq + h) * D + r) * D + cg * 8 + c0;
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) dst[c] = 0.f;
+        }
+        return;
+    }
+    for (int i = 0; i + 1 < np; ++i) {
+        const float* R = rs.pr + (((size_t)(b0 + i) * L.Hq + h) * 2 + 0) * D * D;
+        const float* P = rs.pr + (((size_t)(b0 + i) * L.Hq + h) * 2 + 1) * D * D;
+        float acc[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) acc[c] = R[(size_t)r * D + cg * 8 + c0 + c];
+        const float4* Pr = reinterpret_cast<const float4*>(P + (size_t)r * D);
+#pragma unroll 4
+        for (int k4 = 0; k4 < D / 4; ++k4) {
+            const float4 p = Pr[k4];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                acc[c] = fmaf(p.x, Ss[4 * k4 + 0][c0 + c], acc[c]);
+                acc[c] = fmaf(p.y, Ss[4 * k4 + 1][c0 + c], acc[c]);
+                acc[c] = fmaf(p.z, Ss[4 * k4 + 2][c0 + c], acc[c]);
+                acc[c] = fmaf(p.w, Ss[4 * k4 + 3][c0 + c], acc[c]);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) Ss[r][c0 + c] = acc[c];
+        __syncthreads();
+        float* dst = rs.s_part + ((size_t)(b0 + i + 1) * L.Hq + h) * D * D + (size_t)r * D + cg * 8 + c0;
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) dst[c] = acc[c];
     }
 }
 
 template <typename Tf>
 cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* khat, const Tf* vhat,
                                  const float* g, const float* beta, const int32_t* cu, float* o_lin,
-                                 float* S_out, cudaStream_t st) {
-    dim3 grid(L.Hq, L.n_seqs);
-    if (L.d == 128)
-        gdn_recurrent_kernel<Tf, 128><<<grid, 128 * kRecParts, 0, st>>>(L, qhat, khat, vhat, g, beta, cu, o_lin, S_out);
+                                 float* S_out, const RecScan* rs, cudaStream_t st) {
+    const int D = L.d, nt = D * kRecParts;
+    auto run = [&](dim3 grid, int mode) {
+        const RecScan r = rs ? *rs : RecScan{};
+        if (D == 128)
+            gdn_recurrent_kernel<Tf, 128><<<grid, nt, 0, st>>>(L, qhat, khat, vhat, g, beta, cu, o_lin, S_out, mode, r);
+        else
+            gdn_recurrent_kernel<Tf, 64><<<grid, nt, 0, st>>>(L, qhat, khat, vhat, g, beta, cu, o_lin, S_out, mode, r);
+    };
+    if (!rs) {
+        run(dim3(L.Hq, L.n_seqs), kRecWhole);
+        return cudaGetLastError();
+    }
+    if (rs->part_len <= 0 || rs->n_parts <= 0 || rs->n_parts > 65535) return cudaErrorInvalidValue;
+    run(dim3(L.Hq, rs->n_parts, 2), kRecMap);
+    if (D == 128)
+        gdn_part_scan_kernel<128><<<dim3(L.Hq * 16, L.n_seqs), 256, 0, st>>>(L, *rs, S_out);
     else
-        gdn_recurrent_kernel<Tf, 64><<<grid, 64 * kRecParts, 0, st>>>(L, qhat, khat, vhat, g, beta, cu, o_lin, S_out);
+        gdn_part_scan_kernel<64><<<dim3(L.Hq * 8, L.n_seqs), 256, 0, st>>>(L, *rs, S_out);
+    run(dim3(L.Hq, rs->n_parts), kRecPart);
     return cudaGetLastError();
 }
 
 template cudaError_t launch_gdn_recurrent<float>(const LayerDims&, const float*, const float*,
                                                  const float*, const float*, const float*,
-                                                 const int32_t*, float*, float*, cudaStream_t);
+                                                 const int32_t*, float*, float*, const RecScan*, cudaStream_t);
 template cudaError_t launch_gdn_recurrent<__half>(const LayerDims&, const __half*, const __half*,
                                                   const __half*, const float*, const float*,
-                                                  const int32_t*, float*, float*, cudaStream_t);
+                                                  const int32_t*, float*, float*, const RecScan*, cudaStream_t);
 
 }  // namespace hla

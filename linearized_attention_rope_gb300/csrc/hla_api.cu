@@ -1,5 +1,6 @@
 // Host side of the libhla C ABI: argument checks, workspace layout, launch
 // order.  Declarations and contracts: include/hla.h.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <type_traits>
@@ -23,7 +24,7 @@ int check_params(const hla_params* prm) {
     if (prm->head_dim != 64 && prm->head_dim != 128) return HLA_ERR_UNSUPPORTED;
     if (prm->dtype != HLA_DTYPE_F32 && prm->dtype != HLA_DTYPE_BF16) return HLA_ERR_UNSUPPORTED;
     const unsigned known = HLA_FLAG_L2NORM_Q | HLA_FLAG_SOFTMAX_OFF | HLA_FLAG_LINEAR_OFF |
-                           HLA_FLAG_GDN_RECURRENT | HLA_FLAG_GLA | HLA_FLAG_TEST_STALL;
+                           HLA_FLAG_GDN_RECURRENT | HLA_FLAG_GLA | HLA_FLAG_TEST_STALL | HLA_FLAG_GDN_SCAN;
     if (prm->flags & ~known) return HLA_ERR_INVALID_ARG;
     return HLA_OK;
 }
@@ -51,8 +52,9 @@ size_t feat_bytes(int dtype) { return dtype == HLA_DTYPE_F32 ? 4 : 2; }
 
 // Workspace layout of one prefill.
 struct WsLayout {
-    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, osm, blk_base, chunk_base, counters, tinv, smid, total;
-    int n_coarse;
+    size_t err, fine, coarse, qr, kr, qhat, khat, vhat, olin, osm, blk_base, chunk_base, counters, tinv, smid,
+        part_base, pr, s_part, total;
+    int n_coarse, part_len, n_parts;
 };
 
 // The tensor-core path (chunked GDN + tensor-core softmax) serves bf16 layers
@@ -61,6 +63,18 @@ bool uses_chunked_gdn(const hla_params* prm) {
     const int G = prm->n_kv_heads > 0 ? prm->n_q_heads / prm->n_kv_heads : 0;
     return prm->dtype == HLA_DTYPE_BF16 && prm->head_dim == 128 && !(prm->flags & HLA_FLAG_GDN_RECURRENT) &&
            (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+// Absorptions per part of the context-parallel token-serial GDN (0: not used): enough parts for about
+// 256 (sequence, head, part) CTAs, at least 64 absorptions each, at most 65535 parts in all.
+int scan_part_len(const hla_params* prm, int64_t total, int n_seqs) {
+    if (!(prm->flags & HLA_FLAG_GDN_SCAN) || uses_chunked_gdn(prm) || n_seqs <= 0 || n_seqs >= 65535) return 0;
+    const int64_t units = (int64_t)prm->n_q_heads * n_seqs;
+    const int64_t parts = std::max<int64_t>(1, (256 + units - 1) / units);
+    const int64_t avg = std::max<int64_t>(1, total / n_seqs - prm->window - prm->n_sinks);
+    int64_t pl = std::max<int64_t>(64, ((avg + parts - 1) / parts + 63) / 64 * 64);
+    pl = std::max<int64_t>(pl, (total + (65535 - n_seqs) - 1) / (65535 - n_seqs));
+    return (int)std::min<int64_t>(pl, INT32_MAX);
 }
 
 WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
@@ -87,6 +101,13 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
     w.tinv = off;   off = align_up(off + (chunked ? gdn_chunk_slots(total, n_seqs) * Hq * kRecordBytes : 0));
     // the state between the two halves of the chunked GDN (fp32, per sequence and q-head)
     w.smid = off;   off = align_up(off + (chunked ? (size_t)n_seqs * Hq * d * d * sizeof(float) : 0));
+    // context-parallel token-serial GDN: part table, the parts' maps (R, P) and start states
+    w.part_len = scan_part_len(prm, total, n_seqs);
+    w.n_parts = w.part_len ? (int)(total / w.part_len + n_seqs) : 0;
+    const size_t np = (size_t)w.n_parts;
+    w.part_base = off; off = align_up(off + (w.part_len ? ((size_t)n_seqs + 1) * sizeof(int32_t) : 0));
+    w.pr = off;     off = align_up(off + np * Hq * 2 * d * d * sizeof(float));
+    w.s_part = off; off = align_up(off + np * Hq * d * d * sizeof(float));
     w.total = off;
     return w;
 }
@@ -136,6 +157,13 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     bool chunked = false;
     if constexpr (std::is_same<Tf, __half>::value) chunked = uses_chunked_gdn(prm);
     PrefillTables tabs = {cu, err, nullptr, 0, nullptr, 0, nullptr, 0, st ? st->pos : nullptr, st ? st->err : nullptr};
+    RecScan scan = {};
+    if (w.part_len) {
+        tabs.part_base = reinterpret_cast<int32_t*>(ws + w.part_base);
+        tabs.part_rows = w.part_len;
+        scan = RecScan{tabs.part_base, w.part_len, w.n_parts, reinterpret_cast<float*>(ws + w.pr),
+                       reinterpret_cast<float*>(ws + w.s_part)};
+    }
     if (chunked) {
         tabs.counters = reinterpret_cast<int32_t*>(ws + w.counters);
         tabs.n_counters = kGdnParts;
@@ -201,7 +229,8 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
         // features -> GDN (fp32 o_lin) -> softmax + combine
         HLA_TRY(mark_stage(2, stream));
         HLA_TRY(mark_stage(3, stream));
-        HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, stream));
+        HLA_TRY(launch_gdn_recurrent<Tf>(L, qh, kh, vh, g, beta, cu, olin, S_out, w.part_len ? &scan : nullptr,
+                                         stream));
         HLA_TRY(mark_stage(4, stream));
         HLA_TRY(launch_window_softmax<Tin, Tf>(L, qr, kr, vi, olin, lambda, cu, static_cast<Tin*>(out),
                                                stream));
@@ -374,7 +403,9 @@ HLA_API int hla_prefill_launch_count(const hla_params* prm, int with_state, int*
     if (!out) return HLA_ERR_INVALID_ARG;
     // rope tables, features; tensor-core path: softmax block table + softmax, chunk table, one
     // chunk-local and one state launch per part; token-serial path: GDN, softmax
-    *out = (uses_chunked_gdn(prm) ? 3 + 2 * kGdnParts : 4) + (with_state ? 1 : 0);
+    // (the context-parallel token-serial GDN: three launches in place of one)
+    const bool scan = (prm->flags & HLA_FLAG_GDN_SCAN) && !uses_chunked_gdn(prm);
+    *out = (uses_chunked_gdn(prm) ? 3 + 2 * kGdnParts : scan ? 6 : 4) + (with_state ? 1 : 0);
     return HLA_OK;
 }
 

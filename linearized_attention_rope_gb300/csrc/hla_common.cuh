@@ -188,10 +188,11 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // What the first launch of a prefill writes besides the RoPE tables (device
 // pointers; a null table is skipped): err[0..3] = 0, counters[0..n_counters)
 // = 0 (n_counters <= 32), st_err[0] = kErrState if some st_pos[n] != 0, and
-// per-sequence work tables blk_base / chunk_base
+// per-sequence work tables blk_base / chunk_base / part_base
 // (n_seqs + 1 int32 each): base[s] = the items of sequences before s, where
-// a sequence of len rows has ceil(len / blk_rows) softmax row blocks and
-// ceil((len - n_sinks - W) / chunk_rows) GDN chunks (none if not positive).
+// a sequence of len rows has ceil(len / blk_rows) softmax row blocks,
+// ceil((len - n_sinks - W) / chunk_rows) GDN chunks and
+// ceil((len - n_sinks - W) / part_rows) GDN parts (none if not positive).
 struct PrefillTables {
     const int32_t* cu;
     int32_t* err;
@@ -205,6 +206,8 @@ struct PrefillTables {
     // state that was not freshly initialised; st_err[0] = kErrState then
     const int64_t* st_pos;
     int32_t* st_err;
+    int32_t* part_base;  // parts of the context-parallel token-serial GDN (part_rows absorptions each)
+    int part_rows;
 };
 // RoPE tables: fine[b][i] = (cos, sin)(b * theta_i), b < 64;
 // coarse[a][i] = (cos, sin)(64 a * theta_i), a < n_coarse; plus the tables
@@ -224,12 +227,23 @@ cudaError_t launch_features(const LayerDims& L, const Tin* q, const Tin* k, cons
 
 constexpr int kMaxGdnParts = 4;  // parts of the chunk slots the chunked GDN may run in
 
+// Context-parallel form of the token-serial GDN: part table base [n_seqs + 1] (parts of part_len
+// absorptions per sequence; n_parts bounds base[n_seqs]), the parts' maps pr [n_parts][Hq][2][d][d]
+// (R, then P) and start states s_part [n_parts][Hq][d][d], fp32.
+struct RecScan {
+    const int32_t* base;
+    int part_len;
+    int n_parts;
+    float* pr;
+    float* s_part;
+};
 // Token-serial fp32 GDN with delayed absorption: o_lin [total, Hq, d] fp32
 // for positions p >= n_sinks + window; final S into S_out (may be null).
+// rs != null: the context-parallel form (three launches).
 template <typename Tf>
 cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* khat, const Tf* vhat,
                                  const float* g, const float* beta, const int32_t* cu, float* o_lin,
-                                 float* S_out, cudaStream_t st);
+                                 float* S_out, const RecScan* rs, cudaStream_t st);
 
 // Chunked (C = 64) GDN with delayed absorption on tcgen05 tensor cores,
 // head_dim 128, fp16 features: same outputs as launch_gdn_recurrent.

@@ -32,6 +32,7 @@ FLAG_LINEAR_OFF = 0x4
 FLAG_GDN_RECURRENT = 0x8
 FLAG_GLA = 0x10
 FLAG_TEST_STALL = 0x20
+FLAG_GDN_SCAN = 0x40
 
 STATE_FIELDS = ("S", "k_ring", "v_ring", "pend_k", "pend_v", "pend_g", "pend_beta", "conv_q",
                 "conv_k", "conv_v", "pos", "err", "scratch")

@@ -164,6 +164,16 @@ def test_decode_rejects_head_groups_over_eight_without_gpu(lib):
     assert rc == hla.HLA_ERR_UNSUPPORTED
 
 
+def test_scan_flag_sizes_its_buffers_on_the_token_serial_path_only(lib):
+    f32 = dict(n_q_heads=2, n_kv_heads=1, head_dim=64, dtype=hla.DTYPE_F32)
+    plain = hla.workspace_bytes(_p(**f32), 8192, 1)
+    scan = hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_GDN_SCAN, **f32), 8192, 1)
+    # 127 parts of 64 absorptions (plus the bound's slack): maps (R, P) and start states of d x d fp32
+    assert scan - plain >= 127 * 2 * 3 * 64 * 64 * 4
+    tc = hla.workspace_bytes(_p(), 4096, 1)
+    assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_GDN_SCAN), 4096, 1) == tc
+
+
 def test_gla_and_stall_flags_are_known(lib):
     assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_GLA), 16, 1) > 0
     assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_TEST_STALL), 16, 1) > 0
