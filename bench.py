@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--extra-seconds", type=float, default=0.5,
                     help="approximate timed region of each further workload (steps derived from a trial)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--scan", type=int, default=1,
+                    help="1: also time the context-parallel token-serial GDN on a long fp32 sequence")
     ap.add_argument("--backward", default="c1", choices=["", "c1", "c2", "c4"],
                     help="workload of the backward (hla_backward) measurement; empty to skip")
     ap.add_argument("--backward-seconds", type=float, default=2.0,
@@ -538,6 +540,77 @@ def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_step
     return res
 
 
+SCAN_SEQ = 32768
+
+
+def run_scan_bench(dist, trial_seconds=0.5):
+    """The context-parallel token-serial GDN (HLA_FLAG_GDN_SCAN) against the single pass, on an fp32 layer
+    of the reference config's head shape (2 q / 1 kv heads, d 64, 8 sinks + 56 window) over one long
+    sequence: prefill tokens/s both ways and the GDN launches' time (stage marks 3 -> 4)."""
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.small(f"fp32 layer, 2 q / 1 kv heads, d 64, 8 sinks + 56 window, one {SCAN_SEQ}-token sequence",
+                     [SCAN_SEQ], n_q_heads=2, n_kv_heads=1, head_dim=64, dtype="f32", seed=synth.BASE_SEED + 500)
+    x = synth.make_inputs(wl, "cuda")
+    out = torch.empty_like(x["q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens) * wl.n_q_heads
+    res = {"config": {"workload": wl.name, "l2": "flushed between steps (512 MiB write)"}}
+    for name, flags in (("single_pass", hla.FLAG_L2NORM_Q), ("scan", hla.FLAG_L2NORM_Q | hla.FLAG_GDN_SCAN)):
+        prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window, dtype=hla.DTYPE_F32,
+                         flags=flags)
+        ws = hla.alloc_workspace(prm, wl.total_tokens, wl.n_seqs)
+
+        def step():
+            hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"],
+                        x["cu_seqlens"], out, ws=ws)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        assert hla.check_workspace_error(ws) == 0
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        for e in ev:
+            e.record(stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        steps = int(dist.max(float(max(3, int(trial_seconds / max(a.elapsed_time(b) / 1e3, 1e-6))))))
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        flush.zero_()
+        hla.set_prefill_stage_events(ev)
+        step()
+        hla.set_prefill_stage_events(None)
+        torch.cuda.synchronize()
+        gdn_ms = ev[3].elapsed_time(ev[4])
+        dev_s = dist.max(sum(ms) / 1e3)
+        flops = 6.0 * wl.head_dim ** 2 * absorbed
+        res[name] = {"value": wl.total_tokens * dist.world * steps / dev_s, "unit": "tokens/s", "steps": steps,
+                     "ms_per_step": dev_s * 1e3 / steps, "gdn_ms": round(gdn_ms, 4),
+                     "gpu_launches": hla.prefill_launch_count(prm) * steps,
+                     "roofline": {"kernel": "gdn_recurrent_kernel" + (" (+ gdn_part_scan_kernel)" if name == "scan"
+                                                                      else ""),
+                                  "bound": "alu", "achieved": round(flops / (gdn_ms / 1e3) / 1e12, 4),
+                                  "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                                  "frac": round(flops / (gdn_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS, 5),
+                                  "algorithmic": flops, "peak_source": FP32_ALU_TFLOPS_DERIVATION,
+                                  "traffic": None}}
+        del ws
+    return res
+
+
 def layer_work(wl) -> dict:
     """Algorithmic work of the whole layer per prefill: bytes = q and o in the layer dtype, k and v per kv
     head, g and beta fp32 (intermediates excluded); flops = the chunked GDN's useful flops per absorbed
@@ -887,6 +960,8 @@ def main():
         extras["prefill_" + key] = prefill_line(p, key, dist, with_cpu)
         del p
         torch.cuda.empty_cache()
+    scan = run_scan_bench(dist) if args.scan else None
+    torch.cuda.empty_cache()
     bwd = None
     if args.backward:
         bwd = run_backward_bench(args.backward, dist, peaks, trial_seconds=args.backward_seconds)
@@ -912,6 +987,8 @@ def main():
     line.update(extras)
     if bwd:
         line["backward_" + args.backward] = bwd
+    if scan:
+        line["prefill_scan_fp32"] = scan
     if dec:
         line["decode"] = dec
     if dist.rank == 0:

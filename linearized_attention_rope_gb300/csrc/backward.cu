@@ -9,14 +9,14 @@
 // fp32 throughout, on the CUDA cores; every reduction has a fixed order (no
 // atomics).  Launches, in order:
 //  0. the 64-row block table of the sequences (and a check of cu_seqlens);
-//  1. rope: RoPE'd q and k rows (fp32) for every token and head;
+//  1. rope: RoPE'd q and k rows (fp32) for every token and head; alpha = e^g;
 //  2. conv: q~, k~ (and their L2-normalised qhat, khat) and vhat = conv(v);
 //  3. GDN, a cluster of 8 CTAs per (sequence, q-head) splitting the value
-//     columns: a forward pass that keeps the state every 64 absorptions (and
-//     lambda's partial sum), then per 64-absorption block, last first, the
-//     states every 8 (d 128) or 16 (d 64) absorptions, and per such stage the
-//     states in registers and the read-out and absorption steps differentiated
-//     in reverse (dqhat, and per head dkhat, dvhat, dg, dbeta);
+//     columns: a forward pass that keeps the state every 64 absorptions, then
+//     per 64-absorption block, last first, the states every 4 (d 128) or 8
+//     (d 64) absorptions, and per such stage the states in registers and the
+//     read-out and absorption steps differentiated in reverse (dqhat, lambda's
+//     partial sum, and per head dkhat, dvhat, dg, dbeta);
 //  4. softmax: per 64-query block the rows' max, sum and D = dO . o_sm and dq;
 //     per 64-key block dk, dv of its non-sink keys; the sink keys' sums over
 //     the query blocks' partials;
@@ -30,107 +30,131 @@ namespace hla {
 
 namespace {
 
-constexpr int kWB = 256;    // tokens per block of the conv-filter reduction
+constexpr int kWB = 64;     // tokens per block of the conv-filter reduction
 
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
-// sum over the CTA of v, for every thread (red: 32 floats)
-__device__ __forceinline__ float cta_sum_f(float v, float* red) {
-    v = warp_sum_f(v);
-    const int nw = (blockDim.x + 31) >> 5;
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+// cos/sin of p theta_i, i < d / 2, for one position, into shared memory (threads < d / 2)
+__device__ __forceinline__ void angles(const LayerDims& L, int64_t p, float* cs, float* sn) {
+    if ((int)threadIdx.x < L.d / 2) rope_cs_exact(p, L.theta[threadIdx.x], &cs[threadIdx.x], &sn[threadIdx.x]);
     __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < nw; ++i) t += red[i];
-    __syncthreads();
-    return t;
 }
-// ---- 1. RoPE'd rows: row r < Hq is q-head r, else k-head r - Hq; thread per channel
+
+// ---- 1. RoPE'd rows: CTA per token; rows r < Hq are q-heads, the rest k-heads; a thread per channel pair
+constexpr int kRowThreads = 256;
 template <typename Tin>
-__global__ void bwd_rope_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k,
-                                const int32_t* __restrict__ cu, float* __restrict__ qr, float* __restrict__ kr,
-                                int32_t* __restrict__ err) {
+__global__ void __launch_bounds__(kRowThreads)
+bwd_rope_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __restrict__ g,
+                const int32_t* __restrict__ cu, float* __restrict__ qr, float* __restrict__ kr,
+                float* __restrict__ alpha, int32_t* __restrict__ err) {
+    __shared__ float cs[64], sn[64];
     const int64_t t = blockIdx.x;
-    const int r = blockIdx.y, c = threadIdx.x, D = L.d, half = D / 2;
+    const int tid = threadIdx.x, D = L.d, half = D / 2;
     const int n = seq_of_token(cu, L.n_seqs, t);
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
     const int64_t p = t - start;
     // a token outside every sequence: cu_seqlens is not a monotone table from 0 to total
-    if ((p < 0 || p >= len) && r == 0 && c == 0) atomicExch(err, kErrSeqlens);
-    const bool isq = r < L.Hq;
-    const int hh = isq ? r : r - L.Hq, H = isq ? L.Hq : L.Hkv;
-    const Tin* x = (isq ? q : k) + ((size_t)t * H + hh) * D;
-    const int i = c % half;
-    float cs, sn;
-    rope_cs_exact(p, L.theta[i], &cs, &sn);
-    const float x1 = to_f32(x[i]), x2 = to_f32(x[i + half]);
-    (isq ? qr : kr)[((size_t)t * H + hh) * D + c] = c < half ? x1 * cs - x2 * sn : x2 * cs + x1 * sn;
+    if ((p < 0 || p >= len) && tid == 0) atomicExch(err, kErrSeqlens);
+    for (int h = tid; h < L.Hq; h += kRowThreads) alpha[t * L.Hq + h] = expf(g[t * L.Hq + h]);  // alpha = e^g
+    angles(L, p, cs, sn);
+    for (int idx = tid; idx < (L.Hq + L.Hkv) * half; idx += kRowThreads) {
+        const int r = idx / half, i = idx % half;
+        const bool isq = r < L.Hq;
+        const size_t row = isq ? (size_t)t * L.Hq + r : (size_t)t * L.Hkv + (r - L.Hq);
+        const Tin* x = (isq ? q : k) + row * D;
+        float* y = (isq ? qr : kr) + row * D;
+        const float x1 = to_f32(x[i]), x2 = to_f32(x[i + half]);
+        y[i] = x1 * cs[i] - x2 * sn[i];
+        y[i + half] = x2 * cs[i] + x1 * sn[i];
+    }
 }
 
-// ---- 2. conv (+ L2): rows r < Hq: q-heads, < Hq + Hkv: k-heads, else v-heads; thread per channel
-template <typename Tin>
-__global__ void bwd_conv_kernel(LayerDims L, const Tin* __restrict__ v, const float* __restrict__ wq,
-                                const float* __restrict__ wk, const float* __restrict__ wv,
-                                const int32_t* __restrict__ cu, const float* __restrict__ qr,
-                                const float* __restrict__ kr, float* __restrict__ qt, float* __restrict__ qh,
-                                float* __restrict__ kt, float* __restrict__ kh, float* __restrict__ vh) {
-    __shared__ float red[32];
+// ---- 2. conv (+ L2): CTA per token, a warp per row (rows r < Hq: q-heads, < Hq + Hkv: k-heads, else
+// v-heads), lane l holding channels l + 32 e
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kRowThreads)
+bwd_conv_kernel(LayerDims L, const Tin* __restrict__ v, const float* __restrict__ wq, const float* __restrict__ wk,
+                const float* __restrict__ wv, const int32_t* __restrict__ cu, const float* __restrict__ qr,
+                const float* __restrict__ kr, float* __restrict__ qt, float* __restrict__ qh,
+                float* __restrict__ kt, float* __restrict__ kh, float* __restrict__ vh) {
+    constexpr int E = D / 32;
     const int64_t t = blockIdx.x;
-    const int r = blockIdx.y, c = threadIdx.x, D = L.d;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n = seq_of_token(cu, L.n_seqs, t);
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
     const int64_t p = t - start;
-    const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-    const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-    const int H = kind == 0 ? L.Hq : L.Hkv;
-    const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + ((size_t)hh * D + c) * kConvWidth;
-    float acc = 0.f;
-    for (int m = 0; m < kConvWidth; ++m) {
-        const int64_t pp = p - (kConvWidth - 1) + m;
-        if (pp < 0) continue;
-        const size_t row = ((size_t)(start + pp) * H + hh) * D + c;
-        const float x = kind == 0 ? qr[row] : kind == 1 ? kr[row] : to_f32(v[row]);
-        acc = fmaf(w[m], x, acc);
+    for (int r = warp; r < L.Hq + 2 * L.Hkv; r += kRowThreads / 32) {
+        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
+        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
+        const int H = kind == 0 ? L.Hq : L.Hkv;
+        const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + (size_t)hh * D * kConvWidth;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (int m = 0; m < kConvWidth; ++m) {
+            const int64_t pp = p - (kConvWidth - 1) + m;
+            if (pp < 0) continue;
+            const size_t row = ((size_t)(start + pp) * H + hh) * D;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int c = lane + 32 * e;
+                const float x = kind == 0 ? qr[row + c] : kind == 1 ? kr[row + c] : to_f32(v[row + c]);
+                acc[e] = fmaf(w[c * kConvWidth + m], x, acc[e]);
+            }
+        }
+        const size_t o = ((size_t)t * H + hh) * D;
+        if (kind == 2) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) vh[o + lane + 32 * e] = acc[e];
+            continue;
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss = fmaf(acc[e], acc[e], ss);
+        const bool norm = kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q);
+        const float inv = norm ? rsqrtf(warp_sum_f(ss) + 1e-6f) : 1.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            (kind == 0 ? qt : kt)[o + lane + 32 * e] = acc[e];
+            (kind == 0 ? qh : kh)[o + lane + 32 * e] = acc[e] * inv;
+        }
     }
-    const size_t o = ((size_t)t * H + hh) * D + c;
-    if (kind == 2) {
-        vh[o] = acc;
-        return;
-    }
-    const bool norm = kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q);
-    const float inv = norm ? rsqrtf(cta_sum_f(acc * acc, red) + 1e-6f) : 1.f;
-    (kind == 0 ? qt : kt)[o] = acc;
-    (kind == 0 ? qh : kh)[o] = acc * inv;
 }
 
 // ---- 3. GDN backward: a cluster of kCl CTAs per (q-head, sequence), each CTA D / kCl value columns of S
 // (the columns of the recurrence are independent: only the gradients of q, k, alpha and beta sum over
-// them).  A warp holds CPW columns, lane l rows l, l + 32, ... of each, in registers.  Three passes over
-// the absorptions, all fed by one schedule of K-token stages loaded ahead with cp.async:
-//   0: forward: S every 64 absorptions to the global checkpoints; lambda's gradient sum(dO . o_lin);
+// them).  Eight lanes share a column, lane l holding rows 32 e + 4 (l % 8) + i (i < 4) of it in registers,
+// so a dot product over the key dim ends in three shuffle rounds that serve the warp's four columns at
+// once.  Three passes over the absorptions, all fed by one schedule of K-token stages loaded ahead with
+// cp.async:
+//   0: forward: S every 64 absorptions to the global checkpoints;
 //   1: per 64-absorption block, last block first: from its checkpoint, S every K absorptions to a
 //      per-(sequence, head) scratch (stays in L2);
-//   2: the same block's K-stages, last first: the K + 1 states from the scratch state, in registers; then
-//      the read-out and absorption steps differentiated in reverse.  Per stage the warps' contributions
+//   2: the same block's stages, last first: the K + 1 states from the scratch state, in registers; then
+//      the read-out and absorption steps differentiated in reverse.  Per stage the columns' contributions
 //      to dq, dk, dalpha, dbeta are summed in the CTA, then over the cluster's CTAs through distributed
-//      shared memory (one cluster barrier per stage, double-buffered); dv is per column.
+//      shared memory (one cluster barrier per stage, double-buffered); dv is per column.  lambda's
+//      gradient sum_p dO_p . o_lin,p is sum_p qhat_p . (S_p dO_p), from the same sums.
 constexpr int kCl = 8;      // CTAs per cluster
-constexpr int kGW = 8;      // warps per CTA
-constexpr int kGT = kGW * 32;
 constexpr int kCkB = 64;    // absorptions per global checkpoint
 constexpr int kRing = 3;    // stages in flight
+constexpr int kXB = 4;      // stages per cluster exchange
 template <int D> struct GdnB {
-    static constexpr int K = D == 128 ? 8 : 16;  // absorptions per stage (the states of one stage in registers)
-    static constexpr int E = D / 32, CPC = D / kCl, CPW = CPC / kGW, SPB = kCkB / K;
-    // shared memory (floats): warp partials, cluster exchange (2 buffers), stage ring, dv of a stage, sums
-    static constexpr int PART = K * 2 * kGW * D, SPART = K * 2 * kGW, XCH = 2 * K * 2 * D, XS = 2 * K * 2;
-    static constexpr int SLOT = 2 * K * D + 2 * K * CPC + 2 * K;
-    static constexpr size_t BYTES = (size_t)(PART + SPART + XCH + XS + kRing * SLOT + K * CPC + kGW + 4) * 4;
+    static constexpr int LPC = 8, E = D / LPC, CPW = 32 / LPC;  // lanes per column, rows per lane, columns per warp
+    static constexpr int CPC = D / kCl, NW = CPC / CPW, NT = NW * 32;
+    static constexpr int K = D == 128 ? 4 : 8;  // absorptions per stage (the states of one stage in registers)
+    static constexpr int SPB = kCkB / K;
+    // shared memory (floats): column partials, cluster exchange (2 buffers), stage ring, dv of a stage, sums
+    static constexpr int PART = K * 2 * CPC * D, SPART = K * 2 * CPC;
+    static constexpr int XCH = 2 * kXB * K * 2 * D, XS = 2 * kXB * K * 2, XM = 2 * kXB * 2;
+    static constexpr int SLOT = 2 * K * D + 2 * K * CPC + 2 * K;  // k, q rows; v, dO columns; alpha, beta
+    static constexpr size_t BYTES =
+        (size_t)(PART + SPART + XCH + XS + XM + kRing * SLOT + K * CPC + NW + 4) * 4;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -160,35 +184,57 @@ __device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes16
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_ring() { asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory"); }
 
+// the sum over the 8 lanes of a column (lanes differing in bits 0-2), for N values at once
 template <int N>
-__device__ __forceinline__ void warp_sum_n(float (&x)[N]) {
+__device__ __forceinline__ void col_sum(float (&x)[N]) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
+    for (int o = 1; o < 8; o <<= 1)
 #pragma unroll
         for (int i = 0; i < N; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], o);
 }
+// this lane's E rows of a D-vector in shared memory: rows 32 e + 4 lr + i
+template <int D>
+__device__ __forceinline__ void lane_rows(const float* __restrict__ src, int lr, float* x) {
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+        const float4 v = *reinterpret_cast<const float4*>(src + 32 * e + 4 * lr);
+        x[4 * e] = v.x;
+        x[4 * e + 1] = v.y;
+        x[4 * e + 2] = v.z;
+        x[4 * e + 3] = v.w;
+    }
+}
+template <int D>
+__device__ __forceinline__ void lane_rows_store(float* __restrict__ dst, int lr, const float* x) {
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e)
+        *reinterpret_cast<float4*>(dst + 32 * e + 4 * lr) = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+}
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kGT, 2)
-bwd_gdn_kernel(LayerDims L, const float* __restrict__ g, const float* __restrict__ beta,
+__global__ void __launch_bounds__(GdnB<D>::NT)
+bwd_gdn_kernel(LayerDims L, const float* __restrict__ alpha, const float* __restrict__ beta,
                const float* __restrict__ lambda, const Tin* __restrict__ dout, const int32_t* __restrict__ cu,
                const float* __restrict__ qh, const float* __restrict__ kh, const float* __restrict__ vh,
                float* __restrict__ ckpt, float* __restrict__ sub, float* __restrict__ dqh,
                float* __restrict__ dkh_h, float* __restrict__ dvh_h, float* __restrict__ dg,
                float* __restrict__ dbeta, float* __restrict__ dlam_part) {
     using B = GdnB<D>;
-    constexpr int K = B::K, E = B::E, CPC = B::CPC, CPW = B::CPW, SPB = B::SPB;
+    constexpr int K = B::K, E = B::E, CPC = B::CPC, SPB = B::SPB, NT = B::NT, NW = B::NW;
     extern __shared__ __align__(16) float smem[];
-    float* part = smem;                 // [K][2][kGW][D]: dq (0), dk (1) of each warp's columns
-    float* spart = part + B::PART;      // [K][2][kGW]: dalpha, dbeta
-    float* xch = spart + B::SPART;      // [2][K][2][D]: the CTA's sums
-    float* xs = xch + B::XCH;           // [2][K][2]
-    float* ring = xs + B::XS;           // kRing stage slots
+    float* part = smem;                 // [K][2][CPC][D]: dq (S dO, unscaled) and dk contributions per column
+    float* spart = part + B::PART;      // [K][2][CPC]: dalpha, dbeta
+    float* xch = spart + B::SPART;      // [2][kXB][K][2][D]: the CTA's sums of up to kXB stages
+    float* xs = xch + B::XCH;           // [2][kXB][K][2]: dg (alpha applied), dbeta
+    int* xm = reinterpret_cast<int*>(xs + B::XS);  // [2][kXB][2]: each stage's first absorption and count
+    float* ring = xs + B::XS + B::XM;   // kRing stage slots
     float* dv_s = ring + kRing * B::SLOT;  // [K][CPC]
-    float* red = dv_s + K * CPC;        // [kGW] + 1
+    float* red = dv_s + K * CPC;        // [NW] + 1
     const uint32_t rank = cluster_rank();
     const int h = blockIdx.x / kCl, n = blockIdx.y, kv = h / L.G, tid = threadIdx.x;
-    const int w = tid >> 5, lane = tid & 31;
+    const int w = tid >> 5, lane = tid & 31, lr = lane & 7;
+    const int colL = w * B::CPW + (lane >> 3);            // this lane's column in the CTA
+    const int col = (int)rank * CPC + colL;               // and in S
     const int ns = L.n_sinks, W = L.window;
     const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
     int64_t start, len;
@@ -206,9 +252,9 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ g, const float* __restrict
     const size_t DD = (size_t)D * D;
     const int64_t ck0 = start / kCkB + n;                 // the sequence's first global checkpoint slot
     float* my_sub = sub + ((size_t)n * L.Hq + h) * SPB * DD;
-    auto colg = [&](int cw) { return (int)rank * CPC + w * CPW + cw; };  // global column of (warp, cw)
-    auto ck_col = [&](int blk, int cw) { return ckpt + ((size_t)(ck0 + blk) * L.Hq + h) * DD + (size_t)colg(cw) * D; };
-    auto sub_col = [&](int si, int cw) { return my_sub + (size_t)si * DD + (size_t)colg(cw) * D; };
+    float* ck_col_base = ckpt + (size_t)col * D;
+    auto ck_col = [&](int blk) { return ck_col_base + ((size_t)(ck0 + blk) * L.Hq + h) * DD; };
+    auto sub_col = [&](int si) { return my_sub + (size_t)si * DD + (size_t)col * D; };
 
     // schedule entry i -> (phase, stage)
     auto sched = [&](int i, int* phase, int* s) {
@@ -231,12 +277,12 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ g, const float* __restrict
         *phase = loc < nb ? 1 : 2;
         *s = blk * SPB + (loc < nb ? loc : 2 * nb - 1 - loc);
     };
-    // slot layout: k [K][D], q [K][D], v [K][CPC], dO [K][CPC] (Tin), g [K], beta [K]
+    // slot layout: k [K][D], q [K][D], v [K][CPC], dO [K][CPC] (Tin), alpha [K], beta [K]
     auto slot_k = [&](int sl) { return ring + sl * B::SLOT; };
     auto slot_q = [&](int sl) { return ring + sl * B::SLOT + K * D; };
     auto slot_v = [&](int sl) { return ring + sl * B::SLOT + 2 * K * D; };
     auto slot_o = [&](int sl) { return reinterpret_cast<Tin*>(ring + sl * B::SLOT + 2 * K * D + K * CPC); };
-    auto slot_g = [&](int sl) { return ring + sl * B::SLOT + 2 * K * D + 2 * K * CPC; };
+    auto slot_a = [&](int sl) { return ring + sl * B::SLOT + 2 * K * D + 2 * K * CPC; };
     auto slot_b = [&](int sl) { return ring + sl * B::SLOT + 2 * K * D + 2 * K * CPC + K; };
     auto issue = [&](int i) {
         if (i < n_sched) {
@@ -245,73 +291,56 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ g, const float* __restrict
             const int sl = i % kRing;
             const int64_t m0 = (int64_t)s * K;
             const int cnt = (int)min((int64_t)K, n_abs - m0);
-            for (int idx = tid; idx < K * (D / 4); idx += kGT) {
+            const int64_t j0 = start + ns + m0;  // global row of the stage's first absorbed token
+            for (int idx = tid; idx < K * (D / 4); idx += NT) {
                 const int t = idx / (D / 4), c = (idx % (D / 4)) * 4;
                 if (t < cnt) {
-                    const int64_t j = ns + m0 + t, p = j + W;
-                    cp_async(slot_k(sl) + t * D + c, kh + ((size_t)(start + j) * L.Hkv + kv) * D + c, 16);
-                    cp_async(slot_q(sl) + t * D + c, qh + ((size_t)(start + p) * L.Hq + h) * D + c, 16);
+                    cp_async(slot_k(sl) + t * D + c, kh + ((size_t)(j0 + t) * L.Hkv + kv) * D + c, 16);
+                    if (phase == 2)
+                        cp_async(slot_q(sl) + t * D + c, qh + ((size_t)(j0 + t + W) * L.Hq + h) * D + c, 16);
                 }
             }
-            for (int idx = tid; idx < K * (CPC / 4); idx += kGT) {
+            for (int idx = tid; idx < K * (CPC / 4); idx += NT) {
                 const int t = idx / (CPC / 4), c = (idx % (CPC / 4)) * 4;
-                if (t < cnt) {
-                    const int64_t j = ns + m0 + t;
-                    cp_async(slot_v(sl) + t * CPC + c, vh + ((size_t)(start + j) * L.Hkv + kv) * D + rank * CPC + c, 16);
-                }
+                if (t < cnt)
+                    cp_async(slot_v(sl) + t * CPC + c, vh + ((size_t)(j0 + t) * L.Hkv + kv) * D + rank * CPC + c, 16);
             }
             constexpr int OCH = CPC * (int)sizeof(Tin) / 16;  // 16-byte chunks of a dO row slice
-            for (int idx = tid; idx < K * OCH; idx += kGT) {
-                const int t = idx / OCH, c = (idx % OCH) * (16 / (int)sizeof(Tin));
-                if (t < cnt) {
-                    const int64_t p = ns + m0 + t + W;
-                    cp_async(slot_o(sl) + t * CPC + c, dout + ((size_t)(start + p) * L.Hq + h) * D + rank * CPC + c, 16);
+            if (phase == 2) {
+                for (int idx = tid; idx < K * OCH; idx += NT) {
+                    const int t = idx / OCH, c = (idx % OCH) * (16 / (int)sizeof(Tin));
+                    if (t < cnt)
+                        cp_async(slot_o(sl) + t * CPC + c, dout + ((size_t)(j0 + t + W) * L.Hq + h) * D + rank * CPC + c,
+                                 16);
                 }
             }
             if (tid < cnt) {
-                const int64_t j = ns + m0 + tid;
-                cp_async(slot_g(sl) + tid, g + (size_t)(start + j) * L.Hq + h, 4);
-                cp_async(slot_b(sl) + tid, beta + (size_t)(start + j) * L.Hq + h, 4);
+                cp_async(slot_a(sl) + tid, alpha + (size_t)(j0 + tid) * L.Hq + h, 4);
+                cp_async(slot_b(sl) + tid, beta + (size_t)(j0 + tid) * L.Hq + h, 4);
             }
         }
         cp_async_commit();
     };
     // one absorption of stage token t into S (registers)
-    auto absorb = [&](float (&S)[CPW][E], int sl, int t) {
-        const float* kr = slot_k(sl) + t * D;
+    auto absorb = [&](float (&S)[E], int sl, int t) {
         float k[E];
+        lane_rows<D>(slot_k(sl) + t * D, lr, k);
+        float xp[2] = {0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < E; ++e) k[e] = kr[lane + 32 * e];
-        float x[CPW];
+        for (int e = 0; e < E; ++e) xp[e & 1] = fmaf(k[e], S[e], xp[e & 1]);
+        float x[1] = {xp[0] + xp[1]};
+        col_sum<1>(x);
+        const float a = slot_a(sl)[t], b = slot_b(sl)[t], vv = slot_v(sl)[t * CPC + colL];
+        const float u = gla ? vv : b * (vv - a * x[0]);
 #pragma unroll
-        for (int cw = 0; cw < CPW; ++cw) {
-            x[cw] = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) x[cw] = fmaf(k[e], S[cw][e], x[cw]);
-        }
-        warp_sum_n<CPW>(x);
-        const float a = expf(slot_g(sl)[t]), b = slot_b(sl)[t];
-#pragma unroll
-        for (int cw = 0; cw < CPW; ++cw) {
-            const float vv = slot_v(sl)[t * CPC + w * CPW + cw];
-            const float u = gla ? vv : b * (vv - a * x[cw]);
-#pragma unroll
-            for (int e = 0; e < E; ++e) S[cw][e] = fmaf(a, S[cw][e], k[e] * u);
-        }
+        for (int e = 0; e < E; ++e) S[e] = fmaf(a, S[e], k[e] * u);
     };
 
-    float S[CPW][E];
+    float S[E], dS[E];
 #pragma unroll
-    for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-        for (int e = 0; e < E; ++e) S[cw][e] = 0.f;
-    float dS[CPW][E];
-#pragma unroll
-    for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-        for (int e = 0; e < E; ++e) dS[cw][e] = 0.f;
+    for (int e = 0; e < E; ++e) S[e] = dS[e] = 0.f;
     float dl = 0.f;
-    int buf = 0;
+    int buf = 0, nx = 0;  // exchange buffer, stages in it
     for (int i = 0; i < kRing; ++i) issue(i);
     for (int i = 0; i < n_sched; ++i) {
         cp_async_wait_ring();
@@ -323,208 +352,164 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ g, const float* __restrict
         const int cnt = (int)min((int64_t)K, n_abs - m0);
         const int blk = s / SPB, si = s % SPB;
         if (phase == 0) {
-            if (si == 0) {
+            if (si == 0) lane_rows_store<D>(ck_col(blk), lr, S);
 #pragma unroll
-                for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) ck_col(blk, cw)[lane + 32 * e] = S[cw][e];
-            }
-#pragma unroll
-            for (int t = 0; t < K; ++t) {
-                if (t < cnt) {
-                    absorb(S, sl, t);
-                    // read-out at p = j + W for lambda's gradient
-                    const float* qr = slot_q(sl) + t * D;
-                    float o[CPW];
-#pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw) {
-                        o[cw] = 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) o[cw] = fmaf(qr[lane + 32 * e], S[cw][e], o[cw]);
-                    }
-                    warp_sum_n<CPW>(o);
-#pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw) dl = fmaf(to_f32(slot_o(sl)[t * CPC + w * CPW + cw]), o[cw], dl);
-                }
-            }
+            for (int t = 0; t < K; ++t)
+                if (t < cnt) absorb(S, sl, t);
         } else if (phase == 1) {
-            if (si == 0) {
-#pragma unroll
-                for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) S[cw][e] = ck_col(blk, cw)[lane + 32 * e];
-            }
-#pragma unroll
-            for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                for (int e = 0; e < E; ++e) sub_col(si, cw)[lane + 32 * e] = S[cw][e];
+            if (si == 0) lane_rows<D>(ck_col(blk), lr, S);
+            lane_rows_store<D>(sub_col(si), lr, S);
 #pragma unroll
             for (int t = 0; t < K; ++t)
                 if (t < cnt) absorb(S, sl, t);
         } else {
             // the stage's states S_{m0} .. S_{m0 + cnt}
-            float St[K + 1][CPW][E];
-#pragma unroll
-            for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                for (int e = 0; e < E; ++e) St[0][cw][e] = sub_col(si, cw)[lane + 32 * e];
+            float St[K + 1][E];
+            lane_rows<D>(sub_col(si), lr, St[0]);
 #pragma unroll
             for (int t = 0; t < K; ++t) {
 #pragma unroll
-                for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) St[t + 1][cw][e] = St[t][cw][e];
+                for (int e = 0; e < E; ++e) St[t + 1][e] = St[t][e];
                 if (t < cnt) absorb(St[t + 1], sl, t);
             }
 #pragma unroll
             for (int tt = 0; tt < K; ++tt) {
                 const int t = K - 1 - tt;
                 if (t < cnt) {
-                    const float* kr = slot_k(sl) + t * D;
-                    const float* qr = slot_q(sl) + t * D;
                     float k[E], q[E];
+                    lane_rows<D>(slot_k(sl) + t * D, lr, k);
+                    lane_rows<D>(slot_q(sl) + t * D, lr, q);
+                    const float dor = to_f32(slot_o(sl)[t * CPC + colL]), ldo = lam * dor;
+                    const float vv = slot_v(sl)[t * CPC + colL];
+                    const float a = slot_a(sl)[t], b = slot_b(sl)[t];
+                    // read-out at p: o_lin = S_{m+1}^T qhat -> (S_{m+1} dO) to the partials, dS += qhat lambda dO^T
+                    float pq[E];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        k[e] = kr[lane + 32 * e];
-                        q[e] = qr[lane + 32 * e];
-                    }
-                    float ldo[CPW], vv[CPW];
+                    for (int e = 0; e < E; ++e) pq[e] = St[t + 1][e] * dor;
+                    lane_rows_store<D>(part + ((t * 2 + 0) * CPC + colL) * D, lr, pq);
 #pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw) {
-                        ldo[cw] = lam * to_f32(slot_o(sl)[t * CPC + w * CPW + cw]);
-                        vv[cw] = slot_v(sl)[t * CPC + w * CPW + cw];
-                    }
-                    // read-out at p: o_lin = S_{m+1}^T qhat -> dqhat += S_{m+1} dO_lin, dS += qhat dO_lin^T
-                    float* pq = part + ((t * 2 + 0) * kGW + w) * D;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        float acc = 0.f;
-#pragma unroll
-                        for (int cw = 0; cw < CPW; ++cw) acc = fmaf(St[t + 1][cw][e], ldo[cw], acc);
-                        pq[lane + 32 * e] = acc;
-                    }
-#pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                        for (int e = 0; e < E; ++e) dS[cw][e] = fmaf(q[e], ldo[cw], dS[cw][e]);
+                    for (int e = 0; e < E; ++e) dS[e] = fmaf(q[e], ldo, dS[e]);
                     // absorption of token j from S_prev = S_m
-                    float red3[3 * CPW];
+                    float r6[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw) {
-                        float x = 0.f, du = 0.f, gs = 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            x = fmaf(k[e], St[t][cw][e], x);
-                            du = fmaf(k[e], dS[cw][e], du);
-                            gs = fmaf(dS[cw][e], St[t][cw][e], gs);
-                        }
-                        red3[3 * cw] = x;
-                        red3[3 * cw + 1] = du;
-                        red3[3 * cw + 2] = gs;
+                    for (int e = 0; e < E; ++e) {
+                        r6[(e & 1)] = fmaf(k[e], St[t][e], r6[(e & 1)]);
+                        r6[2 + (e & 1)] = fmaf(k[e], dS[e], r6[2 + (e & 1)]);
+                        r6[4 + (e & 1)] = fmaf(dS[e], St[t][e], r6[4 + (e & 1)]);
                     }
-                    warp_sum_n<3 * CPW>(red3);
-                    const float a = expf(slot_g(sl)[t]), b = slot_b(sl)[t];
-                    float da = 0.f, db = 0.f, u[CPW], du[CPW];
-#pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw) {
-                        const float x = red3[3 * cw];
-                        du[cw] = red3[3 * cw + 1];
-                        u[cw] = gla ? vv[cw] : b * (vv[cw] - a * x);
-                        if (lane == 0) dv_s[t * CPC + w * CPW + cw] = gla ? du[cw] : b * du[cw];
-                        db += gla ? 0.f : du[cw] * (vv[cw] - a * x);
-                        da += red3[3 * cw + 2] - (gla ? 0.f : b * du[cw] * x);
-                    }
-                    if (lane == 0) {
-                        spart[(t * 2 + 0) * kGW + w] = da;
-                        spart[(t * 2 + 1) * kGW + w] = db;
+                    float r3[3] = {r6[0] + r6[1], r6[2] + r6[3], r6[4] + r6[5]};
+                    col_sum<3>(r3);
+                    const float x = r3[0], du = r3[1], gs = r3[2];
+                    const float u = gla ? vv : b * (vv - a * x);
+                    if (lr == 0) {
+                        dv_s[t * CPC + colL] = gla ? du : b * du;
+                        spart[(t * 2 + 0) * CPC + colL] = gs - (gla ? 0.f : b * du * x);
+                        spart[(t * 2 + 1) * CPC + colL] = gla ? 0.f : du * (vv - a * x);
                     }
                     // dk = dS u - a b S_prev du (GLA: dS v); dS_prev = a (dS - b k du^T) (GLA: a dS)
-                    float* pk = part + ((t * 2 + 1) * kGW + w) * D;
+                    float pk[E];
+                    const float abdu = gla ? 0.f : -a * b * du;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        float acc = 0.f;
+                    for (int e = 0; e < E; ++e) pk[e] = fmaf(dS[e], u, abdu * St[t][e]);
+                    lane_rows_store<D>(part + ((t * 2 + 1) * CPC + colL) * D, lr, pk);
+                    const float bdu = gla ? 0.f : -b * du;
 #pragma unroll
-                        for (int cw = 0; cw < CPW; ++cw) {
-                            acc = fmaf(dS[cw][e], u[cw], acc);
-                            if (!gla) acc = fmaf(-a * b * St[t][cw][e], du[cw], acc);
-                        }
-                        pk[lane + 32 * e] = acc;
-                    }
-#pragma unroll
-                    for (int cw = 0; cw < CPW; ++cw)
-#pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            dS[cw][e] = gla ? a * dS[cw][e] : a * fmaf(-b * k[e], du[cw], dS[cw][e]);
+                    for (int e = 0; e < E; ++e) dS[e] = a * fmaf(bdu, k[e], dS[e]);
                 }
             }
             __syncthreads();
-            // the CTA's sums over its warps
-            float* xb = xch + buf * (K * 2 * D);
-            float* xsb = xs + buf * (K * 2);
-            for (int idx = tid; idx < K * 2 * D; idx += kGT) {
-                const int tq = idx / D, r = idx % D;
-                float acc = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kGW; ++ww) acc += part[(tq * kGW + ww) * D + r];
-                xb[idx] = acc;
-            }
-            if (tid < K * 2) {
-                float acc = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kGW; ++ww) acc += spart[tid * kGW + ww];
-                xsb[tid] = acc;
-            }
-            cluster_sync_all();
-            // over the cluster: this CTA finishes rows [rank D / kCl, (rank + 1) D / kCl) of dq and dk
-            constexpr int RS = D / kCl;
-            for (int idx = tid; idx < K * 2 * RS; idx += kGT) {
-                const int tq = idx / RS, t = tq / 2, r = (int)rank * RS + idx % RS;
-                if (t < cnt) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(xb + tq * D + r, rr);
-                    const int64_t j = ns + m0 + t;
-                    if (tq % 2 == 0)
-                        dqh[((size_t)(start + j + W) * L.Hq + h) * D + r] = acc;
-                    else
-                        dkh_h[((size_t)(start + j) * L.Hq + h) * D + r] = acc;
-                }
-            }
-            if (rank == 0 && tid < K * 2) {
-                const int t = tid / 2;
-                if (t < cnt) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(xsb + tid, rr);
-                    const size_t o = (size_t)(start + ns + m0 + t) * L.Hq + h;
-                    if (tid % 2 == 0)
-                        dg[o] = acc * expf(slot_g(sl)[t]);
-                    else
-                        dbeta[o] = acc;
-                }
-            }
-            for (int idx = tid; idx < K * CPC; idx += kGT) {
+            // dv of the stage (this CTA's columns are final)
+            for (int idx = tid; idx < K * CPC; idx += NT) {
                 const int t = idx / CPC, c = idx % CPC;
                 if (t < cnt) dvh_h[((size_t)(start + ns + m0 + t) * L.Hq + h) * D + rank * CPC + c] = dv_s[idx];
             }
-            buf ^= 1;
+            // the CTA's sums over its columns into exchange slot nx; lambda's gradient from the dq rows
+            // (sum_p qhat_p . S_p dO_p), alpha applied to dalpha
+            float* xb = xch + (buf * kXB + nx) * (K * 2 * D);
+            float* xsb = xs + (buf * kXB + nx) * (K * 2);
+            for (int idx = tid; idx < K * 2 * (D / 4); idx += NT) {
+                const int tq = idx / (D / 4), r = (idx % (D / 4)) * 4;
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+                for (int c = 0; c < CPC; c += 2) {
+                    const float4 u0 = *reinterpret_cast<const float4*>(part + (tq * CPC + c) * D + r);
+                    const float4 u1 = *reinterpret_cast<const float4*>(part + (tq * CPC + c + 1) * D + r);
+                    a0.x += u0.x; a0.y += u0.y; a0.z += u0.z; a0.w += u0.w;
+                    a1.x += u1.x; a1.y += u1.y; a1.z += u1.z; a1.w += u1.w;
+                }
+                const float4 sum = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+                *reinterpret_cast<float4*>(xb + tq * D + r) = sum;
+                if (tq % 2 == 0 && tq / 2 < cnt) {
+                    const float4 qv = *reinterpret_cast<const float4*>(slot_q(sl) + (tq / 2) * D + r);
+                    dl = fmaf(qv.x, sum.x, fmaf(qv.y, sum.y, fmaf(qv.z, sum.z, fmaf(qv.w, sum.w, dl))));
+                }
+            }
+            for (int idx = tid; idx < K * 2; idx += NT) {
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < CPC; ++c) acc += spart[idx * CPC + c];
+                xsb[idx] = idx % 2 == 0 && idx / 2 < cnt ? acc * slot_a(sl)[idx / 2] : acc;
+            }
+            if (tid == 0) {
+                xm[(buf * kXB + nx) * 2] = (int)m0;
+                xm[(buf * kXB + nx) * 2 + 1] = cnt;
+            }
+            ++nx;
+            if (nx == kXB || si == 0) {  // exchange: a full buffer, or the block's last stage
+                cluster_sync_all();
+                // over the cluster: this CTA finishes rows [rank D / kCl, (rank + 1) D / kCl) of dq and dk
+                constexpr int RS = D / kCl;
+                const float* xbb = xch + buf * kXB * (K * 2 * D);
+                const int* xmb = xm + buf * kXB * 2;
+                for (int idx = tid; idx < nx * K * 2 * RS; idx += NT) {
+                    const int sx = idx / (K * 2 * RS), rem = idx % (K * 2 * RS);
+                    const int tq = rem / RS, t = tq / 2, r = (int)rank * RS + rem % RS;
+                    if (t < xmb[sx * 2 + 1]) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(xbb + (sx * K * 2 + tq) * D + r, rr);
+                        const int64_t j = start + ns + xmb[sx * 2] + t;
+                        if (tq % 2 == 0)
+                            dqh[((size_t)(j + W) * L.Hq + h) * D + r] = lam * acc;
+                        else
+                            dkh_h[((size_t)j * L.Hq + h) * D + r] = acc;
+                    }
+                }
+                if (rank == 0) {
+                    const float* xsx = xs + buf * kXB * (K * 2);
+                    for (int idx = tid; idx < nx * K * 2; idx += NT) {
+                        const int sx = idx / (K * 2), t = (idx % (K * 2)) / 2;
+                        if (t < xmb[sx * 2 + 1]) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(xsx + idx, rr);
+                            const size_t o = (size_t)(start + ns + xmb[sx * 2] + t) * L.Hq + h;
+                            (idx % 2 == 0 ? dg : dbeta)[o] = acc;
+                        }
+                    }
+                }
+                buf ^= 1;
+                nx = 0;
+            }
         }
         __syncthreads();
         issue(i + kRing);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    // lambda's gradient: over the warps, then over the cluster
+    // lambda's gradient: over the CTA, then over the cluster
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
     if (lane == 0) red[w] = dl;
     __syncthreads();
     if (tid == 0) {
         float acc = 0.f;
-        for (int ww = 0; ww < kGW; ++ww) acc += red[ww];
-        red[kGW] = acc;
+        for (int ww = 0; ww < NW; ++ww) acc += red[ww];
+        red[NW] = acc;
     }
     cluster_sync_all();
     if (rank == 0 && tid == 0) {
         float acc = 0.f;
-        for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(red + kGW, rr);
+        for (int rr = 0; rr < kCl; ++rr) acc += ld_cluster(red + NW, rr);
         dlam_part[(size_t)n * L.Hq + h] = acc;
     }
     cluster_sync_all();  // every CTA's shared memory stays until rank 0 has read it
@@ -958,90 +943,117 @@ __global__ void bwd_sm_sink_kernel(LayerDims L, const int32_t* __restrict__ cu, 
     }
 }
 
-// ---- 5. feature backward: rows r < Hq are q-heads, < Hq + Hkv k-heads, else v-heads; thread per channel.
-// First the L2 backward into d(pre-norm) (kind-specific inputs), written over dpre; the conv and RoPE
-// backward then run in bwd_feat_out_kernel.
-__global__ void bwd_l2_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __restrict__ qt,
-                              const float* __restrict__ kt, const float* __restrict__ dqh,
-                              const float* __restrict__ dkh_h, const float* __restrict__ dvh_h,
-                              float* __restrict__ dqt, float* __restrict__ dkt, float* __restrict__ dvt) {
-    __shared__ float red[32];
+// ---- 5. feature backward: first the L2 backward into the gradient of the pre-norm rows (q-heads, then
+// k-heads with the group's per-head gradients summed) and the group sums of the v rows; the conv and RoPE
+// backward then run in bwd_feat_out_kernel.  CTA per token, a warp per row, lane l channels l + 32 e.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads)
+bwd_l2_kernel(LayerDims L, const float* __restrict__ qt, const float* __restrict__ kt,
+              const float* __restrict__ dqh, const float* __restrict__ dkh_h, const float* __restrict__ dvh_h,
+              float* __restrict__ dqt, float* __restrict__ dkt, float* __restrict__ dvt) {
+    constexpr int E = D / 32;
     const int64_t t = blockIdx.x;
-    const int r = blockIdx.y, c = threadIdx.x, D = L.d;
-    const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-    const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-    if (kind == 2) {  // vhat = conv(v): the per-head gradients of the group summed
-        float s = 0.f;
-        for (int gq = 0; gq < L.G; ++gq) s += dvh_h[((size_t)t * L.Hq + hh * L.G + gq) * D + c];
-        dvt[((size_t)t * L.Hkv + hh) * D + c] = s;
-        return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < L.Hq + 2 * L.Hkv; r += kRowThreads / 32) {
+        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
+        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
+        float dy[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) dy[e] = 0.f;
+        if (kind == 0) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) dy[e] = dqh[((size_t)t * L.Hq + hh) * D + lane + 32 * e];
+        } else {
+            const float* src = kind == 1 ? dkh_h : dvh_h;
+            for (int gq = 0; gq < L.G; ++gq)
+#pragma unroll
+                for (int e = 0; e < E; ++e) dy[e] += src[((size_t)t * L.Hq + hh * L.G + gq) * D + lane + 32 * e];
+        }
+        if (kind == 2) {  // vhat = conv(v): no norm
+#pragma unroll
+            for (int e = 0; e < E; ++e) dvt[((size_t)t * L.Hkv + hh) * D + lane + 32 * e] = dy[e];
+            continue;
+        }
+        const float* pre = kind == 0 ? qt + ((size_t)t * L.Hq + hh) * D : kt + ((size_t)t * L.Hkv + hh) * D;
+        float* dst = kind == 0 ? dqt + ((size_t)t * L.Hq + hh) * D : dkt + ((size_t)t * L.Hkv + hh) * D;
+        if (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q)) {
+            // y = x / nrm, nrm = sqrt(|x|^2 + eps): dx = (dy - x (x . dy) / nrm^2) / nrm
+            float x[E], n2 = 0.f, xd = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                x[e] = pre[lane + 32 * e];
+                n2 = fmaf(x[e], x[e], n2);
+                xd = fmaf(x[e], dy[e], xd);
+            }
+            n2 = warp_sum_f(n2) + 1e-6f;
+            xd = warp_sum_f(xd);
+            const float inv = rsqrtf(n2);
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[lane + 32 * e] = (dy[e] - x[e] * xd / n2) * inv;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[lane + 32 * e] = dy[e];
+        }
     }
-    float dyh;
-    const float* pre;
-    if (kind == 0) {
-        dyh = dqh[((size_t)t * L.Hq + hh) * D + c];
-        pre = qt + ((size_t)t * L.Hq + hh) * D;
-    } else {
-        dyh = 0.f;
-        for (int gq = 0; gq < L.G; ++gq) dyh += dkh_h[((size_t)t * L.Hq + hh * L.G + gq) * D + c];
-        pre = kt + ((size_t)t * L.Hkv + hh) * D;
-    }
-    const bool norm = kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q);
-    float dx = dyh;
-    if (norm) {  // y = x / nrm, nrm = sqrt(|x|^2 + eps): dx = (dy - x (x . dy) / nrm^2) / nrm
-        const float x = pre[c];
-        const float n2 = cta_sum_f(x * x, red) + 1e-6f;
-        const float xd = cta_sum_f(x * dyh, red);
-        dx = (dyh - x * xd / n2) * rsqrtf(n2);
-    }
-    (kind == 0 ? dqt : dkt)[((size_t)t * (kind == 0 ? L.Hq : L.Hkv) + hh) * D + c] = dx;
 }
 
-// conv backward (the taps that read position p, from the later positions of the same sequence),
-// plus the softmax branch's gradient, then RoPE's transpose; writes dq, dk, dv
-__global__ void bwd_feat_out_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __restrict__ wq,
-                                    const float* __restrict__ wk, const float* __restrict__ wv,
-                                    const float* __restrict__ dqt, const float* __restrict__ dkt,
-                                    const float* __restrict__ dvt, const float* __restrict__ dqr_sm,
-                                    const float* __restrict__ dkr_h, const float* __restrict__ dv_h,
-                                    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv) {
-    __shared__ float gx[128];
+// conv backward (the taps that read position p, from the later positions of the same sequence), plus the
+// softmax branch's gradient, then RoPE's transpose; writes dq, dk, dv.  CTA per token; rows r < Hq are
+// q-heads, < Hq + Hkv k-heads, else v-heads; a thread per channel pair (i, i + d / 2).
+__global__ void __launch_bounds__(kRowThreads)
+bwd_feat_out_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __restrict__ wq,
+                    const float* __restrict__ wk, const float* __restrict__ wv, const float* __restrict__ dqt,
+                    const float* __restrict__ dkt, const float* __restrict__ dvt, const float* __restrict__ dqr_sm,
+                    const float* __restrict__ dkr_h, const float* __restrict__ dv_h, float* __restrict__ dq,
+                    float* __restrict__ dk, float* __restrict__ dv) {
+    __shared__ float cs[64], sn[64];
     const int64_t t = blockIdx.x;
-    const int r = blockIdx.y, c = threadIdx.x, D = L.d, half = D / 2;
+    const int tid = threadIdx.x, D = L.d, half = D / 2;
     const int n = seq_of_token(cu, L.n_seqs, t);
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
     const int64_t p = t - start;
-    const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-    const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-    const int H = kind == 0 ? L.Hq : L.Hkv;
-    const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + ((size_t)hh * D + c) * kConvWidth;
-    const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
-    // x_p feeds y_{p + 7 - m} through tap m
-    float acc = 0.f;
-    for (int m = 0; m < kConvWidth; ++m) {
-        const int64_t pp = p + (kConvWidth - 1) - m;
-        if (pp >= len) continue;
-        acc = fmaf(w[m], dy[((size_t)(start + pp) * H + hh) * D + c], acc);
+    angles(L, p, cs, sn);
+    for (int idx = tid; idx < (L.Hq + 2 * L.Hkv) * half; idx += kRowThreads) {
+        const int r = idx / half, i = idx % half;
+        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
+        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
+        const int H = kind == 0 ? L.Hq : L.Hkv;
+        const float* w = kind == 0 ? wq : kind == 1 ? wk : wv;
+        const float* w1 = w + ((size_t)hh * D + i) * kConvWidth;
+        const float* w2 = w + ((size_t)hh * D + i + half) * kConvWidth;
+        const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
+        // x_p feeds y_{p + 7 - m} through tap m
+        float a1 = 0.f, a2 = 0.f;
+        for (int m = 0; m < kConvWidth; ++m) {
+            const int64_t pp = p + (kConvWidth - 1) - m;
+            if (pp >= len) continue;
+            const float* yr = dy + ((size_t)(start + pp) * H + hh) * D;
+            a1 = fmaf(w1[m], yr[i], a1);
+            a2 = fmaf(w2[m], yr[i + half], a2);
+        }
+        // the softmax branch's gradient of the RoPE'd row (q, k) or of raw v, summed over the group for k, v
+        if (kind == 0) {
+            const float* sg = dqr_sm + ((size_t)t * L.Hq + hh) * D;
+            a1 += sg[i];
+            a2 += sg[i + half];
+        } else {
+            for (int gq = 0; gq < L.G; ++gq) {
+                const float* sg = (kind == 1 ? dkr_h : dv_h) + ((size_t)t * L.Hq + hh * L.G + gq) * D;
+                a1 += sg[i];
+                a2 += sg[i + half];
+            }
+        }
+        if (kind == 2) {
+            float* o = dv + ((size_t)t * L.Hkv + hh) * D;
+            o[i] = a1;
+            o[i + half] = a2;
+        } else {  // RoPE's transpose: rotate the pair back by the angle p theta_i
+            float* o = (kind == 0 ? dq : dk) + ((size_t)t * H + hh) * D;
+            o[i] = a1 * cs[i] + a2 * sn[i];
+            o[i + half] = a2 * cs[i] - a1 * sn[i];
+        }
     }
-    // the softmax branch's gradient of the RoPE'd row (q, k) or of raw v, summed over the group for k, v
-    if (kind == 0) {
-        acc += dqr_sm[((size_t)t * L.Hq + hh) * D + c];
-    } else {
-        for (int gq = 0; gq < L.G; ++gq) acc += (kind == 1 ? dkr_h : dv_h)[((size_t)t * L.Hq + hh * L.G + gq) * D + c];
-    }
-    if (kind == 2) {
-        dv[((size_t)t * L.Hkv + hh) * D + c] = acc;
-        return;
-    }
-    // RoPE's transpose: rotate the pair (i, i + D/2) back by the angle p theta_i
-    gx[c] = acc;
-    __syncthreads();
-    const int i = c % half;
-    float cs, sn;
-    rope_cs_exact(p, L.theta[i], &cs, &sn);
-    const float g1 = gx[i], g2 = gx[i + half];
-    (kind == 0 ? dq : dk)[((size_t)t * H + hh) * D + c] = c < half ? g1 * cs + g2 * sn : g2 * cs - g1 * sn;
 }
 
 // ---- 6. conv filters: partial sums over a block of kWB tokens, per (row, channel, tap); then the blocks
@@ -1132,6 +1144,7 @@ BwdLayout bwd_layout(const LayerDims& L) {
     b.dkt = take(T * Hkv * D);
     b.dvt = take(T * Hkv * D);
     b.stats = take(T * Hq * 3);
+    b.alpha = take(T * Hq);
     b.ckpt = take((T / kCkB + N + 1) * Hq * D * D);  // S every 64 absorptions of every sequence and q-head
     b.sub = take(N * Hq * spb * D * D);               // S every stage of one 64-absorption block
     b.dlam_part = take(N * Hq);
@@ -1146,7 +1159,7 @@ BwdLayout bwd_layout(const LayerDims& L) {
 }
 
 template <typename Tin, int D>
-cudaError_t launch_gdn_bwd(const LayerDims& L, const float* g, const float* beta, const float* lambda,
+cudaError_t launch_gdn_bwd(const LayerDims& L, const float* alpha, const float* beta, const float* lambda,
                            const Tin* dout, const int32_t* cu, const float* qh, const float* kh, const float* vh,
                            float* ckpt, float* sub, float* dqh, float* dkh_h, float* dvh_h, float* dg, float* dbeta,
                            float* dlam_part, cudaStream_t st) {
@@ -1158,7 +1171,7 @@ cudaError_t launch_gdn_bwd(const LayerDims& L, const float* g, const float* beta
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCl * L.Hq, L.n_seqs);
-    cfg.blockDim = dim3(kGT);
+    cfg.blockDim = dim3(GdnB<D>::NT);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
@@ -1168,7 +1181,7 @@ cudaError_t launch_gdn_bwd(const LayerDims& L, const float* g, const float* beta
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_gdn_kernel<Tin, D>, L, g, beta, lambda, dout, cu, qh, kh, vh, ckpt, sub, dqh,
+    return cudaLaunchKernelEx(&cfg, bwd_gdn_kernel<Tin, D>, L, alpha, beta, lambda, dout, cu, qh, kh, vh, ckpt, sub, dqh,
                               dkh_h, dvh_h, dg, dbeta, dlam_part);
 }
 
@@ -1215,15 +1228,19 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
     if ((e = mark(0)) != cudaSuccess) return e;
     int32_t* sm_base = reinterpret_cast<int32_t*>(ws + b.sm_base);
     bwd_blocks_kernel<<<1, 1024, 0, st>>>(L, cu, sm_base, reinterpret_cast<int32_t*>(ws + b.err));
-    bwd_rope_kernel<Tin><<<dim3((unsigned)T, L.Hq + L.Hkv), D, 0, st>>>(L, q, k, cu, F(b.qr), F(b.kr),
+    bwd_rope_kernel<Tin><<<(unsigned)T, kRowThreads, 0, st>>>(L, q, k, g, cu, F(b.qr), F(b.kr), F(b.alpha),
                                                                         reinterpret_cast<int32_t*>(ws + b.err));
     if ((e = mark(1)) != cudaSuccess) return e;
-    bwd_conv_kernel<Tin><<<dim3((unsigned)T, rows), D, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt), F(b.qh),
-                                                                F(b.kt), F(b.kh), F(b.vh));
+    if (D == 128)
+        bwd_conv_kernel<Tin, 128><<<(unsigned)T, kRowThreads, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
+                                                                       F(b.qh), F(b.kt), F(b.kh), F(b.vh));
+    else
+        bwd_conv_kernel<Tin, 64><<<(unsigned)T, kRowThreads, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
+                                                                      F(b.qh), F(b.kt), F(b.kh), F(b.vh));
     if ((e = mark(2)) != cudaSuccess) return e;
-    e = D == 128 ? launch_gdn_bwd<Tin, 128>(L, g, beta, lambda, dout, cu, F(b.qh), F(b.kh), F(b.vh), F(b.ckpt),
+    e = D == 128 ? launch_gdn_bwd<Tin, 128>(L, F(b.alpha), beta, lambda, dout, cu, F(b.qh), F(b.kh), F(b.vh), F(b.ckpt),
                                             F(b.sub), F(b.dqh), F(b.dkh_h), F(b.dvh_h), dg, dbeta, F(b.dlam_part), st)
-                 : launch_gdn_bwd<Tin, 64>(L, g, beta, lambda, dout, cu, F(b.qh), F(b.kh), F(b.vh), F(b.ckpt),
+                 : launch_gdn_bwd<Tin, 64>(L, F(b.alpha), beta, lambda, dout, cu, F(b.qh), F(b.kh), F(b.vh), F(b.ckpt),
                                            F(b.sub), F(b.dqh), F(b.dkh_h), F(b.dvh_h), dg, dbeta, F(b.dlam_part), st);
     if (e != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
@@ -1233,10 +1250,14 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
                                           F(b.dqr_sm), F(b.dkr_h), F(b.dv_h), F(b.sink_k), F(b.sink_v), st);
     if (e != cudaSuccess) return e;
     if ((e = mark(4)) != cudaSuccess) return e;
-    bwd_l2_kernel<<<dim3((unsigned)T, rows), D, 0, st>>>(L, cu, F(b.qt), F(b.kt), F(b.dqh), F(b.dkh_h), F(b.dvh_h),
-                                                         F(b.dqt), F(b.dkt), F(b.dvt));
+    if (D == 128)
+        bwd_l2_kernel<128><<<(unsigned)T, kRowThreads, 0, st>>>(L, F(b.qt), F(b.kt), F(b.dqh), F(b.dkh_h), F(b.dvh_h),
+                                                                F(b.dqt), F(b.dkt), F(b.dvt));
+    else
+        bwd_l2_kernel<64><<<(unsigned)T, kRowThreads, 0, st>>>(L, F(b.qt), F(b.kt), F(b.dqh), F(b.dkh_h), F(b.dvh_h),
+                                                               F(b.dqt), F(b.dkt), F(b.dvt));
     if ((e = mark(5)) != cudaSuccess) return e;
-    bwd_feat_out_kernel<<<dim3((unsigned)T, rows), D, 0, st>>>(L, cu, wq, wk, wv, F(b.dqt), F(b.dkt), F(b.dvt),
+    bwd_feat_out_kernel<<<(unsigned)T, kRowThreads, 0, st>>>(L, cu, wq, wk, wv, F(b.dqt), F(b.dkt), F(b.dvt),
                                                                F(b.dqr_sm), F(b.dkr_h), F(b.dv_h), dq, dk, dv);
     if ((e = mark(6)) != cudaSuccess) return e;
     bwd_convw_part_kernel<Tin><<<dim3(b.n_blocks, rows), D, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),

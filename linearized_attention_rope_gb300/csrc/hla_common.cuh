@@ -114,8 +114,9 @@ __device__ __forceinline__ void seq_range(const int32_t* __restrict__ cu, int s,
 // double precision, then evaluated in fp32 (used where few angles are needed).
 __device__ __forceinline__ void rope_cs_exact(int64_t p, double theta, float* c, float* s) {
     const double two_pi = 6.283185307179586476925286766559;
+    const double inv_two_pi = 0.15915494309189533576888376337251;
     double a = (double)p * theta;
-    a -= two_pi * rint(a / two_pi);
+    a -= two_pi * rint(a * inv_two_pi);  // any integer near a / 2 pi leaves |a| within pi and a rounding
     sincosf((float)a, s, c);
 }
 
@@ -322,8 +323,8 @@ cudaError_t launch_prefill_continue(const LayerDims& L, const Tin* q, const Tin*
 // sum(dout . o): dq [total, Hq, d], dk, dv [total, Hkv, d], dg, dbeta [total, Hq], dlam [Hq],
 // dwq [Hq, d, 8], dwk, dwv [Hkv, d, 8], all fp32.
 struct BwdLayout {
-    size_t err, qr, kr, qt, qh, kt, kh, vh, dqh, dkh_h, dvh_h, dqr_sm, dkr_h, dv_h, dqt, dkt, dvt, stats, ckpt,
-        sub, dlam_part, convw_part, sm_base, sink_k, sink_v, total;
+    size_t err, qr, kr, qt, qh, kt, kh, vh, dqh, dkh_h, dvh_h, dqr_sm, dkr_h, dv_h, dqt, dkt, dvt, stats, alpha,
+        ckpt, sub, dlam_part, convw_part, sm_base, sink_k, sink_v, total;
     int n_blocks, n_sm_blocks;
 };
 BwdLayout bwd_layout(const LayerDims& L);
