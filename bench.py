@@ -499,7 +499,7 @@ def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_step
         achieved = w["flops"] / (stage_ms[name] / 1e3) / 1e12
         return {"kernel": w["kernel"], "bound": "alu", "achieved": round(achieved, 4), "peak": FP32_ALU_TFLOPS,
                 "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 5),
-                "traffic": kernel_traffic(w["kernel"], BWD_SOURCES, key), "algorithmic": w["flops"],
+                "traffic": kernel_traffic(w["kernel"], BWD_SOURCES, key + "_backward"), "algorithmic": w["flops"],
                 "peak_source": FP32_ALU_TFLOPS_DERIVATION}
 
     dominant = max(work, key=lambda n: stage_ms[n])
@@ -541,6 +541,12 @@ def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_step
 
 
 SCAN_SEQ = 32768
+
+
+def scan_traffic(key):
+    """DRAM bytes per prefill of the token-serial GDN launches (and the scan's) recorded under `key`."""
+    parts = [kernel_traffic(k, GDN_RECURRENT_SOURCES, key) for k in ("gdn_recurrent_kernel", "gdn_part_scan_kernel")]
+    return None if parts[0] is None else parts[0] + (parts[1] or 0.0)
 
 
 def run_scan_bench(dist, trial_seconds=0.5):
@@ -606,7 +612,7 @@ def run_scan_bench(dist, trial_seconds=0.5):
                                   "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
                                   "frac": round(flops / (gdn_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS, 5),
                                   "algorithmic": flops, "peak_source": FP32_ALU_TFLOPS_DERIVATION,
-                                  "traffic": None}}
+                                  "traffic": scan_traffic("scan_fp32" if name == "scan" else "scan_fp32_single")}}
         del ws
     return res
 
@@ -801,13 +807,16 @@ def cpu_baseline(wl, x, seconds: float = 10.0):
     cores = os.cpu_count() or 1
     units = oracle_units(wl, seconds * cores * ORACLE_TOKEN_HEADS_PER_CORE_S)
     times, used = time_oracle(wl, x, units)
+    if times[0] < seconds / 2:  # the whole workload is a short sample: repeat it up to about `seconds`
+        more, _ = time_oracle(wl, x, units, reps=max(0, min(30, int(seconds / max(times[0], 1e-3))) - 1))
+        times += more
     seqlens = wl.seqlens
     token_heads = sum(seqlens[n] for n, _ in units)
     tokens = token_heads / wl.n_q_heads
-    return {"value": tokens / times[0], "unit": "tokens/s", "cores": used, "kind": "oracle",
+    return {"value": tokens * len(times) / sum(times), "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"{wl.name}: {len(units)} (sequence, q-head) units, q-heads strided evenly over every "
-                      f"sequence ({token_heads} token-heads = {tokens:.0f} token-equivalents), one pass, "
-                      f"fp64 C oracle, {used} threads, {times[0]:.1f} s"}
+                      f"sequence ({token_heads} token-heads = {tokens:.0f} token-equivalents), {len(times)} "
+                      f"pass(es), fp64 C oracle, {used} threads, {sum(times):.1f} s"}
 
 
 def run_reference(args, dist):
@@ -844,6 +853,11 @@ TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
     "decode_features_kernel": DECODE_SOURCES,
     "decode_attn_state_kernel": DECODE_SOURCES,
     "decode_combine_kernel": DECODE_SOURCES,
+    "bwd_gdn_kernel": BWD_SOURCES,
+    "bwd_sm_query_kernel": BWD_SOURCES,
+    "bwd_sm_key_kernel": BWD_SOURCES,
+    "gdn_recurrent_kernel": GDN_RECURRENT_SOURCES,
+    "gdn_part_scan_kernel": GDN_RECURRENT_SOURCES,
 }
 
 

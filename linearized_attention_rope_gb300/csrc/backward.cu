@@ -24,6 +24,8 @@
 //     gradients of each kv group are summed;
 //  6. the conv filters' gradients (per token block, then over the blocks);
 //  7. lambda's gradient over the sequences.
+#include <type_traits>
+
 #include "hla_common.cuh"
 
 namespace hla {
@@ -351,31 +353,24 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ alpha, const float* __rest
         const int64_t m0 = (int64_t)s * K;
         const int cnt = (int)min((int64_t)K, n_abs - m0);
         const int blk = s / SPB, si = s % SPB;
-        if (phase == 0) {
-            if (si == 0) lane_rows_store<D>(ck_col(blk), lr, S);
-#pragma unroll
-            for (int t = 0; t < K; ++t)
-                if (t < cnt) absorb(S, sl, t);
-        } else if (phase == 1) {
-            if (si == 0) lane_rows<D>(ck_col(blk), lr, S);
-            lane_rows_store<D>(sub_col(si), lr, S);
-#pragma unroll
-            for (int t = 0; t < K; ++t)
-                if (t < cnt) absorb(S, sl, t);
-        } else {
-            // the stage's states S_{m0} .. S_{m0 + cnt}
+        // a full stage (cnt == K, all but a sequence's last) runs without per-token tests, so that the
+        // compiler can overlap one token's loads with the previous token's chain
+
+        // the stage's states S_{m0} .. S_{m0 + cnt}, then the read-out and absorption steps in reverse
+        auto reverse_stage = [&](auto full) {
+            constexpr bool FULL = decltype(full)::value;
             float St[K + 1][E];
             lane_rows<D>(sub_col(si), lr, St[0]);
 #pragma unroll
             for (int t = 0; t < K; ++t) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) St[t + 1][e] = St[t][e];
-                if (t < cnt) absorb(St[t + 1], sl, t);
+                if (FULL || t < cnt) absorb(St[t + 1], sl, t);
             }
 #pragma unroll
             for (int tt = 0; tt < K; ++tt) {
                 const int t = K - 1 - tt;
-                if (t < cnt) {
+                if (FULL || t < cnt) {
                     float k[E], q[E];
                     lane_rows<D>(slot_k(sl) + t * D, lr, k);
                     lane_rows<D>(slot_q(sl) + t * D, lr, q);
@@ -417,6 +412,23 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ alpha, const float* __rest
                     for (int e = 0; e < E; ++e) dS[e] = a * fmaf(bdu, k[e], dS[e]);
                 }
             }
+        };
+        if (phase < 2) {
+            if (phase == 0 && si == 0) lane_rows_store<D>(ck_col(blk), lr, S);
+            if (phase == 1) {
+                if (si == 0) lane_rows<D>(ck_col(blk), lr, S);
+                lane_rows_store<D>(sub_col(si), lr, S);
+            }
+            if (cnt == K) {
+#pragma unroll
+                for (int t = 0; t < K; ++t) absorb(S, sl, t);
+            } else {
+#pragma unroll
+                for (int t = 0; t < K; ++t)
+                    if (t < cnt) absorb(S, sl, t);
+            }
+        } else {
+            if (cnt == K) reverse_stage(std::true_type{}); else reverse_stage(std::false_type{});
             __syncthreads();
             // dv of the stage (this CTA's columns are final)
             for (int idx = tid; idx < K * CPC; idx += NT) {
@@ -529,8 +541,8 @@ template <int D> constexpr size_t sm_smem_bytes(int n_tiles64) {
     return (size_t)(4 * kSB * (D + 4) + n_tiles64 * kSB * kLP + 3 * kSB) * sizeof(float);
 }
 
-// acc[i][j] += sum_k A[ty + 16 i][k] B[tx + 16 j][k] (row pitch D + 4, 16-byte rows)
-template <int D>
+// acc[i][j] += sum_k A[ty + 16 i][k] B[tx + 16 j][k], j < NJ (row pitch D + 4, 16-byte rows)
+template <int D, int NJ = 4>
 __device__ __forceinline__ void mm_abT(const float* __restrict__ A, const float* __restrict__ B, int ty, int tx,
                                        float acc[4][4]) {
     constexpr int LD = D + 4;
@@ -540,11 +552,11 @@ __device__ __forceinline__ void mm_abT(const float* __restrict__ A, const float*
 #pragma unroll
         for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(A + (ty + 16 * i) * LD + k);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(B + (tx + 16 * j) * LD + k);
+        for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4*>(B + (tx + 16 * j) * LD + k);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
                 acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
                 acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
@@ -556,23 +568,23 @@ __device__ __forceinline__ void mm_abT(const float* __restrict__ A, const float*
 // Column c of a thread's D / 16 output columns: tx * 4 + (c % 4) + 64 (c / 4).
 __device__ __forceinline__ int sm_col(int tx, int c) { return tx * 4 + (c & 3) + 64 * (c >> 2); }
 
-// acc[i][c] += sum_j P[ty + 16 i][j] X[j][sm_col(tx, c)], j < 64 (P pitch kLP, X pitch D + 4)
-template <int D>
+// acc[i][c] += sum_j P[ty + 16 i][j] X[j][sm_col(tx, c)], j < JB, i < NI (P pitch kLP, X pitch D + 4)
+template <int D, int JB = kSB, int NI = 4>
 __device__ __forceinline__ void mm_ab(const float* __restrict__ P, const float* __restrict__ X, int ty, int tx,
                                       float acc[4][D / 16]) {
     constexpr int LD = D + 4, CC = D / 64;
 #pragma unroll 2
-    for (int j = 0; j < kSB; j += 4) {
+    for (int j = 0; j < JB; j += 4) {
         float4 p[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = *reinterpret_cast<const float4*>(P + (ty + 16 * i) * kLP + j);
+        for (int i = 0; i < NI; ++i) p[i] = *reinterpret_cast<const float4*>(P + (ty + 16 * i) * kLP + j);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             float4 x[CC];
 #pragma unroll
             for (int cc = 0; cc < CC; ++cc) x[cc] = *reinterpret_cast<const float4*>(X + (j + jj) * LD + tx * 4 + 64 * cc);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < NI; ++i) {
                 const float pv = jj == 0 ? p[i].x : jj == 1 ? p[i].y : jj == 2 ? p[i].z : p[i].w;
 #pragma unroll
                 for (int cc = 0; cc < CC; ++cc) {
@@ -721,18 +733,16 @@ bwd_sm_query_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restric
 #pragma unroll
         for (int c = 0; c < NC; ++c) O[i][c] = 0.f;
     }
-    for (int t = 0; t < n_tiles; ++t) {
-        int64_t j0;
-        int nk;
-        tile(t, &j0, &nk);
-        load_kv(j0, nk);
+    // a tile of at most 16 keys (the sinks) runs on the first 16 columns only (NJ = 1)
+    auto pass1 = [&](auto nj, int64_t j0, int nk) {
+        constexpr int NJ = decltype(nj)::value;
         float s[4][4] = {};
-        mm_abT<D>(Qs, Ks, ty, tx, s);
+        mm_abT<D, NJ>(Qs, Ks, ty, tx, s);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 s[i][j] = visible(ty + 16 * i, tx + 16 * j, j0, nk) ? s[i][j] * scale : -INFINITY;
                 mx = fmaxf(mx, s[i][j]);
             }
@@ -742,7 +752,7 @@ bwd_sm_query_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restric
             const float r = m[i] == -INFINITY ? 0.f : expf(m[i] - basev);
             float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const float e = expf(s[i][j] - basev);
                 sum += e;
                 Ps[(ty + 16 * i) * kLP + tx + 16 * j] = e;
@@ -753,7 +763,17 @@ bwd_sm_query_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restric
             for (int c = 0; c < NC; ++c) O[i][c] *= r;
         }
         __syncthreads();
-        mm_ab<D>(Ps, Vs, ty, tx, O);
+        mm_ab<D, 16 * NJ>(Ps, Vs, ty, tx, O);
+    };
+    for (int t = 0; t < n_tiles; ++t) {
+        int64_t j0;
+        int nk;
+        tile(t, &j0, &nk);
+        load_kv(j0, nk);
+        if (nk <= 16)
+            pass1(std::integral_constant<int, 1>{}, j0, nk);
+        else
+            pass1(std::integral_constant<int, 4>{}, j0, nk);
     }
     float Dp[4];
 #pragma unroll
@@ -777,19 +797,15 @@ bwd_sm_query_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restric
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < NC; ++c) dq[i][c] = 0.f;
-    for (int t = 0; t < n_tiles; ++t) {
-        int64_t j0;
-        int nk;
-        tile(t, &j0, &nk);
-        const bool sink = t < n_sink_tiles;
-        load_kv(j0, nk);
+    auto pass2 = [&](auto nj, int64_t j0, int nk, bool sink) {
+        constexpr int NJ = decltype(nj)::value;
         float s[4][4] = {}, dp[4][4] = {};
-        mm_abT<D>(Qs, Ks, ty, tx, s);
-        mm_abT<D>(dOs, Vs, ty, tx, dp);
+        mm_abT<D, NJ>(Qs, Ks, ty, tx, s);
+        mm_abT<D, NJ>(dOs, Vs, ty, tx, dp);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const int row = ty + 16 * i, col = tx + 16 * j;
                 const bool vis = sm_on && visible(row, col, j0, nk);
                 const float P = vis ? expf(s[i][j] * scale - m[i]) / l[i] : 0.f;
@@ -801,28 +817,39 @@ bwd_sm_query_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restric
                 }
             }
         __syncthreads();
-        mm_ab<D>(dSs, Ks, ty, tx, dq);
-        if (sink) {
-            float pk[4][NC], pv[4][NC];
+        mm_ab<D, 16 * NJ>(dSs, Ks, ty, tx, dq);
+        if (sink) {  // the block's partial sums for the sink keys (rows of the transposed tiles)
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                float acc[4][NC];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int c = 0; c < NC; ++c) pk[i][c] = pv[i][c] = 0.f;
-            mm_ab<D>(Ts, Qs, ty, tx, pk);
-            mm_ab<D>(Ps, dOs, ty, tx, pv);
+                    for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
+                mm_ab<D, kSB, NJ>(which ? Ps : Ts, which ? dOs : Qs, ty, tx, acc);
+                float* dst = which ? sink_v : sink_k;
+                const float f = which ? 1.f : scale;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int key = ty + 16 * i;
-                if (key < nk) {
-                    const size_t o = (((size_t)b * L.Hq + h) * ns + j0 + key) * D;
+                for (int i = 0; i < NJ; ++i) {
+                    const int key = ty + 16 * i;
+                    if (key < nk) {
+                        const size_t o = (((size_t)b * L.Hq + h) * ns + j0 + key) * D;
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        sink_k[o + sm_col(tx, c)] = pk[i][c] * scale;
-                        sink_v[o + sm_col(tx, c)] = pv[i][c];
+                        for (int c = 0; c < NC; ++c) dst[o + sm_col(tx, c)] = acc[i][c] * f;
                     }
                 }
             }
         }
+    };
+    for (int t = 0; t < n_tiles; ++t) {
+        int64_t j0;
+        int nk;
+        tile(t, &j0, &nk);
+        load_kv(j0, nk);
+        if (nk <= 16)
+            pass2(std::integral_constant<int, 1>{}, j0, nk, t < n_sink_tiles);
+        else
+            pass2(std::integral_constant<int, 4>{}, j0, nk, t < n_sink_tiles);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
