@@ -95,9 +95,16 @@ bwd_conv_kernel(LayerDims L, const Tin* __restrict__ v, const float* __restrict_
         const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
         const int H = kind == 0 ? L.Hq : L.Hkv;
         const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + (size_t)hh * D * kConvWidth;
-        float acc[E];
+        float acc[E], wt[E][kConvWidth];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (int e = 0; e < E; ++e) {
+            acc[e] = 0.f;
+            const float4* w4 = reinterpret_cast<const float4*>(w + (size_t)(lane + 32 * e) * kConvWidth);
+            const float4 a = w4[0], b = w4[1];
+            wt[e][0] = a.x; wt[e][1] = a.y; wt[e][2] = a.z; wt[e][3] = a.w;
+            wt[e][4] = b.x; wt[e][5] = b.y; wt[e][6] = b.z; wt[e][7] = b.w;
+        }
+#pragma unroll
         for (int m = 0; m < kConvWidth; ++m) {
             const int64_t pp = p - (kConvWidth - 1) + m;
             if (pp < 0) continue;
@@ -106,7 +113,7 @@ bwd_conv_kernel(LayerDims L, const Tin* __restrict__ v, const float* __restrict_
             for (int e = 0; e < E; ++e) {
                 const int c = lane + 32 * e;
                 const float x = kind == 0 ? qr[row + c] : kind == 1 ? kr[row + c] : to_f32(v[row + c]);
-                acc[e] = fmaf(w[c * kConvWidth + m], x, acc[e]);
+                acc[e] = fmaf(wt[e][m], x, acc[e]);
             }
         }
         const size_t o = ((size_t)t * H + hh) * D;
@@ -947,8 +954,8 @@ bwd_sm_key_kernel(LayerDims L, const Tin* __restrict__ v, const Tin* __restrict_
     }
 }
 
-// Sink keys: CTA per (sequence, q-head), thread per channel; the sums over the sequence's query blocks
-// (those whose last query is at or after the key) of the partials.
+// Sink keys: CTA per (sequence, q-head, sink key), thread per channel; the sums over the sequence's query
+// blocks (those whose last query is at or after the key) of the partials, in four interleaved chains.
 __global__ void bwd_sm_sink_kernel(LayerDims L, const int32_t* __restrict__ cu, const int32_t* __restrict__ base,
                                    int n_blk, const float* __restrict__ sink_k, const float* __restrict__ sink_v,
                                    float* __restrict__ dkr_h, float* __restrict__ dv_h) {
@@ -956,17 +963,18 @@ __global__ void bwd_sm_sink_kernel(LayerDims L, const int32_t* __restrict__ cu, 
     int64_t start, len;
     seq_range(cu, n, L.total, &start, &len);
     const int b0 = __ldg(base + n), nb = (int)((len + kSB - 1) / kSB);
-    for (int64_t j = 0; j < min((int64_t)ns, len); ++j) {
-        float sk = 0.f, sv = 0.f;
-        for (int qb = 0; qb < nb && b0 + qb < n_blk; ++qb) {
-            if (j > min(len, (int64_t)(qb + 1) * kSB) - 1) continue;
+    for (int j = blockIdx.z; j < min((int64_t)ns, len); j += gridDim.z) {
+        const int qb_lo = j / kSB;  // blocks whose last query is before key j see nothing of it
+        const int qb_hi = min(nb, n_blk - b0);
+        float sk[4] = {0.f, 0.f, 0.f, 0.f}, sv[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int qb = qb_lo; qb < qb_hi; ++qb) {
             const size_t o = (((size_t)(b0 + qb) * L.Hq + h) * ns + j) * D + c;
-            sk += sink_k[o];
-            sv += sink_v[o];
+            sk[qb & 3] += sink_k[o];
+            sv[qb & 3] += sink_v[o];
         }
         const size_t o = ((size_t)(start + j) * L.Hq + h) * D + c;
-        dkr_h[o] = sk;
-        dv_h[o] = sv;
+        dkr_h[o] = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+        dv_h[o] = (sv[0] + sv[1]) + (sv[2] + sv[3]);
     }
 }
 
@@ -1047,17 +1055,21 @@ bwd_feat_out_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __
         const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
         const int H = kind == 0 ? L.Hq : L.Hkv;
         const float* w = kind == 0 ? wq : kind == 1 ? wk : wv;
-        const float* w1 = w + ((size_t)hh * D + i) * kConvWidth;
-        const float* w2 = w + ((size_t)hh * D + i + half) * kConvWidth;
+        const float4* w1 = reinterpret_cast<const float4*>(w + ((size_t)hh * D + i) * kConvWidth);
+        const float4* w2 = reinterpret_cast<const float4*>(w + ((size_t)hh * D + i + half) * kConvWidth);
+        const float4 w1a = w1[0], w1b = w1[1], w2a = w2[0], w2b = w2[1];
+        const float t1[kConvWidth] = {w1a.x, w1a.y, w1a.z, w1a.w, w1b.x, w1b.y, w1b.z, w1b.w};
+        const float t2[kConvWidth] = {w2a.x, w2a.y, w2a.z, w2a.w, w2b.x, w2b.y, w2b.z, w2b.w};
         const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
         // x_p feeds y_{p + 7 - m} through tap m
         float a1 = 0.f, a2 = 0.f;
+#pragma unroll
         for (int m = 0; m < kConvWidth; ++m) {
             const int64_t pp = p + (kConvWidth - 1) - m;
             if (pp >= len) continue;
             const float* yr = dy + ((size_t)(start + pp) * H + hh) * D;
-            a1 = fmaf(w1[m], yr[i], a1);
-            a2 = fmaf(w2[m], yr[i + half], a2);
+            a1 = fmaf(t1[m], yr[i], a1);
+            a2 = fmaf(t2[m], yr[i + half], a2);
         }
         // the softmax branch's gradient of the RoPE'd row (q, k) or of raw v, summed over the group for k, v
         if (kind == 0) {
@@ -1083,35 +1095,56 @@ bwd_feat_out_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __
     }
 }
 
-// ---- 6. conv filters: partial sums over a block of kWB tokens, per (row, channel, tap); then the blocks
+// ---- 6. conv filters: partial sums over a block of kWB tokens, per (row, channel, tap); then the blocks.
+// A thread walks its channel through the block's tokens with the last 8 inputs of the sequence in
+// registers (zeros before the sequence start), so every input is read once.
 template <typename Tin>
 __global__ void bwd_convw_part_kernel(LayerDims L, const Tin* __restrict__ v, const int32_t* __restrict__ cu,
                                       const float* __restrict__ qr, const float* __restrict__ kr,
                                       const float* __restrict__ dqt, const float* __restrict__ dkt,
                                       const float* __restrict__ dvt, float* __restrict__ part) {
+    __shared__ int32_t pos_s[kWB];  // position of each token of the block in its sequence
     const int blk = blockIdx.x, r = blockIdx.y, c = threadIdx.x, D = L.d;
     const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
     const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
     const int H = kind == 0 ? L.Hq : L.Hkv;
     const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
-    float acc[kConvWidth];
-#pragma unroll
-    for (int m = 0; m < kConvWidth; ++m) acc[m] = 0.f;
     const int64_t t0 = (int64_t)blk * kWB, t1 = min(L.total, t0 + kWB);
-    for (int64_t t = t0; t < t1; ++t) {
-        const int n = seq_of_token(cu, L.n_seqs, t);
+    for (int64_t t = t0 + c; t < t1; t += blockDim.x) {
         int64_t start, len;
-        seq_range(cu, n, L.total, &start, &len);
-        const int64_t p = t - start;
+        seq_range(cu, seq_of_token(cu, L.n_seqs, t), L.total, &start, &len);
+        pos_s[t - t0] = (int32_t)min(t - start, (int64_t)INT32_MAX);
+    }
+    __syncthreads();
+    auto input = [&](int64_t t) {
+        const size_t row = ((size_t)t * H + hh) * D + c;
+        return kind == 0 ? qr[row] : kind == 1 ? kr[row] : to_f32(v[row]);
+    };
+    float acc[kConvWidth], win[kConvWidth];  // win[m]: the input at position p - 7 + m
+#pragma unroll
+    for (int m = 0; m < kConvWidth; ++m) acc[m] = win[m] = 0.f;
+    // the window before the block's first token
+    if (t1 > t0) {
+        const int p0 = pos_s[0];
+#pragma unroll
+        for (int m = 1; m < kConvWidth; ++m) {
+            const int back = kConvWidth - m;  // position p0 - back sits at win[m - 1] before the shift
+            win[m] = back <= p0 ? input(t0 - back) : 0.f;
+        }
+    }
+    for (int64_t t = t0; t < t1; ++t) {
+        const int p = pos_s[t - t0];
+        if (p == 0) {  // a sequence starts: nothing before it
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) win[m] = 0.f;
+        } else {
+#pragma unroll
+            for (int m = 0; m + 1 < kConvWidth; ++m) win[m] = win[m + 1];
+        }
+        win[kConvWidth - 1] = input(t);
         const float d_y = dy[((size_t)t * H + hh) * D + c];
 #pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) {
-            const int64_t pp = p - (kConvWidth - 1) + m;
-            if (pp < 0) continue;
-            const size_t row = ((size_t)(start + pp) * H + hh) * D + c;
-            const float x = kind == 0 ? qr[row] : kind == 1 ? kr[row] : to_f32(v[row]);
-            acc[m] = fmaf(d_y, x, acc[m]);
-        }
+        for (int m = 0; m < kConvWidth; ++m) acc[m] = fmaf(d_y, win[m], acc[m]);
     }
     const int rows = L.Hq + 2 * L.Hkv;
 #pragma unroll
@@ -1230,7 +1263,8 @@ cudaError_t launch_sm_bwd(const LayerDims& L, const Tin* v, const Tin* dout, con
     bwd_sm_key_kernel<Tin, D><<<dim3(n_blk, L.Hq), kSmThreads, bk, st>>>(L, v, dout, cu, base, qr, kr, stats, dkr_h,
                                                                          dv_h);
     if (L.n_sinks > 0)
-        bwd_sm_sink_kernel<<<dim3(L.n_seqs, L.Hq), D, 0, st>>>(L, cu, base, n_blk, sink_k, sink_v, dkr_h, dv_h);
+        bwd_sm_sink_kernel<<<dim3(L.n_seqs, L.Hq, min(L.n_sinks, 64)), D, 0, st>>>(L, cu, base, n_blk, sink_k, sink_v,
+                                                                                 dkr_h, dv_h);
     return cudaGetLastError();
 }
 

@@ -164,17 +164,28 @@ gdn_recurrent_kernel(LayerDims L, const Tf* __restrict__ qhat, const Tf* __restr
 }
 
 // The scan over a sequence's parts, for 8 value columns of one q-head: S_0 = 0, S_{i+1} = P_i S_i + R_i
-// (fp32, fixed order) into s_part for parts 1 ..; a sequence without parts gets S_out = 0 here.
+// (fp32, fixed order) into s_part for parts 1 ..; a sequence without parts gets S_out = 0 here.  P_{i+1}
+// and the columns of R_{i+1} are copied into shared memory (cp.async) while step i computes.
+constexpr int kScanThreads = 256;
+template <int D> constexpr size_t scan_smem_bytes() { return (size_t)(2 * D * (D + 4) + 2 * D * 8 + D * 8) * 4; }
+
+__device__ __forceinline__ void scan_cp16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src) : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kScanThreads)
 gdn_part_scan_kernel(LayerDims L, RecScan rs, float* __restrict__ S_out) {
-    constexpr int TPR = 256 / D, CPT = 8 / TPR;  // threads per row, columns per thread
-    __shared__ __align__(16) float Ss[D][8];
+    constexpr int TPR = kScanThreads / D, CPT = 8 / TPR, LDP = D + 4;  // threads per row, columns per thread
+    extern __shared__ __align__(16) float scan_sm[];
+    float* Pb = scan_sm;                 // [2][D][LDP]
+    float* Rb = Pb + 2 * D * LDP;        // [2][D][8]
+    float* Ss = Rb + 2 * D * 8;          // [D][8]
     const int h = blockIdx.x / (D / 8), cg = blockIdx.x % (D / 8), n = blockIdx.y, tid = threadIdx.x;
     const int r = tid / TPR, c0 = (tid % TPR) * CPT;
     const int b0 = __ldg(rs.base + n), np = __ldg(rs.base + n + 1) - b0;
-    for (int idx = tid; idx < D * 8; idx += 256) Ss[idx / 8][idx % 8] = 0.f;
-    __syncthreads();
+    for (int idx = tid; idx < D * 8; idx += kScanThreads) Ss[idx] = 0.f;
     if (np <= 0) {
         if (S_out) {
             float* dst = S_out + (((size_t)n * L.Hq + h) * D + r) * D + cg * 8 + c0;
@@ -183,28 +194,49 @@ gdn_part_scan_kernel(LayerDims L, RecScan rs, float* __restrict__ S_out) {
         }
         return;
     }
-    for (int i = 0; i + 1 < np; ++i) {
+    auto fetch = [&](int i) {  // P_i and R_i's 8 columns into buffer i & 1
         const float* R = rs.pr + (((size_t)(b0 + i) * L.Hq + h) * 2 + 0) * D * D;
         const float* P = rs.pr + (((size_t)(b0 + i) * L.Hq + h) * 2 + 1) * D * D;
+        float* pb = Pb + (i & 1) * D * LDP;
+        float* rb = Rb + (i & 1) * D * 8;
+        for (int idx = tid; idx < D * D / 4; idx += kScanThreads) {
+            const int row = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+            scan_cp16(pb + row * LDP + c4, P + (size_t)row * D + c4);
+        }
+        for (int idx = tid; idx < D * 2; idx += kScanThreads) {
+            const int row = idx / 2, c4 = (idx % 2) * 4;
+            scan_cp16(rb + row * 8 + c4, R + (size_t)row * D + cg * 8 + c4);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (np > 1) fetch(0);
+    for (int i = 0; i + 1 < np; ++i) {
+        if (i + 2 < np) {
+            fetch(i + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();  // P_i, R_i and the previous step's S are visible
+        const float* pr = Pb + (i & 1) * D * LDP + r * LDP;
+        const float* rb = Rb + (i & 1) * D * 8 + r * 8;
         float acc[CPT];
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) acc[c] = R[(size_t)r * D + cg * 8 + c0 + c];
-        const float4* Pr = reinterpret_cast<const float4*>(P + (size_t)r * D);
+        for (int c = 0; c < CPT; ++c) acc[c] = rb[c0 + c];
 #pragma unroll 4
         for (int k4 = 0; k4 < D / 4; ++k4) {
-            const float4 p = Pr[k4];
+            const float4 p = *reinterpret_cast<const float4*>(pr + 4 * k4);
 #pragma unroll
             for (int c = 0; c < CPT; ++c) {
-                acc[c] = fmaf(p.x, Ss[4 * k4 + 0][c0 + c], acc[c]);
-                acc[c] = fmaf(p.y, Ss[4 * k4 + 1][c0 + c], acc[c]);
-                acc[c] = fmaf(p.z, Ss[4 * k4 + 2][c0 + c], acc[c]);
-                acc[c] = fmaf(p.w, Ss[4 * k4 + 3][c0 + c], acc[c]);
+                acc[c] = fmaf(p.x, Ss[(4 * k4 + 0) * 8 + c0 + c], acc[c]);
+                acc[c] = fmaf(p.y, Ss[(4 * k4 + 1) * 8 + c0 + c], acc[c]);
+                acc[c] = fmaf(p.z, Ss[(4 * k4 + 2) * 8 + c0 + c], acc[c]);
+                acc[c] = fmaf(p.w, Ss[(4 * k4 + 3) * 8 + c0 + c], acc[c]);
             }
         }
-        __syncthreads();
+        __syncthreads();  // every thread has read S_i (and this buffer) before they change
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) Ss[r][c0 + c] = acc[c];
-        __syncthreads();
+        for (int c = 0; c < CPT; ++c) Ss[r * 8 + c0 + c] = acc[c];
         float* dst = rs.s_part + ((size_t)(b0 + i + 1) * L.Hq + h) * D * D + (size_t)r * D + cg * 8 + c0;
 #pragma unroll
         for (int c = 0; c < CPT; ++c) dst[c] = acc[c];
@@ -229,10 +261,20 @@ cudaError_t launch_gdn_recurrent(const LayerDims& L, const Tf* qhat, const Tf* k
     }
     if (rs->part_len <= 0 || rs->n_parts <= 0 || rs->n_parts > 65535) return cudaErrorInvalidValue;
     run(dim3(L.Hq, rs->n_parts, 2), kRecMap);
+    static DeviceCache cache;  // the scan's shared-memory attribute, per device
+    cudaError_t e = device_cached(cache, nullptr, [](int, int*) {
+        cudaError_t r = cudaFuncSetAttribute(gdn_part_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)scan_smem_bytes<128>());
+        return r == cudaSuccess ? cudaFuncSetAttribute(gdn_part_scan_kernel<64>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)scan_smem_bytes<64>())
+                                : r;
+    });
+    if (e != cudaSuccess) return e;
     if (D == 128)
-        gdn_part_scan_kernel<128><<<dim3(L.Hq * 16, L.n_seqs), 256, 0, st>>>(L, *rs, S_out);
+        gdn_part_scan_kernel<128><<<dim3(L.Hq * 16, L.n_seqs), kScanThreads, scan_smem_bytes<128>(), st>>>(L, *rs, S_out);
     else
-        gdn_part_scan_kernel<64><<<dim3(L.Hq * 8, L.n_seqs), 256, 0, st>>>(L, *rs, S_out);
+        gdn_part_scan_kernel<64><<<dim3(L.Hq * 8, L.n_seqs), kScanThreads, scan_smem_bytes<64>(), st>>>(L, *rs, S_out);
     run(dim3(L.Hq, rs->n_parts), kRecPart);
     return cudaGetLastError();
 }
