@@ -257,14 +257,26 @@ HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q,
  * of decoding the new tokens one at a time).  A state that never passed
  * through hla_state_init starts from whatever its buffers hold; pos < 0 is
  * flagged in the state's error word (HLA_ERR_STATE) and that sequence is left
- * as it is.  Token-serial inside each sequence (one CTA per query head), a
- * path for prompts appended to live sequences, not the throughput path of a
- * fresh prefill.  ws as for hla_prefill.  Asynchronous; no allocation. */
+ * as it is (its output rows are undefined).  ws, ws_bytes: a workspace of at
+ * least hla_prefill_continue_workspace_bytes bytes (its error word as for
+ * hla_prefill).  On the tensor-core path (bf16, head_dim 128, 1, 2, 4 or 8
+ * query heads per kv head) each sequence's cached sinks and window are laid
+ * in front of its new tokens, the positions between them left out, and the
+ * prefill's softmax and chunked GDN kernels run on these rows from the cached
+ * S; the other layers take a token-serial path (one CTA per query head).
+ * Asynchronous; no allocation. */
 HLA_API int hla_prefill_continue(const hla_params* params, const void* q, const void* k, const void* v,
                                  const float* g, const float* beta, const float* lambda,
                                  const float* conv_wq, const float* conv_wk, const float* conv_wv,
                                  const int32_t* cu_seqlens, int n_seqs, int64_t total_tokens, void* out,
                                  const hla_state* st, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes hla_prefill_continue needs for total_tokens new tokens in
+ * n_seqs sequences (host only): on the tensor-core path the prefill's
+ * workspace for the new tokens plus every sequence's n_sinks + window cached
+ * rows, and the extended rows' v, g, beta and output. */
+HLA_API int hla_prefill_continue_workspace_bytes(const hla_params* params, int64_t total_tokens, int n_seqs,
+                                                 size_t* bytes);
 
 /* Component-usage diagnostics of a prefill (synthetic analysis; not part of
  * the layer's output path).  Arguments as for hla_prefill, without a decode

@@ -112,7 +112,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
                    const int32_t* __restrict__ chunk_base, int slot_lo, int slot_hi,
                    const unsigned char* __restrict__ rec_in, const __half* __restrict__ o_sm,
                    const float* __restrict__ lambda, __nv_bfloat16* __restrict__ out,
-                   const float* __restrict__ S_in, float* __restrict__ S_out, int32_t* __restrict__ err) {
+                   const float* __restrict__ S_in, const float* __restrict__ S_init, float* __restrict__ S_out,
+                   int32_t* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     // A launch that follows this one with programmatic stream serialization (the next part's chunk-local
     // kernel) may start as soon as every CTA of this grid has reached this point, i.e. is resident, even
@@ -162,7 +163,9 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     // loop index c = chunk - c_lo
     const int c_lo = min(max(slot_lo - slot0, 0), seq_chunks);
     const int n_chunks = min(max(slot_hi - slot0, 0), seq_chunks) - c_lo;
-    const bool resume = S_in && c_lo > 0;  // continue from the state the previous launch left
+    // continue from the state the previous launch left, or (a sequence's first chunks) from S_init
+    const float* S_src = c_lo > 0 ? S_in : S_init;
+    const bool resume = S_src != nullptr;
 
     // The stall test hook: the loader issues nothing, so every wait below runs out (after a millisecond
     // instead of the usual two seconds) and the kernel reports a timeout without any copy or MMA in flight.
@@ -202,7 +205,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 #pragma unroll
         for (int i = 0; i < kNS; ++i) S[i] = 0.f;
         if (resume) {  // the saved state and its fp16 image (the zero image above is overwritten)
-            const float* src = S_in + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
+            const float* src = S_src + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
 #pragma unroll
             for (int i = 0; i < kNS; i += 4) {
                 const float4 x = *reinterpret_cast<const float4*>(src + i);
@@ -382,8 +385,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
                                const unsigned char* rec_in, const __half* o_sm, const float* lambda,
-                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, bool beside_prior,
-                               cudaStream_t st) {
+                               __nv_bfloat16* out, const float* S_in, const float* S_init, float* S_out, int32_t* err,
+                               bool beside_prior, cudaStream_t st) {
     static DeviceCache cache;  // the shared-memory attribute, per device
     cudaError_t e = device_cached(cache, nullptr, [](int, int*) {
         return cudaFuncSetAttribute(gdn_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
@@ -398,7 +401,7 @@ cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __h
         return cudaErrorInvalidValue;
     LaunchCfg lc(dim3(L.Hq * kSlices, L.n_seqs), dim3(kThreads), kSmemAlloc, st, beside_prior);
     return cudaLaunchKernelEx(&lc.cfg, gdn_chunked_kernel, L, mq, mk, mv, cu, chunk_base, slot_lo, slot_hi, rec_in, o_sm,
-                              lambda, out, S_in, S_out, err);
+                              lambda, out, S_in, S_init, S_out, err);
 }
 
 }  // namespace hla

@@ -114,6 +114,34 @@ WsLayout ws_layout(const hla_params* prm, int64_t total, int n_seqs) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HLA_OK : HLA_ERR_CUDA; }
 
+// Workspace of a continuation on the tensor-core path: the prefill layout for the extended rows
+// (every sequence's cached sinks and window in front of its new tokens; this bounds them), then the
+// extended sequence table and the extended v, g, beta and output.
+struct ContLayout {
+    WsLayout w;
+    int64_t ext_bound;
+    size_t ext_cu, ev, eg, eb, eo, total;
+};
+bool continue_on_tensor_cores(const hla_params* prm) { return uses_chunked_gdn(prm); }
+ContLayout cont_layout(const hla_params* prm, int64_t total, int n_seqs) {
+    ContLayout c;
+    c.ext_bound = total + (int64_t)n_seqs * (prm->n_sinks + prm->window);
+    c.w = ws_layout(prm, c.ext_bound, n_seqs);
+    const size_t X = (size_t)c.ext_bound, Hq = (size_t)prm->n_q_heads, Hkv = (size_t)prm->n_kv_heads;
+    const size_t d = (size_t)prm->head_dim;
+    size_t off = c.w.total;
+    c.ext_cu = off; off = align_up(off + ((size_t)n_seqs + 1) * sizeof(int32_t));
+    c.ev = off;     off = align_up(off + X * Hkv * d * sizeof(__nv_bfloat16));
+    c.eg = off;     off = align_up(off + X * Hq * sizeof(float));
+    c.eb = off;     off = align_up(off + X * Hq * sizeof(float));
+    c.eo = off;     off = align_up(off + X * Hq * d * sizeof(__nv_bfloat16));
+    c.total = off;
+    return c;
+}
+size_t continue_workspace_bytes(const hla_params* prm, int64_t total, int n_seqs) {
+    return continue_on_tensor_cores(prm) ? cont_layout(prm, total, n_seqs).total : ws_layout(prm, total, n_seqs).total;
+}
+
 // Parts of the chunk slots the chunked GDN runs in (1 .. kMaxGdnParts).
 constexpr int kGdnParts = 2;
 static_assert(kGdnParts >= 1 && kGdnParts <= kMaxGdnParts, "GDN parts");
@@ -218,8 +246,8 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
                 HLA_TRY(mark_stage(8 + 4 * p, stream));
                 HLA_TRY(mark_stage(9 + 4 * p, stream));
                 HLA_TRY(launch_gdn_chunked(L, qh, kh, vh, cu, chunk_base, bound[p], bound[p + 1], rec, osm, lambda, o,
-                                           p > 0 ? smid : nullptr, p + 1 < kGdnParts ? smid : S_out, err, overlap,
-                                           stream));
+                                           p > 0 ? smid : nullptr, nullptr, p + 1 < kGdnParts ? smid : S_out, err,
+                                           overlap, stream));
                 HLA_TRY(mark_stage(10 + 4 * p, stream));
             }
             for (int p = kGdnParts; p < kMaxGdnParts; ++p)  // absent parts: zero-length marks
@@ -238,6 +266,56 @@ int run_prefill(const hla_params* prm, const LayerDims& L, const void* q, const 
     HLA_TRY(mark_stage(5, stream));
     if (st) HLA_TRY(launch_state_fill<Tin, Tf>(L, qi, ki, vi, g, beta, kh, vh, cu, *st, stream));
     HLA_TRY(mark_stage(6, stream));
+    return HLA_OK;
+}
+
+// Continuation on the tensor-core path: the prefill's kernels on the extended rows (see continue_tc.cu).
+int run_continue_tc(const hla_params* prm, const LayerDims& L, const void* q, const void* k, const void* v,
+                    const float* g, const float* beta, const float* lambda, const float* wq, const float* wk,
+                    const float* wv, const int32_t* cu, void* out, const hla_state* st, char* ws, const ContLayout& c,
+                    cudaStream_t stream) {
+    const WsLayout& w = c.w;
+    const LayerDims Lx = make_dims(prm, L.n_seqs, c.ext_bound);
+    int32_t* err = reinterpret_cast<int32_t*>(ws + w.err);
+    int32_t* ext_cu = reinterpret_cast<int32_t*>(ws + c.ext_cu);
+    __half* qr = reinterpret_cast<__half*>(ws + w.qr);
+    __half* kr = reinterpret_cast<__half*>(ws + w.kr);
+    __half* qh = reinterpret_cast<__half*>(ws + w.qhat);
+    __half* kh = reinterpret_cast<__half*>(ws + w.khat);
+    __half* vh = reinterpret_cast<__half*>(ws + w.vhat);
+    __nv_bfloat16* ev = reinterpret_cast<__nv_bfloat16*>(ws + c.ev);
+    float* eg = reinterpret_cast<float*>(ws + c.eg);
+    float* eb = reinterpret_cast<float*>(ws + c.eb);
+    __nv_bfloat16* eo = reinterpret_cast<__nv_bfloat16*>(ws + c.eo);
+    __half* osm = reinterpret_cast<__half*>(ws + w.osm);
+    int32_t* blk_base = reinterpret_cast<int32_t*>(ws + w.blk_base);
+    int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
+    int32_t* counters = reinterpret_cast<int32_t*>(ws + w.counters);
+    unsigned char* rec = reinterpret_cast<unsigned char*>(ws + w.tinv);
+    float* smid = reinterpret_cast<float*>(ws + w.smid);
+    const __nv_bfloat16* qi = static_cast<const __nv_bfloat16*>(q);
+    const __nv_bfloat16* ki = static_cast<const __nv_bfloat16*>(k);
+    const __nv_bfloat16* vi = static_cast<const __nv_bfloat16*>(v);
+    HLA_TRY(launch_continue_table(L, cu, *st, ext_cu, stream));
+    PrefillTables tabs = {ext_cu, err, counters, kGdnParts, blk_base, window_softmax_tc_rows(Lx), chunk_base,
+                          kGdnChunk, nullptr, nullptr};
+    HLA_TRY(launch_prefill_tables(Lx, reinterpret_cast<float2*>(ws + w.fine), reinterpret_cast<float2*>(ws + w.coarse),
+                                  w.n_coarse, tabs, stream));
+    HLA_TRY(launch_continue_rows(L, Lx, cu, *st, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb, qi, ki, vi, g, beta, wq, wk,
+                                 wv, stream));
+    HLA_TRY(launch_window_softmax_tc(Lx, qr, kr, ev, ext_cu, blk_base, osm, eo, err, false, stream));
+    const int n_slots = (int)gdn_chunk_slots(Lx.total, Lx.n_seqs);
+    int bound[kGdnParts + 1];
+    for (int p = 0; p <= kGdnParts; ++p) bound[p] = (int)((int64_t)n_slots * p / kGdnParts);
+    for (int p = 0; p < kGdnParts; ++p) {
+        HLA_TRY(launch_gdn_inverse(Lx, qh, kh, eg, eb, ext_cu, chunk_base, bound[p], bound[p + 1], counters + p, rec,
+                                   err, true, stream));
+        HLA_TRY(launch_gdn_chunked(Lx, qh, kh, vh, ext_cu, chunk_base, bound[p], bound[p + 1], rec, osm, lambda, eo,
+                                   p > 0 ? smid : nullptr, st->S, p + 1 < kGdnParts ? smid : st->S, err, true,
+                                   stream));
+    }
+    HLA_TRY(launch_continue_finish(L, cu, *st, ext_cu, eo, static_cast<__nv_bfloat16*>(out), qi, ki, vi, g, beta, kh,
+                                   vh, stream));
     return HLA_OK;
 }
 
@@ -424,12 +502,19 @@ HLA_API int hla_prefill_continue(const hla_params* prm, const void* q, const voi
         if (!ptrs[i] || !aligned16(ptrs[i])) return HLA_ERR_INVALID_ARG;
     }
     if (!state_ok(st)) return HLA_ERR_INVALID_ARG;
+    if (ws_bytes < continue_workspace_bytes(prm, total_tokens, n_seqs)) return HLA_ERR_WORKSPACE;
     const WsLayout w = ws_layout(prm, total_tokens, n_seqs);
-    if (ws_bytes < w.total) return HLA_ERR_WORKSPACE;
     if (total_tokens == 0) return HLA_OK;  // nothing appended; the state is unchanged
     const LayerDims L = make_dims(prm, n_seqs, total_tokens);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* wsb = static_cast<char*>(ws);
+    if (continue_on_tensor_cores(prm)) {
+        const ContLayout c = cont_layout(prm, total_tokens, n_seqs);
+        if (c.ext_bound > (int64_t)INT32_MAX) return HLA_ERR_UNSUPPORTED;
+        HLA_TRY(cudaMemsetAsync(wsb + w.err, 0, 16, s));
+        return run_continue_tc(prm, L, q, k, v, g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, out, st, wsb,
+                               c, s);
+    }
     if (prm->dtype == HLA_DTYPE_F32)
         return cuda_status(launch_prefill_continue<float, float>(
             L, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), g, beta,
@@ -441,6 +526,15 @@ HLA_API int hla_prefill_continue(const hla_params* prm, const void* q, const voi
         static_cast<const __nv_bfloat16*>(v), g, beta, lambda, conv_wq, conv_wk, conv_wv, cu_seqlens, *st,
         reinterpret_cast<__half*>(wsb + w.kr), reinterpret_cast<__half*>(wsb + w.khat),
         reinterpret_cast<__half*>(wsb + w.vhat), static_cast<__nv_bfloat16*>(out), s));
+}
+
+HLA_API int hla_prefill_continue_workspace_bytes(const hla_params* prm, int64_t total_tokens, int n_seqs,
+                                                 size_t* bytes) {
+    int rc = check_params(prm);
+    if (rc) return rc;
+    if (total_tokens < 0 || n_seqs < 0 || !bytes) return HLA_ERR_INVALID_ARG;
+    *bytes = continue_workspace_bytes(prm, total_tokens, n_seqs);
+    return HLA_OK;
 }
 
 HLA_API int hla_prefill_diagnostics(const hla_params* prm, const void* q, const void* k, const void* v,

@@ -270,7 +270,8 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
                                cudaStream_t st);
 // The chunks of slots [slot_lo, slot_hi) of every sequence, continuing from
 // S_in (fp32 [n_seqs][Hq][d][d]; read only for sequences with chunks before
-// slot_lo, zero state otherwise; may be null if none has).  out rows of
+// slot_lo; may be null if none has), a sequence's first chunks from S_init
+// (same layout; null: the zero state).  out rows of
 // positions >= n_sinks + W of those chunks: bf16(o_sm + lambda_h o_lin) (none
 // if out is null or the linear branch is switched off); the state after the
 // last chunk in range into S_out (may be null).  With beside_prior it is
@@ -280,8 +281,24 @@ cudaError_t launch_gdn_inverse(const LayerDims& L, const __half* qhat, const __h
 cudaError_t launch_gdn_chunked(const LayerDims& L, const __half* qhat, const __half* khat, const __half* vhat,
                                const int32_t* cu, const int32_t* chunk_base, int slot_lo, int slot_hi,
                                const unsigned char* rec_in, const __half* o_sm, const float* lambda,
-                               __nv_bfloat16* out, const float* S_in, float* S_out, int32_t* err, bool beside_prior,
-                               cudaStream_t st);
+                               __nv_bfloat16* out, const float* S_in, const float* S_init, float* S_out, int32_t* err,
+                               bool beside_prior, cudaStream_t st);
+
+// Tensor-core continuation (bf16, head_dim 128): the extended sequence table ext_cu [n_seqs + 1] from
+// the state's positions; the extended rows (cached rows from the state, new rows from the inputs) of the
+// RoPE'd q, k, qhat, khat, vhat (fp16), v (bf16), g, beta (fp32); then the new output rows into out and
+// the state (ring, pending ring, conv histories, pos).  L: the call's own dims (total = new tokens).
+cudaError_t launch_continue_table(const LayerDims& L, const int32_t* cu, const hla_state& s, int32_t* ext_cu,
+                                  cudaStream_t st);
+cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const int32_t* cu, const hla_state& s,
+                                 const int32_t* ext_cu, __half* qr, __half* kr, __half* qh, __half* kh, __half* vh,
+                                 __nv_bfloat16* ev, float* eg, float* eb, const __nv_bfloat16* q,
+                                 const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
+                                 const float* wq, const float* wk, const float* wv, cudaStream_t st);
+cudaError_t launch_continue_finish(const LayerDims& L, const int32_t* cu, const hla_state& s, const int32_t* ext_cu,
+                                   const __nv_bfloat16* ext_out, __nv_bfloat16* out, const __nv_bfloat16* q,
+                                   const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
+                                   const __half* kh, const __half* vh, cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>

@@ -90,6 +90,9 @@ def load():
         lib.hla_prefill_continue.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, S, _vp,
                                                                 ctypes.c_size_t, _vp]
         lib.hla_prefill_continue.restype = ctypes.c_int
+        lib.hla_prefill_continue_workspace_bytes.argtypes = [P, ctypes.c_int64, ctypes.c_int,
+                                                             ctypes.POINTER(ctypes.c_size_t)]
+        lib.hla_prefill_continue_workspace_bytes.restype = ctypes.c_int
         lib.hla_prefill_diagnostics.argtypes = [P] + [_vp] * 10 + [ctypes.c_int, ctypes.c_int64, _vp, _vp, _vp,
                                                                    _vp, ctypes.c_size_t, _vp]
         lib.hla_prefill_diagnostics.restype = ctypes.c_int
@@ -215,13 +218,20 @@ def prefill(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out, 
     return ws
 
 
+def continue_workspace_bytes(params: Params, total_tokens: int, n_seqs: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().hla_prefill_continue_workspace_bytes(ctypes.byref(params.c()), total_tokens, n_seqs,
+                                                       ctypes.byref(n)), "hla_prefill_continue_workspace_bytes")
+    return n.value
+
+
 def prefill_continue(params: Params, q, k, v, g, beta, lam, wq, wk, wv, cu_seqlens, out, state: State, ws=None,
                      stream=None):
     """hla_prefill_continue: appends the tokens of every sequence to the context `state` holds."""
     n_seqs = cu_seqlens.numel() - 1
     total = q.shape[0]
     if ws is None:
-        ws = alloc_workspace(params, total, n_seqs, q.device)
+        ws = torch.empty(continue_workspace_bytes(params, total, n_seqs), dtype=torch.uint8, device=q.device)
     rc = load().hla_prefill_continue(ctypes.byref(params.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                      _ptr(lam), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(cu_seqlens), n_seqs, total,
                                      _ptr(out), ctypes.byref(state.c), _ptr(ws), ws.numel(), _stream(stream))

@@ -4,8 +4,9 @@ the oracle's layer over the concatenated sequence (the continuation's rows and
 the final state), and decoding afterwards must go on as if the whole sequence
 had been one prefill.  Cases cover prefills shorter than the budget (ring not
 full), continuations that cross the start of absorption, varlen batches, a
-fresh state, two continuations in a row, the GLA variant, and the three
-layer types."""
+fresh state, two continuations in a row, the GLA variant, windows up to the
+decode budget (8 + 888), the tensor-core path (bf16, d 128, GQA 2/4/8) and the
+token-serial one."""
 import numpy as np
 import pytest
 import torch
@@ -60,7 +61,13 @@ def _inputs(wl, seqlens, seed):
 
 CASES = [
     # dtype, d, hq, hkv, n_sinks, window, first lengths, continuation lengths
+    # bf16 d128 (tensor-core path): GQA 2, 8 and 4; windows of 24, 56, 120 and 888; contexts shorter than
+    # the budget (no gap between sinks and window) and longer; continuations of 1 token to a few chunks
     ("bf16", 128, 4, 2, 8, 24, [10, 200, 0], [70, 5, 130]),
+    ("bf16", 128, 8, 1, 8, 56, [300, 1000], [64, 700]),
+    ("bf16", 128, 4, 1, 8, 120, [129, 2000, 0], [1, 300, 128]),
+    ("bf16", 128, 2, 1, 8, 888, [1000, 50], [500, 900]),
+    # token-serial path
     ("bf16", 64, 4, 1, 3, 40, [30, 100], [90, 1]),
     ("f32", 64, 2, 1, 8, 56, [512, 20], [100, 300]),
 ]
@@ -134,8 +141,9 @@ def test_continue_from_a_fresh_state_equals_prefill(oracle_mod):
     assert st.view("pos").cpu().tolist() == [300, 64, 7]
 
 
-def test_two_continuations_in_a_row(oracle_mod):
-    wl = synth.small("cont twice", [40], n_q_heads=2, n_kv_heads=1, head_dim=64, n_sinks=4, window=16)
+@pytest.mark.parametrize("d", [64, 128])
+def test_two_continuations_in_a_row(oracle_mod, d):
+    wl = synth.small("cont twice", [40], n_q_heads=2, n_kv_heads=1, head_dim=d, n_sinks=4, window=16)
     x1 = synth.make_inputs(wl, "cuda")
     x2 = _inputs(wl, [25], synth.BASE_SEED + 11)
     x3 = _inputs(wl, [33], synth.BASE_SEED + 12)
@@ -151,4 +159,29 @@ def test_two_continuations_in_a_row(oracle_mod):
         ref = _oracle(wl, parts, 0, h, oracle_mod)
         assert_close(_np(o2[:, h]), ref["o"][40:65], "bf16", f"second part head {h}")
         assert_close(_np(o3[:, h]), ref["o"][65:], "bf16", f"third part head {h}")
-        assert_close(st.view("S").view(1, 2, 64, 64)[0, h].cpu().numpy(), ref["S"], "bf16", f"S head {h}")
+        assert_close(st.view("S").view(1, 2, d, d)[0, h].cpu().numpy(), ref["S"], "bf16", f"S head {h}")
+
+
+def test_stale_workspace_contents_do_not_leak(oracle_mod):
+    """The same calls with a workspace full of non-finite bytes give the same bits as with a zeroed one: the
+    tensor-core kernels read whole tiles past a sequence's end, and those rows must be written or zeroed."""
+    wl = synth.small("cont stale", [300, 50], n_q_heads=4, n_kv_heads=1, head_dim=128, n_sinks=8, window=56)
+    x1 = synth.make_inputs(wl, "cuda")
+    x2 = _inputs(wl, [130, 7], synth.BASE_SEED + 33)
+    prm = params_for(wl)
+    outs = []
+    for fill in (0x00, 0xFF):
+        st = hla.State(prm, wl.n_seqs).init()
+        ws1 = torch.full((hla.workspace_bytes(prm, x1["q"].shape[0], wl.n_seqs),), fill, dtype=torch.uint8,
+                         device="cuda")
+        o1 = torch.empty_like(x1["q"])
+        hla.prefill(prm, *_args(x1), o1, state=st, ws=ws1)
+        ws2 = torch.full((hla.continue_workspace_bytes(prm, x2["q"].shape[0], wl.n_seqs),), fill, dtype=torch.uint8,
+                         device="cuda")
+        o2 = torch.empty_like(x2["q"])
+        hla.prefill_continue(prm, *_args(x2), o2, st, ws=ws2)
+        torch.cuda.synchronize()
+        outs.append((o1.clone(), o2.clone(), st.view("S").clone()))
+    for a, b in zip(*outs):
+        assert torch.isfinite(b.float()).all()
+        assert torch.equal(a, b)
