@@ -48,7 +48,8 @@ def parse():
                     help="approximate timed region of each further workload (steps derived from a trial)")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--scan", type=int, default=1,
-                    help="1: also time the context-parallel token-serial GDN on a long fp32 sequence")
+                    help="1: also time the context-parallel token-serial GDN on a long fp32 sequence and the "
+                         "prefill continuation (chunked prefill)")
     ap.add_argument("--backward", default="c1", choices=["", "c1", "c2", "c4"],
                     help="workload of the backward (hla_backward) measurement; empty to skip")
     ap.add_argument("--backward-seconds", type=float, default=2.0,
@@ -617,6 +618,49 @@ def run_scan_bench(dist, trial_seconds=0.5):
     return res
 
 
+def run_continue_bench(dist, steps=30, warmup=3):
+    """hla_prefill_continue on the LLaMA-3.1-8B-shaped layer: a 4096-token prefill with a decode state, then
+    chunks of 4096 tokens appended one after another (chunked prefill), each call timed with CUDA events
+    (L2 flushed between calls)."""
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.workloads()["c1"]
+    x0 = synth.make_inputs(wl, "cuda")
+    x1 = synth.make_inputs(synth.small("chunk", [4096], n_q_heads=32, n_kv_heads=8, head_dim=128,
+                                       seed=synth.BASE_SEED + 601), "cuda")
+    for kk in ("wq", "wk", "wv", "lam"):
+        x1[kk] = x0[kk]
+    prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window)
+    args = lambda x: [x[k] for k in ("q", "k", "v", "g", "beta", "lam", "wq", "wk", "wv", "cu_seqlens")]  # noqa: E731
+    st = hla.State(prm, 1).init()
+    hla.prefill(prm, *args(x0), torch.empty_like(x0["q"]), state=st)
+    out = torch.empty_like(x1["q"])
+    ws = torch.empty(hla.continue_workspace_bytes(prm, 4096, 1), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        hla.prefill_continue(prm, *args(x1), out, st, ws=ws)
+    torch.cuda.synchronize()
+    assert st.check_error() == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a.record()
+        hla.prefill_continue(prm, *args(x1), out, st, ws=ws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    dev_s = dist.max(sum(ms) / 1e3)
+    del ws, flush
+    return {"value": 4096 * dist.world * steps / dev_s, "unit": "tokens/s", "steps": steps, "warmup": warmup,
+            "ms_per_step": dev_s * 1e3 / steps,
+            "config": {"workload": "LLaMA-3.1-8B layer shape (32q/8kv d128 bf16, 8 sinks + 56 window): 4096-token "
+                                   "chunks appended to one sequence after a 4096-token prefill",
+                       "l2": "flushed between calls (512 MiB write)"}}
+
+
 def layer_work(wl) -> dict:
     """Algorithmic work of the whole layer per prefill: bytes = q and o in the layer dtype, k and v per kv
     head, g and beta fp32 (intermediates excluded); flops = the chunked GDN's useful flops per absorbed
@@ -975,6 +1019,7 @@ def main():
         del p
         torch.cuda.empty_cache()
     scan = run_scan_bench(dist) if args.scan else None
+    cont = run_continue_bench(dist) if args.scan else None
     torch.cuda.empty_cache()
     bwd = None
     if args.backward:
@@ -1003,6 +1048,8 @@ def main():
         line["backward_" + args.backward] = bwd
     if scan:
         line["prefill_scan_fp32"] = scan
+    if cont:
+        line["prefill_continue_c1"] = cont
     if dec:
         line["decode"] = dec
     if dist.rank == 0:

@@ -138,8 +138,11 @@ cont_gather_kernel(LayerDims L, hla_state s, const int32_t* __restrict__ ext_cu,
     }
 }
 
-// 4. the new rows: CTA per new token, a warp per feature row (q-heads, k-heads, v-heads), lane l holding
-// channels l + 32 e (RoPE pairs (l + 32 e, l + 32 e + 64) in the same lane)
+// 4. the new rows: CTA per (block of kTB new tokens, group of 8 feature rows), a warp per feature row
+// (q-heads, then k-heads, then v-heads) walking the block's tokens in order with the last 8 conv inputs of
+// its lane's channels (l + 32 e; RoPE pairs (l + 32 e, l + 32 e + 64) in the same lane) in registers, fed at
+// the block's start from the tokens before it (the state's history before the call)
+constexpr int kTB = 32;  // new tokens per CTA
 template <typename Tin>
 __global__ void __launch_bounds__(kCT)
 cont_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
@@ -148,93 +151,170 @@ cont_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restri
                      hla_state s, const int32_t* __restrict__ ext_cu, __half* __restrict__ qr, __half* __restrict__ kr,
                      __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
                      __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb) {
-    constexpr int D = kCD, HALF = D / 2, E = D / 32;
-    __shared__ float cs[kConvWidth][HALF], sn[kConvWidth][HALF];  // angles of positions p - 7 .. p
-    const int64_t t = blockIdx.x;
+    constexpr int D = kCD, HALF = D / 2, E = D / 32, NP = kTB + kConvHalo;  // positions t0 - 7 .. t0 + kTB - 1
+    __shared__ float cs[NP][HALF], sn[NP][HALF];
+    __shared__ int64_t tok_pos[kTB];   // true position of each token of the block (-1: not a new token)
+    __shared__ int64_t tok_ext[kTB];   // its extended row
+    const int64_t t0 = (int64_t)blockIdx.x * kTB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = seq_of_token(cu, L.n_seqs, t);
-    int64_t start, len;
-    seq_range(cu, n, L.total, &start, &len);
-    const int64_t pos = s.pos[n];
-    if (pos < 0 || t < start || t >= start + len) return;  // flagged, or outside every sequence
-    const int64_t i = t - start, p = pos + i;
-    const size_t e = (size_t)__ldg(ext_cu + n) + (size_t)cont_n_old(pos, L.n_sinks, L.window) + (size_t)i;
-    for (int idx = tid; idx < kConvWidth * HALF; idx += kCT) {
-        const int m = idx / HALF, ii = idx % HALF;
-        const int64_t pp = p - (kConvWidth - 1) + m;
-        float c = 1.f, sv = 0.f;
-        if (pp >= 0) rope_cs_exact(pp, L.theta[ii], &c, &sv);
-        cs[m][ii] = c;
-        sn[m][ii] = sv;
+    const int n_rows = L.Hq + 2 * L.Hkv;
+    // the block's tokens (they may span sequences)
+    if (tid < kTB) {
+        const int64_t t = t0 + tid;
+        int64_t p = -1, e = 0;
+        if (t < L.total) {
+            const int n = seq_of_token(cu, L.n_seqs, t);
+            int64_t start, len;
+            seq_range(cu, n, L.total, &start, &len);
+            const int64_t pos = s.pos[n];
+            if (pos >= 0 && t >= start && t < start + len) {
+                p = pos + (t - start);
+                e = (int64_t)__ldg(ext_cu + n) + cont_n_old(pos, L.n_sinks, L.window) + (t - start);
+            }
+        }
+        tok_pos[tid] = p;
+        tok_ext[tid] = e;
     }
     __syncthreads();
-    for (int r = warp; r < L.Hq + 2 * L.Hkv; r += kCT / 32) {
+    // angles: slot u < 7 for the positions before the first token, 7 + i for token i (at its position)
+    for (int idx = tid; idx < NP * HALF; idx += kCT) {
+        const int u = idx / HALF, ii = idx % HALF;
+        int64_t pp;
+        if (u < kConvHalo) pp = tok_pos[0] < 0 ? -1 : tok_pos[0] - kConvHalo + u;
+        else pp = tok_pos[u - kConvHalo];
+        float c = 1.f, sv = 0.f;
+        if (pp >= 0) rope_cs_exact(pp, L.theta[ii], &c, &sv);
+        cs[u][ii] = c;
+        sn[u][ii] = sv;
+    }
+    __syncthreads();
+    const int r = blockIdx.y * (kCT / 32) + warp;
+    if (r < n_rows) {
         const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
         const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
         const int H = kind == 0 ? L.Hq : L.Hkv;
         const Tin* src = kind == 0 ? q : kind == 1 ? k : v;
         const float* hist = kind == 0 ? s.conv_q : kind == 1 ? s.conv_k : s.conv_v;
-        const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + (size_t)hh * D * kConvWidth;
-        float acc[E], cur[E];
-#pragma unroll
-        for (int ee = 0; ee < E; ++ee) acc[ee] = cur[ee] = 0.f;
-#pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) {
-            const int64_t pp = p - (kConvWidth - 1) + m;
-            if (pp < 0) continue;
-            float x[E];
-            if (pp >= pos) {  // a new token of this call
-                const Tin* row = src + ((size_t)(t - (kConvWidth - 1) + m) * H + hh) * D;
-                if (kind == 2) {
-#pragma unroll
-                    for (int ee = 0; ee < E; ++ee) x[ee] = to_f32(row[lane + 32 * ee]);
-                } else {
-#pragma unroll
-                    for (int ee = 0; ee < E / 2; ++ee) {
-                        const int ii = lane + 32 * ee;
-                        const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
-                        x[ee] = x1 * cs[m][ii] - x2 * sn[m][ii];
-                        x[ee + E / 2] = x2 * cs[m][ii] + x1 * sn[m][ii];
-                    }
-                }
-            } else {  // before the call: the state's history (RoPE'd q, k and raw v of pos - 7 .. pos - 1)
-                const float* hr = hist + (((size_t)n * kConvHalo + (size_t)(pp - pos + kConvHalo)) * H + hh) * D;
-#pragma unroll
-                for (int ee = 0; ee < E; ++ee) x[ee] = hr[lane + 32 * ee];
-            }
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) acc[ee] = fmaf(w[(size_t)(lane + 32 * ee) * kConvWidth + m], x[ee], acc[ee]);
-            if (m == kConvWidth - 1) {
-#pragma unroll
-                for (int ee = 0; ee < E; ++ee) cur[ee] = x[ee];
-            }
-        }
-        const size_t o = (e * H + hh) * D;
-        if (kind == 2) {
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) {
-                vh[o + lane + 32 * ee] = __float2half_rn(acc[ee]);
-                ev[o + lane + 32 * ee] = __float2bfloat16_rn(cur[ee]);
-            }
-            continue;
-        }
-        float ss = 0.f;
-#pragma unroll
-        for (int ee = 0; ee < E; ++ee) ss = fmaf(acc[ee], acc[ee], ss);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float inv = (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q)) ? rsqrtf(ss + 1e-6f) : 1.f;
-        __half* xr = kind == 0 ? qr : kr;
-        __half* xh = kind == 0 ? qh : kh;
+        float w[E][kConvWidth];
 #pragma unroll
         for (int ee = 0; ee < E; ++ee) {
-            xr[o + lane + 32 * ee] = __float2half_rn(cur[ee]);
-            xh[o + lane + 32 * ee] = __float2half_rn(acc[ee] * inv);
+            const float4* w4 = reinterpret_cast<const float4*>((kind == 0 ? wq : kind == 1 ? wk : wv) +
+                                                               ((size_t)hh * D + lane + 32 * ee) * kConvWidth);
+            const float4 a4 = w4[0], b4 = w4[1];
+            w[ee][0] = a4.x; w[ee][1] = a4.y; w[ee][2] = a4.z; w[ee][3] = a4.w;
+            w[ee][4] = b4.x; w[ee][5] = b4.y; w[ee][6] = b4.z; w[ee][7] = b4.w;
+        }
+        // the conv input of token t (global row) at position p, angle slot u
+        auto input = [&](int64_t t, int u, float* x) {
+            const Tin* row = src + ((size_t)t * H + hh) * D;
+            if (kind == 2) {
+#pragma unroll
+                for (int ee = 0; ee < E; ++ee) x[ee] = to_f32(row[lane + 32 * ee]);
+            } else {
+#pragma unroll
+                for (int ee = 0; ee < E / 2; ++ee) {
+                    const int ii = lane + 32 * ee;
+                    const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
+                    x[ee] = x1 * cs[u][ii] - x2 * sn[u][ii];
+                    x[ee + E / 2] = x2 * cs[u][ii] + x1 * sn[u][ii];
+                }
+            }
+        };
+        float win[kConvWidth][E];  // win[m]: the input at position p - 7 + m
+#pragma unroll
+        for (int m = 0; m < kConvWidth; ++m)
+#pragma unroll
+            for (int ee = 0; ee < E; ++ee) win[m][ee] = 0.f;
+        int64_t prev_p = -2;  // position of the last token processed (the window follows it)
+        for (int i = 0; i < kTB; ++i) {
+            const int64_t p = tok_pos[i], t = t0 + i;
+            if (p < 0) {
+                prev_p = -2;
+                continue;
+            }
+            if (p == prev_p + 1) {  // the next token of the same sequence: shift
+#pragma unroll
+                for (int m = 0; m + 1 < kConvWidth; ++m)
+#pragma unroll
+                    for (int ee = 0; ee < E; ++ee) win[m][ee] = win[m + 1][ee];
+            } else {  // a block or sequence start: the 7 inputs before p
+                const int n = seq_of_token(cu, L.n_seqs, t);
+                int64_t start, len;
+                seq_range(cu, n, L.total, &start, &len);
+                const int64_t pos = s.pos[n];
+#pragma unroll
+                for (int m = 0; m < kConvHalo; ++m) {
+                    const int64_t pp = p - kConvHalo + m;
+                    if (pp < 0) {
+#pragma unroll
+                        for (int ee = 0; ee < E; ++ee) win[m][ee] = 0.f;
+                    } else if (pp >= pos) {  // a new token before this block: RoPE at its own position
+                        const Tin* row = src + ((size_t)(t - kConvHalo + m) * H + hh) * D;
+                        float cv[E / 2], sv[E / 2];
+                        if (kind != 2) {
+#pragma unroll
+                            for (int ee = 0; ee < E / 2; ++ee) rope_cs_exact(pp, L.theta[lane + 32 * ee], &cv[ee], &sv[ee]);
+                        }
+#pragma unroll
+                        for (int ee = 0; ee < E / 2; ++ee) {
+                            const int ii = lane + 32 * ee;
+                            if (kind == 2) {
+                                win[m][ee] = to_f32(row[ii]);
+                                win[m][ee + E / 2] = to_f32(row[ii + HALF]);
+                            } else {
+                                const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
+                                win[m][ee] = x1 * cv[ee] - x2 * sv[ee];
+                                win[m][ee + E / 2] = x2 * cv[ee] + x1 * sv[ee];
+                            }
+                        }
+                    } else {  // before the call: the state's history
+                        const float* hr = hist + (((size_t)n * kConvHalo + (size_t)(pp - pos + kConvHalo)) * H + hh) * D;
+#pragma unroll
+                        for (int ee = 0; ee < E; ++ee) win[m][ee] = hr[lane + 32 * ee];
+                    }
+                }
+            }
+            input(t, kConvHalo + i, win[kConvWidth - 1]);
+            prev_p = p;
+            float acc[E];
+#pragma unroll
+            for (int ee = 0; ee < E; ++ee) {
+                acc[ee] = 0.f;
+#pragma unroll
+                for (int m = 0; m < kConvWidth; ++m) acc[ee] = fmaf(w[ee][m], win[m][ee], acc[ee]);
+            }
+            const size_t o = ((size_t)tok_ext[i] * H + hh) * D;
+            if (kind == 2) {
+#pragma unroll
+                for (int ee = 0; ee < E; ++ee) {
+                    vh[o + lane + 32 * ee] = __float2half_rn(acc[ee]);
+                    ev[o + lane + 32 * ee] = __float2bfloat16_rn(win[kConvWidth - 1][ee]);
+                }
+                continue;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int ee = 0; ee < E; ++ee) ss = fmaf(acc[ee], acc[ee], ss);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q)) ? rsqrtf(ss + 1e-6f) : 1.f;
+            __half* xr = kind == 0 ? qr : kr;
+            __half* xh = kind == 0 ? qh : kh;
+#pragma unroll
+            for (int ee = 0; ee < E; ++ee) {
+                xr[o + lane + 32 * ee] = __float2half_rn(win[kConvWidth - 1][ee]);
+                xh[o + lane + 32 * ee] = __float2half_rn(acc[ee] * inv);
+            }
         }
     }
-    for (int h = tid; h < L.Hq; h += kCT) {
-        eg[e * L.Hq + h] = g[(size_t)t * L.Hq + h];
-        eb[e * L.Hq + h] = beta[(size_t)t * L.Hq + h];
+    if (blockIdx.y == 0) {  // the gates
+        for (int idx = tid; idx < kTB * L.Hq; idx += kCT) {
+            const int i = idx / L.Hq, h = idx % L.Hq;
+            if (tok_pos[i] < 0) continue;
+            const size_t e = (size_t)tok_ext[i];
+            eg[e * L.Hq + h] = g[(size_t)(t0 + i) * L.Hq + h];
+            eb[e * L.Hq + h] = beta[(size_t)(t0 + i) * L.Hq + h];
+        }
     }
 }
 
@@ -254,8 +334,8 @@ cont_out_kernel(LayerDims L, const int32_t* __restrict__ cu, hla_state s, const 
     for (int idx = threadIdx.x; idx < L.Hq * kCD / 8; idx += kCT) dst[idx] = src[idx];
 }
 
-// 7. the state after the call: CTA per (sequence, row group); y = 0: the q-heads' conv histories and
-// pending gates; y = 1 + kv: that kv head's ring entries, pending khat / vhat and conv histories
+// 7. the state after the call: CTA per (sequence, y); y = 0: the pending gates; y = 1 + kv: that kv head's
+// ring entries, pending khat / vhat and conv histories; y = 1 + Hkv + h: q-head h's conv history
 template <typename Tin>
 __global__ void __launch_bounds__(kCT)
 cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
@@ -295,16 +375,19 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
             }
         }
     };
-    if (y == 0) {
-        for (int h = 0; h < L.Hq; ++h) advance_history(s.conv_q, q, L.Hq, h, true);
-        for (int64_t i = tid; i < (int64_t)len * L.Hq; i += kCT) {  // gates of the new tokens still waiting
+    if (y == 0) {  // gates of the new tokens still waiting to be absorbed
+        const int64_t i0 = max((int64_t)0, max(len - W, ns - pos));
+        for (int64_t i = i0 * L.Hq + tid; i < (int64_t)len * L.Hq; i += kCT) {
             const int64_t tt = i / L.Hq, p = pos + tt;
             const int h = (int)(i % L.Hq);
-            if (p < p_end - W || p < ns) continue;
             const size_t gs = ((size_t)n * L.Hq + h) * P + (size_t)(p % P);
             s.pend_g[gs] = g[(size_t)(start + tt) * L.Hq + h];
             s.pend_beta[gs] = beta[(size_t)(start + tt) * L.Hq + h];
         }
+        return;
+    }
+    if (y > L.Hkv) {  // a q-head's conv history
+        advance_history(s.conv_q, q, L.Hq, y - 1 - L.Hkv, true);
         return;
     }
     const int kv = y - 1;
@@ -364,9 +447,11 @@ cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const 
     cont_zero_tail_kernel<<<1024, kCT, 0, st>>>(Lx, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb);
     cont_gather_kernel<<<dim3(L.n_sinks + L.window, L.n_seqs), kCT, 0, st>>>(L, s, ext_cu, qr, kr, qh, kh, vh, ev, eg,
                                                                              eb);
-    if (L.total > 0)
-        cont_features_kernel<__nv_bfloat16><<<(unsigned)L.total, kCT, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, cu, s,
-                                                                               ext_cu, qr, kr, qh, kh, vh, ev, eg, eb);
+    if (L.total > 0) {
+        const dim3 grid((unsigned)((L.total + kTB - 1) / kTB), (unsigned)((L.Hq + 2 * L.Hkv + kCT / 32 - 1) / (kCT / 32)));
+        cont_features_kernel<__nv_bfloat16><<<grid, kCT, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, cu, s, ext_cu, qr,
+                                                                  kr, qh, kh, vh, ev, eg, eb);
+    }
     return cudaGetLastError();
 }
 
@@ -375,8 +460,8 @@ cudaError_t launch_continue_finish(const LayerDims& L, const int32_t* cu, const 
                                    const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
                                    const __half* kh, const __half* vh, cudaStream_t st) {
     if (L.total > 0) cont_out_kernel<<<(unsigned)L.total, kCT, 0, st>>>(L, cu, s, ext_cu, ext_out, out);
-    cont_state_kernel<__nv_bfloat16><<<dim3(L.n_seqs, 1 + L.Hkv), kCT, 0, st>>>(L, q, k, v, g, beta, cu, s, ext_cu, kh,
-                                                                                vh);
+    cont_state_kernel<__nv_bfloat16><<<dim3(L.n_seqs, 1 + L.Hkv + L.Hq), kCT, 0, st>>>(L, q, k, v, g, beta, cu, s,
+                                                                                       ext_cu, kh, vh);
     cont_tc_advance_kernel<<<(L.n_seqs + 127) / 128, 128, 0, st>>>(L, cu, s.pos);
     return cudaGetLastError();
 }
