@@ -528,40 +528,59 @@ decode_attn_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
 // maxima (read sixteen at a time, so their loads overlap: one batch for an
 // 896-slot ring), o = o_sm + lambda_h o_lin; then the sequence's position
 // advances (CTA of head 0: no CTA of this launch reads it).
-constexpr int kCombineBatch = 16;
+// Merge of the softmax splits of (q-head h, sequence n): warp 0 forms the splits' weights
+// 2^(m_r - M) (M the largest split maximum, splits without keys weighted 0) and the normaliser
+// sum_r 2^(m_r - M) l_r once, a tile of kCombineTile weights at a time in shared memory; every thread then
+// sums its value dim over the splits' partial outputs.  Then + lambda_h o_lin, and pos advances.
+constexpr int kCombineTile = 256;
 template <typename Tin, int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lambda, Tin* __restrict__ out,
                       int64_t* __restrict__ pos) {
     // (a negative position was flagged by the features launch; it is left as it is)
-    const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x;
+    __shared__ float w_s[kCombineTile];
+    __shared__ float mx_s, inv_s;
+    const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x, lane = c & 31;
     const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
-    float m = -INFINITY, l = 0.f, o = 0.f;  // running merge
-    for (int r0 = 0; r0 < sc.splits; r0 += kCombineBatch) {
-        float pm[kCombineBatch], pl[kCombineBatch], pa[kCombineBatch];
+    if (c < 32) {
+        float m = -INFINITY;
+        for (int r = lane; r < sc.splits; r += 32)
+            if (sc.pl[hs + r] > 0.f) m = fmaxf(m, sc.pm[hs + r]);
 #pragma unroll
-        for (int u = 0; u < kCombineBatch; ++u) {
-            const bool in = r0 + u < sc.splits;
-            pm[u] = in ? sc.pm[hs + r0 + u] : -INFINITY;
-            pl[u] = in ? sc.pl[hs + r0 + u] : 0.f;
-            pa[u] = in ? sc.pacc[(hs + r0 + u) * D + c] : 0.f;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        if (m != -INFINITY)
+            for (int r = lane; r < sc.splits; r += 32) {
+                const float pl = sc.pl[hs + r];
+                if (pl > 0.f) l = fmaf(pl, exp2f(sc.pm[hs + r] - m), l);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            mx_s = m;
+            inv_s = l > 0.f ? 1.f / l : 0.f;
         }
-        float mb = m;
-#pragma unroll
-        for (int u = 0; u < kCombineBatch; ++u) mb = fmaxf(mb, pl[u] > 0.f ? pm[u] : -INFINITY);
-        if (mb == -INFINITY) continue;  // nothing in this batch or before it
-        const float w0 = l > 0.f ? exp2f(m - mb) : 0.f;
-        l *= w0;
-        o *= w0;
-#pragma unroll
-        for (int u = 0; u < kCombineBatch; ++u) {
-            const float w = pl[u] > 0.f ? exp2f(pm[u] - mb) : 0.f;
-            l = fmaf(pl[u], w, l);
-            o = fmaf(pa[u], w, o);
-        }
-        m = mb;
     }
-    o = (L.flags & HLA_FLAG_SOFTMAX_OFF) || l <= 0.f ? 0.f : o / l;
+    __syncthreads();
+    const float m = mx_s;
+    float o0 = 0.f, o1 = 0.f;  // two chains
+    for (int r0 = 0; r0 < sc.splits && m != -INFINITY; r0 += kCombineTile) {
+        const int nr = min(kCombineTile, sc.splits - r0);
+        __syncthreads();  // the previous tile's weights are no longer read
+        for (int r = c; r < nr; r += D) {
+            const float pl = sc.pl[hs + r0 + r];
+            w_s[r] = pl > 0.f ? exp2f(sc.pm[hs + r0 + r] - m) : 0.f;
+        }
+        __syncthreads();
+        const float* pa = sc.pacc + (hs + r0) * D + c;
+        int r = 0;
+        for (; r + 1 < nr; r += 2) {
+            o0 = fmaf(w_s[r], pa[(size_t)r * D], o0);
+            o1 = fmaf(w_s[r + 1], pa[(size_t)(r + 1) * D], o1);
+        }
+        if (r < nr) o0 = fmaf(w_s[r], pa[(size_t)r * D], o0);
+    }
+    float o = (L.flags & HLA_FLAG_SOFTMAX_OFF) ? 0.f : (o0 + o1) * inv_s;
     if (!(L.flags & HLA_FLAG_LINEAR_OFF)) o = fmaf(__ldg(lambda + h), sc.olin[((size_t)n * L.Hq + h) * D + c], o);
     out[((size_t)n * L.Hq + h) * D + c] = from_f32<Tin>(o);
     if (h == 0 && c == 0 && pos[n] >= 0) pos[n] += 1;
