@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--scan", type=int, default=1,
                     help="1: also time the context-parallel token-serial GDN on a long fp32 sequence and the "
                          "prefill continuation (chunked prefill)")
+    ap.add_argument("--only", default="", choices=["", "backward", "scan", "continue"],
+                    help="run one secondary measurement alone with few calls (--warmup warm-up calls; --steps timed "
+                         "calls for continue; 3 for backward and scan): the form the profiler captures use")
     ap.add_argument("--backward", default="c1", choices=["", "c1", "c2", "c4"],
                     help="workload of the backward (hla_backward) measurement; empty to skip")
     ap.add_argument("--backward-seconds", type=float, default=2.0,
@@ -550,7 +553,7 @@ def scan_traffic(key):
     return None if parts[0] is None else parts[0] + (parts[1] or 0.0)
 
 
-def run_scan_bench(dist, trial_seconds=0.5):
+def run_scan_bench(dist, trial_seconds=0.5, warmup=3):
     """The context-parallel token-serial GDN (HLA_FLAG_GDN_SCAN) against the single pass, on an fp32 layer
     of the reference config's head shape (2 q / 1 kv heads, d 64, 8 sinks + 56 window) over one long
     sequence: prefill tokens/s both ways and the GDN launches' time (stage marks 3 -> 4)."""
@@ -575,7 +578,7 @@ def run_scan_bench(dist, trial_seconds=0.5):
             hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"],
                         x["cu_seqlens"], out, ws=ws)
 
-        for _ in range(3):
+        for _ in range(warmup):
             step()
         torch.cuda.synchronize()
         assert hla.check_workspace_error(ws) == 0
@@ -1003,6 +1006,18 @@ def main():
         dec = run_decode_bench(args, dist, peaks)
         if dist.rank == 0:
             print(json.dumps({"decode": dec}), flush=True)
+        dist.close()
+        return
+    if args.only:  # one secondary measurement alone, with few calls (for profiler captures)
+        if args.only == "backward":
+            part = run_backward_bench(args.backward or "c1", dist, peaks, trial_seconds=0.0, warmup=args.warmup,
+                                      stage_steps=1, e2e_steps=1)
+        elif args.only == "scan":
+            part = run_scan_bench(dist, trial_seconds=0.0, warmup=args.warmup)
+        else:
+            part = run_continue_bench(dist, steps=args.steps, warmup=args.warmup)
+        if dist.rank == 0:
+            print(json.dumps({args.only: part}), flush=True)
         dist.close()
         return
     with_cpu = dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline
