@@ -358,21 +358,29 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
         const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
         return c < HALF ? x1 * cv - x2 * sv : x2 * cv + x1 * sv;
     };
-    // conv history of a row (H heads, head hh): entry m <- position p_end - 7 + m, in order (entry m reads
-    // the old entry m + len before the loop reaches that one)
+    // conv history of a row (H heads, head hh): entry m <- position p_end - 7 + m; the values are all read
+    // (old entries from m + len) before any is written
     auto advance_history = [&](float* hist, const Tin* src, int H, int hh, bool rotate) {
-        for (int c = tid; c < D; c += kCT) {
-            for (int m = 0; m < kConvHalo; ++m) {
-                const int64_t pp = p_end - kConvHalo + m;
-                float x = 0.f;
-                if (pp >= pos) {
-                    const Tin* row = src + ((size_t)(start + (pp - pos)) * H + hh) * D;
-                    x = rotate ? rope(row, c, pp) : to_f32(row[c]);
-                } else if (pp >= 0) {
-                    x = hist[(((size_t)n * kConvHalo + (size_t)(m + len)) * H + hh) * D + c];
-                }
-                hist[(((size_t)n * kConvHalo + m) * H + hh) * D + c] = x;
+        constexpr int PER = (kConvHalo * D + kCT - 1) / kCT;
+        float val[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int idx = tid + u * kCT, m = idx / D, c = idx % D;
+            val[u] = 0.f;
+            if (idx >= kConvHalo * D) continue;
+            const int64_t pp = p_end - kConvHalo + m;
+            if (pp >= pos) {
+                const Tin* row = src + ((size_t)(start + (pp - pos)) * H + hh) * D;
+                val[u] = rotate ? rope(row, c, pp) : to_f32(row[c]);
+            } else if (pp >= 0) {
+                val[u] = hist[(((size_t)n * kConvHalo + (size_t)(m + len)) * H + hh) * D + c];
             }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int idx = tid + u * kCT, m = idx / D, c = idx % D;
+            if (idx < kConvHalo * D) hist[(((size_t)n * kConvHalo + m) * H + hh) * D + c] = val[u];
         }
     };
     if (y == 0) {  // gates of the new tokens still waiting to be absorbed
@@ -395,28 +403,33 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
     Tin* vring = static_cast<Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
     // the new tokens that stay in the ring (sinks, and the final window) and in the pending ring
     const int64_t first = max((int64_t)0, min(len, p_end - W - pos));  // index of the first final-window token
-    auto ring_rows = [&](int64_t i) {
-        const int64_t p = pos + i;
+    // the rows that stay: new sinks [0, i_sink) and the final window [i_win, len), all at once
+    const int64_t i_sink = min(len, max((int64_t)0, ns - pos));
+    const int64_t i_win = max(first, i_sink);
+    const int64_t n_rows = i_sink + (len - i_win);
+    auto row_of = [&](int64_t r) { return r < i_sink ? r : i_win + (r - i_sink); };
+    for (int64_t idx = tid; idx < n_rows * HALF; idx += kCT) {  // RoPE'd key pairs (ii, ii + d/2): one angle
+        const int64_t i = row_of(idx / HALF), p = pos + i;
+        const int ii = (int)(idx % HALF);
         const size_t row = ((size_t)(start + i) * L.Hkv + kv) * D, slot = (size_t)cont_ring_slot(p, ns, W) * D;
-        for (int ii = tid; ii < HALF; ii += kCT) {  // RoPE'd key pair (ii, ii + d/2): one angle
-            float cv, sv;
-            rope_cs_exact(p, L.theta[ii], &cv, &sv);
-            const float x1 = to_f32(k[row + ii]), x2 = to_f32(k[row + ii + HALF]);
-            kring[slot + ii] = from_f32<Tin>(x1 * cv - x2 * sv);
-            kring[slot + ii + HALF] = from_f32<Tin>(x2 * cv + x1 * sv);
+        float cv, sv;
+        rope_cs_exact(p, L.theta[ii], &cv, &sv);
+        const float x1 = to_f32(k[row + ii]), x2 = to_f32(k[row + ii + HALF]);
+        kring[slot + ii] = from_f32<Tin>(x1 * cv - x2 * sv);
+        kring[slot + ii + HALF] = from_f32<Tin>(x2 * cv + x1 * sv);
+    }
+    for (int64_t idx = tid; idx < n_rows * D; idx += kCT) {
+        const int64_t i = row_of(idx / D), p = pos + i;
+        const int c = (int)(idx % D);
+        const size_t row = ((size_t)(start + i) * L.Hkv + kv) * D, slot = (size_t)cont_ring_slot(p, ns, W) * D;
+        vring[slot + c] = v[row + c];
+        if (p >= ns && p >= p_end - W) {
+            const size_t ps = (((size_t)n * L.Hkv + kv) * P + (size_t)(p % P)) * D + c;
+            const size_t er = ((e0 + (size_t)i) * L.Hkv + kv) * D + c;
+            s.pend_k[ps] = __half2float(kh[er]);
+            s.pend_v[ps] = __half2float(vh[er]);
         }
-        for (int c = tid; c < D; c += kCT) {
-            vring[slot + c] = v[row + c];
-            if (p >= ns && p >= p_end - W) {
-                const size_t ps = (((size_t)n * L.Hkv + kv) * P + (size_t)(p % P)) * D + c;
-                const size_t er = ((e0 + (size_t)i) * L.Hkv + kv) * D + c;
-                s.pend_k[ps] = __half2float(kh[er]);
-                s.pend_v[ps] = __half2float(vh[er]);
-            }
-        }
-    };
-    for (int64_t i = 0; i < min(len, max((int64_t)0, ns - pos)); ++i) ring_rows(i);  // new sinks
-    for (int64_t i = max(first, max((int64_t)0, ns - pos)); i < len; ++i) ring_rows(i);
+    }
     advance_history(s.conv_k, k, L.Hkv, kv, true);
     advance_history(s.conv_v, v, L.Hkv, kv, false);
 }
