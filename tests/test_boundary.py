@@ -177,3 +177,13 @@ def test_scan_flag_sizes_its_buffers_on_the_token_serial_path_only(lib):
 def test_gla_and_stall_flags_are_known(lib):
     assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_GLA), 16, 1) > 0
     assert hla.workspace_bytes(_p(flags=hla.FLAG_L2NORM_Q | hla.FLAG_TEST_STALL), 16, 1) > 0
+
+
+def test_continue_workspace_covers_the_cached_rows(lib):
+    # tensor-core path: the prefill's workspace for the new tokens plus every sequence's n_sinks + window
+    # cached rows, and the extended rows' v, g, beta and output; token-serial path: the prefill's
+    tc = _p()
+    assert hla.continue_workspace_bytes(tc, 1000, 4) >= hla.workspace_bytes(tc, 1000 + 4 * 64, 4)
+    assert hla.continue_workspace_bytes(tc, 1000, 4) > hla.continue_workspace_bytes(tc, 1000, 1)
+    serial = _p(head_dim=64)
+    assert hla.continue_workspace_bytes(serial, 1000, 4) == hla.workspace_bytes(serial, 1000, 4)

@@ -220,3 +220,16 @@ def test_zero_tokens_and_errors():
     with pytest.raises(hla.HlaError) as e:
         hla.backward(params_for(wl), *_args(x), dout, ws=small_ws)
     assert e.value.status == hla.HLA_ERR_WORKSPACE
+
+
+def test_malformed_seqlens_are_flagged_not_faulting():
+    # the table ends at 40 although 64 tokens are passed: tokens 40..63 belong to no sequence; every access
+    # stays clamped inside [0, total) and the workspace's error word reports the table
+    wl = synth.small("bwd bad cu", [40, 24], n_q_heads=2, n_kv_heads=1, head_dim=64)
+    x = synth.make_inputs(wl, "cuda")
+    x["cu_seqlens"] = torch.tensor([0, 20, 40], dtype=torch.int32, device="cuda")
+    prm = params_for(wl)
+    ws = torch.empty(hla.backward_workspace_bytes(prm, 64, 2), dtype=torch.uint8, device="cuda")
+    hla.backward(prm, *_args(x), synth.cotangent(wl, "cuda"), ws=ws)
+    torch.cuda.synchronize()
+    assert hla.check_workspace_error(ws) != 0

@@ -185,3 +185,23 @@ def test_stale_workspace_contents_do_not_leak(oracle_mod):
     for a, b in zip(*outs):
         assert torch.isfinite(b.float()).all()
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_negative_position_is_flagged_and_left_alone(d):
+    wl = synth.small("cont neg", [100, 80], n_q_heads=4, n_kv_heads=2, head_dim=d)
+    x1 = synth.make_inputs(wl, "cuda")
+    x2 = _inputs(wl, [30, 20], synth.BASE_SEED + 44)
+    prm = params_for(wl)
+    st = hla.State(prm, 2).init()
+    hla.prefill(prm, *_args(x1), torch.empty_like(x1["q"]), state=st)
+    torch.cuda.synchronize()
+    st.view("pos")[1] = -5  # a position no prefill or decode step leaves
+    before = {name: st.view(name)[:].clone() for name in ("S", "k_ring", "conv_k")}
+    hla.prefill_continue(prm, *_args(x2), torch.empty_like(x2["q"]), st)
+    torch.cuda.synchronize()
+    assert st.check_error() != 0
+    assert st.view("pos").cpu().tolist() == [130, -5]
+    half = lambda t: t.view(2, -1)[1]  # noqa: E731  sequence 1's part of a per-sequence buffer
+    for name, b in before.items():
+        assert torch.equal(half(st.view(name)), half(b)), name
