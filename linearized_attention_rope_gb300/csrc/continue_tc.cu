@@ -11,8 +11,10 @@
 // waiting, absorbed W rows later, at a new position.  So the prefill's softmax and chunked GDN kernels
 // run unchanged on the extended rows, the GDN starting from the cached S, and the new rows of their
 // output are the continuation's output.  Launches:
-//  1. the extended sequence table (and positions < 0 flagged in the state's error word);
-//  2. the prefill's work tables on it; rows past the last sequence (up to the workspace's bound) zeroed;
+//  1. the extended sequence table (positions < 0 and overlapping sequences flagged in the state's error
+//     word);
+//  2. the prefill's work tables on it; rows past the last sequence (up to the workspace's bound) zeroed, the
+//     new tokens' gates placed on their rows and their RoPE angles tabulated;
 //  3. the cached rows: RoPE'd keys and values from the ring, khat, vhat, g and beta from the pending ring;
 //  4. the new rows: RoPE at the true position, the short conv fed by the state's conv histories, L2;
 //  5. softmax, chunk-local GDN and GDN state + combine (the prefill's kernels, S from the state);
@@ -41,7 +43,7 @@ __device__ __forceinline__ int64_t cont_old_pos(int64_t pos, int64_t i, int ns, 
 }
 
 // 1. ext_cu[n] = the extended rows of the sequences before n (a sequence with pos < 0 has none and is
-// flagged).  One CTA of 1024 threads.
+// flagged; so is a table whose sequences overlap).  One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) cont_ext_table_kernel(LayerDims L, const int32_t* __restrict__ cu, hla_state s,
                                                               int32_t* __restrict__ ext_cu) {
     __shared__ int32_t part[1024];
@@ -53,6 +55,16 @@ __global__ void __launch_bounds__(1024) cont_ext_table_kernel(LayerDims L, const
         const int64_t p = s.pos[i];
         return p < 0 ? 0 : (int32_t)(cont_n_old(p, L.n_sinks, L.window) + len);
     };
+    // sequences must not overlap (cu non-decreasing once clamped into [0, total]): otherwise their extended
+    // rows could add up past the workspace's bound, so the table is flagged and every sequence given ext_cu = 0
+    // (the extended rows then overlap, but every row a kernel below forms stays below the bound)
+    bool bad = false;
+    for (int i = lo; i < hi; ++i) bad = bad || clamp_i64(__ldg(cu + i + 1), 0, L.total) < clamp_i64(__ldg(cu + i), 0, L.total);
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) atomicExch(s.err, kErrSeqlens);
+        for (int i = tid; i <= N; i += 1024) ext_cu[i] = 0;
+        return;
+    }
     int32_t sum = 0;
     for (int i = lo; i < hi; ++i) {
         if (s.pos[i] < 0) atomicExch(s.err, kErrState);
@@ -74,15 +86,20 @@ __global__ void __launch_bounds__(1024) cont_ext_table_kernel(LayerDims L, const
     if (tid == 1023) ext_cu[N] = part[1023];
 }
 
-// 2b. rows past the last extended row, up to the workspace's bound: zero.  The tensor-core kernels read
+// 2b. (i) rows past the last extended row, up to the workspace's bound: zero.  The tensor-core kernels read
 // whole tiles, and a tile that runs past a sequence's end must meet finite rows (masked rows are multiplied
-// by zero, and zero times a stale non-finite value would not vanish).
+// by zero, and zero times a stale non-finite value would not vanish).  (ii) g and beta of every new token onto
+// its extended row.  (iii) ang[t][i] = (cos, sin) of p theta_i for every new token t at its true position p
+// (angle formed and reduced in double precision), and ang[total][i] that of one position step, read by the
+// feature kernel.
 __global__ void __launch_bounds__(kCT)
-cont_zero_tail_kernel(LayerDims Lx, const int32_t* __restrict__ ext_cu, __half* __restrict__ qr,
-                      __half* __restrict__ kr, __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
-                      __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb) {
+cont_prep_kernel(LayerDims L, LayerDims Lx, const int32_t* __restrict__ cu, hla_state s,
+                 const int32_t* __restrict__ ext_cu, __half* __restrict__ qr, __half* __restrict__ kr,
+                 __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
+                 __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb,
+                 const float* __restrict__ g, const float* __restrict__ beta, float2* __restrict__ ang) {
     const int64_t first = __ldg(ext_cu + Lx.n_seqs);
-    const int D = kCD;
+    const int D = kCD, HALF = kCD / 2;
     for (int64_t r = first + blockIdx.x; r < Lx.total; r += gridDim.x) {
         for (int idx = threadIdx.x; idx < Lx.Hq * D; idx += kCT) {
             qr[r * Lx.Hq * D + idx] = __float2half_rn(0.f);
@@ -98,6 +115,36 @@ cont_zero_tail_kernel(LayerDims Lx, const int32_t* __restrict__ ext_cu, __half* 
             eg[r * Lx.Hq + h] = 0.f;
             eb[r * Lx.Hq + h] = 0.f;
         }
+    }
+    const int64_t stride = (int64_t)gridDim.x * kCT, id = (int64_t)blockIdx.x * kCT + threadIdx.x;
+    // (token, item) pairs: the 64 angles of a token are two whole warps, the gates of a token one warp when
+    // Hq = 32, so the sequence lookup is warp-uniform there
+    for (int64_t idx = id; idx < (L.total + 1) * HALF; idx += stride) {
+        const int64_t t = idx / HALF;
+        const int i = (int)(idx % HALF);
+        int64_t p = 1;
+        if (t < L.total) {
+            const int n = seq_of_token(cu, L.n_seqs, t);
+            int64_t start, len;
+            seq_range(cu, n, L.total, &start, &len);
+            const int64_t pos = s.pos[n];
+            p = pos >= 0 && t >= start && t < start + len ? pos + (t - start) : 0;
+        }
+        float c, sv;
+        rope_cs_exact(p, L.theta[i], &c, &sv);
+        ang[idx] = make_float2(c, sv);
+    }
+    for (int64_t idx = id; idx < L.total * L.Hq; idx += stride) {
+        const int64_t t = idx / L.Hq;
+        const int h = (int)(idx % L.Hq);
+        const int n = seq_of_token(cu, L.n_seqs, t);
+        int64_t start, len;
+        seq_range(cu, n, L.total, &start, &len);
+        const int64_t pos = s.pos[n];
+        if (pos < 0 || t < start || t >= start + len) continue;
+        const size_t e = (size_t)__ldg(ext_cu + n) + (size_t)cont_n_old(pos, L.n_sinks, L.window) + (size_t)(t - start);
+        eg[e * L.Hq + h] = g[idx];
+        eb[e * L.Hq + h] = beta[idx];
     }
 }
 
@@ -138,184 +185,253 @@ cont_gather_kernel(LayerDims L, hla_state s, const int32_t* __restrict__ ext_cu,
     }
 }
 
-// 4. the new rows: CTA per (block of kTB new tokens, group of 8 feature rows), a warp per feature row
-// (q-heads, then k-heads, then v-heads) walking the block's tokens in order with the last 8 conv inputs of
-// its lane's channels (l + 32 e; RoPE pairs (l + 32 e, l + 32 e + 64) in the same lane) in registers, fed at
-// the block's start from the tokens before it (the state's history before the call)
-constexpr int kTB = 32;  // new tokens per CTA
-template <typename Tin>
-__global__ void __launch_bounds__(kCT)
-cont_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-                     const float* __restrict__ g, const float* __restrict__ beta, const float* __restrict__ wq,
-                     const float* __restrict__ wk, const float* __restrict__ wv, const int32_t* __restrict__ cu,
-                     hla_state s, const int32_t* __restrict__ ext_cu, __half* __restrict__ qr, __half* __restrict__ kr,
-                     __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
-                     __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb) {
-    constexpr int D = kCD, HALF = D / 2, E = D / 32, NP = kTB + kConvHalo;  // positions t0 - 7 .. t0 + kTB - 1
-    __shared__ float cs[NP][HALF], sn[NP][HALF];
-    __shared__ int64_t tok_pos[kTB];   // true position of each token of the block (-1: not a new token)
-    __shared__ int64_t tok_ext[kTB];   // its extended row
-    const int64_t t0 = (int64_t)blockIdx.x * kTB;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n_rows = L.Hq + 2 * L.Hkv;
-    // the block's tokens (they may span sequences)
-    if (tid < kTB) {
-        const int64_t t = t0 + tid;
-        int64_t p = -1, e = 0;
-        if (t < L.total) {
-            const int n = seq_of_token(cu, L.n_seqs, t);
-            int64_t start, len;
-            seq_range(cu, n, L.total, &start, &len);
-            const int64_t pos = s.pos[n];
-            if (pos >= 0 && t >= start && t < start + len) {
-                p = pos + (t - start);
-                e = (int64_t)__ldg(ext_cu + n) + cont_n_old(pos, L.n_sinks, L.window) + (t - start);
+// 4. the new rows.  A warp per (feature row, span of new tokens): q-heads, then k-heads, then v-heads, 4 rows
+// to a CTA, the span a multiple of 8 tokens chosen so that the grid is one wave.  Lane l owns the RoPE pairs
+// 2l and 2l + 1 (channels 2l, 2l + 1, 64 + 2l, 64 + 2l + 1), so every row is read and written as whole lines.
+// The warp walks its span in steps of 8 tokens, the input rows of 4 steps in flight by cp.async in the warp's
+// slice of shared memory (no CTA-wide barrier).  Each token is rotated at its true position (the angle from
+// the table at a step's first token, then advanced by one position step per token), stored as the RoPE'd row,
+// and enters a register ring of the last 8 inputs; the width-8 causal conv reads the ring, except for the
+// taps of a sequence's first 7 new tokens that fall before the call, which read the state's conv history of
+// that sequence (the roped inputs of positions pos - 7 .. pos - 1; none before position 0).  The conv of q
+// and k is L2-normalised (q only under HLA_FLAG_L2NORM_Q); the v rows also keep the raw value for the softmax.
+// Every output lands on the token's extended row, t + (ext_cu[n] + n_old - start of n) for its sequence n.
+constexpr int kFW = 4;     // feature rows (warps) per CTA
+constexpr int kFB = 8;     // tokens per step = conv width
+constexpr int kFRing = 4;  // steps of input rows in flight per warp
+constexpr size_t kFeatSmem = (size_t)kFW * kFRing * kFB * kCD * sizeof(__nv_bfloat16);
+
+struct ContSeq {  // the sequence a warp is in (token indices fit the int32 sequence table)
+    int n, start, len;
+    int pos7;  // its position before the call, clamped to [-1, 7] (-1: not live; 7: no tap reaches position 0)
+    int off;   // extended row minus token index
+};
+__device__ __forceinline__ void cont_seq_at(const LayerDims& L, const int32_t* cu, const hla_state& s,
+                                            const int32_t* ext_cu, int n, ContSeq& q) {
+    int64_t start, len;
+    seq_range(cu, n, L.total, &start, &len);
+    const int64_t pos = s.pos[n];
+    q.n = n;
+    q.start = (int)start;
+    q.len = (int)len;
+    q.pos7 = pos < 0 ? -1 : (int)min(pos, (int64_t)kConvHalo);
+    q.off = pos < 0 ? 0 : (int)((int64_t)__ldg(ext_cu + n) + cont_n_old(pos, L.n_sinks, L.window) - start);
+}
+
+struct ContRow {
+    const float2* ang;   // angle table, lane's first pair added
+    const float* hist;   // conv history of the row (n = 0, m = 0), lane's first channel added
+    size_t hstride;      // floats between consecutive (n, m) entries of the history
+    __half* rot;         // RoPE'd rows (q, k), head and lane offsets added
+    __half* hat;         // conv (+ norm) rows
+    __nv_bfloat16* raw;  // v: the raw rows
+    size_t rowstride;    // elements between consecutive rows of one head
+    float2 w[2][kConvWidth];   // taps of the channel pairs (2l, 2l + 1) and (64 + 2l, 64 + 2l + 1)
+    float2 ring[kFB][2];       // the last 8 inputs, same pairing
+    float2 step1[2];           // (cos, sin) of one position step for the lane's pairs
+};
+
+// Eight tokens t_first .. + 7, the inputs in the warp's slot `rows` (lane offset added).  CHECK = false: every
+// token lies in one live sequence at index >= 7 (straight-line code); CHECK = true follows the sequences token
+// by token, skips tokens of no live sequence and feeds the early taps from the history.  OUT = false only
+// fills the ring.
+template <bool ROPE, bool NORM, bool CHECK, bool OUT>
+__device__ __forceinline__ void cont_feat_step(ContRow& fr, const __nv_bfloat16* rows, int64_t t_first, ContSeq& sq,
+                                               const LayerDims& L, const int32_t* cu, const hla_state& s,
+                                               const int32_t* ext_cu) {
+    constexpr int HALF = kCD / 2;
+    float2 cs_run[2];
+#pragma unroll
+    for (int u = 0; u < kFB; ++u) {
+        const int64_t t = t_first + u;
+        bool live = true;
+        if constexpr (CHECK) {  // warp-uniform
+            live = false;
+            if (t >= 0 && t < L.total) {
+                while (t >= sq.start + sq.len && sq.n + 1 < L.n_seqs) cont_seq_at(L, cu, s, ext_cu, sq.n + 1, sq);
+                live = sq.pos7 >= 0 && t >= sq.start && t < sq.start + sq.len;
             }
         }
-        tok_pos[tid] = p;
-        tok_ext[tid] = e;
-    }
-    __syncthreads();
-    // angles: slot u < 7 for the positions before the first token, 7 + i for token i (at its position)
-    for (int idx = tid; idx < NP * HALF; idx += kCT) {
-        const int u = idx / HALF, ii = idx % HALF;
-        int64_t pp;
-        if (u < kConvHalo) pp = tok_pos[0] < 0 ? -1 : tok_pos[0] - kConvHalo + u;
-        else pp = tok_pos[u - kConvHalo];
-        float c = 1.f, sv = 0.f;
-        if (pp >= 0) rope_cs_exact(pp, L.theta[ii], &c, &sv);
-        cs[u][ii] = c;
-        sn[u][ii] = sv;
-    }
-    __syncthreads();
-    const int r = blockIdx.y * (kCT / 32) + warp;
-    if (r < n_rows) {
-        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-        const int H = kind == 0 ? L.Hq : L.Hkv;
-        const Tin* src = kind == 0 ? q : kind == 1 ? k : v;
-        const float* hist = kind == 0 ? s.conv_q : kind == 1 ? s.conv_k : s.conv_v;
-        float w[E][kConvWidth];
+        const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162*>(rows + u * kCD);
+        const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162*>(rows + u * kCD + HALF);
+        const float2 a0 = __bfloat1622float2(r0), a1 = __bfloat1622float2(r1);
+        float x[4] = {a0.x, a0.y, a1.x, a1.y};  // channels 2l, 2l + 1, 64 + 2l, 64 + 2l + 1
+        if constexpr (ROPE) {
+            if (live) {
+                float2 csn[2];
+                if (CHECK || u == 0) {
+                    const float4 f = __ldg(reinterpret_cast<const float4*>(fr.ang + (size_t)t * HALF));
+                    csn[0] = make_float2(f.x, f.y);
+                    csn[1] = make_float2(f.z, f.w);
+                } else {
 #pragma unroll
-        for (int ee = 0; ee < E; ++ee) {
-            const float4* w4 = reinterpret_cast<const float4*>((kind == 0 ? wq : kind == 1 ? wk : wv) +
-                                                               ((size_t)hh * D + lane + 32 * ee) * kConvWidth);
-            const float4 a4 = w4[0], b4 = w4[1];
-            w[ee][0] = a4.x; w[ee][1] = a4.y; w[ee][2] = a4.z; w[ee][3] = a4.w;
-            w[ee][4] = b4.x; w[ee][5] = b4.y; w[ee][6] = b4.z; w[ee][7] = b4.w;
-        }
-        // the conv input of token t (global row) at position p, angle slot u
-        auto input = [&](int64_t t, int u, float* x) {
-            const Tin* row = src + ((size_t)t * H + hh) * D;
-            if (kind == 2) {
+                    for (int c = 0; c < 2; ++c)
+                        csn[c] = make_float2(cs_run[c].x * fr.step1[c].x - cs_run[c].y * fr.step1[c].y,
+                                             cs_run[c].y * fr.step1[c].x + cs_run[c].x * fr.step1[c].y);
+                }
 #pragma unroll
-                for (int ee = 0; ee < E; ++ee) x[ee] = to_f32(row[lane + 32 * ee]);
-            } else {
-#pragma unroll
-                for (int ee = 0; ee < E / 2; ++ee) {
-                    const int ii = lane + 32 * ee;
-                    const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
-                    x[ee] = x1 * cs[u][ii] - x2 * sn[u][ii];
-                    x[ee + E / 2] = x2 * cs[u][ii] + x1 * sn[u][ii];
+                for (int c = 0; c < 2; ++c) {
+                    cs_run[c] = csn[c];
+                    const float p1 = x[c], p2 = x[2 + c];
+                    x[c] = p1 * csn[c].x - p2 * csn[c].y;
+                    x[2 + c] = p2 * csn[c].x + p1 * csn[c].y;
                 }
             }
-        };
-        float win[kConvWidth][E];  // win[m]: the input at position p - 7 + m
+        }
+        fr.ring[u][0] = make_float2(x[0], x[1]);
+        fr.ring[u][1] = make_float2(x[2], x[3]);
+        if constexpr (OUT) {
+            if (!live) continue;
+            // tap m reads token t - 7 + m (ring slot (u + 1 + m) mod 8); in CHECK mode, taps before the
+            // sequence's first new token read the history entry i + m (position pos - 7 + i + m)
+            const int64_t i = t - sq.start;
+            float2 y2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int m = 0; m < kConvWidth; ++m)
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) win[m][ee] = 0.f;
-        int64_t prev_p = -2;  // position of the last token processed (the window follows it)
-        for (int i = 0; i < kTB; ++i) {
-            const int64_t p = tok_pos[i], t = t0 + i;
-            if (p < 0) {
-                prev_p = -2;
-                continue;
-            }
-            if (p == prev_p + 1) {  // the next token of the same sequence: shift
-#pragma unroll
-                for (int m = 0; m + 1 < kConvWidth; ++m)
-#pragma unroll
-                    for (int ee = 0; ee < E; ++ee) win[m][ee] = win[m + 1][ee];
-            } else {  // a block or sequence start: the 7 inputs before p
-                const int n = seq_of_token(cu, L.n_seqs, t);
-                int64_t start, len;
-                seq_range(cu, n, L.total, &start, &len);
-                const int64_t pos = s.pos[n];
-#pragma unroll
-                for (int m = 0; m < kConvHalo; ++m) {
-                    const int64_t pp = p - kConvHalo + m;
-                    if (pp < 0) {
-#pragma unroll
-                        for (int ee = 0; ee < E; ++ee) win[m][ee] = 0.f;
-                    } else if (pp >= pos) {  // a new token before this block: RoPE at its own position
-                        const Tin* row = src + ((size_t)(t - kConvHalo + m) * H + hh) * D;
-                        float cv[E / 2], sv[E / 2];
-                        if (kind != 2) {
-#pragma unroll
-                            for (int ee = 0; ee < E / 2; ++ee) rope_cs_exact(pp, L.theta[lane + 32 * ee], &cv[ee], &sv[ee]);
-                        }
-#pragma unroll
-                        for (int ee = 0; ee < E / 2; ++ee) {
-                            const int ii = lane + 32 * ee;
-                            if (kind == 2) {
-                                win[m][ee] = to_f32(row[ii]);
-                                win[m][ee + E / 2] = to_f32(row[ii + HALF]);
-                            } else {
-                                const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
-                                win[m][ee] = x1 * cv[ee] - x2 * sv[ee];
-                                win[m][ee + E / 2] = x2 * cv[ee] + x1 * sv[ee];
-                            }
-                        }
-                    } else {  // before the call: the state's history
-                        const float* hr = hist + (((size_t)n * kConvHalo + (size_t)(pp - pos + kConvHalo)) * H + hh) * D;
-#pragma unroll
-                        for (int ee = 0; ee < E; ++ee) win[m][ee] = hr[lane + 32 * ee];
+            for (int m = 0; m < kConvWidth; ++m) {
+                float2 in0 = fr.ring[(u + 1 + m) & (kFB - 1)][0], in1 = fr.ring[(u + 1 + m) & (kFB - 1)][1];
+                if (CHECK && i + m < kConvHalo) {
+                    if (sq.pos7 + i - kConvHalo + m < 0) {
+                        in0 = in1 = make_float2(0.f, 0.f);
+                    } else {
+                        const float* h = fr.hist + ((size_t)sq.n * kConvHalo + (size_t)(i + m)) * fr.hstride;
+                        in0 = *reinterpret_cast<const float2*>(h);
+                        in1 = *reinterpret_cast<const float2*>(h + HALF);
                     }
                 }
+                y2[0] = ffma2(fr.w[0][m], in0, y2[0]);
+                y2[1] = ffma2(fr.w[1][m], in1, y2[1]);
             }
-            input(t, kConvHalo + i, win[kConvWidth - 1]);
-            prev_p = p;
-            float acc[E];
+            if constexpr (NORM) {
+                float ss = y2[0].x * y2[0].x;
+                ss = fmaf(y2[0].y, y2[0].y, ss);
+                ss = fmaf(y2[1].x, y2[1].x, ss);
+                ss = fmaf(y2[1].y, y2[1].y, ss);
 #pragma unroll
-            for (int ee = 0; ee < E; ++ee) {
-                acc[ee] = 0.f;
-#pragma unroll
-                for (int m = 0; m < kConvWidth; ++m) acc[ee] = fmaf(w[ee][m], win[m][ee], acc[ee]);
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float rs = rsqrtf(ss + 1e-6f);
+                y2[0].x *= rs; y2[0].y *= rs; y2[1].x *= rs; y2[1].y *= rs;
             }
-            const size_t o = ((size_t)tok_ext[i] * H + hh) * D;
-            if (kind == 2) {
-#pragma unroll
-                for (int ee = 0; ee < E; ++ee) {
-                    vh[o + lane + 32 * ee] = __float2half_rn(acc[ee]);
-                    ev[o + lane + 32 * ee] = __float2bfloat16_rn(win[kConvWidth - 1][ee]);
-                }
-                continue;
-            }
-            float ss = 0.f;
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) ss = fmaf(acc[ee], acc[ee], ss);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q)) ? rsqrtf(ss + 1e-6f) : 1.f;
-            __half* xr = kind == 0 ? qr : kr;
-            __half* xh = kind == 0 ? qh : kh;
-#pragma unroll
-            for (int ee = 0; ee < E; ++ee) {
-                xr[o + lane + 32 * ee] = __float2half_rn(win[kConvWidth - 1][ee]);
-                xh[o + lane + 32 * ee] = __float2half_rn(acc[ee] * inv);
+            const size_t o = (size_t)(t + sq.off) * fr.rowstride;
+            *reinterpret_cast<__half2*>(fr.hat + o) = __floats2half2_rn(y2[0].x, y2[0].y);
+            *reinterpret_cast<__half2*>(fr.hat + o + HALF) = __floats2half2_rn(y2[1].x, y2[1].y);
+            if constexpr (ROPE) {
+                *reinterpret_cast<__half2*>(fr.rot + o) = __floats2half2_rn(x[0], x[1]);
+                *reinterpret_cast<__half2*>(fr.rot + o + HALF) = __floats2half2_rn(x[2], x[3]);
+            } else {
+                *reinterpret_cast<__nv_bfloat162*>(fr.raw + o) = r0;
+                *reinterpret_cast<__nv_bfloat162*>(fr.raw + o + HALF) = r1;
             }
         }
     }
-    if (blockIdx.y == 0) {  // the gates
-        for (int idx = tid; idx < kTB * L.Hq; idx += kCT) {
-            const int i = idx / L.Hq, h = idx % L.Hq;
-            if (tok_pos[i] < 0) continue;
-            const size_t e = (size_t)tok_ext[i];
-            eg[e * L.Hq + h] = g[(size_t)(t0 + i) * L.Hq + h];
-            eb[e * L.Hq + h] = beta[(size_t)(t0 + i) * L.Hq + h];
+}
+
+template <bool ROPE, bool NORM>
+__device__ __forceinline__ void cont_feat_row(ContRow& fr, const __nv_bfloat16* src, size_t H, unsigned char* wring,
+                                              int64_t tb, int span, const LayerDims& L, const int32_t* cu,
+                                              const hla_state& s, const int32_t* ext_cu, int lane) {
+    constexpr int ROWB = kCD * (int)sizeof(__nv_bfloat16), STEPB = kFB * ROWB, CPT = ROWB / 16;
+    const int n_steps = span / kFB + 1;  // the first step only fills the ring
+    ContSeq sq;
+    cont_seq_at(L, cu, s, ext_cu, seq_of_token(cu, L.n_seqs, tb < 0 ? 0 : tb), sq);
+    // the rows of step `st` into slot st % kFRing, one commit group per step (empty past the end)
+    auto issue = [&](int st) {
+        if (st < n_steps) {
+            unsigned char* dst = wring + (size_t)(st % kFRing) * STEPB;
+#pragma unroll
+            for (int e = lane; e < kFB * CPT; e += 32) {
+                const int u = e / CPT, ch = e % CPT;
+                const int64_t t = tb + (int64_t)kFB * st + u;
+                const bool in = t >= 0 && t < L.total;
+                const __nv_bfloat16* gp = src + (size_t)(in ? t : 0) * H * kCD + ch * 8;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                 (uint32_t)__cvta_generic_to_shared(dst + u * ROWB + ch * 16)),
+                             "l"(gp), "r"(in ? 16u : 0u)
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int st = 0; st < kFRing - 1; ++st) issue(st);
+#pragma unroll 1
+    for (int step = 0; step < n_steps; ++step) {
+        const int64_t t_first = tb + (int64_t)kFB * step;
+        issue(step + kFRing - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kFRing - 1) : "memory");
+        __syncwarp();
+        const __nv_bfloat16* rows = reinterpret_cast<const __nv_bfloat16*>(wring + (size_t)(step % kFRing) * STEPB) +
+                                    2 * lane;
+        if (step == 0) {
+            cont_feat_step<ROPE, NORM, true, false>(fr, rows, t_first, sq, L, cu, s, ext_cu);
+        } else {
+            while (t_first >= sq.start + sq.len && sq.n + 1 < L.n_seqs) cont_seq_at(L, cu, s, ext_cu, sq.n + 1, sq);
+            const bool fast = sq.pos7 >= 0 && t_first >= sq.start + kConvHalo && t_first + kFB <= sq.start + sq.len &&
+                              t_first + kFB <= L.total;
+            if (fast)
+                cont_feat_step<ROPE, NORM, false, true>(fr, rows, t_first, sq, L, cu, s, ext_cu);
+            else
+                cont_feat_step<ROPE, NORM, true, true>(fr, rows, t_first, sq, L, cu, s, ext_cu);
+        }
+        __syncwarp();  // the slot is refilled by the next step's issue
+    }
+}
+
+__global__ void __launch_bounds__(32 * kFW, 4)
+cont_features_kernel(LayerDims L, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                     const __nv_bfloat16* __restrict__ v, const float* __restrict__ wq, const float* __restrict__ wk,
+                     const float* __restrict__ wv, const int32_t* __restrict__ cu, hla_state s,
+                     const int32_t* __restrict__ ext_cu, const float2* __restrict__ ang, __half* __restrict__ qr,
+                     __half* __restrict__ kr, __half* __restrict__ qh, __half* __restrict__ kh,
+                     __half* __restrict__ vh, __nv_bfloat16* __restrict__ ev, int span) {
+    constexpr int D = kCD, HALF = D / 2;
+    extern __shared__ __align__(16) unsigned char ring_s[];  // [warp][kFRing][kFB tokens][D]
+    const int lane = threadIdx.x & 31;
+    unsigned char* wring = ring_s + (size_t)(threadIdx.x >> 5) * kFRing * kFB * D * sizeof(__nv_bfloat16);
+    int head = blockIdx.y * kFW + (threadIdx.x >> 5);
+    if (head >= L.Hq + 2 * L.Hkv) return;  // whole warp; no CTA-wide barrier below
+    int kind = 0;
+    if (head >= L.Hq + L.Hkv) { kind = 2; head -= L.Hq + L.Hkv; }
+    else if (head >= L.Hq) { kind = 1; head -= L.Hq; }
+    const size_t H = kind == 0 ? L.Hq : L.Hkv;
+    const __nv_bfloat16* src = (kind == 0 ? q : (kind == 1 ? k : v)) + (size_t)head * D;
+    ContRow fr;
+    fr.ang = ang + 2 * lane;
+    fr.hist = (kind == 0 ? s.conv_q : (kind == 1 ? s.conv_k : s.conv_v)) + (size_t)head * D + 2 * lane;
+    fr.hstride = H * D;
+    fr.rowstride = H * D;
+    fr.rot = (kind == 0 ? qr : kr) + (size_t)head * D + 2 * lane;
+    fr.hat = (kind == 0 ? qh : (kind == 1 ? kh : vh)) + (size_t)head * D + 2 * lane;
+    fr.raw = ev + (size_t)head * D + 2 * lane;
+    {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(fr.ang + (size_t)L.total * HALF));
+        fr.step1[0] = make_float2(f.x, f.y);
+        fr.step1[1] = make_float2(f.z, f.w);
+    }
+    {  // conv taps: pair j = 0 -> channels 2l, 2l + 1; j = 1 -> 64 + 2l, 64 + 2l + 1
+        const float* wb = (kind == 0 ? wq : (kind == 1 ? wk : wv)) + (size_t)head * D * kConvWidth;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float wc[2][kConvWidth];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float4* w4 = reinterpret_cast<const float4*>(wb + (size_t)(j * HALF + 2 * lane + c) * kConvWidth);
+                const float4 a = __ldg(w4), b = __ldg(w4 + 1);
+                wc[c][0] = a.x; wc[c][1] = a.y; wc[c][2] = a.z; wc[c][3] = a.w;
+                wc[c][4] = b.x; wc[c][5] = b.y; wc[c][6] = b.z; wc[c][7] = b.w;
+            }
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) fr.w[j][m] = make_float2(wc[0][m], wc[1][m]);
         }
     }
+#pragma unroll
+    for (int u = 0; u < kFB; ++u) fr.ring[u][0] = fr.ring[u][1] = make_float2(0.f, 0.f);
+    const int64_t tb = (int64_t)blockIdx.x * span - kFB;
+    if (kind == 2)
+        cont_feat_row<false, false>(fr, src, H, wring, tb, span, L, cu, s, ext_cu, lane);
+    else if (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q))
+        cont_feat_row<true, true>(fr, src, H, wring, tb, span, L, cu, s, ext_cu, lane);
+    else
+        cont_feat_row<true, false>(fr, src, H, wring, tb, span, L, cu, s, ext_cu, lane);
 }
 
 // 6. the new rows of the extended output into out (16-byte copies)
@@ -334,14 +450,18 @@ cont_out_kernel(LayerDims L, const int32_t* __restrict__ cu, hla_state s, const 
     for (int idx = threadIdx.x; idx < L.Hq * kCD / 8; idx += kCT) dst[idx] = src[idx];
 }
 
-// 7. the state after the call: CTA per (sequence, y); y = 0: the pending gates; y = 1 + kv: that kv head's
-// ring entries, pending khat / vhat and conv histories; y = 1 + Hkv + h: q-head h's conv history
+// 7. the state after the call.  CTA per (sequence, y): y = 0: the pending gates; y = 1 + h: q-head h's conv
+// history; y = 1 + Hq + kv: kv head kv's k and v conv histories; y = 1 + Hq + Hkv + kStGroups kv + j: group j
+// of the new rows of kv head kv that stay in the ring (new sinks and the final window) and in the pending
+// ring.  RoPE angles of new tokens come from the table of step 2.  Loads are issued in batches ahead of their
+// stores.
+constexpr int kStGroups = 8;
 template <typename Tin>
 __global__ void __launch_bounds__(kCT)
 cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
                   hla_state s, const int32_t* __restrict__ ext_cu, const __half* __restrict__ kh,
-                  const __half* __restrict__ vh) {
+                  const __half* __restrict__ vh, const float2* __restrict__ ang) {
     constexpr int D = kCD, HALF = D / 2;
     const int n = blockIdx.x, y = blockIdx.y, tid = threadIdx.x;
     const int ns = L.n_sinks, W = L.window, P = W + 1, R = ns + W;
@@ -350,13 +470,12 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
     const int64_t pos = s.pos[n];
     if (pos < 0 || len == 0) return;
     const int64_t p_end = pos + len;
-    const size_t e0 = (size_t)__ldg(ext_cu + n) + (size_t)cont_n_old(pos, ns, W);  // extended row of position pos
-    auto rope = [&](const Tin* row, int c, int64_t p) {
+    // channel c of new token i, RoPE'd (c and c +- d/2 form a pair; the angle from the table)
+    auto rope = [&](const Tin* row, int c, int64_t i) {
         const int ii = c % HALF;
-        float cv, sv;
-        rope_cs_exact(p, L.theta[ii], &cv, &sv);
+        const float2 cs = __ldg(ang + (size_t)(start + i) * HALF + ii);
         const float x1 = to_f32(row[ii]), x2 = to_f32(row[ii + HALF]);
-        return c < HALF ? x1 * cv - x2 * sv : x2 * cv + x1 * sv;
+        return c < HALF ? x1 * cs.x - x2 * cs.y : x2 * cs.x + x1 * cs.y;
     };
     // conv history of a row (H heads, head hh): entry m <- position p_end - 7 + m; the values are all read
     // (old entries from m + len) before any is written
@@ -371,7 +490,7 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
             const int64_t pp = p_end - kConvHalo + m;
             if (pp >= pos) {
                 const Tin* row = src + ((size_t)(start + (pp - pos)) * H + hh) * D;
-                val[u] = rotate ? rope(row, c, pp) : to_f32(row[c]);
+                val[u] = rotate ? rope(row, c, pp - pos) : to_f32(row[c]);
             } else if (pp >= 0) {
                 val[u] = hist[(((size_t)n * kConvHalo + (size_t)(m + len)) * H + hh) * D + c];
             }
@@ -384,54 +503,104 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
         }
     };
     if (y == 0) {  // gates of the new tokens still waiting to be absorbed
+        constexpr int U = 8;
         const int64_t i0 = max((int64_t)0, max(len - W, ns - pos));
-        for (int64_t i = i0 * L.Hq + tid; i < (int64_t)len * L.Hq; i += kCT) {
-            const int64_t tt = i / L.Hq, p = pos + tt;
-            const int h = (int)(i % L.Hq);
-            const size_t gs = ((size_t)n * L.Hq + h) * P + (size_t)(p % P);
-            s.pend_g[gs] = g[(size_t)(start + tt) * L.Hq + h];
-            s.pend_beta[gs] = beta[(size_t)(start + tt) * L.Hq + h];
+        for (int64_t b = i0 * L.Hq + tid; b < len * L.Hq; b += (int64_t)U * kCT) {
+            float gv[U], bv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = b + (int64_t)u * kCT;
+                if (i < len * L.Hq) {
+                    gv[u] = g[(size_t)(start * L.Hq + i)];
+                    bv[u] = beta[(size_t)(start * L.Hq + i)];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = b + (int64_t)u * kCT;
+                if (i >= len * L.Hq) continue;
+                const int64_t tt = i / L.Hq, p = pos + tt;
+                const int h = (int)(i % L.Hq);
+                const size_t gs = ((size_t)n * L.Hq + h) * P + (size_t)(p % P);
+                s.pend_g[gs] = gv[u];
+                s.pend_beta[gs] = bv[u];
+            }
         }
         return;
     }
-    if (y > L.Hkv) {  // a q-head's conv history
-        advance_history(s.conv_q, q, L.Hq, y - 1 - L.Hkv, true);
+    if (y <= L.Hq) {  // a q-head's conv history
+        advance_history(s.conv_q, q, L.Hq, y - 1, true);
         return;
     }
-    const int kv = y - 1;
+    if (y <= L.Hq + L.Hkv) {  // a kv head's conv histories
+        const int kv = y - 1 - L.Hq;
+        advance_history(s.conv_k, k, L.Hkv, kv, true);
+        advance_history(s.conv_v, v, L.Hkv, kv, false);
+        return;
+    }
+    const int kv = (y - 1 - L.Hq - L.Hkv) / kStGroups, grp = (y - 1 - L.Hq - L.Hkv) % kStGroups;
     Tin* kring = static_cast<Tin*>(s.k_ring) + ((size_t)n * L.Hkv + kv) * R * D;
     Tin* vring = static_cast<Tin*>(s.v_ring) + ((size_t)n * L.Hkv + kv) * R * D;
-    // the new tokens that stay in the ring (sinks, and the final window) and in the pending ring
+    // the rows that stay: new sinks [0, i_sink) and the final window [i_win, len); this CTA's share of them
     const int64_t first = max((int64_t)0, min(len, p_end - W - pos));  // index of the first final-window token
-    // the rows that stay: new sinks [0, i_sink) and the final window [i_win, len), all at once
     const int64_t i_sink = min(len, max((int64_t)0, ns - pos));
     const int64_t i_win = max(first, i_sink);
     const int64_t n_rows = i_sink + (len - i_win);
+    const int64_t per = (n_rows + kStGroups - 1) / kStGroups;
+    const int64_t r_lo = min(n_rows, grp * per), r_hi = min(n_rows, r_lo + per);
     auto row_of = [&](int64_t r) { return r < i_sink ? r : i_win + (r - i_sink); };
-    for (int64_t idx = tid; idx < n_rows * HALF; idx += kCT) {  // RoPE'd key pairs (ii, ii + d/2): one angle
-        const int64_t i = row_of(idx / HALF), p = pos + i;
-        const int ii = (int)(idx % HALF);
-        const size_t row = ((size_t)(start + i) * L.Hkv + kv) * D, slot = (size_t)cont_ring_slot(p, ns, W) * D;
-        float cv, sv;
-        rope_cs_exact(p, L.theta[ii], &cv, &sv);
-        const float x1 = to_f32(k[row + ii]), x2 = to_f32(k[row + ii + HALF]);
-        kring[slot + ii] = from_f32<Tin>(x1 * cv - x2 * sv);
-        kring[slot + ii + HALF] = from_f32<Tin>(x2 * cv + x1 * sv);
-    }
-    for (int64_t idx = tid; idx < n_rows * D; idx += kCT) {
-        const int64_t i = row_of(idx / D), p = pos + i;
-        const int c = (int)(idx % D);
-        const size_t row = ((size_t)(start + i) * L.Hkv + kv) * D, slot = (size_t)cont_ring_slot(p, ns, W) * D;
-        vring[slot + c] = v[row + c];
-        if (p >= ns && p >= p_end - W) {
-            const size_t ps = (((size_t)n * L.Hkv + kv) * P + (size_t)(p % P)) * D + c;
-            const size_t er = ((e0 + (size_t)i) * L.Hkv + kv) * D + c;
-            s.pend_k[ps] = __half2float(kh[er]);
-            s.pend_v[ps] = __half2float(vh[er]);
+    const size_t e0 = (size_t)__ldg(ext_cu + n) + (size_t)cont_n_old(pos, ns, W);  // extended row of position pos
+    constexpr int U = 4;
+    for (int64_t b = r_lo * HALF + tid; b < r_hi * HALF; b += (int64_t)U * kCT) {  // RoPE'd key pairs
+        float2 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t idx = b + (int64_t)u * kCT;
+            if (idx >= r_hi * HALF) continue;
+            const int64_t i = row_of(idx / HALF);
+            const int ii = (int)(idx % HALF);
+            const Tin* row = k + ((size_t)(start + i) * L.Hkv + kv) * D;
+            val[u] = make_float2(rope(row, ii, i), rope(row, ii + HALF, i));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t idx = b + (int64_t)u * kCT;
+            if (idx >= r_hi * HALF) continue;
+            const int64_t i = row_of(idx / HALF);
+            const int ii = (int)(idx % HALF);
+            const size_t slot = (size_t)cont_ring_slot(pos + i, ns, W) * D;
+            kring[slot + ii] = from_f32<Tin>(val[u].x);
+            kring[slot + ii + HALF] = from_f32<Tin>(val[u].y);
         }
     }
-    advance_history(s.conv_k, k, L.Hkv, kv, true);
-    advance_history(s.conv_v, v, L.Hkv, kv, false);
+    for (int64_t b = r_lo * D + tid; b < r_hi * D; b += (int64_t)U * kCT) {  // values and pending features
+        Tin vv[U];
+        float pk[U], pv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t idx = b + (int64_t)u * kCT;
+            if (idx >= r_hi * D) continue;
+            const int64_t i = row_of(idx / D);
+            const int c = (int)(idx % D);
+            vv[u] = v[((size_t)(start + i) * L.Hkv + kv) * D + c];
+            const size_t er = ((e0 + (size_t)i) * L.Hkv + kv) * D + c;
+            pk[u] = __half2float(kh[er]);
+            pv[u] = __half2float(vh[er]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t idx = b + (int64_t)u * kCT;
+            if (idx >= r_hi * D) continue;
+            const int64_t i = row_of(idx / D), p = pos + i;
+            const int c = (int)(idx % D);
+            vring[(size_t)cont_ring_slot(p, ns, W) * D + c] = vv[u];
+            if (p >= ns && p >= p_end - W) {
+                const size_t ps = (((size_t)n * L.Hkv + kv) * P + (size_t)(p % P)) * D + c;
+                s.pend_k[ps] = pk[u];
+                s.pend_v[ps] = pv[u];
+            }
+        }
+    }
 }
 
 // 8. pos += len, after every launch above has read it
@@ -454,16 +623,31 @@ cudaError_t launch_continue_table(const LayerDims& L, const int32_t* cu, const h
 
 cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const int32_t* cu, const hla_state& s,
                                  const int32_t* ext_cu, __half* qr, __half* kr, __half* qh, __half* kh, __half* vh,
-                                 __nv_bfloat16* ev, float* eg, float* eb, const __nv_bfloat16* q,
+                                 __nv_bfloat16* ev, float* eg, float* eb, float2* ang, const __nv_bfloat16* q,
                                  const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
                                  const float* wq, const float* wk, const float* wv, cudaStream_t st) {
-    cont_zero_tail_kernel<<<1024, kCT, 0, st>>>(Lx, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb);
+    cont_prep_kernel<<<1024, kCT, 0, st>>>(L, Lx, cu, s, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb, g, beta, ang);
     cont_gather_kernel<<<dim3(L.n_sinks + L.window, L.n_seqs), kCT, 0, st>>>(L, s, ext_cu, qr, kr, qh, kh, vh, ev, eg,
                                                                              eb);
     if (L.total > 0) {
-        const dim3 grid((unsigned)((L.total + kTB - 1) / kTB), (unsigned)((L.Hq + 2 * L.Hkv + kCT / 32 - 1) / (kCT / 32)));
-        cont_features_kernel<__nv_bfloat16><<<grid, kCT, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, cu, s, ext_cu, qr,
-                                                                  kr, qh, kh, vh, ev, eg, eb);
+        static DeviceCache cache;  // CTAs of the feature kernel resident on the device at once
+        int resident = 0;
+        cudaError_t e = device_cached(cache, &resident, [](int dev, int* val) {
+            int n_sm = 0, per_sm = 0;
+            cudaError_t r = sm_count(dev, &n_sm);
+            if (r == cudaSuccess)
+                r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cont_features_kernel, 32 * kFW, kFeatSmem);
+            *val = std::max(1, n_sm * std::max(1, per_sm));
+            return r;
+        });
+        if (e != cudaSuccess) return e;
+        // the smallest multiple of 8 tokens per span for which the grid (spans x row groups) is one wave
+        const int row_groups = (L.Hq + 2 * L.Hkv + kFW - 1) / kFW;
+        const int64_t spans = std::max<int64_t>(1, resident / row_groups);
+        const int64_t span = std::max<int64_t>(kFB, ((L.total + spans - 1) / spans + kFB - 1) / kFB * kFB);
+        const dim3 grid((unsigned)((L.total + span - 1) / span), (unsigned)row_groups);
+        cont_features_kernel<<<grid, 32 * kFW, kFeatSmem, st>>>(L, q, k, v, wq, wk, wv, cu, s, ext_cu, ang, qr, kr, qh,
+                                                                kh, vh, ev, (int)span);
     }
     return cudaGetLastError();
 }
@@ -471,10 +655,10 @@ cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const 
 cudaError_t launch_continue_finish(const LayerDims& L, const int32_t* cu, const hla_state& s, const int32_t* ext_cu,
                                    const __nv_bfloat16* ext_out, __nv_bfloat16* out, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
-                                   const __half* kh, const __half* vh, cudaStream_t st) {
+                                   const __half* kh, const __half* vh, const float2* ang, cudaStream_t st) {
     if (L.total > 0) cont_out_kernel<<<(unsigned)L.total, kCT, 0, st>>>(L, cu, s, ext_cu, ext_out, out);
-    cont_state_kernel<__nv_bfloat16><<<dim3(L.n_seqs, 1 + L.Hkv + L.Hq), kCT, 0, st>>>(L, q, k, v, g, beta, cu, s,
-                                                                                       ext_cu, kh, vh);
+    cont_state_kernel<__nv_bfloat16><<<dim3(L.n_seqs, 1 + L.Hq + L.Hkv * (1 + kStGroups)), kCT, 0, st>>>(
+        L, q, k, v, g, beta, cu, s, ext_cu, kh, vh, ang);
     cont_tc_advance_kernel<<<(L.n_seqs + 127) / 128, 128, 0, st>>>(L, cu, s.pos);
     return cudaGetLastError();
 }

@@ -120,7 +120,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? HLA_OK : HLA_ERR_CUDA
 struct ContLayout {
     WsLayout w;
     int64_t ext_bound;
-    size_t ext_cu, ev, eg, eb, eo, total;
+    size_t ext_cu, ev, eg, eb, eo, ang, total;
 };
 bool continue_on_tensor_cores(const hla_params* prm) { return uses_chunked_gdn(prm); }
 ContLayout cont_layout(const hla_params* prm, int64_t total, int n_seqs) {
@@ -135,6 +135,7 @@ ContLayout cont_layout(const hla_params* prm, int64_t total, int n_seqs) {
     c.eg = off;     off = align_up(off + X * Hq * sizeof(float));
     c.eb = off;     off = align_up(off + X * Hq * sizeof(float));
     c.eo = off;     off = align_up(off + X * Hq * d * sizeof(__nv_bfloat16));
+    c.ang = off;    off = align_up(off + ((size_t)total + 1) * (d / 2) * sizeof(float2));
     c.total = off;
     return c;
 }
@@ -301,8 +302,8 @@ int run_continue_tc(const hla_params* prm, const LayerDims& L, const void* q, co
                           kGdnChunk, nullptr, nullptr};
     HLA_TRY(launch_prefill_tables(Lx, reinterpret_cast<float2*>(ws + w.fine), reinterpret_cast<float2*>(ws + w.coarse),
                                   w.n_coarse, tabs, stream));
-    HLA_TRY(launch_continue_rows(L, Lx, cu, *st, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb, qi, ki, vi, g, beta, wq, wk,
-                                 wv, stream));
+    HLA_TRY(launch_continue_rows(L, Lx, cu, *st, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb,
+                                 reinterpret_cast<float2*>(ws + c.ang), qi, ki, vi, g, beta, wq, wk, wv, stream));
     HLA_TRY(launch_window_softmax_tc(Lx, qr, kr, ev, ext_cu, blk_base, osm, eo, err, false, stream));
     const int n_slots = (int)gdn_chunk_slots(Lx.total, Lx.n_seqs);
     int bound[kGdnParts + 1];
@@ -315,7 +316,7 @@ int run_continue_tc(const hla_params* prm, const LayerDims& L, const void* q, co
                                    stream));
     }
     HLA_TRY(launch_continue_finish(L, cu, *st, ext_cu, eo, static_cast<__nv_bfloat16*>(out), qi, ki, vi, g, beta, kh,
-                                   vh, stream));
+                                   vh, reinterpret_cast<const float2*>(ws + c.ang), stream));
     return HLA_OK;
 }
 

@@ -292,13 +292,13 @@ cudaError_t launch_continue_table(const LayerDims& L, const int32_t* cu, const h
                                   cudaStream_t st);
 cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const int32_t* cu, const hla_state& s,
                                  const int32_t* ext_cu, __half* qr, __half* kr, __half* qh, __half* kh, __half* vh,
-                                 __nv_bfloat16* ev, float* eg, float* eb, const __nv_bfloat16* q,
+                                 __nv_bfloat16* ev, float* eg, float* eb, float2* ang, const __nv_bfloat16* q,
                                  const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
                                  const float* wq, const float* wk, const float* wv, cudaStream_t st);
 cudaError_t launch_continue_finish(const LayerDims& L, const int32_t* cu, const hla_state& s, const int32_t* ext_cu,
                                    const __nv_bfloat16* ext_out, __nv_bfloat16* out, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
-                                   const __half* kh, const __half* vh, cudaStream_t st);
+                                   const __half* kh, const __half* vh, const float2* ang, cudaStream_t st);
 
 // Sink + window softmax with the lambda-weighted linear branch added.
 template <typename Tin, typename Tf>

@@ -205,3 +205,64 @@ def test_negative_position_is_flagged_and_left_alone(d):
     half = lambda t: t.view(2, -1)[1]  # noqa: E731  sequence 1's part of a per-sequence buffer
     for name, b in before.items():
         assert torch.equal(half(st.view(name)), half(b)), name
+
+
+def test_continue_layer_shape_wide_spans(oracle_mod):
+    # the LLaMA-3.1-8B layer shape (32 q-heads, 8 kv-heads) with about 4,200 new tokens: the feature kernel's
+    # token spans are then many steps long (one wave of CTAs), and steps cross sequence starts inside a span
+    first, second = [600, 3000, 5], [2500, 1700, 13]
+    wl = synth.small("cont wide", first, n_q_heads=32, n_kv_heads=8, head_dim=128)
+    x1 = synth.make_inputs(wl, "cuda")
+    x2 = _inputs(wl, second, synth.BASE_SEED + 45)
+    prm = params_for(wl)
+    st = hla.State(prm, 3).init()
+    hla.prefill(prm, *_args(x1), torch.empty_like(x1["q"]), state=st)
+    out2 = torch.full_like(x2["q"], float("nan"))
+    hla.prefill_continue(prm, *_args(x2), out2, st)
+    # every head: the same sequences in one prefill
+    xw = {key: torch.cat([torch.cat([_rows(x1, key, n), _rows(x2, key, n)]) for n in range(3)])
+          for key in ("q", "k", "v", "g", "beta")}
+    xw.update({key: x1[key] for key in ("wq", "wk", "wv", "lam")})
+    lens = [a + b for a, b in zip(first, second)]
+    xw["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device="cuda")
+    st_w = hla.State(prm, 3).init()
+    out_w = torch.empty_like(xw["q"])
+    hla.prefill(prm, *_args(xw), out_w, state=st_w)
+    torch.cuda.synchronize()
+    assert st.check_error() == 0
+    cw, c2 = xw["cu_seqlens"].tolist(), x2["cu_seqlens"].tolist()
+    for n in range(3):
+        assert_close(_np(out2[c2[n]:c2[n + 1]]), _np(out_w[cw[n] + first[n]:cw[n + 1]]), "bf16", f"seq {n} vs one prefill")
+    for name in ("S", "k_ring", "v_ring", "conv_q", "conv_k", "conv_v"):
+        assert_close(st.view(name).float().cpu().numpy(), st_w.view(name).float().cpu().numpy(), "bf16", name)
+    # the pending ring on its live slots (the tokens still waiting; the slot of the token absorbed last is
+    # never read again and keeps whatever the earlier call left there)
+    P = wl.window + 1
+    for name, heads in (("pend_k", 8), ("pend_v", 8), ("pend_g", 32), ("pend_beta", 32)):
+        a = st.view(name).float().cpu().numpy().reshape(3, heads, P, -1)
+        b = st_w.view(name).float().cpu().numpy().reshape(3, heads, P, -1)
+        for n, L in enumerate(lens):
+            live = [p % P for p in range(max(L - wl.window, wl.n_sinks), L)]
+            assert_close(a[n][:, live], b[n][:, live], "bf16", f"{name} seq {n}")
+    # sampled heads (three kv groups) against the oracle
+    for n in (0, 1):
+        for h in (0, 13, 31):
+            ref = _oracle(wl, [x1, x2], n, h, oracle_mod)
+            assert_close(_np(out2[c2[n]:c2[n + 1], h]), ref["o"][first[n]:], "bf16", f"seq {n} head {h}")
+            S = st.view("S").view(3, 32, 128, 128)[n, h].cpu().numpy()
+            assert_close(S, ref["S"], "bf16", f"S seq {n} head {h}")
+
+
+def test_overlapping_sequences_are_flagged():
+    # sequences 0 and 2 overlap (cu not monotone): their extended rows would add up past the workspace's
+    # bound, so the table is flagged and every row stays inside the workspace
+    wl = synth.small("cont overlap", [100, 80, 60], n_q_heads=4, n_kv_heads=2, head_dim=128)
+    x1 = synth.make_inputs(wl, "cuda")
+    x2 = _inputs(wl, [45, 0, 5], synth.BASE_SEED + 46)
+    x2["cu_seqlens"] = torch.tensor([0, 45, 5, 50], dtype=torch.int32, device="cuda")
+    prm = params_for(wl)
+    st = hla.State(prm, 3).init()
+    hla.prefill(prm, *_args(x1), torch.empty_like(x1["q"]), state=st)
+    hla.prefill_continue(prm, *_args(x2), torch.empty_like(x2["q"]), st)
+    torch.cuda.synchronize()
+    assert st.check_error() == 1  # the sequence-table error
