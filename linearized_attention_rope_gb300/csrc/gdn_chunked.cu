@@ -23,24 +23,28 @@
 // fp16 operands in shared memory, fp32 accumulators in TMEM; the zero blocks
 // pad the 64-row operands to M = 128.  S0, V, U are MN-major B operands (one
 // 128-byte row per key dim or token), so every epilogue thread writes its
-// own row.  S0 stays in fp32 registers (one key row per thread) and is
+// own row.  S0 stays in fp32 registers (32 columns of a key row per thread) and is
 // re-rounded to fp16 for the next chunk's MMA.
 //
-// Roles (256 threads; the rest of warps 4-5 idle): one thread of warp 4 loads chunk c+1 into the other
-// buffer (TMA: tensor copies of the query, key and value rows, bulk copies
-// of the record) and starts its D1 with the S-independent [T diag(beta) ; 0] V;
-// warps 0-3 run the chain: D1 += [-Wm ; Q] S0, the U epilogue, DS and then
-// D2 (whose issue hides under DS's latency), the S epilogue; warps 6-7 turn
-// the double-buffered D1/D2 rows 64..127 into the layer output of their
-// positions: out = o_sm + lambda_h (gamma Q S0 + P U), o_sm being the
-// normalised softmax branch the softmax kernel left for these rows.  Handoffs use mbarriers: loaded[b] (TMA bytes),
-// ready[b] (the V MMAs -> chain), free[b] (chain + output -> load), ofull[b]
-// (MMA -> output).  Token rows past a chunk's end hold whatever follows
-// (zeros past the tensor): they meet zero rows of -Wm, T diag(beta) and U,
-// or produce output rows that are not stored.  Every wait has an iteration limit; on expiry the kernel records
-// a timeout in the error word and all roles stop.  Loops stay rolled
-// where registers allow: the whole kernel is executed once per chunk by
-// every role, and compact code keeps it resident in the instruction cache.
+// Roles (384 threads; the rest of warps 8-9 idle).  One thread of warp 8 loads chunk c+2 into the buffer
+// of chunk c (TMA: tensor copies of the query, key and value rows, bulk copies of the record), each of
+// three groups as soon as chunk c is done with its region (T diag(beta) and V once its V product
+// completed, [-Wm ; Q] once its D1 product completed, P, K and the gate vectors once it was released),
+// and queues chunk c+1's S-independent D1 = [T diag(beta) ; 0] V right after chunk c's D1 product, so
+// the tensor pipe runs it while the chain forms U.  Warps 0-7 run the chain (warps w and w + 4 on the
+// same TMEM lanes, each with half of the slice's columns): D1 += [-Wm ; Q] S0, the U epilogue, DS, the S
+// epilogue.  One thread of warp 9 queues D2 behind DS.  Warps 10-11 turn the
+// double-buffered D1/D2 rows 64..127 into the layer output of their positions:
+// out = o_sm + lambda_h (gamma Q S0 + P U), o_sm being the normalised softmax branch the softmax kernel
+// left for these rows.  Handoffs use mbarriers: loadedv[b] and loaded[b] (TMA bytes of the V product's
+// operands and of the rest), ready[b] (the V product's commit and the loader's arrival once every byte is
+// in -> chain and load), d1done[b] (the chain's D1 MMAs -> load), dsqueued[b] (chain -> D2 issue),
+// free[b] (chain + output -> load), ofull[b] (D2 -> output).  Token rows past a chunk's end hold
+// whatever follows (zeros past the tensor): they meet zero rows of -Wm, T diag(beta) and U, or produce
+// output rows that are not stored.  Every wait has an iteration limit; on expiry the kernel records a
+// timeout in the error word and all roles stop.  Loops stay rolled where registers allow: the whole
+// kernel is executed once per chunk by every role, and compact code keeps it resident in the instruction
+// cache.
 #include "hla_common.cuh"
 #include "tma.cuh"
 #include "umma.cuh"
@@ -53,7 +57,7 @@ constexpr int kC = kGdnChunk;  // chunk length (absorbed tokens)
 constexpr int kD = 128;   // head dim
 constexpr int kNS = 64;   // value columns per CTA
 constexpr int kSlices = kD / kNS;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 // shared-memory plan (bytes from a 1024-aligned base); one chunk buffer:
@@ -65,17 +69,19 @@ constexpr uint32_t kVec = 81920;    // gamma[64], key decay[64]
 constexpr uint32_t kBuf = 82944;
 // chain operands
 constexpr uint32_t kS = 2 * kBuf;   // S0 slice rows 128 x 64 (MN-major B)
-constexpr uint32_t kU = kS + 16384;   // U slice rows 64 x 64 (MN-major B)
-constexpr uint32_t kUk = kU + 8192;   // diag(key decay) U
+constexpr uint32_t kU = kS + 16384;     // U slice rows 64 x 64 (MN-major B), one per buffer
+constexpr uint32_t kUk = kU + 2 * 8192;  // diag(key decay) U
 constexpr uint32_t kBar = kUk + 8192;
-constexpr uint32_t kSmemAlloc = kBar + 128 + 1024;
+constexpr uint32_t kSmemAlloc = kBar + 256 + 1024;
 // TMEM columns
 constexpr uint32_t kColD1 = 0, kColD2 = 128, kColS = 256, kTmemCols = 512;
 
 // mbarrier indices
-constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kNumBars = 10;
-static_assert(8 * kNumBars + 8 + 32 <= 128, "barrier area: mbarriers, TMEM base, abort flag, 2 slots x 4 ids");
+constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kD1Done = 10, kLoadedV = 12,
+              kDsQueued = 14, kNumBars = 16;
+static_assert(8 * kNumBars + 8 + 32 <= 256, "barrier area: mbarriers, TMEM base, abort flag, 2 slots x 4 ids");
 constexpr uint32_t kLoadBytes = kRecordBytes + 5 * 8192;  // record + query, key rows (2 boxes each) + value slice
+constexpr uint32_t kLoadVBytes = 2 * 8192;                // T diag(beta) + value slice (the V product's operands)
 
 __device__ __forceinline__ void st16(unsigned char* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -86,12 +92,6 @@ __device__ __forceinline__ uint4 pack8(const float* v, float s) {
     return make_uint4(pack_h2(v[0] * s, v[1] * s), pack_h2(v[2] * s, v[3] * s), pack_h2(v[4] * s, v[5] * s),
                       pack_h2(v[6] * s, v[7] * s));
 }
-// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // barrier among the `count` threads of one role (ids 1-3; 0 is __syncthreads)
 __device__ __forceinline__ void group_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -134,7 +134,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) umma::mbar_init(bar(i), (i == kFree || i == kFree + 1) ? 2 : 1);
+        for (int i = 0; i < kNumBars; ++i)
+            umma::mbar_init(bar(i), (i == kFree || i == kFree + 1 || i == kReady || i == kReady + 1) ? 2 : 1);
         umma::fence_mbar_init();
         *abort_flag = 0;
     }
@@ -199,24 +200,27 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
         return w;
     };
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ================= the state chain =================
-        float S[kNS];  // S0[tid][slice columns]: fp32 master copy
+        // key row `row` (the thread's TMEM lane), value columns col0 .. col0 + 31 of the slice: warps w and
+        // w + 4 share a lane quarter and split its columns
+        const int row = tid & 127, col0 = 32 * (warp >> 2);
+        float S[32];  // S0[row][col0 ..]: fp32 master copy
 #pragma unroll
-        for (int i = 0; i < kNS; ++i) S[i] = 0.f;
+        for (int i = 0; i < 32; ++i) S[i] = 0.f;
         if (resume) {  // the saved state and its fp16 image (the zero image above is overwritten)
-            const float* src = S_src + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
+            const float* src = S_src + (((size_t)n * L.Hq + h) * kD + row) * kD + slice * kNS + col0;
 #pragma unroll
-            for (int i = 0; i < kNS; i += 4) {
+            for (int i = 0; i < 32; i += 4) {
                 const float4 x = *reinterpret_cast<const float4*>(src + i);
                 S[i] = x.x; S[i + 1] = x.y; S[i + 2] = x.z; S[i + 3] = x.w;
             }
 #pragma unroll
-            for (int j = 0; j < kNS / 8; ++j)
-                st16(sm + kS + umma::sw128_offset(tid, 8 * j, 128), pack8(S + 8 * j, 1.f));
+            for (int j = 0; j < 4; ++j)
+                st16(sm + kS + umma::sw128_offset(row, col0 + 8 * j, 128), pack8(S + 8 * j, 1.f));
             umma::fence_async_smem();
             umma::fence_before_sync();
-            group_sync(1, 128);
+            group_sync(1, 256);
         }
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
         const uint32_t id_ab = umma::idesc_f16(128, kNS, true, true, false);
@@ -229,7 +233,8 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
             const uint32_t buf = (uint32_t)b * kBuf;
             // ready[b]: the chunk is loaded and D1[b] holds [T diag(beta) ; 0] V; the
             // loader waited for free[b], so the output rows of chunk c - 2 are out of D1/D2[b]
-            if (!(ok = role_wait(kReady + b, (uint32_t)((c >> 1) & 1), 1, 128, tid == 0, kr))) break;
+            if (!(ok = role_wait(kReady + b, (uint32_t)((c >> 1) & 1), 1, 256, tid == 0, kr))) break;
+            const uint32_t ub = kU + (uint32_t)b * 8192u;  // this chunk's U image
 
             // D1[b] += [-Wm ; Q] S0
             if (tid == 0) {
@@ -238,102 +243,152 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
 #pragma unroll
                 for (int s = 0; s < kD / 16; ++s) umma::mma(d1, a1 + kstep128(s), bs + mnstep(s), id_b, true);
                 umma::commit(bar(kMma1));
+                umma::commit(bar(kD1Done + b));
             }
-            if (!(ok = role_wait(kMma1, ph1, 1, 128, tid == 0, kr))) break;
+            if (!(ok = role_wait(kMma1, ph1, 1, 256, tid == 0, kr))) break;
             ph1 ^= 1u;
 
             // U (rows 0..63) -> fp16 rows of U and diag(key decay) U
-            if (warp < 2) {
-                const float kd = reinterpret_cast<const float*>(sm + buf + kVec)[kC + tid];
-#pragma unroll 1
-                for (int q = 0; q < 2; ++q) {
-                    float u[32];
-                    umma::tmem_ld32(tmem + lane_base + kColD1 + kNS * b + 32 * q, u);
+            if (row < kC) {
+                const float kd = reinterpret_cast<const float*>(sm + buf + kVec)[kC + row];
+                uint32_t u[32];
+                umma::tmem_ld32_async(tmem + lane_base + kColD1 + kNS * b + col0, u);
+                umma::tmem_wait_ld();
+                umma::reg_fence32(u);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t off = umma::sw128_offset(tid, 32 * q + 8 * j, 64);
-                        st16(sm + kU + off, pack8(u + 8 * j, 1.f));
-                        st16(sm + kUk + off, pack8(u + 8 * j, kd));
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(u[8 * j + e]);
+                    const uint32_t off = umma::sw128_offset(row, col0 + 8 * j, 64);
+                    st16(sm + ub + off, pack8(x, 1.f));
+                    st16(sm + kUk + off, pack8(x, kd));
                 }
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
-            group_sync(1, 128);
+            group_sync(1, 256);
 
-            // DS = K^T diag(key decay) U (the chain waits for this), then D2[b] = [0 ; P] U
+            // DS = K^T diag(key decay) U, which the chain waits for; the output role queues D2[b] = [0 ; P] U
+            // behind it
             if (tid == 0) {
                 umma::fence_after_sync();
-                const uint64_t zp = umma::kmajor(sbase + buf + kTZP + 8192, 128, 0), bu = umma::mnmajor(sbase + kU, 8192u, 0);
                 const uint64_t ak = umma::mnmajor(sbase + buf + kK, 8192u, 0), buk = umma::mnmajor(sbase + kUk, 8192u, 0);
 #pragma unroll
                 for (int s = 0; s < kC / 16; ++s) umma::mma(tmem + kColS, ak + mnstep(s), buk + mnstep(s), id_ab, s > 0);
                 umma::commit(bar(kMma2));
-#pragma unroll
-                for (int s = 0; s < kC / 16; ++s)
-                    umma::mma(tmem + kColD2 + kNS * b, zp + kstep128(s), bu + mnstep(s), id_b, s > 0);
-                umma::commit(bar(kOFull + b));
+                mbar_arrive(bar(kDsQueued + b));
             }
-            if (!(ok = role_wait(kMma2, ph2, 1, 128, tid == 0, kr))) break;
-            ph2 ^= 1u;
             const float gC = reinterpret_cast<const float*>(sm + buf + kVec)[kC - 1];  // gamma_C
-            group_sync(1, 128);
-            // the chain is done with buffer b (D2's reads of it end before the output arrives)
+            if (!(ok = role_wait(kMma2, ph2, 1, 256, tid == 0, kr))) break;
+            ph2 ^= 1u;
+            // the chain is done with buffer b (every thread read gamma_C before the wait's barrier; D2's reads
+            // of the buffer end before the output role arrives)
             if (tid == 0) mbar_arrive(bar(kFree + b));
 
             // S <- gamma_C S + DS; fp16 row for the next chunk
+            {
+                uint32_t ds[32];
+                umma::tmem_ld32_async(tmem + lane_base + kColS + col0, ds);
+                umma::tmem_wait_ld();
+                umma::reg_fence32(ds);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float ds[32];
-                umma::tmem_ld32(tmem + lane_base + kColS + 32 * q, ds);
+                for (int i = 0; i < 32; ++i) S[i] = fmaf(gC, S[i], __uint_as_float(ds[i]));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) S[32 * q + i] = fmaf(gC, S[32 * q + i], ds[i]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    st16(sm + kS + umma::sw128_offset(tid, 32 * q + 8 * j, 128), pack8(S + 32 * q + 8 * j, 1.f));
+                for (int j = 0; j < 4; ++j) st16(sm + kS + umma::sw128_offset(row, col0 + 8 * j, 128), pack8(S + 8 * j, 1.f));
             }
+            // the barrier of the next chunk's ready wait orders these rows before its D1 MMAs
             umma::fence_async_smem();
             umma::fence_before_sync();
-            group_sync(1, 128);
         }
         if (ok && S_out) {
-            float* dst = S_out + (((size_t)n * L.Hq + h) * kD + tid) * kD + slice * kNS;
+            float* dst = S_out + (((size_t)n * L.Hq + h) * kD + row) * kD + slice * kNS + col0;
 #pragma unroll
-            for (int i = 0; i < kNS; i += 4)
+            for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
         }
-    } else if (tid == 128) {
-        // ================= loads, one chunk ahead (one thread) =================
+    } else if (tid == 256) {
+        // ================= loads, one chunk ahead of the V products (one thread) =================
+        // Iteration c: chunk c's T diag(beta) and V (once chunk c - 2's V product completed) and [-Wm ; Q]
+        // (once its D1 product completed); chunk c - 1's V product, after chunk c - 2's D1 product so that
+        // it runs while the chain forms U; chunk c - 1 released to the chain once all its bytes are in
+        // (ready[b] takes the V product's commit and that arrival); then chunk c's P, gate vectors and key
+        // rows once chunk c - 2 was released by the chain and the output role (which also frees D1/D2 of
+        // the buffer in TMEM).
         const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
         int kl = 0;  // (unused by one-thread waits)
-#pragma unroll 1
-        for (int c = 0; c < (stall ? 0 : n_chunks); ++c) {
+        auto loads_early = [&](int c) -> bool {
             const int b = c & 1;
-            if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true, kl)) break;
-            const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
-            const int tok = (int)(start + L.n_sinks + (int64_t)(c_lo + c) * kC);  // first absorbed token of the chunk
+            const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b), ldv = bar(kLoadedV + b);
+            const uint32_t prev = (uint32_t)(((c - 2) >> 1) & 1);  // phase of chunk c - 2 (same buffer)
+            const int tok = (int)(start + L.n_sinks + (int64_t)(c_lo + c) * kC);  // first absorbed token
             const unsigned char* rec = rec_in + ((size_t)(slot0 + c_lo + c) * L.Hq + h) * kRecordBytes;
-            tma::expect_tx(ld, kLoadBytes);
+            if (c >= 2 && !role_wait(kReady + b, prev, 0, 0, true, kl)) return false;
+            tma::expect_tx(ldv, kLoadVBytes);
+            tma::bulk_load(buf + kTZP, rec + kRecTb, 8192, ldv);
+            tma::tensor_load_3d(buf + kV, &map_v, slice * kNS, kv, tok, ldv);
+            if (c >= 2 && !role_wait(kD1Done + b, prev, 0, 0, true, kl)) return false;
+            tma::expect_tx(ld, kLoadBytes - kLoadVBytes);
             tma::bulk_load(buf + kA1, rec + kRecWm, 8192, ld);                   // -Wm, key dims 0..63
             tma::bulk_load(buf + kA1 + 16384, rec + kRecWm + 8192, 8192, ld);    // key dims 64..127
-            tma::bulk_load(buf + kTZP, rec + kRecTb, 8192, ld);
-            tma::bulk_load(buf + kTZP + 16384, rec + kRecP, 8192, ld);
-            tma::bulk_load(buf + kVec, rec + kRecVec, kRecordBytes - kRecVec, ld);
             tma::tensor_load_3d(buf + kA1 + 8192, &map_q, 0, h, tok + W, ld);    // query rows (positions j + W)
             tma::tensor_load_3d(buf + kA1 + 16384 + 8192, &map_q, 64, h, tok + W, ld);
+            return true;
+        };
+        auto loads_late = [&](int c) -> bool {
+            const int b = c & 1;
+            const uint32_t buf = sbase + (uint32_t)b * kBuf, ld = bar(kLoaded + b);
+            const int tok = (int)(start + L.n_sinks + (int64_t)(c_lo + c) * kC);
+            const unsigned char* rec = rec_in + ((size_t)(slot0 + c_lo + c) * L.Hq + h) * kRecordBytes;
+            if (c >= 2 && !role_wait(kFree + b, (uint32_t)(((c - 2) >> 1) & 1), 0, 0, true, kl)) return false;
+            tma::bulk_load(buf + kTZP + 16384, rec + kRecP, 8192, ld);
+            tma::bulk_load(buf + kVec, rec + kRecVec, kRecordBytes - kRecVec, ld);
             tma::tensor_load_3d(buf + kK, &map_k, 0, kv, tok, ld);
             tma::tensor_load_3d(buf + kK + 8192, &map_k, 64, kv, tok, ld);
-            tma::tensor_load_3d(buf + kV, &map_v, slice * kNS, kv, tok, ld);
-            if (!role_wait(kLoaded + b, (uint32_t)((c >> 1) & 1), 0, 0, true, kl)) break;
-            // D1[b] = [T diag(beta) ; 0] V; its completion releases the chunk to the chain
+            return true;
+        };
+        // D1[b] = [T diag(beta) ; 0] V, committed to ready[b]; then, once every byte of the chunk is in,
+        // ready[b]'s other arrival
+        auto start_chunk = [&](int c) -> bool {
+            const int b = c & 1;
+            const uint32_t buf = sbase + (uint32_t)b * kBuf, par = (uint32_t)((c >> 1) & 1);
+            if (!role_wait(kLoadedV + b, par, 0, 0, true, kl)) return false;
+            if (c >= 1 && !role_wait(kD1Done + (b ^ 1), (uint32_t)(((c - 1) >> 1) & 1), 0, 0, true, kl)) return false;
             const uint64_t tb = umma::kmajor(buf + kTZP, 128, 0), bv = umma::mnmajor(buf + kV, 8192u, 0);
 #pragma unroll
             for (int s = 0; s < kC / 16; ++s) umma::mma(tmem + kColD1 + kNS * b, tb + kstep128(s), bv + mnstep(s), id_b, s > 0);
             umma::commit(bar(kReady + b));
+            if (!role_wait(kLoaded + b, par, 0, 0, true, kl)) return false;
+            mbar_arrive(bar(kReady + b));
+            return true;
+        };
+        const int n_load = stall ? 0 : n_chunks;
+#pragma unroll 1
+        for (int c = 0; c <= n_load; ++c) {
+            if (c < n_load && !loads_early(c)) break;
+            if (c >= 1 && !start_chunk(c - 1)) break;
+            if (c < n_load && !loads_late(c)) break;
         }
-    } else if (warp >= 6) {
+    } else if (tid == 288) {
+        // ================= D2[b] = [0 ; P] U (one thread) =================
+        // queued once the chain has queued its DS, so it runs behind DS, beside the S epilogue.  D2[b] in TMEM
+        // was read out for chunk c - 2 and U[b] is rewritten for chunk c + 2 only: the chain starts a chunk
+        // once its last load group is in, which waits for the output role to release the chunk two back.
+        const uint32_t id_b = umma::idesc_f16(128, kNS, false, true, false);
+        int kq = 0;  // (unused by one-thread waits)
+#pragma unroll 1
+        for (int c = 0; c < n_chunks; ++c) {
+            const int b = c & 1;
+            if (!role_wait(kDsQueued + b, (uint32_t)((c >> 1) & 1), 0, 0, true, kq)) break;
+            const uint64_t zp = umma::kmajor(sbase + (uint32_t)b * kBuf + kTZP + 8192, 128, 0);
+            const uint64_t bu = umma::mnmajor(sbase + kU + (uint32_t)b * 8192u, 8192u, 0);
+#pragma unroll
+            for (int s = 0; s < kC / 16; ++s) umma::mma(tmem + kColD2 + kNS * b, zp + kstep128(s), bu + mnstep(s), id_b, s > 0);
+            umma::commit(bar(kOFull + b));
+        }
+    } else if (warp >= 10) {
         // ================= output rows: o_sm + lambda_h (gamma (Q S0) + P U) =================
-        const int r = tid - 192;  // chunk row; TMEM lane 64 + r
+        const int r = tid - 320;  // chunk row; TMEM lane 64 + r
         const bool emit = out && !(L.flags & HLA_FLAG_LINEAR_OFF);
         const float lam = __ldg(lambda + h);
         int ko = 0;
