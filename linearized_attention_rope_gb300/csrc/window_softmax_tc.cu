@@ -72,11 +72,12 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
     const int G = L.G, QB = kD / G;
     const int qi = row / G, gq = row % G;
     const uint32_t sbase = umma::smem_addr(sm);
-    const uint32_t bar_ld = umma::smem_addr(sm + kBar), bar_mma = bar_ld + 8;
+    const uint32_t bar_ld = umma::smem_addr(sm + kBar), bar_mma = bar_ld + 8, bar_q = bar_ld + 24;
     const float qscale = 0.088388347648318447f * 1.4426950408889634f;  // 1/sqrt(128) * log2(e)
     if (tid == 0) {
         umma::mbar_init(bar_ld, 1);
         umma::mbar_init(bar_mma, 1);
+        umma::mbar_init(bar_q, 1);
         umma::fence_mbar_init();
     }
     if (warp == 0) umma::tmem_alloc(tmem_slot, kTmemCols);
@@ -98,7 +99,7 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
         return;
     }
-    uint32_t ph_ld = 0, ph_mma = 0;
+    uint32_t ph_ld = 0, ph_mma = 0, ph_q = 0;
 
     // tid 0 waits with a bound; the CTA then agrees on the outcome
     auto cta_wait = [&](uint32_t mbar, uint32_t& ph) -> bool {
@@ -113,26 +114,84 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         return ok;
     };
 
-    const bool sm_on = !(L.flags & HLA_FLAG_SOFTMAX_OFF), lin_off = (L.flags & HLA_FLAG_LINEAR_OFF) != 0;
-    bool ok = true;
-#pragma unroll 1
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int kv = (int)(item / n_blocks);
+    // an item's block of query positions and its key slots [sinks (padded to 8) | window span]
+    struct Item {
+        int kv, sink_pad, n_slots, n_groups;
+        int64_t start, pa, pb, n_sink, span_lo;
+    };
+    auto describe = [&](int64_t item) {
+        Item it;
+        it.kv = (int)(item / n_blocks);
         const int blk = (int)(item % n_blocks);
         int lo = 0, hi = L.n_seqs - 1;  // sequence owning the block
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (__ldg(blk_base + mid) <= blk) lo = mid; else hi = mid - 1;
         }
-        int64_t start, len;
-        seq_range(cu, lo, L.total, &start, &len);
-        const int64_t pa = (int64_t)(blk - __ldg(blk_base + lo)) * QB, pb = min(len, pa + QB);
-        const int64_t n_sink = min((int64_t)L.n_sinks, pb);
-        const int sink_pad = (int)((n_sink + 7) & ~7);
-        const int64_t span_lo = max((int64_t)L.n_sinks, pa - L.window + 1);
-        const int64_t n_span = pb > span_lo ? pb - span_lo : 0;
-        const int n_slots = (int)((sink_pad + n_span + 15) & ~15);
-        const int n_groups = (n_slots + kGroup - 1) / kGroup;
+        int64_t len;
+        seq_range(cu, lo, L.total, &it.start, &len);
+        it.pa = (int64_t)(blk - __ldg(blk_base + lo)) * QB;
+        it.pb = min(len, it.pa + QB);
+        it.n_sink = min((int64_t)L.n_sinks, it.pb);
+        it.sink_pad = (int)((it.n_sink + 7) & ~7);
+        it.span_lo = max((int64_t)L.n_sinks, it.pa - L.window + 1);
+        const int64_t n_span = it.pb > it.span_lo ? it.pb - it.span_lo : 0;
+        it.n_slots = (int)((it.sink_pad + n_span + 15) & ~15);
+        it.n_groups = (it.n_slots + kGroup - 1) / kGroup;
+        return it;
+    };
+    // the query tile (thread 0)
+    auto issue_q = [&](const Item& it) {
+        if (tid == 0) {
+            tma::expect_tx(bar_q, 32768u);
+            const int tq = (int)(it.start + it.pa);
+            tma::tensor_load_3d(sbase + kQ, &map_q, 0, it.kv * G, tq, bar_q);
+            tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, it.kv * G, tq, bar_q);
+        }
+    };
+    // one group's keys and values (every thread): thread 0 posts the byte count; box b goes to lane b / 8
+    // of warp b % 8, so the copies are issued by all warps at once (copies issued back to back by one
+    // thread serialise; an early complete_tx just leaves the count below zero until the post); boxes of
+    // 8 slots, a 64-slot run of window rows at a 64-aligned offset is one box
+    auto issue_kv = [&](const Item& it, int grp) {
+        const int g0 = grp * kGroup, n = min(kGroup, it.n_slots - g0);
+        if (tid == 0) tma::expect_tx(bar_ld, (uint32_t)n * 2u * 2u * 128u);
+        for (int j = 8 * (warp + 8 * lane); j < n; j += 8 * kThreads) {
+            const int slot = g0 + j;
+            const bool wide = slot >= it.sink_pad && (j & 63) == 0 && j + 64 <= n;
+            const bool covered = slot >= it.sink_pad && (j & 63) != 0 && (j & ~63) + 64 <= n &&
+                                 g0 + (j & ~63) >= it.sink_pad;  // inside a wide box issued by another lane
+            if (covered) continue;
+            const int tk = (int)(it.start + (slot < it.sink_pad ? slot : it.span_lo + (slot - it.sink_pad)));
+            const uint32_t off = (uint32_t)j * 128u;
+            const CUtensorMap* mk = wide ? &map_k64 : &map_k;
+            const CUtensorMap* mv = wide ? &map_v64 : &map_v;
+            tma::tensor_load_3d(sbase + kK + off, mk, 0, it.kv, tk, bar_ld);
+            tma::tensor_load_3d(sbase + kK + 16384 + off, mk, 64, it.kv, tk, bar_ld);
+            tma::tensor_load_3d(sbase + kV + off, mv, 0, it.kv, tk, bar_ld);
+            tma::tensor_load_3d(sbase + kV + 16384 + off, mv, 64, it.kv, tk, bar_ld);
+        }
+    };
+
+    const bool sm_on = !(L.flags & HLA_FLAG_SOFTMAX_OFF), lin_off = (L.flags & HLA_FLAG_LINEAR_OFF) != 0;
+    bool ok = true;
+    // The next item's loads are issued while this one finishes: its query tile once this item's last
+    // Q K^T has completed (the query region is free), its first keys and values once this item's last
+    // P V has completed (the key / P and value regions are free), so they land during the epilogue.
+    Item it = describe(blockIdx.x);
+    if (it.n_groups > 0) {
+        issue_q(it);
+        issue_kv(it, 0);
+    }
+#pragma unroll 1
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int64_t next = item + gridDim.x;
+        const bool has_next = next < n_items;
+        const Item nx = has_next ? describe(next) : it;
+        const bool pref = has_next && nx.n_groups > 0;
+        const int kv = it.kv;
+        const int64_t start = it.start, pa = it.pa, pb = it.pb, n_sink = it.n_sink, span_lo = it.span_lo;
+        const int sink_pad = it.sink_pad, n_slots = it.n_slots, n_groups = it.n_groups;
 
         // this row's query position and its visible key slots [0, hi1) and [lo2, hi2)
         const int64_t p = pa + qi;
@@ -147,36 +206,8 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         float m_run = -INFINITY, l_run = 0.f;
         for (int grp = 0; grp < n_groups && ok; ++grp) {
             const int g0 = grp * kGroup, n = min(kGroup, n_slots - g0);  // a multiple of 16
-            // ---- loads: the query tile with the first group, then this group's keys and values;
-            //      thread 0 posts the byte count; box b goes to lane b / 8 of warp b % 8, so the
-            //      copies are issued by all warps at once (copies issued back to back by one thread
-            //      serialise; an early complete_tx just leaves the count below zero until the post)
-            if (tid == 0) {
-                tma::expect_tx(bar_ld, (grp == 0 ? 32768u : 0u) + (uint32_t)n * 2u * 2u * 128u);
-                if (grp == 0) {
-                    const int tq = (int)(start + pa);
-                    tma::tensor_load_3d(sbase + kQ, &map_q, 0, kv * G, tq, bar_ld);
-                    tma::tensor_load_3d(sbase + kQ + 16384, &map_q, 64, kv * G, tq, bar_ld);
-                }
-            }
-            {
-                // boxes of 8 slots; a 64-slot run of window rows at a 64-aligned offset is one box
-                for (int j = 8 * (warp + 8 * lane); j < n; j += 8 * kThreads) {
-                    const int slot = g0 + j;
-                    const bool wide = slot >= sink_pad && (j & 63) == 0 && j + 64 <= n;
-                    const bool covered = slot >= sink_pad && (j & 63) != 0 && (j & ~63) + 64 <= n &&
-                                         g0 + (j & ~63) >= sink_pad;  // inside a wide box issued by another lane
-                    if (covered) continue;
-                    const int tk = (int)(start + (slot < sink_pad ? slot : span_lo + (slot - sink_pad)));
-                    const uint32_t off = (uint32_t)j * 128u;
-                    const CUtensorMap* mk = wide ? &map_k64 : &map_k;
-                    const CUtensorMap* mv = wide ? &map_v64 : &map_v;
-                    tma::tensor_load_3d(sbase + kK + off, mk, 0, kv, tk, bar_ld);
-                    tma::tensor_load_3d(sbase + kK + 16384 + off, mk, 64, kv, tk, bar_ld);
-                    tma::tensor_load_3d(sbase + kV + off, mv, 0, kv, tk, bar_ld);
-                    tma::tensor_load_3d(sbase + kV + 16384 + off, mv, 64, kv, tk, bar_ld);
-                }
-            }
+            if (grp > 0) issue_kv(it, grp);
+            if (grp == 0 && !(ok = cta_wait(bar_q, ph_q))) break;
             if (!(ok = cta_wait(bar_ld, ph_ld))) break;
 
             // ---- D_S = Q K^T (N = n)
@@ -191,7 +222,7 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
                 umma::commit(bar_mma);
             }
             if (!(ok = cta_wait(bar_mma, ph_mma))) break;
-
+            if (grp == n_groups - 1 && pref) issue_q(nx);
             // ---- online softmax: this thread covers slots [c_lo, c_hi) of the group (16-slot chunks,
             //      split evenly between the two threads of the row), read from TMEM once: 64 columns
             //      from c_lo (inside the 128 allocated), the ones at or past c_hi masked
@@ -268,6 +299,7 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
             if (!(ok = cta_wait(bar_mma, ph_mma))) break;
         }
         if (!ok) break;
+        if (pref) issue_kv(nx, 0);
 
         // ---- epilogue: this thread's 64 output columns of its row
         {
@@ -303,6 +335,7 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
         }
         umma::fence_before_sync();
         __syncthreads();  // shared tiles and TMEM are reused by the next item
+        it = nx;
     }
 
     umma::fence_before_sync();
