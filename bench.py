@@ -379,14 +379,17 @@ def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_step
     layer_roof = {"bytes": layer["bytes"], "flops": layer["flops"], "bound_ms": round(t_bound * 1e3, 5),
                   "frac": round(t_bound / (device_s / steps), 5)}
 
-    # end to end through the C ABI: pinned host inputs in, result back to pinned host memory
+    # end to end through the C ABI: every step's inputs copied in from pinned host memory and its result
+    # copied back to pinned host memory, inside the timed region
     host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out.numel() * host_out.element_size()
     e2e_n = max(1, min(e2e_steps, steps))
+    # (a) serial: copy in, prefill, copy out on one stream, one step at a time (L2 flushed before each)
+    serial_n = max(1, min(e2e_n, 20))
     e2e_ms = []
-    for i in range(2 + e2e_n):
+    for i in range(2 + serial_n):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -398,8 +401,48 @@ def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_step
         b.synchronize()
         if i >= 2:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_s = dist.max(sum(e2e_ms) / 1e3)
-    del host, host_out
+    serial_s = dist.max(sum(e2e_ms) / 1e3)
+    # (b) pipelined, as a serving loop runs it: step i's inputs are copied in on one stream while step i - 1
+    # computes and step i - 2's result is copied out on a third; two device input sets and outputs
+    # alternate, each reused only once the step two back has finished with it (events)
+    xs = [x, dict(x, **{k: torch.empty_like(x[k]) for k in host})]
+    outs = [out, torch.empty_like(out)]
+    host_outs = [host_out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)]
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in, ev_c, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def pipe(i):
+        bi = i & 1
+        xb = xs[bi]
+        if i >= 2:
+            s_in.wait_event(ev_c[bi])  # step i - 2 has read this input set
+        with torch.cuda.stream(s_in):
+            for k in host:
+                xb[k].copy_(host[k], non_blocking=True)
+        ev_in[bi].record(s_in)
+        s_c.wait_event(ev_in[bi])
+        if i >= 2:
+            s_c.wait_event(ev_out[bi])  # step i - 2's result has been copied out of this output
+        hla.prefill(prm, xb["q"], xb["k"], xb["v"], xb["g"], xb["beta"], xb["lam"], xb["wq"], xb["wk"],
+                    xb["wv"], xb["cu_seqlens"], outs[bi], ws=ws, stream=s_c)
+        ev_c[bi].record(s_c)
+        s_out.wait_event(ev_c[bi])
+        with torch.cuda.stream(s_out):
+            host_outs[bi].copy_(outs[bi], non_blocking=True)
+        ev_out[bi].record(s_out)
+
+    for i in range(4):
+        pipe(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    for i in range(e2e_n):
+        pipe(i)
+    b.record(s_out)
+    b.synchronize()
+    e2e_s = dist.max(a.elapsed_time(b) / 1e3)
+    assert hla.check_workspace_error(ws) == 0
+    del host, host_out, host_outs, xs, outs
     tokens = wl.total_tokens * dist.world
     res = {
         "value": tokens * steps / device_s, "unit": "tokens/s", "steps": steps, "warmup": warmup,
@@ -408,7 +451,11 @@ def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_step
         "stage_roofline": stage_roofline, "layer_roofline": layer_roof,
         "clocks": clocks.summary(), "gpu_launches": launches_per_step * steps,
         "e2e": {"value": tokens * e2e_n / e2e_s, "unit": "tokens/s", "steps": e2e_n,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "mode": "pipelined: step i's inputs copied in while step i-1 computes and step i-2's result is "
+                        "copied out (three streams, two device input sets and outputs); no L2 flush, every step's "
+                        "inputs arrive by copy",
+                "serial_value": tokens * serial_n / serial_s, "serial_steps": serial_n},
         "workload": wl, "inputs": x,
     }
     del ws, out, flush
@@ -768,17 +815,40 @@ def run_decode_bench(args, dist, peaks):
     h2d = sum(dev_in[k].numel() * dev_in[k].element_size() for k in keys)
     d2h = host_out.numel() * host_out.element_size()
     e2e_n = min(K, 1000)
+    # pipelined, as a serving loop runs it: step i's inputs are copied in on one stream while step i - 1
+    # runs and step i - 2's output is copied out on a third (two device input sets and outputs, each reused
+    # once the step two back is done with it); the steps themselves stay in order on one stream
+    dev_ins = [dev_in, {k: torch.empty_like(x[k][0]) for k in keys}]
+    douts = [dout, torch.empty_like(dout)]
+    host_outs = [host_out, torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)]
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in, ev_c, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(s_in)
     for i in range(e2e_n):
-        for k in keys:
-            dev_in[k].copy_(host[k][i % 8], non_blocking=True)
-        hla.decode_step(prm, dev_in["dq"], dev_in["dk"], dev_in["dv"], dev_in["dg"], dev_in["dbeta"], x["lam"],
-                        x["wq"], x["wk"], x["wv"], st, dout)
-        host_out.copy_(dout, non_blocking=True)
-    b.record(stream)
+        bi = i & 1
+        if i >= 2:
+            s_in.wait_event(ev_c[bi])
+        with torch.cuda.stream(s_in):
+            for k in keys:
+                dev_ins[bi][k].copy_(host[k][i % 8], non_blocking=True)
+        ev_in[bi].record(s_in)
+        s_c.wait_event(ev_in[bi])
+        if i >= 2:
+            s_c.wait_event(ev_out[bi])
+        d = dev_ins[bi]
+        hla.decode_step(prm, d["dq"], d["dk"], d["dv"], d["dg"], d["dbeta"], x["lam"], x["wq"], x["wk"], x["wv"],
+                        st, douts[bi], stream=s_c)
+        ev_c[bi].record(s_c)
+        s_out.wait_event(ev_c[bi])
+        with torch.cuda.stream(s_out):
+            host_outs[bi].copy_(douts[bi], non_blocking=True)
+        ev_out[bi].record(s_out)
+    b.record(s_out)
     b.synchronize()
     e2e_s = dist.max(a.elapsed_time(b) / 1e3)
+    assert st.check_error() == 0
     traffic = decode_traffic()
     return {"value": K * dist.world / dev_s, "unit": "steps/s", "steps": K, "warmup": W,
             "ms_per_step": per_step * 1e3, "tokens_per_s": K * dist.world * wl.n_seqs / dev_s,
@@ -791,7 +861,9 @@ def run_decode_bench(args, dist, peaks):
                          "traffic": traffic, "algorithmic_bytes_per_step": nbytes,
                          "peak_source": peaks["source"]},
             "e2e": {"value": e2e_n * dist.world / e2e_s, "unit": "steps/s", "steps": e2e_n,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "mode": "pipelined: step i's inputs copied in while step i-1 runs and step i-2's output is "
+                            "copied out (three streams, two device input sets and outputs)"},
             "clocks": clocks.summary(), "gpu_launches": DECODE_LAUNCHES * K}
 
 
