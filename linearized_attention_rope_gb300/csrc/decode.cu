@@ -175,6 +175,11 @@ decode_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __rest
     __shared__ __align__(16) float qhat_s[kMaxG][D];
     __shared__ __align__(16) float krot_s[D], vraw_s[D], khat_s[D], vhat_s[D];
     __shared__ float cs_s[HALF], sn_s[HALF], inv_s[kMaxG + 1];
+    // Launched with programmatic stream serialization: wait for the launch before this one (the previous
+    // step's combine, which advanced pos) to complete before any read, then let the next launch place its
+    // CTAs (it waits the same way).  No effect on a plain launch.
+    pdl_wait();
+    pdl_trigger();
     const int kv = blockIdx.x, n = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = L.G, ns = L.n_sinks, W = L.window, R = ns + W, P = W + 1;
     const int64_t p = s.pos[n];
@@ -519,6 +524,8 @@ __global__ void __launch_bounds__(kSmThreads, 3)
 decode_attn_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
     static_assert(kStateThreads == kSmThreads, "one CTA shape for both units");
     extern __shared__ __align__(16) float fsm[];
+    pdl_wait();  // the features launch has completed (see decode_features_kernel)
+    pdl_trigger();
     const int run = L.G + sc.splits, kv = blockIdx.x / run, r = blockIdx.x % run, n = blockIdx.y;
     if (r < L.G) decode_state_unit<D>(L, s, sc, kv * L.G + r, n);
     else decode_softmax_unit<Tin, D, GM>(L, s, sc, r - L.G, kv, n, fsm);
@@ -540,6 +547,8 @@ decode_combine_kernel(LayerDims L, DecScratch sc, const float* __restrict__ lamb
     // (a negative position was flagged by the features launch; it is left as it is)
     __shared__ float w_s[kCombineTile];
     __shared__ float mx_s, inv_s;
+    pdl_wait();  // the state + softmax launch has completed (see decode_features_kernel)
+    pdl_trigger();
     const int h = blockIdx.x, n = blockIdx.y, c = threadIdx.x, lane = c & 31;
     const size_t hs = ((size_t)n * L.Hq + h) * sc.splits;
     if (c < 32) {
@@ -595,9 +604,8 @@ cudaError_t launch_decode_attn_state(const LayerDims& L, const hla_state& s, con
                                     (int)P::kSmemBytes);
     });
     if (e != cudaSuccess) return e;
-    decode_attn_state_kernel<Tin, D, GM><<<dim3(L.Hkv * (L.G + sc.splits), L.n_seqs), kSmThreads, P::kSmemBytes,
-                                           st>>>(L, s, sc);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3(L.Hkv * (L.G + sc.splits), L.n_seqs), dim3(kSmThreads), P::kSmemBytes, st, true);
+    return cudaLaunchKernelEx(&lc.cfg, decode_attn_state_kernel<Tin, D, GM>, L, s, sc);
 }
 
 template <typename Tin, int D>
@@ -605,14 +613,21 @@ cudaError_t decode_kernels(const LayerDims& L, const Tin* q, const Tin* k, const
                            const float* beta, const float* lambda, const float* wq, const float* wk,
                            const float* wv, const hla_state& s, Tin* out, cudaStream_t st) {
     const DecScratch sc = dec_scratch(static_cast<float*>(s.scratch), L.n_seqs, L.Hq, D, decode_splits(L.n_sinks, L.window));
-    decode_features_kernel<Tin, D><<<dim3(L.Hkv, L.n_seqs), kFeatThreads, 0, st>>>(L, q, k, v, g, beta, wq, wk, wv, s, sc);
+    // three launches, each placed while the one before it finishes (programmatic dependent launch; every
+    // kernel waits for its predecessor to complete before its first read)
+    {
+        LaunchCfg lc(dim3(L.Hkv, L.n_seqs), dim3(kFeatThreads), 0, st, true);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, decode_features_kernel<Tin, D>, L, q, k, v, g, beta, wq, wk, wv, s,
+                                           sc);
+        if (e != cudaSuccess) return e;
+    }
     cudaError_t e0 = L.G <= 1 ? launch_decode_attn_state<Tin, D, 1>(L, s, sc, st)
                    : L.G <= 2 ? launch_decode_attn_state<Tin, D, 2>(L, s, sc, st)
                    : L.G <= 4 ? launch_decode_attn_state<Tin, D, 4>(L, s, sc, st)
                               : launch_decode_attn_state<Tin, D, 8>(L, s, sc, st);
     if (e0 != cudaSuccess) return e0;
-    decode_combine_kernel<Tin, D><<<dim3(L.Hq, L.n_seqs), D, 0, st>>>(L, sc, lambda, out, s.pos);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3(L.Hq, L.n_seqs), dim3(D), 0, st, true);
+    return cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<Tin, D>, L, sc, lambda, out, s.pos);
 }
 
 template <typename Tin>
