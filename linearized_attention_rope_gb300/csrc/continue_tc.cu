@@ -46,6 +46,8 @@ __device__ __forceinline__ int64_t cont_old_pos(int64_t pos, int64_t i, int ns, 
 // flagged; so is a table whose sequences overlap).  One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) cont_ext_table_kernel(LayerDims L, const int32_t* __restrict__ cu, hla_state s,
                                                               int32_t* __restrict__ ext_cu) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     __shared__ int32_t part[1024];
     const int N = L.n_seqs, tid = threadIdx.x, per = (N + 1023) / 1024;
     const int lo = min(N, tid * per), hi = min(N, lo + per);
@@ -98,6 +100,8 @@ cont_prep_kernel(LayerDims L, LayerDims Lx, const int32_t* __restrict__ cu, hla_
                  __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
                  __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb,
                  const float* __restrict__ g, const float* __restrict__ beta, float2* __restrict__ ang) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     const int64_t first = __ldg(ext_cu + Lx.n_seqs);
     const int D = kCD, HALF = kCD / 2;
     for (int64_t r = first + blockIdx.x; r < Lx.total; r += gridDim.x) {
@@ -153,6 +157,8 @@ __global__ void __launch_bounds__(kCT)
 cont_gather_kernel(LayerDims L, hla_state s, const int32_t* __restrict__ ext_cu, __half* __restrict__ qr,
                    __half* __restrict__ kr, __half* __restrict__ qh, __half* __restrict__ kh, __half* __restrict__ vh,
                    __nv_bfloat16* __restrict__ ev, float* __restrict__ eg, float* __restrict__ eb) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     const int i = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
     const int ns = L.n_sinks, W = L.window, P = W + 1, R = ns + W, D = kCD;
     const int64_t pos = s.pos[n];
@@ -385,6 +391,8 @@ cont_features_kernel(LayerDims L, const __nv_bfloat16* __restrict__ q, const __n
                      __half* __restrict__ vh, __nv_bfloat16* __restrict__ ev, int span) {
     constexpr int D = kCD, HALF = D / 2;
     extern __shared__ __align__(16) unsigned char ring_s[];  // [warp][kFRing][kFB tokens][D]
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     unsigned char* wring = ring_s + (size_t)(threadIdx.x >> 5) * kFRing * kFB * D * sizeof(__nv_bfloat16);
     int head = blockIdx.y * kFW + (threadIdx.x >> 5);
@@ -438,6 +446,8 @@ cont_features_kernel(LayerDims L, const __nv_bfloat16* __restrict__ q, const __n
 __global__ void __launch_bounds__(kCT)
 cont_out_kernel(LayerDims L, const int32_t* __restrict__ cu, hla_state s, const int32_t* __restrict__ ext_cu,
                 const __nv_bfloat16* __restrict__ eo, __nv_bfloat16* __restrict__ out) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     const int64_t t = blockIdx.x;
     const int n = seq_of_token(cu, L.n_seqs, t);
     int64_t start, len;
@@ -462,6 +472,8 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
                   const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
                   hla_state s, const int32_t* __restrict__ ext_cu, const __half* __restrict__ kh,
                   const __half* __restrict__ vh, const float2* __restrict__ ang) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     constexpr int D = kCD, HALF = D / 2;
     const int n = blockIdx.x, y = blockIdx.y, tid = threadIdx.x;
     const int ns = L.n_sinks, W = L.window, P = W + 1, R = ns + W;
@@ -605,6 +617,8 @@ cont_state_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict_
 
 // 8. pos += len, after every launch above has read it
 __global__ void cont_tc_advance_kernel(LayerDims L, const int32_t* __restrict__ cu, int64_t* __restrict__ pos) {
+    pdl_wait();  // programmatic dependent launch: the launch before this one has completed
+    pdl_trigger();
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= L.n_seqs) return;
     int64_t start, len;
@@ -617,8 +631,8 @@ __global__ void cont_tc_advance_kernel(LayerDims L, const int32_t* __restrict__ 
 cudaError_t launch_continue_table(const LayerDims& L, const int32_t* cu, const hla_state& s, int32_t* ext_cu,
                                   cudaStream_t st) {
     if (L.d != kCD) return cudaErrorInvalidValue;
-    cont_ext_table_kernel<<<1, 1024, 0, st>>>(L, cu, s, ext_cu);
-    return cudaGetLastError();
+    LaunchCfg lc(dim3(1), dim3(1024), 0, st, true);
+    return cudaLaunchKernelEx(&lc.cfg, cont_ext_table_kernel, L, cu, s, ext_cu);
 }
 
 cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const int32_t* cu, const hla_state& s,
@@ -626,9 +640,17 @@ cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const 
                                  __nv_bfloat16* ev, float* eg, float* eb, float2* ang, const __nv_bfloat16* q,
                                  const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
                                  const float* wq, const float* wk, const float* wv, cudaStream_t st) {
-    cont_prep_kernel<<<1024, kCT, 0, st>>>(L, Lx, cu, s, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb, g, beta, ang);
-    cont_gather_kernel<<<dim3(L.n_sinks + L.window, L.n_seqs), kCT, 0, st>>>(L, s, ext_cu, qr, kr, qh, kh, vh, ev, eg,
-                                                                             eb);
+    {
+        LaunchCfg lc(dim3(1024), dim3(kCT), 0, st, true);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, cont_prep_kernel, L, Lx, cu, s, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb,
+                                           g, beta, ang);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        LaunchCfg lc(dim3(L.n_sinks + L.window, L.n_seqs), dim3(kCT), 0, st, true);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, cont_gather_kernel, L, s, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb);
+        if (e != cudaSuccess) return e;
+    }
     if (L.total > 0) {
         static DeviceCache cache;  // CTAs of the feature kernel resident on the device at once
         int resident = 0;
@@ -646,8 +668,10 @@ cudaError_t launch_continue_rows(const LayerDims& L, const LayerDims& Lx, const 
         const int64_t spans = std::max<int64_t>(1, resident / row_groups);
         const int64_t span = std::max<int64_t>(kFB, ((L.total + spans - 1) / spans + kFB - 1) / kFB * kFB);
         const dim3 grid((unsigned)((L.total + span - 1) / span), (unsigned)row_groups);
-        cont_features_kernel<<<grid, 32 * kFW, kFeatSmem, st>>>(L, q, k, v, wq, wk, wv, cu, s, ext_cu, ang, qr, kr, qh,
-                                                                kh, vh, ev, (int)span);
+        LaunchCfg lc(grid, dim3(32 * kFW), kFeatSmem, st, true);
+        e = cudaLaunchKernelEx(&lc.cfg, cont_features_kernel, L, q, k, v, wq, wk, wv, cu, s, ext_cu,
+                               static_cast<const float2*>(ang), qr, kr, qh, kh, vh, ev, (int)span);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -656,11 +680,19 @@ cudaError_t launch_continue_finish(const LayerDims& L, const int32_t* cu, const 
                                    const __nv_bfloat16* ext_out, __nv_bfloat16* out, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v, const float* g, const float* beta,
                                    const __half* kh, const __half* vh, const float2* ang, cudaStream_t st) {
-    if (L.total > 0) cont_out_kernel<<<(unsigned)L.total, kCT, 0, st>>>(L, cu, s, ext_cu, ext_out, out);
-    cont_state_kernel<__nv_bfloat16><<<dim3(L.n_seqs, 1 + L.Hq + L.Hkv * (1 + kStGroups)), kCT, 0, st>>>(
-        L, q, k, v, g, beta, cu, s, ext_cu, kh, vh, ang);
-    cont_tc_advance_kernel<<<(L.n_seqs + 127) / 128, 128, 0, st>>>(L, cu, s.pos);
-    return cudaGetLastError();
+    if (L.total > 0) {
+        LaunchCfg lc(dim3((unsigned)L.total), dim3(kCT), 0, st, true);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, cont_out_kernel, L, cu, s, ext_cu, ext_out, out);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        LaunchCfg lc(dim3(L.n_seqs, 1 + L.Hq + L.Hkv * (1 + kStGroups)), dim3(kCT), 0, st, true);
+        cudaError_t e = cudaLaunchKernelEx(&lc.cfg, cont_state_kernel<__nv_bfloat16>, L, q, k, v, g, beta, cu, s, ext_cu,
+                                           kh, vh, ang);
+        if (e != cudaSuccess) return e;
+    }
+    LaunchCfg lc(dim3((L.n_seqs + 127) / 128), dim3(128), 0, st, true);
+    return cudaLaunchKernelEx(&lc.cfg, cont_tc_advance_kernel, L, cu, s.pos);
 }
 
 }  // namespace hla

@@ -304,7 +304,7 @@ int run_continue_tc(const hla_params* prm, const LayerDims& L, const void* q, co
                                   w.n_coarse, tabs, stream));
     HLA_TRY(launch_continue_rows(L, Lx, cu, *st, ext_cu, qr, kr, qh, kh, vh, ev, eg, eb,
                                  reinterpret_cast<float2*>(ws + c.ang), qi, ki, vi, g, beta, wq, wk, wv, stream));
-    HLA_TRY(launch_window_softmax_tc(Lx, qr, kr, ev, ext_cu, blk_base, osm, eo, err, false, stream));
+    HLA_TRY(launch_window_softmax_tc(Lx, qr, kr, ev, ext_cu, blk_base, osm, eo, err, true, stream));
     const int n_slots = (int)gdn_chunk_slots(Lx.total, Lx.n_seqs);
     int bound[kGdnParts + 1];
     for (int p = 0; p <= kGdnParts; ++p) bound[p] = (int)((int64_t)n_slots * p / kGdnParts);
