@@ -39,8 +39,8 @@ constexpr int kSA = 65;                           // row stride of A (odd: row-p
 constexpr uint32_t kA32 = 32768;                  // A fp32 [64][kSA]
 constexpr uint32_t kT32 = kA32 + 64 * 68 * 4;     // T fp32 [64][68] (rows 16-byte aligned)
 constexpr uint32_t kX32 = kT32 + 64 * 68 * 4;     // [32][36]
-constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta, gamma
-constexpr uint32_t kMisc = kVec + 3 * 64 * 4;
+constexpr uint32_t kVec = kX32 + 32 * 36 * 4;     // G (log2 units), beta, gamma, 2^-G
+constexpr uint32_t kMisc = kVec + 4 * 64 * 4;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -91,6 +91,7 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     float* sG = reinterpret_cast<float*>(sm + kVec);
     float* sBeta = sG + 64;
     float* sGam = sG + 128;
+    float* sEg = sG + 192;  // 2^-G_i, the column factor of e^(G_r - G_i) (see the A and P tiles)
     uint64_t* mbar_p = reinterpret_cast<uint64_t*>(sm + kMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
     float* carry = reinterpret_cast<float*>(sm + kMisc + 16);
@@ -172,7 +173,10 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
     __syncthreads();
     umma::fence_after_sync();
     if (tid >= 32 && tid < kC) gi += *carry;
-    if (tid < kC) sG[tid] = gi;
+    if (tid < kC) {
+        sG[tid] = gi;
+        sEg[tid] = exp2f(-gi);
+    }
 
     // ---- Gram: D = [K; Q] K^T
     if (tid == 0) {
@@ -196,37 +200,52 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
         umma::reg_fence32(dg[0]);
         umma::reg_fence32(dg[1]);
     }
-    if (warp < 2 && done) {  // rows 0..63: K K^T -> A
-        const int r = tid;
-        const float br = sBeta[r], gr = sG[r];
+    // e^(G_r - G_i) (i <= r, so at most 1): as 2^G_r 2^-G_i, one exponential per row and per column, while
+    // the chunk's gates keep both factors inside fp32 (G_63 >= -100 in log2 units); else per entry.  The
+    // choice is uniform over the CTA, so only one of the two forms runs.
+    const bool split_exp = sG[kC - 1] >= -100.f;  // G is non-increasing
+    // w[ii] = e^(G_r - G_i) for columns i = 32 half + ii
+    auto weights = [&](int r, int half, float* w) {
+        const float gr = sG[r];
+        if (split_exp) {
+            const float er = exp2f(gr);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+            for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 e4 = *reinterpret_cast<const float4*>(sEg + 32 * half + 4 * i4);
+                w[4 * i4] = er * e4.x; w[4 * i4 + 1] = er * e4.y; w[4 * i4 + 2] = er * e4.z; w[4 * i4 + 3] = er * e4.w;
+            }
+        } else {
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
                 const float4 g4 = *reinterpret_cast<const float4*>(sG + 32 * half + 4 * i4);
-                const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+                w[4 * i4] = exp2f(gr - g4.x); w[4 * i4 + 1] = exp2f(gr - g4.y);
+                w[4 * i4 + 2] = exp2f(gr - g4.z); w[4 * i4 + 3] = exp2f(gr - g4.w);
+            }
+        }
+    };
+    if (warp < 2 && done) {  // rows 0..63: K K^T -> A
+        const int r = tid;
+        const float br = sBeta[r];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int ii = 4 * i4 + e, i = 32 * half + ii;
-                    sA[r * kSA + i] = (i < r && !gla) ? br * exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
-                }
+        for (int half = 0; half < 2; ++half) {
+            float w[32];
+            weights(r, half, w);
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * half + ii;
+                sA[r * kSA + i] = (i < r && !gla) ? br * w[ii] * __uint_as_float(dg[half][ii]) : 0.f;
             }
         }
     } else if (done) {  // rows 64..127: Q K^T -> P
         const int r = tid - 64;
-        const float gr = sG[r];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float d[32];
+            weights(r, half, d);
 #pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 g4 = *reinterpret_cast<const float4*>(sG + 32 * half + 4 * i4);
-                const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int ii = 4 * i4 + e, i = 32 * half + ii;
-                    d[ii] = (i <= r) ? exp2f(gr - gg[e]) * __uint_as_float(dg[half][ii]) : 0.f;
-                }
+            for (int ii = 0; ii < 32; ++ii) {
+                const int i = 32 * half + ii;
+                d[ii] = (i <= r) ? d[ii] * __uint_as_float(dg[half][ii]) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
