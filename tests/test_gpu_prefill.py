@@ -209,3 +209,18 @@ def test_large_magnitude_activations(oracle_mod, d):
     x["v"] = (x["v"].float() * 300.0).to(torch.bfloat16)
     out, st = run_prefill(wl, x, with_state=True)
     check_prefill(wl, x, out, st, all_units(wl), oracle_mod)
+
+
+@pytest.mark.parametrize("gate_scale", [2.0, 30.0])
+def test_strong_and_mixed_gates(oracle_mod, gate_scale):
+    # gates 20x and 300x the unit recipe (log-gate per token about -1.6 and -24 on average): a 64-token
+    # chunk then spans far more than 100 powers of two, where the chunk-local kernel forms e^(G_r - G_i)
+    # entry by entry instead of as a product of row and column factors; the second sequence keeps the
+    # unit gates, so one launch holds chunks of both kinds
+    wl = synth.small(f"gates x{gate_scale}", [700, 300], n_q_heads=4, n_kv_heads=2, head_dim=128,
+                     seed=synth.BASE_SEED + 430)
+    x = synth.make_inputs(wl, "cuda")
+    cu = x["cu_seqlens"].tolist()
+    x["g"][cu[0]:cu[1]] *= 10.0 * gate_scale
+    out, st = run_prefill(wl, x, with_state=True)
+    check_prefill(wl, x, out, st, all_units(wl), oracle_mod)
