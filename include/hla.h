@@ -264,6 +264,10 @@ HLA_API int hla_decode_step(const hla_params* params, int n_seqs, const void* q,
  * in front of its new tokens, the positions between them left out, and the
  * prefill's softmax and chunked GDN kernels run on these rows from the cached
  * S; the other layers take a token-serial path (one CTA per query head).
+ * There, a sequence table whose sequences overlap (cu_seqlens decreasing once
+ * clamped to [0, total_tokens]) is flagged in the state's error word (the
+ * sequence-table code, 1) and the outputs and the state are undefined; every
+ * write still stays inside ws, out and the state.
  * Asynchronous; no allocation. */
 HLA_API int hla_prefill_continue(const hla_params* params, const void* q, const void* k, const void* v,
                                  const float* g, const float* beta, const float* lambda,
