@@ -67,6 +67,8 @@ CASES = [
     ("bf16", 128, 8, 1, 8, 56, [300, 1000], [64, 700]),
     ("bf16", 128, 4, 1, 8, 120, [129, 2000, 0], [1, 300, 128]),
     ("bf16", 128, 2, 1, 8, 888, [1000, 50], [500, 900]),
+    # contexts of 1 to 6 tokens: the first new tokens' conv taps reach positions before 0
+    ("bf16", 128, 4, 2, 8, 24, [3, 5, 1, 6], [20, 9, 70, 2]),
     # token-serial path
     ("bf16", 64, 4, 1, 3, 40, [30, 100], [90, 1]),
     ("f32", 64, 2, 1, 8, 56, [512, 20], [100, 300]),
