@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--scan", type=int, default=1,
                     help="1: also time the context-parallel token-serial GDN on a long fp32 sequence and the "
                          "prefill continuation (chunked prefill)")
-    ap.add_argument("--only", default="", choices=["", "backward", "scan", "continue", "diagnostics"],
+    ap.add_argument("--only", default="", choices=["", "backward", "scan", "continue", "diagnostics", "gla"],
                     help="run one secondary measurement alone with few calls (--warmup warm-up calls; --steps timed "
                          "calls for continue; 3 for backward and scan): the form the profiler captures use")
     ap.add_argument("--backward", default="c1", choices=["", "c1", "c2", "c4"],
@@ -668,6 +668,49 @@ def run_scan_bench(dist, trial_seconds=0.5, warmup=3):
     return res
 
 
+def run_gla_bench(dist, steps=200, warmup=5):
+    """The LLaMA-3.1-8B-shaped prefill (4096 tokens) with the gated-linear-attention update
+    (HLA_FLAG_GLA: S <- alpha S + k v^T, no erase) in place of the delta rule; each call timed with CUDA
+    events (L2 flushed between calls)."""
+    import torch
+
+    from linearized_attention_rope_gb300 import hla, synth
+
+    wl = synth.workloads()["c1"]
+    x = synth.make_inputs(wl, "cuda")
+    prm = hla.Params(wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.n_sinks, wl.window,
+                     flags=hla.FLAG_L2NORM_Q | hla.FLAG_GLA)
+    ws = hla.alloc_workspace(prm, wl.total_tokens, wl.n_seqs)
+    out = torch.empty_like(x["q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call():
+        hla.prefill(prm, x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"], x["wq"], x["wk"], x["wv"],
+                    x["cu_seqlens"], out, ws=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    assert hla.check_workspace_error(ws) == 0
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    dev_s = dist.max(sum(ms) / 1e3)
+    del ws, out, flush
+    return {"value": wl.total_tokens * dist.world * steps / dev_s, "unit": "tokens/s", "steps": steps,
+            "warmup": warmup, "ms_per_step": dev_s * 1e3 / steps,
+            "config": {"workload": "LLaMA-3.1-8B layer shape (32q/8kv d128 bf16, 8 sinks + 56 window), B1 T4096, "
+                                   "gated linear attention update (no erase)",
+                       "l2": "flushed between calls (512 MiB write)"}}
+
+
 def run_diagnostics_bench(dist, steps=30, warmup=3):
     """hla_prefill_diagnostics on the LLaMA-3.1-8B-shaped layer (4096 tokens): the prefill run with each
     branch alone, the two branch sums and the key statistics; each call timed with CUDA events (L2 flushed
@@ -1129,6 +1172,8 @@ def main():
             part = run_scan_bench(dist, trial_seconds=0.0, warmup=args.warmup)
         elif args.only == "diagnostics":
             part = run_diagnostics_bench(dist, steps=args.steps, warmup=args.warmup)
+        elif args.only == "gla":
+            part = run_gla_bench(dist, steps=args.steps, warmup=args.warmup)
         else:
             part = run_continue_bench(dist, steps=args.steps, warmup=args.warmup)
         if dist.rank == 0:
@@ -1151,6 +1196,7 @@ def main():
     scan = run_scan_bench(dist) if args.scan else None
     cont = run_continue_bench(dist) if args.scan else None
     diag = run_diagnostics_bench(dist) if args.scan else None
+    gla = run_gla_bench(dist) if args.scan else None
     torch.cuda.empty_cache()
     bwd = None
     if args.backward:
@@ -1183,6 +1229,8 @@ def main():
         line["prefill_continue_c1"] = cont
     if diag:
         line["prefill_diagnostics_c1"] = diag
+    if gla:
+        line["prefill_gla_c1"] = gla
     if dec:
         line["decode"] = dec
     if dist.rank == 0:
