@@ -69,6 +69,10 @@ CASES = [
     ("bf16", 128, 2, 1, 8, 888, [1000, 50], [500, 900]),
     # contexts of 1 to 6 tokens: the first new tokens' conv taps reach positions before 0
     ("bf16", 128, 4, 2, 8, 24, [3, 5, 1, 6], [20, 9, 70, 2]),
+    # sequences with no new tokens beside ones with many
+    ("bf16", 128, 4, 2, 8, 24, [40, 90, 7], [0, 133, 0]),
+    # forty sequences: many sequence starts inside one feature span
+    ("bf16", 128, 4, 1, 8, 24, [5, 100] * 20, [7, 3] * 20),
     # token-serial path
     ("bf16", 64, 4, 1, 3, 40, [30, 100], [90, 1]),
     ("f32", 64, 2, 1, 8, 56, [512, 20], [100, 300]),
