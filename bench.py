@@ -463,8 +463,14 @@ def run_prefill_bench(key, steps, warmup, dist, peaks, e2e_steps=200, stage_step
 
 
 BWD_SOURCES = [CSRC + "backward.cu", CSRC + "hla_common.cuh"]
-# hla_backward's launches, in order (stage marks 1 .. 8 follow them)
+# hla_backward's stages, in order (stage marks 1 .. 8 follow them; the L2 backward runs inside the
+# feat_out launch, so its interval is empty)
 BWD_STAGES = ("rope", "conv", "gdn", "softmax", "l2", "feat_out", "conv_filters", "lambda")
+
+
+def bwd_launches(wl) -> int:
+    """Kernels one hla_backward call launches."""
+    return 10 + (1 if wl.n_sinks > 0 else 0)
 
 
 def backward_work(wl) -> dict:
@@ -583,8 +589,10 @@ def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_step
                       "precision": "fp32 recompute and gradients from the stored bf16/fp32 inputs"},
            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
            "roofline": roof(dominant), "stage_roofline": {n: roof(n) for n in work},
-           "clocks": clocks.summary(), "gpu_launches": len(BWD_STAGES) * steps + steps,
-           "gpu_launches_note": "9 kernels per call (the conv-filter stage is two launches)",
+           "clocks": clocks.summary(), "gpu_launches": bwd_launches(wl) * steps,
+           "gpu_launches_note": "per call: the block table, RoPE, conv, GDN, softmax query and key (and the "
+                                "sink keys' sums where there are sinks), feature backward, filter partial "
+                                "sums and their reduction, lambda",
            "e2e": {"value": tokens * e2e_steps / e2e_s, "unit": "tokens/s", "steps": e2e_steps,
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
     del ws, grads, flush, host, host_g

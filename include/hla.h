@@ -388,10 +388,11 @@ HLA_API int hla_check_workspace_error(void* ws, void* stream, int32_t* code);
  * Token-serial path: 0, 1 as above, 2 = 3 = 1, 4 after the GDN kernel, 5
  * after the softmax + combine, 6 after the hand-off (7 to 22 not recorded).
  * hla_backward, with the hook on, records 0 before its first kernel and
- * i = 1 .. 8 after its i-th launch (RoPE rows, conv and L2 features, GDN
+ * i = 1 .. 8 after its i-th stage (RoPE rows, conv and L2 features, GDN
  * backward, softmax backward, L2 backward, conv and RoPE backward, filter
- * partial sums + their reduction as one, lambda reduction); its launches run
- * one after another either way.
+ * partial sums + their reduction as one, lambda reduction); the L2, conv and
+ * RoPE backward are one launch, so 5 = 4; its launches run one after another
+ * either way.
  * Entries beyond n_events, or NULL entries, are skipped; n_events = 0
  * switches the hook off.  The array must stay valid while the hook is on. */
 HLA_API int hla_prefill_stage_events(void** events, int n_events);

@@ -9,8 +9,10 @@
 // fp32 throughout, on the CUDA cores; every reduction has a fixed order (no
 // atomics).  Launches, in order:
 //  0. the 64-row block table of the sequences (and a check of cu_seqlens);
-//  1. rope: RoPE'd q and k rows (fp32) for every token and head; alpha = e^g;
-//  2. conv: q~, k~ (and their L2-normalised qhat, khat) and vhat = conv(v);
+//  1. rope: RoPE'd q and k rows (fp32) for every token and head, the angle
+//     table; alpha = e^g;
+//  2. conv: q~, k~ (and their L2-normalised qhat, khat) and vhat = conv(v),
+//     a warp per (row, span of tokens) with the conv window in registers;
 //  3. GDN, a cluster of 8 CTAs per (sequence, q-head) splitting the value
 //     columns: a forward pass that keeps the state every 64 absorptions, then
 //     per 64-absorption block, last first, the states every 4 (d 128) or 8
@@ -21,8 +23,8 @@
 //     per 64-key block dk, dv of its non-sink keys; the sink keys' sums over
 //     the query blocks' partials;
 //  5. feature backward of q (L2, conv, RoPE); of k and v after the per-head
-//     gradients of each kv group are summed;
-//  6. the conv filters' gradients (per token block, then over the blocks);
+//     gradients of each kv group are summed; one launch, streaming like 2;
+//  6. the conv filters' gradients (per span of tokens, then over the spans);
 //  7. lambda's gradient over the sequences.
 #include <type_traits>
 
@@ -32,13 +34,8 @@ namespace hla {
 
 namespace {
 
-constexpr int kWB = 64;     // tokens per block of the conv-filter reduction
+constexpr int kWB = 64;  // the shortest span of the conv-filter partial sums (at most ceil(T / 64) of them)
 
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 // cos/sin of p theta_i, i < d / 2, for one position, into shared memory (threads < d / 2)
 __device__ __forceinline__ void angles(const LayerDims& L, int64_t p, float* cs, float* sn) {
     if ((int)threadIdx.x < L.d / 2) rope_cs_exact(p, L.theta[threadIdx.x], &cs[threadIdx.x], &sn[threadIdx.x]);
@@ -51,7 +48,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kRowThreads)
 bwd_rope_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ k, const float* __restrict__ g,
                 const int32_t* __restrict__ cu, float* __restrict__ qr, float* __restrict__ kr,
-                float* __restrict__ alpha, int32_t* __restrict__ err) {
+                float* __restrict__ alpha, float2* __restrict__ ang, int32_t* __restrict__ err) {
     __shared__ float cs[64], sn[64];
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x, D = L.d, half = D / 2;
@@ -63,6 +60,7 @@ bwd_rope_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
     if ((p < 0 || p >= len) && tid == 0) atomicExch(err, kErrSeqlens);
     for (int h = tid; h < L.Hq; h += kRowThreads) alpha[t * L.Hq + h] = expf(g[t * L.Hq + h]);  // alpha = e^g
     angles(L, p, cs, sn);
+    if (tid < half) ang[(size_t)t * half + tid] = make_float2(cs[tid], sn[tid]);  // for the RoPE backward
     for (int idx = tid; idx < (L.Hq + L.Hkv) * half; idx += kRowThreads) {
         const int r = idx / half, i = idx % half;
         const bool isq = r < L.Hq;
@@ -75,64 +73,174 @@ bwd_rope_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __restrict__ 
     }
 }
 
-// ---- 2. conv (+ L2): CTA per token, a warp per row (rows r < Hq: q-heads, < Hq + Hkv: k-heads, else
-// v-heads), lane l holding channels l + 32 e
+// Sums of eight per-lane values over a warp, reduced together: the lanes exchange halves of the set in three
+// butterfly steps and then add across 8 and 16 lanes, so lane l returns the sum of v[red8_slot(l)] (lanes l,
+// l ^ 8, l ^ 16 and l ^ 24 alike); 9 shuffles in place of 40.
+__device__ __forceinline__ int red8_slot(int lane) { return ((lane & 1) << 2) | (lane & 2) | ((lane >> 2) & 1); }
+__device__ __forceinline__ float warp_reduce8(const float (&v)[8], int lane) {
+    const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
+    float a[4], b[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        a[j] = (b0 ? v[4 + j] : v[j]) + __shfl_xor_sync(0xffffffffu, b0 ? v[j] : v[4 + j], 1);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        b[j] = (b1 ? a[2 + j] : a[j]) + __shfl_xor_sync(0xffffffffu, b1 ? a[j] : a[2 + j], 2);
+    float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, b2 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 8);
+    return c + __shfl_xor_sync(0xffffffffu, c, 16);
+}
+// Rows of one tensor laid out [token][head][D] for a CTA of D threads: the rows of head hh at tokens
+// tb .. tb + 7 into dst[8][D] by 16-byte cp.async (rows at or past t_end zero-filled, read from token 0's
+// row, which exists whenever there are tokens).
+template <typename T, int D>
+__device__ __forceinline__ void stage_rows8(T* dst, const T* __restrict__ src, int64_t tb, int64_t t_end, int H,
+                                            int hh) {
+    constexpr int CPR = D * (int)sizeof(T) / 16;  // 16-byte pieces per row
+    constexpr int PER = 8 * CPR / D;              // pieces per thread
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = (int)threadIdx.x + D * i, u = j / CPR, piece = j % CPR;
+        const int64_t t = tb + u;
+        const bool in = t < t_end;
+        const char* g = reinterpret_cast<const char*>(src + ((size_t)(in ? t : 0) * H + hh) * D) + 16 * piece;
+        const uint32_t d = (uint32_t)__cvta_generic_to_shared(reinterpret_cast<char*>(dst + u * D) + 16 * piece);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(g), "r"(in ? 16 : 0) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// ---- 2. conv (+ L2): a CTA per (row, span of tokens) with a thread per channel; rows r < Hq are q-heads,
+// < Hq + Hkv k-heads, else v-heads.  The CTA streams its span's input rows through a shared-memory ring of
+// kCvRing blocks of 8 tokens (cp.async, kCvRing - 1 blocks in flight) and keeps the last 8 inputs of each
+// channel in a register ring (token t in slot (t - span start) mod 8), zeroed where a sequence starts so
+// that the taps before a sequence's first token read zero.  Every input row is read once (the 7 rows before
+// a span twice).  One CTA barrier per block: it makes the block's rows visible, frees the slot the next copy
+// refills, and closes the previous block's L2 row sums, whose outputs are written then.
+constexpr int kCvRing = 4;
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(D)
 bwd_conv_kernel(LayerDims L, const Tin* __restrict__ v, const float* __restrict__ wq, const float* __restrict__ wk,
                 const float* __restrict__ wv, const int32_t* __restrict__ cu, const float* __restrict__ qr,
                 const float* __restrict__ kr, float* __restrict__ qt, float* __restrict__ qh,
-                float* __restrict__ kt, float* __restrict__ kh, float* __restrict__ vh) {
-    constexpr int E = D / 32;
-    const int64_t t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int n = seq_of_token(cu, L.n_seqs, t);
-    int64_t start, len;
-    seq_range(cu, n, L.total, &start, &len);
-    const int64_t p = t - start;
-    for (int r = warp; r < L.Hq + 2 * L.Hkv; r += kRowThreads / 32) {
-        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-        const int H = kind == 0 ? L.Hq : L.Hkv;
-        const float* w = (kind == 0 ? wq : kind == 1 ? wk : wv) + (size_t)hh * D * kConvWidth;
-        float acc[E], wt[E][kConvWidth];
+                float* __restrict__ kt, float* __restrict__ kh, float* __restrict__ vh, int64_t span) {
+    constexpr int B = kConvWidth;
+    __shared__ __align__(16) float ring_f[kCvRing][B][D];  // q, k rows (v rows use the first half, as Tin)
+    __shared__ float part[2][B][D / 32];
+    const int c = threadIdx.x, r = blockIdx.y;
+    const int64_t t0 = (int64_t)blockIdx.x * span;
+    if (t0 >= L.total) return;  // whole CTA
+    const int64_t t1 = min(L.total, t0 + span);
+    const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
+    const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
+    const int H = kind == 0 ? L.Hq : L.Hkv;
+    const bool norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));  // uniform over the CTA
+    const float* src = kind == 0 ? qr : kr;
+    auto issue = [&](int64_t tb, int slot) {
+        if (kind == 2)
+            stage_rows8<Tin, D>(reinterpret_cast<Tin*>(&ring_f[slot][0][0]), v, tb, t1, H, hh);
+        else
+            stage_rows8<float, D>(&ring_f[slot][0][0], src, tb, t1, H, hh);
+        cp_async_commit_group();
+    };
+    auto staged = [&](int slot, int u) {
+        return kind == 2 ? to_f32(reinterpret_cast<const Tin*>(&ring_f[slot][0][0])[u * D + c]) : ring_f[slot][u][c];
+    };
+    const int64_t n_blk = (t1 - t0 + B - 1) / B;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            acc[e] = 0.f;
-            const float4* w4 = reinterpret_cast<const float4*>(w + (size_t)(lane + 32 * e) * kConvWidth);
-            const float4 a = w4[0], b = w4[1];
-            wt[e][0] = a.x; wt[e][1] = a.y; wt[e][2] = a.z; wt[e][3] = a.w;
-            wt[e][4] = b.x; wt[e][5] = b.y; wt[e][6] = b.z; wt[e][7] = b.w;
-        }
-#pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) {
-            const int64_t pp = p - (kConvWidth - 1) + m;
-            if (pp < 0) continue;
-            const size_t row = ((size_t)(start + pp) * H + hh) * D;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int c = lane + 32 * e;
-                const float x = kind == 0 ? qr[row + c] : kind == 1 ? kr[row + c] : to_f32(v[row + c]);
-                acc[e] = fmaf(wt[e][m], x, acc[e]);
-            }
-        }
-        const size_t o = ((size_t)t * H + hh) * D;
-        if (kind == 2) {
-#pragma unroll
-            for (int e = 0; e < E; ++e) vh[o + lane + 32 * e] = acc[e];
-            continue;
-        }
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) ss = fmaf(acc[e], acc[e], ss);
-        const bool norm = kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q);
-        const float inv = norm ? rsqrtf(warp_sum_f(ss) + 1e-6f) : 1.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            (kind == 0 ? qt : kt)[o + lane + 32 * e] = acc[e];
-            (kind == 0 ? qh : kh)[o + lane + 32 * e] = acc[e] * inv;
+    for (int i = 0; i < kCvRing - 1; ++i) {
+        if (i < n_blk) {
+            issue(t0 + (int64_t)B * i, i);
+        } else {
+            cp_async_commit_group();  // empty groups keep the count per block uniform
         }
     }
+    float wt[kConvWidth];
+    {
+        const float4* w4 = reinterpret_cast<const float4*>((kind == 0 ? wq : kind == 1 ? wk : wv) +
+                                                           ((size_t)hh * D + c) * kConvWidth);
+        const float4 a = w4[0], b = w4[1];
+        wt[0] = a.x; wt[1] = a.y; wt[2] = a.z; wt[3] = a.w;
+        wt[4] = b.x; wt[5] = b.y; wt[6] = b.z; wt[7] = b.w;
+    }
+    int s = seq_of_token(cu, L.n_seqs, t0);
+    int64_t s_start, s_len;
+    seq_range(cu, s, L.total, &s_start, &s_len);
+    float ring[B];
+    ring[0] = 0.f;
+#pragma unroll
+    for (int m = 0; m < B - 1; ++m) {  // tokens t0 - 7 .. t0 - 1 in slots 1..7: those of t0's sequence
+        const int64_t t = t0 - (B - 1) + m;
+        const size_t i = ((size_t)t * H + hh) * D + c;
+        ring[m + 1] = t >= s_start && t >= 0 ? (kind == 2 ? to_f32(v[i]) : src[i]) : 0.f;
+    }
+    float* out_t = kind == 0 ? qt : kind == 1 ? kt : vh;
+    float* out_h = kind == 0 ? qh : kh;
+    float y[B];  // the previous block's conv outputs, written after the next barrier
+    // the outputs of block tb (its row sums in part[p] for the normalised rows)
+    auto finish = [&](int64_t tb, int p) {
+        float inv[B];
+        if (norm) {
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) acc += part[p][u][k];
+                inv[u] = rsqrtf(acc + 1e-6f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            if (t >= t1) break;
+            const size_t o = ((size_t)t * H + hh) * D + c;
+            out_t[o] = y[u];
+            if (kind != 2) out_h[o] = norm ? y[u] * inv[u] : y[u];
+        }
+    };
+#pragma unroll 1
+    for (int64_t b = 0; b < n_blk; ++b) {
+        const int64_t tb = t0 + B * b;
+        cp_async_wait_group<kCvRing - 2>();
+        __syncthreads();
+        if (b > 0) finish(tb - B, (int)((b - 1) & 1));
+        if (b + kCvRing - 1 < n_blk) {
+            issue(tb + (int64_t)B * (kCvRing - 1), (int)((b + kCvRing - 1) % kCvRing));
+        } else {
+            cp_async_commit_group();
+        }
+        const int slot = (int)(b % kCvRing);
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            while (t >= s_start + s_len && s + 1 < L.n_seqs) {  // uniform over the CTA
+                ++s;
+                seq_range(cu, s, L.total, &s_start, &s_len);
+            }
+            if (t == s_start) {  // a sequence starts here: nothing before it feeds the conv
+#pragma unroll
+                for (int m = 0; m < B; ++m) ring[m] = 0.f;
+            }
+            ring[u] = staged(slot, u);
+            // tap m reads token t - 7 + m: slot (u + 1 + m) mod 8
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) acc = fmaf(wt[m], ring[(u + 1 + m) & (B - 1)], acc);
+            y[u] = acc;
+        }
+        if (norm) {
+            float sq[B];
+#pragma unroll
+            for (int u = 0; u < B; ++u) sq[u] = y[u] * y[u];
+            const int lane = c & 31;
+            const float w = warp_reduce8(sq, lane);
+            if (lane < 8) part[b & 1][red8_slot(lane)][c >> 5] = w;
+        }
+    }
+    __syncthreads();
+    if (n_blk > 0) finish(t0 + B * (n_blk - 1), (int)((n_blk - 1) & 1));
 }
 
 // ---- 3. GDN backward: a cluster of kCl CTAs per (q-head, sequence), each CTA D / kCl value columns of S
@@ -978,190 +1086,266 @@ __global__ void bwd_sm_sink_kernel(LayerDims L, const int32_t* __restrict__ cu, 
     }
 }
 
-// ---- 5. feature backward: first the L2 backward into the gradient of the pre-norm rows (q-heads, then
-// k-heads with the group's per-head gradients summed) and the group sums of the v rows; the conv and RoPE
-// backward then run in bwd_feat_out_kernel.  CTA per token, a warp per row, lane l channels l + 32 e.
+// ---- 5. feature backward, a CTA per (row, span of tokens) with a thread per channel, as in the conv above.
+// Per token t' of the row the L2 backward gives y(t'), the gradient of the conv output (q-heads: from dqhat;
+// k-heads: from the sum of the group's per-head dkhat; v-heads: the sum of the group's per-head dvhat, no
+// norm), kept for the filter gradients; the conv's transpose then gives the input's gradient,
+// dx(t) = sum_m w_m y(t + 7 - m) over the t + 7 - m inside t's sequence, to which the softmax branch's
+// gradient of the same row is added (summed over the group for k and v) before RoPE's transpose (q, k),
+// which pairs channel i with i + d / 2.  Walking the span in blocks of 8 tokens, the CTA holds y of the
+// current block and the next one; per block it forms y of the block after those (its two row sums through
+// shared memory) and dx of the current block (the RoPE partner channels through shared memory), all behind
+// one CTA barrier.  The 15 rows of y past the span are formed again by the next span's CTA, which writes them.
+struct FeatOutArgs {
+    const int32_t* cu;
+    const float *wq, *wk, *wv, *qt, *kt, *dqh, *dkh_h, *dvh_h, *dqr_sm, *dkr_h, *dv_h;
+    const float2* ang;
+    float *dqt, *dkt, *dvt, *dq, *dk, *dv;
+};
+
 template <int D>
-__global__ void __launch_bounds__(kRowThreads)
-bwd_l2_kernel(LayerDims L, const float* __restrict__ qt, const float* __restrict__ kt,
-              const float* __restrict__ dqh, const float* __restrict__ dkh_h, const float* __restrict__ dvh_h,
-              float* __restrict__ dqt, float* __restrict__ dkt, float* __restrict__ dvt) {
-    constexpr int E = D / 32;
-    const int64_t t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < L.Hq + 2 * L.Hkv; r += kRowThreads / 32) {
-        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-        float dy[E];
+__global__ void __launch_bounds__(D, 1024 / D)
+bwd_feat_out_kernel(LayerDims L, FeatOutArgs A, int64_t span) {
+    constexpr int B = kConvWidth, half = D / 2;
+    __shared__ float part[2][2][B][D / 32];  // [parity][|x|^2, x . dy][token][warp]
+    __shared__ float dxs[2][B][D];           // [parity][token][channel]: dx before RoPE's transpose
+    const int c = threadIdx.x, r = blockIdx.y;
+    const int64_t t0 = (int64_t)blockIdx.x * span;
+    if (t0 >= L.total) return;  // whole CTA
+    const int64_t t1 = min(L.total, t0 + span);
+    const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
+    const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
+    const int H = kind == 0 ? L.Hq : L.Hkv, G = L.G;
+    const bool norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));  // uniform over the CTA
+    float wt[kConvWidth];
+    {
+        const float4* w4 = reinterpret_cast<const float4*>((kind == 0 ? A.wq : kind == 1 ? A.wk : A.wv) +
+                                                           ((size_t)hh * D + c) * kConvWidth);
+        const float4 a = w4[0], b = w4[1];
+        wt[0] = a.x; wt[1] = a.y; wt[2] = a.z; wt[3] = a.w;
+        wt[4] = b.x; wt[5] = b.y; wt[6] = b.z; wt[7] = b.w;
+    }
+    // per-head gradients of the row: one row (q) or the group's G rows (k, v), at channel c of token t
+    const float* ysrc = kind == 0 ? A.dqh : kind == 1 ? A.dkh_h : A.dvh_h;
+    const float* gsrc = kind == 0 ? A.dqr_sm : kind == 1 ? A.dkr_h : A.dv_h;
+    const int n_src = kind == 0 ? 1 : G;
+    auto src_sum = [&](const float* base, int64_t t) {
+        const float* p = base + ((size_t)t * L.Hq + (size_t)hh * n_src) * D + c;
+        float acc = 0.f;
+        for (int g = 0; g < n_src; ++g) acc += p[(size_t)g * D];
+        return acc;
+    };
+    const float* pre = kind == 0 ? A.qt : A.kt;
+    float* ydst = kind == 0 ? A.dqt : kind == 1 ? A.dkt : A.dvt;
+    // y of the 8 tokens from tb (zero past the last token), written out for the tokens of the span
+    auto y_block = [&](int64_t tb, float (&y)[B], float (&x)[B], float (*p)[B][D / 32]) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) dy[e] = 0.f;
-        if (kind == 0) {
-#pragma unroll
-            for (int e = 0; e < E; ++e) dy[e] = dqh[((size_t)t * L.Hq + hh) * D + lane + 32 * e];
-        } else {
-            const float* src = kind == 1 ? dkh_h : dvh_h;
-            for (int gq = 0; gq < L.G; ++gq)
-#pragma unroll
-                for (int e = 0; e < E; ++e) dy[e] += src[((size_t)t * L.Hq + hh * L.G + gq) * D + lane + 32 * e];
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            const bool in = t < L.total;
+            y[u] = in ? src_sum(ysrc, t) : 0.f;
+            x[u] = in && norm ? pre[((size_t)t * H + hh) * D + c] : 0.f;
         }
-        if (kind == 2) {  // vhat = conv(v): no norm
-#pragma unroll
-            for (int e = 0; e < E; ++e) dvt[((size_t)t * L.Hkv + hh) * D + lane + 32 * e] = dy[e];
-            continue;
-        }
-        const float* pre = kind == 0 ? qt + ((size_t)t * L.Hq + hh) * D : kt + ((size_t)t * L.Hkv + hh) * D;
-        float* dst = kind == 0 ? dqt + ((size_t)t * L.Hq + hh) * D : dkt + ((size_t)t * L.Hkv + hh) * D;
-        if (kind == 1 || (L.flags & HLA_FLAG_L2NORM_Q)) {
+        if (norm) {
             // y = x / nrm, nrm = sqrt(|x|^2 + eps): dx = (dy - x (x . dy) / nrm^2) / nrm
-            float x[E], n2 = 0.f, xd = 0.f;
+            float n2[B], xd[B];
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                x[e] = pre[lane + 32 * e];
-                n2 = fmaf(x[e], x[e], n2);
-                xd = fmaf(x[e], dy[e], xd);
+            for (int u = 0; u < B; ++u) {
+                n2[u] = x[u] * x[u];
+                xd[u] = x[u] * y[u];
             }
-            n2 = warp_sum_f(n2) + 1e-6f;
-            xd = warp_sum_f(xd);
-            const float inv = rsqrtf(n2);
+            const int lane = c & 31, warp = c >> 5;
+            const float wn = warp_reduce8(n2, lane), wd = warp_reduce8(xd, lane);
+            if (lane < 8) {  // the caller finishes after a barrier
+                p[0][red8_slot(lane)][warp] = wn;
+                p[1][red8_slot(lane)][warp] = wd;
+            }
+        }
+    };
+    auto y_finish = [&](int64_t tb, float (&y)[B], const float (&x)[B], float (*p)[B][D / 32]) {
+        if (norm) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) dst[lane + 32 * e] = (dy[e] - x[e] * xd / n2) * inv;
-        } else {
+            for (int u = 0; u < B; ++u) {
+                float n2 = 0.f, xd = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) dst[lane + 32 * e] = dy[e];
+                for (int k = 0; k < D / 32; ++k) {
+                    n2 += p[0][u][k];
+                    xd += p[1][u][k];
+                }
+                n2 += 1e-6f;
+                y[u] = (y[u] - x[u] * xd / n2) * rsqrtf(n2);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+            if (tb + u >= t0 && tb + u < t1) ydst[((size_t)(tb + u) * H + hh) * D + c] = y[u];
+    };
+    int s = seq_of_token(A.cu, L.n_seqs, t0);
+    int64_t s_start, s_len;
+    seq_range(A.cu, s, L.total, &s_start, &s_len);
+    float y0[B], y1[B], y2[B], x[B];  // y of tokens tb .. tb + 7, tb + 8 .. tb + 15, tb + 16 .. tb + 23
+    y_block(t0, y0, x, part[0]);
+    if (norm) __syncthreads();
+    y_finish(t0, y0, x, part[0]);
+    y_block(t0 + B, y1, x, part[1]);
+    if (norm) __syncthreads();
+    y_finish(t0 + B, y1, x, part[1]);
+    if (norm) __syncthreads();  // the reads of part[0] and part[1] above come before the loop writes them
+    int par = 0;
+    float* dst = kind == 0 ? A.dq : kind == 1 ? A.dk : A.dv;
+#pragma unroll 1
+    for (int64_t tb = t0; tb < t1; tb += B, par ^= 1) {
+        y_block(tb + 2 * B, y2, x, part[par]);
+        float dx[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            while (t >= s_start + s_len && s + 1 < L.n_seqs) {  // uniform over the CTA
+                ++s;
+                seq_range(A.cu, s, L.total, &s_start, &s_len);
+            }
+            const int64_t s_end = s_start + s_len;
+            float acc = 0.f;
+            // x_t feeds the conv output at t + 7 - m through tap m
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) {
+                const int j = u + (kConvWidth - 1) - m;
+                if (tb + j < s_end) acc = fmaf(wt[m], j < B ? y0[j] : y1[j - B], acc);
+            }
+            dx[u] = t < t1 ? acc + src_sum(gsrc, t) : 0.f;
+            if (kind != 2) dxs[par][u][c] = dx[u];
+        }
+        if (kind != 2) __syncthreads();
+        y_finish(tb + 2 * B, y2, x, part[par]);
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            if (t >= t1) break;
+            const size_t o = ((size_t)t * H + hh) * D + c;
+            if (kind == 2) {
+                dst[o] = dx[u];
+            } else {  // RoPE's transpose: rotate the pair (i, i + d / 2) back by the angle p theta_i
+                const float2 a = A.ang[(size_t)t * half + (c & (half - 1))];
+                const float other = dxs[par][u][c ^ half];
+                dst[o] = c < half ? dx[u] * a.x + other * a.y : dx[u] * a.x - other * a.y;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            y0[u] = y1[u];
+            y1[u] = y2[u];
         }
     }
 }
 
-// conv backward (the taps that read position p, from the later positions of the same sequence), plus the
-// softmax branch's gradient, then RoPE's transpose; writes dq, dk, dv.  CTA per token; rows r < Hq are
-// q-heads, < Hq + Hkv k-heads, else v-heads; a thread per channel pair (i, i + d / 2).
-__global__ void __launch_bounds__(kRowThreads)
-bwd_feat_out_kernel(LayerDims L, const int32_t* __restrict__ cu, const float* __restrict__ wq,
-                    const float* __restrict__ wk, const float* __restrict__ wv, const float* __restrict__ dqt,
-                    const float* __restrict__ dkt, const float* __restrict__ dvt, const float* __restrict__ dqr_sm,
-                    const float* __restrict__ dkr_h, const float* __restrict__ dv_h, float* __restrict__ dq,
-                    float* __restrict__ dk, float* __restrict__ dv) {
-    __shared__ float cs[64], sn[64];
-    const int64_t t = blockIdx.x;
-    const int tid = threadIdx.x, D = L.d, half = D / 2;
-    const int n = seq_of_token(cu, L.n_seqs, t);
-    int64_t start, len;
-    seq_range(cu, n, L.total, &start, &len);
-    const int64_t p = t - start;
-    angles(L, p, cs, sn);
-    for (int idx = tid; idx < (L.Hq + 2 * L.Hkv) * half; idx += kRowThreads) {
-        const int r = idx / half, i = idx % half;
-        const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
-        const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-        const int H = kind == 0 ? L.Hq : L.Hkv;
-        const float* w = kind == 0 ? wq : kind == 1 ? wk : wv;
-        const float4* w1 = reinterpret_cast<const float4*>(w + ((size_t)hh * D + i) * kConvWidth);
-        const float4* w2 = reinterpret_cast<const float4*>(w + ((size_t)hh * D + i + half) * kConvWidth);
-        const float4 w1a = w1[0], w1b = w1[1], w2a = w2[0], w2b = w2[1];
-        const float t1[kConvWidth] = {w1a.x, w1a.y, w1a.z, w1a.w, w1b.x, w1b.y, w1b.z, w1b.w};
-        const float t2[kConvWidth] = {w2a.x, w2a.y, w2a.z, w2a.w, w2b.x, w2b.y, w2b.z, w2b.w};
-        const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
-        // x_p feeds y_{p + 7 - m} through tap m
-        float a1 = 0.f, a2 = 0.f;
-#pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) {
-            const int64_t pp = p + (kConvWidth - 1) - m;
-            if (pp >= len) continue;
-            const float* yr = dy + ((size_t)(start + pp) * H + hh) * D;
-            a1 = fmaf(t1[m], yr[i], a1);
-            a2 = fmaf(t2[m], yr[i + half], a2);
-        }
-        // the softmax branch's gradient of the RoPE'd row (q, k) or of raw v, summed over the group for k, v
-        if (kind == 0) {
-            const float* sg = dqr_sm + ((size_t)t * L.Hq + hh) * D;
-            a1 += sg[i];
-            a2 += sg[i + half];
-        } else {
-            for (int gq = 0; gq < L.G; ++gq) {
-                const float* sg = (kind == 1 ? dkr_h : dv_h) + ((size_t)t * L.Hq + hh * L.G + gq) * D;
-                a1 += sg[i];
-                a2 += sg[i + half];
-            }
-        }
-        if (kind == 2) {
-            float* o = dv + ((size_t)t * L.Hkv + hh) * D;
-            o[i] = a1;
-            o[i + half] = a2;
-        } else {  // RoPE's transpose: rotate the pair back by the angle p theta_i
-            float* o = (kind == 0 ? dq : dk) + ((size_t)t * H + hh) * D;
-            o[i] = a1 * cs[i] + a2 * sn[i];
-            o[i + half] = a2 * cs[i] - a1 * sn[i];
-        }
-    }
-}
-
-// ---- 6. conv filters: partial sums over a block of kWB tokens, per (row, channel, tap); then the blocks.
-// A thread walks its channel through the block's tokens with the last 8 inputs of the sequence in
-// registers (zeros before the sequence start), so every input is read once.
-template <typename Tin>
-__global__ void bwd_convw_part_kernel(LayerDims L, const Tin* __restrict__ v, const int32_t* __restrict__ cu,
-                                      const float* __restrict__ qr, const float* __restrict__ kr,
-                                      const float* __restrict__ dqt, const float* __restrict__ dkt,
-                                      const float* __restrict__ dvt, float* __restrict__ part) {
-    __shared__ int32_t pos_s[kWB];  // position of each token of the block in its sequence
-    const int blk = blockIdx.x, r = blockIdx.y, c = threadIdx.x, D = L.d;
+// ---- 6. conv filters: partial sums over a span of tokens per (row, channel, tap), then over the spans.
+// A CTA per (row, span of at least kWB tokens) with a thread per channel streams the span's conv inputs and
+// the gradients y of the conv outputs through a shared-memory ring as in the conv launch, with the last 8
+// inputs of each channel in registers (zeros before a sequence's start), so every row is read once.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(D)
+bwd_convw_part_kernel(LayerDims L, const Tin* __restrict__ v, const int32_t* __restrict__ cu,
+                      const float* __restrict__ qr, const float* __restrict__ kr, const float* __restrict__ dqt,
+                      const float* __restrict__ dkt, const float* __restrict__ dvt, float* __restrict__ part,
+                      int64_t span) {
+    constexpr int B = kConvWidth;
+    __shared__ __align__(16) float xs[kCvRing][B][D];  // conv inputs (v rows use the first half, as Tin)
+    __shared__ __align__(16) float ys[kCvRing][B][D];  // gradients of the conv outputs
+    const int c = threadIdx.x, r = blockIdx.y, rows = L.Hq + 2 * L.Hkv;
+    const int64_t t0 = (int64_t)blockIdx.x * span;
+    if (t0 >= L.total) return;  // whole CTA
+    const int64_t t1 = min(L.total, t0 + span);
     const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
     const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
     const int H = kind == 0 ? L.Hq : L.Hkv;
+    const float* src = kind == 0 ? qr : kr;
     const float* dy = kind == 0 ? dqt : kind == 1 ? dkt : dvt;
-    const int64_t t0 = (int64_t)blk * kWB, t1 = min(L.total, t0 + kWB);
-    for (int64_t t = t0 + c; t < t1; t += blockDim.x) {
-        int64_t start, len;
-        seq_range(cu, seq_of_token(cu, L.n_seqs, t), L.total, &start, &len);
-        pos_s[t - t0] = (int32_t)min(t - start, (int64_t)INT32_MAX);
-    }
-    __syncthreads();
-    auto input = [&](int64_t t) {
-        const size_t row = ((size_t)t * H + hh) * D + c;
-        return kind == 0 ? qr[row] : kind == 1 ? kr[row] : to_f32(v[row]);
+    auto issue = [&](int64_t tb, int slot) {
+        if (kind == 2)
+            stage_rows8<Tin, D>(reinterpret_cast<Tin*>(&xs[slot][0][0]), v, tb, t1, H, hh);
+        else
+            stage_rows8<float, D>(&xs[slot][0][0], src, tb, t1, H, hh);
+        stage_rows8<float, D>(&ys[slot][0][0], dy, tb, t1, H, hh);
+        cp_async_commit_group();
     };
-    float acc[kConvWidth], win[kConvWidth];  // win[m]: the input at position p - 7 + m
+    const int64_t n_blk = (t1 - t0 + B - 1) / B;
 #pragma unroll
-    for (int m = 0; m < kConvWidth; ++m) acc[m] = win[m] = 0.f;
-    // the window before the block's first token
-    if (t1 > t0) {
-        const int p0 = pos_s[0];
-#pragma unroll
-        for (int m = 1; m < kConvWidth; ++m) {
-            const int back = kConvWidth - m;  // position p0 - back sits at win[m - 1] before the shift
-            win[m] = back <= p0 ? input(t0 - back) : 0.f;
-        }
-    }
-    for (int64_t t = t0; t < t1; ++t) {
-        const int p = pos_s[t - t0];
-        if (p == 0) {  // a sequence starts: nothing before it
-#pragma unroll
-            for (int m = 0; m < kConvWidth; ++m) win[m] = 0.f;
+    for (int i = 0; i < kCvRing - 1; ++i) {
+        if (i < n_blk) {
+            issue(t0 + (int64_t)B * i, i);
         } else {
-#pragma unroll
-            for (int m = 0; m + 1 < kConvWidth; ++m) win[m] = win[m + 1];
+            cp_async_commit_group();
         }
-        win[kConvWidth - 1] = input(t);
-        const float d_y = dy[((size_t)t * H + hh) * D + c];
-#pragma unroll
-        for (int m = 0; m < kConvWidth; ++m) acc[m] = fmaf(d_y, win[m], acc[m]);
     }
-    const int rows = L.Hq + 2 * L.Hkv;
+    int s = seq_of_token(cu, L.n_seqs, t0);
+    int64_t s_start, s_len;
+    seq_range(cu, s, L.total, &s_start, &s_len);
+    float ring[B], acc[kConvWidth];
+    ring[0] = 0.f;
 #pragma unroll
-    for (int m = 0; m < kConvWidth; ++m) part[(((size_t)blk * rows + r) * D + c) * kConvWidth + m] = acc[m];
+    for (int m = 0; m < B - 1; ++m) {  // tokens t0 - 7 .. t0 - 1 in slots 1..7: those of t0's sequence
+        const int64_t t = t0 - (B - 1) + m;
+        const size_t i = ((size_t)t * H + hh) * D + c;
+        ring[m + 1] = t >= s_start && t >= 0 ? (kind == 2 ? to_f32(v[i]) : src[i]) : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < kConvWidth; ++m) acc[m] = 0.f;
+#pragma unroll 1
+    for (int64_t b = 0; b < n_blk; ++b) {
+        const int64_t tb = t0 + B * b;
+        cp_async_wait_group<kCvRing - 2>();
+        __syncthreads();
+        if (b + kCvRing - 1 < n_blk) {
+            issue(tb + (int64_t)B * (kCvRing - 1), (int)((b + kCvRing - 1) % kCvRing));
+        } else {
+            cp_async_commit_group();
+        }
+        const int slot = (int)(b % kCvRing);
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            while (t >= s_start + s_len && s + 1 < L.n_seqs) {  // uniform over the CTA
+                ++s;
+                seq_range(cu, s, L.total, &s_start, &s_len);
+            }
+            if (t == s_start) {  // a sequence starts here: nothing before it
+#pragma unroll
+                for (int m = 0; m < B; ++m) ring[m] = 0.f;
+            }
+            ring[u] = kind == 2 ? to_f32(reinterpret_cast<const Tin*>(&xs[slot][0][0])[u * D + c]) : xs[slot][u][c];
+            const float d_y = ys[slot][u][c];  // zero past the span
+            // tap m multiplies the input at t - 7 + m: slot (u + 1 + m) mod 8
+#pragma unroll
+            for (int m = 0; m < kConvWidth; ++m) acc[m] = fmaf(d_y, ring[(u + 1 + m) & (B - 1)], acc[m]);
+        }
+    }
+    float4* o = reinterpret_cast<float4*>(part + (((size_t)blockIdx.x * rows + r) * D + c) * kConvWidth);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-__global__ void bwd_convw_sum_kernel(LayerDims L, int n_blocks, const float* __restrict__ part,
-                                     float* __restrict__ dwq, float* __restrict__ dwk, float* __restrict__ dwv) {
-    const int r = blockIdx.x, c = threadIdx.x, D = L.d, rows = L.Hq + 2 * L.Hkv;
+// the sum of the spans' partial sums, in span order; a thread per (row, channel, tap) of the filters
+constexpr int kWsThreads = 256;
+__global__ void __launch_bounds__(kWsThreads)
+bwd_convw_sum_kernel(LayerDims L, int n_spans, const float* __restrict__ part, float* __restrict__ dwq,
+                     float* __restrict__ dwk, float* __restrict__ dwv) {
+    const int r = blockIdx.x, f = blockIdx.y * kWsThreads + threadIdx.x, D = L.d, rows = L.Hq + 2 * L.Hkv;
+    if (f >= D * kConvWidth) return;
     const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
     const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-    float* dw = (kind == 0 ? dwq : kind == 1 ? dwk : dwv) + ((size_t)hh * D + c) * kConvWidth;
-    for (int m = 0; m < kConvWidth; ++m) {
-        float s = 0.f;
-        for (int b = 0; b < n_blocks; ++b) s += part[(((size_t)b * rows + r) * D + c) * kConvWidth + m];
-        dw[m] = s;
+    const size_t stride = (size_t)rows * D * kConvWidth;
+    const float* p = part + (size_t)r * D * kConvWidth + f;
+    float s = 0.f;
+    int b = 0;
+    for (; b + 8 <= n_spans; b += 8) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = p[(size_t)(b + k) * stride];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += x[k];
     }
+    for (; b < n_spans; ++b) s += p[(size_t)b * stride];
+    (kind == 0 ? dwq : kind == 1 ? dwk : dwv)[(size_t)hh * D * kConvWidth + f] = s;
 }
 
 // ---- 7. lambda: partial sums over the sequences
@@ -1208,15 +1392,46 @@ BwdLayout bwd_layout(const LayerDims& L) {
     b.ckpt = take((T / kCkB + N + 1) * Hq * D * D);  // S every 64 absorptions of every sequence and q-head
     b.sub = take(N * Hq * spb * D * D);               // S every stage of one 64-absorption block
     b.dlam_part = take(N * Hq);
-    b.convw_part = take(nblk * rows * D * kConvWidth);
+    b.convw_part = take(nblk * rows * D * kConvWidth);  // per span of at least kWB tokens
     b.n_blocks = (int)nblk;
     b.n_sm_blocks = (int)(T / kSB + N);                // bounds the 64-row softmax blocks of all sequences
     b.sm_base = take(N + 1);                           // int32
     b.sink_k = take((size_t)b.n_sm_blocks * Hq * (size_t)L.n_sinks * D);
     b.sink_v = take((size_t)b.n_sm_blocks * Hq * (size_t)L.n_sinks * D);
+    take(T * D);  // the RoPE angle table, the last region (bwd_ang_offset)
     b.total = off;
     return b;
 }
+
+namespace {
+// The RoPE cos/sin of every token, a float2 per channel pair (written by the RoPE launch, read by the RoPE
+// backward): the last region of the workspace
+size_t bwd_ang_offset(const LayerDims& L, const BwdLayout& b) {
+    return b.total - ((size_t)L.total * L.d * sizeof(float) + 255) / 256 * 256;
+}
+
+// Token spans of a launch with a CTA of `threads` per (row, span of tokens): the smallest multiple of 8 tokens
+// (at least min_span, itself a multiple of 8) for which the grid (spans x rows) is one wave of the CTAs the
+// device holds at once
+template <class K>
+cudaError_t row_span_grid(DeviceCache& cache, K kernel, int threads, int64_t min_span, const LayerDims& L,
+                          int64_t* span, dim3* grid) {
+    int resident = 0;
+    cudaError_t e = device_cached(cache, &resident, [kernel, threads](int dev, int* val) {
+        int n_sm = 0, per_sm = 0;
+        cudaError_t r = sm_count(dev, &n_sm);
+        if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        *val = std::max(1, n_sm * std::max(1, per_sm));
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    const int rows = L.Hq + 2 * L.Hkv;
+    const int64_t spans = std::max<int64_t>(1, resident / rows);
+    *span = std::max<int64_t>(min_span, ((L.total + spans - 1) / spans + kConvWidth - 1) / kConvWidth * kConvWidth);
+    *grid = dim3((unsigned)((L.total + *span - 1) / *span), (unsigned)rows);
+    return cudaSuccess;
+}
+}  // namespace
 
 template <typename Tin, int D>
 cudaError_t launch_gdn_bwd(const LayerDims& L, const float* alpha, const float* beta, const float* lambda,
@@ -1276,7 +1491,7 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
                             const BwdLayout& b, const cudaEvent_t* marks, int n_marks, cudaStream_t st) {
     auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     auto mark = [&](int i) { return i < n_marks && marks[i] ? cudaEventRecord(marks[i], st) : cudaSuccess; };
-    const size_t T = (size_t)L.total;
+    const size_t T = (size_t)L.total;  // > 0: with no tokens hla_backward returns before the launches
     const int D = L.d, rows = L.Hq + 2 * L.Hkv;
     cudaError_t e;
     // tokens that no state absorbs keep zero gradients of g, beta, khat, vhat
@@ -1289,15 +1504,25 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
     if ((e = mark(0)) != cudaSuccess) return e;
     int32_t* sm_base = reinterpret_cast<int32_t*>(ws + b.sm_base);
     bwd_blocks_kernel<<<1, 1024, 0, st>>>(L, cu, sm_base, reinterpret_cast<int32_t*>(ws + b.err));
-    bwd_rope_kernel<Tin><<<(unsigned)T, kRowThreads, 0, st>>>(L, q, k, g, cu, F(b.qr), F(b.kr), F(b.alpha),
-                                                                        reinterpret_cast<int32_t*>(ws + b.err));
+    bwd_rope_kernel<Tin><<<(unsigned)T, kRowThreads, 0, st>>>(
+        L, q, k, g, cu, F(b.qr), F(b.kr), F(b.alpha), reinterpret_cast<float2*>(ws + bwd_ang_offset(L, b)),
+        reinterpret_cast<int32_t*>(ws + b.err));
     if ((e = mark(1)) != cudaSuccess) return e;
-    if (D == 128)
-        bwd_conv_kernel<Tin, 128><<<(unsigned)T, kRowThreads, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
-                                                                       F(b.qh), F(b.kt), F(b.kh), F(b.vh));
-    else
-        bwd_conv_kernel<Tin, 64><<<(unsigned)T, kRowThreads, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
-                                                                      F(b.qh), F(b.kt), F(b.kh), F(b.vh));
+    {
+        int64_t span = 0;
+        dim3 grid;
+        if (D == 128) {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 128>, 128, kConvWidth, L, &span, &grid)) != cudaSuccess) return e;
+            bwd_conv_kernel<Tin, 128><<<grid, 128, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
+                                                                     F(b.qh), F(b.kt), F(b.kh), F(b.vh), span);
+        } else {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 64>, 64, kConvWidth, L, &span, &grid)) != cudaSuccess) return e;
+            bwd_conv_kernel<Tin, 64><<<grid, 64, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
+                                                                    F(b.qh), F(b.kt), F(b.kh), F(b.vh), span);
+        }
+    }
     if ((e = mark(2)) != cudaSuccess) return e;
     e = D == 128 ? launch_gdn_bwd<Tin, 128>(L, F(b.alpha), beta, lambda, dout, cu, F(b.qh), F(b.kh), F(b.vh), F(b.ckpt),
                                             F(b.sub), F(b.dqh), F(b.dkh_h), F(b.dvh_h), dg, dbeta, F(b.dlam_part), st)
@@ -1311,19 +1536,46 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
                                           F(b.dqr_sm), F(b.dkr_h), F(b.dv_h), F(b.sink_k), F(b.sink_v), st);
     if (e != cudaSuccess) return e;
     if ((e = mark(4)) != cudaSuccess) return e;
-    if (D == 128)
-        bwd_l2_kernel<128><<<(unsigned)T, kRowThreads, 0, st>>>(L, F(b.qt), F(b.kt), F(b.dqh), F(b.dkh_h), F(b.dvh_h),
-                                                                F(b.dqt), F(b.dkt), F(b.dvt));
-    else
-        bwd_l2_kernel<64><<<(unsigned)T, kRowThreads, 0, st>>>(L, F(b.qt), F(b.kt), F(b.dqh), F(b.dkh_h), F(b.dvh_h),
-                                                               F(b.dqt), F(b.dkt), F(b.dvt));
-    if ((e = mark(5)) != cudaSuccess) return e;
-    bwd_feat_out_kernel<<<(unsigned)T, kRowThreads, 0, st>>>(L, cu, wq, wk, wv, F(b.dqt), F(b.dkt), F(b.dvt),
-                                                               F(b.dqr_sm), F(b.dkr_h), F(b.dv_h), dq, dk, dv);
+    if ((e = mark(5)) != cudaSuccess) return e;  // the L2 backward runs inside the next launch
+    {
+        const FeatOutArgs A{cu,        wq,         wk,         wv,          F(b.qt),    F(b.kt),
+                            F(b.dqh),  F(b.dkh_h), F(b.dvh_h), F(b.dqr_sm), F(b.dkr_h), F(b.dv_h),
+                            reinterpret_cast<const float2*>(ws + bwd_ang_offset(L, b)),
+                            F(b.dqt),  F(b.dkt),   F(b.dvt),   dq,          dk,         dv};
+        int64_t span = 0;
+        dim3 grid;
+        if (D == 128) {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_feat_out_kernel<128>, 128, kConvWidth, L, &span, &grid)) != cudaSuccess)
+                return e;
+            bwd_feat_out_kernel<128><<<grid, 128, 0, st>>>(L, A, span);
+        } else {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_feat_out_kernel<64>, 64, kConvWidth, L, &span, &grid)) != cudaSuccess)
+                return e;
+            bwd_feat_out_kernel<64><<<grid, 64, 0, st>>>(L, A, span);
+        }
+    }
     if ((e = mark(6)) != cudaSuccess) return e;
-    bwd_convw_part_kernel<Tin><<<dim3(b.n_blocks, rows), D, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),
-                                                                      F(b.dvt), F(b.convw_part));
-    bwd_convw_sum_kernel<<<rows, D, 0, st>>>(L, b.n_blocks, F(b.convw_part), dwq, dwk, dwv);
+    {
+        int64_t span = 0;
+        dim3 grid;  // spans of at least kWB tokens: at most b.n_blocks partial sums
+        if (D == 128) {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 128>, 128, kWB, L, &span, &grid)) != cudaSuccess)
+                return e;
+            bwd_convw_part_kernel<Tin, 128><<<grid, 128, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),
+                                                                   F(b.dvt), F(b.convw_part), span);
+        } else {
+            static DeviceCache cache;
+            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 64>, 64, kWB, L, &span, &grid)) != cudaSuccess)
+                return e;
+            bwd_convw_part_kernel<Tin, 64><<<grid, 64, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),
+                                                                 F(b.dvt), F(b.convw_part), span);
+        }
+        bwd_convw_sum_kernel<<<dim3(rows, (D * kConvWidth + kWsThreads - 1) / kWsThreads), kWsThreads, 0, st>>>(
+            L, (int)grid.x, F(b.convw_part), dwq, dwk, dwv);
+    }
     if ((e = mark(7)) != cudaSuccess) return e;
     bwd_lambda_kernel<<<(L.Hq + 127) / 128, 128, 0, st>>>(L, F(b.dlam_part), dlam);
     if ((e = mark(8)) != cudaSuccess) return e;
