@@ -1093,30 +1093,69 @@ __global__ void bwd_sm_sink_kernel(LayerDims L, const int32_t* __restrict__ cu, 
 // dx(t) = sum_m w_m y(t + 7 - m) over the t + 7 - m inside t's sequence, to which the softmax branch's
 // gradient of the same row is added (summed over the group for k and v) before RoPE's transpose (q, k),
 // which pairs channel i with i + d / 2.  Walking the span in blocks of 8 tokens, the CTA holds y of the
-// current block and the next one; per block it forms y of the block after those (its two row sums through
-// shared memory) and dx of the current block (the RoPE partner channels through shared memory), all behind
-// one CTA barrier.  The 15 rows of y past the span are formed again by the next span's CTA, which writes them.
+// current block and the next one, and per block forms y of the block after those and dx of the current one.
+// Its rows stream through a shared-memory ring of kFoRing units (cp.async, kFoRing - 1 in flight); a unit
+// holds, for one head g of the row's group (one head for q), 8 rows of y's source for a later block and of
+// the softmax gradient for the current one, and with g = 0 also the 8 pre-norm rows and RoPE angles.  The
+// first 2 units per head carry y's sources of the span's first two blocks.  One CTA barrier per unit; the
+// row sums of the L2 backward and the RoPE partners cross the CTA in shared memory (double-buffered by block
+// parity) and are read after the next unit's barrier.  The 15 rows of y past the span are formed again by
+// the next span's CTA, which writes them.
 struct FeatOutArgs {
     const int32_t* cu;
     const float *wq, *wk, *wv, *qt, *kt, *dqh, *dkh_h, *dvh_h, *dqr_sm, *dkr_h, *dv_h;
     const float2* ang;
     float *dqt, *dkt, *dvt, *dq, *dk, *dv;
 };
+constexpr int kFoRing = 4;
+template <int D>
+constexpr size_t feat_out_smem() {  // the unit ring, then part[2][2][8][D / 32], dxs[2][8][D]
+    return ((size_t)kFoRing * 4 * kConvWidth * D + 2 * 2 * kConvWidth * (D / 32) + 2 * kConvWidth * D) * sizeof(float);
+}
 
 template <int D>
-__global__ void __launch_bounds__(D, 1024 / D)
+__global__ void __launch_bounds__(D, 512 / D)
 bwd_feat_out_kernel(LayerDims L, FeatOutArgs A, int64_t span) {
-    constexpr int B = kConvWidth, half = D / 2;
-    __shared__ float part[2][2][B][D / 32];  // [parity][|x|^2, x . dy][token][warp]
-    __shared__ float dxs[2][B][D];           // [parity][token][channel]: dx before RoPE's transpose
-    const int c = threadIdx.x, r = blockIdx.y;
+    constexpr int B = kConvWidth, half = D / 2, NW = D / 32, SLOT = 4 * B * D;
+    extern __shared__ __align__(16) float fo_smem[];
+    float* slots = fo_smem;
+    float (*part)[2][B][NW] = reinterpret_cast<float (*)[2][B][NW]>(fo_smem + kFoRing * SLOT);
+    float (*dxs)[B][D] = reinterpret_cast<float (*)[B][D]>(fo_smem + kFoRing * SLOT + 2 * 2 * B * NW);
+    const int c = threadIdx.x, r = blockIdx.y, lane = c & 31, warp = c >> 5;
     const int64_t t0 = (int64_t)blockIdx.x * span;
     if (t0 >= L.total) return;  // whole CTA
     const int64_t t1 = min(L.total, t0 + span);
     const int kind = r < L.Hq ? 0 : (r < L.Hq + L.Hkv ? 1 : 2);
     const int hh = kind == 0 ? r : (kind == 1 ? r - L.Hq : r - L.Hq - L.Hkv);
-    const int H = kind == 0 ? L.Hq : L.Hkv, G = L.G;
+    const int H = kind == 0 ? L.Hq : L.Hkv;
+    const int U = kind == 0 ? 1 : L.G;  // heads summed per row: units per block
     const bool norm = kind == 1 || (kind == 0 && (L.flags & HLA_FLAG_L2NORM_Q));  // uniform over the CTA
+    const float* ysrc = kind == 0 ? A.dqh : kind == 1 ? A.dkh_h : A.dvh_h;
+    const float* gsrc = kind == 0 ? A.dqr_sm : kind == 1 ? A.dkr_h : A.dv_h;
+    const float* pre = kind == 0 ? A.qt : A.kt;
+    float* ydst = kind == 0 ? A.dqt : kind == 1 ? A.dkt : A.dvt;
+    float* dst = kind == 0 ? A.dq : kind == 1 ? A.dk : A.dv;
+    const int64_t n_blk = (t1 - t0 + B - 1) / B;
+    const int64_t n_units = (2 + n_blk) * U;
+    // unit n: n < 2U carries y's sources of block n / U (head n % U); after those, unit (b + 2) U + g carries
+    // y's sources of block b + 2 and the softmax gradient and angles of block b (head g)
+    auto issue = [&](int64_t n) {
+        if (n < n_units) {
+            float* sl = slots + (size_t)(n % kFoRing) * SLOT;
+            const int64_t j = n / U;
+            const int g = (int)(n % U);
+            const int64_t ty = t0 + B * j;  // y's block: j
+            stage_rows8<float, D>(sl, ysrc, ty, L.total, L.Hq, hh * U + g);
+            if (g == 0 && norm) stage_rows8<float, D>(sl + 2 * B * D, pre, ty, L.total, H, hh);
+            if (j >= 2) {
+                const int64_t tb = t0 + B * (j - 2);
+                stage_rows8<float, D>(sl + B * D, gsrc, tb, t1, L.Hq, hh * U + g);
+                if (g == 0 && kind != 2)
+                    stage_rows8<float, D>(sl + 3 * B * D, reinterpret_cast<const float*>(A.ang), tb, t1, 1, 0);
+            }
+        }
+        cp_async_commit_group();  // (empty past the last unit: the count per unit stays uniform)
+    };
     float wt[kConvWidth];
     {
         const float4* w4 = reinterpret_cast<const float4*>((kind == 0 ? A.wq : kind == 1 ? A.wk : A.wv) +
@@ -1125,78 +1164,118 @@ bwd_feat_out_kernel(LayerDims L, FeatOutArgs A, int64_t span) {
         wt[0] = a.x; wt[1] = a.y; wt[2] = a.z; wt[3] = a.w;
         wt[4] = b.x; wt[5] = b.y; wt[6] = b.z; wt[7] = b.w;
     }
-    // per-head gradients of the row: one row (q) or the group's G rows (k, v), at channel c of token t
-    const float* ysrc = kind == 0 ? A.dqh : kind == 1 ? A.dkh_h : A.dvh_h;
-    const float* gsrc = kind == 0 ? A.dqr_sm : kind == 1 ? A.dkr_h : A.dv_h;
-    const int n_src = kind == 0 ? 1 : G;
-    auto src_sum = [&](const float* base, int64_t t) {
-        const float* p = base + ((size_t)t * L.Hq + (size_t)hh * n_src) * D + c;
-        float acc = 0.f;
-        for (int g = 0; g < n_src; ++g) acc += p[(size_t)g * D];
-        return acc;
-    };
-    const float* pre = kind == 0 ? A.qt : A.kt;
-    float* ydst = kind == 0 ? A.dqt : kind == 1 ? A.dkt : A.dvt;
-    // y of the 8 tokens from tb (zero past the last token), written out for the tokens of the span
-    auto y_block = [&](int64_t tb, float (&y)[B], float (&x)[B], float (*p)[B][D / 32]) {
+    for (int i = 0; i < kFoRing - 1; ++i) issue(i);
+    int s = seq_of_token(A.cu, L.n_seqs, t0);
+    int64_t s_start, s_len;
+    seq_range(A.cu, s, L.total, &s_start, &s_len);
+    float y0[B], y1[B];     // y of the current block and the next one
+    float ya[B], xa[B];     // y's source summed over the heads so far, and the pre-norm rows, of the block in hand
+    float sa[B], dx[B];     // the softmax gradient summed over the heads so far; dx of the current block
+    float2 an[B];           // RoPE cos / sin of the current block's tokens at this thread's channel pair
 #pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int64_t t = tb + u;
-            const bool in = t < L.total;
-            y[u] = in ? src_sum(ysrc, t) : 0.f;
-            x[u] = in && norm ? pre[((size_t)t * H + hh) * D + c] : 0.f;
-        }
-        if (norm) {
-            // y = x / nrm, nrm = sqrt(|x|^2 + eps): dx = (dy - x (x . dy) / nrm^2) / nrm
-            float n2[B], xd[B];
-#pragma unroll
-            for (int u = 0; u < B; ++u) {
-                n2[u] = x[u] * x[u];
-                xd[u] = x[u] * y[u];
-            }
-            const int lane = c & 31, warp = c >> 5;
-            const float wn = warp_reduce8(n2, lane), wd = warp_reduce8(xd, lane);
-            if (lane < 8) {  // the caller finishes after a barrier
-                p[0][red8_slot(lane)][warp] = wn;
-                p[1][red8_slot(lane)][warp] = wd;
-            }
-        }
-    };
-    auto y_finish = [&](int64_t tb, float (&y)[B], const float (&x)[B], float (*p)[B][D / 32]) {
+    for (int u = 0; u < B; ++u) ya[u] = xa[u] = sa[u] = 0.f;
+    // the block of y whose row sums are in part[jp & 1] (pending after its last unit), and the block whose dx
+    // waits for its RoPE partners in dxs
+    int64_t y_pending = -1, dx_pending = -1;
+    auto finish_y = [&](int64_t j, float (&y)[B]) {
         if (norm) {
 #pragma unroll
             for (int u = 0; u < B; ++u) {
                 float n2 = 0.f, xd = 0.f;
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k) {
-                    n2 += p[0][u][k];
-                    xd += p[1][u][k];
+                for (int k = 0; k < NW; ++k) {
+                    n2 += part[j & 1][0][u][k];
+                    xd += part[j & 1][1][u][k];
                 }
                 n2 += 1e-6f;
-                y[u] = (y[u] - x[u] * xd / n2) * rsqrtf(n2);
+                // y = x / nrm, nrm = sqrt(|x|^2 + eps): dx = (dy - x (x . dy) / nrm^2) / nrm
+                y[u] = (ya[u] - xa[u] * xd / n2) * rsqrtf(n2);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < B; ++u) y[u] = ya[u];
+        }
+        const int64_t tb = t0 + B * j;
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            if (tb + u < t1) ydst[((size_t)(tb + u) * H + hh) * D + c] = y[u];
+            ya[u] = xa[u] = 0.f;
+        }
+    };
+    auto finish_dx = [&](int64_t b) {
+        const int64_t tb = t0 + B * b;
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t t = tb + u;
+            if (t >= t1) break;
+            const float other = dxs[b & 1][u][c ^ half];
+            dst[((size_t)t * H + hh) * D + c] = c < half ? dx[u] * an[u].x + other * an[u].y
+                                                         : dx[u] * an[u].x - other * an[u].y;
+        }
+    };
+#pragma unroll 1
+    for (int64_t n = 0; n < n_units; ++n) {
+        cp_async_wait_group<kFoRing - 2>();
+        __syncthreads();
+        issue(n + kFoRing - 1);
+        // work whose shared sums were written before this barrier
+        if (y_pending >= 0) {
+            if (y_pending == 0) {
+                finish_y(0, y0);
+            } else if (y_pending == 1) {
+                finish_y(1, y1);
+            } else {
+                float y2[B];
+                finish_y(y_pending, y2);
+#pragma unroll
+                for (int u = 0; u < B; ++u) {
+                    y0[u] = y1[u];
+                    y1[u] = y2[u];
+                }
+            }
+            y_pending = -1;
+        }
+        if (dx_pending >= 0) {
+            finish_dx(dx_pending);
+            dx_pending = -1;
+        }
+        // this unit
+        const float* sl = slots + (size_t)(n % kFoRing) * SLOT;
+        const int64_t j = n / U;
+        const int g = (int)(n % U);
+#pragma unroll
+        for (int u = 0; u < B; ++u) ya[u] += sl[u * D + c];
+        if (g == 0 && norm) {
+#pragma unroll
+            for (int u = 0; u < B; ++u) xa[u] = sl[2 * B * D + u * D + c];
+        }
+        if (j >= 2) {
+#pragma unroll
+            for (int u = 0; u < B; ++u) sa[u] += sl[B * D + u * D + c];
+            if (g == 0 && kind != 2) {
+#pragma unroll
+                for (int u = 0; u < B; ++u)
+                    an[u] = reinterpret_cast<const float2*>(sl + 3 * B * D + u * D)[c & (half - 1)];
             }
         }
+        if (g != U - 1) continue;
+        // the block's last unit: y's row sums to part, then (main units) dx of block j - 2
+        if (norm) {
+            float n2[B], xd[B];
 #pragma unroll
-        for (int u = 0; u < B; ++u)
-            if (tb + u >= t0 && tb + u < t1) ydst[((size_t)(tb + u) * H + hh) * D + c] = y[u];
-    };
-    int s = seq_of_token(A.cu, L.n_seqs, t0);
-    int64_t s_start, s_len;
-    seq_range(A.cu, s, L.total, &s_start, &s_len);
-    float y0[B], y1[B], y2[B], x[B];  // y of tokens tb .. tb + 7, tb + 8 .. tb + 15, tb + 16 .. tb + 23
-    y_block(t0, y0, x, part[0]);
-    if (norm) __syncthreads();
-    y_finish(t0, y0, x, part[0]);
-    y_block(t0 + B, y1, x, part[1]);
-    if (norm) __syncthreads();
-    y_finish(t0 + B, y1, x, part[1]);
-    if (norm) __syncthreads();  // the reads of part[0] and part[1] above come before the loop writes them
-    int par = 0;
-    float* dst = kind == 0 ? A.dq : kind == 1 ? A.dk : A.dv;
-#pragma unroll 1
-    for (int64_t tb = t0; tb < t1; tb += B, par ^= 1) {
-        y_block(tb + 2 * B, y2, x, part[par]);
-        float dx[B];
+            for (int u = 0; u < B; ++u) {
+                n2[u] = xa[u] * xa[u];
+                xd[u] = xa[u] * ya[u];
+            }
+            const float wn = warp_reduce8(n2, lane), wd = warp_reduce8(xd, lane);
+            if (lane < 8) {
+                part[j & 1][0][red8_slot(lane)][warp] = wn;
+                part[j & 1][1][red8_slot(lane)][warp] = wd;
+            }
+        }
+        y_pending = j;
+        if (j < 2) continue;
+        const int64_t b = j - 2, tb = t0 + B * b;
 #pragma unroll
         for (int u = 0; u < B; ++u) {
             const int64_t t = tb + u;
@@ -1209,33 +1288,28 @@ bwd_feat_out_kernel(LayerDims L, FeatOutArgs A, int64_t span) {
             // x_t feeds the conv output at t + 7 - m through tap m
 #pragma unroll
             for (int m = 0; m < kConvWidth; ++m) {
-                const int j = u + (kConvWidth - 1) - m;
-                if (tb + j < s_end) acc = fmaf(wt[m], j < B ? y0[j] : y1[j - B], acc);
+                const int jj = u + (kConvWidth - 1) - m;
+                if (tb + jj < s_end) acc = fmaf(wt[m], jj < B ? y0[jj] : y1[jj - B], acc);
             }
-            dx[u] = t < t1 ? acc + src_sum(gsrc, t) : 0.f;
-            if (kind != 2) dxs[par][u][c] = dx[u];
+            dx[u] = acc + sa[u];
+            sa[u] = 0.f;
         }
-        if (kind != 2) __syncthreads();
-        y_finish(tb + 2 * B, y2, x, part[par]);
+        if (kind == 2) {
 #pragma unroll
-        for (int u = 0; u < B; ++u) {
-            const int64_t t = tb + u;
-            if (t >= t1) break;
-            const size_t o = ((size_t)t * H + hh) * D + c;
-            if (kind == 2) {
-                dst[o] = dx[u];
-            } else {  // RoPE's transpose: rotate the pair (i, i + d / 2) back by the angle p theta_i
-                const float2 a = A.ang[(size_t)t * half + (c & (half - 1))];
-                const float other = dxs[par][u][c ^ half];
-                dst[o] = c < half ? dx[u] * a.x + other * a.y : dx[u] * a.x - other * a.y;
-            }
-        }
+            for (int u = 0; u < B; ++u)
+                if (tb + u < t1) dst[((size_t)(tb + u) * H + hh) * D + c] = dx[u];
+        } else {
 #pragma unroll
-        for (int u = 0; u < B; ++u) {
-            y0[u] = y1[u];
-            y1[u] = y2[u];
+            for (int u = 0; u < B; ++u) dxs[b & 1][u][c] = dx[u];
+            dx_pending = b;
         }
     }
+    __syncthreads();
+    if (y_pending >= 0) {  // the last unit's block of y: past the span, nothing to write
+        float y2[B];
+        finish_y(y_pending, y2);
+    }
+    if (dx_pending >= 0) finish_dx(dx_pending);
 }
 
 // ---- 6. conv filters: partial sums over a span of tokens per (row, channel, tap), then over the spans.
@@ -1410,17 +1484,20 @@ size_t bwd_ang_offset(const LayerDims& L, const BwdLayout& b) {
     return b.total - ((size_t)L.total * L.d * sizeof(float) + 255) / 256 * 256;
 }
 
-// Token spans of a launch with a CTA of `threads` per (row, span of tokens): the smallest multiple of 8 tokens
+// Token spans of a launch with a CTA of `threads` (and smem bytes of dynamic shared memory) per (row, span of
+// tokens): the smallest multiple of 8 tokens
 // (at least min_span, itself a multiple of 8) for which the grid (spans x rows) is one wave of the CTAs the
 // device holds at once
 template <class K>
-cudaError_t row_span_grid(DeviceCache& cache, K kernel, int threads, int64_t min_span, const LayerDims& L,
-                          int64_t* span, dim3* grid) {
+cudaError_t row_span_grid(DeviceCache& cache, K kernel, int threads, size_t smem, int64_t min_span,
+                          const LayerDims& L, int64_t* span, dim3* grid) {
     int resident = 0;
-    cudaError_t e = device_cached(cache, &resident, [kernel, threads](int dev, int* val) {
+    cudaError_t e = device_cached(cache, &resident, [kernel, threads, smem](int dev, int* val) {
         int n_sm = 0, per_sm = 0;
         cudaError_t r = sm_count(dev, &n_sm);
-        if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        if (r == cudaSuccess && smem > 48 * 1024)
+            r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
         *val = std::max(1, n_sm * std::max(1, per_sm));
         return r;
     });
@@ -1513,12 +1590,16 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
         dim3 grid;
         if (D == 128) {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 128>, 128, kConvWidth, L, &span, &grid)) != cudaSuccess) return e;
+            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 128>, 128, 0, kConvWidth, L, &span, &grid)) !=
+                cudaSuccess)
+                return e;
             bwd_conv_kernel<Tin, 128><<<grid, 128, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
                                                                      F(b.qh), F(b.kt), F(b.kh), F(b.vh), span);
         } else {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 64>, 64, kConvWidth, L, &span, &grid)) != cudaSuccess) return e;
+            if ((e = row_span_grid(cache, bwd_conv_kernel<Tin, 64>, 64, 0, kConvWidth, L, &span, &grid)) !=
+                cudaSuccess)
+                return e;
             bwd_conv_kernel<Tin, 64><<<grid, 64, 0, st>>>(L, v, wq, wk, wv, cu, F(b.qr), F(b.kr), F(b.qt),
                                                                     F(b.qh), F(b.kt), F(b.kh), F(b.vh), span);
         }
@@ -1546,14 +1627,16 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
         dim3 grid;
         if (D == 128) {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_feat_out_kernel<128>, 128, kConvWidth, L, &span, &grid)) != cudaSuccess)
+            if ((e = row_span_grid(cache, bwd_feat_out_kernel<128>, 128, feat_out_smem<128>(), kConvWidth, L, &span,
+                                   &grid)) != cudaSuccess)
                 return e;
-            bwd_feat_out_kernel<128><<<grid, 128, 0, st>>>(L, A, span);
+            bwd_feat_out_kernel<128><<<grid, 128, feat_out_smem<128>(), st>>>(L, A, span);
         } else {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_feat_out_kernel<64>, 64, kConvWidth, L, &span, &grid)) != cudaSuccess)
+            if ((e = row_span_grid(cache, bwd_feat_out_kernel<64>, 64, feat_out_smem<64>(), kConvWidth, L, &span,
+                                   &grid)) != cudaSuccess)
                 return e;
-            bwd_feat_out_kernel<64><<<grid, 64, 0, st>>>(L, A, span);
+            bwd_feat_out_kernel<64><<<grid, 64, feat_out_smem<64>(), st>>>(L, A, span);
         }
     }
     if ((e = mark(6)) != cudaSuccess) return e;
@@ -1562,13 +1645,13 @@ cudaError_t launch_backward(const LayerDims& L, const Tin* q, const Tin* k, cons
         dim3 grid;  // spans of at least kWB tokens: at most b.n_blocks partial sums
         if (D == 128) {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 128>, 128, kWB, L, &span, &grid)) != cudaSuccess)
+            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 128>, 128, 0, kWB, L, &span, &grid)) != cudaSuccess)
                 return e;
             bwd_convw_part_kernel<Tin, 128><<<grid, 128, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),
                                                                    F(b.dvt), F(b.convw_part), span);
         } else {
             static DeviceCache cache;
-            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 64>, 64, kWB, L, &span, &grid)) != cudaSuccess)
+            if ((e = row_span_grid(cache, bwd_convw_part_kernel<Tin, 64>, 64, 0, kWB, L, &span, &grid)) != cudaSuccess)
                 return e;
             bwd_convw_part_kernel<Tin, 64><<<grid, 64, 0, st>>>(L, v, cu, F(b.qr), F(b.kr), F(b.dqt), F(b.dkt),
                                                                  F(b.dvt), F(b.convw_part), span);
