@@ -474,18 +474,32 @@ def bwd_launches(wl) -> int:
 
 
 def backward_work(wl) -> dict:
-    """Algorithmic fp32 flops of the backward's two compute stages.  GDN, per absorbed token and
+    """Algorithmic work of the backward's stages: fp32 flops of the two compute stages, bytes of the three
+    streaming ones (counted per entry below).  GDN, per absorbed token and
     q-head (every such token is also a read-out position): the forward's absorption (k^T S and the
     rank-1 update, 4 d^2) and read-out (2 d^2, for lambda's gradient), the read-out backward (S dO and
     q dO^T, 4 d^2) and the absorption backward (k^T S again, k^T dS, <dS, S_prev>, dS u, S_prev du and
     the dS update, 12 d^2): 22 d^2; the checkpoint recompute is overhead, not counted.  Softmax, per
     visible (query, key) pair and q-head: the logit, dP = dO . v, and the three products into dq, dk,
     dv, 2 d each: 10 d."""
-    d, Hq = wl.head_dim, wl.n_q_heads
+    d, Hq, Hkv, T = wl.head_dim, wl.n_q_heads, wl.n_kv_heads, wl.total_tokens
     absorbed = sum(max(0, L - wl.window - wl.n_sinks) for L in wl.seqlens) * Hq
     keys = sum(visible_keys(L, wl.n_sinks, wl.window) for L in wl.seqlens) * Hq
+    vb = 2 if wl.dtype == "bf16" else 4
+    row = 4.0 * d  # one fp32 row of the workspace
     return {"gdn": {"bound": "alu", "flops": 22.0 * d * d * absorbed, "kernel": "bwd_gdn_kernel"},
-            "softmax": {"bound": "alu", "flops": 10.0 * d * keys, "kernel": "bwd_softmax_kernel"}}
+            "softmax": {"bound": "alu", "flops": 10.0 * d * keys, "kernel": "bwd_softmax_kernel"},
+            # the streaming launches, HBM-bound, per token: reads RoPE'd q and k and v; writes q~, qhat, k~,
+            # khat, vhat (fp32)
+            "conv": {"bound": "hbm", "kernel": "bwd_conv_kernel",
+                     "bytes": T * (row * (Hq + Hkv) + vb * d * Hkv + row * (2 * Hq + 3 * Hkv))},
+            # reads dqhat, the group's per-head dkhat, dvhat and softmax gradients (each Hq rows), q~ and k~,
+            # the RoPE angles; writes the conv-output gradients and dq, dk, dv
+            "feat_out": {"bound": "hbm", "kernel": "bwd_feat_out_kernel",
+                         "bytes": T * (row * (6 * Hq + Hq + Hkv) + row + 2 * row * (Hq + 2 * Hkv))},
+            # reads the conv inputs and the conv-output gradients (the partial sums are small)
+            "conv_filters": {"bound": "hbm", "kernel": "bwd_convw_part_kernel",
+                             "bytes": T * (row * (Hq + Hkv) + vb * d * Hkv + row * (Hq + 2 * Hkv))}}
 
 
 def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_steps=5, e2e_steps=5):
@@ -553,11 +567,17 @@ def run_backward_bench(key, dist, peaks, trial_seconds=2.0, warmup=3, stage_step
 
     def roof(name):
         w = work[name]
-        achieved = w["flops"] / (stage_ms[name] / 1e3) / 1e12
+        sec = stage_ms[name] / 1e3
+        traffic = kernel_traffic(w["kernel"], BWD_SOURCES, key + "_backward")
+        if w["bound"] == "hbm":
+            achieved = w["bytes"] / sec / 1e9
+            return {"kernel": w["kernel"], "bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 5), "traffic": traffic,
+                    "algorithmic": w["bytes"], "peak_source": peaks["source"]}
+        achieved = w["flops"] / sec / 1e12
         return {"kernel": w["kernel"], "bound": "alu", "achieved": round(achieved, 4), "peak": FP32_ALU_TFLOPS,
-                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 5),
-                "traffic": kernel_traffic(w["kernel"], BWD_SOURCES, key + "_backward"), "algorithmic": w["flops"],
-                "peak_source": FP32_ALU_TFLOPS_DERIVATION}
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_ALU_TFLOPS, 5), "traffic": traffic,
+                "algorithmic": w["flops"], "peak_source": FP32_ALU_TFLOPS_DERIVATION}
 
     dominant = max(work, key=lambda n: stage_ms[n])
     # end to end: inputs and dO from pinned host memory, every gradient back to pinned host memory
@@ -1067,6 +1087,9 @@ TRAFFIC_KERNELS = {  # kernel name -> the sources its counters are keyed by
     "bwd_gdn_kernel": BWD_SOURCES,
     "bwd_sm_query_kernel": BWD_SOURCES,
     "bwd_sm_key_kernel": BWD_SOURCES,
+    "bwd_conv_kernel": BWD_SOURCES,
+    "bwd_feat_out_kernel": BWD_SOURCES,
+    "bwd_convw_part_kernel": BWD_SOURCES,
     "gdn_recurrent_kernel": GDN_RECURRENT_SOURCES,
     "gdn_part_scan_kernel": GDN_RECURRENT_SOURCES,
 }
