@@ -150,6 +150,20 @@ def test_f32_d64_small_budget(oracle_bw):
     check(wl, oracle_bw)
 
 
+def test_bf16_d128_group8_short_sequences(oracle_bw):
+    # 8 q-heads per kv head (8 units per 8-token block in the feature backward); sequences shorter than
+    # one 8-token block and than the budget, and boundaries inside blocks
+    wl = synth.small("bwd-g8", [37, 200, 5, 64, 3, 71], n_q_heads=8, n_kv_heads=1, head_dim=128,
+                     seed=synth.BASE_SEED + 307)
+    check(wl, oracle_bw)
+
+
+def test_f32_d64_group8(oracle_bw):
+    wl = synth.small("bwd-g8f", [90, 7, 130], n_q_heads=16, n_kv_heads=2, head_dim=64, dtype="f32",
+                     seed=synth.BASE_SEED + 308)
+    check(wl, oracle_bw)
+
+
 def test_gla_variant(oracle_bw):
     wl = synth.small("bwd-gla", [180, 97], n_q_heads=4, n_kv_heads=2, head_dim=64, seed=synth.BASE_SEED + 303)
     got, _ = check(wl, oracle_bw, flags=hla.FLAG_L2NORM_Q | hla.FLAG_GLA, erase_off=True)
