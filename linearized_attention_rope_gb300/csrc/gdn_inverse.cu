@@ -299,12 +299,18 @@ gdn_inverse_kernel(LayerDims L, const __half* __restrict__ qhat, const __half* _
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int e = tid + kThreads * u, r = e >> 3, c8 = (e & 7) * 8;
-        const float* tr = sT + r * 68 + c8;
-        float tb[8], tbg[8];
+        float tr[8], be[8], ga[8], tb[8], tbg[8];
+        // 16-byte reads (rows of sT start on 16-byte boundaries, as do sBeta and sGam)
+        *reinterpret_cast<float4*>(tr) = *reinterpret_cast<const float4*>(sT + r * 68 + c8);
+        *reinterpret_cast<float4*>(tr + 4) = *reinterpret_cast<const float4*>(sT + r * 68 + c8 + 4);
+        *reinterpret_cast<float4*>(be) = *reinterpret_cast<const float4*>(sBeta + c8);
+        *reinterpret_cast<float4*>(be + 4) = *reinterpret_cast<const float4*>(sBeta + c8 + 4);
+        *reinterpret_cast<float4*>(ga) = *reinterpret_cast<const float4*>(sGam + c8);
+        *reinterpret_cast<float4*>(ga + 4) = *reinterpret_cast<const float4*>(sGam + c8 + 4);
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
-            tb[x] = tr[x] * sBeta[c8 + x];
-            tbg[x] = gla ? 0.f : tb[x] * sGam[c8 + x];
+            tb[x] = tr[x] * be[x];
+            tbg[x] = gla ? 0.f : tb[x] * ga[x];
         }
         const uint32_t off = umma::sw128_offset(r, c8, 64);
         *reinterpret_cast<uint4*>(rec + kRecTb + off) =
