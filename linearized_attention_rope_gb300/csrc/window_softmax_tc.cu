@@ -46,6 +46,13 @@ constexpr uint32_t kBar = kRed + 2048;
 constexpr uint32_t kSmemAlloc = kBar + 64 + 1024;
 constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
 
+// 2^x by the PTX approximate base-2 exponential (one special-function-unit op; flush-to-zero; 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -256,7 +263,7 @@ window_softmax_tc_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q,
             float lsum = 0.f;
 #pragma unroll
             for (int x = 0; x < 64; ++x) {
-                sc[x] = sc[x] == -INFINITY ? 0.f : exp2f(sc[x] * qscale - m_new);
+                sc[x] = sc[x] == -INFINITY ? 0.f : ex2_approx(fmaf(sc[x], qscale, -m_new));
                 lsum += sc[x];
             }
 #pragma unroll
