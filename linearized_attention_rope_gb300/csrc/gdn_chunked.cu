@@ -79,7 +79,9 @@ constexpr uint32_t kColD1 = 0, kColD2 = 128, kColS = 256, kTmemCols = 512;
 // mbarrier indices
 constexpr int kReady = 0, kFree = 2, kMma1 = 4, kMma2 = 5, kOFull = 6, kLoaded = 8, kD1Done = 10, kLoadedV = 12,
               kDsQueued = 14, kNumBars = 16;
-static_assert(8 * kNumBars + 8 + 32 <= 256, "barrier area: mbarriers, TMEM base, abort flag, 2 slots x 4 ids");
+static_assert(8 * kNumBars + 8 + 32 + 4 <= 256,
+              "barrier area: mbarriers, TMEM base, abort flag, 2 slots x 4 ids, the CTA's sequence");
+constexpr int kMaxRankedSeqs = 64;  // up to this many sequences, the grid takes them longest first
 constexpr uint32_t kLoadBytes = kRecordBytes + 5 * 8192;  // record + query, key rows (2 boxes each) + value slice
 constexpr uint32_t kLoadVBytes = 2 * 8192;                // T diag(beta) + value slice (the V product's operands)
 
@@ -124,10 +126,30 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
     volatile int* decision = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 8);  // [role id][2]
+    volatile int* seq_slot = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 40);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const int h = blockIdx.x / kSlices, slice = blockIdx.x % kSlices, n = blockIdx.y;
+    const int h = blockIdx.x / kSlices, slice = blockIdx.x % kSlices;
+    // The CTA's sequence: row y of the grid takes the sequence of rank y by length, longest first (ties in
+    // index order), so that with sequences of mixed lengths the longest chains start in the first wave of
+    // CTAs (the rows are placed in order) rather than behind shorter ones.  The ranking reads only
+    // cu_seqlens, an input of the call, so it runs before the wait for the launch before this one.
+    if (L.n_seqs <= kMaxRankedSeqs) {
+        for (int q = tid; q < L.n_seqs; q += kThreads) {
+            int64_t qs, ql;
+            seq_range(cu, q, L.total, &qs, &ql);
+            int rank = 0;
+            for (int o = 0; o < L.n_seqs; ++o) {
+                int64_t os, ol;
+                seq_range(cu, o, L.total, &os, &ol);
+                rank += (ol > ql || (ol == ql && o < q)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.y) *seq_slot = q;  // exactly one sequence has each rank
+        }
+    } else if (tid == 0) {
+        *seq_slot = blockIdx.y;
+    }
     const int kv = h / L.G, W = L.window;
     const uint32_t sbase = umma::smem_addr(sm);
     const uint32_t bar0 = umma::smem_addr(sm + kBar);
@@ -150,6 +172,7 @@ gdn_chunked_kernel(LayerDims L, const __grid_constant__ CUtensorMap map_q, const
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int n = *seq_slot;
     // Launched with programmatic stream serialization, the CTAs get here while the launch before this
     // one (the chunk-local kernel) may still run: wait for it to complete, and its writes (and those of
     // every launch before it) to be visible, before the first global read.  No effect on a plain launch.
