@@ -301,6 +301,28 @@ __device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes16
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_ring() { asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory"); }
 
+// Row y of a grid over sequences takes the sequence of rank y by length, longest first (ties in index order),
+// so that with sequences of mixed lengths the longest chains start in the first wave of CTAs (the rows are
+// placed in order); more than kMaxRankedSeqs sequences keep index order.  Reads only cu_seqlens; every
+// thread of the CTA calls it (one CTA barrier); `slot` is a shared int.
+constexpr int kMaxRankedSeqs = 64;
+__device__ __forceinline__ int ranked_seq(const LayerDims& L, const int32_t* __restrict__ cu, int y, int* slot) {
+    if (L.n_seqs > kMaxRankedSeqs) return y;
+    for (int q = threadIdx.x; q < L.n_seqs; q += blockDim.x) {
+        int64_t qs, ql;
+        seq_range(cu, q, L.total, &qs, &ql);
+        int r = 0;
+        for (int o = 0; o < L.n_seqs; ++o) {
+            int64_t os, ol;
+            seq_range(cu, o, L.total, &os, &ol);
+            r += (ol > ql || (ol == ql && o < q)) ? 1 : 0;
+        }
+        if (r == y) *slot = q;  // exactly one sequence has each rank
+    }
+    __syncthreads();
+    return *slot;
+}
+
 // the sum over the 8 lanes of a column (lanes differing in bits 0-2), for N values at once
 template <int N>
 __device__ __forceinline__ void col_sum(float (&x)[N]) {
@@ -346,9 +368,10 @@ bwd_gdn_kernel(LayerDims L, const float* __restrict__ alpha, const float* __rest
     int* xm = reinterpret_cast<int*>(xs + B::XS);  // [2][kXB][2]: each stage's first absorption and count
     float* ring = xs + B::XS + B::XM;   // kRing stage slots
     float* dv_s = ring + kRing * B::SLOT;  // [K][CPC]
-    float* red = dv_s + K * CPC;        // [NW] + 1
+    float* red = dv_s + K * CPC;        // [NW] + 1, then the CTA's sequence (an int)
     const uint32_t rank = cluster_rank();
-    const int h = blockIdx.x / kCl, n = blockIdx.y, kv = h / L.G, tid = threadIdx.x;
+    const int h = blockIdx.x / kCl, kv = h / L.G, tid = threadIdx.x;
+    const int n = ranked_seq(L, cu, (int)blockIdx.y, reinterpret_cast<int*>(red + NW + 1));
     const int w = tid >> 5, lane = tid & 31, lr = lane & 7;
     const int colL = w * B::CPW + (lane >> 3);            // this lane's column in the CTA
     const int col = (int)rank * CPC + colL;               // and in S

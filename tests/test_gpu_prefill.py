@@ -211,6 +211,17 @@ def test_large_magnitude_activations(oracle_mod, d):
     check_prefill(wl, x, out, st, all_units(wl), oracle_mod)
 
 
+def test_many_sequences_keep_index_order(oracle_mod):
+    # 70 sequences of mixed lengths: more than the state kernel ranks by length, so its grid rows take the
+    # sequences in index order (the ranked order is covered by every other varlen case)
+    lens = [65, 130, 7, 200, 64, 129, 1]
+    wl = synth.small("many seqs", [lens[i % len(lens)] for i in range(70)], n_q_heads=2, n_kv_heads=1,
+                     head_dim=128, seed=synth.BASE_SEED + 431)
+    x = synth.make_inputs(wl, "cuda")
+    out, st = run_prefill(wl, x, with_state=True)
+    check_prefill(wl, x, out, st, all_units(wl), oracle_mod)
+
+
 @pytest.mark.parametrize("gate_scale", [2.0, 30.0])
 def test_strong_and_mixed_gates(oracle_mod, gate_scale):
     # gates 20x and 300x the unit recipe (log-gate per token about -1.6 and -24 on average): a 64-token
