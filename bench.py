@@ -1114,6 +1114,8 @@ def write_traffic(reps: str, key: str, calls: int = 1):
             raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], check=True, capture_output=True,
                                  text=True).stdout
         entry.update(traffic_from_csv(raw, calls))
+    if "_command" in data.get(key, {}):  # the capture command recorded with the earlier counters
+        entry["_command"] = data[key]["_command"]
     data[key] = entry
     data[key]["_reports"] = [os.path.basename(r) for r in reps.split(",")]
     with open(path, "w") as f:
