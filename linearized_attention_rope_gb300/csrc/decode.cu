@@ -118,9 +118,10 @@ template cudaError_t launch_state_fill<__nv_bfloat16, __half>(
 //     histories; L2 norms.  The new token goes into the KV ring (slot p, or
 //     n_sinks + (p - n_sinks) % W) and the pending ring (slot p % (W + 1))
 //     with each head's g and beta; RoPE'd q and qhat go to scratch.
-//  2. state (CTA per q-head and sequence): if token j = p - W is not a sink it
-//     leaves the window now: the 64 KiB state is read once into registers,
-//     x = khat_j^T S and y = qhat_p^T S are reduced across the CTA, and
+//  2. state (CTA per q-head, half of the value columns and sequence): if token
+//     j = p - W is not a sink it leaves the window now: the half's 32 KiB of
+//     the state are read once into registers, x = khat_j^T S and
+//     y = qhat_p^T S (the half's columns) are reduced across the CTA, and
 //     S <- alpha S + khat_j u^T with u = beta (vhat_j - alpha x) is written
 //     back; o_lin = alpha y + (qhat_p . khat_j) u.  Otherwise o_lin = 0.
 //  3. softmax (CTA per kv head, key split and sequence): the ring's valid slots
@@ -261,37 +262,38 @@ decode_features_kernel(LayerDims L, const Tin* __restrict__ q, const Tin* __rest
     }
 }
 
-// State unit (q-head h, sequence n), one CTA.  Thread t owns column group
-// t % (D/4) (four value dims, float4) of rows (t / (D/4)) * RPT .. + RPT - 1;
-// the 64 KiB state is read once into registers and written back once.
+// State unit (q-head h, sequence n, value-column half hf), one CTA: the state's columns never mix, so
+// each half of a head's state is its own unit.  Thread t owns column group t % (D/8) (four value dims,
+// float4) of the half's columns, rows (t / (D/8)) * RPT .. + RPT - 1; the half's 32 KiB are read once into
+// registers and written back once.
 template <int D>
 __device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_state& s, const DecScratch& sc,
-                                                  int h, int n) {
-    constexpr int CG = D / 4, RG = kStateThreads / CG, RPT = D / RG;
-    __shared__ __align__(16) float kj_s[D], vj_s[D], qh_s[D];
-    __shared__ __align__(16) float redx[RG][D], redy[RG][D];
+                                                  int h, int n, int hf) {
+    constexpr int NC = D / 2, CG = NC / 4, RG = kStateThreads / CG, RPT = D / RG;
+    __shared__ __align__(16) float kj_s[D], vj_s[NC], qh_s[D];
+    __shared__ __align__(16) float redx[RG][NC], redy[RG][NC];
     __shared__ float cdot_s;
-    const int tid = threadIdx.x, kv = h / L.G;
+    const int tid = threadIdx.x, kv = h / L.G, c0 = hf * NC;
     const int ns = L.n_sinks, W = L.window, P = W + 1;
     const bool gla = (L.flags & HLA_FLAG_GLA) != 0;
     const int64_t p = s.pos[n], j = p - W;  // the token leaving the window
-    float* olin = sc.olin + ((size_t)n * L.Hq + h) * D;
+    float* olin = sc.olin + ((size_t)n * L.Hq + h) * D + c0;
     if (j < ns) {  // nothing leaves the window into the state this step
-        for (int c = tid; c < D; c += kStateThreads) olin[c] = 0.f;
+        for (int c = tid; c < NC; c += kStateThreads) olin[c] = 0.f;
         return;
     }
     const size_t jslot = (size_t)(j % P);
     const size_t gs = ((size_t)n * L.Hq + h) * P + jslot;
     const float alpha = expf(s.pend_g[gs]), b = s.pend_beta[gs];
     const int cg = tid % CG, rg = tid / CG;
-    float4* S4 = reinterpret_cast<float4*>(s.S + ((size_t)n * L.Hq + h) * D * D);
+    float4* S4 = reinterpret_cast<float4*>(s.S + ((size_t)n * L.Hq + h) * D * D + c0);
     float4 Sr[RPT];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) Sr[r] = S4[(size_t)(rg * RPT + r) * CG + cg];
+    for (int r = 0; r < RPT; ++r) Sr[r] = S4[(size_t)(rg * RPT + r) * (D / 4) + cg];
     for (int c = tid; c < D; c += kStateThreads) {
         const size_t ps = (((size_t)n * L.Hkv + kv) * P + jslot) * D + c;
         kj_s[c] = s.pend_k[ps];
-        vj_s[c] = s.pend_v[ps];
+        if (c < NC) vj_s[c] = s.pend_v[ps + c0];
         qh_s[c] = sc.qhat[((size_t)n * L.Hq + h) * D + c];
     }
     __syncthreads();
@@ -332,7 +334,7 @@ __device__ __forceinline__ void decode_state_unit(const LayerDims& L, const hla_
         o.y = fmaf(alpha, Sr[r].y, kk * u[1]);
         o.z = fmaf(alpha, Sr[r].z, kk * u[2]);
         o.w = fmaf(alpha, Sr[r].w, kk * u[3]);
-        S4[(size_t)(rg * RPT + r) * CG + cg] = o;
+        S4[(size_t)(rg * RPT + r) * (D / 4) + cg] = o;
     }
 }
 
@@ -517,18 +519,21 @@ __device__ __forceinline__ void decode_softmax_unit(const LayerDims& L, const hl
 }
 
 // One launch for the step's two streams over HBM: per (kv head, sequence) a
-// run of G state units (the group's heads) followed by the softmax splits, so
-// the state updates and the ring reads share every wave of CTAs.
+// run of 2G state units (the two value-column halves of each of the group's
+// heads) followed by the softmax splits, so the state updates and the ring
+// reads share every wave of CTAs.  Half-head state units keep 64 floats of
+// state per thread, which lets five CTAs share an SM (bf16 rings; fp32 rings
+// need the registers of three) and so keeps more of the stream in flight.
 template <typename Tin, int D, int GM>
-__global__ void __launch_bounds__(kSmThreads, 3)
+__global__ void __launch_bounds__(kSmThreads, sizeof(Tin) == 2 ? 5 : 3)
 decode_attn_state_kernel(LayerDims L, hla_state s, DecScratch sc) {
     static_assert(kStateThreads == kSmThreads, "one CTA shape for both units");
     extern __shared__ __align__(16) float fsm[];
     pdl_wait();  // the features launch has completed (see decode_features_kernel)
     pdl_trigger();
-    const int run = L.G + sc.splits, kv = blockIdx.x / run, r = blockIdx.x % run, n = blockIdx.y;
-    if (r < L.G) decode_state_unit<D>(L, s, sc, kv * L.G + r, n);
-    else decode_softmax_unit<Tin, D, GM>(L, s, sc, r - L.G, kv, n, fsm);
+    const int run = 2 * L.G + sc.splits, kv = blockIdx.x / run, r = blockIdx.x % run, n = blockIdx.y;
+    if (r < 2 * L.G) decode_state_unit<D>(L, s, sc, kv * L.G + (r >> 1), n, r & 1);
+    else decode_softmax_unit<Tin, D, GM>(L, s, sc, r - 2 * L.G, kv, n, fsm);
 }
 
 // CTA per (q-head, sequence), thread per channel: splits merged by their
@@ -604,7 +609,7 @@ cudaError_t launch_decode_attn_state(const LayerDims& L, const hla_state& s, con
                                     (int)P::kSmemBytes);
     });
     if (e != cudaSuccess) return e;
-    LaunchCfg lc(dim3(L.Hkv * (L.G + sc.splits), L.n_seqs), dim3(kSmThreads), P::kSmemBytes, st, true);
+    LaunchCfg lc(dim3(L.Hkv * (2 * L.G + sc.splits), L.n_seqs), dim3(kSmThreads), P::kSmemBytes, st, true);
     return cudaLaunchKernelEx(&lc.cfg, decode_attn_state_kernel<Tin, D, GM>, L, s, sc);
 }
 
